@@ -1,0 +1,504 @@
+#!/usr/bin/env python
+"""Benchmark of the rotated low-bit linear projection on GB300.
+
+Metric: weight GB/s at M = 1 (decode) and TOPS at M = 4032 (DiT W8A8), each
+as a fraction of the measured roofline.  The headline line is the decode
+workload: a Qwen2.5-0.5B-like FFN (gate/up 896 -> 4864, down 4864 -> 896),
+1000 seeded calls cycling gate, up, down through enough layer sets that the
+distinct weights exceed three times L2; one step = the 1000 calls (replayed as
+one CUDA graph).  The W4A16 decode and the M = 4032 W8A8 DiT projections are
+reported beside it in the same JSON line.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(weak scaling; the projection has no exchange step), and rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "rotated low-bit linear: TOPS at M=4032, weight GB/s at M=1; % of roofline"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--calls", type=int, default=1000)
+    ap.add_argument("--skip-dit", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return FALLBACK_PEAKS, "fallback"
+
+
+def source_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "dit_convrot_linear_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel, sources):
+    """DRAM bytes per launch from a committed ncu capture, or None when the
+    kernel's source changed since the counters were taken."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            t = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not t or t.get("source_sha") != source_sha(*sources):
+        return None
+    return t.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        rows = []
+        with open(self.path) as f:
+            for r in csv.reader(f):
+                if len(r) >= 9:
+                    rows.append([c.strip() for c in r])
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_init(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ workloads
+
+def bf16_dev(bits_np, device):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits_np).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def decode_layers(bits, l2_bytes):
+    """Layer sets so that the distinct weights exceed 3x L2 (at least the
+    0.5B model's 24 layers)."""
+    from dit_convrot_linear_gb300 import synth
+    per_layer = sum(p.N * p.K * bits // 8 + 4 * p.N for p in synth.DECODE.projs)
+    need = -(-3 * l2_bytes // per_layer)
+    return max(synth.DECODE.layers, int(need))
+
+
+class Decode:
+    """1000 seeded M=1 calls cycling gate, up, down through the layer sets."""
+
+    def __init__(self, bits, calls, device, l2_bytes):
+        import torch
+        from dit_convrot_linear_gb300 import synth, tq
+        self.bits, self.calls, self.device = bits, calls, device
+        self.mode = "W8A16" if bits == 8 else "W4A16"
+        w = synth.DECODE
+        self.layers = decode_layers(bits, l2_bytes)
+        self.weights = []   # [layer][proj] -> (codes, sw)
+        for L in range(self.layers):
+            row = []
+            for p in w.projs:
+                Wd = bf16_dev(w.weight(L, p), device)
+                row.append(tq.quantize_weights(Wd, bits))
+                del Wd
+            self.weights.append(row)
+        torch.cuda.synchronize()
+        # inputs and outputs of all calls, contiguous (one copy each way for e2e)
+        self.plan = []
+        xoff = yoff = 0
+        for i in range(calls):
+            p = w.projs[i % 3]
+            self.plan.append((i, (i // 3) % self.layers, i % 3, p, xoff, yoff))
+            xoff += p.K
+            yoff += p.N
+        xs_host = torch.empty(xoff, dtype=torch.bfloat16).pin_memory()
+        for (i, L, j, p, xo, yo) in self.plan:
+            xs_host[xo:xo + p.K] = bf16_dev(w.activation(i, p, 1), "cpu").view(-1)
+        self.x_host = xs_host
+        self.x_dev = xs_host.to(device)
+        self.y_dev = torch.empty(yoff, dtype=torch.float32, device=device)
+        self.y_host = torch.empty(yoff, dtype=torch.float32).pin_memory()
+        self.weight_bytes = sum(p.N * p.K * bits // 8 + 4 * p.N for (_, _, _, p, _, _) in self.plan)
+        self.distinct_bytes = self.layers * sum(p.N * p.K * bits // 8 + 4 * p.N for p in w.projs)
+        self.graph = None
+
+    def run_calls(self):
+        from dit_convrot_linear_gb300 import tq
+        for (i, L, j, p, xo, yo) in self.plan:
+            codes, sw = self.weights[L][j]
+            X = self.x_dev[xo:xo + p.K].view(1, p.K)
+            Y = self.y_dev[yo:yo + p.N].view(1, p.N)
+            tq.linear(X, codes, sw, p.N, self.bits, self.mode, Y=Y)
+
+    def capture(self):
+        import torch
+        self.run_calls()            # first calls set kernel attributes outside capture
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                self.run_calls()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = g
+
+    def step(self):
+        self.graph.replay()
+
+    def step_e2e(self):
+        self.x_dev.copy_(self.x_host, non_blocking=True)
+        self.graph.replay()
+        self.y_host.copy_(self.y_dev, non_blocking=True)
+
+    def isolated_call_us(self, reps=50):
+        """One call at a time (no graph), CUDA events around each."""
+        import torch
+        from dit_convrot_linear_gb300 import tq
+        times = []
+        for r in range(reps):
+            i, L, j, p, xo, yo = self.plan[(r * 7) % len(self.plan)]
+            codes, sw = self.weights[L][j]
+            X = self.x_dev[xo:xo + p.K].view(1, p.K)
+            Y = self.y_dev[yo:yo + p.N].view(1, p.N)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            tq.linear(X, codes, sw, p.N, self.bits, self.mode, Y=Y)
+            e1.record()
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(times)
+
+
+def time_steps(fn, steps, warmup, world):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    return max_over_ranks(ms, world)
+
+
+def dit_measure(device, reps=5):
+    """M = 4032 W8A8 (DiT FFN up and down): TOPS = 2 M N K / t per GEMM, L2
+    flushed between timed calls (a 512 MB write)."""
+    import torch
+    from dit_convrot_linear_gb300 import synth, tq
+    w = synth.DIT
+    M = 4032
+    out = {}
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
+    tot_ops = tot_ms = 0.0
+    gemm_ms_tot = 0.0
+    for p in w.projs:
+        codes, sw = tq.quantize_weights(bf16_dev(w.weight(0, p), device), 8)
+        X = bf16_dev(w.activation(0, p, M), device)
+        Y = torch.empty((M, p.N), dtype=torch.float32, device=device)
+        ws = torch.empty(tq.linear_workspace_bytes(M, p.K, p.N, 8, "W8A8"), dtype=torch.uint8,
+                         device=device)
+        Xq = ws[:M * p.K].view(M, p.K).view(torch.int8)
+        for _ in range(3):
+            tq.linear(X, codes, sw, p.N, 8, "W8A8", Y=Y, workspace=ws)
+        torch.cuda.synchronize()
+        ms, gms = [], []
+        for _ in range(reps):
+            flush.fill_(1)
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record()
+            tq.linear(X, codes, sw, p.N, 8, "W8A8", Y=Y, workspace=ws)
+            e1.record()
+            flush.fill_(2)
+            sx = ws[(M * p.K + 255) // 256 * 256:].view(torch.float32)[:M]
+            e2a = torch.cuda.Event(enable_timing=True)
+            e2a.record()
+            tq.linear_q8(Xq, sx, codes, sw, p.N, 8, Y=Y)
+            e2.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+            gms.append(e2a.elapsed_time(e2))
+        t = statistics.median(ms)
+        tg = statistics.median(gms)
+        ops = 2.0 * M * p.N * p.K
+        out[p.name] = {"N": p.N, "K": p.K, "ms": round(t, 4), "gemm_ms": round(tg, 4),
+                       "tops": round(ops / t / 1e9, 2), "gemm_tops": round(ops / tg / 1e9, 2)}
+        tot_ops += ops
+        tot_ms += t
+        gemm_ms_tot += tg
+        del codes, sw, X, Y, ws
+    return out, tot_ops / tot_ms / 1e9, tot_ops / gemm_ms_tot / 1e9
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def cpu_oracle_decode(bits, budget_s=12.0, min_calls=3):
+    """The oracle (as it stands) on a bounded sample of the decode workload:
+    per call, the rotation of the input row and the A16 product with the
+    oracle's own weight codes (quantised once, untimed)."""
+    import numpy as np
+    import oracle
+    from dit_convrot_linear_gb300 import synth
+    w = synth.DECODE
+    qw = {}
+    for j, p in enumerate(w.projs):
+        Wq, sw = oracle.quantize_weights(w.weight(0, p), bits)
+        qw[j] = (Wq, sw, p)
+    xs = [w.activation(i, w.projs[i % 3], 1) for i in range(60)]
+    nbytes = 0
+    n = 0
+    t0 = time.perf_counter()
+    while n < min_calls or (time.perf_counter() - t0 < budget_s and n < 60):
+        Wq, sw, p = qw[n % 3]
+        codes = oracle.weight_codes(Wq, bits, p.K)
+        xr = oracle.rotate_act_bf16(xs[n])
+        oracle.linear_a16(xr, codes, sw)
+        nbytes += p.N * p.K * bits // 8 + 4 * p.N
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"{n} decode calls (gate/up/down of layer 0, M=1, {bits}-bit), "
+                      f"{dt:.1f} s: rotation + A16 product per call"}
+
+
+# ------------------------------------------------------------------ main
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cb = cpu_oracle_decode(8, budget_s=2.0)
+    vals = []
+    for _ in range(args.warmup):
+        cpu_oracle_decode(8, budget_s=0.5, min_calls=3)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_oracle_decode(8, budget_s=2.0, min_calls=3)["value"])
+    dt = time.perf_counter() - t0
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3 / max(1, args.steps), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode M=1 W8A16, Qwen2.5-0.5B-like FFN "
+                                   "(gate/up 896->4864, down 4864->896), seeded calls"},
+            "cpu_baseline": dict(cb, value=v),
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    from dit_convrot_linear_gb300 import build, tq
+    rank, world, local = dist_init(args.gpus)
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    if rank == 0 or world > 1:
+        build.build()
+    barrier(world)
+    tq.load()
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+    pk, pk_kind = peaks()
+
+    # headline: decode W8A16
+    dec8 = Decode(8, args.calls, device, l2)
+    dec8.capture()
+    with Clocks(local) as clk:
+        ms = time_steps(dec8.step, args.steps, args.warmup, world)
+    clocks = clk.summary()
+    ms_step = ms / args.steps
+    gbs = dec8.weight_bytes / (ms_step * 1e-3) / 1e9 * world
+    per_launch_us = ms_step * 1e3 / args.calls
+    bytes_per_launch = dec8.weight_bytes / args.calls
+    achieved = bytes_per_launch / (per_launch_us * 1e-6) / 1e9
+    hbm = float(pk["hbm_gbs"])
+    traffic = traffic_for("k_gemv_a16", ["k_gemv.cu", "tq_internal.cuh"])
+    roof = {"bound": "hbm", "kernel": "k_gemv_a16<8,1,4>", "achieved": round(achieved, 1),
+            "peak": hbm, "peak_kind": f"{pk_kind} HBM copy", "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "traffic": traffic,
+            "bytes_per_launch_algorithmic": round(bytes_per_launch, 1)}
+    iso8 = dec8.isolated_call_us()
+    ms_e2e = time_steps(dec8.step_e2e, max(1, args.steps // 2), 2, world) / max(1, args.steps // 2)
+    e2e = {"value": round(dec8.weight_bytes / (ms_e2e * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": dec8.x_host.numel() * 2,
+           "d2h_bytes_per_step": dec8.y_host.numel() * 4}
+    launches = args.steps * args.calls
+    del dec8
+    torch.cuda.empty_cache()
+
+    # W4A16 decode beside it
+    extra = {}
+    try:
+        dec4 = Decode(4, args.calls, device, l2)
+        dec4.capture()
+        ms4 = time_steps(dec4.step, args.steps, args.warmup, world) / args.steps
+        a4 = dec4.weight_bytes / (ms4 * 1e-3) / 1e9
+        extra["decode_w4a16"] = {"value": round(a4 * world, 1), "unit": "GB/s",
+                                 "ms_per_step": round(ms4, 4), "frac": round(a4 / hbm, 4),
+                                 "isolated_call_us": round(dec4.isolated_call_us(), 2),
+                                 "layers": dec4.layers,
+                                 "distinct_weight_mb": round(dec4.distinct_bytes / 2 ** 20, 1)}
+        del dec4
+        torch.cuda.empty_cache()
+    except Exception as exc:  # reported, never hidden
+        extra["decode_w4a16"] = {"error": repr(exc)}
+
+    if not args.skip_dit:
+        try:
+            per, tops, gemm_tops = dit_measure(device)
+            bf16_peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+            extra["dit_w8a8_m4032"] = {
+                "value": round(tops, 2), "unit": "TOPS", "per_gemm": per,
+                "gemm_only_tops": round(gemm_tops, 2),
+                "roofline": {"bound": "tensor", "achieved": round(gemm_tops, 2),
+                             "peak": bf16_peak, "unit": "TFLOP/s",
+                             "peak_kind": f"{pk_kind} bf16 dense (int8 codes run on the bf16-class tensor path)",
+                             "frac": round(gemm_tops / bf16_peak, 4)}}
+        except Exception as exc:
+            extra["dit_w8a8_m4032"] = {"error": repr(exc)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        try:
+            cpu = cpu_oracle_decode(8)
+        except Exception as exc:
+            cpu = {"error": repr(exc)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8 x bf16 (fp32 sums)", "data": "synthetic",
+            "config": {"workload": "decode M=1 W8A16, Qwen2.5-0.5B-like FFN (gate/up 896->4864, "
+                                   "down 4864->896), 1000 seeded calls cycling gate, up, down",
+                       "calls_per_step": args.calls,
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks, "isolated_call_us": round(iso8, 2), **extra,
+        }
+        line["config"]["l2"] = (f"inputs larger than L2 ({l2 / 2 ** 20:.0f} MB): "
+                                f"{decode_layers(8, l2)} layer sets of weights cycled per step")
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,254 @@
+// C-ABI entry points of libtq: host-side validation, then dispatch to the
+// kernels.  Every check runs before any launch, and a refusal names its reason
+// (the pages' practice of refusing bad sizes "up front instead of failing
+// halfway": kvad-gpu internals, "Quantised weights on the GPU"; and of checking
+// every size product for overflow: TensorFold PR #948, review follow-up).
+
+#include <limits.h>
+
+#include "tq_internal.cuh"
+
+namespace tq {
+
+static thread_local int g_last_cuda_error = 0;
+
+// Status word written by kernels whose bounded waits expire.
+__device__ unsigned int g_status_word = 0;
+
+tq_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return TQ_ERR_CUDA;
+}
+
+unsigned int *status_word() {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    return static_cast<unsigned int *>(p);
+}
+
+tq_status current_device(DeviceInfo *out) {
+    static DeviceInfo cache[64];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return TQ_ERR_DEVICE;
+    }
+    if (dev < 64 && cache[dev].id == dev) {
+        *out = cache[dev];
+        return cache[dev].ok ? TQ_OK : TQ_ERR_DEVICE;
+    }
+    DeviceInfo d;
+    d.id = dev;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return TQ_ERR_DEVICE;
+    }
+    d.ok = (major == 10 && minor == 3);
+    if (dev < 64) cache[dev] = d;
+    *out = d;
+    return d.ok ? TQ_OK : TQ_ERR_DEVICE;
+}
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_k(int64_t K) {
+    if (K <= 0 || K > TQ_MAX_K) return false;
+    const int64_t t = K % kGroup;
+    return t == 0 || t == 32 || t == 64 || t == 128;
+}
+
+// a * b without int64 overflow, and within `limit`
+bool mul_ok(int64_t a, int64_t b, int64_t limit = INT64_MAX / 4) {
+    if (a < 0 || b < 0) return false;
+    if (a == 0 || b == 0) return true;
+    return a <= limit / b;
+}
+
+// Shared checks of a bf16 [rows, K] input with row stride ld.
+tq_status check_bf16_rows(const void *p, int64_t rows, int64_t K, int64_t ld) {
+    if (!p) return TQ_ERR_NULL;
+    if (ld < K) return TQ_ERR_SHAPE;
+    if (!mul_ok(rows, ld) || !mul_ok(rows * ld, 2)) return TQ_ERR_OVERFLOW;
+    if (!aligned(p, 16) || ld % 8) return TQ_ERR_ALIGN;
+    return TQ_OK;
+}
+
+tq_status check_output(const void *Y, int64_t M, int64_t N, int64_t ldy, int esize) {
+    if (!Y) return TQ_ERR_NULL;
+    if (ldy < N) return TQ_ERR_SHAPE;
+    if (!mul_ok(M, ldy) || !mul_ok(M * ldy, esize)) return TQ_ERR_OVERFLOW;
+    if (!aligned(Y, 16) || (ldy * esize) % 16) return TQ_ERR_ALIGN;
+    return TQ_OK;
+}
+
+tq_status check_weights(const void *Wq, const float *sw, int64_t N, int64_t K, int bits) {
+    if (bits != 8 && bits != 4) return TQ_ERR_BITS;
+    if (!Wq || !sw) return TQ_ERR_NULL;
+    if (!mul_ok(N, K)) return TQ_ERR_OVERFLOW;
+    if (!aligned(Wq, 16) || !aligned(sw, 4)) return TQ_ERR_ALIGN;
+    return TQ_OK;
+}
+
+int out_size(tq_out y) { return y == TQ_OUT_BF16 ? 2 : 4; }
+
+}  // namespace
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" {
+
+const char *tq_status_str(tq_status s) {
+    switch (s) {
+        case TQ_OK: return "TQ_OK";
+        case TQ_ERR_NULL: return "TQ_ERR_NULL: a required pointer is NULL";
+        case TQ_ERR_SHAPE: return "TQ_ERR_SHAPE: a size, stride or group width is not allowed";
+        case TQ_ERR_BITS: return "TQ_ERR_BITS: bits must be 8 or 4";
+        case TQ_ERR_MODE: return "TQ_ERR_MODE: unknown mode or output type, or bits disagree with the mode";
+        case TQ_ERR_OVERFLOW: return "TQ_ERR_OVERFLOW: a size product overflows";
+        case TQ_ERR_ALIGN: return "TQ_ERR_ALIGN: a pointer or stride breaks the 16-byte rule";
+        case TQ_ERR_WORKSPACE: return "TQ_ERR_WORKSPACE: workspace missing or too small";
+        case TQ_ERR_CUDA: return "TQ_ERR_CUDA: a CUDA call failed";
+        case TQ_ERR_DEVICE_TIMEOUT: return "TQ_ERR_DEVICE_TIMEOUT: a bounded device wait expired";
+        case TQ_ERR_DEVICE: return "TQ_ERR_DEVICE: no usable sm_103 device is current";
+    }
+    return "TQ_ERR_UNKNOWN";
+}
+
+int tq_last_cuda_error(void) { return g_last_cuda_error; }
+
+int tq_version(void) { return 100; }
+
+tq_status tq_quantize_weights(const void *W, int64_t N, int64_t K, int64_t ldw,
+                              int bits, int group, void *codes, float *scales,
+                              cudaStream_t stream) {
+    if (bits != 8 && bits != 4) return TQ_ERR_BITS;
+    if (group != kGroup || N < 0 || !valid_k(K)) return TQ_ERR_SHAPE;
+    if (N == 0) return TQ_OK;
+    tq_status st = check_bf16_rows(W, N, K, ldw);
+    if (st != TQ_OK) return st;
+    if (!codes || !scales) return TQ_ERR_NULL;
+    if (!mul_ok(N, K)) return TQ_ERR_OVERFLOW;
+    if (!aligned(codes, 16) || !aligned(scales, 4)) return TQ_ERR_ALIGN;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    return launch_quantize_weights(static_cast<const uint16_t *>(W), N, K, ldw, bits,
+                                   codes, scales, stream);
+}
+
+tq_status tq_rotate_quant_act(const void *X, int64_t M, int64_t K, int64_t ldx,
+                              int8_t *Xq, float *sx, cudaStream_t stream) {
+    if (M < 0 || !valid_k(K)) return TQ_ERR_SHAPE;
+    if (M == 0) return TQ_OK;
+    tq_status st = check_bf16_rows(X, M, K, ldx);
+    if (st != TQ_OK) return st;
+    if (!Xq || !sx) return TQ_ERR_NULL;
+    if (!mul_ok(M, K)) return TQ_ERR_OVERFLOW;
+    if (!aligned(Xq, 16) || !aligned(sx, 4)) return TQ_ERR_ALIGN;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    return launch_rotate_quant_act(static_cast<const uint16_t *>(X), M, K, ldx, Xq, sx, stream);
+}
+
+tq_status tq_rotate_act_bf16(const void *X, int64_t M, int64_t K, int64_t ldx,
+                             void *Xr, cudaStream_t stream) {
+    if (M < 0 || !valid_k(K)) return TQ_ERR_SHAPE;
+    if (M == 0) return TQ_OK;
+    tq_status st = check_bf16_rows(X, M, K, ldx);
+    if (st != TQ_OK) return st;
+    if (!Xr) return TQ_ERR_NULL;
+    if (!mul_ok(M, K) || !mul_ok(M * K, 2)) return TQ_ERR_OVERFLOW;
+    if (!aligned(Xr, 16)) return TQ_ERR_ALIGN;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    return launch_rotate_bf16(static_cast<const uint16_t *>(X), M, K, ldx,
+                              static_cast<uint16_t *>(Xr), stream);
+}
+
+size_t tq_linear_workspace_bytes(int64_t M, int64_t K, int64_t N, int bits, tq_mode mode) {
+    (void)N;
+    (void)bits;
+    if (mode != TQ_W8A8 || M <= 0 || K <= 0) return 0;
+    if (!mul_ok(M, K)) return 0;
+    // int8 codes [M, K] then fp32 token scales [M], each 256-byte aligned
+    const size_t codes = (static_cast<size_t>(M) * K + 255) / 256 * 256;
+    const size_t scales = (static_cast<size_t>(M) * 4 + 255) / 256 * 256;
+    return codes + scales;
+}
+
+tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
+                    const void *Wq, const float *sw, int64_t N, int bits,
+                    tq_mode mode, void *Y, tq_out ytype, int64_t ldy,
+                    void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (mode != TQ_W8A16 && mode != TQ_W4A16 && mode != TQ_W8A8) return TQ_ERR_MODE;
+    if (ytype != TQ_OUT_F32 && ytype != TQ_OUT_BF16) return TQ_ERR_MODE;
+    if (bits != 8 && bits != 4) return TQ_ERR_BITS;
+    if ((mode == TQ_W8A16 && bits != 8) || (mode == TQ_W4A16 && bits != 4)) return TQ_ERR_MODE;
+    if (M < 0 || N < 0 || !valid_k(K)) return TQ_ERR_SHAPE;
+    if (mode != TQ_W8A8 && M > TQ_MAX_M_A16) return TQ_ERR_SHAPE;
+    if (M == 0 || N == 0) return TQ_OK;
+    tq_status st = check_bf16_rows(X, M, K, ldx);
+    if (st != TQ_OK) return st;
+    if ((st = check_weights(Wq, sw, N, K, bits)) != TQ_OK) return st;
+    if ((st = check_output(Y, M, N, ldy, out_size(ytype))) != TQ_OK) return st;
+    const size_t need = tq_linear_workspace_bytes(M, K, N, bits, mode);
+    if (need > 0 && (!workspace || ws_bytes < need)) return TQ_ERR_WORKSPACE;
+    if (need > 0 && !aligned(workspace, 256)) return TQ_ERR_ALIGN;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    if (mode != TQ_W8A8) {
+        if (!gemv_fits(M, K, dev)) return TQ_ERR_SHAPE;
+        return launch_gemv_a16(static_cast<const uint16_t *>(X), M, K, ldx,
+                               static_cast<const uint8_t *>(Wq), sw, N, bits, Y,
+                               ytype == TQ_OUT_BF16 ? 1 : 0, ldy, dev, stream);
+    }
+    int8_t *Xq = static_cast<int8_t *>(workspace);
+    float *sx = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                          (static_cast<size_t>(M) * K + 255) / 256 * 256);
+    st = launch_rotate_quant_act(static_cast<const uint16_t *>(X), M, K, ldx, Xq, sx, stream);
+    if (st != TQ_OK) return st;
+    return launch_gemm_a8_mma(Xq, sx, M, K, static_cast<const uint8_t *>(Wq), sw, N, bits,
+                              Y, ytype == TQ_OUT_BF16 ? 1 : 0, ldy, stream);
+}
+
+tq_status tq_linear_q8(const int8_t *Xq, const float *sx, int64_t M, int64_t K,
+                       const void *Wq, const float *sw, int64_t N, int bits,
+                       void *Y, tq_out ytype, int64_t ldy, cudaStream_t stream) {
+    if (ytype != TQ_OUT_F32 && ytype != TQ_OUT_BF16 && ytype != TQ_OUT_I32) return TQ_ERR_MODE;
+    if (bits != 8 && bits != 4) return TQ_ERR_BITS;
+    if (M < 0 || N < 0 || !valid_k(K)) return TQ_ERR_SHAPE;
+    if (M == 0 || N == 0) return TQ_OK;
+    if (!Xq || (ytype != TQ_OUT_I32 && !sx)) return TQ_ERR_NULL;
+    if (!mul_ok(M, K)) return TQ_ERR_OVERFLOW;
+    if (!aligned(Xq, 16) || (sx && !aligned(sx, 4))) return TQ_ERR_ALIGN;
+    tq_status st = check_weights(Wq, sw, N, K, bits);
+    if (st != TQ_OK) return st;
+    if ((st = check_output(Y, M, N, ldy, out_size(ytype))) != TQ_OK) return st;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    return launch_gemm_a8_mma(Xq, sx, M, K, static_cast<const uint8_t *>(Wq), sw, N, bits, Y,
+                              static_cast<int>(ytype), ldy, stream);
+}
+
+tq_status tq_device_status(cudaStream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (v != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero));
+        if (e != cudaSuccess) return cuda_fail(e);
+        return TQ_ERR_DEVICE_TIMEOUT;
+    }
+    return TQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,177 @@
+// Internal declarations shared by the CUDA translation units of libtq.
+// Everything here runs on the device path; nothing is shared with the CPU
+// oracle that checks it.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tq.h"
+
+namespace tq {
+
+constexpr int kGroup = 256;       // rotation group width
+constexpr int kThreads = 256;     // threads of the row kernels
+
+// ---------------------------------------------------------------- host side
+
+struct DeviceInfo {
+    int id = -1;
+    int sms = 0;
+    int smem_optin = 0;      // max dynamic shared memory per block (bytes)
+    bool ok = false;         // compute capability 10.3
+};
+
+// Cached properties of the current device (TQ_ERR_DEVICE if none usable).
+tq_status current_device(DeviceInfo *out);
+// Records a CUDA error code for tq_last_cuda_error and returns TQ_ERR_CUDA.
+tq_status cuda_fail(cudaError_t e);
+// Device address of the library's status word on the current device.
+unsigned int *status_word();
+
+// Launchers (one per kernel family).  Arguments are validated by the caller.
+tq_status launch_quantize_weights(const uint16_t *W, int64_t N, int64_t K,
+                                  int64_t ldw, int bits, void *codes,
+                                  float *scales, cudaStream_t s);
+tq_status launch_rotate_quant_act(const uint16_t *X, int64_t M, int64_t K,
+                                  int64_t ldx, int8_t *Xq, float *sx,
+                                  cudaStream_t s);
+tq_status launch_rotate_bf16(const uint16_t *X, int64_t M, int64_t K,
+                             int64_t ldx, uint16_t *Xr, cudaStream_t s);
+
+// Skinny A16 product (M <= 64): rotation fused into the prologue.
+bool gemv_fits(int64_t M, int64_t K, const DeviceInfo &dev);
+tq_status launch_gemv_a16(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
+                          const uint8_t *Wq, const float *sw, int64_t N,
+                          int bits, void *Y, int ytype, int64_t ldy,
+                          const DeviceInfo &dev, cudaStream_t s);
+
+// A8 product on quantised activations: legacy mma.sync path (exact int32).
+tq_status launch_gemm_a8_mma(const int8_t *Xq, const float *sx, int64_t M,
+                             int64_t K, const uint8_t *Wq, const float *sw,
+                             int64_t N, int bits, void *Y, int ytype,
+                             int64_t ldy, cudaStream_t s);
+// A8 product on quantised activations: tcgen05 / TMEM path.
+tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M,
+                         int64_t K, const uint8_t *Wq, const float *sw,
+                         int64_t N, int bits, void *Y, int ytype, int64_t ldy,
+                         const DeviceInfo &dev, cudaStream_t s);
+
+// ---------------------------------------------------------------- device side
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// Widen E consecutive bf16 values (E in {1,2,4,8}) from an aligned pointer.
+template <int E, typename T>
+__device__ __forceinline__ void load_bf16(const uint16_t *p, T (&v)[8]) {
+    if constexpr (E == 8) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = static_cast<T>(__uint_as_float(w[i] << 16));
+            v[2 * i + 1] = static_cast<T>(__uint_as_float(w[i] & 0xFFFF0000u));
+        }
+    } else if constexpr (E == 4) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+        v[0] = static_cast<T>(__uint_as_float(u.x << 16));
+        v[1] = static_cast<T>(__uint_as_float(u.x & 0xFFFF0000u));
+        v[2] = static_cast<T>(__uint_as_float(u.y << 16));
+        v[3] = static_cast<T>(__uint_as_float(u.y & 0xFFFF0000u));
+    } else if constexpr (E == 2) {
+        const uint32_t u = __ldg(reinterpret_cast<const unsigned int *>(p));
+        v[0] = static_cast<T>(__uint_as_float(u << 16));
+        v[1] = static_cast<T>(__uint_as_float(u & 0xFFFF0000u));
+    } else {
+        v[0] = static_cast<T>(bf16_bits_to_f32(__ldg(reinterpret_cast<const unsigned short *>(p))));
+    }
+}
+
+// Unnormalised Walsh-Hadamard transform, natural (Sylvester) order, of one
+// group of 32*E values held E per lane (element index = lane*E + e): the
+// in-place butterfly (a, b) -> (a + b, a - b) over every bit of the index,
+// first the bits inside a lane, then the lane bits through shuffles.
+template <int E, typename T>
+__device__ __forceinline__ void warp_fwht(T (&v)[8]) {
+#pragma unroll
+    for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            if (!(i & h)) {
+                const T a = v[i], b = v[i + h];
+                v[i] = a + b;
+                v[i + h] = a - b;
+            }
+        }
+    }
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            const T o = __shfl_xor_sync(0xffffffffu, v[i], m);
+            v[i] = (lane & m) ? (o - v[i]) : (v[i] + o);
+        }
+    }
+}
+
+// Width of the group starting at column g0 of a K-wide row (256 or the tail).
+__device__ __forceinline__ int group_width(int64_t K, int64_t g0) {
+    const int64_t rest = K - g0;
+    return rest >= kGroup ? kGroup : static_cast<int>(rest);
+}
+
+// Rotate one group (width n = 32*E: 256, 128, 64 or 32) of a bf16 row in
+// fp32: v = c_n * Hs_n * x with c_n = sqrt(1/n) correctly rounded in fp32.
+template <int E>
+__device__ __forceinline__ void rotate_group32(const uint16_t *src, float (&v)[8]) {
+    const int lane = threadIdx.x & 31;
+    load_bf16<E, float>(src + lane * E, v);
+    warp_fwht<E, float>(v);
+    const float c = sqrtf(1.0f / (32.0f * E));
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = c * v[e];
+}
+
+// Returns E, the number of values each lane holds.
+__device__ __forceinline__ int rotate_group32_any(const uint16_t *src, int n, float (&v)[8]) {
+    switch (n) {
+        case 256: rotate_group32<8>(src, v); return 8;
+        case 128: rotate_group32<4>(src, v); return 4;
+        case 64: rotate_group32<2>(src, v); return 2;
+        default: rotate_group32<1>(src, v); return 1;
+    }
+}
+
+// ---- PTX wrappers
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Asynchronous prefetch of [p, p + bytes) into L2 (p and bytes 16-aligned).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+}  // namespace tq

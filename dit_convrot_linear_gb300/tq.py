@@ -1,0 +1,169 @@
+"""Python binding of ``libtq.so`` (the C ABI of ``include/tq.h``).
+
+Argument marshalling only: every step of the projection runs in the CUDA
+library.  Tensors are PyTorch device tensors (PyTorch provides memory and
+streams); the functions pass their pointers, sizes and the current stream to
+the C entry points of the same names and raise ``TQError`` on any status other
+than ``TQ_OK``.  There is no fallback: if the library is missing, ``load()``
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtq.so")
+
+TQ_OK = 0
+STATUS = {0: "TQ_OK", 1: "TQ_ERR_NULL", 2: "TQ_ERR_SHAPE", 3: "TQ_ERR_BITS",
+          4: "TQ_ERR_MODE", 5: "TQ_ERR_OVERFLOW", 6: "TQ_ERR_ALIGN",
+          7: "TQ_ERR_WORKSPACE", 8: "TQ_ERR_CUDA", 9: "TQ_ERR_DEVICE_TIMEOUT",
+          10: "TQ_ERR_DEVICE"}
+MODES = {"W8A16": 0, "W4A16": 1, "W8A8": 2}
+OUT = {"f32": 0, "bf16": 1, "i32": 2}
+
+# exported symbol -> (restype, argtypes)
+_P, _I, _Z, _C = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+SIGNATURES = {
+    "tq_status_str": (ctypes.c_char_p, [_C]),
+    "tq_last_cuda_error": (_C, []),
+    "tq_version": (_C, []),
+    "tq_quantize_weights": (_C, [_P, _I, _I, _I, _C, _C, _P, _P, _P]),
+    "tq_rotate_quant_act": (_C, [_P, _I, _I, _I, _P, _P, _P]),
+    "tq_rotate_act_bf16": (_C, [_P, _I, _I, _I, _P, _P]),
+    "tq_linear_workspace_bytes": (_Z, [_I, _I, _I, _C, _C]),
+    "tq_linear": (_C, [_P, _I, _I, _I, _P, _P, _I, _C, _C, _P, _C, _I, _P, _Z, _P]),
+    "tq_linear_q8": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
+    "tq_device_status": (_C, [_P]),
+}
+
+_lib = None
+
+
+class TQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        name = STATUS.get(status, str(status))
+        extra = ""
+        if status == 8 and _lib is not None:
+            extra = f" (cuda error {_lib.tq_last_cuda_error()})"
+        super().__init__(f"{where}: {name}{extra}")
+
+
+def load(path: str = LIB_PATH):
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "dit_convrot_linear_gb300.build.build()")
+        import torch  # noqa: F401  (load PyTorch's CUDA runtime first)
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def lib():
+    return load()
+
+
+def _stream(stream=None) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _check(rc: int, where: str):
+    if rc != TQ_OK:
+        raise TQError(rc, where)
+
+
+def status_str(s: int) -> str:
+    return lib().tq_status_str(s).decode()
+
+
+def version() -> int:
+    return lib().tq_version()
+
+
+def quantize_weights(W, bits: int, codes=None, scales=None, stream=None):
+    """bf16 W [N, K] (row stride W.stride(0)) -> (codes, fp32 scales [N])."""
+    import torch
+    N, K = W.shape
+    if codes is None:
+        codes = torch.empty((N, K if bits == 8 else K // 2),
+                            dtype=torch.int8 if bits == 8 else torch.uint8, device=W.device)
+    if scales is None:
+        scales = torch.empty(N, dtype=torch.float32, device=W.device)
+    _check(lib().tq_quantize_weights(_ptr(W), N, K, W.stride(0), bits, 256, _ptr(codes),
+                                     _ptr(scales), _stream(stream)), "tq_quantize_weights")
+    return codes, scales
+
+
+def rotate_quant_act(X, Xq=None, sx=None, stream=None):
+    import torch
+    M, K = X.shape
+    if Xq is None:
+        Xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    if sx is None:
+        sx = torch.empty(M, dtype=torch.float32, device=X.device)
+    _check(lib().tq_rotate_quant_act(_ptr(X), M, K, X.stride(0), _ptr(Xq), _ptr(sx),
+                                     _stream(stream)), "tq_rotate_quant_act")
+    return Xq, sx
+
+
+def rotate_act_bf16(X, Xr=None, stream=None):
+    import torch
+    M, K = X.shape
+    if Xr is None:
+        Xr = torch.empty((M, K), dtype=torch.bfloat16, device=X.device)
+    _check(lib().tq_rotate_act_bf16(_ptr(X), M, K, X.stride(0), _ptr(Xr), _stream(stream)),
+           "tq_rotate_act_bf16")
+    return Xr
+
+
+def linear_workspace_bytes(M: int, K: int, N: int, bits: int, mode: str) -> int:
+    return int(lib().tq_linear_workspace_bytes(M, K, N, bits, MODES[mode]))
+
+
+def linear(X, Wq, sw, N: int, bits: int, mode: str, Y=None, out: str = "f32",
+           workspace=None, stream=None):
+    """Y [M, N] = the rotated low-bit product of bf16 X [M, K] with (Wq, sw)."""
+    import torch
+    M, K = X.shape
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32 if out == "f32" else torch.bfloat16,
+                        device=X.device)
+    need = linear_workspace_bytes(M, K, N, bits, mode)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().tq_linear(_ptr(X), M, K, X.stride(0), _ptr(Wq), _ptr(sw), N, bits,
+                           MODES[mode], _ptr(Y), OUT[out], Y.stride(0), _ptr(workspace),
+                           ws_bytes, _stream(stream)), "tq_linear")
+    return Y
+
+
+def linear_q8(Xq, sx, Wq, sw, N: int, bits: int, Y=None, out: str = "f32", stream=None):
+    import torch
+    M, K = Xq.shape
+    if Y is None:
+        dt = {"f32": torch.float32, "bf16": torch.bfloat16, "i32": torch.int32}[out]
+        Y = torch.empty((M, N), dtype=dt, device=Xq.device)
+    _check(lib().tq_linear_q8(_ptr(Xq), _ptr(sx), M, K, _ptr(Wq), _ptr(sw), N, bits, _ptr(Y),
+                              OUT[out], Y.stride(0), _stream(stream)), "tq_linear_q8")
+    return Y
+
+
+def device_status(stream=None) -> int:
+    """Synchronise and return the library's device status (0 = TQ_OK)."""
+    return int(lib().tq_device_status(_stream(stream)))

@@ -1,0 +1,189 @@
+/*
+ * tq.h -- rotated low-bit linear projection on GB300 (sm_103a), C ABI.
+ *
+ * The method.  Weight rows are rotated by a normalised Hadamard matrix over
+ * every group of 256 input columns and quantised to int8 (or int4) with one
+ * fp32 scale per output row; the matching input rows get the same rotation,
+ * so the product is unchanged (tensai docs, "画像生成" / Image generation,
+ * sections "チェックポイントの入手" and "幅とメモリ").  The formats are
+ * TensorPencil's "INT8 ConvRot" and "INT4 ConvRot" (README, "Details").
+ *
+ * Readings where the pages are silent, fixed by this library:
+ *   - H is Sylvester's matrix, Hs[i][j] = (-1)^popcount(i & j), times
+ *     c_n = 1/sqrt(n), so H is symmetric and orthogonal.
+ *   - K is 256*q + t with t in {0, 32, 64, 128}; the last group of width
+ *     t < 256 uses its own H_t.
+ *   - Quantisation is symmetric, nearest-even: s = fp32(amax / qmax),
+ *     q = clamp(rint(v' / s), -qmax, qmax), qmax = 127 (8-bit) or 7 (4-bit).
+ *     A zero row (or one whose scale rounds to 0 in fp32) has s = 0 and all
+ *     codes 0.
+ *   - int4 codes are packed two per byte along K: byte k/2 holds code k (even
+ *     k) in its low nibble and code k+1 in its high nibble, two's complement.
+ *   - A8 activations: one int8 scale per token row over all of K (the pages
+ *     say only that the device quantises each product's activations finely;
+ *     tensai docs, section "GPU").
+ *   - A16 activations: the rotated row rounded to bf16 (nearest even).
+ *
+ * Conventions for every entry point.
+ *   - Every pointer is device memory owned by the caller (allocated, for
+ *     example, by PyTorch).  The library never allocates or frees memory,
+ *     never synchronises the host, and runs everything asynchronously on
+ *     `stream` (0 = the legacy default stream).
+ *   - All checks (null pointers, shapes, strides, alignment, 64-bit size
+ *     overflow, enum values) happen on the host before any launch; a refused
+ *     call launches nothing and returns the status naming the reason.
+ *   - A launch error is returned as TQ_ERR_CUDA; tq_last_cuda_error() gives
+ *     the CUDA error code.
+ *   - M == 0 or N == 0 is an empty call: TQ_OK, nothing launched.
+ *   - Inputs must be finite; non-finite bf16 inputs give unspecified codes.
+ *   - Strided inputs are honoured: X row m starts at X + m * ldx elements.
+ *   - Results are deterministic: the same inputs give the same bytes.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TQ_OK = 0,
+    TQ_ERR_NULL = 1,        /* a required pointer is NULL */
+    TQ_ERR_SHAPE = 2,       /* M, N, K, a stride or the group width is not allowed */
+    TQ_ERR_BITS = 3,        /* bits is not 8 or 4 */
+    TQ_ERR_MODE = 4,        /* unknown mode / output type, or bits disagree with mode */
+    TQ_ERR_OVERFLOW = 5,    /* a size product overflows 64 bits or a kernel index */
+    TQ_ERR_ALIGN = 6,       /* a pointer or stride breaks the alignment rule */
+    TQ_ERR_WORKSPACE = 7,   /* workspace missing or smaller than required */
+    TQ_ERR_CUDA = 8,        /* a CUDA call failed (see tq_last_cuda_error) */
+    TQ_ERR_DEVICE_TIMEOUT = 9, /* a bounded device-side wait expired */
+    TQ_ERR_DEVICE = 10      /* no usable sm_103 device is current */
+} tq_status;
+
+typedef enum {
+    TQ_W8A16 = 0,  /* int8 weights x rotated bf16 activations, fp32 sums */
+    TQ_W4A16 = 1,  /* int4 weights x rotated bf16 activations, fp32 sums */
+    TQ_W8A8 = 2    /* int8 (bits=8) or int4 (bits=4) weights x int8 activations */
+} tq_mode;
+
+typedef enum {
+    TQ_OUT_F32 = 0,
+    TQ_OUT_BF16 = 1,
+    TQ_OUT_I32 = 2  /* tq_linear_q8 only: the raw int32 code products */
+} tq_out;
+
+/* Largest K any entry point accepts. */
+#define TQ_MAX_K 65536
+/* Largest M the A16 modes accept (the skinny decode kernel). */
+#define TQ_MAX_M_A16 64
+
+/* Human-readable name of a status. Never NULL. */
+const char *tq_status_str(tq_status s);
+
+/* CUDA error code of the most recent TQ_ERR_CUDA on this host thread. */
+int tq_last_cuda_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int tq_version(void);
+
+/*
+ * Weight rotate + quantise + pack (one-time; tensai docs, "画像生成",
+ * section "チェックポイントの入手").
+ *
+ *   W       bf16 [N, K], row n at W + n * ldw elements; ldw >= K,
+ *           ldw % 8 == 0, W 16-byte aligned.
+ *   bits    8 or 4.
+ *   group   must be 256 (the group width of the method).
+ *   codes   bits = 8: int8 [N, K] dense (row stride K).
+ *           bits = 4: packed bytes [N, K / 2] dense, layout above.
+ *           16-byte aligned.
+ *   scales  fp32 [N], 4-byte aligned.
+ * Codes and scales are bit-exact with an fp64 explicit-product reference for
+ * every row whose group sums are exact in fp64 (true whenever a group's
+ * nonzero magnitudes span fewer than about 37 binades).
+ */
+tq_status tq_quantize_weights(const void *W, int64_t N, int64_t K, int64_t ldw,
+                              int bits, int group, void *codes, float *scales,
+                              cudaStream_t stream);
+
+/*
+ * Activation rotation (256-wide fast Walsh-Hadamard transform, fp32) fused
+ * with per-token symmetric int8 quantisation (tensai docs, "画像生成", sections
+ * "幅とメモリ" and "GPU").
+ *
+ *   X   bf16 [M, K], row m at X + m * ldx; ldx >= K, ldx % 8 == 0,
+ *       X 16-byte aligned.
+ *   Xq  int8 [M, K] dense, 16-byte aligned.
+ *   sx  fp32 [M]: the token scales, s = amax / 127.
+ * The transform sums in fp32, so a code may differ by one from the fp64
+ * reference where the sum lands within rounding of a .5 boundary.
+ */
+tq_status tq_rotate_quant_act(const void *X, int64_t M, int64_t K, int64_t ldx,
+                              int8_t *Xq, float *sx, cudaStream_t stream);
+
+/*
+ * Activation rotation rounded to bf16: the A16 operand (same passages).
+ *   X   as tq_rotate_quant_act.
+ *   Xr  bf16 [M, K] dense, 16-byte aligned.
+ */
+tq_status tq_rotate_act_bf16(const void *X, int64_t M, int64_t K, int64_t ldx,
+                             void *Xr, cudaStream_t stream);
+
+/*
+ * Bytes of workspace tq_linear needs for these sizes (0 when none).  The
+ * projections are about 80% of a DiT step's GPU time (TensorFold PR #948,
+ * "What comes next" and "Receipts").
+ */
+size_t tq_linear_workspace_bytes(int64_t M, int64_t K, int64_t N, int bits,
+                                 tq_mode mode);
+
+/*
+ * The rotated low-bit linear projection: Y[m][n] = sum_k W[n][k] x[m][k],
+ * computed on the rotated, quantised operands.
+ *
+ *   X        bf16 [M, K] (unrotated), layout as tq_rotate_quant_act.
+ *   Wq, sw   codes and row scales from tq_quantize_weights with `bits`.
+ *   mode     TQ_W8A16 (bits = 8) or TQ_W4A16 (bits = 4): M <= 64; the
+ *            rotated activations are rounded to bf16 and multiplied with the
+ *            weight codes in fp32, Y = sw[n] * sum_k q_w x'_bf16.
+ *            TQ_W8A8 (bits = 8 or 4): activations are quantised per token
+ *            (tq_rotate_quant_act) and Y = sx[m] * sw[n] * acc[m][n], acc the
+ *            exact int32 sum of code products.
+ *   Y        fp32 or bf16 [M, N], row m at Y + m * ldy; ldy >= N; Y 16-byte
+ *            aligned and ldy * element size a multiple of 16 bytes.
+ *   workspace, ws_bytes   device scratch of at least
+ *            tq_linear_workspace_bytes(M, K, N, bits, mode) bytes, 256-byte
+ *            aligned (may be NULL when that is 0).  Its contents on entry do
+ *            not matter; the call overwrites it.
+ */
+tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
+                    const void *Wq, const float *sw, int64_t N, int bits,
+                    tq_mode mode, void *Y, tq_out ytype, int64_t ldy,
+                    void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * The A8 product on activations that are already rotated and quantised
+ * (tq_rotate_quant_act): Y = sx[m] * sw[n] * acc[m][n].
+ *   Xq   int8 [M, K] dense, 16-byte aligned;  sx fp32 [M].
+ *   ytype TQ_OUT_I32 writes acc itself (int32 [M, N], ldy as for fp32).
+ */
+tq_status tq_linear_q8(const int8_t *Xq, const float *sx, int64_t M, int64_t K,
+                       const void *Wq, const float *sw, int64_t N, int bits,
+                       void *Y, tq_out ytype, int64_t ldy, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device.  Returns TQ_ERR_DEVICE_TIMEOUT if a bounded
+ * device-side wait expired in any call since the last check (that call's
+ * output is then invalid), TQ_ERR_CUDA on a CUDA error, else TQ_OK.
+ */
+tq_status tq_device_status(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H */
