@@ -1,0 +1,483 @@
+// A8 product on the 5th-generation tensor cores (tcgen05, TMEM accumulators):
+//   acc[m][n] = sum_k Xq[m][k] * Wq[n][k]  (exact int32),
+//   Y[m][n]   = (sx[m] * sw[n]) * acc[m][n].
+// The DiT projections at large M are compute-bound (kvad-gpu internals,
+// "Quantised weights on the GPU": past the crossover every matmul is real
+// work); they are about 80% of a denoising step (TensorFold PR #948, "What
+// comes next").
+//
+// sm_103a has no integer tcgen05 MMA, so the codes are widened to fp16 (every
+// int8 and int4 code is exact in fp16; every product, at most 127*127, is
+// exact in fp32) and multiplied by tcgen05.mma kind::f16 into an fp32 TMEM
+// accumulator.  An fp32 sum of integers stays exact while every partial sum
+// is below 2^24, which 1024 products of int8 codes (1024 * 127^2 < 2^24) or
+// 16384 products of int8 x int4 codes (16384 * 127 * 7 < 2^24) guarantee.  So
+// the accumulator is drained every such chunk of K into an exact int32 running
+// sum kept in a second TMEM region, and the result is bit-exact int32.
+//
+// Tile 128 (M) x 256 (N) x 64 (K) per stage, 4 stages, one CTA per SM,
+// persistent over tiles.  Warp roles:
+//   warps 0-7   convert: load int8/int4 codes with 16-byte loads, widen to
+//               fp16 in registers, store the K-major 8x8 core-matrix layout
+//               the MMA reads (no swizzle), signal the stage full;
+//   warp 8      allocates TMEM; lane 0 issues the MMAs and the commits;
+//   warps 9-12  drain the accumulator (one TMEM lane quarter each) and write Y.
+// Every wait is bounded: on expiry the CTA records the failure in the library
+// status word, stops issuing work, lets in-flight MMAs finish (bounded), frees
+// its TMEM and returns.
+
+#include "tq_internal.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int NCONV = 8, MMA_WARP = 8, EPI0 = 9, NWARPS = 13;
+constexpr int THREADS = NWARPS * 32;
+constexpr int A_STAGE = BM * BK * 2;   // 16 KB fp16
+constexpr int B_STAGE = BN * BK * 2;   // 32 KB fp16
+constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024;
+constexpr uint32_t TMEM_COLS = 512;    // acc [0, 256) + running int32 sum [256, 512)
+constexpr uint32_t RUN_COL = 256;
+constexpr long long kWaitLimit = 4000000000ll;  // clock cycles, about 2 s
+constexpr unsigned int kStatusGemmTimeout = 2u;
+// instruction descriptor: D f32, A/B f16, K-major, N = 256, M = 128
+constexpr uint32_t IDESC = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+
+struct TcParams {
+    const int8_t *Xq;
+    const float *sx;
+    int64_t M, K;
+    const uint8_t *Wq;
+    const float *sw;
+    int64_t N;
+    void *Y;
+    int64_t ldy;
+    int ytype;            // 0 fp32, 1 bf16, 2 int32
+    int mtiles, ntiles, ksteps, chunk_steps;
+    unsigned int *status;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// byte offset of (row r, k) in a [rows x 64] fp16 tile of 8x8 core matrices:
+// core matrix (r/8, k/8) is 128 contiguous bytes, K-adjacent ones 128 bytes
+// apart (leading offset), row groups 1024 bytes apart (stride offset)
+__device__ __forceinline__ int cm_off(int r, int k) {
+    return ((r >> 3) * 8 + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+    constexpr uint64_t lbo = 128, sbo = 1024;
+    return static_cast<uint64_t>((addr & 0x3FFFF) >> 4) | ((lbo >> 4) << 16) | ((sbo >> 4) << 32) |
+           (1ull << 46);
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; on expiry raises the CTA abort flag and the status word.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          unsigned int *status) {
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity)) {
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimit) {
+            *abort = 1;
+            atomicOr(status, kStatusGemmTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// four int8 codes -> fp16 pairs (k0,k1), (k2,k3): 0x64xx is 1024 + xx, and
+// xx = code + 128 after flipping the sign bit; subtract 1152.
+__device__ __forceinline__ void widen8(uint32_t w, uint32_t &p01, uint32_t &p23) {
+    const uint32_t u = w ^ 0x80808080u;
+    p01 = hsub2(prmt(u, 0x64646464u, 0x4140u), 0x64806480u);
+    p23 = hsub2(prmt(u, 0x64646464u, 0x4342u), 0x64806480u);
+}
+
+// eight int4 codes (low nibble first) -> fp16 pairs (k0,k1) .. (k6,k7).  With
+// u = code + 8: the low half is 0x6400 | u = 1024 + u, the high half
+// 0x6400 | (u << 4) = 1024 + 16u; one fma with (1, 1/16) and (-1032, -72).
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t (&p)[4]) {
+    const uint32_t u = w ^ 0x88888888u;
+    const uint32_t scale = 0x2C003C00u;   // (1/16, 1.0)
+    const uint32_t bias = 0xD480E408u;    // (-72, -1032)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t t = prmt(u, 0u, 0x4040u + 0x0101u * i);  // byte i in both halves
+        p[i] = hfma2((t & 0x00F0000Fu) | 0x64006400u, scale, bias);
+    }
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+          "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+          "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]),
+          "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+          "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 ldg16(const void *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(THREADS, 1)
+k_gemm_a8_tc(const TcParams p) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    unsigned char *sA = smem;
+    unsigned char *sB = smem + STAGES * A_STAGE;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * (A_STAGE + B_STAGE));
+    // bars: full[STAGES], empty[STAGES], acc_full, acc_empty, done
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+    const uint32_t acc_full = smem_u32(bars + 2 * STAGES), acc_empty = smem_u32(bars + 2 * STAGES + 1);
+    const uint32_t done = smem_u32(bars + 2 * STAGES + 2);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * s), "r"(NCONV * 32));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(empty0 + 8 * s));
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(acc_full));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(acc_empty));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        abort_sh = 0;
+    }
+    if (warp == MMA_WARP) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&tmem_base_sh)), "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = tmem_base_sh;
+
+    const int ntiles_total = p.mtiles * p.ntiles;
+    const int64_t wld = BITS == 8 ? p.K : p.K / 2;
+
+    if (warp < NCONV) {
+        // ------------------------------------------------ converters
+        const int tid = threadIdx.x;  // 0..255
+        uint32_t it = 0;
+        for (int tile = blockIdx.x; tile < ntiles_total && !abort_sh; tile += gridDim.x) {
+            const int64_t m0 = static_cast<int64_t>(tile % p.mtiles) * BM;
+            const int64_t n0 = static_cast<int64_t>(tile / p.mtiles) * BN;
+            for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
+                const int s = it % STAGES;
+                const int64_t k0 = static_cast<int64_t>(ks) * BK;
+                // global loads first (independent of the stage being free)
+                uint4 ra[2], rb[4];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int c = tid + 256 * j, r = c >> 2, seg = c & 3;
+                    const int64_t gm = m0 + r, gk = k0 + seg * 16;
+                    ra[j] = (gm < p.M && gk < p.K) ? ldg16(p.Xq + gm * p.K + gk) : make_uint4(0, 0, 0, 0);
+                }
+                if constexpr (BITS == 8) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int c = tid + 256 * j, r = c >> 2, seg = c & 3;
+                        const int64_t gn = n0 + r, gk = k0 + seg * 16;
+                        rb[j] = (gn < p.N && gk < p.K) ? ldg16(p.Wq + gn * wld + gk) : make_uint4(0, 0, 0, 0);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int c = tid + 256 * j, r = c >> 1, seg = c & 1;
+                        const int64_t gn = n0 + r, gk = k0 + seg * 32;
+                        rb[j] = (gn < p.N && gk < p.K) ? ldg16(p.Wq + gn * wld + gk / 2) : make_uint4(0, 0, 0, 0);
+                    }
+                }
+                if (!mbar_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1, &abort_sh, p.status)) break;
+                unsigned char *a = sA + s * A_STAGE;
+                unsigned char *b = sB + s * B_STAGE;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int c = tid + 256 * j, r = c >> 2, seg = c & 3;
+                    uint4 lo, hi;
+                    widen8(ra[j].x, lo.x, lo.y);
+                    widen8(ra[j].y, lo.z, lo.w);
+                    widen8(ra[j].z, hi.x, hi.y);
+                    widen8(ra[j].w, hi.z, hi.w);
+                    *reinterpret_cast<uint4 *>(a + cm_off(r, seg * 16)) = lo;
+                    *reinterpret_cast<uint4 *>(a + cm_off(r, seg * 16 + 8)) = hi;
+                }
+                if constexpr (BITS == 8) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int c = tid + 256 * j, r = c >> 2, seg = c & 3;
+                        uint4 lo, hi;
+                        widen8(rb[j].x, lo.x, lo.y);
+                        widen8(rb[j].y, lo.z, lo.w);
+                        widen8(rb[j].z, hi.x, hi.y);
+                        widen8(rb[j].w, hi.z, hi.w);
+                        *reinterpret_cast<uint4 *>(b + cm_off(r, seg * 16)) = lo;
+                        *reinterpret_cast<uint4 *>(b + cm_off(r, seg * 16 + 8)) = hi;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int c = tid + 256 * j, r = c >> 1, seg = c & 1;
+                        const uint32_t w[4] = {rb[j].x, rb[j].y, rb[j].z, rb[j].w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t pr[4];
+                            widen4(w[q], pr);
+                            *reinterpret_cast<uint4 *>(b + cm_off(r, seg * 32 + q * 8)) =
+                                make_uint4(pr[0], pr[1], pr[2], pr[3]);
+                        }
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(full0 + 8 * s);
+            }
+        }
+    } else if (warp == MMA_WARP) {
+        // ------------------------------------------------ MMA issue (one thread)
+        if (lane == 0) {
+            uint32_t it = 0, ch = 0;
+            bool issued = false;
+            for (int tile = blockIdx.x; tile < ntiles_total && !abort_sh; tile += gridDim.x) {
+                for (int c0 = 0; c0 < p.ksteps && !abort_sh; c0 += p.chunk_steps) {
+                    const int c1 = min(c0 + p.chunk_steps, p.ksteps);
+                    if (ch > 0 && !mbar_wait(acc_empty, (ch - 1) & 1, &abort_sh, p.status)) break;
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    for (int ks = c0; ks < c1; ++ks, ++it) {
+                        const int s = it % STAGES;
+                        if (!mbar_wait(full0 + 8 * s, (it / STAGES) & 1, &abort_sh, p.status)) break;
+                        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                        const uint32_t a = smem_u32(sA + s * A_STAGE), b = smem_u32(sB + s * B_STAGE);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            const uint64_t ad = smem_desc(a + kk * 256), bd = smem_desc(b + kk * 256);
+                            const uint32_t accum = (ks > c0 || kk > 0) ? 1u : 0u;
+                            asm volatile(
+                                "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+                                ::"r"(tmem), "l"(ad), "l"(bd), "r"(IDESC), "r"(accum));
+                        }
+                        issued = true;
+                        asm volatile(
+                            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                            ::"r"(empty0 + 8 * s) : "memory");
+                    }
+                    if (abort_sh) break;
+                    asm volatile(
+                        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                        ::"r"(acc_full) : "memory");
+                    ++ch;
+                }
+            }
+            // let every issued MMA finish before the TMEM is released
+            if (issued) {
+                asm volatile(
+                    "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                    ::"r"(done) : "memory");
+                const long long t0 = clock64();
+                while (!mbar_try(done, 0) && clock64() - t0 < kWaitLimit) {
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (TMEM drain)
+        const int q = warp & 3;                       // TMEM lane quarter of this warp
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        uint32_t ch = 0;
+        const bool vec_ok = p.ytype == 0 ? ((reinterpret_cast<uintptr_t>(p.Y) & 15) == 0 && (p.ldy & 3) == 0)
+                          : p.ytype == 1 ? ((reinterpret_cast<uintptr_t>(p.Y) & 15) == 0 && (p.ldy & 7) == 0)
+                                         : ((reinterpret_cast<uintptr_t>(p.Y) & 15) == 0 && (p.ldy & 3) == 0);
+        for (int tile = blockIdx.x; tile < ntiles_total && !abort_sh; tile += gridDim.x) {
+            const int64_t m0 = static_cast<int64_t>(tile % p.mtiles) * BM;
+            const int64_t n0 = static_cast<int64_t>(tile / p.mtiles) * BN;
+            const int64_t m = m0 + q * 32 + lane;
+            for (int c0 = 0; c0 < p.ksteps; c0 += p.chunk_steps, ++ch) {
+                const bool first = c0 == 0;
+                if (!mbar_wait(acc_full, ch & 1, &abort_sh, p.status)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                for (int col = 0; col < BN; col += 32) {
+                    uint32_t v[32], r[32];
+                    tmem_ld32(tmem + lane_base + col, v);
+                    if (!first) tmem_ld32(tmem + lane_base + RUN_COL + col, r);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int x = __float2int_rn(__uint_as_float(v[j]));
+                        r[j] = first ? static_cast<uint32_t>(x) : static_cast<uint32_t>(static_cast<int>(r[j]) + x);
+                    }
+                    tmem_st32(tmem + lane_base + RUN_COL + col, r);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+            }
+            if (abort_sh) break;
+            // the tile's exact int32 sums are in the running region: write Y
+            const float xs = (p.ytype == 2 || m >= p.M) ? 1.0f : p.sx[m];
+            for (int col = 0; col < BN; col += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + RUN_COL + col, r);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (m >= p.M) continue;
+                const int64_t nb = n0 + col;
+                if (p.ytype == 2) {
+                    int32_t *y = static_cast<int32_t *>(p.Y) + m * p.ldy + nb;
+                    if (vec_ok && nb + 32 <= p.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<uint4 *>(y + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+                    } else {
+                        for (int j = 0; j < 32; ++j)
+                            if (nb + j < p.N) y[j] = static_cast<int32_t>(r[j]);
+                    }
+                    continue;
+                }
+                float f[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int64_t n = nb + j;
+                    const float wsc = n < p.N ? __ldg(p.sw + n) : 0.0f;
+                    f[j] = (xs * wsc) * static_cast<float>(static_cast<int>(r[j]));
+                }
+                if (p.ytype == 0) {
+                    float *y = static_cast<float *>(p.Y) + m * p.ldy + nb;
+                    if (vec_ok && nb + 32 <= p.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4 *>(y + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+                    } else {
+                        for (int j = 0; j < 32; ++j)
+                            if (nb + j < p.N) y[j] = f[j];
+                    }
+                } else {
+                    uint16_t *y = static_cast<uint16_t *>(p.Y) + m * p.ldy + nb;
+                    if (vec_ok && nb + 32 <= p.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 8) {
+                            uint4 u;
+                            u.x = f32_to_bf16_bits(f[j]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[j + 1])) << 16);
+                            u.y = f32_to_bf16_bits(f[j + 2]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[j + 3])) << 16);
+                            u.z = f32_to_bf16_bits(f[j + 4]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[j + 5])) << 16);
+                            u.w = f32_to_bf16_bits(f[j + 6]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[j + 7])) << 16);
+                            *reinterpret_cast<uint4 *>(y + j) = u;
+                        }
+                    } else {
+                        for (int j = 0; j < 32; ++j)
+                            if (nb + j < p.N) y[j] = f32_to_bf16_bits(f[j]);
+                    }
+                }
+            }
+        }
+    }
+
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+    }
+}
+
+}  // namespace
+
+tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M, int64_t K,
+                         const uint8_t *Wq, const float *sw, int64_t N, int bits,
+                         void *Y, int ytype, int64_t ldy, const DeviceInfo &dev,
+                         cudaStream_t s) {
+    unsigned int *status = status_word();
+    if (!status) return TQ_ERR_DEVICE;
+    TcParams p{};
+    p.Xq = Xq;
+    p.sx = sx;
+    p.M = M;
+    p.K = K;
+    p.Wq = Wq;
+    p.sw = sw;
+    p.N = N;
+    p.Y = Y;
+    p.ldy = ldy;
+    p.ytype = ytype;
+    p.mtiles = static_cast<int>((M + BM - 1) / BM);
+    p.ntiles = static_cast<int>((N + BN - 1) / BN);
+    p.ksteps = static_cast<int>((K + BK - 1) / BK);
+    // K per exact fp32 chunk: 1024 * 127^2 < 2^24 (int8), 16384 * 127 * 7 < 2^24 (int4)
+    p.chunk_steps = bits == 8 ? 1024 / BK : 16384 / BK;
+    p.status = status;
+    const int64_t tiles = static_cast<int64_t>(p.mtiles) * p.ntiles;
+    if (tiles > (1ll << 31) - 1) return TQ_ERR_OVERFLOW;
+    auto kern = bits == 8 ? k_gemm_a8_tc<8> : k_gemm_a8_tc<4>;
+    static int configured_for[64][2] = {{0}};
+    const int bi = bits == 8 ? 0 : 1;
+    if (dev.id >= 0 && dev.id < 64 && !configured_for[dev.id][bi]) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e);
+        configured_for[dev.id][bi] = 1;
+    }
+    const unsigned grid = static_cast<unsigned>(tiles < dev.sms ? tiles : dev.sms);
+    kern<<<grid, THREADS, SMEM_BYTES, s>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+}  // namespace tq

@@ -5,21 +5,27 @@
 // the product gets the same rotation as the weights).  Decode is bound by the
 // weight stream (kvad-gpu internals, "Numbers": decode is memory-bound).
 //
-// Design (one launch, no workspace):
-//   - A CTA owns RT = 16*WR weight rows and a K range of whole 256-groups;
-//     C CTAs of a thread-block cluster split K, and their partial sums are
-//     added in a fixed order through distributed shared memory (no float
-//     atomics, so repeated calls give identical bytes).
-//   - Prologue: the CTA rotates its K range of every token row in fp32 (warp
-//     butterfly), rounds to bf16 and keeps it in shared memory, laid out so
-//     that each mma B fragment is one conflict-free 8-byte load.
-//   - Main loop: each lane streams 16-byte chunks of two weight rows with
-//     non-allocating loads, PF blocks ahead, widens int8/int4 codes to bf16
-//     pairs in registers (exact integers), and feeds mma.sync m16n8k16.
-//   - Programmatic dependent launch: the CTA lets the next kernel launch at
-//     once, prefetches its weight rows into L2 (L2 is coherent, so this is
-//     safe before the dependency is met), then waits for the previous kernel
-//     before it reads X or writes Y.
+// One call moves a few MB, so latency, not bandwidth, decides its time.  The
+// kernel is laid out so that the weight stream never waits for anything:
+//   1. Each CTA owns RT = 16*WR weight rows and a K range of whole 256-groups
+//      (C CTAs of a thread-block cluster split K).  Its first thread issues
+//      bulk copies (cp.async.bulk, through L2) of the CTA's whole weight slice
+//      into shared memory, then lets the next kernel on the stream launch
+//      (programmatic dependent launch), so the next calls' weight streams
+//      start while this call still computes.
+//   2. Only then does it wait for the previous kernel (griddepcontrol.wait),
+//      rotate its K range of every token row in fp32 (warp butterfly), round
+//      to bf16 and keep it in shared memory.
+//   3. Warps widen int8/int4 codes to exact bf16 pairs in registers and feed
+//      mma.sync m16n8k16 from shared memory.
+//   4. Partial sums are added in a fixed order: warps along K through shared
+//      memory, then the CTAs of the cluster through distributed shared memory
+//      (no atomics: repeated calls give identical bytes).
+// Weights are read before the wait, so Wq/sw must not be written by a kernel
+// that may still be running when this one starts (only this library's product
+// kernels trigger early, and they write Y alone).
+// Every wait is bounded: on expiry the kernel sets the library status word and
+// skips its arithmetic (tq_device_status reports it), never hangs.
 
 #include <cooperative_groups.h>
 
@@ -44,12 +50,17 @@ struct GemvParams {
     int64_t ldy;
     int ytype;      // 0 fp32, 1 bf16
     int WR, WK, C;  // warps along rows, warps along K, cluster size
-    int SX;         // shared-memory row stride of x' (bf16 elements)
+    int WS;         // shared row stride of the weight slice (bytes, = 64 mod 128)
+    int SX;         // shared row stride of x' (bf16 elements, 2*SX = 32 mod 128)
+    int w_off, x_off;  // byte offsets of the weight slice and of x' in shared memory
+    unsigned int *status;
 };
 
-// Each lane's 16-byte chunk of a block covers the block's k in a fixed way;
-// x' is stored so that the 4 values one lane needs for one mma (its k-slots
-// 2t, 2t+1, 2t+8, 2t+9) are contiguous at jj*16 + 4t.
+constexpr long long kWaitLimit = 4000000000ll;  // clock cycles (about 2 s)
+constexpr unsigned int kStatusGemvTimeout = 1u;
+
+// x' layout inside each K block so that the 4 values one lane needs for one
+// mma (its k-slots 2t, 2t+1, 2t+8, 2t+9) are contiguous at jj*16 + 4t.
 //   int8 (64 k per block):  lane t holds k = 16t..16t+15; word q -> mma q,
 //     pairs (k0, k2) and (k1, k3) of the word.
 //   int4 (128 k per block): lane t holds k = 32t..32t+31; word q -> mmas 2q
@@ -101,11 +112,35 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int BITS, int NT, int PF>
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity))
+        if (clock64() - t0 > kWaitLimit) return false;
+    return true;
+}
+
+template <int BITS, int NT>
 __global__ void __launch_bounds__(kThreads)
 k_gemv_a16(const GemvParams p) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem_raw);
+    unsigned char *ws = smem_raw + p.w_off;
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw + p.x_off);
     constexpr int KB = BITS == 8 ? 64 : 128;  // k per block
     constexpr int BB = 64;                    // bytes per row per block
 
@@ -122,15 +157,36 @@ k_gemv_a16(const GemvParams p) {
     const int nblk = (nk + KB - 1) / KB;
     const int64_t wbyte0 = kbeg * BITS / 8;
     const int rbytes = nk * BITS / 8;  // this CTA's bytes of one weight row
+    const int rows = static_cast<int>(min(static_cast<int64_t>(RT), p.N - n0));
+    const uint32_t wbar = smem_addr(bar);
 
-    pdl_launch_dependents();
-    for (int r = threadIdx.x; r < RT; r += kThreads) {
-        const int64_t n = n0 + r;
-        if (n < p.N && rbytes > 0) prefetch_l2(p.W + n * p.wld + wbyte0, static_cast<uint32_t>(rbytes));
+    // ---- 1. weight slice -> shared memory, before anything else
+    if (warp == 0) {
+        if (lane == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(wbar));
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(wbar),
+                         "r"(static_cast<uint32_t>(rows * rbytes))
+                         : "memory");
+        }
+        __syncwarp();
+        for (int r = lane; r < rows; r += 32) {
+            const unsigned char *src = p.W + (n0 + r) * p.wld + wbyte0;
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                ::"r"(smem_addr(ws + r * p.WS)), "l"(src), "r"(static_cast<uint32_t>(rbytes)), "r"(wbar)
+                : "memory");
+        }
+    } else if (warp == 1) {
+        // the token rows this CTA rotates: warm L2 (coherent, so safe before the wait)
+        for (int m = lane; m < p.M; m += 32)
+            prefetch_l2(p.X + m * p.ldx + kbeg, static_cast<uint32_t>(nk * 2));
     }
+    pdl_launch_dependents();
     pdl_wait();
+    __syncthreads();  // barrier initialised before anyone waits on it
 
-    // ---- prologue: rotated, bf16-rounded x' of this K range in shared memory
+    // ---- 2. rotated, bf16-rounded x' of this K range in shared memory
     const int M = p.M, SX = p.SX;
     if (nblk > 0) {
         const int z0 = (nblk - 1) * KB;  // the last block may be partial: zero it
@@ -154,21 +210,21 @@ k_gemv_a16(const GemvParams p) {
     }
     __syncthreads();
 
-    // ---- main loop
+    // ---- 3. products from shared memory
+    const bool have_w = mbar_wait_bounded(wbar, 0);
+    if (!have_w && threadIdx.x == 0) atomicOr(p.status, kStatusGemvTimeout);
     const int WR = p.WR, WK = p.WK;
     const int wr = warp % WR, wk = warp / WR;
     const int g = lane >> 2, t = lane & 3;
-    const int64_t rA = n0 + wr * 16 + g, rB = rA + 8;
-    const bool okA = rA < p.N, okB = rB < p.N;
-    const uint8_t *pA = p.W + (okA ? rA : 0) * p.wld + wbyte0 + t * 16;
-    const uint8_t *pB = p.W + (okB ? rB : 0) * p.wld + wbyte0 + t * 16;
-    const int nbw = nblk > wk ? (nblk - wk + WK - 1) / WK : 0;
+    const int rA = wr * 16 + g, rB = rA + 8;
+    const bool okA = rA < rows, okB = rB < rows;
+    const unsigned char *pA = ws + rA * p.WS + t * 16;
+    const unsigned char *pB = ws + rB * p.WS + t * 16;
+    const int nbw = (have_w && nblk > wk) ? (nblk - wk + WK - 1) / WK : 0;
 
     float acc[NT][4];
 #pragma unroll
     for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-
-    // B fragment base for each n-tile (token nt*8 + g); tokens >= M read zeros
     const uint16_t *xb[NT];
     bool xin[NT];
 #pragma unroll
@@ -177,13 +233,6 @@ k_gemv_a16(const GemvParams p) {
         xin[nt] = tok < M;
         xb[nt] = xs + (xin[nt] ? tok : 0) * SX + 4 * t;
     }
-
-    auto load = [&](int i, uint4 &a, uint4 &b) {
-        const int off = (wk + i * WK) * BB;
-        const bool in = (i < nbw) && (off + t * 16 < rbytes);
-        a = (in && okA) ? ldg_stream(pA + off) : make_uint4(0, 0, 0, 0);
-        b = (in && okB) ? ldg_stream(pB + off) : make_uint4(0, 0, 0, 0);
-    };
     auto mma_all = [&](int blk, int jj, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -192,44 +241,37 @@ k_gemv_a16(const GemvParams p) {
             mma_bf16(acc[nt], a0, a1, a2, a3, bv.x, bv.y);
         }
     };
-
-    uint4 ra[PF], rb[PF];
+    for (int i = 0; i < nbw; ++i) {
+        const int blk = wk + i * WK;
+        const int off = blk * BB;
+        const bool in = off + t * 16 < rbytes;
+        const uint4 wa = (in && okA) ? *reinterpret_cast<const uint4 *>(pA + off) : make_uint4(0, 0, 0, 0);
+        const uint4 wb = (in && okB) ? *reinterpret_cast<const uint4 *>(pB + off) : make_uint4(0, 0, 0, 0);
+        const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w};
+        const uint32_t B[4] = {wb.x, wb.y, wb.z, wb.w};
+        if constexpr (BITS == 8) {
 #pragma unroll
-    for (int s = 0; s < PF; ++s) load(s, ra[s], rb[s]);
-    for (int i0 = 0; i0 < nbw; i0 += PF) {
-#pragma unroll
-        for (int s = 0; s < PF; ++s) {
-            const int i = i0 + s;
-            if (i < nbw) {
-                const int blk = wk + i * WK;
-                const uint32_t A[4] = {ra[s].x, ra[s].y, ra[s].z, ra[s].w};
-                const uint32_t B[4] = {rb[s].x, rb[s].y, rb[s].z, rb[s].w};
-                if constexpr (BITS == 8) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t a0, a1, a2, a3;
-                        widen_i8(A[q], a0, a2);
-                        widen_i8(B[q], a1, a3);
-                        mma_all(blk, q, a0, a1, a2, a3);
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t pa[4], pb[4];
-                        widen_i4(A[q], pa);
-                        widen_i4(B[q], pb);
-                        mma_all(blk, 2 * q, pa[0], pb[0], pa[1], pb[1]);
-                        mma_all(blk, 2 * q + 1, pa[2], pb[2], pa[3], pb[3]);
-                    }
-                }
+            for (int q = 0; q < 4; ++q) {
+                uint32_t a0, a1, a2, a3;
+                widen_i8(A[q], a0, a2);
+                widen_i8(B[q], a1, a3);
+                mma_all(blk, q, a0, a1, a2, a3);
             }
-            load(i + PF, ra[s], rb[s]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t pa[4], pb[4];
+                widen_i4(A[q], pa);
+                widen_i4(B[q], pb);
+                mma_all(blk, 2 * q, pa[0], pb[0], pa[1], pb[1]);
+                mma_all(blk, 2 * q + 1, pa[2], pb[2], pa[3], pb[3]);
+            }
         }
     }
 
-    // ---- reduction: warps along K, then CTAs of the cluster, fixed order
+    // ---- 4. reduction: warps along K, then CTAs of the cluster, fixed order
     __syncthreads();
-    float *red = reinterpret_cast<float *>(smem_raw);  // [WK][RT][M]
+    float *red = reinterpret_cast<float *>(smem_raw + p.x_off);  // [WK][RT][M], over x'
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -249,7 +291,7 @@ k_gemv_a16(const GemvParams p) {
     }
     if (C > 1) cg::this_cluster().sync();
     else __syncthreads();
-    if (crank == 0) {
+    if (crank == 0 && have_w) {
         for (int idx = threadIdx.x; idx < RM; idx += kThreads) {
             const int m = idx / RT, r = idx % RT;
             const int li = r * M + m;
@@ -266,54 +308,69 @@ k_gemv_a16(const GemvParams p) {
         }
     }
     if (C > 1) cg::this_cluster().sync();
+    // never leave with bulk copies still landing in this CTA's shared memory
+    if (!have_w) mbar_wait_bounded(wbar, 0);
 }
 
 struct Plan {
-    int WR, WK, C, SX;
+    int WR, WK, C, WS, SX, w_off, x_off;
     size_t smem;
 };
 
 constexpr size_t kGemvSmemMax = 200 * 1024;
 
-size_t smem_for(int64_t M, int SX, int WR, int WK) {
-    const size_t xs = static_cast<size_t>(M) * SX * 2;
-    const size_t red = static_cast<size_t>(WK) * 16 * WR * M * 4;
-    return xs > red ? xs : red;
+Plan make_plan(int64_t M, int64_t K, int bits, int WR, int C) {
+    const int64_t G = (K + kGroup - 1) / kGroup;
+    const int64_t gmax = (G + C - 1) / C;       // most groups any CTA of the cluster gets
+    Plan pl{};
+    pl.WR = WR;
+    pl.WK = 8 / WR;
+    pl.C = C;
+    const int64_t kr = gmax * kGroup;
+    const int64_t rb = kr * bits / 8;
+    pl.WS = static_cast<int>((rb + 127) / 128 * 128 + 64);  // 64 mod 128: conflict-free A loads
+    pl.SX = static_cast<int>(kr + 16);                     // 2*SX = 32 mod 128: B loads
+    const int RT = 16 * WR;
+    pl.w_off = 128;
+    pl.x_off = pl.w_off + RT * pl.WS;
+    const size_t xs = static_cast<size_t>(M) * pl.SX * 2;
+    const size_t red = static_cast<size_t>(pl.WK) * RT * M * 4;
+    pl.smem = static_cast<size_t>(pl.x_off) + (xs > red ? xs : red);
+    return pl;
 }
 
-int sx_for(int64_t G, int C) {
-    const int64_t gmax = (G + C - 1) / C;   // most groups any CTA of the cluster gets
-    return static_cast<int>(gmax * kGroup + 16);  // 2*SX = 32 mod 128: conflict-free B loads
-}
-
-Plan plan_gemv(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev) {
+Plan plan_gemv(int64_t M, int64_t N, int64_t K, int bits, const DeviceInfo &dev) {
     const int64_t G = (K + kGroup - 1) / kGroup;
     Plan pl{};
-    pl.WR = M <= 4 ? 1 : (M <= 16 ? 2 : 8);
-    pl.WK = 8 / pl.WR;
-    const int64_t tiles = (N + 16 * pl.WR - 1) / (16 * pl.WR);
-    int C = 1;
-    while (C < 8 && 2 * C <= G &&
-           (tiles * C < 2 * dev.sms || smem_for(M, sx_for(G, C), pl.WR, pl.WK) > kGemvSmemMax))
-        C *= 2;
-    pl.C = C;
-    pl.SX = sx_for(G, C);
-    pl.smem = smem_for(M, pl.SX, pl.WR, pl.WK);
+    // prefer more rows per CTA for more tokens (x' is shared by the rows);
+    // fall back to fewer rows when the slices do not fit in shared memory
+    for (int WR = M <= 4 ? 1 : (M <= 16 ? 2 : 8); WR >= 1; WR /= 2) {
+        const int64_t tiles = (N + 16 * WR - 1) / (16 * WR);
+        int C = 1;
+        pl = make_plan(M, K, bits, WR, C);
+        // split K over a cluster until the slices fit and the grid covers the GPU
+        while (2 * C <= G &&
+               ((C < 8 && tiles * C < dev.sms) || (C < 16 && pl.smem > 96 * 1024))) {
+            C *= 2;
+            pl = make_plan(M, K, bits, WR, C);
+        }
+        if (pl.smem <= kGemvSmemMax) return pl;
+    }
     return pl;
 }
 
 template <int BITS, int NT>
 tq_status launch_typed(const GemvParams &p, const Plan &pl, int64_t tiles,
                        const DeviceInfo &dev, cudaStream_t s) {
-    auto kern = k_gemv_a16<BITS, NT, 4>;
+    auto kern = k_gemv_a16<BITS, NT>;
     static int configured_for[64] = {0};  // per device: max dynamic smem set
     if (dev.id >= 0 && dev.id < 64 && !configured_for[dev.id]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kGemvSmemMax));
         if (e != cudaSuccess) return cuda_fail(e);
+        // clusters of 16 CTAs (the largest split of K, used for M up to 64)
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        (void)e;
-        cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e);
         configured_for[dev.id] = 1;
     }
     cudaLaunchConfig_t cfg = {};
@@ -341,18 +398,19 @@ tq_status launch_typed(const GemvParams &p, const Plan &pl, int64_t tiles,
 
 }  // namespace
 
-bool gemv_fits(int64_t M, int64_t K, const DeviceInfo &dev) {
+bool gemv_fits(int64_t M, int64_t K, int bits, const DeviceInfo &dev) {
     if (M < 1 || M > TQ_MAX_M_A16) return false;
-    const Plan pl = plan_gemv(M, 1 << 20, K, dev);
-    return pl.smem <= kGemvSmemMax;
+    return plan_gemv(M, 1 << 20, K, bits, dev).smem <= kGemvSmemMax;
 }
 
 tq_status launch_gemv_a16(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
                           const uint8_t *Wq, const float *sw, int64_t N,
                           int bits, void *Y, int ytype, int64_t ldy,
                           const DeviceInfo &dev, cudaStream_t s) {
-    const Plan pl = plan_gemv(M, N, K, dev);
+    const Plan pl = plan_gemv(M, N, K, bits, dev);
     if (pl.smem > kGemvSmemMax) return TQ_ERR_SHAPE;
+    unsigned int *status = status_word();
+    if (!status) return TQ_ERR_DEVICE;
     GemvParams p{};
     p.X = X;
     p.ldx = ldx;
@@ -369,7 +427,11 @@ tq_status launch_gemv_a16(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
     p.WR = pl.WR;
     p.WK = pl.WK;
     p.C = pl.C;
+    p.WS = pl.WS;
     p.SX = pl.SX;
+    p.w_off = pl.w_off;
+    p.x_off = pl.x_off;
+    p.status = status;
     const int64_t tiles = (N + 16 * pl.WR - 1) / (16 * pl.WR);
     const int nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
     if (bits == 8) {

@@ -83,7 +83,7 @@ tq_status check_output(const void *Y, int64_t M, int64_t N, int64_t ldy, int esi
     if (!Y) return TQ_ERR_NULL;
     if (ldy < N) return TQ_ERR_SHAPE;
     if (!mul_ok(M, ldy) || !mul_ok(M * ldy, esize)) return TQ_ERR_OVERFLOW;
-    if (!aligned(Y, 16) || (ldy * esize) % 16) return TQ_ERR_ALIGN;
+    if (!aligned(Y, static_cast<uintptr_t>(esize))) return TQ_ERR_ALIGN;
     return TQ_OK;
 }
 
@@ -203,7 +203,7 @@ tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
     DeviceInfo dev;
     if ((st = current_device(&dev)) != TQ_OK) return st;
     if (mode != TQ_W8A8) {
-        if (!gemv_fits(M, K, dev)) return TQ_ERR_SHAPE;
+        if (!gemv_fits(M, K, bits, dev)) return TQ_ERR_SHAPE;
         return launch_gemv_a16(static_cast<const uint16_t *>(X), M, K, ldx,
                                static_cast<const uint8_t *>(Wq), sw, N, bits, Y,
                                ytype == TQ_OUT_BF16 ? 1 : 0, ldy, dev, stream);
@@ -213,8 +213,8 @@ tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
                                           (static_cast<size_t>(M) * K + 255) / 256 * 256);
     st = launch_rotate_quant_act(static_cast<const uint16_t *>(X), M, K, ldx, Xq, sx, stream);
     if (st != TQ_OK) return st;
-    return launch_gemm_a8_mma(Xq, sx, M, K, static_cast<const uint8_t *>(Wq), sw, N, bits,
-                              Y, ytype == TQ_OUT_BF16 ? 1 : 0, ldy, stream);
+    return launch_gemm_a8(Xq, sx, M, K, static_cast<const uint8_t *>(Wq), sw, N, bits,
+                          Y, ytype == TQ_OUT_BF16 ? 1 : 0, ldy, dev, stream);
 }
 
 tq_status tq_linear_q8(const int8_t *Xq, const float *sx, int64_t M, int64_t K,
@@ -232,8 +232,8 @@ tq_status tq_linear_q8(const int8_t *Xq, const float *sx, int64_t M, int64_t K,
     if ((st = check_output(Y, M, N, ldy, out_size(ytype))) != TQ_OK) return st;
     DeviceInfo dev;
     if ((st = current_device(&dev)) != TQ_OK) return st;
-    return launch_gemm_a8_mma(Xq, sx, M, K, static_cast<const uint8_t *>(Wq), sw, N, bits, Y,
-                              static_cast<int>(ytype), ldy, stream);
+    return launch_gemm_a8(Xq, sx, M, K, static_cast<const uint8_t *>(Wq), sw, N, bits, Y,
+                          static_cast<int>(ytype), ldy, dev, stream);
 }
 
 tq_status tq_device_status(cudaStream_t stream) {

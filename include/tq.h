@@ -153,8 +153,8 @@ size_t tq_linear_workspace_bytes(int64_t M, int64_t K, int64_t N, int bits,
  *            TQ_W8A8 (bits = 8 or 4): activations are quantised per token
  *            (tq_rotate_quant_act) and Y = sx[m] * sw[n] * acc[m][n], acc the
  *            exact int32 sum of code products.
- *   Y        fp32 or bf16 [M, N], row m at Y + m * ldy; ldy >= N; Y 16-byte
- *            aligned and ldy * element size a multiple of 16 bytes.
+ *   Y        fp32 or bf16 [M, N], row m at Y + m * ldy; ldy >= N; Y aligned
+ *            to its element size.
  *   workspace, ws_bytes   device scratch of at least
  *            tq_linear_workspace_bytes(M, K, N, bits, mode) bytes, 256-byte
  *            aligned (may be NULL when that is 0).  Its contents on entry do

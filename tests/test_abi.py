@@ -92,8 +92,9 @@ def test_linear_refusals(L):
     assert lin(L, ldy=100) == SHAPE
     assert lin(L, ldx=520 + 4) == ALIGN
     assert lin(L, X=FAKE + 16) != ALIGN              # a 16-byte offset view is fine
-    assert lin(L, ldy=258) == ALIGN                  # 1032 bytes: not a 16-byte multiple
-    assert lin(L, Y=FAKE + 4) == ALIGN
+    assert lin(L, ldy=257) != ALIGN                  # any row stride >= N is fine
+    assert lin(L, Y=FAKE + 2) == ALIGN               # fp32 output must be 4-byte aligned
+    assert lin(L, Y=FAKE + 2, yt=1) != ALIGN         # bf16 output: 2-byte alignment
     assert lin(L, mode=2, ws=0, wsb=0) == WORKSPACE
     need = L.tq_linear_workspace_bytes(4, 512, 256, 8, 2)
     assert need >= 4 * 512 + 16
