@@ -36,6 +36,7 @@ SIGNATURES = {
     "tq_linear": (_C, [_P, _I, _I, _I, _P, _P, _I, _C, _C, _P, _C, _I, _P, _Z, _P]),
     "tq_linear_q8": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
     "tq_device_status": (_C, [_P]),
+    "tq_linear_a8_static": (_C, [_P, _I, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
 }
 
 _lib = None
@@ -161,6 +162,17 @@ def linear_q8(Xq, sx, Wq, sw, N: int, bits: int, Y=None, out: str = "f32", strea
         Y = torch.empty((M, N), dtype=dt, device=Xq.device)
     _check(lib().tq_linear_q8(_ptr(Xq), _ptr(sx), M, K, _ptr(Wq), _ptr(sw), N, bits, _ptr(Y),
                               OUT[out], Y.stride(0), _stream(stream)), "tq_linear_q8")
+    return Y
+
+
+def linear_a8_static(X, Wq, sw, N: int, bits: int, Y, out: str = "f32", stream=None):
+    """The W8A8 / W4A8 product using the library's fixed device scratch
+    instead of a workspace (for callers that may not allocate device memory).
+    ``Y`` must be given; nothing is allocated."""
+    M, K = X.shape
+    _check(lib().tq_linear_a8_static(_ptr(X), M, K, X.stride(0), _ptr(Wq), _ptr(sw), N, bits,
+                                     _ptr(Y), OUT[out], Y.stride(0), _stream(stream)),
+           "tq_linear_a8_static")
     return Y
 
 

@@ -183,6 +183,39 @@ tq_status tq_linear_q8(const int8_t *Xq, const float *sx, int64_t M, int64_t K,
  */
 tq_status tq_device_status(cudaStream_t stream);
 
+/* Bytes of device memory the library keeps for tq_linear_a8_static. */
+#define TQ_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * tq_linear in mode TQ_W8A8 (bits = 8 or 4) without a workspace argument,
+ * for callers that cannot allocate device memory.  The pages have no
+ * counterpart: this is a library convenience.
+ *
+ * tq_linear needs scratch for the quantised activations and expects the
+ * caller to pass it.  A plugin whose host application owns every device
+ * allocation, or a service that reserves all device memory at start-up and
+ * may not allocate afterwards, has none to pass.  This entry point instead
+ * uses one fixed array of TQ_STATIC_SCRATCH_BYTES compiled into the library;
+ * each GPU that loads the library holds that memory until the process exits.
+ * It allocates nothing and frees nothing.
+ *
+ *   Arguments and results are those of tq_linear with mode TQ_W8A8.
+ *   Limit: the int8 codes (M * K bytes) and the token scales (4 * M bytes),
+ *   each rounded up to 256 bytes, must fit in TQ_STATIC_SCRATCH_BYTES; larger
+ *   calls are refused with TQ_ERR_WORKSPACE before any launch.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (with that device current); make that first call before any stream
+ *   capture.
+ *   Sharing: every call uses the same array and leaves its contents there.
+ *   Nothing in it has to start at zero (each call writes what it reads), but
+ *   calls that overlap on the GPU (for example on two streams) race on it:
+ *   keep them ordered, for example on one stream.
+ */
+tq_status tq_linear_a8_static(const void *X, int64_t M, int64_t K, int64_t ldx,
+                              const void *Wq, const float *sw, int64_t N, int bits,
+                              void *Y, tq_out ytype, int64_t ldy,
+                              cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
