@@ -69,6 +69,23 @@ __device__ __forceinline__ int cm_off(int r, int k) {
     return ((r >> 3) * 8 + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2;
 }
 
+// Converter thread -> (row, 16-byte segment) for pass j.  Each group of 8
+// consecutive lanes (one shared-store phase) takes 8 consecutive rows of one
+// segment, so its 16-byte stores fill one 128-byte core-matrix block
+// (conflict-free), while a warp still loads whole 32-byte sectors.
+// 64-byte rows (int8 codes, 4 segments):
+__device__ __forceinline__ void rows64(int tid, int j, int &r, int &seg) {
+    const int lane = tid & 31, grp = (256 * j + tid) >> 5;
+    r = grp * 8 + (lane & 7);
+    seg = lane >> 3;
+}
+// 32-byte rows (packed int4 codes, 2 segments):
+__device__ __forceinline__ void rows32(int tid, int j, int &r, int &seg) {
+    const int lane = tid & 31, grp = (256 * j + tid) >> 5;
+    r = grp * 16 + ((lane >> 4) << 3) + (lane & 7);
+    seg = (lane >> 3) & 1;
+}
+
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
     constexpr uint64_t lbo = 128, sbo = 1024;
     return static_cast<uint64_t>((addr & 0x3FFFF) >> 4) | ((lbo >> 4) << 16) | ((sbo >> 4) << 32) |
@@ -229,21 +246,24 @@ k_gemm_a8_tc(const TcParams p) {
                 uint4 ra[2], rb[4];
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    const int c = tid + 256 * j, r = c >> 2, seg = c & 3;
+                    int r, seg;
+                    rows64(tid, j, r, seg);
                     const int64_t gm = m0 + r, gk = k0 + seg * 16;
                     ra[j] = (gm < p.M && gk < p.K) ? ldg16(p.Xq + gm * p.K + gk) : make_uint4(0, 0, 0, 0);
                 }
                 if constexpr (BITS == 8) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const int c = tid + 256 * j, r = c >> 2, seg = c & 3;
+                        int r, seg;
+                        rows64(tid, j, r, seg);
                         const int64_t gn = n0 + r, gk = k0 + seg * 16;
                         rb[j] = (gn < p.N && gk < p.K) ? ldg16(p.Wq + gn * wld + gk) : make_uint4(0, 0, 0, 0);
                     }
                 } else {
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        const int c = tid + 256 * j, r = c >> 1, seg = c & 1;
+                        int r, seg;
+                        rows32(tid, j, r, seg);
                         const int64_t gn = n0 + r, gk = k0 + seg * 32;
                         rb[j] = (gn < p.N && gk < p.K) ? ldg16(p.Wq + gn * wld + gk / 2) : make_uint4(0, 0, 0, 0);
                     }
@@ -253,7 +273,8 @@ k_gemm_a8_tc(const TcParams p) {
                 unsigned char *b = sB + s * B_STAGE;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    const int c = tid + 256 * j, r = c >> 2, seg = c & 3;
+                    int r, seg;
+                    rows64(tid, j, r, seg);
                     uint4 lo, hi;
                     widen8(ra[j].x, lo.x, lo.y);
                     widen8(ra[j].y, lo.z, lo.w);
@@ -265,7 +286,8 @@ k_gemm_a8_tc(const TcParams p) {
                 if constexpr (BITS == 8) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const int c = tid + 256 * j, r = c >> 2, seg = c & 3;
+                        int r, seg;
+                        rows64(tid, j, r, seg);
                         uint4 lo, hi;
                         widen8(rb[j].x, lo.x, lo.y);
                         widen8(rb[j].y, lo.z, lo.w);
@@ -277,7 +299,8 @@ k_gemm_a8_tc(const TcParams p) {
                 } else {
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        const int c = tid + 256 * j, r = c >> 1, seg = c & 1;
+                        int r, seg;
+                        rows32(tid, j, r, seg);
                         const uint32_t w[4] = {rb[j].x, rb[j].y, rb[j].z, rb[j].w};
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
