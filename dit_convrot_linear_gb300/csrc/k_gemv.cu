@@ -182,17 +182,16 @@ k_gemv_a16(const GemvParams p) {
         for (int m = lane; m < p.M; m += 32)
             prefetch_l2(p.X + m * p.ldx + kbeg, static_cast<uint32_t>(nk * 2));
     }
+    // the row scales of this tile, read under the same rule as the weights
+    float *sws = reinterpret_cast<float *>(smem_raw + 128);  // [RT], before the weight slice
+    if (threadIdx.x < rows) sws[threadIdx.x] = __ldg(p.sw + n0 + threadIdx.x);
     pdl_launch_dependents();
     pdl_wait();
-    __syncthreads();  // barrier initialised before anyone waits on it
 
-    // ---- 2. rotated, bf16-rounded x' of this K range in shared memory
+    // ---- 2. rotated, bf16-rounded x' of this K range in shared memory.  The
+    // warp that writes a token's last group also zeroes the padding of the
+    // last (partial) K block, so one barrier covers both.
     const int M = p.M, SX = p.SX;
-    if (nblk > 0) {
-        const int z0 = (nblk - 1) * KB;  // the last block may be partial: zero it
-        for (int i = threadIdx.x; i < M * KB; i += kThreads) xs[(i / KB) * SX + z0 + (i % KB)] = 0;
-    }
-    __syncthreads();
     const int ngrp = ge - gb;
     for (int w = warp; w < M * ngrp; w += kThreads / 32) {
         const int m = w / ngrp, gi = w % ngrp;
@@ -206,6 +205,10 @@ k_gemv_a16(const GemvParams p) {
                 const int kl = gi * kGroup + lane * E + e;
                 xrow[(kl / KB) * KB + xpos<BITS>(kl % KB)] = f32_to_bf16_bits(v[e]);
             }
+        }
+        if (gi == ngrp - 1) {
+            for (int kl = nk + lane; kl < nblk * KB; kl += 32)
+                xrow[(kl / KB) * KB + xpos<BITS>(kl % KB)] = 0;
         }
     }
     __syncthreads();
@@ -222,9 +225,13 @@ k_gemv_a16(const GemvParams p) {
     const unsigned char *pB = ws + rB * p.WS + t * 16;
     const int nbw = (have_w && nblk > wk) ? (nblk - wk + WK - 1) / WK : 0;
 
-    float acc[NT][4];
+    // two accumulator sets, alternating by mma index, halve the dependent chain
+    float acc[NT][4], acc2[NT][4];
 #pragma unroll
-    for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+    for (int i = 0; i < NT; ++i) {
+        acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+        acc2[i][0] = acc2[i][1] = acc2[i][2] = acc2[i][3] = 0.0f;
+    }
     const uint16_t *xb[NT];
     bool xin[NT];
 #pragma unroll
@@ -238,7 +245,7 @@ k_gemv_a16(const GemvParams p) {
         for (int nt = 0; nt < NT; ++nt) {
             uint2 bv = make_uint2(0, 0);
             if (xin[nt]) bv = *reinterpret_cast<const uint2 *>(xb[nt] + blk * KB + jj * 16);
-            mma_bf16(acc[nt], a0, a1, a2, a3, bv.x, bv.y);
+            mma_bf16((jj & 1) ? acc2[nt] : acc[nt], a0, a1, a2, a3, bv.x, bv.y);
         }
     };
     for (int i = 0; i < nbw; ++i) {
@@ -278,8 +285,8 @@ k_gemv_a16(const GemvParams p) {
         for (int h = 0; h < 2; ++h) {
             const int row = wr * 16 + g + 8 * h;
             const int m0 = nt * 8 + 2 * t;
-            if (m0 < M) red[(wk * RT + row) * M + m0] = acc[nt][2 * h];
-            if (m0 + 1 < M) red[(wk * RT + row) * M + m0 + 1] = acc[nt][2 * h + 1];
+            if (m0 < M) red[(wk * RT + row) * M + m0] = acc[nt][2 * h] + acc2[nt][2 * h];
+            if (m0 + 1 < M) red[(wk * RT + row) * M + m0 + 1] = acc[nt][2 * h + 1] + acc2[nt][2 * h + 1];
         }
     }
     __syncthreads();
@@ -299,7 +306,7 @@ k_gemv_a16(const GemvParams p) {
             for (int q = 1; q < C; ++q) s += cg::this_cluster().map_shared_rank(red, q)[li];
             const int64_t n = n0 + r;
             if (n < p.N) {
-                const float y = p.sw[n] * s;
+                const float y = sws[r] * s;
                 if (p.ytype == 0)
                     static_cast<float *>(p.Y)[m * p.ldy + n] = y;
                 else
@@ -331,7 +338,7 @@ Plan make_plan(int64_t M, int64_t K, int bits, int WR, int C) {
     pl.WS = static_cast<int>((rb + 127) / 128 * 128 + 64);  // 64 mod 128: conflict-free A loads
     pl.SX = static_cast<int>(kr + 16);                     // 2*SX = 32 mod 128: B loads
     const int RT = 16 * WR;
-    pl.w_off = 128;
+    pl.w_off = 128 + (4 * RT + 127) / 128 * 128;  // barrier, then the row scales
     pl.x_off = pl.w_off + RT * pl.WS;
     const size_t xs = static_cast<size_t>(M) * pl.SX * 2;
     const size_t red = static_cast<size_t>(pl.WK) * RT * M * 4;
