@@ -44,6 +44,9 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--calls", type=int, default=1000)
     ap.add_argument("--skip-dit", action="store_true")
+    ap.add_argument("--only", default="all", choices=["all", "decode", "dit"],
+                    help="profiling cases: only the W8A16 decode graph, or only the DiT GEMMs")
+    ap.add_argument("--dit-m", type=int, default=4032, help="token rows of the DiT case")
     ap.add_argument("--skip-cpu", action="store_true")
     return ap.parse_args()
 
@@ -288,13 +291,12 @@ def time_steps(fn, steps, warmup, world):
     return max_over_ranks(ms, world)
 
 
-def dit_measure(device, reps=5):
+def dit_measure(device, reps=5, M=4032):
     """M = 4032 W8A8 (DiT FFN up and down): TOPS = 2 M N K / t per GEMM, L2
     flushed between timed calls (a 512 MB write)."""
     import torch
     from dit_convrot_linear_gb300 import synth, tq
     w = synth.DIT
-    M = 4032
     out = {}
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
     tot_ops = tot_ms = 0.0
@@ -414,6 +416,13 @@ def main():
     l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
     pk, pk_kind = peaks()
 
+    if args.only == "dit":   # profiling case: the DiT GEMMs alone
+        per, tops, gemm_tops = dit_measure(device, reps=args.steps, M=args.dit_m)
+        if rank == 0:
+            print(json.dumps({"case": f"dit W8A8 M={args.dit_m}", "tops": round(tops, 2),
+                              "gemm_only_tops": round(gemm_tops, 2), "per_gemm": per}))
+        return 0
+
     # headline: decode W8A16
     dec8 = Decode(8, args.calls, device, l2)
     dec8.capture()
@@ -442,7 +451,11 @@ def main():
 
     # W4A16 decode beside it
     extra = {}
+    if args.only == "decode":
+        args.skip_dit = args.skip_cpu = True
     try:
+        if args.only == "decode":
+            raise RuntimeError("skipped (--only decode)")
         dec4 = Decode(4, args.calls, device, l2)
         dec4.capture()
         ms4 = time_steps(dec4.step, args.steps, args.warmup, world) / args.steps

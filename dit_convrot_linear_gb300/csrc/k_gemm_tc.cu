@@ -15,12 +15,18 @@
 // the accumulator is drained every such chunk of K into an exact int32 running
 // sum kept in a second TMEM region, and the result is bit-exact int32.
 //
-// Tile 128 (M) x 256 (N) x 64 (K) per stage, 4 stages, one CTA per SM,
-// persistent over tiles.  Warp roles:
-//   warps 0-7   convert: load int8/int4 codes with 16-byte loads, widen to
-//               fp16 in registers, store the K-major 8x8 core-matrix layout
-//               the MMA reads (no swizzle), signal the stage full;
-//   warp 8      allocates TMEM; lane 0 issues the MMAs and the commits;
+// A pair of CTAs (a cluster of 2, tcgen05 cta_group::2) computes a 256 x 256
+// output tile: each CTA holds 128 rows of A (activations) and 128 rows of B
+// (weights), and the MMA, issued by the even CTA, multiplies the pair's whole
+// A by the pair's whole B, leaving each CTA its 128 rows x 256 columns in its
+// own TMEM.  Each SM thus converts and stages half of B.  K steps of 64, six
+// stages, persistent over tiles.  Warp roles in each CTA:
+//   warps 0-7   convert: load int8/int4 codes with 16-byte loads one step
+//               ahead, widen to fp16 in registers, store the K-major 8x8
+//               core-matrix layout the MMA reads, arrive on the even CTA's
+//               stage barrier;
+//   warp 8      allocates TMEM for the pair; in the even CTA, lane 0 issues the
+//               MMAs and the commits (multicast to both CTAs);
 //   warps 9-12  drain the accumulator (one TMEM lane quarter each) and write Y.
 // Every wait is bounded: on expiry the CTA records the failure in the library
 // status word, stops issuing work, lets in-flight MMAs finish (bounded), frees
@@ -31,18 +37,18 @@
 namespace tq {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int NCONV = 8, MMA_WARP = 8, EPI0 = 9, NWARPS = 13;
+constexpr int HM = 128, BN = 256, HN = BN / 2, BK = 64, STAGES = 6;
+constexpr int NCONV = 8, MMA_WARP = 8, NWARPS = 13;
 constexpr int THREADS = NWARPS * 32;
-constexpr int A_STAGE = BM * BK * 2;   // 16 KB fp16
-constexpr int B_STAGE = BN * BK * 2;   // 32 KB fp16
+constexpr int A_STAGE = HM * BK * 2;   // 16 KB fp16: this CTA's 128 rows of A
+constexpr int B_STAGE = HN * BK * 2;   // 16 KB fp16: this CTA's 128 rows of B
 constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024;
 constexpr uint32_t TMEM_COLS = 512;    // acc [0, 256) + running int32 sum [256, 512)
 constexpr uint32_t RUN_COL = 256;
 constexpr long long kWaitLimit = 4000000000ll;  // clock cycles, about 2 s
 constexpr unsigned int kStatusGemmTimeout = 2u;
-// instruction descriptor: D f32, A/B f16, K-major, N = 256, M = 128
-constexpr uint32_t IDESC = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+// instruction descriptor: D f32, A/B f16, K-major, N = 256, M = 256 (pair)
+constexpr uint32_t IDESC = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(256 >> 4) << 24);
 
 struct TcParams {
     const int8_t *Xq;
@@ -69,19 +75,19 @@ __device__ __forceinline__ int cm_off(int r, int k) {
     return ((r >> 3) * 8 + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2;
 }
 
-// Converter thread -> (row, 16-byte segment) for pass j.  Each group of 8
-// consecutive lanes (one shared-store phase) takes 8 consecutive rows of one
-// segment, so its 16-byte stores fill one 128-byte core-matrix block
-// (conflict-free), while a warp still loads whole 32-byte sectors.
-// 64-byte rows (int8 codes, 4 segments):
+// Converter thread -> (row, 16-byte segment) of a 128-row tile for pass j.
+// Each group of 8 consecutive lanes (one shared-store phase) takes 8
+// consecutive rows of one segment, so its 16-byte stores fill one 128-byte
+// core-matrix block (conflict-free), while a warp still loads whole sectors.
+// 64-byte rows (int8 codes, 4 segments): passes 0..1
 __device__ __forceinline__ void rows64(int tid, int j, int &r, int &seg) {
     const int lane = tid & 31, grp = (256 * j + tid) >> 5;
     r = grp * 8 + (lane & 7);
     seg = lane >> 3;
 }
-// 32-byte rows (packed int4 codes, 2 segments):
-__device__ __forceinline__ void rows32(int tid, int j, int &r, int &seg) {
-    const int lane = tid & 31, grp = (256 * j + tid) >> 5;
+// 32-byte rows (packed int4 codes, 2 segments): pass 0
+__device__ __forceinline__ void rows32(int tid, int &r, int &seg) {
+    const int lane = tid & 31, grp = tid >> 5;
     r = grp * 16 + ((lane >> 4) << 3) + (lane & 7);
     seg = (lane >> 3) & 1;
 }
@@ -95,7 +101,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
         "selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -118,8 +124,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     return true;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+// arrive on the barrier at the same offset in CTA 0 of the cluster
+__device__ __forceinline__ void mbar_arrive_leader(uint32_t bar) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(remote) : "r"(bar));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+__device__ __forceinline__ void commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(bar), "h"(static_cast<uint16_t>(3)) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -162,6 +182,26 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t (&p)[4]) {
     }
 }
 
+__device__ __forceinline__ void store_i8x16(unsigned char *tile, int r, int seg, const uint4 &w) {
+    uint4 lo, hi;
+    widen8(w.x, lo.x, lo.y);
+    widen8(w.y, lo.z, lo.w);
+    widen8(w.z, hi.x, hi.y);
+    widen8(w.w, hi.z, hi.w);
+    *reinterpret_cast<uint4 *>(tile + cm_off(r, seg * 16)) = lo;
+    *reinterpret_cast<uint4 *>(tile + cm_off(r, seg * 16 + 8)) = hi;
+}
+
+__device__ __forceinline__ void store_i4x32(unsigned char *tile, int r, int seg, const uint4 &w) {
+    const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t pr[4];
+        widen4(v[q], pr);
+        *reinterpret_cast<uint4 *>(tile + cm_off(r, seg * 32 + q * 8)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+    }
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -193,134 +233,146 @@ __device__ __forceinline__ uint4 ldg16(const void *p) {
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(THREADS, 1)
+struct Loads {
+    uint4 a[2];                        // A: 128 rows x 64 bytes, two 16-byte chunks per thread
+    uint4 b[BITS == 8 ? 2 : 1];        // B: 128 rows x 64 (int8) or 32 (int4) bytes
+};
+
+template <int BITS>
+__device__ __forceinline__ void load_step(const TcParams &p, int tid, int64_t m0, int64_t n0,
+                                          int64_t k0, int64_t wld, Loads<BITS> &L) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        int r, seg;
+        rows64(tid, j, r, seg);
+        const int64_t gm = m0 + r, gk = k0 + seg * 16;
+        L.a[j] = (gm < p.M && gk < p.K) ? ldg16(p.Xq + gm * p.K + gk) : make_uint4(0, 0, 0, 0);
+    }
+    if constexpr (BITS == 8) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            int r, seg;
+            rows64(tid, j, r, seg);
+            const int64_t gn = n0 + r, gk = k0 + seg * 16;
+            L.b[j] = (gn < p.N && gk < p.K) ? ldg16(p.Wq + gn * wld + gk) : make_uint4(0, 0, 0, 0);
+        }
+    } else {
+        int r, seg;
+        rows32(tid, r, seg);
+        const int64_t gn = n0 + r, gk = k0 + seg * 32;
+        L.b[0] = (gn < p.N && gk < p.K) ? ldg16(p.Wq + gn * wld + gk / 2) : make_uint4(0, 0, 0, 0);
+    }
+}
+
+template <int BITS>
+__device__ __forceinline__ void store_step(int tid, unsigned char *a, unsigned char *b, const Loads<BITS> &L) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        int r, seg;
+        rows64(tid, j, r, seg);
+        store_i8x16(a, r, seg, L.a[j]);
+    }
+    if constexpr (BITS == 8) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            int r, seg;
+            rows64(tid, j, r, seg);
+            store_i8x16(b, r, seg, L.b[j]);
+        }
+    } else {
+        int r, seg;
+        rows32(tid, r, seg);
+        store_i4x32(b, r, seg, L.b[0]);
+    }
+}
+
+template <int BITS>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 k_gemm_a8_tc(const TcParams p) {
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *sA = smem;
     unsigned char *sB = smem + STAGES * A_STAGE;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * (A_STAGE + B_STAGE));
-    // bars: full[STAGES], empty[STAGES], acc_full, acc_empty, done
+    // bars: full[STAGES] (used in CTA 0), empty[STAGES], acc_full, acc_empty (CTA 0), done
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
     const uint32_t acc_full = smem_u32(bars + 2 * STAGES), acc_empty = smem_u32(bars + 2 * STAGES + 1);
     const uint32_t done = smem_u32(bars + 2 * STAGES + 2);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * s), "r"(NCONV * 32));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * s), "r"(2 * NCONV));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(empty0 + 8 * s));
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(acc_full));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(acc_empty));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(acc_empty));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         abort_sh = 0;
     }
     if (warp == MMA_WARP) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_u32(&tmem_base_sh)), "r"(TMEM_COLS));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
+    cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tmem_base_sh;
 
     const int ntiles_total = p.mtiles * p.ntiles;
+    const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
     const int64_t wld = BITS == 8 ? p.K : p.K / 2;
 
     if (warp < NCONV) {
         // ------------------------------------------------ converters
         const int tid = threadIdx.x;  // 0..255
         uint32_t it = 0;
-        for (int tile = blockIdx.x; tile < ntiles_total && !abort_sh; tile += gridDim.x) {
-            const int64_t m0 = static_cast<int64_t>(tile % p.mtiles) * BM;
-            const int64_t n0 = static_cast<int64_t>(tile / p.mtiles) * BN;
-            for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
-                const int s = it % STAGES;
-                const int64_t k0 = static_cast<int64_t>(ks) * BK;
-                // global loads first (independent of the stage being free)
-                uint4 ra[2], rb[4];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    int r, seg;
-                    rows64(tid, j, r, seg);
-                    const int64_t gm = m0 + r, gk = k0 + seg * 16;
-                    ra[j] = (gm < p.M && gk < p.K) ? ldg16(p.Xq + gm * p.K + gk) : make_uint4(0, 0, 0, 0);
-                }
-                if constexpr (BITS == 8) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        int r, seg;
-                        rows64(tid, j, r, seg);
-                        const int64_t gn = n0 + r, gk = k0 + seg * 16;
-                        rb[j] = (gn < p.N && gk < p.K) ? ldg16(p.Wq + gn * wld + gk) : make_uint4(0, 0, 0, 0);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        int r, seg;
-                        rows32(tid, j, r, seg);
-                        const int64_t gn = n0 + r, gk = k0 + seg * 32;
-                        rb[j] = (gn < p.N && gk < p.K) ? ldg16(p.Wq + gn * wld + gk / 2) : make_uint4(0, 0, 0, 0);
-                    }
-                }
-                if (!mbar_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1, &abort_sh, p.status)) break;
-                unsigned char *a = sA + s * A_STAGE;
-                unsigned char *b = sB + s * B_STAGE;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    int r, seg;
-                    rows64(tid, j, r, seg);
-                    uint4 lo, hi;
-                    widen8(ra[j].x, lo.x, lo.y);
-                    widen8(ra[j].y, lo.z, lo.w);
-                    widen8(ra[j].z, hi.x, hi.y);
-                    widen8(ra[j].w, hi.z, hi.w);
-                    *reinterpret_cast<uint4 *>(a + cm_off(r, seg * 16)) = lo;
-                    *reinterpret_cast<uint4 *>(a + cm_off(r, seg * 16 + 8)) = hi;
-                }
-                if constexpr (BITS == 8) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        int r, seg;
-                        rows64(tid, j, r, seg);
-                        uint4 lo, hi;
-                        widen8(rb[j].x, lo.x, lo.y);
-                        widen8(rb[j].y, lo.z, lo.w);
-                        widen8(rb[j].z, hi.x, hi.y);
-                        widen8(rb[j].w, hi.z, hi.w);
-                        *reinterpret_cast<uint4 *>(b + cm_off(r, seg * 16)) = lo;
-                        *reinterpret_cast<uint4 *>(b + cm_off(r, seg * 16 + 8)) = hi;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        int r, seg;
-                        rows32(tid, j, r, seg);
-                        const uint32_t w[4] = {rb[j].x, rb[j].y, rb[j].z, rb[j].w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t pr[4];
-                            widen4(w[q], pr);
-                            *reinterpret_cast<uint4 *>(b + cm_off(r, seg * 32 + q * 8)) =
-                                make_uint4(pr[0], pr[1], pr[2], pr[3]);
-                        }
-                    }
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(full0 + 8 * s);
+        Loads<BITS> cur, nxt;
+        // the (tile, k-step) sequence of this CTA, with one step of load lookahead
+        int tile = cluster_id, ks = 0;
+        auto coords = [&](int t, int64_t &m0, int64_t &n0) {
+            m0 = static_cast<int64_t>(t % p.mtiles) * 2 * HM + rank * HM;
+            n0 = static_cast<int64_t>(t / p.mtiles) * BN + rank * HN;
+        };
+        int64_t m0, n0;
+        if (tile < ntiles_total) {
+            coords(tile, m0, n0);
+            load_step<BITS>(p, tid, m0, n0, 0, wld, cur);
+        }
+        while (tile < ntiles_total && !abort_sh) {
+            // next step's coordinates, loaded ahead of this step's stores
+            int ntile = tile, nks = ks + 1;
+            if (nks == p.ksteps) { nks = 0; ntile += nclusters; }
+            if (ntile < ntiles_total) {
+                int64_t nm0, nn0;
+                coords(ntile, nm0, nn0);
+                load_step<BITS>(p, tid, nm0, nn0, static_cast<int64_t>(nks) * BK, wld, nxt);
             }
+            const int s = it % STAGES;
+            if (!mbar_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1, &abort_sh, p.status)) break;
+            store_step<BITS>(tid, sA + s * A_STAGE, sB + s * B_STAGE, cur);
+            // every lane makes its stores visible to the tensor core (async
+            // proxy); the warp then arrives once, ordered after all its lanes
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive_leader(full0 + 8 * s);
+            cur = nxt;
+            tile = ntile;
+            ks = nks;
+            ++it;
         }
     } else if (warp == MMA_WARP) {
-        // ------------------------------------------------ MMA issue (one thread)
-        if (lane == 0) {
+        // ------------------------------------------------ MMA issue (CTA 0, one thread)
+        if (rank == 0 && lane == 0) {
             uint32_t it = 0, ch = 0;
             bool issued = false;
-            for (int tile = blockIdx.x; tile < ntiles_total && !abort_sh; tile += gridDim.x) {
+            for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
                 for (int c0 = 0; c0 < p.ksteps && !abort_sh; c0 += p.chunk_steps) {
                     const int c1 = min(c0 + p.chunk_steps, p.ksteps);
                     if (ch > 0 && !mbar_wait(acc_empty, (ch - 1) & 1, &abort_sh, p.status)) break;
@@ -336,25 +388,21 @@ k_gemm_a8_tc(const TcParams p) {
                             const uint32_t accum = (ks > c0 || kk > 0) ? 1u : 0u;
                             asm volatile(
                                 "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-                                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+                                "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n"
                                 ::"r"(tmem), "l"(ad), "l"(bd), "r"(IDESC), "r"(accum));
                         }
                         issued = true;
-                        asm volatile(
-                            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                            ::"r"(empty0 + 8 * s) : "memory");
+                        commit_pair(empty0 + 8 * s);
                     }
                     if (abort_sh) break;
-                    asm volatile(
-                        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                        ::"r"(acc_full) : "memory");
+                    commit_pair(acc_full);
                     ++ch;
                 }
             }
-            // let every issued MMA finish before the TMEM is released
+            // let every issued MMA finish before the pair's TMEM is released
             if (issued) {
                 asm volatile(
-                    "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                    "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                     ::"r"(done) : "memory");
                 const long long t0 = clock64();
                 while (!mbar_try(done, 0) && clock64() - t0 < kWaitLimit) {
@@ -367,11 +415,10 @@ k_gemm_a8_tc(const TcParams p) {
         const int q = warp & 3;                       // TMEM lane quarter of this warp
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         uint32_t ch = 0;
-        const bool vec_ok = p.ytype == 0 ? ((reinterpret_cast<uintptr_t>(p.Y) & 15) == 0 && (p.ldy & 3) == 0)
-                          : p.ytype == 1 ? ((reinterpret_cast<uintptr_t>(p.Y) & 15) == 0 && (p.ldy & 7) == 0)
-                                         : ((reinterpret_cast<uintptr_t>(p.Y) & 15) == 0 && (p.ldy & 3) == 0);
-        for (int tile = blockIdx.x; tile < ntiles_total && !abort_sh; tile += gridDim.x) {
-            const int64_t m0 = static_cast<int64_t>(tile % p.mtiles) * BM;
+        const bool y16 = (reinterpret_cast<uintptr_t>(p.Y) & 15) == 0;
+        const bool vec_ok = y16 && (p.ytype == 1 ? (p.ldy & 7) == 0 : (p.ldy & 3) == 0);
+        for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
+            const int64_t m0 = static_cast<int64_t>(tile % p.mtiles) * 2 * HM + rank * HM;
             const int64_t n0 = static_cast<int64_t>(tile / p.mtiles) * BN;
             const int64_t m = m0 + q * 32 + lane;
             for (int c0 = 0; c0 < p.ksteps; c0 += p.chunk_steps, ++ch) {
@@ -393,7 +440,7 @@ k_gemm_a8_tc(const TcParams p) {
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(acc_empty);
+                if (lane == 0) mbar_arrive_leader(acc_empty);
             }
             if (abort_sh) break;
             // the tile's exact int32 sums are in the running region: write Y
@@ -454,11 +501,13 @@ k_gemm_a8_tc(const TcParams p) {
         }
     }
 
+    // nobody leaves while the peer may still arrive on this CTA's barriers or
+    // while MMAs of the pair are in flight (CTA 0 waited for them above)
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
+    cluster_sync_all();
     if (warp == MMA_WARP) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
     }
 }
 
@@ -481,14 +530,14 @@ tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M, int64_t K
     p.Y = Y;
     p.ldy = ldy;
     p.ytype = ytype;
-    p.mtiles = static_cast<int>((M + BM - 1) / BM);
+    p.mtiles = static_cast<int>((M + 2 * HM - 1) / (2 * HM));
     p.ntiles = static_cast<int>((N + BN - 1) / BN);
     p.ksteps = static_cast<int>((K + BK - 1) / BK);
     // K per exact fp32 chunk: 1024 * 127^2 < 2^24 (int8), 16384 * 127 * 7 < 2^24 (int4)
     p.chunk_steps = bits == 8 ? 1024 / BK : 16384 / BK;
     p.status = status;
     const int64_t tiles = static_cast<int64_t>(p.mtiles) * p.ntiles;
-    if (tiles > (1ll << 31) - 1) return TQ_ERR_OVERFLOW;
+    if (tiles > (1ll << 30)) return TQ_ERR_OVERFLOW;
     auto kern = bits == 8 ? k_gemm_a8_tc<8> : k_gemm_a8_tc<4>;
     static int configured_for[64][2] = {{0}};
     const int bi = bits == 8 ? 0 : 1;
@@ -497,8 +546,8 @@ tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M, int64_t K
         if (e != cudaSuccess) return cuda_fail(e);
         configured_for[dev.id][bi] = 1;
     }
-    const unsigned grid = static_cast<unsigned>(tiles < dev.sms ? tiles : dev.sms);
-    kern<<<grid, THREADS, SMEM_BYTES, s>>>(p);
+    const int64_t pairs = tiles < dev.sms / 2 ? tiles : dev.sms / 2;
+    kern<<<static_cast<unsigned>(2 * pairs), THREADS, SMEM_BYTES, s>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }

@@ -1,0 +1,373 @@
+// Decode product for M <= 8 tokens, built for the shortest dependent path:
+//   Y[m][n] = sw[n] * sum_k q_w[n][k] * x'_bf16[m][k],  fp32 sums,
+// x' the group-256 Hadamard rotation of the token row rounded to bf16 (tensai
+// docs, "画像生成" / Image generation, section "幅とメモリ").  Decode is bound by
+// the weight stream (kvad-gpu internals, "Numbers"), but one call moves only a
+// few MB, so what decides its time is the chain of latencies that must follow
+// the previous call: read X, rotate, multiply, reduce, store.
+//
+// Layout of one call:
+//   - A CTA owns RT = 16*WR weight rows and the whole of K: no cross-CTA
+//     reduction.  Its 8 warps are WR row groups x WK = 8/WR K slices; a K
+//     slice is a run of whole 256-groups.
+//   - Before waiting for the previous kernel, the CTA bulk-copies its weight
+//     slice (and row scales) into shared memory and releases the next launch
+//     (programmatic dependent launch), so the weight stream of the following
+//     calls overlaps this one.  Bulk copies read through the coherent L2, so
+//     weights and scales must not be written by a kernel that may still be
+//     running; only this library's product kernels trigger early, and they
+//     write nothing but Y.
+//   - After the wait, each warp reads and rotates only the groups of its own
+//     K slice, keeping x' in its private shared memory (no block barrier),
+//     widens weight codes to exact bf16 pairs and runs mma.sync m16n8k16 on
+//     four independent accumulator chains.
+//   - One barrier, then the K slices are added in a fixed order (deterministic)
+//     and scaled.
+// Waits are bounded: on expiry the status word is set and the call's output
+// is left unwritten (tq_device_status reports it).
+
+#include "tq_internal.cuh"
+
+namespace tq {
+namespace {
+
+struct SmallParams {
+    const uint16_t *X;
+    int64_t ldx;
+    int M;
+    int64_t K;
+    int G;
+    const uint8_t *W;
+    int64_t wld;
+    const float *sw;
+    int64_t N;
+    void *Y;
+    int64_t ldy;
+    int ytype;
+    int WR, WK;
+    int gpw;        // most groups in any warp's K slice
+    int WS;         // shared row stride of the weight slice (bytes, = 64 mod 128)
+    int XS;         // per-warp x' row stride (bf16 elements, 2*XS = 32 mod 128)
+    int w_off, x_off, r_off;
+    unsigned int *status;
+};
+
+constexpr long long kWaitLimit = 4000000000ll;  // clock cycles (about 2 s)
+constexpr unsigned int kStatusSmallTimeout = 4u;
+constexpr int NCH = 4;                          // accumulator chains per warp
+
+template <int BITS>
+__device__ __forceinline__ int xpos(int kl) {
+    if constexpr (BITS == 8) {
+        const int t = kl >> 4, q = (kl >> 2) & 3, r = kl & 3;
+        return q * 16 + 4 * t + (((r & 1) << 1) | (r >> 1));
+    } else {
+        const int t = kl >> 5, q = (kl >> 3) & 3, r = kl & 7;
+        const int jj = 2 * q + ((r >> 1) & 1);
+        return jj * 16 + 4 * t + ((r >> 2) | ((r & 1) << 1));
+    }
+}
+
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// int8 codes (k0..k3) -> bf16 pairs (k0,k2), (k1,k3), exact.
+__device__ __forceinline__ void widen_i8(uint32_t x, uint32_t &p02, uint32_t &p13) {
+    p02 = bf16x2_sub((x & 0x007F007Fu) | 0x43004300u, (x & 0x00800080u) ^ 0x43004300u);
+    const uint32_t y = x >> 8;
+    p13 = bf16x2_sub((y & 0x007F007Fu) | 0x43004300u, (y & 0x00800080u) ^ 0x43004300u);
+}
+
+// int4 codes (k0..k7) -> bf16 pairs (k0,k4), (k1,k5), (k2,k6), (k3,k7), exact.
+__device__ __forceinline__ void widen_i4(uint32_t w, uint32_t (&p)[4]) {
+    const uint32_t c = 0x43084308u;
+    p[0] = bf16x2_sub((w & 0x000F000Fu) ^ c, c);
+    p[1] = bf16x2_sub(((w >> 4) & 0x000F000Fu) ^ c, c);
+    p[2] = bf16x2_sub(((w >> 8) & 0x000F000Fu) ^ c, c);
+    p[3] = bf16x2_sub(((w >> 12) & 0x000F000Fu) ^ c, c);
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            "selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (clock64() - t0 > kWaitLimit) return false;
+    }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads)
+k_gemv_small(const SmallParams p) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    constexpr int KB = BITS == 8 ? 64 : 128;  // k per block (one 16-byte chunk per lane)
+    constexpr int BB = 64;                    // weight bytes per row per block
+    constexpr int BPG = kGroup / KB;          // blocks per full group
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem_raw);
+    float *sws = reinterpret_cast<float *>(smem_raw + 128);
+    unsigned char *ws = smem_raw + p.w_off;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int RT = 16 * p.WR;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * RT;
+    const int rows = static_cast<int>(min(static_cast<int64_t>(RT), p.N - n0));
+    const int rbytes = static_cast<int>(p.K * BITS / 8);
+    const uint32_t wbar = smem_addr(bar);
+
+    // ---- before the wait: weight slice and row scales of this tile
+    if (warp == 0) {
+        if (lane == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(wbar));
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(wbar),
+                         "r"(static_cast<uint32_t>(rows * rbytes))
+                         : "memory");
+        }
+        __syncwarp();
+        for (int r = lane; r < rows; r += 32) {
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                ::"r"(smem_addr(ws + r * p.WS)), "l"(p.W + (n0 + r) * p.wld),
+                  "r"(static_cast<uint32_t>(rbytes)), "r"(wbar)
+                : "memory");
+        }
+    }
+    if (threadIdx.x < rows) sws[threadIdx.x] = __ldg(p.sw + n0 + threadIdx.x);
+    const int WR = p.WR, WK = p.WK;
+    const int wr = warp % WR, wk = warp / WR;
+    const int g0 = static_cast<int>(static_cast<int64_t>(p.G) * wk / WK);
+    const int g1 = static_cast<int>(static_cast<int64_t>(p.G) * (wk + 1) / WK);
+    if (wr == 0) {  // warm L2 with this slice's token rows (coherent: safe before the wait)
+        for (int m = lane; m < p.M; m += 32) {
+            const int64_t k0 = static_cast<int64_t>(g0) * kGroup;
+            const int64_t k1 = min(static_cast<int64_t>(g1) * kGroup, p.K);
+            if (k1 > k0) prefetch_l2(p.X + m * p.ldx + k0, static_cast<uint32_t>((k1 - k0) * 2));
+        }
+    }
+    __syncthreads();  // barrier initialised; row scales in place
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // ---- rotate this warp's groups into its private x' (token rows of XS)
+    const int M = p.M, XS = p.XS;
+    uint16_t *xw = reinterpret_cast<uint16_t *>(smem_raw + p.x_off) + static_cast<size_t>(warp) * M * XS;
+    const int64_t kslice0 = static_cast<int64_t>(g0) * kGroup;
+    const int nk = static_cast<int>(min(static_cast<int64_t>(g1) * kGroup, p.K) - kslice0);
+    const int nblk = (nk + KB - 1) / KB;
+    for (int m = 0; m < M; ++m) {
+        uint16_t *xrow = xw + m * XS;
+        for (int gi = 0; gi < g1 - g0; ++gi) {
+            const int64_t gk = kslice0 + static_cast<int64_t>(gi) * kGroup;
+            float v[8] = {};
+            const int E = rotate_group32_any(p.X + m * p.ldx + gk, group_width(p.K, gk), v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (e < E) {
+                    const int kl = gi * kGroup + lane * E + e;
+                    xrow[(kl / KB) * KB + xpos<BITS>(kl % KB)] = f32_to_bf16_bits(v[e]);
+                }
+            }
+        }
+        for (int kl = nk + lane; kl < nblk * KB; kl += 32)   // padding of a partial last block
+            xrow[(kl / KB) * KB + xpos<BITS>(kl % KB)] = 0;
+    }
+    __syncwarp();
+
+    // ---- products: this warp's 16 rows x its K slice
+    const bool have_w = mbar_wait_bounded(wbar, 0);
+    if (!have_w && lane == 0) atomicOr(p.status, kStatusSmallTimeout);
+    const int g = lane >> 2, t = lane & 3;
+    const int rA = wr * 16 + g, rB = rA + 8;
+    const bool okA = rA < rows, okB = rB < rows;
+    const int boff0 = g0 * BPG * BB;   // byte offset of the slice in a weight row
+    const unsigned char *pA = ws + rA * p.WS + boff0 + t * 16;
+    const unsigned char *pB = ws + rB * p.WS + boff0 + t * 16;
+    const bool xin = g < M;            // this lane's token (B column) exists
+    const uint16_t *xb = xw + (xin ? g : 0) * XS + 4 * t;
+    const int slice_bytes = nk * BITS / 8;
+
+    float acc[NCH][4];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.0f;
+    if (have_w) {
+        for (int blk = 0; blk < nblk; ++blk) {
+            const int off = blk * BB;
+            const bool in = off + t * 16 < slice_bytes;
+            const uint4 wa = (in && okA) ? *reinterpret_cast<const uint4 *>(pA + off) : make_uint4(0, 0, 0, 0);
+            const uint4 wb = (in && okB) ? *reinterpret_cast<const uint4 *>(pB + off) : make_uint4(0, 0, 0, 0);
+            const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w};
+            const uint32_t B[4] = {wb.x, wb.y, wb.z, wb.w};
+            const uint16_t *xblk = xb + blk * KB;
+            if constexpr (BITS == 8) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t a0, a1, a2, a3;
+                    widen_i8(A[q], a0, a2);
+                    widen_i8(B[q], a1, a3);
+                    uint2 bv = make_uint2(0, 0);
+                    if (xin) bv = *reinterpret_cast<const uint2 *>(xblk + q * 16);
+                    mma_bf16(acc[q], a0, a1, a2, a3, bv.x, bv.y);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t pa[4], pb[4];
+                    widen_i4(A[q], pa);
+                    widen_i4(B[q], pb);
+                    uint2 b0 = make_uint2(0, 0), b1 = make_uint2(0, 0);
+                    if (xin) {
+                        b0 = *reinterpret_cast<const uint2 *>(xblk + (2 * q) * 16);
+                        b1 = *reinterpret_cast<const uint2 *>(xblk + (2 * q + 1) * 16);
+                    }
+                    mma_bf16(acc[(2 * q) % NCH], pa[0], pb[0], pa[1], pb[1], b0.x, b0.y);
+                    mma_bf16(acc[(2 * q + 1) % NCH], pa[2], pb[2], pa[3], pb[3], b1.x, b1.y);
+                }
+            }
+        }
+    }
+
+    // ---- fixed-order sum over the K slices, scale, store
+    float *red = reinterpret_cast<float *>(smem_raw + p.r_off);   // [WK][RT][M]
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int row = wr * 16 + g + 8 * h;
+        const int m0 = 2 * t;
+        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            s0 += acc[c][2 * h];
+            s1 += acc[c][2 * h + 1];
+        }
+        if (m0 < M) red[(wk * RT + row) * M + m0] = s0;
+        if (m0 + 1 < M) red[(wk * RT + row) * M + m0 + 1] = s1;
+    }
+    __syncthreads();
+    if (have_w) {
+        for (int idx = threadIdx.x; idx < rows * M; idx += kThreads) {
+            const int m = idx / rows, r = idx % rows;   // consecutive threads -> consecutive n
+            float s = 0.0f;
+            for (int k = 0; k < WK; ++k) s += red[(k * RT + r) * M + m];
+            const float y = sws[r] * s;
+            const int64_t n = n0 + r;
+            if (p.ytype == 0)
+                static_cast<float *>(p.Y)[m * p.ldy + n] = y;
+            else
+                static_cast<uint16_t *>(p.Y)[m * p.ldy + n] = f32_to_bf16_bits(y);
+        }
+    } else {
+        mbar_wait_bounded(wbar, 0);  // never leave with copies landing in shared memory
+    }
+}
+
+struct SmallPlan {
+    int WR, WK, gpw, WS, XS, w_off, x_off, r_off;
+    size_t smem;
+};
+
+constexpr size_t kSmallSmemMax = 200 * 1024;
+
+SmallPlan plan_small(int64_t M, int64_t N, int64_t K, int bits, const DeviceInfo &dev) {
+    const int64_t G = (K + kGroup - 1) / kGroup;
+    SmallPlan pl{};
+    // rows per CTA: the most (up to 128) that still give one CTA per SM
+    int WR = 1;
+    while (WR < 8 && (N + 32 * WR - 1) / (32 * WR) >= dev.sms) WR *= 2;
+    pl.WR = WR;
+    pl.WK = 8 / WR;
+    pl.gpw = static_cast<int>((G + pl.WK - 1) / pl.WK);
+    const int RT = 16 * WR;
+    const int64_t rb = K * bits / 8;
+    pl.WS = static_cast<int>((rb + 127) / 128 * 128 + 64);
+    pl.XS = pl.gpw * kGroup + 16;
+    pl.w_off = 128 + (4 * RT + 127) / 128 * 128;
+    pl.x_off = pl.w_off + RT * pl.WS;
+    pl.r_off = pl.x_off + static_cast<int>(8 * M * pl.XS * 2);
+    pl.r_off = (pl.r_off + 15) / 16 * 16;
+    pl.smem = static_cast<size_t>(pl.r_off) + static_cast<size_t>(pl.WK) * RT * M * 4;
+    return pl;
+}
+
+}  // namespace
+
+bool gemv_small_fits(int64_t M, int64_t N, int64_t K, int bits, const DeviceInfo &dev) {
+    if (M < 1 || M > 8) return false;
+    return plan_small(M, N, K, bits, dev).smem <= kSmallSmemMax;
+}
+
+tq_status launch_gemv_small(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
+                            const uint8_t *Wq, const float *sw, int64_t N, int bits,
+                            void *Y, int ytype, int64_t ldy, const DeviceInfo &dev,
+                            cudaStream_t s) {
+    const SmallPlan pl = plan_small(M, N, K, bits, dev);
+    if (pl.smem > kSmallSmemMax) return TQ_ERR_SHAPE;
+    unsigned int *status = status_word();
+    if (!status) return TQ_ERR_DEVICE;
+    SmallParams p{};
+    p.X = X;
+    p.ldx = ldx;
+    p.M = static_cast<int>(M);
+    p.K = K;
+    p.G = static_cast<int>((K + kGroup - 1) / kGroup);
+    p.W = Wq;
+    p.wld = bits == 8 ? K : K / 2;
+    p.sw = sw;
+    p.N = N;
+    p.Y = Y;
+    p.ldy = ldy;
+    p.ytype = ytype;
+    p.WR = pl.WR;
+    p.WK = pl.WK;
+    p.gpw = pl.gpw;
+    p.WS = pl.WS;
+    p.XS = pl.XS;
+    p.w_off = pl.w_off;
+    p.x_off = pl.x_off;
+    p.r_off = pl.r_off;
+    p.status = status;
+    auto kern = bits == 8 ? k_gemv_small<8> : k_gemv_small<4>;
+    static int configured_for[64][2] = {{0}};
+    const int bi = bits == 8 ? 0 : 1;
+    if (dev.id >= 0 && dev.id < 64 && !configured_for[dev.id][bi]) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(kSmallSmemMax));
+        if (e != cudaSuccess) return cuda_fail(e);
+        configured_for[dev.id][bi] = 1;
+    }
+    const int64_t tiles = (N + 16 * pl.WR - 1) / (16 * pl.WR);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+}  // namespace tq

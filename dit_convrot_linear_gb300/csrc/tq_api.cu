@@ -203,6 +203,10 @@ tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
     DeviceInfo dev;
     if ((st = current_device(&dev)) != TQ_OK) return st;
     if (mode != TQ_W8A8) {
+        if (gemv_small_fits(M, N, K, bits, dev))
+            return launch_gemv_small(static_cast<const uint16_t *>(X), M, K, ldx,
+                                     static_cast<const uint8_t *>(Wq), sw, N, bits, Y,
+                                     ytype == TQ_OUT_BF16 ? 1 : 0, ldy, dev, stream);
         if (!gemv_fits(M, K, bits, dev)) return TQ_ERR_SHAPE;
         return launch_gemv_a16(static_cast<const uint16_t *>(X), M, K, ldx,
                                static_cast<const uint8_t *>(Wq), sw, N, bits, Y,

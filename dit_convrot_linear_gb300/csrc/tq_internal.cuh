@@ -47,6 +47,13 @@ tq_status launch_gemv_a16(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
                           int bits, void *Y, int ytype, int64_t ldy,
                           const DeviceInfo &dev, cudaStream_t s);
 
+// Decode product for M <= 8: whole rows per CTA, no cluster reduction.
+bool gemv_small_fits(int64_t M, int64_t N, int64_t K, int bits, const DeviceInfo &dev);
+tq_status launch_gemv_small(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
+                            const uint8_t *Wq, const float *sw, int64_t N, int bits,
+                            void *Y, int ytype, int64_t ldy, const DeviceInfo &dev,
+                            cudaStream_t s);
+
 // A8 product on quantised activations: tcgen05 / TMEM, exact int32 sums.
 tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M,
                          int64_t K, const uint8_t *Wq, const float *sw,
