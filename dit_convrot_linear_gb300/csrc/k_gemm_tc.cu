@@ -19,30 +19,38 @@
 // output tile: each CTA holds 128 rows of A (activations) and 128 rows of B
 // (weights), and the MMA, issued by the even CTA, multiplies the pair's whole
 // A by the pair's whole B, leaving each CTA its 128 rows x 256 columns in its
-// own TMEM.  Each SM thus converts and stages half of B.  K steps of 64, six
-// stages, persistent over tiles.  Warp roles in each CTA:
-//   warps 0-7   convert: load int8/int4 codes with 16-byte loads one step
-//               ahead, widen to fp16 in registers, store the K-major 8x8
-//               core-matrix layout the MMA reads, arrive on the even CTA's
-//               stage barrier;
-//   warp 8      allocates TMEM for the pair; in the even CTA, lane 0 issues the
-//               MMAs and the commits (multicast to both CTAs);
+// own TMEM.  K steps of 64.  Per CTA:
+//   warp 13     TMA producer: 2-D tensor copies of the raw int8 / packed int4
+//               code tiles into a raw ring (64- or 32-byte swizzle, so the
+//               converters' reads are bank-conflict free);
+//   warps 0-7   convert raw codes to fp16 in the K-major 8x8 core-matrix
+//               layout the MMA reads (operand ring), shared to shared, and
+//               arrive on the even CTA's stage barrier;
+//   warp 8      allocates TMEM for the pair; in the even CTA, lane 0 issues
+//               the MMAs and the commits (multicast to both CTAs);
 //   warps 9-12  drain the accumulator (one TMEM lane quarter each) and write Y.
 // Every wait is bounded: on expiry the CTA records the failure in the library
 // status word, stops issuing work, lets in-flight MMAs finish (bounded), frees
 // its TMEM and returns.
+
+#include <cuda.h>
 
 #include "tq_internal.cuh"
 
 namespace tq {
 namespace {
 
-constexpr int HM = 128, BN = 256, HN = BN / 2, BK = 64, STAGES = 6;
-constexpr int NCONV = 8, MMA_WARP = 8, NWARPS = 13;
+constexpr int HM = 128, BN = 256, HN = BN / 2, BK = 64;
+constexpr int OSTAGES = 4, RSTAGES = 4;
+constexpr int NCONV = 8, MMA_WARP = 8, TMA_WARP = 13, NWARPS = 14;
 constexpr int THREADS = NWARPS * 32;
-constexpr int A_STAGE = HM * BK * 2;   // 16 KB fp16: this CTA's 128 rows of A
-constexpr int B_STAGE = HN * BK * 2;   // 16 KB fp16: this CTA's 128 rows of B
-constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024;
+constexpr int A_OP = HM * BK * 2;      // 16 KB fp16: this CTA's 128 rows of A
+constexpr int B_OP = HN * BK * 2;      // 16 KB fp16: this CTA's 128 rows of B
+constexpr int A_RAW = HM * BK;         // 8 KB int8 codes
+constexpr int B_RAW = HN * BK;         // 8 KB int8 codes (int4: half used)
+constexpr int OP_BYTES = OSTAGES * (A_OP + B_OP);
+constexpr int RAW_BYTES = RSTAGES * (A_RAW + B_RAW);
+constexpr int SMEM_BYTES = OP_BYTES + RAW_BYTES + 1024;
 constexpr uint32_t TMEM_COLS = 512;    // acc [0, 256) + running int32 sum [256, 512)
 constexpr uint32_t RUN_COL = 256;
 constexpr long long kWaitLimit = 4000000000ll;  // clock cycles, about 2 s
@@ -51,10 +59,8 @@ constexpr unsigned int kStatusGemmTimeout = 2u;
 constexpr uint32_t IDESC = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(256 >> 4) << 24);
 
 struct TcParams {
-    const int8_t *Xq;
     const float *sx;
     int64_t M, K;
-    const uint8_t *Wq;
     const float *sw;
     int64_t N;
     void *Y;
@@ -228,86 +234,58 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
         : "memory");
 }
 
-__device__ __forceinline__ uint4 ldg16(const void *p) {
-    return __ldg(reinterpret_cast<const uint4 *>(p));
+
+// byte offset of the 16-byte chunk c of row r in a TMA tile with 64-byte rows
+// and 64-byte swizzle (chunk index XOR address bits 7-8), or with 32-byte rows
+// and 32-byte swizzle (chunk bit XOR address bit 7)
+__device__ __forceinline__ int swz64(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
+__device__ __forceinline__ int swz32(int r, int c) { return r * 32 + ((c ^ ((r >> 2) & 1)) << 4); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
 }
 
-template <int BITS>
-struct Loads {
-    uint4 a[2];                        // A: 128 rows x 64 bytes, two 16-byte chunks per thread
-    uint4 b[BITS == 8 ? 2 : 1];        // B: 128 rows x 64 (int8) or 32 (int4) bytes
-};
-
-template <int BITS>
-__device__ __forceinline__ void load_step(const TcParams &p, int tid, int64_t m0, int64_t n0,
-                                          int64_t k0, int64_t wld, Loads<BITS> &L) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        int r, seg;
-        rows64(tid, j, r, seg);
-        const int64_t gm = m0 + r, gk = k0 + seg * 16;
-        L.a[j] = (gm < p.M && gk < p.K) ? ldg16(p.Xq + gm * p.K + gk) : make_uint4(0, 0, 0, 0);
-    }
-    if constexpr (BITS == 8) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            int r, seg;
-            rows64(tid, j, r, seg);
-            const int64_t gn = n0 + r, gk = k0 + seg * 16;
-            L.b[j] = (gn < p.N && gk < p.K) ? ldg16(p.Wq + gn * wld + gk) : make_uint4(0, 0, 0, 0);
-        }
-    } else {
-        int r, seg;
-        rows32(tid, r, seg);
-        const int64_t gn = n0 + r, gk = k0 + seg * 32;
-        L.b[0] = (gn < p.N && gk < p.K) ? ldg16(p.Wq + gn * wld + gk / 2) : make_uint4(0, 0, 0, 0);
-    }
-}
-
-template <int BITS>
-__device__ __forceinline__ void store_step(int tid, unsigned char *a, unsigned char *b, const Loads<BITS> &L) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        int r, seg;
-        rows64(tid, j, r, seg);
-        store_i8x16(a, r, seg, L.a[j]);
-    }
-    if constexpr (BITS == 8) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            int r, seg;
-            rows64(tid, j, r, seg);
-            store_i8x16(b, r, seg, L.b[j]);
-        }
-    } else {
-        int r, seg;
-        rows32(tid, r, seg);
-        store_i4x32(b, r, seg, L.b[0]);
-    }
+__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 template <int BITS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-k_gemm_a8_tc(const TcParams p) {
+k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+             const TcParams p) {
     extern __shared__ __align__(1024) unsigned char smem[];
-    unsigned char *sA = smem;
-    unsigned char *sB = smem + STAGES * A_STAGE;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * (A_STAGE + B_STAGE));
-    // bars: full[STAGES] (used in CTA 0), empty[STAGES], acc_full, acc_empty (CTA 0), done
+    unsigned char *opA = smem;                                   // [OSTAGES][A_OP]
+    unsigned char *opB = smem + OSTAGES * A_OP;                  // [OSTAGES][B_OP]
+    unsigned char *rawA = smem + OP_BYTES;                       // [RSTAGES][A_RAW]
+    unsigned char *rawB = smem + OP_BYTES + RSTAGES * A_RAW;     // [RSTAGES][B_RAW]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OP_BYTES + RAW_BYTES);
+    // bars: raw_full[R], raw_empty[R], op_full[O] (used in CTA 0), op_empty[O],
+    //       acc_full, acc_empty (CTA 0), done
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint32_t rank;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
-    const uint32_t acc_full = smem_u32(bars + 2 * STAGES), acc_empty = smem_u32(bars + 2 * STAGES + 1);
-    const uint32_t done = smem_u32(bars + 2 * STAGES + 2);
+    const uint32_t raw_full0 = smem_u32(bars), raw_empty0 = smem_u32(bars + RSTAGES);
+    const uint32_t op_full0 = smem_u32(bars + 2 * RSTAGES);
+    const uint32_t op_empty0 = smem_u32(bars + 2 * RSTAGES + OSTAGES);
+    const uint32_t acc_full = smem_u32(bars + 2 * RSTAGES + 2 * OSTAGES);
+    const uint32_t acc_empty = acc_full + 8, done = acc_full + 16;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * s), "r"(2 * NCONV));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(empty0 + 8 * s));
+        for (int s = 0; s < RSTAGES; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(raw_full0 + 8 * s));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(raw_empty0 + 8 * s), "r"(NCONV));
+        }
+        for (int s = 0; s < OSTAGES; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(op_full0 + 8 * s), "r"(2 * NCONV));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(op_empty0 + 8 * s));
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(acc_full));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(acc_empty));
@@ -327,45 +305,89 @@ k_gemm_a8_tc(const TcParams p) {
 
     const int ntiles_total = p.mtiles * p.ntiles;
     const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
-    const int64_t wld = BITS == 8 ? p.K : p.K / 2;
+    constexpr int BRAW = BITS == 8 ? B_RAW : B_RAW / 2;   // bytes of one raw B tile
 
-    if (warp < NCONV) {
-        // ------------------------------------------------ converters
+    if (warp == TMA_WARP) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
+                const int m0 = (tile % p.mtiles) * 2 * HM + static_cast<int>(rank) * HM;
+                const int n0 = (tile / p.mtiles) * BN + static_cast<int>(rank) * HN;
+                for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
+                    const int s = it % RSTAGES;
+                    if (!mbar_wait(raw_empty0 + 8 * s, ((it / RSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                                 ::"r"(raw_full0 + 8 * s), "r"(static_cast<uint32_t>(A_RAW + BRAW)) : "memory");
+                    tma_load_2d(smem_u32(rawA + s * A_RAW), &tmA, ks * BK, m0, raw_full0 + 8 * s);
+                    tma_load_2d(smem_u32(rawB + s * B_RAW), &tmB, ks * BK * BITS / 8, n0, raw_full0 + 8 * s);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp < NCONV) {
+        // ------------------------------------------------ converters (shared -> shared)
         const int tid = threadIdx.x;  // 0..255
         uint32_t it = 0;
-        Loads<BITS> cur, nxt;
-        // the (tile, k-step) sequence of this CTA, with one step of load lookahead
-        int tile = cluster_id, ks = 0;
-        auto coords = [&](int t, int64_t &m0, int64_t &n0) {
-            m0 = static_cast<int64_t>(t % p.mtiles) * 2 * HM + rank * HM;
-            n0 = static_cast<int64_t>(t / p.mtiles) * BN + rank * HN;
-        };
-        int64_t m0, n0;
-        if (tile < ntiles_total) {
-            coords(tile, m0, n0);
-            load_step<BITS>(p, tid, m0, n0, 0, wld, cur);
-        }
-        while (tile < ntiles_total && !abort_sh) {
-            // next step's coordinates, loaded ahead of this step's stores
-            int ntile = tile, nks = ks + 1;
-            if (nks == p.ksteps) { nks = 0; ntile += nclusters; }
-            if (ntile < ntiles_total) {
-                int64_t nm0, nn0;
-                coords(ntile, nm0, nn0);
-                load_step<BITS>(p, tid, nm0, nn0, static_cast<int64_t>(nks) * BK, wld, nxt);
+        for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
+            for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
+                const int rs = it % RSTAGES, os = it % OSTAGES;
+                if (!mbar_wait(raw_full0 + 8 * rs, (it / RSTAGES) & 1, &abort_sh, p.status)) break;
+                const unsigned char *ra = rawA + rs * A_RAW;
+                const unsigned char *rb = rawB + rs * B_RAW;
+                uint4 a[2], b[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    int r, seg;
+                    rows64(tid, j, r, seg);
+                    a[j] = *reinterpret_cast<const uint4 *>(ra + swz64(r, seg));
+                }
+                if constexpr (BITS == 8) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        int r, seg;
+                        rows64(tid, j, r, seg);
+                        b[j] = *reinterpret_cast<const uint4 *>(rb + swz64(r, seg));
+                    }
+                } else {
+                    int r, seg;
+                    rows32(tid, r, seg);
+                    b[0] = *reinterpret_cast<const uint4 *>(rb + swz32(r, seg));
+                }
+                if (!mbar_wait(op_empty0 + 8 * os, ((it / OSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
+                unsigned char *oa = opA + os * A_OP;
+                unsigned char *ob = opB + os * B_OP;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    int r, seg;
+                    rows64(tid, j, r, seg);
+                    store_i8x16(oa, r, seg, a[j]);
+                }
+                if constexpr (BITS == 8) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        int r, seg;
+                        rows64(tid, j, r, seg);
+                        store_i8x16(ob, r, seg, b[j]);
+                    }
+                } else {
+                    int r, seg;
+                    rows32(tid, r, seg);
+                    store_i4x32(ob, r, seg, b[0]);
+                }
+                // One proxy fence serves both hand-offs: it makes this lane's
+                // operand stores visible to the tensor core, and it orders this
+                // lane's plain reads of the raw slot before the next TMA write
+                // into that slot (both are async-proxy accesses; without the
+                // fence the TMA was seen to overwrite a slot still being read).
+                // The warp then arrives once on each barrier, after all its lanes.
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_leader(op_full0 + 8 * os);
+                    mbar_arrive_local(raw_empty0 + 8 * rs);
+                }
             }
-            const int s = it % STAGES;
-            if (!mbar_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1, &abort_sh, p.status)) break;
-            store_step<BITS>(tid, sA + s * A_STAGE, sB + s * B_STAGE, cur);
-            // every lane makes its stores visible to the tensor core (async
-            // proxy); the warp then arrives once, ordered after all its lanes
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive_leader(full0 + 8 * s);
-            cur = nxt;
-            tile = ntile;
-            ks = nks;
-            ++it;
         }
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------ MMA issue (CTA 0, one thread)
@@ -378,10 +400,10 @@ k_gemm_a8_tc(const TcParams p) {
                     if (ch > 0 && !mbar_wait(acc_empty, (ch - 1) & 1, &abort_sh, p.status)) break;
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     for (int ks = c0; ks < c1; ++ks, ++it) {
-                        const int s = it % STAGES;
-                        if (!mbar_wait(full0 + 8 * s, (it / STAGES) & 1, &abort_sh, p.status)) break;
+                        const int s = it % OSTAGES;
+                        if (!mbar_wait(op_full0 + 8 * s, (it / OSTAGES) & 1, &abort_sh, p.status)) break;
                         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                        const uint32_t a = smem_u32(sA + s * A_STAGE), b = smem_u32(sB + s * B_STAGE);
+                        const uint32_t a = smem_u32(opA + s * A_OP), b = smem_u32(opB + s * B_OP);
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk) {
                             const uint64_t ad = smem_desc(a + kk * 256), bd = smem_desc(b + kk * 256);
@@ -392,7 +414,7 @@ k_gemm_a8_tc(const TcParams p) {
                                 ::"r"(tmem), "l"(ad), "l"(bd), "r"(IDESC), "r"(accum));
                         }
                         issued = true;
-                        commit_pair(empty0 + 8 * s);
+                        commit_pair(op_empty0 + 8 * s);
                     }
                     if (abort_sh) break;
                     commit_pair(acc_full);
@@ -511,6 +533,41 @@ k_gemm_a8_tc(const TcParams p) {
     }
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+        cudaGetLastError();
+    }
+    return fn;
+}
+
+// 2-D map of a row-major byte matrix [rows][cols] (cols bytes per row), read in
+// boxes of box_cols bytes x 128 rows, out-of-range elements filled with zero.
+bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int box_cols,
+              CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), 128u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M, int64_t K,
@@ -519,12 +576,16 @@ tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M, int64_t K
                          cudaStream_t s) {
     unsigned int *status = status_word();
     if (!status) return TQ_ERR_DEVICE;
+    if (M > (1ll << 31) - 1 || N > (1ll << 31) - 1) return TQ_ERR_OVERFLOW;
+    CUtensorMap tmA, tmB;
+    if (!make_map(&tmA, Xq, M, K, BK, CU_TENSOR_MAP_SWIZZLE_64B)) return TQ_ERR_DEVICE;
+    const bool mapped = bits == 8 ? make_map(&tmB, Wq, N, K, BK, CU_TENSOR_MAP_SWIZZLE_64B)
+                                  : make_map(&tmB, Wq, N, K / 2, BK / 2, CU_TENSOR_MAP_SWIZZLE_32B);
+    if (!mapped) return TQ_ERR_DEVICE;
     TcParams p{};
-    p.Xq = Xq;
     p.sx = sx;
     p.M = M;
     p.K = K;
-    p.Wq = Wq;
     p.sw = sw;
     p.N = N;
     p.Y = Y;
@@ -547,7 +608,7 @@ tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M, int64_t K
         configured_for[dev.id][bi] = 1;
     }
     const int64_t pairs = tiles < dev.sms / 2 ? tiles : dev.sms / 2;
-    kern<<<static_cast<unsigned>(2 * pairs), THREADS, SMEM_BYTES, s>>>(p);
+    kern<<<static_cast<unsigned>(2 * pairs), THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }

@@ -176,17 +176,37 @@ k_gemv_small(const SmallParams p) {
     const int64_t kslice0 = static_cast<int64_t>(g0) * kGroup;
     const int nk = static_cast<int>(min(static_cast<int64_t>(g1) * kGroup, p.K) - kslice0);
     const int nblk = (nk + KB - 1) / KB;
+    // groups are taken GB at a time: all their loads are issued before any
+    // butterfly, so the row reads of a slice overlap instead of queueing
+    constexpr int GB = 4;
+    const int ng = g1 - g0;
     for (int m = 0; m < M; ++m) {
         uint16_t *xrow = xw + m * XS;
-        for (int gi = 0; gi < g1 - g0; ++gi) {
-            const int64_t gk = kslice0 + static_cast<int64_t>(gi) * kGroup;
-            float v[8] = {};
-            const int E = rotate_group32_any(p.X + m * p.ldx + gk, group_width(p.K, gk), v);
+        for (int gb = 0; gb < ng; gb += GB) {
+            uint4 raw[GB];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (e < E) {
-                    const int kl = gi * kGroup + lane * E + e;
-                    xrow[(kl / KB) * KB + xpos<BITS>(kl % KB)] = f32_to_bf16_bits(v[e]);
+            for (int u = 0; u < GB; ++u) {
+                raw[u] = make_uint4(0, 0, 0, 0);
+                const int gi = gb + u;
+                if (gi < ng) {
+                    const int64_t gk = kslice0 + static_cast<int64_t>(gi) * kGroup;
+                    const int E = group_width(p.K, gk) / 32;
+                    raw[u] = load_group_raw(p.X + m * p.ldx + gk + lane * E, E);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < GB; ++u) {
+                const int gi = gb + u;
+                if (gi >= ng) break;
+                const int64_t gk = kslice0 + static_cast<int64_t>(gi) * kGroup;
+                float v[8] = {};
+                const int E = fwht_group_raw(raw[u], group_width(p.K, gk), v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (e < E) {
+                        const int kl = gi * kGroup + lane * E + e;
+                        xrow[(kl / KB) * KB + xpos<BITS>(kl % KB)] = f32_to_bf16_bits(v[e]);
+                    }
                 }
             }
         }

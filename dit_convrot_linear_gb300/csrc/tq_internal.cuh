@@ -152,6 +152,39 @@ __device__ __forceinline__ int rotate_group32_any(const uint16_t *src, int n, fl
     }
 }
 
+// The same rotation split in two, so that a warp can issue the loads of several
+// groups before transforming any: the raw bits of this lane's E = n/32 values...
+__device__ __forceinline__ uint4 load_group_raw(const uint16_t *p, int E) {
+    if (E == 8) return __ldg(reinterpret_cast<const uint4 *>(p));
+    if (E == 4) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+        return make_uint4(u.x, u.y, 0, 0);
+    }
+    if (E == 2) return make_uint4(__ldg(reinterpret_cast<const unsigned int *>(p)), 0, 0, 0);
+    return make_uint4(__ldg(reinterpret_cast<const unsigned short *>(p)), 0, 0, 0);
+}
+
+// ...and their transform: widen, butterfly, scale by sqrt(1/n).  Returns E.
+__device__ __forceinline__ int fwht_group_raw(const uint4 &r, int n, float (&v)[8]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    int E;
+    switch (n) {
+        case 256: warp_fwht<8, float>(v); E = 8; break;
+        case 128: warp_fwht<4, float>(v); E = 4; break;
+        case 64: warp_fwht<2, float>(v); E = 2; break;
+        default: warp_fwht<1, float>(v); E = 1; break;
+    }
+    const float c = sqrtf(1.0f / static_cast<float>(n));
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = e < E ? c * v[e] : 0.0f;
+    return E;
+}
+
 // ---- PTX wrappers
 
 __device__ __forceinline__ void pdl_launch_dependents() {
