@@ -291,14 +291,32 @@ def time_steps(fn, steps, warmup, world):
     return max_over_ranks(ms, world)
 
 
+class L2Flush:
+    """Empties L2 between timed calls: writes a buffer larger than L2, then
+    reads another one, so the written lines are back in HBM (not dirty in L2,
+    where their write-back would be charged to the next timed kernel)."""
+
+    def __init__(self, device, mb=512):
+        import torch
+        self.w = torch.empty(mb * 2 ** 20, dtype=torch.uint8, device=device)
+        self.r = torch.zeros(mb * 2 ** 18, dtype=torch.int32, device=device)
+        self.n = 0
+
+    def __call__(self):
+        self.n += 1
+        self.w.fill_(self.n & 0xFF)
+        return self.r.max()
+
+
 def dit_measure(device, reps=5, M=4032):
     """M = 4032 W8A8 (DiT FFN up and down): TOPS = 2 M N K / t per GEMM, L2
-    flushed between timed calls (a 512 MB write)."""
+    flushed between timed calls (a 512 MB write, then a 512 MB read so that
+    the flush's dirty lines are written back before the timed call starts)."""
     import torch
     from dit_convrot_linear_gb300 import synth, tq
     w = synth.DIT
     out = {}
-    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     tot_ops = tot_ms = 0.0
     gemm_ms_tot = 0.0
     for p in w.projs:
@@ -313,12 +331,12 @@ def dit_measure(device, reps=5, M=4032):
         torch.cuda.synchronize()
         ms, gms = [], []
         for _ in range(reps):
-            flush.fill_(1)
+            flush()
             e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             e0.record()
             tq.linear(X, codes, sw, p.N, 8, "W8A8", Y=Y, workspace=ws)
             e1.record()
-            flush.fill_(2)
+            flush()
             sx = ws[(M * p.K + 255) // 256 * 256:].view(torch.float32)[:M]
             e2a = torch.cuda.Event(enable_timing=True)
             e2a.record()

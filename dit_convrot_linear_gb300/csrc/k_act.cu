@@ -6,24 +6,227 @@
 // "幅とメモリ"); the device quantises each product's activations finely
 // (section "GPU"), here with one scale per token over all of K.
 //
-// Memory-bound: read 2 B and write 1 B (A8) or 2 B (A16) per element.  Each
-// lane moves 16-byte vectors; one warp holds one 256-group (8 values a lane)
-// through the whole butterfly in registers and shuffles.
+// Memory-bound: read 2 B and write 1 B (A8) or 2 B (A16) per element.  One
+// warp holds one 256-group (8 values a lane) through the whole butterfly in
+// registers and shuffles.  For the A8 path, rows of up to 16384 values are
+// streamed through a ring of shared-memory row buffers filled by bulk copies
+// several rows ahead (persistent CTAs), so the HBM reads of the next rows
+// overlap the transform, amax and stores of the current one; longer rows use
+// a plain one-CTA-per-row kernel that loads each group straight from global.
 
 #include "tq_internal.cuh"
 
 namespace tq {
 namespace {
 
-__device__ __forceinline__ uint32_t quant4(const float *v, float s) {
+// Code of one value: clamp(rint(v / s)) with the quotient correctly rounded
+// (IEEE division), as the scale formula reads.  r = 1/s when that is finite,
+// else 0.  The product t = v * r is within a few ulps of v / s (|v / s| <= 127
+// here, an ulp at most 2^-17), so rint(t) equals rint of the rounded quotient
+// unless t lies near a half-integer; only there is the division taken.
+__device__ __forceinline__ int quant_code(float v, float s, float r) {
+    if (s == 0.0f) return 0;
+    float t = v * r;
+    if (r == 0.0f || fabsf((t - floorf(t)) - 0.5f) < 1e-3f) t = __fdiv_rn(v, s);
+    return min(max(__float2int_rn(t), -127), 127);
+}
+
+__device__ __forceinline__ float recip_or_zero(float s) {
+    const float r = __frcp_rn(s);
+    return (s != 0.0f && isfinite(r)) ? r : 0.0f;
+}
+
+__device__ __forceinline__ uint32_t quant4(const float *v, float s, float r) {
     uint32_t w = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        int q = 0;
-        if (s != 0.0f) q = min(max(__float2int_rn(__fdiv_rn(v[e], s)), -127), 127);
-        w |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * e);
-    }
+    for (int e = 0; e < 4; ++e)
+        w |= (static_cast<uint32_t>(quant_code(v[e], s, r)) & 0xFFu) << (8 * e);
     return w;
+}
+
+constexpr long long kWaitLimit = 4000000000ll;  // clock cycles (about 2 s)
+constexpr unsigned int kStatusActTimeout = 8u;
+constexpr int64_t kRingMaxK = 16384;             // longest row the ring path takes
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Rotate one group (width n = 32*E) read from a shared-memory row buffer:
+// v = c_n * Hs_n * x in fp32, the same butterfly and scale as the global path.
+__device__ __forceinline__ int rotate_group_shared(const unsigned char *grp, int n, float (&v)[8]) {
+    const int lane = threadIdx.x & 31;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    const int E = n >> 5;
+    const unsigned char *src = grp + lane * E * 2;
+    if (E == 8) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(src);
+        w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+    } else if (E == 4) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(src);
+        w[0] = u.x; w[1] = u.y;
+    } else if (E == 2) {
+        w[0] = *reinterpret_cast<const uint32_t *>(src);
+    } else {
+        w[0] = *reinterpret_cast<const uint16_t *>(src);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    switch (E) {
+        case 8: warp_fwht<8, float>(v); break;
+        case 4: warp_fwht<4, float>(v); break;
+        case 2: warp_fwht<2, float>(v); break;
+        default: warp_fwht<1, float>(v); break;
+    }
+    const float c = sqrtf(1.0f / static_cast<float>(n));
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = e < E ? c * v[e] : 0.0f;
+    return E;
+}
+
+__device__ __forceinline__ void store_codes(int8_t *dst, int e_per_lane, const float *vals, float s,
+                                            float r) {
+    const uint32_t lo = quant4(vals, s, r);
+    if (e_per_lane == 8) {
+        const uint32_t hi = quant4(vals + 4, s, r);
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(lo, hi);
+    } else if (e_per_lane == 4) {
+        *reinterpret_cast<uint32_t *>(dst) = lo;
+    } else if (e_per_lane == 2) {
+        *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(lo);
+    } else {
+        *reinterpret_cast<uint8_t *>(dst) = static_cast<uint8_t>(lo);
+    }
+}
+
+// Persistent CTAs (8 warps); CTA b takes rows b, b + gridDim.x, ...  Thread 0
+// keeps S rows in flight: row i of this CTA goes to buffer i % S, copied by
+// one bulk copy that completes on that buffer's barrier.  Warp w owns groups
+// w, w + 8, ...; the first GPW stay in registers between the amax pass and
+// the quantise pass, further ones are recomputed from the buffer.
+template <int GPW>
+__global__ void __launch_bounds__(kThreads)
+k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx,
+                    int8_t *__restrict__ Xq, float *__restrict__ sx, int S,
+                    unsigned int *status) {
+    extern __shared__ __align__(128) unsigned char ring[];   // [S][2K] then S barriers
+    __shared__ float red[kThreads / 32];
+    __shared__ int abort_sh;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int W = kThreads / 32;
+    const int64_t G = (K + kGroup - 1) / kGroup;
+    const uint32_t row_bytes = static_cast<uint32_t>(K * 2);
+    const uint32_t ring0 = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+    const uint32_t bar0 = ring0 + static_cast<uint32_t>(S) * row_bytes;
+    const int64_t nrows = blockIdx.x < M ? (M - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    auto issue = [&](int64_t i) {   // thread 0: row i of this CTA into buffer i % S
+        const int slot = static_cast<int>(i % S);
+        const uint32_t bar = bar0 + 8u * slot;
+        const uint16_t *src = X + (blockIdx.x + i * gridDim.x) * ldx;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(row_bytes)
+                     : "memory");
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+            ::"r"(ring0 + static_cast<uint32_t>(slot) * row_bytes), "l"(src), "r"(row_bytes), "r"(bar)
+            : "memory");
+    };
+
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        for (int i = 0; i < S; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8u * i));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int64_t i = 0; i < nrows && i < S; ++i) issue(i);
+    }
+    __syncthreads();
+
+    int64_t i = 0;
+    for (; i < nrows; ++i) {
+        const int slot = static_cast<int>(i % S);
+        const uint32_t parity = static_cast<uint32_t>((i / S) & 1);
+        const long long t0 = clock64();
+        bool ok = true;
+        while (!mbar_try(bar0 + 8u * slot, parity)) {
+            if (abort_sh || clock64() - t0 > kWaitLimit) { ok = false; break; }
+        }
+        if (!ok) {
+            abort_sh = 1;
+            if (lane == 0) atomicOr(status, kStatusActTimeout);
+        }
+        __syncthreads();
+        if (abort_sh) break;
+        const unsigned char *buf = ring + static_cast<size_t>(slot) * row_bytes;
+        const int64_t m = blockIdx.x + i * gridDim.x;
+
+        float v[GPW][8];
+        int E[GPW];
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < GPW; ++j) {
+            const int64_t g = warp + static_cast<int64_t>(j) * W;
+            E[j] = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[j][e] = 0.0f;
+            if (g < G) E[j] = rotate_group_shared(buf + g * kGroup * 2, group_width(K, g * kGroup), v[j]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[j][e]));
+        }
+        for (int64_t g = warp + static_cast<int64_t>(GPW) * W; g < G; g += W) {
+            float t[8];
+            rotate_group_shared(buf + g * kGroup * 2, group_width(K, g * kGroup), t);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(t[e]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) red[warp] = amax;
+        __syncthreads();
+        amax = red[0];
+#pragma unroll
+        for (int w = 1; w < W; ++w) amax = fmaxf(amax, red[w]);
+
+        const float s = __fdiv_rn(amax, 127.0f);
+        const float r = recip_or_zero(s);
+        if (threadIdx.x == 0) sx[m] = s;
+        int8_t *qrow = Xq + m * K;
+#pragma unroll
+        for (int j = 0; j < GPW; ++j) {
+            const int64_t g = warp + static_cast<int64_t>(j) * W;
+            if (g < G) store_codes(qrow + g * kGroup + static_cast<int64_t>(lane) * E[j], E[j], v[j], s, r);
+        }
+        for (int64_t g = warp + static_cast<int64_t>(GPW) * W; g < G; g += W) {
+            float t[8];
+            const int e = rotate_group_shared(buf + g * kGroup * 2, group_width(K, g * kGroup), t);
+            store_codes(qrow + g * kGroup + static_cast<int64_t>(lane) * e, e, t, s, r);
+        }
+        // This thread's reads of the buffer are ordered before the bulk copy
+        // (async proxy) that will refill it; the barrier then makes every
+        // thread's reads, and the reads of red[], precede the refill.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (threadIdx.x == 0 && i + S < nrows) issue(i + S);
+    }
+    // After an expired wait, let the copies still in flight land (bounded)
+    // before the CTA's shared memory is released.
+    if (threadIdx.x == 0 && i < nrows) {
+        const long long t0 = clock64();
+        for (int64_t j = i; j < nrows && j < i + S; ++j) {
+            while (!mbar_try(bar0 + 8u * static_cast<uint32_t>(j % S), static_cast<uint32_t>((j / S) & 1)) &&
+                   clock64() - t0 < kWaitLimit) {
+            }
+        }
+    }
 }
 
 // One CTA (8 warps) per token row.  Warp w owns groups w, w+8, ...; the first
@@ -69,22 +272,12 @@ k_rotate_quant_act(const uint16_t *__restrict__ X, int64_t M, int64_t K,
         __syncthreads();
 
         const float s = __fdiv_rn(amax, 127.0f);
+        const float r = recip_or_zero(s);
         if (threadIdx.x == 0) sx[m] = s;
         int8_t *qrow = Xq + m * K;
 
         auto store = [&](int64_t g, int e_per_lane, const float *vals) {
-            int8_t *dst = qrow + g * kGroup + static_cast<int64_t>(lane) * e_per_lane;
-            const uint32_t lo = quant4(vals, s);
-            if (e_per_lane == 8) {
-                const uint32_t hi = quant4(vals + 4, s);
-                *reinterpret_cast<uint2 *>(dst) = make_uint2(lo, hi);
-            } else if (e_per_lane == 4) {
-                *reinterpret_cast<uint32_t *>(dst) = lo;
-            } else if (e_per_lane == 2) {
-                *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(lo);
-            } else {
-                *reinterpret_cast<uint8_t *>(dst) = static_cast<uint8_t>(lo);
-            }
+            store_codes(qrow + g * kGroup + static_cast<int64_t>(lane) * e_per_lane, e_per_lane, vals, s, r);
         };
 #pragma unroll
         for (int i = 0; i < GPW; ++i) {
@@ -132,6 +325,43 @@ tq_status launch_rotate_quant_act(const uint16_t *X, int64_t M, int64_t K,
                                   cudaStream_t s) {
     const int64_t G = (K + kGroup - 1) / kGroup;
     const int64_t gpw = (G + 7) / 8;
+    if (M == 0) return TQ_OK;
+    DeviceInfo dev;
+    const tq_status ds = current_device(&dev);
+    if (ds != TQ_OK) return ds;
+    if (K <= kRingMaxK) {
+        unsigned int *status = status_word();
+        if (!status) return TQ_ERR_DEVICE;
+        // rows in flight per CTA: about 48 KB of them, 2 to 8 rows; up to 4
+        // CTAs per SM while their buffers fit
+        const int64_t rb = 2 * K;
+        int S = static_cast<int>((48 * 1024) / rb);
+        S = S < 2 ? 2 : (S > 8 ? 8 : S);
+        const size_t smem = static_cast<size_t>(S) * rb + 8 * S;
+        auto kern = gpw <= 1 ? k_rotate_quant_ring<1>
+                  : gpw <= 2 ? k_rotate_quant_ring<2>
+                  : gpw <= 4 ? k_rotate_quant_ring<4>
+                             : k_rotate_quant_ring<8>;
+        const int ki = gpw <= 1 ? 0 : gpw <= 2 ? 1 : gpw <= 4 ? 2 : 3;
+        static bool configured[64][4] = {{false}};
+        if (dev.id < 0 || dev.id >= 64) return TQ_ERR_DEVICE;
+        if (!configured[dev.id][ki]) {
+            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(kRingMaxK * 2 * 2 + 64));
+            if (e != cudaSuccess) return cuda_fail(e);
+            configured[dev.id][ki] = true;
+        }
+        // persistent: as many CTAs as are resident at once, at most 4 per SM
+        int per_sm = 0;
+        const cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+        if (oe != cudaSuccess) return cuda_fail(oe);
+        per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
+        const int64_t want = static_cast<int64_t>(dev.sms) * per_sm;
+        const unsigned grid = static_cast<unsigned>(M < want ? M : want);
+        kern<<<grid, kThreads, smem, s>>>(X, M, K, ldx, Xq, sx, S, status);
+        const cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+    }
     const unsigned grid = static_cast<unsigned>(M < (1ll << 30) ? M : (1ll << 30));
     if (gpw <= 1) k_rotate_quant_act<1><<<grid, kThreads, 0, s>>>(X, M, K, ldx, Xq, sx);
     else if (gpw <= 2) k_rotate_quant_act<2><<<grid, kThreads, 0, s>>>(X, M, K, ldx, Xq, sx);

@@ -25,7 +25,9 @@
 //               converters' reads are bank-conflict free);
 //   warps 0-7   convert raw codes to fp16 in the K-major 8x8 core-matrix
 //               layout the MMA reads (operand ring), shared to shared, and
-//               arrive on the even CTA's stage barrier;
+//               arrive on the even CTA's stage barrier; they work in groups
+//               that take turns over the K steps, so one group's proxy fence
+//               and cluster arrive overlap the others' conversions;
 //   warp 8      allocates TMEM for the pair; in the even CTA, lane 0 issues
 //               the MMAs and the commits (multicast to both CTAs);
 //   warps 9-12  drain the accumulator (one TMEM lane quarter each) and write Y.
@@ -43,6 +45,18 @@ namespace {
 constexpr int HM = 128, BN = 256, HN = BN / 2, BK = 64;
 constexpr int OSTAGES = 4, RSTAGES = 4;
 constexpr int NCONV = 8, MMA_WARP = 8, TMA_WARP = 13, NWARPS = 14;
+// The converter warps form CONV_GROUPS groups; group g converts the K steps
+// it with it % CONV_GROUPS == g, so the fence-and-arrive latency at the end of
+// one group's step overlaps the other groups' conversions.
+#ifndef TQ_CONV_GROUPS
+#define TQ_CONV_GROUPS 4
+#endif
+constexpr int CONV_GROUPS = TQ_CONV_GROUPS;
+constexpr int WPG = NCONV / CONV_GROUPS;       // warps per group
+constexpr int TPG = 32 * WPG;                  // threads per group
+// Each use of a ring slot is converted by one group, so a slot's barriers
+// count one group's warps whatever the ring depths are.
+static_assert(NCONV % CONV_GROUPS == 0, "groups of whole warps");
 constexpr int THREADS = NWARPS * 32;
 constexpr int A_OP = HM * BK * 2;      // 16 KB fp16: this CTA's 128 rows of A
 constexpr int B_OP = HN * BK * 2;      // 16 KB fp16: this CTA's 128 rows of B
@@ -81,19 +95,20 @@ __device__ __forceinline__ int cm_off(int r, int k) {
     return ((r >> 3) * 8 + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2;
 }
 
-// Converter thread -> (row, 16-byte segment) of a 128-row tile for pass j.
-// Each group of 8 consecutive lanes (one shared-store phase) takes 8
-// consecutive rows of one segment, so its 16-byte stores fill one 128-byte
-// core-matrix block (conflict-free), while a warp still loads whole sectors.
-// 64-byte rows (int8 codes, 4 segments): passes 0..1
+// Converter thread (tid < TPG within its group) -> (row, 16-byte segment) of
+// a 128-row tile for pass j.  Each run of 8 consecutive lanes (one shared-store
+// phase) takes 8 consecutive rows of one segment, so its 16-byte stores fill
+// one 128-byte core-matrix block (conflict-free), while a warp still loads
+// whole sectors.
+// 64-byte rows (int8 codes, 4 segments): passes 0 .. 512/TPG - 1
 __device__ __forceinline__ void rows64(int tid, int j, int &r, int &seg) {
-    const int lane = tid & 31, grp = (256 * j + tid) >> 5;
+    const int lane = tid & 31, grp = (TPG * j + tid) >> 5;
     r = grp * 8 + (lane & 7);
     seg = lane >> 3;
 }
-// 32-byte rows (packed int4 codes, 2 segments): pass 0
-__device__ __forceinline__ void rows32(int tid, int &r, int &seg) {
-    const int lane = tid & 31, grp = tid >> 5;
+// 32-byte rows (packed int4 codes, 2 segments): passes 0 .. 256/TPG - 1
+__device__ __forceinline__ void rows32(int tid, int j, int &r, int &seg) {
+    const int lane = tid & 31, grp = (TPG * j + tid) >> 5;
     r = grp * 16 + ((lane >> 4) << 3) + (lane & 7);
     seg = (lane >> 3) & 1;
 }
@@ -281,10 +296,10 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     if (threadIdx.x == 0) {
         for (int s = 0; s < RSTAGES; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(raw_full0 + 8 * s));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(raw_empty0 + 8 * s), "r"(NCONV));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(raw_empty0 + 8 * s), "r"(WPG));
         }
         for (int s = 0; s < OSTAGES; ++s) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(op_full0 + 8 * s), "r"(2 * NCONV));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(op_full0 + 8 * s), "r"(2 * WPG));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(op_empty0 + 8 * s));
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(acc_full));
@@ -327,53 +342,59 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         __syncwarp();
     } else if (warp < NCONV) {
         // ------------------------------------------------ converters (shared -> shared)
-        const int tid = threadIdx.x;  // 0..255
+        const int g = warp / WPG, tid = threadIdx.x % TPG;
+        constexpr int NA = 512 / TPG;                          // A passes (and int8 B passes)
+        constexpr int NB = BITS == 8 ? 512 / TPG : 256 / TPG;  // B passes
         uint32_t it = 0;
         for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
             for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
+                if (static_cast<int>(it % CONV_GROUPS) != g) continue;
                 const int rs = it % RSTAGES, os = it % OSTAGES;
                 if (!mbar_wait(raw_full0 + 8 * rs, (it / RSTAGES) & 1, &abort_sh, p.status)) break;
+                if (!mbar_wait(op_empty0 + 8 * os, ((it / OSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
                 const unsigned char *ra = rawA + rs * A_RAW;
                 const unsigned char *rb = rawB + rs * B_RAW;
-                uint4 a[2], b[2];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    int r, seg;
-                    rows64(tid, j, r, seg);
-                    a[j] = *reinterpret_cast<const uint4 *>(ra + swz64(r, seg));
-                }
-                if constexpr (BITS == 8) {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        int r, seg;
-                        rows64(tid, j, r, seg);
-                        b[j] = *reinterpret_cast<const uint4 *>(rb + swz64(r, seg));
-                    }
-                } else {
-                    int r, seg;
-                    rows32(tid, r, seg);
-                    b[0] = *reinterpret_cast<const uint4 *>(rb + swz32(r, seg));
-                }
-                if (!mbar_wait(op_empty0 + 8 * os, ((it / OSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
                 unsigned char *oa = opA + os * A_OP;
                 unsigned char *ob = opB + os * B_OP;
+                {
+                    uint4 a[NA];
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    int r, seg;
-                    rows64(tid, j, r, seg);
-                    store_i8x16(oa, r, seg, a[j]);
-                }
-                if constexpr (BITS == 8) {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
+                    for (int j = 0; j < NA; ++j) {
                         int r, seg;
                         rows64(tid, j, r, seg);
-                        store_i8x16(ob, r, seg, b[j]);
+                        a[j] = *reinterpret_cast<const uint4 *>(ra + swz64(r, seg));
                     }
-                } else {
-                    int r, seg;
-                    rows32(tid, r, seg);
-                    store_i4x32(ob, r, seg, b[0]);
+#pragma unroll
+                    for (int j = 0; j < NA; ++j) {
+                        int r, seg;
+                        rows64(tid, j, r, seg);
+                        store_i8x16(oa, r, seg, a[j]);
+                    }
+                }
+                {
+                    uint4 b[NB];
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) {
+                        int r, seg;
+                        if constexpr (BITS == 8) {
+                            rows64(tid, j, r, seg);
+                            b[j] = *reinterpret_cast<const uint4 *>(rb + swz64(r, seg));
+                        } else {
+                            rows32(tid, j, r, seg);
+                            b[j] = *reinterpret_cast<const uint4 *>(rb + swz32(r, seg));
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) {
+                        int r, seg;
+                        if constexpr (BITS == 8) {
+                            rows64(tid, j, r, seg);
+                            store_i8x16(ob, r, seg, b[j]);
+                        } else {
+                            rows32(tid, j, r, seg);
+                            store_i4x32(ob, r, seg, b[j]);
+                        }
+                    }
                 }
                 // One proxy fence serves both hand-offs: it makes this lane's
                 // operand stores visible to the tensor core, and it orders this

@@ -96,6 +96,10 @@ __device__ __forceinline__ void load_bf16(const uint16_t *p, T (&v)[8]) {
     }
 }
 
+// Fused multiply-add in the type of the operands (one rounding).
+__device__ __forceinline__ float fused_madd(float a, float b, float c) { return fmaf(a, b, c); }
+__device__ __forceinline__ double fused_madd(double a, double b, double c) { return fma(a, b, c); }
+
 // Unnormalised Walsh-Hadamard transform, natural (Sylvester) order, of one
 // group of 32*E values held E per lane (element index = lane*E + e): the
 // in-place butterfly (a, b) -> (a + b, a - b) over every bit of the index,
@@ -113,13 +117,17 @@ __device__ __forceinline__ void warp_fwht(T (&v)[8]) {
             }
         }
     }
+    // Across lanes: the lane with bit m set keeps o - v, its partner v + o.
+    // Both are one fused multiply-add with a +-1 factor, which rounds the
+    // exact sum or difference once, like the plain add or subtract.
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1) {
+        const T sg = (lane & m) ? T(-1) : T(1);
 #pragma unroll
         for (int i = 0; i < E; ++i) {
             const T o = __shfl_xor_sync(0xffffffffu, v[i], m);
-            v[i] = (lane & m) ? (o - v[i]) : (v[i] + o);
+            v[i] = fused_madd(sg, v[i], o);
         }
     }
 }
