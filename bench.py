@@ -325,7 +325,8 @@ def dit_measure(device, reps=5, M=4032):
         Y = torch.empty((M, p.N), dtype=torch.float32, device=device)
         ws = torch.empty(tq.linear_workspace_bytes(M, p.K, p.N, 8, "W8A8"), dtype=torch.uint8,
                          device=device)
-        Xq = ws[:M * p.K].view(M, p.K).view(torch.int8)
+        # the product alone, on the operand tq_linear builds in its workspace
+        At, sxt = tq.rotate_quant_act_tiled(X)
         for _ in range(3):
             tq.linear(X, codes, sw, p.N, 8, "W8A8", Y=Y, workspace=ws)
         torch.cuda.synchronize()
@@ -337,10 +338,9 @@ def dit_measure(device, reps=5, M=4032):
             tq.linear(X, codes, sw, p.N, 8, "W8A8", Y=Y, workspace=ws)
             e1.record()
             flush()
-            sx = ws[(M * p.K + 255) // 256 * 256:].view(torch.float32)[:M]
             e2a = torch.cuda.Event(enable_timing=True)
             e2a.record()
-            tq.linear_q8(Xq, sx, codes, sw, p.N, 8, Y=Y)
+            tq.linear_tiled(At, sxt, M, p.K, codes, sw, p.N, 8, Y=Y)
             e2.record()
             torch.cuda.synchronize()
             ms.append(e0.elapsed_time(e1))
@@ -353,7 +353,7 @@ def dit_measure(device, reps=5, M=4032):
         tot_ops += ops
         tot_ms += t
         gemm_ms_tot += tg
-        del codes, sw, X, Y, ws
+        del codes, sw, X, Y, ws, At, sxt
     return out, tot_ops / tot_ms / 1e9, tot_ops / gemm_ms_tot / 1e9
 
 

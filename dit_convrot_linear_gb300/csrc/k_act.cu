@@ -1,10 +1,11 @@
 // Activation rotation: a 256-wide fast Walsh-Hadamard transform per group of
 // each token row, fused with the per-token symmetric int8 quantisation (A8),
 // or rounded to bf16 (A16 operand).  The input rows of a product get the same
-// rotation as the weights, "viewing a row as groups of 256 and taking one
-// product with H" (tensai docs, "画像生成" / Image generation, section
-// "幅とメモリ"); the device quantises each product's activations finely
-// (section "GPU"), here with one scale per token over all of K.
+// rotation as the weights: each row is cut into 256-wide groups and each group
+// is multiplied by H (tensai docs, "画像生成" / Image generation, section
+// "幅とメモリ"); on the device the activations of each product are quantised
+// at a finer grain than the weights (section "GPU"), here one scale per token
+// over all of K.
 //
 // Memory-bound: read 2 B and write 1 B (A8) or 2 B (A16) per element.  One
 // warp holds one 256-group (8 values a lane) through the whole butterfly in
@@ -13,6 +14,8 @@
 // several rows ahead (persistent CTAs), so the HBM reads of the next rows
 // overlap the transform, amax and stores of the current one; longer rows use
 // a plain one-CTA-per-row kernel that loads each group straight from global.
+
+#include <cfloat>
 
 #include "tq_internal.cuh"
 
@@ -46,7 +49,7 @@ __device__ __forceinline__ uint32_t quant4(const float *v, float s, float r) {
 
 constexpr long long kWaitLimit = 4000000000ll;  // clock cycles (about 2 s)
 constexpr unsigned int kStatusActTimeout = 8u;
-constexpr int64_t kRingMaxK = 16384;             // longest row the ring path takes
+constexpr int64_t kRingMaxK = TQ_MAX_K_TILED;    // longest row the ring path takes
 
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -109,22 +112,97 @@ __device__ __forceinline__ void store_codes(int8_t *dst, int e_per_lane, const f
     }
 }
 
+// Unnormalised transform (Hs x, Sylvester order) of one full 256-group read
+// from a shared-memory row buffer: 8 values a lane.
+__device__ __forceinline__ void fwht256_shared(const unsigned char *grp, float (&v)[8]) {
+    const int lane = threadIdx.x & 31;
+    const uint4 u = *reinterpret_cast<const uint4 *>(grp + lane * 16);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    warp_fwht<8, float>(v);
+}
+
+// Code of one rotated value x = k * v (k a power of two, so x is exact):
+// rint(x / s) with the quotient correctly rounded, as a float (|code| <= 127;
+// no clamp is needed, as |x| <= amax and s = amax / 127 rounded give
+// |x / s| <= 127 (1 + 2^-23) < 127.5).  rk = k / s when that is a normal
+// number, else 0.  v * rk is within a few ulps of x / s (an ulp at most
+// 2^-17 here), so its rounding matches that of the exact quotient unless it
+// lies near a half-integer; only there, or without rk, is the division taken.
+__device__ __forceinline__ float code_of(float v, float k, float rk, float s) {
+    const float t = v * rk;
+    float q = rintf(t);
+    if (rk == 0.0f || fabsf(t - q) > 0.499f) q = s == 0.0f ? 0.0f : rintf(__fdiv_rn(v * k, s));
+    return q;
+}
+
+__device__ __forceinline__ void put_int8(int8_t *dst, int e_per_lane, const float (&q)[8]) {
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        if (e < e_per_lane) w[e >> 2] |= (static_cast<uint32_t>(__float2int_rz(q[e])) & 0xFFu) << (8 * (e & 3));
+    if (e_per_lane == 8) *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+    else if (e_per_lane == 4) *reinterpret_cast<uint32_t *>(dst) = w[0];
+    else if (e_per_lane == 2) *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(w[0]);
+    else *reinterpret_cast<uint8_t *>(dst) = static_cast<uint8_t>(w[0]);
+}
+
+// The codes as fp16 in the tensor core's operand layout: tile (m / 128,
+// k / 64) is the 8192 values at ((m / 128) * KT + k / 64) * 8192; inside it,
+// 8x8 core matrices of 128 contiguous bytes, K-adjacent ones 128 bytes apart,
+// row groups 1024 bytes apart.  A lane's E values (columns k0 .. k0 + E - 1,
+// k0 a multiple of E) are contiguous there.  Where K % 64 == 32 the tail
+// group's lanes also write the zeros that pad the last tile.
+__device__ __forceinline__ void put_tiled(uint16_t *At, int64_t KT, int64_t K, int64_t m, int64_t k0,
+                                          int E, const float (&q)[8]) {
+    const int64_t mt = m >> 7;
+    const int rr = static_cast<int>(m & 127);
+    auto at = [&](int64_t k) {
+        const int kk = static_cast<int>(k & 63);
+        return At + ((mt * KT + (k >> 6)) << 13) + ((((rr >> 3) << 3) + (kk >> 3)) << 6) + ((rr & 7) << 3) +
+               (kk & 7);
+    };
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 p = __floats2half2_rn(q[2 * i], q[2 * i + 1]);   // exact: small integers
+        h[i] = *reinterpret_cast<const uint32_t *>(&p);
+    }
+    uint16_t *dst = at(k0);
+    if (E == 8) {
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
+    } else if (E == 4) {
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(h[0], h[1]);
+    } else if (E == 2) {
+        *reinterpret_cast<uint32_t *>(dst) = h[0];
+    } else {
+        *dst = static_cast<uint16_t>(h[0]);
+        if ((K & 63) == 32) *at(k0 + 32) = 0;
+    }
+}
+
 // Persistent CTAs (8 warps); CTA b takes rows b, b + gridDim.x, ...  Thread 0
 // keeps S rows in flight: row i of this CTA goes to buffer i % S, copied by
 // one bulk copy that completes on that buffer's barrier.  Warp w owns groups
 // w, w + 8, ...; the first GPW stay in registers between the amax pass and
 // the quantise pass, further ones are recomputed from the buffer.
-template <int GPW>
+template <int GPW, bool TILED>
 __global__ void __launch_bounds__(kThreads)
 k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx,
-                    int8_t *__restrict__ Xq, float *__restrict__ sx, int S,
+                    void *__restrict__ out, float *__restrict__ sx, int S,
                     unsigned int *status) {
     extern __shared__ __align__(128) unsigned char ring[];   // [S][2K] then S barriers
     __shared__ float red[kThreads / 32];
     __shared__ int abort_sh;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int W = kThreads / 32;
-    const int64_t G = (K + kGroup - 1) / kGroup;
+    const int64_t Gf = K / kGroup;                        // full 256-groups
+    const int tail = static_cast<int>(K % kGroup);        // 0, 32, 64 or 128
+    const int tail_warp = static_cast<int>(Gf % W);
     const uint32_t row_bytes = static_cast<uint32_t>(K * 2);
     const uint32_t ring0 = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
     const uint32_t bar0 = ring0 + static_cast<uint32_t>(S) * row_bytes;
@@ -169,25 +247,35 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
         const unsigned char *buf = ring + static_cast<size_t>(slot) * row_bytes;
         const int64_t m = blockIdx.x + i * gridDim.x;
 
+        // Pass 1: the full 256-groups unscaled (Hs x; their factor 1/16 is a
+        // power of two, applied exactly later), the tail group scaled.
         float v[GPW][8];
-        int E[GPW];
-        float amax = 0.0f;
+        float amax_full = 0.0f, amax_tail = 0.0f;
 #pragma unroll
         for (int j = 0; j < GPW; ++j) {
             const int64_t g = warp + static_cast<int64_t>(j) * W;
-            E[j] = 0;
+            if (g < Gf) {
+                fwht256_shared(buf + g * kGroup * 2, v[j]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[j][e] = 0.0f;
-            if (g < G) E[j] = rotate_group_shared(buf + g * kGroup * 2, group_width(K, g * kGroup), v[j]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[j][e]));
+                for (int e = 0; e < 8; ++e) amax_full = fmaxf(amax_full, fabsf(v[j][e]));
+            }
         }
-        for (int64_t g = warp + static_cast<int64_t>(GPW) * W; g < G; g += W) {
+        for (int64_t g = warp + static_cast<int64_t>(GPW) * W; g < Gf; g += W) {
             float t[8];
-            rotate_group_shared(buf + g * kGroup * 2, group_width(K, g * kGroup), t);
+            fwht256_shared(buf + g * kGroup * 2, t);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(t[e]));
+            for (int e = 0; e < 8; ++e) amax_full = fmaxf(amax_full, fabsf(t[e]));
         }
+        float vt[8];
+        int Et = 0;
+        if (tail && warp == tail_warp) {
+            Et = rotate_group_shared(buf + Gf * kGroup * 2, tail, vt);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax_tail = fmaxf(amax_tail, fabsf(vt[e]));
+        }
+        // max |c x| over the row: fl(c v) is monotone in |v|, so the largest
+        // scaled value of the full groups is (largest unscaled) / 16 exactly
+        float amax = fmaxf(amax_full * 0.0625f, amax_tail);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if (lane == 0) red[warp] = amax;
@@ -198,17 +286,39 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
 
         const float s = __fdiv_rn(amax, 127.0f);
         const float r = recip_or_zero(s);
+        const float r16 = r * 0.0625f >= FLT_MIN ? r * 0.0625f : 0.0f;   // exact: a power of two
         if (threadIdx.x == 0) sx[m] = s;
-        int8_t *qrow = Xq + m * K;
+        const int64_t KT = (K + 63) >> 6;
+        auto put = [&](int64_t g, int e, const float (&q)[8]) {
+            const int64_t k0 = g * kGroup + static_cast<int64_t>(lane) * e;
+            if constexpr (TILED)
+                put_tiled(static_cast<uint16_t *>(out), KT, K, m, k0, e, q);
+            else
+                put_int8(static_cast<int8_t *>(out) + m * K + k0, e, q);
+        };
+        // Pass 2: codes.  Full groups: x = v / 16.  Tail: x = v.
 #pragma unroll
         for (int j = 0; j < GPW; ++j) {
             const int64_t g = warp + static_cast<int64_t>(j) * W;
-            if (g < G) store_codes(qrow + g * kGroup + static_cast<int64_t>(lane) * E[j], E[j], v[j], s, r);
+            if (g < Gf) {
+                float q[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q[e] = code_of(v[j][e], 0.0625f, r16, s);
+                put(g, 8, q);
+            }
         }
-        for (int64_t g = warp + static_cast<int64_t>(GPW) * W; g < G; g += W) {
-            float t[8];
-            const int e = rotate_group_shared(buf + g * kGroup * 2, group_width(K, g * kGroup), t);
-            store_codes(qrow + g * kGroup + static_cast<int64_t>(lane) * e, e, t, s, r);
+        for (int64_t g = warp + static_cast<int64_t>(GPW) * W; g < Gf; g += W) {
+            float t[8], q[8];
+            fwht256_shared(buf + g * kGroup * 2, t);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[e] = code_of(t[e], 0.0625f, r16, s);
+            put(g, 8, q);
+        }
+        if (Et) {
+            float q[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[e] = code_of(vt[e], 1.0f, r, s);
+            put(Gf, Et, q);
         }
         // This thread's reads of the buffer are ordered before the bulk copy
         // (async proxy) that will refill it; the barrier then makes every
@@ -318,7 +428,58 @@ k_rotate_bf16(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx,
     }
 }
 
+template <bool TILED>
+tq_status launch_ring(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void *out, float *sx,
+                      cudaStream_t s) {
+    const int64_t G = (K + kGroup - 1) / kGroup;
+    const int64_t gpw = (G + 7) / 8;
+    DeviceInfo dev;
+    const tq_status ds = current_device(&dev);
+    if (ds != TQ_OK) return ds;
+    unsigned int *status = status_word();
+    if (!status) return TQ_ERR_DEVICE;
+    // rows in flight per CTA: about 48 KB of them, 2 to 8 rows
+    const int64_t rb = 2 * K;
+    int S = static_cast<int>((48 * 1024) / rb);
+    S = S < 2 ? 2 : (S > 8 ? 8 : S);
+    const size_t smem = static_cast<size_t>(S) * rb + 8 * S;
+    auto kern = gpw <= 1 ? k_rotate_quant_ring<1, TILED>
+              : gpw <= 2 ? k_rotate_quant_ring<2, TILED>
+              : gpw <= 4 ? k_rotate_quant_ring<4, TILED>
+                         : k_rotate_quant_ring<8, TILED>;
+    const int ki = gpw <= 1 ? 0 : gpw <= 2 ? 1 : gpw <= 4 ? 2 : 3;
+    static bool configured[64][4] = {{false}};
+    if (dev.id < 0 || dev.id >= 64) return TQ_ERR_DEVICE;
+    if (!configured[dev.id][ki]) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(kRingMaxK * 2 * 2 + 64));
+        if (e != cudaSuccess) return cuda_fail(e);
+        configured[dev.id][ki] = true;
+    }
+    // persistent: as many CTAs as are resident at once, at most 4 per SM
+    int per_sm = 0;
+    const cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (oe != cudaSuccess) return cuda_fail(oe);
+    per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
+    const int64_t want = static_cast<int64_t>(dev.sms) * per_sm;
+    const unsigned grid = static_cast<unsigned>(M < want ? M : want);
+    kern<<<grid, kThreads, smem, s>>>(X, M, K, ldx, out, sx, S, status);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
 }  // namespace
+
+int64_t tiled_act_bytes(int64_t M, int64_t K) {
+    return ((M + 255) / 256) * 2 * ((K + 63) / 64) * 16384;
+}
+
+tq_status launch_rotate_quant_tiled(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
+                                    void *At, float *sx, cudaStream_t s) {
+    if (M == 0) return TQ_OK;
+    if (K > kRingMaxK) return TQ_ERR_SHAPE;
+    return launch_ring<true>(X, M, K, ldx, At, sx, s);
+}
 
 tq_status launch_rotate_quant_act(const uint16_t *X, int64_t M, int64_t K,
                                   int64_t ldx, int8_t *Xq, float *sx,
@@ -326,42 +487,7 @@ tq_status launch_rotate_quant_act(const uint16_t *X, int64_t M, int64_t K,
     const int64_t G = (K + kGroup - 1) / kGroup;
     const int64_t gpw = (G + 7) / 8;
     if (M == 0) return TQ_OK;
-    DeviceInfo dev;
-    const tq_status ds = current_device(&dev);
-    if (ds != TQ_OK) return ds;
-    if (K <= kRingMaxK) {
-        unsigned int *status = status_word();
-        if (!status) return TQ_ERR_DEVICE;
-        // rows in flight per CTA: about 48 KB of them, 2 to 8 rows; up to 4
-        // CTAs per SM while their buffers fit
-        const int64_t rb = 2 * K;
-        int S = static_cast<int>((48 * 1024) / rb);
-        S = S < 2 ? 2 : (S > 8 ? 8 : S);
-        const size_t smem = static_cast<size_t>(S) * rb + 8 * S;
-        auto kern = gpw <= 1 ? k_rotate_quant_ring<1>
-                  : gpw <= 2 ? k_rotate_quant_ring<2>
-                  : gpw <= 4 ? k_rotate_quant_ring<4>
-                             : k_rotate_quant_ring<8>;
-        const int ki = gpw <= 1 ? 0 : gpw <= 2 ? 1 : gpw <= 4 ? 2 : 3;
-        static bool configured[64][4] = {{false}};
-        if (dev.id < 0 || dev.id >= 64) return TQ_ERR_DEVICE;
-        if (!configured[dev.id][ki]) {
-            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       static_cast<int>(kRingMaxK * 2 * 2 + 64));
-            if (e != cudaSuccess) return cuda_fail(e);
-            configured[dev.id][ki] = true;
-        }
-        // persistent: as many CTAs as are resident at once, at most 4 per SM
-        int per_sm = 0;
-        const cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
-        if (oe != cudaSuccess) return cuda_fail(oe);
-        per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
-        const int64_t want = static_cast<int64_t>(dev.sms) * per_sm;
-        const unsigned grid = static_cast<unsigned>(M < want ? M : want);
-        kern<<<grid, kThreads, smem, s>>>(X, M, K, ldx, Xq, sx, S, status);
-        const cudaError_t e = cudaGetLastError();
-        return e == cudaSuccess ? TQ_OK : cuda_fail(e);
-    }
+    if (K <= kRingMaxK) return launch_ring<false>(X, M, K, ldx, Xq, sx, s);
     const unsigned grid = static_cast<unsigned>(M < (1ll << 30) ? M : (1ll << 30));
     if (gpw <= 1) k_rotate_quant_act<1><<<grid, kThreads, 0, s>>>(X, M, K, ldx, Xq, sx);
     else if (gpw <= 2) k_rotate_quant_act<2><<<grid, kThreads, 0, s>>>(X, M, K, ldx, Xq, sx);

@@ -2,9 +2,9 @@
 //   acc[m][n] = sum_k Xq[m][k] * Wq[n][k]  (exact int32),
 //   Y[m][n]   = (sx[m] * sw[n]) * acc[m][n].
 // The DiT projections at large M are compute-bound (kvad-gpu internals,
-// "Quantised weights on the GPU": past the crossover every matmul is real
-// work); they are about 80% of a denoising step (TensorFold PR #948, "What
-// comes next").
+// "Quantised weights on the GPU": beyond a prompt length of roughly a thousand
+// tokens the arithmetic, not the weight stream, sets the time); they are about
+// 80% of a denoising step (TensorFold PR #948, "What comes next").
 //
 // sm_103a has no integer tcgen05 MMA, so the codes are widened to fp16 (every
 // int8 and int4 code is exact in fp16; every product, at most 127*127, is
@@ -43,8 +43,7 @@ namespace tq {
 namespace {
 
 constexpr int HM = 128, BN = 256, HN = BN / 2, BK = 64;
-constexpr int OSTAGES = 4, RSTAGES = 4;
-constexpr int NCONV = 8, MMA_WARP = 8, TMA_WARP = 13, NWARPS = 14;
+constexpr int NCONV = 8, MMA_WARP = 8, TMA_WARP = 13, A_WARP = 14;
 // The converter warps form CONV_GROUPS groups; group g converts the K steps
 // it with it % CONV_GROUPS == g, so the fence-and-arrive latency at the end of
 // one group's step overlaps the other groups' conversions.
@@ -57,14 +56,26 @@ constexpr int TPG = 32 * WPG;                  // threads per group
 // Each use of a ring slot is converted by one group, so a slot's barriers
 // count one group's warps whatever the ring depths are.
 static_assert(NCONV % CONV_GROUPS == 0, "groups of whole warps");
-constexpr int THREADS = NWARPS * 32;
 constexpr int A_OP = HM * BK * 2;      // 16 KB fp16: this CTA's 128 rows of A
 constexpr int B_OP = HN * BK * 2;      // 16 KB fp16: this CTA's 128 rows of B
 constexpr int A_RAW = HM * BK;         // 8 KB int8 codes
 constexpr int B_RAW = HN * BK;         // 8 KB int8 codes (int4: half used)
-constexpr int OP_BYTES = OSTAGES * (A_OP + B_OP);
-constexpr int RAW_BYTES = RSTAGES * (A_RAW + B_RAW);
-constexpr int SMEM_BYTES = OP_BYTES + RAW_BYTES + 1024;
+// Shared-memory plan of the two operand sources.  With raw A (AT false) the
+// TMA brings int8 codes of both operands and the converters widen both; with
+// pre-tiled A (AT true) the activations arrive as fp16 codes already in the
+// tensor core's layout, one 16 KB bulk copy per K step straight into the
+// operand ring (loaded by warp 14), and only B is widened.
+template <bool AT>
+struct Plan {
+    static constexpr int O = AT ? 5 : 4;            // operand ring depth
+    static constexpr int R = AT ? 6 : 4;            // raw ring depth
+    static constexpr int NWARPS = AT ? 15 : 14;
+    static constexpr int THREADS = NWARPS * 32;
+    static constexpr int RAW_A = AT ? 0 : A_RAW;    // raw A bytes per slot
+    static constexpr int OP_BYTES = O * (A_OP + B_OP);
+    static constexpr int RAW_BYTES = R * (RAW_A + B_RAW);
+    static constexpr int SMEM_BYTES = OP_BYTES + RAW_BYTES + 1024;
+};
 constexpr uint32_t TMEM_COLS = 512;    // acc [0, 256) + running int32 sum [256, 512)
 constexpr uint32_t RUN_COL = 256;
 constexpr long long kWaitLimit = 4000000000ll;  // clock cycles, about 2 s
@@ -82,6 +93,7 @@ struct TcParams {
     int ytype;            // 0 fp32, 1 bf16, 2 int32
     int mtiles, ntiles, ksteps, chunk_steps;
     unsigned int *status;
+    const unsigned char *At;   // pre-tiled fp16 A codes (AT path), else null
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -269,18 +281,20 @@ __device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-template <int BITS>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+template <int BITS, bool AT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Plan<AT>::THREADS, 1)
 k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const TcParams p) {
+    using P = Plan<AT>;
+    constexpr int OSTAGES = P::O, RSTAGES = P::R;
     extern __shared__ __align__(1024) unsigned char smem[];
-    unsigned char *opA = smem;                                   // [OSTAGES][A_OP]
-    unsigned char *opB = smem + OSTAGES * A_OP;                  // [OSTAGES][B_OP]
-    unsigned char *rawA = smem + OP_BYTES;                       // [RSTAGES][A_RAW]
-    unsigned char *rawB = smem + OP_BYTES + RSTAGES * A_RAW;     // [RSTAGES][B_RAW]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OP_BYTES + RAW_BYTES);
+    unsigned char *opA = smem;                                       // [O][A_OP]
+    unsigned char *opB = smem + OSTAGES * A_OP;                      // [O][B_OP]
+    unsigned char *rawA = smem + P::OP_BYTES;                        // [R][RAW_A]
+    unsigned char *rawB = smem + P::OP_BYTES + RSTAGES * P::RAW_A;   // [R][B_RAW]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::OP_BYTES + P::RAW_BYTES);
     // bars: raw_full[R], raw_empty[R], op_full[O] (used in CTA 0), op_empty[O],
-    //       acc_full, acc_empty (CTA 0), done
+    //       acc_full, acc_empty (CTA 0), done, a_full[O] (AT)
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
 
@@ -292,6 +306,7 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     const uint32_t op_empty0 = smem_u32(bars + 2 * RSTAGES + OSTAGES);
     const uint32_t acc_full = smem_u32(bars + 2 * RSTAGES + 2 * OSTAGES);
     const uint32_t acc_empty = acc_full + 8, done = acc_full + 16;
+    const uint32_t a_full0 = acc_full + 24;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < RSTAGES; ++s) {
@@ -305,6 +320,10 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(acc_full));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(acc_empty));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done));
+        if constexpr (AT) {
+            for (int s = 0; s < OSTAGES; ++s)
+                asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(a_full0 + 8 * s));
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         abort_sh = 0;
     }
@@ -333,9 +352,33 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                     const int s = it % RSTAGES;
                     if (!mbar_wait(raw_empty0 + 8 * s, ((it / RSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
                     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                                 ::"r"(raw_full0 + 8 * s), "r"(static_cast<uint32_t>(A_RAW + BRAW)) : "memory");
-                    tma_load_2d(smem_u32(rawA + s * A_RAW), &tmA, ks * BK, m0, raw_full0 + 8 * s);
+                                 ::"r"(raw_full0 + 8 * s), "r"(static_cast<uint32_t>(P::RAW_A + BRAW)) : "memory");
+                    if constexpr (!AT) tma_load_2d(smem_u32(rawA + s * A_RAW), &tmA, ks * BK, m0, raw_full0 + 8 * s);
                     tma_load_2d(smem_u32(rawB + s * B_RAW), &tmB, ks * BK * BITS / 8, n0, raw_full0 + 8 * s);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (AT && warp == A_WARP) {
+        // ------------------------------------------------ A loader (pre-tiled fp16 codes)
+        // Tile (mt, ks) of the activations is 16 KB contiguous, already in the
+        // operand layout: one bulk copy into the stage once the MMA is done
+        // with the stage's previous use.
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
+                const int64_t mt = static_cast<int64_t>(tile % p.mtiles) * 2 + rank;
+                for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
+                    const int s = it % OSTAGES;
+                    if (!mbar_wait(op_empty0 + 8 * s, ((it / OSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
+                    const unsigned char *src = p.At + (mt * p.ksteps + ks) * static_cast<int64_t>(A_OP);
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                                 ::"r"(a_full0 + 8 * s), "r"(static_cast<uint32_t>(A_OP)) : "memory");
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                        ::"r"(smem_u32(opA + s * A_OP)), "l"(src), "r"(static_cast<uint32_t>(A_OP)),
+                          "r"(a_full0 + 8 * s)
+                        : "memory");
                 }
             }
         }
@@ -356,7 +399,7 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 const unsigned char *rb = rawB + rs * B_RAW;
                 unsigned char *oa = opA + os * A_OP;
                 unsigned char *ob = opB + os * B_OP;
-                {
+                if constexpr (!AT) {
                     uint4 a[NA];
 #pragma unroll
                     for (int j = 0; j < NA; ++j) {
@@ -405,8 +448,15 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive_leader(op_full0 + 8 * os);
-                    mbar_arrive_local(raw_empty0 + 8 * rs);
+                    // with pre-tiled A, the stage is complete once its bulk copy
+                    // has landed too (this CTA's half; the even CTA's MMA cannot
+                    // wait on the odd CTA's barrier, so the converters pass it on)
+                    bool ok = true;
+                    if constexpr (AT) ok = mbar_wait(a_full0 + 8 * os, (it / OSTAGES) & 1, &abort_sh, p.status);
+                    if (ok) {
+                        mbar_arrive_leader(op_full0 + 8 * os);
+                        mbar_arrive_local(raw_empty0 + 8 * rs);
+                    }
                 }
             }
         }
@@ -589,20 +639,25 @@ bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M, int64_t K,
-                         const uint8_t *Wq, const float *sw, int64_t N, int bits,
-                         void *Y, int ytype, int64_t ldy, const DeviceInfo &dev,
-                         cudaStream_t s) {
+// Shared launch of both operand paths: Xq int8 codes (AT false, A through a
+// tensor map) or At pre-tiled fp16 codes (AT true).
+template <bool AT>
+tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const float *sx, int64_t M, int64_t K,
+                    const uint8_t *Wq, const float *sw, int64_t N, int bits, void *Y, int ytype,
+                    int64_t ldy, const DeviceInfo &dev, cudaStream_t s) {
+    using P = Plan<AT>;
     unsigned int *status = status_word();
     if (!status) return TQ_ERR_DEVICE;
     if (M > (1ll << 31) - 1 || N > (1ll << 31) - 1) return TQ_ERR_OVERFLOW;
     CUtensorMap tmA, tmB;
-    if (!make_map(&tmA, Xq, M, K, BK, CU_TENSOR_MAP_SWIZZLE_64B)) return TQ_ERR_DEVICE;
     const bool mapped = bits == 8 ? make_map(&tmB, Wq, N, K, BK, CU_TENSOR_MAP_SWIZZLE_64B)
                                   : make_map(&tmB, Wq, N, K / 2, BK / 2, CU_TENSOR_MAP_SWIZZLE_32B);
     if (!mapped) return TQ_ERR_DEVICE;
+    if constexpr (AT) {
+        tmA = tmB;   // not read on this path
+    } else {
+        if (!make_map(&tmA, Xq, M, K, BK, CU_TENSOR_MAP_SWIZZLE_64B)) return TQ_ERR_DEVICE;
+    }
     TcParams p{};
     p.sx = sx;
     p.M = M;
@@ -618,20 +673,40 @@ tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M, int64_t K
     // K per exact fp32 chunk: 1024 * 127^2 < 2^24 (int8), 16384 * 127 * 7 < 2^24 (int4)
     p.chunk_steps = bits == 8 ? 1024 / BK : 16384 / BK;
     p.status = status;
+    p.At = At;
     const int64_t tiles = static_cast<int64_t>(p.mtiles) * p.ntiles;
     if (tiles > (1ll << 30)) return TQ_ERR_OVERFLOW;
-    auto kern = bits == 8 ? k_gemm_a8_tc<8> : k_gemm_a8_tc<4>;
-    static int configured_for[64][2] = {{0}};
+    auto kern = bits == 8 ? k_gemm_a8_tc<8, AT> : k_gemm_a8_tc<4, AT>;
+    static bool configured_for[64][2] = {{false}};
     const int bi = bits == 8 ? 0 : 1;
-    if (dev.id >= 0 && dev.id < 64 && !configured_for[dev.id][bi]) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (dev.id < 0 || dev.id >= 64) return TQ_ERR_DEVICE;
+    if (!configured_for[dev.id][bi]) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   P::SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e);
-        configured_for[dev.id][bi] = 1;
+        configured_for[dev.id][bi] = true;
     }
     const int64_t pairs = tiles < dev.sms / 2 ? tiles : dev.sms / 2;
-    kern<<<static_cast<unsigned>(2 * pairs), THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
+    kern<<<static_cast<unsigned>(2 * pairs), P::THREADS, P::SMEM_BYTES, s>>>(tmA, tmB, p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M, int64_t K,
+                         const uint8_t *Wq, const float *sw, int64_t N, int bits,
+                         void *Y, int ytype, int64_t ldy, const DeviceInfo &dev,
+                         cudaStream_t s) {
+    return launch_tc<false>(Xq, nullptr, sx, M, K, Wq, sw, N, bits, Y, ytype, ldy, dev, s);
+}
+
+tq_status launch_gemm_a8_tiled(const void *At, const float *sx, int64_t M, int64_t K,
+                               const uint8_t *Wq, const float *sw, int64_t N, int bits,
+                               void *Y, int ytype, int64_t ldy, const DeviceInfo &dev,
+                               cudaStream_t s) {
+    return launch_tc<true>(nullptr, static_cast<const unsigned char *>(At), sx, M, K, Wq, sw, N,
+                           bits, Y, ytype, ldy, dev, s);
 }
 
 }  // namespace tq

@@ -1,8 +1,9 @@
 // C-ABI entry points of libtq: host-side validation, then dispatch to the
-// kernels.  Every check runs before any launch, and a refusal names its reason
-// (the pages' practice of refusing bad sizes "up front instead of failing
-// halfway": kvad-gpu internals, "Quantised weights on the GPU"; and of checking
-// every size product for overflow: TensorFold PR #948, review follow-up).
+// kernels.  Every check runs before any launch, and a refusal names its reason.
+// The pages do the same: a format the sizes do not allow is rejected with a
+// message before any work starts (kvad-gpu internals, "Quantised weights on
+// the GPU"), and size products are checked for overflow (TensorFold PR #948,
+// review follow-up).
 
 #include <limits.h>
 
@@ -171,15 +172,23 @@ tq_status tq_rotate_act_bf16(const void *X, int64_t M, int64_t K, int64_t ldx,
                               static_cast<uint16_t *>(Xr), stream);
 }
 
+size_t tq_act_tiled_bytes(int64_t M, int64_t K) {
+    if (M <= 0 || !valid_k(K) || K > TQ_MAX_K_TILED) return 0;
+    if (!mul_ok(M + 256, K + 64, INT64_MAX / 8)) return 0;
+    return static_cast<size_t>(tiled_act_bytes(M, K));
+}
+
 size_t tq_linear_workspace_bytes(int64_t M, int64_t K, int64_t N, int bits, tq_mode mode) {
     (void)N;
     (void)bits;
     if (mode != TQ_W8A8 || M <= 0 || K <= 0) return 0;
     if (!mul_ok(M, K)) return 0;
-    // int8 codes [M, K] then fp32 token scales [M], each 256-byte aligned
-    const size_t codes = (static_cast<size_t>(M) * K + 255) / 256 * 256;
     const size_t scales = (static_cast<size_t>(M) * 4 + 255) / 256 * 256;
-    return codes + scales;
+    // K <= TQ_MAX_K_TILED: tiled fp16 codes, then fp32 token scales;
+    // longer rows: int8 codes [M, K], then the scales; each 256-byte aligned
+    const size_t tiled = tq_act_tiled_bytes(M, K);
+    if (tiled > 0) return tiled + scales;
+    return (static_cast<size_t>(M) * K + 255) / 256 * 256 + scales;
 }
 
 tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
@@ -212,6 +221,14 @@ tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
                                static_cast<const uint8_t *>(Wq), sw, N, bits, Y,
                                ytype == TQ_OUT_BF16 ? 1 : 0, ldy, dev, stream);
     }
+    const size_t tiled = tq_act_tiled_bytes(M, K);
+    if (tiled > 0) {
+        float *sx = reinterpret_cast<float *>(static_cast<char *>(workspace) + tiled);
+        st = launch_rotate_quant_tiled(static_cast<const uint16_t *>(X), M, K, ldx, workspace, sx, stream);
+        if (st != TQ_OK) return st;
+        return launch_gemm_a8_tiled(workspace, sx, M, K, static_cast<const uint8_t *>(Wq), sw, N, bits,
+                                    Y, ytype == TQ_OUT_BF16 ? 1 : 0, ldy, dev, stream);
+    }
     int8_t *Xq = static_cast<int8_t *>(workspace);
     float *sx = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                           (static_cast<size_t>(M) * K + 255) / 256 * 256);
@@ -238,6 +255,41 @@ tq_status tq_linear_q8(const int8_t *Xq, const float *sx, int64_t M, int64_t K,
     if ((st = current_device(&dev)) != TQ_OK) return st;
     return launch_gemm_a8(Xq, sx, M, K, static_cast<const uint8_t *>(Wq), sw, N, bits, Y,
                           static_cast<int>(ytype), ldy, dev, stream);
+}
+
+tq_status tq_rotate_quant_act_tiled(const void *X, int64_t M, int64_t K, int64_t ldx, void *At,
+                                    size_t at_bytes, float *sx, cudaStream_t stream) {
+    if (M < 0 || !valid_k(K) || K > TQ_MAX_K_TILED) return TQ_ERR_SHAPE;
+    if (M == 0) return TQ_OK;
+    tq_status st = check_bf16_rows(X, M, K, ldx);
+    if (st != TQ_OK) return st;
+    if (!At || !sx) return TQ_ERR_NULL;
+    const size_t need = tq_act_tiled_bytes(M, K);
+    if (need == 0) return TQ_ERR_OVERFLOW;
+    if (at_bytes < need) return TQ_ERR_WORKSPACE;
+    if (!aligned(At, 256) || !aligned(sx, 4)) return TQ_ERR_ALIGN;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    return launch_rotate_quant_tiled(static_cast<const uint16_t *>(X), M, K, ldx, At, sx, stream);
+}
+
+tq_status tq_linear_tiled(const void *At, const float *sx, int64_t M, int64_t K, const void *Wq,
+                          const float *sw, int64_t N, int bits, void *Y, tq_out ytype, int64_t ldy,
+                          cudaStream_t stream) {
+    if (ytype != TQ_OUT_F32 && ytype != TQ_OUT_BF16 && ytype != TQ_OUT_I32) return TQ_ERR_MODE;
+    if (bits != 8 && bits != 4) return TQ_ERR_BITS;
+    if (M < 0 || N < 0 || !valid_k(K) || K > TQ_MAX_K_TILED) return TQ_ERR_SHAPE;
+    if (M == 0 || N == 0) return TQ_OK;
+    if (!At || (ytype != TQ_OUT_I32 && !sx)) return TQ_ERR_NULL;
+    if (tq_act_tiled_bytes(M, K) == 0) return TQ_ERR_OVERFLOW;
+    if (!aligned(At, 256) || (sx && !aligned(sx, 4))) return TQ_ERR_ALIGN;
+    tq_status st = check_weights(Wq, sw, N, K, bits);
+    if (st != TQ_OK) return st;
+    if ((st = check_output(Y, M, N, ldy, out_size(ytype))) != TQ_OK) return st;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    return launch_gemm_a8_tiled(At, sx, M, K, static_cast<const uint8_t *>(Wq), sw, N, bits, Y,
+                                static_cast<int>(ytype), ldy, dev, stream);
 }
 
 tq_status tq_device_status(cudaStream_t stream) {

@@ -60,6 +60,20 @@ tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M,
                          int64_t N, int bits, void *Y, int ytype, int64_t ldy,
                          const DeviceInfo &dev, cudaStream_t s);
 
+// The activation codes as fp16 in the tensor core's operand layout ("tiled"):
+// 128-row x 64-column tiles, tile (mt, kt) the 16 KB at byte
+// (mt * ceil(K/64) + kt) * 16384, inside a tile the K-major 8x8 core-matrix
+// order (core matrix (r/8, k/8) is 128 contiguous bytes, K-adjacent ones 128
+// bytes apart, row groups 1024 bytes apart).  Rows are padded to a whole
+// number of 256-row tile pairs; columns past K inside the last tile are zero.
+int64_t tiled_act_bytes(int64_t M, int64_t K);
+tq_status launch_rotate_quant_tiled(const uint16_t *X, int64_t M, int64_t K,
+                                    int64_t ldx, void *At, float *sx, cudaStream_t s);
+tq_status launch_gemm_a8_tiled(const void *At, const float *sx, int64_t M, int64_t K,
+                               const uint8_t *Wq, const float *sw, int64_t N, int bits,
+                               void *Y, int ytype, int64_t ldy, const DeviceInfo &dev,
+                               cudaStream_t s);
+
 // ---------------------------------------------------------------- device side
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {

@@ -37,6 +37,9 @@ SIGNATURES = {
     "tq_linear_q8": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
     "tq_device_status": (_C, [_P]),
     "tq_linear_a8_static": (_C, [_P, _I, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
+    "tq_act_tiled_bytes": (_Z, [_I, _I]),
+    "tq_rotate_quant_act_tiled": (_C, [_P, _I, _I, _I, _P, _Z, _P, _P]),
+    "tq_linear_tiled": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
 }
 
 _lib = None
@@ -88,6 +91,43 @@ def _check(rc: int, where: str):
         raise TQError(rc, where)
 
 
+# ---- host-side checks of what the C ABI cannot see: tensor sizes and types.
+# A call with a buffer smaller than its sizes say would write or read past it
+# on the device, so the binding refuses it before the call.
+
+def _dt(name):
+    import torch
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "i32": torch.int32,
+            "i8": torch.int8, "u8": torch.uint8}[name]
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _req(t, what: str, dtype=None, rows: int = None, cols: int = None, nbytes: int = None,
+         dense: bool = False):
+    if t is None:
+        raise ValueError(f"{what} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{what} is {t.dtype}, expected {dtype}")
+    if rows is not None:
+        if t.dim() != 2 or t.shape[0] < rows or t.shape[1] < cols or (t.numel() and t.stride(1) != 1):
+            raise ValueError(f"{what} must be a row-major [>= {rows}, >= {cols}] matrix, got "
+                             f"shape {tuple(t.shape)} strides {t.stride()}")
+        if dense and t.numel() and t.stride(0) != cols:
+            raise ValueError(f"{what} must be dense (row stride {cols})")
+    if nbytes is not None and _nbytes(t) < nbytes:
+        raise ValueError(f"{what} holds {_nbytes(t)} bytes, needs {nbytes}")
+
+
+def _weights(Wq, sw, N: int, K: int, bits: int):
+    _req(Wq, "Wq", nbytes=N * K * bits // 8)
+    _req(sw, "sw", dtype=_dt("f32"), nbytes=4 * N)
+
+
 def status_str(s: int) -> str:
     return lib().tq_status_str(s).decode()
 
@@ -105,6 +145,9 @@ def quantize_weights(W, bits: int, codes=None, scales=None, stream=None):
                             dtype=torch.int8 if bits == 8 else torch.uint8, device=W.device)
     if scales is None:
         scales = torch.empty(N, dtype=torch.float32, device=W.device)
+    _req(W, "W", dtype=torch.bfloat16, rows=N, cols=K)
+    _req(codes, "codes", nbytes=N * K * bits // 8)
+    _req(scales, "scales", dtype=torch.float32, nbytes=4 * N)
     _check(lib().tq_quantize_weights(_ptr(W), N, K, W.stride(0), bits, 256, _ptr(codes),
                                      _ptr(scales), _stream(stream)), "tq_quantize_weights")
     return codes, scales
@@ -117,6 +160,9 @@ def rotate_quant_act(X, Xq=None, sx=None, stream=None):
         Xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
     if sx is None:
         sx = torch.empty(M, dtype=torch.float32, device=X.device)
+    _req(X, "X", dtype=torch.bfloat16, rows=M, cols=K)
+    _req(Xq, "Xq", dtype=torch.int8, rows=M, cols=K, dense=True)
+    _req(sx, "sx", dtype=torch.float32, nbytes=4 * M)
     _check(lib().tq_rotate_quant_act(_ptr(X), M, K, X.stride(0), _ptr(Xq), _ptr(sx),
                                      _stream(stream)), "tq_rotate_quant_act")
     return Xq, sx
@@ -127,6 +173,8 @@ def rotate_act_bf16(X, Xr=None, stream=None):
     M, K = X.shape
     if Xr is None:
         Xr = torch.empty((M, K), dtype=torch.bfloat16, device=X.device)
+    _req(X, "X", dtype=torch.bfloat16, rows=M, cols=K)
+    _req(Xr, "Xr", dtype=torch.bfloat16, rows=M, cols=K, dense=True)
     _check(lib().tq_rotate_act_bf16(_ptr(X), M, K, X.stride(0), _ptr(Xr), _stream(stream)),
            "tq_rotate_act_bf16")
     return Xr
@@ -141,9 +189,13 @@ def linear(X, Wq, sw, N: int, bits: int, mode: str, Y=None, out: str = "f32",
     """Y [M, N] = the rotated low-bit product of bf16 X [M, K] with (Wq, sw)."""
     import torch
     M, K = X.shape
+    if out not in ("f32", "bf16"):
+        raise ValueError("tq_linear writes f32 or bf16")
     if Y is None:
-        Y = torch.empty((M, N), dtype=torch.float32 if out == "f32" else torch.bfloat16,
-                        device=X.device)
+        Y = torch.empty((M, N), dtype=_dt(out), device=X.device)
+    _req(X, "X", dtype=torch.bfloat16, rows=M, cols=K)
+    _weights(Wq, sw, N, K, bits)
+    _req(Y, "Y", dtype=_dt(out), rows=M, cols=N)
     need = linear_workspace_bytes(M, K, N, bits, mode)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
@@ -158,10 +210,51 @@ def linear_q8(Xq, sx, Wq, sw, N: int, bits: int, Y=None, out: str = "f32", strea
     import torch
     M, K = Xq.shape
     if Y is None:
-        dt = {"f32": torch.float32, "bf16": torch.bfloat16, "i32": torch.int32}[out]
-        Y = torch.empty((M, N), dtype=dt, device=Xq.device)
+        Y = torch.empty((M, N), dtype=_dt(out), device=Xq.device)
+    _req(Xq, "Xq", dtype=torch.int8, rows=M, cols=K, dense=True)
+    if out != "i32":
+        _req(sx, "sx", dtype=torch.float32, nbytes=4 * M)
+    _weights(Wq, sw, N, K, bits)
+    _req(Y, "Y", dtype=_dt(out), rows=M, cols=N)
     _check(lib().tq_linear_q8(_ptr(Xq), _ptr(sx), M, K, _ptr(Wq), _ptr(sw), N, bits, _ptr(Y),
                               OUT[out], Y.stride(0), _stream(stream)), "tq_linear_q8")
+    return Y
+
+
+def act_tiled_bytes(M: int, K: int) -> int:
+    return int(lib().tq_act_tiled_bytes(M, K))
+
+
+def rotate_quant_act_tiled(X, At=None, sx=None, stream=None):
+    """Rotation + per-token int8 quantisation written in the A8 product's own
+    operand form (fp16 codes, tiled); returns (At, sx) for linear_tiled."""
+    import torch
+    M, K = X.shape
+    need = act_tiled_bytes(M, K)
+    if At is None:
+        At = torch.empty(max(need, 1), dtype=torch.uint8, device=X.device)
+    if sx is None:
+        sx = torch.empty(M, dtype=torch.float32, device=X.device)
+    _req(X, "X", dtype=torch.bfloat16, rows=M, cols=K)
+    _req(At, "At", nbytes=need)
+    _req(sx, "sx", dtype=torch.float32, nbytes=4 * M)
+    _check(lib().tq_rotate_quant_act_tiled(_ptr(X), M, K, X.stride(0), _ptr(At), _nbytes(At),
+                                           _ptr(sx), _stream(stream)), "tq_rotate_quant_act_tiled")
+    return At, sx
+
+
+def linear_tiled(At, sx, M: int, K: int, Wq, sw, N: int, bits: int, Y=None, out: str = "f32",
+                 stream=None):
+    import torch
+    if Y is None:
+        Y = torch.empty((M, N), dtype=_dt(out), device=At.device)
+    _req(At, "At", nbytes=act_tiled_bytes(M, K))
+    if out != "i32":
+        _req(sx, "sx", dtype=torch.float32, nbytes=4 * M)
+    _weights(Wq, sw, N, K, bits)
+    _req(Y, "Y", dtype=_dt(out), rows=M, cols=N)
+    _check(lib().tq_linear_tiled(_ptr(At), _ptr(sx), M, K, _ptr(Wq), _ptr(sw), N, bits, _ptr(Y),
+                                 OUT[out], Y.stride(0), _stream(stream)), "tq_linear_tiled")
     return Y
 
 
@@ -169,7 +262,13 @@ def linear_a8_static(X, Wq, sw, N: int, bits: int, Y, out: str = "f32", stream=N
     """The W8A8 / W4A8 product using the library's fixed device scratch
     instead of a workspace (for callers that may not allocate device memory).
     ``Y`` must be given; nothing is allocated."""
+    import torch
     M, K = X.shape
+    if out not in ("f32", "bf16"):
+        raise ValueError("tq_linear_a8_static writes f32 or bf16")
+    _req(X, "X", dtype=torch.bfloat16, rows=M, cols=K)
+    _weights(Wq, sw, N, K, bits)
+    _req(Y, "Y", dtype=_dt(out), rows=M, cols=N)
     _check(lib().tq_linear_a8_static(_ptr(X), M, K, X.stride(0), _ptr(Wq), _ptr(sw), N, bits,
                                      _ptr(Y), OUT[out], Y.stride(0), _stream(stream)),
            "tq_linear_a8_static")

@@ -73,7 +73,7 @@ typedef enum {
 typedef enum {
     TQ_OUT_F32 = 0,
     TQ_OUT_BF16 = 1,
-    TQ_OUT_I32 = 2  /* tq_linear_q8 only: the raw int32 code products */
+    TQ_OUT_I32 = 2  /* tq_linear_q8 and tq_linear_tiled only: the raw int32 sums */
 } tq_out;
 
 /* Largest K any entry point accepts. */
@@ -174,6 +174,39 @@ tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
 tq_status tq_linear_q8(const int8_t *Xq, const float *sx, int64_t M, int64_t K,
                        const void *Wq, const float *sw, int64_t N, int bits,
                        void *Y, tq_out ytype, int64_t ldy, cudaStream_t stream);
+
+/* Longest row (K) the tiled activation operand takes. */
+#define TQ_MAX_K_TILED 16384
+
+/*
+ * Bytes of the tiled activation operand of an M x K input: 0 when K is not a
+ * valid row length or is above TQ_MAX_K_TILED.
+ */
+size_t tq_act_tiled_bytes(int64_t M, int64_t K);
+
+/*
+ * tq_rotate_quant_act writing its codes in the A8 product's own operand form
+ * ("tiled"): the same codes and token scales (same passages), stored as fp16
+ * in 128-row x 64-column tiles laid out as the tensor cores read them, so the
+ * product loads each tile with one copy.  A caller that multiplies one input
+ * by several weight matrices (the query/key/value or gate/up projections of a
+ * DiT block) rotates and quantises it once.
+ *   X        as tq_rotate_quant_act; K <= TQ_MAX_K_TILED.
+ *   At       at least tq_act_tiled_bytes(M, K) bytes, 256-byte aligned; its
+ *            layout is private to this library (read it only through
+ *            tq_linear_tiled).
+ *   sx       fp32 [M]: the token scales.
+ */
+tq_status tq_rotate_quant_act_tiled(const void *X, int64_t M, int64_t K, int64_t ldx, void *At,
+                                    size_t at_bytes, float *sx, cudaStream_t stream);
+
+/*
+ * The A8 product on a tiled operand: as tq_linear_q8 with At, sx from
+ * tq_rotate_quant_act_tiled (same M and K) in place of Xq, sx.
+ */
+tq_status tq_linear_tiled(const void *At, const float *sx, int64_t M, int64_t K, const void *Wq,
+                          const float *sw, int64_t N, int bits, void *Y, tq_out ytype, int64_t ldy,
+                          cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the library's device status

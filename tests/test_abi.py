@@ -119,6 +119,23 @@ def test_linear_q8_refusals(L):
     assert f(FAKE + 1, FAKE, 4, 512, FAKE, FAKE, 256, 8, FAKE, 0, 256, S0) == ALIGN
 
 
+def test_tiled_refusals(L):
+    assert L.tq_act_tiled_bytes(4, 16384 + 256) == 0          # above TQ_MAX_K_TILED
+    assert L.tq_act_tiled_bytes(4, 500) == 0
+    need = L.tq_act_tiled_bytes(300, 3072)
+    assert need == 4 * 48 * 16384        # rows padded to two 256-row tile pairs, 48 K steps
+    r = L.tq_rotate_quant_act_tiled
+    assert r(FAKE, 4, 16384 + 256, 16384 + 256, FAKE, 1 << 30, FAKE, S0) == SHAPE
+    assert r(FAKE, 4, 512, 512, 0, 1 << 20, FAKE, S0) == NULL
+    assert r(FAKE, 4, 512, 512, FAKE, 100, FAKE, S0) == WORKSPACE
+    assert r(FAKE, 4, 512, 512, FAKE + 16, 1 << 20, FAKE, S0) == ALIGN
+    f = L.tq_linear_tiled
+    assert f(FAKE, FAKE, 4, 512, FAKE, FAKE, 256, 8, FAKE, 5, 256, S0) == MODE
+    assert f(0, FAKE, 4, 512, FAKE, FAKE, 256, 8, FAKE, 0, 256, S0) == NULL
+    assert f(FAKE, FAKE, 4, 16384 + 256, FAKE, FAKE, 256, 8, FAKE, 0, 256, S0) == SHAPE
+    assert f(FAKE + 16, FAKE, 4, 512, FAKE, FAKE, 256, 8, FAKE, 0, 256, S0) == ALIGN
+
+
 def test_rotate_refusals(L):
     assert L.tq_rotate_quant_act(FAKE, 4, 96, 96, FAKE, FAKE, S0) == SHAPE
     assert L.tq_rotate_quant_act(FAKE, 4, 512, 512, 0, FAKE, S0) == NULL

@@ -223,6 +223,27 @@ def test_a8_product(tq, M, N, K, bits):
     assert np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
 
 
+@pytest.mark.parametrize("M,N,K,bits", [(300, 129, 3072, 8), (257, 300, 4096 + 32, 4), (1, 64, 288, 8),
+                                          (600, 512, 12288, 8)])
+def test_tiled_operand_matches_int8_path(tq, M, N, K, bits):
+    """The tiled activation operand carries the same codes and scales as
+    tq_rotate_quant_act and gives the same exact int32 sums.  The buffer is
+    filled with 0xFF first (fp16 NaN) so that padding it fails to zero, or a
+    pad row leaking into real rows, would show."""
+    import torch
+    X = to_dev_bf16(xgen(f"gpu/tiled/x{M}x{K}", M, K, XD))
+    codes, sw = gpu_weights(tq, wgen(f"gpu/tiled/w{N}x{K}", N, K, WD if bits == 8 else WB), bits)
+    At = torch.full((tq.act_tiled_bytes(M, K),), 0xFF, dtype=torch.uint8, device="cuda")
+    At, sxt = tq.rotate_quant_act_tiled(X, At=At)
+    Xq, sx = tq.rotate_quant_act(X)
+    assert np.array_equal(to_np(sxt).view(np.uint32), to_np(sx).view(np.uint32))
+    acc_t = to_np(tq.linear_tiled(At, sxt, M, K, codes, sw, N, bits, out="i32"))
+    acc = to_np(tq.linear_q8(Xq, sx, codes, sw, N, bits, out="i32"))
+    assert np.array_equal(acc_t, acc)
+    ref_acc, _ = oracle.linear_a8(to_np(Xq), to_np(sx), codes_np(codes, bits, K), to_np(sw))
+    assert np.array_equal(acc_t, ref_acc)
+
+
 def test_a8_extreme_accumulators(tq):
     import torch
     K = 12288
@@ -294,6 +315,26 @@ def test_empty_calls(tq):
     assert Y.shape == (0, 16)
     Y = tq.linear(to_dev_bf16(xgen("gpu/empty/x", 2, 512)), codes, sw, 0, 8, "W8A8")
     assert Y.shape == (2, 0)
+
+
+def test_binding_refuses_buffers_smaller_than_their_sizes(tq):
+    """The C ABI sees only pointers, so the binding checks that each tensor is
+    as large, and of the type, that the call will read or write."""
+    import torch
+    M, N, K = 8, 256, 512
+    X = to_dev_bf16(xgen("gpu/guard/x", M, K, XD))
+    codes, sw = gpu_weights(tq, wgen("gpu/guard/w", N, K), 8)
+    Xq, sx = tq.rotate_quant_act(X)
+    with pytest.raises(ValueError):    # an fp32 product into a bf16 buffer
+        tq.linear_q8(Xq, sx, codes, sw, N, 8, Y=torch.empty(M, N, dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError):    # too few rows
+        tq.linear(X, codes, sw, N, 8, "W8A8", Y=torch.empty(M - 1, N, device="cuda"))
+    with pytest.raises(ValueError):    # weights for fewer rows than N
+        tq.linear(X, codes[: N // 2], sw, N, 8, "W8A16")
+    with pytest.raises(ValueError):    # tiled operand smaller than its size
+        At, sxt = tq.rotate_quant_act_tiled(X)
+        tq.linear_tiled(At[:100], sxt, M, K, codes, sw, N, 8)
+    assert tq.device_status() == 0
 
 
 def test_device_status_clean(tq):
