@@ -495,8 +495,11 @@ def main():
             extra["dit_w8a8_m4032"] = {
                 "value": round(tops, 2), "unit": "TOPS", "per_gemm": per,
                 "gemm_only_tops": round(gemm_tops, 2),
-                "roofline": {"bound": "tensor", "achieved": round(gemm_tops, 2),
+                "roofline": {"bound": "tensor", "kernel": "k_gemm_a8_tc<8, tiled>",
+                             "achieved": round(gemm_tops, 2),
                              "peak": bf16_peak, "unit": "TFLOP/s",
+                             "traffic": traffic_for("k_gemm_a8_tc<8, tiled>", ["k_gemm_tc.cu", "tq_internal.cuh"]),
+                             "traffic_launch": "FFN up (N=12288, K=3072), DRAM bytes per launch",
                              "peak_kind": f"{pk_kind} bf16 dense (int8 codes run on the bf16-class tensor path)",
                              "frac": round(gemm_tops / bf16_peak, 4)}}
         except Exception as exc:
