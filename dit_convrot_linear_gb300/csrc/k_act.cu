@@ -194,9 +194,10 @@ template <int GPW, bool TILED>
 __global__ void __launch_bounds__(kThreads)
 k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx,
                     void *__restrict__ out, float *__restrict__ sx, int S,
-                    unsigned int *status) {
+                    unsigned int *status, unsigned int *max_l1) {
     extern __shared__ __align__(128) unsigned char ring[];   // [S][2K] then S barriers
     __shared__ float red[kThreads / 32];
+    __shared__ unsigned int red_sq[kThreads / 32];
     __shared__ int abort_sh;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int W = kThreads / 32;
@@ -289,11 +290,17 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
         const float r16 = r * 0.0625f >= FLT_MIN ? r * 0.0625f : 0.0f;   // exact: a power of two
         if (threadIdx.x == 0) sx[m] = s;
         const int64_t KT = (K + 63) >> 6;
+        // with the tiled operand, also the row's sum of |codes| (at most
+        // 127 * 16384)
+        unsigned int sq = 0;
         auto put = [&](int64_t g, int e, const float (&q)[8]) {
             const int64_t k0 = g * kGroup + static_cast<int64_t>(lane) * e;
-            if constexpr (TILED)
+            if constexpr (TILED) {
                 put_tiled(static_cast<uint16_t *>(out), KT, K, m, k0, e, q);
-            else
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < e) sq += static_cast<unsigned int>(fabsf(q[j]));
+            } else
                 put_int8(static_cast<int8_t *>(out) + m * K + k0, e, q);
         };
         // Pass 2: codes.  Full groups: x = v / 16.  Tail: x = v.
@@ -320,12 +327,25 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
             for (int e = 0; e < 8; ++e) q[e] = code_of(vt[e], 1.0f, r, s);
             put(Gf, Et, q);
         }
+        if constexpr (TILED) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            if (lane == 0) red_sq[warp] = sq;
+        }
         // This thread's reads of the buffer are ordered before the bulk copy
         // (async proxy) that will refill it; the barrier then makes every
         // thread's reads, and the reads of red[], precede the refill.
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
-        if (threadIdx.x == 0 && i + S < nrows) issue(i + S);
+        if (threadIdx.x == 0) {
+            if constexpr (TILED) {
+                unsigned int t = 0;
+#pragma unroll
+                for (int w = 0; w < W; ++w) t += red_sq[w];
+                atomicMax(max_l1, t);
+            }
+            if (i + S < nrows) issue(i + S);
+        }
     }
     // After an expired wait, let the copies still in flight land (bounded)
     // before the CTA's shared memory is released.
@@ -430,7 +450,7 @@ k_rotate_bf16(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx,
 
 template <bool TILED>
 tq_status launch_ring(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void *out, float *sx,
-                      cudaStream_t s) {
+                      unsigned int *max_l1, cudaStream_t s) {
     const int64_t G = (K + kGroup - 1) / kGroup;
     const int64_t gpw = (G + 7) / 8;
     DeviceInfo dev;
@@ -463,22 +483,28 @@ tq_status launch_ring(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void
     per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
     const int64_t want = static_cast<int64_t>(dev.sms) * per_sm;
     const unsigned grid = static_cast<unsigned>(M < want ? M : want);
-    kern<<<grid, kThreads, smem, s>>>(X, M, K, ldx, out, sx, S, status);
+    kern<<<grid, kThreads, smem, s>>>(X, M, K, ldx, out, sx, S, status, max_l1);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 
 }  // namespace
 
-int64_t tiled_act_bytes(int64_t M, int64_t K) {
+int64_t tiled_act_tiles_bytes(int64_t M, int64_t K) {
     return ((M + 255) / 256) * 2 * ((K + 63) / 64) * 16384;
 }
+
+int64_t tiled_act_bytes(int64_t M, int64_t K) { return tiled_act_tiles_bytes(M, K) + 256; }
 
 tq_status launch_rotate_quant_tiled(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
                                     void *At, float *sx, cudaStream_t s) {
     if (M == 0) return TQ_OK;
     if (K > kRingMaxK) return TQ_ERR_SHAPE;
-    return launch_ring<true>(X, M, K, ldx, At, sx, s);
+    unsigned int *max_l1 = reinterpret_cast<unsigned int *>(static_cast<unsigned char *>(At) +
+                                                            tiled_act_tiles_bytes(M, K));
+    const cudaError_t e = cudaMemsetAsync(max_l1, 0, sizeof(unsigned int), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return launch_ring<true>(X, M, K, ldx, At, sx, max_l1, s);
 }
 
 tq_status launch_rotate_quant_act(const uint16_t *X, int64_t M, int64_t K,
@@ -487,7 +513,7 @@ tq_status launch_rotate_quant_act(const uint16_t *X, int64_t M, int64_t K,
     const int64_t G = (K + kGroup - 1) / kGroup;
     const int64_t gpw = (G + 7) / 8;
     if (M == 0) return TQ_OK;
-    if (K <= kRingMaxK) return launch_ring<false>(X, M, K, ldx, Xq, sx, s);
+    if (K <= kRingMaxK) return launch_ring<false>(X, M, K, ldx, Xq, sx, nullptr, s);
     const unsigned grid = static_cast<unsigned>(M < (1ll << 30) ? M : (1ll << 30));
     if (gpw <= 1) k_rotate_quant_act<1><<<grid, kThreads, 0, s>>>(X, M, K, ldx, Xq, sx);
     else if (gpw <= 2) k_rotate_quant_act<2><<<grid, kThreads, 0, s>>>(X, M, K, ldx, Xq, sx);

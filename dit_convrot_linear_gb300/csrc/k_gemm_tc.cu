@@ -94,6 +94,7 @@ struct TcParams {
     int mtiles, ntiles, ksteps, chunk_steps;
     unsigned int *status;
     const unsigned char *At;   // pre-tiled fp16 A codes (AT path), else null
+    const unsigned int *max_l1;  // largest row sum of |A codes| (tiled operand), or null
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -294,7 +295,7 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     unsigned char *rawB = smem + P::OP_BYTES + RSTAGES * P::RAW_A;   // [R][B_RAW]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::OP_BYTES + P::RAW_BYTES);
     // bars: raw_full[R], raw_empty[R], op_full[O] (used in CTA 0), op_empty[O],
-    //       acc_full, acc_empty (CTA 0), done, a_full[O] (AT)
+    //       acc_full[2], acc_empty[2] (CTA 0), done, a_full[O] (AT)
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
 
@@ -304,9 +305,9 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     const uint32_t raw_full0 = smem_u32(bars), raw_empty0 = smem_u32(bars + RSTAGES);
     const uint32_t op_full0 = smem_u32(bars + 2 * RSTAGES);
     const uint32_t op_empty0 = smem_u32(bars + 2 * RSTAGES + OSTAGES);
-    const uint32_t acc_full = smem_u32(bars + 2 * RSTAGES + 2 * OSTAGES);
-    const uint32_t acc_empty = acc_full + 8, done = acc_full + 16;
-    const uint32_t a_full0 = acc_full + 24;
+    const uint32_t acc_full0 = smem_u32(bars + 2 * RSTAGES + 2 * OSTAGES);   // [2]
+    const uint32_t acc_empty0 = acc_full0 + 16, done = acc_full0 + 32;        // [2], 1
+    const uint32_t a_full0 = acc_full0 + 40;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < RSTAGES; ++s) {
@@ -317,8 +318,10 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(op_full0 + 8 * s), "r"(2 * WPG));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(op_empty0 + 8 * s));
         }
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(acc_full));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(acc_empty));
+        for (int h = 0; h < 2; ++h) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(acc_full0 + 8 * h));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(acc_empty0 + 8 * h));
+        }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done));
         if constexpr (AT) {
             for (int s = 0; s < OSTAGES; ++s)
@@ -338,6 +341,16 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     const uint32_t tmem = tmem_base_sh;
 
     const int ntiles_total = p.mtiles * p.ntiles;
+    // One fp32 accumulation per tile is exact when no partial sum can reach
+    // 2^24: K within one chunk, or the tiled operand's largest row sum of
+    // |codes| times the largest weight code, since any partial sum of
+    // a_k * b_k is at most sum_k |a_k| * qmax (and some int8 weights reach it,
+    // so the bound cannot be tightened without the weights).  Then two
+    // accumulators [0, 256) and [256, 512) alternate between tiles and the
+    // drain of one overlaps the MMAs of the next tile; otherwise one
+    // accumulator is drained per chunk into the running sum.
+    bool single = p.ksteps <= p.chunk_steps;
+    if (!single && p.max_l1) single = static_cast<double>(*p.max_l1) * (BITS == 8 ? 127.0 : 7.0) < 16777216.0;
     const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
     constexpr int BRAW = BITS == 8 ? B_RAW : B_RAW / 2;   // bytes of one raw B tile
 
@@ -463,12 +476,17 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------ MMA issue (CTA 0, one thread)
         if (rank == 0 && lane == 0) {
-            uint32_t it = 0, ch = 0;
+            uint32_t it = 0, ch = 0, tl = 0;
             bool issued = false;
-            for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
-                for (int c0 = 0; c0 < p.ksteps && !abort_sh; c0 += p.chunk_steps) {
-                    const int c1 = min(c0 + p.chunk_steps, p.ksteps);
-                    if (ch > 0 && !mbar_wait(acc_empty, (ch - 1) & 1, &abort_sh, p.status)) break;
+            for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters, ++tl) {
+                // single: one chunk per tile into accumulator tl & 1;
+                // else: chunks into accumulator 0, each drained before the next
+                const uint32_t buf = single ? (tl & 1) : 0;
+                const int cstep = single ? p.ksteps : p.chunk_steps;
+                for (int c0 = 0; c0 < p.ksteps && !abort_sh; c0 += cstep) {
+                    const int c1 = min(c0 + cstep, p.ksteps);
+                    const uint32_t use = single ? (tl >> 1) : ch;   // earlier uses of this accumulator
+                    if (use > 0 && !mbar_wait(acc_empty0 + 8 * buf, (use - 1) & 1, &abort_sh, p.status)) break;
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     for (int ks = c0; ks < c1; ++ks, ++it) {
                         const int s = it % OSTAGES;
@@ -482,13 +500,13 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                             asm volatile(
                                 "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
                                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-                                ::"r"(tmem), "l"(ad), "l"(bd), "r"(IDESC), "r"(accum));
+                                ::"r"(tmem + 256u * buf), "l"(ad), "l"(bd), "r"(IDESC), "r"(accum));
                         }
                         issued = true;
                         commit_pair(op_empty0 + 8 * s);
                     }
                     if (abort_sh) break;
-                    commit_pair(acc_full);
+                    commit_pair(acc_full0 + 8 * buf);
                     ++ch;
                 }
             }
@@ -507,42 +525,18 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         // ------------------------------------------------ epilogue (TMEM drain)
         const int q = warp & 3;                       // TMEM lane quarter of this warp
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        uint32_t ch = 0;
+        uint32_t ch = 0, tl = 0;
         const bool y16 = (reinterpret_cast<uintptr_t>(p.Y) & 15) == 0;
         const bool vec_ok = y16 && (p.ytype == 1 ? (p.ldy & 7) == 0 : (p.ldy & 3) == 0);
-        for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
+        for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters, ++tl) {
             const int64_t m0 = static_cast<int64_t>(tile % p.mtiles) * 2 * HM + rank * HM;
             const int64_t n0 = static_cast<int64_t>(tile / p.mtiles) * BN;
             const int64_t m = m0 + q * 32 + lane;
-            for (int c0 = 0; c0 < p.ksteps; c0 += p.chunk_steps, ++ch) {
-                const bool first = c0 == 0;
-                if (!mbar_wait(acc_full, ch & 1, &abort_sh, p.status)) break;
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                for (int col = 0; col < BN; col += 32) {
-                    uint32_t v[32], r[32];
-                    tmem_ld32(tmem + lane_base + col, v);
-                    if (!first) tmem_ld32(tmem + lane_base + RUN_COL + col, r);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int x = __float2int_rn(__uint_as_float(v[j]));
-                        r[j] = first ? static_cast<uint32_t>(x) : static_cast<uint32_t>(static_cast<int>(r[j]) + x);
-                    }
-                    tmem_st32(tmem + lane_base + RUN_COL + col, r);
-                }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive_leader(acc_empty);
-            }
-            if (abort_sh) break;
-            // the tile's exact int32 sums are in the running region: write Y
             const float xs = (p.ytype == 2 || m >= p.M) ? 1.0f : p.sx[m];
-            for (int col = 0; col < BN; col += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + RUN_COL + col, r);
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (m >= p.M) continue;
+            // Y of this thread's row for output columns n0 + col .. + 31 from
+            // their exact int32 sums
+            auto y_block = [&](int col, const uint32_t (&r)[32]) {
+                if (m >= p.M) return;
                 const int64_t nb = n0 + col;
                 if (p.ytype == 2) {
                     int32_t *y = static_cast<int32_t *>(p.Y) + m * p.ldy + nb;
@@ -554,7 +548,7 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                         for (int j = 0; j < 32; ++j)
                             if (nb + j < p.N) y[j] = static_cast<int32_t>(r[j]);
                     }
-                    continue;
+                    return;
                 }
                 float f[32];
 #pragma unroll
@@ -590,6 +584,54 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                             if (nb + j < p.N) y[j] = f32_to_bf16_bits(f[j]);
                     }
                 }
+            };
+            if (single) {
+                // the tile's one chunk: fp32 sums, exact integers, straight to Y
+                const uint32_t buf = tl & 1;
+                if (!mbar_wait(acc_full0 + 8 * buf, (tl >> 1) & 1, &abort_sh, p.status)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                for (int col = 0; col < BN; col += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + 256u * buf + col, v);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[j])));
+                    y_block(col, v);
+                }
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive_leader(acc_empty0 + 8 * buf);
+                continue;
+            }
+            for (int c0 = 0; c0 < p.ksteps; c0 += p.chunk_steps, ++ch) {
+                const bool first = c0 == 0;
+                if (!mbar_wait(acc_full0, ch & 1, &abort_sh, p.status)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                for (int col = 0; col < BN; col += 32) {
+                    uint32_t v[32], r[32];
+                    tmem_ld32(tmem + lane_base + col, v);
+                    if (!first) tmem_ld32(tmem + lane_base + RUN_COL + col, r);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int x = __float2int_rn(__uint_as_float(v[j]));
+                        r[j] = first ? static_cast<uint32_t>(x) : static_cast<uint32_t>(static_cast<int>(r[j]) + x);
+                    }
+                    tmem_st32(tmem + lane_base + RUN_COL + col, r);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive_leader(acc_empty0);
+            }
+            if (abort_sh) break;
+            // the tile's exact int32 sums are in the running region: write Y
+            for (int col = 0; col < BN; col += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + RUN_COL + col, r);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                y_block(col, r);
             }
         }
     }
@@ -674,6 +716,7 @@ tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const float *sx, 
     p.chunk_steps = bits == 8 ? 1024 / BK : 16384 / BK;
     p.status = status;
     p.At = At;
+    p.max_l1 = AT ? reinterpret_cast<const unsigned int *>(At + tiled_act_tiles_bytes(M, K)) : nullptr;
     const int64_t tiles = static_cast<int64_t>(p.mtiles) * p.ntiles;
     if (tiles > (1ll << 30)) return TQ_ERR_OVERFLOW;
     auto kern = bits == 8 ? k_gemm_a8_tc<8, AT> : k_gemm_a8_tc<4, AT>;

@@ -244,6 +244,28 @@ def test_tiled_operand_matches_int8_path(tq, M, N, K, bits):
     assert np.array_equal(acc_t, ref_acc)
 
 
+@pytest.mark.parametrize("bits", [8, 4])
+def test_tiled_operand_flat_rows(tq, bits):
+    """Rows whose rotation is flat (one nonzero per 256-group, so every rotated
+    value of a group is equal): all codes are +-127, the row norms are as large
+    as they can be, and the product must fall back from one fp32 accumulation
+    per tile to exact chunks (8-bit weights) and still be exact."""
+    import torch
+    M, N, K = 300, 129, 3072
+    X = np.zeros((M, K), np.float32)
+    rng = np.random.default_rng(bits)
+    mag = rng.choice([0.5, 0.75, 1.0, 1.5, 2.0], size=(M, 1)).astype(np.float32)   # exact in bf16
+    X[:, ::256] = rng.choice([-1.0, 1.0], size=(M, K // 256)).astype(np.float32) * mag
+    Xd = to_dev_bf16((X.view(np.uint32) >> 16).astype(np.uint16))
+    codes, sw = gpu_weights(tq, wgen(f"gpu/flat/w{bits}", N, K, WD if bits == 8 else WB), bits)
+    At, sxt = tq.rotate_quant_act_tiled(Xd)
+    Xq, sx = tq.rotate_quant_act(Xd)
+    assert np.all(np.abs(to_np(Xq).astype(np.int32)) == 127)
+    acc_t = to_np(tq.linear_tiled(At, sxt, M, K, codes, sw, N, bits, out="i32"))
+    ref_acc, _ = oracle.linear_a8(to_np(Xq), to_np(sx), codes_np(codes, bits, K), to_np(sw))
+    assert np.array_equal(acc_t, ref_acc)
+
+
 def test_a8_extreme_accumulators(tq):
     import torch
     K = 12288
