@@ -197,7 +197,7 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
                     unsigned int *status, unsigned int *max_l1) {
     extern __shared__ __align__(128) unsigned char ring[];   // [S][2K] then S barriers
     __shared__ float red[kThreads / 32];
-    __shared__ unsigned int red_sq[kThreads / 32];
+    __shared__ unsigned int win[16];   // a row's sum of |codes| per 1024-column window
     __shared__ int abort_sh;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int W = kThreads / 32;
@@ -221,6 +221,7 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
             : "memory");
     };
 
+    if (threadIdx.x < 16) win[threadIdx.x] = 0;
     if (threadIdx.x == 0) {
         abort_sh = 0;
         for (int i = 0; i < S; ++i)
@@ -290,16 +291,19 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
         const float r16 = r * 0.0625f >= FLT_MIN ? r * 0.0625f : 0.0f;   // exact: a power of two
         if (threadIdx.x == 0) sx[m] = s;
         const int64_t KT = (K + 63) >> 6;
-        // with the tiled operand, also the row's sum of |codes| (at most
-        // 127 * 16384)
-        unsigned int sq = 0;
+        // with the tiled operand, also the row's sum of |codes| per 1024-column
+        // window (each at most 127 * 1024)
         auto put = [&](int64_t g, int e, const float (&q)[8]) {
             const int64_t k0 = g * kGroup + static_cast<int64_t>(lane) * e;
             if constexpr (TILED) {
                 put_tiled(static_cast<uint16_t *>(out), KT, K, m, k0, e, q);
+                unsigned int gs = 0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    if (j < e) sq += static_cast<unsigned int>(fabsf(q[j]));
+                    if (j < e) gs += static_cast<unsigned int>(fabsf(q[j]));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
+                if (lane == 0) atomicAdd(&win[g >> 2], gs);
             } else
                 put_int8(static_cast<int8_t *>(out) + m * K + k0, e, q);
         };
@@ -327,11 +331,6 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
             for (int e = 0; e < 8; ++e) q[e] = code_of(vt[e], 1.0f, r, s);
             put(Gf, Et, q);
         }
-        if constexpr (TILED) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-            if (lane == 0) red_sq[warp] = sq;
-        }
         // This thread's reads of the buffer are ordered before the bulk copy
         // (async proxy) that will refill it; the barrier then makes every
         // thread's reads, and the reads of red[], precede the refill.
@@ -339,10 +338,23 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
         __syncthreads();
         if (threadIdx.x == 0) {
             if constexpr (TILED) {
-                unsigned int t = 0;
-#pragma unroll
-                for (int w = 0; w < W; ++w) t += red_sq[w];
-                atomicMax(max_l1, t);
+                // word 0: the whole row; word 1 + j: the largest aligned window
+                // of 1024 << j columns
+                const int nw = static_cast<int>((K + 1023) >> 10);
+                unsigned int total = 0;
+                for (int w = 0; w < nw; ++w) total += win[w];
+                atomicMax(max_l1, total);
+                for (int j = 0; j < 5; ++j) {
+                    const int span = 1 << j;
+                    unsigned int mx = 0;
+                    for (int w0 = 0; w0 < nw; w0 += span) {
+                        unsigned int t = 0;
+                        for (int w = w0; w < w0 + span && w < nw; ++w) t += win[w];
+                        mx = t > mx ? t : mx;
+                    }
+                    atomicMax(max_l1 + 1 + j, mx);
+                }
+                for (int w = 0; w < nw; ++w) win[w] = 0;
             }
             if (i + S < nrows) issue(i + S);
         }
@@ -502,7 +514,7 @@ tq_status launch_rotate_quant_tiled(const uint16_t *X, int64_t M, int64_t K, int
     if (K > kRingMaxK) return TQ_ERR_SHAPE;
     unsigned int *max_l1 = reinterpret_cast<unsigned int *>(static_cast<unsigned char *>(At) +
                                                             tiled_act_tiles_bytes(M, K));
-    const cudaError_t e = cudaMemsetAsync(max_l1, 0, sizeof(unsigned int), s);
+    const cudaError_t e = cudaMemsetAsync(max_l1, 0, 6 * sizeof(unsigned int), s);
     if (e != cudaSuccess) return cuda_fail(e);
     return launch_ring<true>(X, M, K, ldx, At, sx, max_l1, s);
 }

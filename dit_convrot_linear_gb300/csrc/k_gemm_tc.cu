@@ -349,8 +349,22 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     // accumulators [0, 256) and [256, 512) alternate between tiles and the
     // drain of one overlaps the MMAs of the next tile; otherwise one
     // accumulator is drained per chunk into the running sum.
-    bool single = p.ksteps <= p.chunk_steps;
-    if (!single && p.max_l1) single = static_cast<double>(*p.max_l1) * (BITS == 8 ? 127.0 : 7.0) < 16777216.0;
+    // The same bound per aligned window of K picks the longest chunk that
+    // stays exact when one accumulation per tile does not.
+    const double qmax = BITS == 8 ? 127.0 : 7.0;
+    int cs = p.chunk_steps;
+    bool single = p.ksteps <= cs;
+    if (!single && p.max_l1) {
+        single = static_cast<double>(p.max_l1[0]) * qmax < 16777216.0;
+        for (int j = 4; j >= 0 && !single; --j) {
+            const int steps = (1024 << j) / BK;
+            if (steps > cs && static_cast<double>(p.max_l1[1 + j]) * qmax < 16777216.0) {
+                cs = steps;
+                break;
+            }
+        }
+        single = single || p.ksteps <= cs;
+    }
     const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
     constexpr int BRAW = BITS == 8 ? B_RAW : B_RAW / 2;   // bytes of one raw B tile
 
@@ -482,7 +496,7 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 // single: one chunk per tile into accumulator tl & 1;
                 // else: chunks into accumulator 0, each drained before the next
                 const uint32_t buf = single ? (tl & 1) : 0;
-                const int cstep = single ? p.ksteps : p.chunk_steps;
+                const int cstep = single ? p.ksteps : cs;
                 for (int c0 = 0; c0 < p.ksteps && !abort_sh; c0 += cstep) {
                     const int c1 = min(c0 + cstep, p.ksteps);
                     const uint32_t use = single ? (tl >> 1) : ch;   // earlier uses of this accumulator
@@ -604,7 +618,7 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 if (lane == 0) mbar_arrive_leader(acc_empty0 + 8 * buf);
                 continue;
             }
-            for (int c0 = 0; c0 < p.ksteps; c0 += p.chunk_steps, ++ch) {
+            for (int c0 = 0; c0 < p.ksteps; c0 += cs, ++ch) {
                 const bool first = c0 == 0;
                 if (!mbar_wait(acc_full0, ch & 1, &abort_sh, p.status)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");

@@ -67,7 +67,8 @@ tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M,
 // bytes apart, row groups 1024 bytes apart).  Rows are padded to a whole
 // number of 256-row tile pairs; columns past K inside the last tile are zero.
 // After the tiles (at byte tiled_act_tiles_bytes), a 256-byte trailer whose
-// first word is the largest sum of |codes| over the rows.
+// first word is the largest sum of |codes| over the rows, word 1 + j the
+// largest such sum over an aligned window of 1024 << j columns (j < 5).
 int64_t tiled_act_tiles_bytes(int64_t M, int64_t K);
 int64_t tiled_act_bytes(int64_t M, int64_t K);
 tq_status launch_rotate_quant_tiled(const uint16_t *X, int64_t M, int64_t K,
