@@ -118,7 +118,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     }
 }
 
-template <int BITS>
+// PRE: every warp's K slice is at most one group (256 columns), so the warp's
+// weight fragments, widened to bf16 (16 MMA A-operands of 4 registers), fit in
+// registers.  They are read and widened before the dependency wait, in the
+// shadow of the previous kernel; after it only the x' loads and the MMAs remain.
+template <int BITS, bool PRE>
 __global__ void __launch_bounds__(kThreads)
 k_gemv_small(const SmallParams p) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -168,6 +172,46 @@ k_gemv_small(const SmallParams p) {
     }
     __syncthreads();  // barrier initialised; row scales in place
     pdl_launch_dependents();
+
+    constexpr int QPB = BITS == 8 ? 4 : 8;          // MMAs per weight block
+    constexpr int NBP = kGroup / KB;                // blocks in a one-group slice
+    uint32_t fr[PRE ? NBP * QPB : 1][4];            // widened A operands
+    bool have_w = false;
+    if constexpr (PRE) {
+        have_w = mbar_wait_bounded(wbar, 0);
+        const int g = lane >> 2, t = lane & 3;
+        const int rA = wr * 16 + g, rB = rA + 8;
+        const bool okA = rA < rows, okB = rB < rows;
+        const int nk0 = static_cast<int>(min(static_cast<int64_t>(g1) * kGroup, p.K) -
+                                         static_cast<int64_t>(g0) * kGroup);
+        const unsigned char *pA = ws + rA * p.WS + g0 * BPG * BB + t * 16;
+        const unsigned char *pB = ws + rB * p.WS + g0 * BPG * BB + t * 16;
+        const int sbytes = nk0 * BITS / 8;
+#pragma unroll
+        for (int blk = 0; blk < NBP; ++blk) {
+            const int off = blk * BB;
+            const bool in = have_w && off + t * 16 < sbytes;
+            const uint4 wa = (in && okA) ? *reinterpret_cast<const uint4 *>(pA + off) : make_uint4(0, 0, 0, 0);
+            const uint4 wb = (in && okB) ? *reinterpret_cast<const uint4 *>(pB + off) : make_uint4(0, 0, 0, 0);
+            const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w};
+            const uint32_t B[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if constexpr (BITS == 8) {
+                    uint32_t *f = fr[blk * QPB + q];
+                    widen_i8(A[q], f[0], f[2]);
+                    widen_i8(B[q], f[1], f[3]);
+                } else {
+                    uint32_t pa[4], pb[4];
+                    widen_i4(A[q], pa);
+                    widen_i4(B[q], pb);
+                    uint32_t *f0 = fr[blk * QPB + 2 * q], *f1 = fr[blk * QPB + 2 * q + 1];
+                    f0[0] = pa[0]; f0[1] = pb[0]; f0[2] = pa[1]; f0[3] = pb[1];
+                    f1[0] = pa[2]; f1[1] = pb[2]; f1[2] = pa[3]; f1[3] = pb[3];
+                }
+            }
+        }
+    }
     pdl_wait();
 
     // ---- rotate this warp's groups into its private x' (token rows of XS)
@@ -216,7 +260,7 @@ k_gemv_small(const SmallParams p) {
     __syncwarp();
 
     // ---- products: this warp's 16 rows x its K slice
-    const bool have_w = mbar_wait_bounded(wbar, 0);
+    if constexpr (!PRE) have_w = mbar_wait_bounded(wbar, 0);
     if (!have_w && lane == 0) atomicOr(p.status, kStatusSmallTimeout);
     const int g = lane >> 2, t = lane & 3;
     const int rA = wr * 16 + g, rB = rA + 8;
@@ -231,7 +275,21 @@ k_gemv_small(const SmallParams p) {
     float acc[NCH][4];
 #pragma unroll
     for (int c = 0; c < NCH; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.0f;
-    if (have_w) {
+    if (PRE && have_w) {
+#pragma unroll
+        for (int blk = 0; blk < NBP; ++blk) {
+            if (blk < nblk) {
+                const uint16_t *xblk = xb + blk * KB;
+#pragma unroll
+                for (int q = 0; q < QPB; ++q) {
+                    // token columns >= M read row 0 (valid); their outputs are dropped
+                    const uint2 bv = *reinterpret_cast<const uint2 *>(xblk + q * 16);
+                    const uint32_t *f = fr[blk * QPB + q];
+                    mma_bf16(acc[q % NCH], f[0], f[1], f[2], f[3], bv.x, bv.y);
+                }
+            }
+        }
+    } else if (have_w) {
         for (int blk = 0; blk < nblk; ++blk) {
             const int off = blk * BB;
             const bool in = off + t * 16 < slice_bytes;
@@ -366,9 +424,12 @@ tq_status launch_gemv_small(const uint16_t *X, int64_t M, int64_t K, int64_t ldx
     p.x_off = pl.x_off;
     p.r_off = pl.r_off;
     p.status = status;
-    auto kern = bits == 8 ? k_gemv_small<8> : k_gemv_small<4>;
-    static int configured_for[64][2] = {{0}};
-    const int bi = bits == 8 ? 0 : 1;
+    // weight fragments in registers when every warp's slice is one group
+    const bool pre = pl.gpw == 1;
+    auto kern = bits == 8 ? (pre ? k_gemv_small<8, true> : k_gemv_small<8, false>)
+                          : (pre ? k_gemv_small<4, true> : k_gemv_small<4, false>);
+    static int configured_for[64][4] = {{0}};
+    const int bi = (bits == 8 ? 0 : 2) + (pre ? 1 : 0);
     if (dev.id >= 0 && dev.id < 64 && !configured_for[dev.id][bi]) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(kSmallSmemMax));
