@@ -141,6 +141,8 @@ A16_CASES = [
     (4, 256, 512, 8), (1, 4864, 896, 8), (1, 896, 4864, 8), (1, 4864, 896, 4),
     (1, 896, 4864, 4), (8, 1000, 4096 + 128, 4), (13, 300, 896, 8), (32, 512, 4096, 4),
     (64, 257, 12288, 4), (3, 77, 32, 8), (5, 100, 288, 4), (64, 4096, 4096, 8),
+    # eight-row decode kernel: M <= 2, ragged rows, K with a partial last block
+    (2, 300, 4096 + 32, 8), (2, 77, 4096 + 128, 4), (1, 40, 2304 + 64, 8), (1, 21, 2304 + 32, 4),
 ]
 
 
