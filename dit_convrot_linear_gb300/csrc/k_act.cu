@@ -301,8 +301,7 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     if (j < e) gs += static_cast<unsigned int>(fabsf(q[j]));
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
+                gs = __reduce_add_sync(0xffffffffu, gs);
                 if (lane == 0) atomicAdd(&win[g >> 2], gs);
             } else
                 put_int8(static_cast<int8_t *>(out) + m * K + k0, e, q);
@@ -336,28 +335,26 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
         // thread's reads, and the reads of red[], precede the refill.
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
-        if (threadIdx.x == 0) {
-            if constexpr (TILED) {
-                // word 0: the whole row; word 1 + j: the largest aligned window
-                // of 1024 << j columns
-                const int nw = static_cast<int>((K + 1023) >> 10);
-                unsigned int total = 0;
-                for (int w = 0; w < nw; ++w) total += win[w];
-                atomicMax(max_l1, total);
-                for (int j = 0; j < 5; ++j) {
-                    const int span = 1 << j;
-                    unsigned int mx = 0;
-                    for (int w0 = 0; w0 < nw; w0 += span) {
-                        unsigned int t = 0;
-                        for (int w = w0; w < w0 + span && w < nw; ++w) t += win[w];
-                        mx = t > mx ? t : mx;
-                    }
+        if (TILED && warp == 0) {
+            // lane l holds window l (1024 columns; zero past K).  Word 1 + j:
+            // the largest sum over an aligned run of 2^j windows; word 0: the
+            // whole row.  Sums by butterfly within aligned lane groups, then a
+            // maximum over the lanes.
+            unsigned int ws = lane < 16 ? win[lane] : 0u;
+            if (lane < 16) win[lane] = 0;
+#pragma unroll
+            for (int j = 0; j < 5; ++j) {
+                if (j > 0) ws += __shfl_xor_sync(0xffffffffu, ws, 1 << (j - 1));
+                unsigned int mx = ws;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                if (lane == 0) {
                     atomicMax(max_l1 + 1 + j, mx);
+                    if (j == 4) atomicMax(max_l1, mx);
                 }
-                for (int w = 0; w < nw; ++w) win[w] = 0;
             }
-            if (i + S < nrows) issue(i + S);
         }
+        if (threadIdx.x == 0 && i + S < nrows) issue(i + S);
     }
     // After an expired wait, let the copies still in flight land (bounded)
     // before the CTA's shared memory is released.

@@ -97,6 +97,12 @@ struct TcParams {
     const unsigned int *max_l1;  // largest row sum of |A codes| (tiled operand), or null
 };
 
+// Tile order: N fastest, so the pairs working at one time share a few strips
+// of A (each read from DRAM once) while all of B stays in L2; with M fastest,
+// every strip of A is in flight at once and a long-K product re-reads them.
+__device__ __forceinline__ int tile_m(int tile, const TcParams &p) { return tile / p.ntiles; }
+__device__ __forceinline__ int tile_n(int tile, const TcParams &p) { return tile % p.ntiles; }
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -373,8 +379,8 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         if (lane == 0) {
             uint32_t it = 0;
             for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
-                const int m0 = (tile % p.mtiles) * 2 * HM + static_cast<int>(rank) * HM;
-                const int n0 = (tile / p.mtiles) * BN + static_cast<int>(rank) * HN;
+                const int m0 = tile_m(tile, p) * 2 * HM + static_cast<int>(rank) * HM;
+                const int n0 = tile_n(tile, p) * BN + static_cast<int>(rank) * HN;
                 for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
                     const int s = it % RSTAGES;
                     if (!mbar_wait(raw_empty0 + 8 * s, ((it / RSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
@@ -394,7 +400,7 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         if (lane == 0) {
             uint32_t it = 0;
             for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
-                const int64_t mt = static_cast<int64_t>(tile % p.mtiles) * 2 + rank;
+                const int64_t mt = static_cast<int64_t>(tile_m(tile, p)) * 2 + rank;
                 for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
                     const int s = it % OSTAGES;
                     if (!mbar_wait(op_empty0 + 8 * s, ((it / OSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
@@ -543,8 +549,8 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         const bool y16 = (reinterpret_cast<uintptr_t>(p.Y) & 15) == 0;
         const bool vec_ok = y16 && (p.ytype == 1 ? (p.ldy & 7) == 0 : (p.ldy & 3) == 0);
         for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters, ++tl) {
-            const int64_t m0 = static_cast<int64_t>(tile % p.mtiles) * 2 * HM + rank * HM;
-            const int64_t n0 = static_cast<int64_t>(tile / p.mtiles) * BN;
+            const int64_t m0 = static_cast<int64_t>(tile_m(tile, p)) * 2 * HM + rank * HM;
+            const int64_t n0 = static_cast<int64_t>(tile_n(tile, p)) * BN;
             const int64_t m = m0 + q * 32 + lane;
             const float xs = (p.ytype == 2 || m >= p.M) ? 1.0f : p.sx[m];
             // Y of this thread's row for output columns n0 + col .. + 31 from
