@@ -16,6 +16,7 @@
 // a plain one-CTA-per-row kernel that loads each group straight from global.
 
 #include <cfloat>
+#include <type_traits>
 
 #include "tq_internal.cuh"
 
@@ -190,17 +191,17 @@ __device__ __forceinline__ void put_tiled(uint16_t *At, int64_t KT, int64_t K, i
 // one bulk copy that completes on that buffer's barrier.  Warp w owns groups
 // w, w + 8, ...; the first GPW stay in registers between the amax pass and
 // the quantise pass, further ones are recomputed from the buffer.
-template <int GPW, bool TILED>
-__global__ void __launch_bounds__(kThreads)
+template <int GPW, bool TILED, int NT>
+__global__ void __launch_bounds__(NT)
 k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx,
                     void *__restrict__ out, float *__restrict__ sx, int S,
                     unsigned int *status, unsigned int *max_l1) {
     extern __shared__ __align__(128) unsigned char ring[];   // [S][2K] then S barriers
-    __shared__ float red[kThreads / 32];
+    __shared__ float red[NT / 32];
     __shared__ unsigned int win[16];   // a row's sum of |codes| per 1024-column window
     __shared__ int abort_sh;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int W = kThreads / 32;
+    constexpr int W = NT / 32;
     const int64_t Gf = K / kGroup;                        // full 256-groups
     const int tail = static_cast<int>(K % kGroup);        // 0, 32, 64 or 128
     const int tail_warp = static_cast<int>(Gf % W);
@@ -461,23 +462,31 @@ template <bool TILED>
 tq_status launch_ring(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void *out, float *sx,
                       unsigned int *max_l1, cudaStream_t s) {
     const int64_t G = (K + kGroup - 1) / kGroup;
-    const int64_t gpw = (G + 7) / 8;
+    // rows of up to 16 groups: CTAs of 4 warps, more of them, so that more
+    // rows are in flight per SM; longer rows: 8 warps
+    const bool small = G <= 16;
+    const int NT = small ? 128 : 256;
+    const int64_t gpw = (G + NT / 32 - 1) / (NT / 32);
     DeviceInfo dev;
     const tq_status ds = current_device(&dev);
     if (ds != TQ_OK) return ds;
     unsigned int *status = status_word();
     if (!status) return TQ_ERR_DEVICE;
-    // rows in flight per CTA: about 48 KB of them, 2 to 8 rows
+    // rows in flight per CTA: about 48 KB of them (24 KB with 4 warps), 2 to 8 rows
     const int64_t rb = 2 * K;
-    int S = static_cast<int>((48 * 1024) / rb);
+    int S = static_cast<int>(((small ? 24 : 48) * 1024) / rb);
     S = S < 2 ? 2 : (S > 8 ? 8 : S);
     const size_t smem = static_cast<size_t>(S) * rb + 8 * S;
-    auto kern = gpw <= 1 ? k_rotate_quant_ring<1, TILED>
-              : gpw <= 2 ? k_rotate_quant_ring<2, TILED>
-              : gpw <= 4 ? k_rotate_quant_ring<4, TILED>
-                         : k_rotate_quant_ring<8, TILED>;
-    const int ki = gpw <= 1 ? 0 : gpw <= 2 ? 1 : gpw <= 4 ? 2 : 3;
-    static bool configured[64][4] = {{false}};
+    auto pick = [&](auto nt) {
+        constexpr int N = decltype(nt)::value;
+        return gpw <= 1 ? k_rotate_quant_ring<1, TILED, N>
+             : gpw <= 2 ? k_rotate_quant_ring<2, TILED, N>
+             : gpw <= 4 ? k_rotate_quant_ring<4, TILED, N>
+                        : k_rotate_quant_ring<8, TILED, N>;
+    };
+    auto kern = small ? pick(std::integral_constant<int, 128>{}) : pick(std::integral_constant<int, 256>{});
+    const int ki = (gpw <= 1 ? 0 : gpw <= 2 ? 1 : gpw <= 4 ? 2 : 3) + (small ? 4 : 0);
+    static bool configured[64][8] = {{false}};
     if (dev.id < 0 || dev.id >= 64) return TQ_ERR_DEVICE;
     if (!configured[dev.id][ki]) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -485,14 +494,15 @@ tq_status launch_ring(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void
         if (e != cudaSuccess) return cuda_fail(e);
         configured[dev.id][ki] = true;
     }
-    // persistent: as many CTAs as are resident at once, at most 4 per SM
+    // persistent: as many CTAs as are resident at once, at most 4 (8 with 4 warps) per SM
     int per_sm = 0;
-    const cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    const cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem);
     if (oe != cudaSuccess) return cuda_fail(oe);
-    per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
+    const int cap = small ? 8 : 4;
+    per_sm = per_sm < 1 ? 1 : (per_sm > cap ? cap : per_sm);
     const int64_t want = static_cast<int64_t>(dev.sms) * per_sm;
     const unsigned grid = static_cast<unsigned>(M < want ? M : want);
-    kern<<<grid, kThreads, smem, s>>>(X, M, K, ldx, out, sx, S, status, max_l1);
+    kern<<<grid, NT, smem, s>>>(X, M, K, ldx, out, sx, S, status, max_l1);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
