@@ -75,6 +75,17 @@ struct Plan {
     static constexpr int OP_BYTES = O * (A_OP + B_OP);
     static constexpr int RAW_BYTES = R * (RAW_A + B_RAW);
     static constexpr int SMEM_BYTES = OP_BYTES + RAW_BYTES + 1024;
+    // A parity wait tells only two phases apart, so a waiter must know that
+    // the phase before the one it waits for has completed.  A converter group
+    // takes every CONV_GROUPS-th K step; for step j it waits first for its
+    // operand stage to be free (step j - O consumed, in order, which implies
+    // that every step up to j - O has landed and been converted), then for
+    // its raw slot (previous use j - R, landed when R >= O) and, with pre-tiled
+    // A, for the A tile (previous use j - O).  Its own previous step j - G
+    // waited for step j - G - O to be consumed, so the stage wait cannot see
+    // step j - 2O still pending when G <= O.
+    static_assert(R >= O, "raw slot's previous use covered by the stage wait");
+    static_assert(O >= CONV_GROUPS, "operand stages for every group");
 };
 constexpr uint32_t TMEM_COLS = 512;    // acc [0, 256) + running int32 sum [256, 512)
 constexpr uint32_t RUN_COL = 256;
@@ -426,8 +437,9 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
                 if (static_cast<int>(it % CONV_GROUPS) != g) continue;
                 const int rs = it % RSTAGES, os = it % OSTAGES;
-                if (!mbar_wait(raw_full0 + 8 * rs, (it / RSTAGES) & 1, &abort_sh, p.status)) break;
+                // stage first: see the ring plan for why the order matters
                 if (!mbar_wait(op_empty0 + 8 * os, ((it / OSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
+                if (!mbar_wait(raw_full0 + 8 * rs, (it / RSTAGES) & 1, &abort_sh, p.status)) break;
                 const unsigned char *ra = rawA + rs * A_RAW;
                 const unsigned char *rb = rawB + rs * B_RAW;
                 unsigned char *oa = opA + os * A_OP;
