@@ -246,6 +246,25 @@ class Decode:
         torch.cuda.synchronize()
         self.graph = g
 
+    def make_grouped(self):
+        """The same calls as one grouped plan (they are independent: each has
+        its own input and output)."""
+        from dit_convrot_linear_gb300 import tq
+        calls = []
+        for (i, L, j, p, xo, yo) in self.plan:
+            codes, sw = self.weights[L][j]
+            calls.append((self.x_dev[xo:xo + p.K].view(1, p.K), codes, sw, p.N,
+                          self.y_dev[yo:yo + p.N].view(1, p.N)))
+        self.gplan = tq.GroupedPlan(calls, self.bits)
+
+    def step_grouped(self):
+        self.gplan.run()
+
+    def step_grouped_e2e(self):
+        self.x_dev.copy_(self.x_host, non_blocking=True)
+        self.gplan.run()
+        self.y_host.copy_(self.y_dev, non_blocking=True)
+
     def step(self):
         self.graph.replay()
 

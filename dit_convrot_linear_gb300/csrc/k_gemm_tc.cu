@@ -678,41 +678,6 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-        cudaGetLastError();
-    }
-    return fn;
-}
-
-// 2-D map of a row-major byte matrix [rows][cols] (cols bytes per row), read in
-// boxes of box_cols bytes x 128 rows, out-of-range elements filled with zero.
-bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int box_cols,
-              CUtensorMapSwizzle swz) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), 128u};
-    const cuuint32_t estr[2] = {1u, 1u};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Shared launch of both operand paths: Xq int8 codes (AT false, A through a
 // tensor map) or At pre-tiled fp16 codes (AT true).
 template <bool AT>
@@ -724,13 +689,13 @@ tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const float *sx, 
     if (!status) return TQ_ERR_DEVICE;
     if (M > (1ll << 31) - 1 || N > (1ll << 31) - 1) return TQ_ERR_OVERFLOW;
     CUtensorMap tmA, tmB;
-    const bool mapped = bits == 8 ? make_map(&tmB, Wq, N, K, BK, CU_TENSOR_MAP_SWIZZLE_64B)
-                                  : make_map(&tmB, Wq, N, K / 2, BK / 2, CU_TENSOR_MAP_SWIZZLE_32B);
+    const bool mapped = bits == 8 ? make_map_u8(&tmB, Wq, N, K, BK, 128, CU_TENSOR_MAP_SWIZZLE_64B)
+                                  : make_map_u8(&tmB, Wq, N, K / 2, BK / 2, 128, CU_TENSOR_MAP_SWIZZLE_32B);
     if (!mapped) return TQ_ERR_DEVICE;
     if constexpr (AT) {
         tmA = tmB;   // not read on this path
     } else {
-        if (!make_map(&tmA, Xq, M, K, BK, CU_TENSOR_MAP_SWIZZLE_64B)) return TQ_ERR_DEVICE;
+        if (!make_map_u8(&tmA, Xq, M, K, BK, 128, CU_TENSOR_MAP_SWIZZLE_64B)) return TQ_ERR_DEVICE;
     }
     TcParams p{};
     p.sx = sx;
@@ -782,6 +747,41 @@ tq_status launch_gemm_a8_tiled(const void *At, const float *sx, int64_t M, int64
                                cudaStream_t s) {
     return launch_tc<true>(nullptr, static_cast<const unsigned char *>(At), sx, M, K, Wq, sw, N,
                            bits, Y, ytype, ldy, dev, s);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+        cudaGetLastError();
+    }
+    return fn;
+}
+
+// 2-D map of a row-major byte matrix [rows][cols] (cols bytes per row), read in
+// boxes of box_cols bytes x box_rows rows, out-of-range elements filled with zero.
+bool make_map_u8(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int box_cols,
+                 int box_rows, CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace tq

@@ -1,0 +1,547 @@
+// Grouped A16 product: many independent decode calls in one persistent pass,
+//   Y_c[m][n] = sw_c[n] * sum_k q_c[n][k] * x'_c,bf16[m][k],  fp32 sums,
+// x'_c the group-256 Hadamard rotation of call c's token rows rounded to bf16
+// (tensai docs, "画像生成" / Image generation, section "幅とメモリ": the input of
+// the product gets the same rotation as the weights).  Decode is bound by the
+// weight stream (kvad-gpu internals, "Numbers"), but one call of a small model
+// moves only a few MB: launched one by one, each call waits for the previous
+// one to finish before it may read its input, and that chain of latencies,
+// not the weight stream, sets the time.  Calls that do not depend on one
+// another (gate and up of a layer, or the independent calls of a batch) can
+// instead share one weight stream:
+//   1. k_rotate_grouped rotates every call's token rows once, into a
+//      workspace of the plan, in the lane-contiguous x' order of the MMAs.
+//   2. k_gemv_grouped runs one CTA per SM.  Work items are (call, block of
+//      weight rows, all of K), dealt round-robin, so the SMs sweep through the
+//      calls together and a weight matrix is never read by two SMs at once.
+//      A producer warp bulk-copies each item's weight rows and x' into a ring
+//      of shared-memory stages and stays up to three items ahead; sixteen
+//      consumer warps multiply (codes widened to exact bf16 pairs in
+//      registers, mma.sync m16n8k16, fp32), add the K blocks in a fixed order
+//      and store Y.  The stream never waits for a call to finish.
+// Every wait is bounded: on expiry the status word is set, the CTA stops, and
+// the outputs of the items it had not finished are left unwritten.
+
+#include <new>
+#include <vector>
+
+#include "tq_a16.cuh"
+
+namespace tq {
+namespace {
+
+// One work item, as the producer reads it and copies it into the stage header.
+// Its weight rows reach shared memory in one of two forms:
+//   rows:  one bulk copy per row, rows ws bytes apart (ws = 64 mod 128, so the
+//          lanes of a quarter-warp read distinct banks);
+//   tiles: one tensor copy per 128-byte column chunk of all rows (few copies
+//          for short rows: a bulk copy has a fixed cost of tens of cycles),
+//          chunk c at c * rb * 128, each 128-byte row line stored with the
+//          128-byte swizzle (16-byte unit j of row r at unit j ^ (r & 7)).
+struct GItem {
+    const uint8_t *w;      // rows: first weight row of the item
+    const void *tmap;      // tiles: the call's tensor map (rows x row bytes)
+    const uint16_t *xq;    // the call's x' rows (bf16, M rows of xk)
+    const float *sw;       // row scale of the first row
+    void *y;               // Y of the first row, token 0
+    int64_t ldy;           // Y row stride (elements)
+    int32_t rows;          // valid weight rows
+    int32_t rb;            // rows the stage holds (multiple of 8)
+    int32_t rbytes;        // bytes of one weight row
+    int32_t ws;            // rows: shared row stride (bytes)
+    int32_t xk;            // x' row length: K rounded up to whole blocks
+    int32_t n0;            // tiles: first row of the item in the call
+    int32_t xoff;          // byte offset of x' in the stage
+    int16_t M;             // token rows
+    int16_t tiles;         // 1: tile form
+};
+static_assert(sizeof(GItem) == 80, "item record of 80 bytes");
+
+struct GCall {
+    const uint16_t *X;
+    int64_t ldx;
+    uint16_t *xq;
+    int32_t M, K, xk, pad;
+};
+
+constexpr int kGStages = 3;
+constexpr int kGStageBytes = 64 * 1024;
+constexpr int kGConsWarps = 16;
+constexpr int kGThreads = (kGConsWarps + 1) * 32;     // + the producer warp
+constexpr int kGRed = 128;                            // rows x tokens of one item at most
+constexpr int kGRedOff = kGStages * kGStageBytes;
+constexpr int kGHdrOff = kGRedOff + 2 * kGConsWarps * kGRed * 4;
+constexpr int kGBarOff = kGHdrOff + kGStages * 128;
+constexpr int kGSmem = kGBarOff + 2 * kGStages * 8 + 16 + 1024;   // + alignment of the stages
+constexpr unsigned int kStatusGroupedTimeout = 16u;
+
+struct GroupedParams {
+    const GItem *items;
+    int64_t nitems;
+    int ytype;
+    unsigned int *status;
+};
+
+// Barrier 1 among the consumer threads, returning whether any of them
+// passed `pred`: every consumer reaches it on every item, so the decision to
+// stop is the same in all of them.
+__device__ __forceinline__ bool consumers_sync_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\n"
+        "bar.red.or.pred q, 1, %2, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(kGConsWarps * 32)
+        : "memory");
+    return r != 0;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(256)
+k_rotate_grouped(const GCall *calls, int64_t ncalls) {
+    constexpr int KB = BITS == 8 ? 64 : 128;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t c = blockIdx.x; c < ncalls; c += gridDim.x) {
+        const GCall cl = calls[c];
+        const int G = (cl.K + kGroup - 1) / kGroup;
+        for (int job = warp; job < cl.M * G; job += 8) {
+            const int m = job / G, gi = job % G;
+            const int64_t gk = static_cast<int64_t>(gi) * kGroup;
+            const int n = group_width(cl.K, gk);
+            const int E = n / 32;
+            const uint4 raw = load_group_raw(cl.X + m * cl.ldx + gk + lane * E, E);
+            float v[8];
+            fwht_group_raw(raw, n, v);
+            uint16_t *row = cl.xq + static_cast<int64_t>(m) * cl.xk;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (e < E) {
+                    const int kl = static_cast<int>(gk) + lane * E + e;
+                    row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = f32_to_bf16_bits(v[e]);
+                }
+            }
+        }
+        const int padw = cl.xk - cl.K;   // zeros after K, up to the block edge
+        for (int idx = threadIdx.x; idx < cl.M * padw; idx += blockDim.x) {
+            const int m = idx / padw, kl = cl.K + idx % padw;
+            cl.xq[static_cast<int64_t>(m) * cl.xk + (kl / KB) * KB + xpos<BITS>(kl % KB)] = 0;
+        }
+    }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kGThreads, 1)
+k_gemv_grouped(const GroupedParams p) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    // stages on a 1024-byte boundary (the tensor copies' 128-byte swizzle)
+    unsigned char *smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+    constexpr int KB = BITS == 8 ? 64 : 128;   // k per block (16 bytes per lane)
+    constexpr int BB = 64;                     // weight bytes per row per block
+    float *red = reinterpret_cast<float *>(smem + kGRedOff);
+    unsigned char *hdr = smem + kGHdrOff;      // stage headers, 128 bytes apart
+    const uint32_t full0 = smem_addr(smem + kGBarOff);
+    const uint32_t empty0 = full0 + 8 * kGStages;
+    volatile int *abort_sh = reinterpret_cast<volatile int *>(smem + kGBarOff + 2 * kGStages * 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t grid = gridDim.x;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGStages; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(full0 + 8 * s));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(empty0 + 8 * s));
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        *abort_sh = 0;
+    }
+    __syncthreads();
+
+    if (warp == kGConsWarps) {
+        // ------------------------------------------------ producer
+        // Item k goes to stage k % kGStages once the consumers have released
+        // the stage's previous item (this warp is the only waiter, in order).
+        int64_t k = 0;
+        GItem nxt;                       // the next record, loaded one item ahead
+        if (blockIdx.x < p.nitems) nxt = p.items[blockIdx.x];
+        for (;; ++k) {
+            const int64_t i = blockIdx.x + k * grid;
+            const bool stop = __shfl_sync(0xffffffffu, *abort_sh, 0) != 0;   // one decision per warp
+            if (i >= p.nitems || stop) break;
+            const GItem it = nxt;
+            if (i + grid < p.nitems) nxt = p.items[i + grid];
+            const int s = static_cast<int>(k % kGStages);
+            const int64_t u = k / kGStages;
+            bool ok = true;
+            if (lane == 0 && u > 0) ok = mbar_wait_bounded(empty0 + 8 * s, static_cast<uint32_t>((u - 1) & 1));
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    *abort_sh = 1;
+                    atomicOr(p.status, kStatusGroupedTimeout);
+                }
+                break;
+            }
+            unsigned char *st = smem + s * kGStageBytes;
+            const uint32_t full = full0 + 8 * s;
+            const int nch = (it.rbytes + 127) / 128;
+            if (lane == 0) {
+                *reinterpret_cast<GItem *>(hdr + s * 128) = it;
+                const uint32_t xbytes = static_cast<uint32_t>(it.M) * it.xk * 2;
+                // a tensor copy counts its whole box, zero fill included
+                const uint32_t wbytes = it.tiles ? static_cast<uint32_t>(nch * it.rb * 128)
+                                                 : static_cast<uint32_t>(it.rows * it.rbytes);
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full),
+                             "r"(wbytes + xbytes)
+                             : "memory");
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                    ::"r"(smem_addr(st + it.xoff)), "l"(it.xq), "r"(xbytes), "r"(full)
+                    : "memory");
+            }
+            __syncwarp();
+            if (it.tiles) {
+                for (int c = lane; c < nch; c += 32) {
+                    asm volatile(
+                        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+                        "[%0], [%1, {%2, %3}], [%4];"
+                        ::"r"(smem_addr(st + c * it.rb * 128)), "l"(it.tmap), "r"(c * 128), "r"(it.n0),
+                          "r"(full)
+                        : "memory");
+                }
+            } else {
+                for (int r = lane; r < it.rows; r += 32) {
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                        ::"r"(smem_addr(st + r * it.ws)), "l"(it.w + static_cast<int64_t>(r) * it.rbytes),
+                          "r"(static_cast<uint32_t>(it.rbytes)), "r"(full)
+                        : "memory");
+                }
+            }
+        }
+        // never leave with copies still landing: wait for the last issued use
+        // of every stage (already complete unless the consumers stopped)
+        if (lane == 0) {
+            for (int s = 0; s < kGStages; ++s) {
+                const int64_t uses = k > s ? (k - s + kGStages - 1) / kGStages : 0;
+                if (uses > 0) mbar_wait_bounded(full0 + 8 * s, static_cast<uint32_t>((uses - 1) & 1));
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumers
+    // Units of an item are (16-row tile, K block), tile-major; warp w takes a
+    // contiguous run of them and keeps one tile's sums in registers until its
+    // run leaves the tile.  The partial sums of a row are then added over the
+    // warps in warp order: the result does not depend on timing.
+    const int g = lane >> 2, t = lane & 3;
+    for (int64_t k = 0;; ++k) {
+        const int64_t i = blockIdx.x + k * grid;
+        if (i >= p.nitems) break;
+        const int s = static_cast<int>(k % kGStages);
+        const bool ok = mbar_wait_bounded(full0 + 8 * s, static_cast<uint32_t>((k / kGStages) & 1));
+        float *rd = red + (k & 1) * kGConsWarps * kGRed;
+        // the header is read before the stage is released
+        int rows = 0, rb = 0, ws = 0, xk = KB, M = 1, xoff = 0;
+        bool tiles = false;
+        const float *swp = nullptr;
+        void *y = nullptr;
+        int64_t ldy = 0;
+        if (ok) {
+            const GItem &h = *reinterpret_cast<const GItem *>(hdr + s * 128);
+            rows = h.rows;
+            rb = h.rb;
+            ws = h.ws;
+            xk = h.xk;
+            M = h.M;
+            xoff = h.xoff;
+            tiles = h.tiles != 0;
+            swp = h.sw;
+            y = h.y;
+            ldy = h.ldy;
+        }
+        const int NB = xk / KB, U = ((rb + 15) / 16) * NB;
+        const int u0 = U * warp / kGConsWarps, u1 = U * (warp + 1) / kGConsWarps;
+        const int j = threadIdx.x;
+        const bool store = ok && j < rows * M;
+        const int m_st = store ? j / rows : 0, r_st = store ? j % rows : 0;
+        const float swv = store ? __ldg(swp + r_st) : 0.0f;
+        if (ok && u0 < u1) {
+            const unsigned char *st = smem + s * kGStageBytes;
+            const uint16_t *xb = reinterpret_cast<const uint16_t *>(st + xoff) + (g < M ? g : 0) * xk + 4 * t;
+            // shared row of fragment row g: in the tile form the two rows a
+            // quarter-warp reads are 4 apart, so their swizzled units fall in
+            // opposite halves of the 128-byte line (no bank conflict)
+            const int gr = tiles ? ((g >> 1) | ((g & 1) << 2)) : g;
+            const int cst = rb * 128;
+            // the run, one tile at a time: blocks [b, bend) of tile `tile`
+            for (int u = u0; u < u1;) {
+                const int tile = u / NB;
+                int b = u - tile * NB;
+                const int bend = min(u1 - tile * NB, NB);
+                u = tile * NB + bend;
+                const int rA = tile * 16 + gr, rB = rA + 8;
+                const bool hasA = rA < rb, hasB = rB < rb;
+                const unsigned char *pA = tiles ? st + rA * 128 : st + rA * ws + t * 16;
+                const unsigned char *pB = tiles ? st + rB * 128 : st + rB * ws + t * 16;
+                const int sw7 = rA & 7;          // = rB & 7
+                float acc[4][4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.0f;
+#pragma unroll 2
+                for (; b < bend; ++b) {
+                    const int off = tiles ? (b >> 1) * cst + (((((b & 1) << 2) | t) ^ sw7) << 4) : b * BB;
+                    const uint4 wa = hasA ? *reinterpret_cast<const uint4 *>(pA + off) : make_uint4(0, 0, 0, 0);
+                    const uint4 wb = hasB ? *reinterpret_cast<const uint4 *>(pB + off) : make_uint4(0, 0, 0, 0);
+                    const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w};
+                    const uint32_t B[4] = {wb.x, wb.y, wb.z, wb.w};
+                    const uint16_t *xblk = xb + b * KB;
+                    if constexpr (BITS == 8) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t a0, a1 = 0, a2, a3 = 0;
+                            widen_i8(A[q], a0, a2);
+                            if (hasB) widen_i8(B[q], a1, a3);
+                            const uint2 bv = *reinterpret_cast<const uint2 *>(xblk + q * 16);
+                            mma_bf16(acc[q], a0, a1, a2, a3, bv.x, bv.y);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t pa[4], pb[4] = {0, 0, 0, 0};
+                            widen_i4(A[q], pa);
+                            if (hasB) widen_i4(B[q], pb);
+                            const uint2 b0 = *reinterpret_cast<const uint2 *>(xblk + (2 * q) * 16);
+                            const uint2 b1 = *reinterpret_cast<const uint2 *>(xblk + (2 * q + 1) * 16);
+                            mma_bf16(acc[(2 * q) % 4], pa[0], pb[0], pa[1], pb[1], b0.x, b0.y);
+                            mma_bf16(acc[(2 * q + 1) % 4], pa[2], pb[2], pa[3], pb[3], b1.x, b1.y);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = tile * 16 + gr + 8 * h;
+                    if (row >= rb) continue;
+                    const float s0 = (acc[0][2 * h] + acc[1][2 * h]) + (acc[2][2 * h] + acc[3][2 * h]);
+                    const float s1 = (acc[0][2 * h + 1] + acc[1][2 * h + 1]) + (acc[2][2 * h + 1] + acc[3][2 * h + 1]);
+                    if (2 * t < M) rd[warp * kGRed + row * M + 2 * t] = s0;
+                    if (2 * t + 1 < M) rd[warp * kGRed + row * M + 2 * t + 1] = s1;
+                }
+            }
+        }
+        // shared reads of the stage end here; the next bulk copy into it is
+        // ordered after them by the proxy fence and the release below
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (consumers_sync_any(!ok)) {
+            if (threadIdx.x == 0) {
+                *abort_sh = 1;
+                atomicOr(p.status, kStatusGroupedTimeout);
+            }
+            break;
+        }
+        if (threadIdx.x == 0)
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8 * s) : "memory");
+        if (store) {
+            const int tile = r_st / 16;
+            float sum = 0.0f;
+            for (int w = 0; w < kGConsWarps; ++w) {
+                const int a = U * w / kGConsWarps, b = U * (w + 1) / kGConsWarps;
+                // warps whose (non-empty) run touches the row's tile wrote a partial
+                if (a < b && a < (tile + 1) * NB && b > tile * NB) sum += rd[w * kGRed + r_st * M + m_st];
+            }
+            const float yv = swv * sum;
+            const int64_t off = static_cast<int64_t>(m_st) * ldy + r_st;
+            if (p.ytype == 0)
+                static_cast<float *>(y)[off] = yv;
+            else
+                static_cast<uint16_t *>(y)[off] = f32_to_bf16_bits(yv);
+        }
+    }
+}
+
+}  // namespace
+
+// Rows of one work item for calls of these sizes: the largest multiple of 16
+// whose weight rows and the call's x' fit one stage (rows x tokens <= kGRed),
+// else 8, else 0 (the call cannot be grouped).
+int grouped_item_rows(int64_t M, int64_t K, int bits) {
+    if (M < 1 || M > TQ_MAX_M_GROUPED || K < 1) return 0;
+    const int64_t KB = bits == 8 ? 64 : 128;
+    const int64_t rbytes = K * bits / 8;
+    const int64_t ws = (rbytes + 127) / 128 * 128 + 64;
+    const int64_t xbytes = M * ((K + KB - 1) / KB * KB) * 2;
+    int64_t rb = (kGStageBytes - xbytes) / ws;
+    if (rb > kGRed / M) rb = kGRed / M;
+    return rb >= 16 ? static_cast<int>(rb / 16 * 16) : (rb >= 8 ? 8 : 0);
+}
+
+}  // namespace tq
+
+// The plan: where its tables and x' workspace sit in the caller's device
+// buffer, and what a run launches.
+struct tq_grouped_s {
+    int device;
+    int bits;
+    int ytype;
+    int grid;
+    int64_t ncalls;       // calls with work (M > 0 and N > 0)
+    int64_t nitems;
+    tq::GCall *calls;
+    tq::GItem *items;
+    int64_t weight_bytes;
+};
+
+namespace tq {
+
+namespace {
+
+struct GroupedTables {
+    std::vector<GCall> calls;
+    std::vector<GItem> items;
+    std::vector<CUtensorMap> maps;     // one per call in the tile form
+    size_t calls_bytes = 0, items_bytes = 0, maps_bytes = 0, x_bytes = 0;
+    int64_t weight_bytes = 0;
+    size_t total() const { return calls_bytes + items_bytes + maps_bytes + x_bytes; }
+};
+
+// Host tables of a plan, with x' and tensor-map addresses as offsets into
+// their areas.  `encode` false: sizes only (every short-row call counted in
+// the tile form).
+tq_status grouped_tables(const tq_a16_call *calls, int64_t n, int bits, int ytype, bool encode,
+                         GroupedTables &t) {
+    const int64_t KB = bits == 8 ? 64 : 128;
+    for (int64_t c = 0; c < n; ++c) {
+        const tq_a16_call &a = calls[c];
+        if (a.M == 0 || a.N == 0) continue;
+        const int rb = grouped_item_rows(a.M, a.K, bits);
+        if (rb == 0) return TQ_ERR_SHAPE;
+        GCall g{};
+        g.X = static_cast<const uint16_t *>(a.X);
+        g.ldx = a.ldx;
+        g.M = static_cast<int32_t>(a.M);
+        g.K = static_cast<int32_t>(a.K);
+        g.xk = static_cast<int32_t>((a.K + KB - 1) / KB * KB);
+        g.xq = reinterpret_cast<uint16_t *>(static_cast<uintptr_t>(t.x_bytes));
+        t.calls.push_back(g);
+        t.x_bytes += static_cast<size_t>(a.M) * g.xk * 2;     // a multiple of 128
+        const int64_t rbytes = a.K * bits / 8;
+        const int64_t ws = (rbytes + 127) / 128 * 128 + 64;
+        const int64_t nch = (rbytes + 127) / 128;
+        t.weight_bytes += a.N * rbytes + 4 * a.N;
+        // the tile form when its copies (one per 128-byte chunk) are fewer
+        // than the rows of an item
+        bool tiles = nch < rb;
+        const void *map_off = nullptr;
+        if (tiles) {
+            CUtensorMap m;
+            if (encode && !make_map_u8(&m, a.Wq, a.N, rbytes, 128, rb, CU_TENSOR_MAP_SWIZZLE_128B)) {
+                tiles = false;               // no encoder: rows instead
+            } else {
+                map_off = reinterpret_cast<const void *>(static_cast<uintptr_t>(t.maps.size() * sizeof(CUtensorMap)));
+                t.maps.push_back(m);
+            }
+        }
+        for (int64_t n0 = 0; n0 < a.N; n0 += rb) {
+            GItem it{};
+            it.w = static_cast<const uint8_t *>(a.Wq) + n0 * rbytes;
+            it.tmap = map_off;
+            it.n0 = static_cast<int32_t>(n0);
+            it.tiles = tiles ? 1 : 0;
+            it.xoff = static_cast<int32_t>(tiles ? nch * rb * 128 : rb * ws);
+            it.xq = g.xq;
+            it.sw = a.sw + n0;
+            it.y = static_cast<unsigned char *>(a.Y) + n0 * (ytype == 0 ? 4 : 2);
+            it.ldy = a.ldy;
+            it.rows = static_cast<int32_t>(a.N - n0 < rb ? a.N - n0 : rb);
+            it.rb = rb;
+            it.rbytes = static_cast<int32_t>(rbytes);
+            it.ws = static_cast<int32_t>(ws);
+            it.xk = g.xk;
+            it.M = static_cast<int16_t>(a.M);
+            t.items.push_back(it);
+        }
+    }
+    t.calls_bytes = (t.calls.size() * sizeof(GCall) + 255) / 256 * 256;
+    t.items_bytes = (t.items.size() * sizeof(GItem) + 255) / 256 * 256;
+    t.maps_bytes = (t.maps.size() * sizeof(CUtensorMap) + 255) / 256 * 256;
+    return TQ_OK;
+}
+
+}  // namespace
+
+tq_status grouped_bytes(const tq_a16_call *calls, int64_t n, int bits, size_t *bytes) {
+    GroupedTables t;
+    const tq_status st = grouped_tables(calls, n, bits, 0, false, t);
+    if (st == TQ_OK) *bytes = t.total();
+    return st;
+}
+
+tq_status grouped_create(const tq_a16_call *calls, int64_t n, int bits, int ytype, void *dmem,
+                         size_t dbytes, const DeviceInfo &dev, tq_grouped *out) {
+    GroupedTables t;
+    tq_status st = grouped_tables(calls, n, bits, ytype, true, t);
+    if (st != TQ_OK) return st;
+    if (t.total() > 0 && (!dmem || dbytes < t.total())) return TQ_ERR_WORKSPACE;
+    unsigned char *base = static_cast<unsigned char *>(dmem);
+    unsigned char *mbase = base + t.calls_bytes + t.items_bytes;
+    unsigned char *xbase = mbase + t.maps_bytes;
+    for (GCall &g : t.calls) g.xq = reinterpret_cast<uint16_t *>(xbase + reinterpret_cast<uintptr_t>(g.xq));
+    for (GItem &it : t.items) {
+        it.xq = reinterpret_cast<const uint16_t *>(xbase + reinterpret_cast<uintptr_t>(it.xq));
+        if (it.tiles) it.tmap = mbase + reinterpret_cast<uintptr_t>(it.tmap);
+    }
+    cudaError_t e = cudaSuccess;
+    if (!t.calls.empty()) e = cudaMemcpy(base, t.calls.data(), t.calls.size() * sizeof(GCall), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !t.items.empty())
+        e = cudaMemcpy(base + t.calls_bytes, t.items.data(), t.items.size() * sizeof(GItem),
+                       cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !t.maps.empty())
+        e = cudaMemcpy(mbase, t.maps.data(), t.maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e);
+    tq_grouped plan = new (std::nothrow) tq_grouped_s;
+    if (!plan) return TQ_ERR_WORKSPACE;
+    plan->device = dev.id;
+    plan->bits = bits;
+    plan->ytype = ytype;
+    plan->ncalls = static_cast<int64_t>(t.calls.size());
+    plan->nitems = static_cast<int64_t>(t.items.size());
+    plan->grid = static_cast<int>(plan->nitems < dev.sms ? plan->nitems : dev.sms);
+    plan->calls = reinterpret_cast<GCall *>(base);
+    plan->items = reinterpret_cast<GItem *>(base + t.calls_bytes);
+    plan->weight_bytes = t.weight_bytes;
+    *out = plan;
+    return TQ_OK;
+}
+
+tq_status grouped_run(tq_grouped plan, const DeviceInfo &dev, cudaStream_t s) {
+    if (plan->device != dev.id) return TQ_ERR_DEVICE;
+    if (plan->nitems == 0) return TQ_OK;
+    auto rot = plan->bits == 8 ? k_rotate_grouped<8> : k_rotate_grouped<4>;
+    auto kern = plan->bits == 8 ? k_gemv_grouped<8> : k_gemv_grouped<4>;
+    static int configured_for[64][2] = {{0}};
+    const int bi = plan->bits == 8 ? 0 : 1;
+    if (dev.id >= 0 && dev.id < 64 && !configured_for[dev.id][bi]) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem);
+        if (e != cudaSuccess) return cuda_fail(e);
+        configured_for[dev.id][bi] = 1;
+    }
+    unsigned int *status = status_word();
+    if (!status) return TQ_ERR_CUDA;
+    const int64_t rgrid = plan->ncalls < 65536 ? plan->ncalls : 65536;
+    rot<<<static_cast<unsigned>(rgrid), 256, 0, s>>>(plan->calls, plan->ncalls);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    GroupedParams p;
+    p.items = plan->items;
+    p.nitems = plan->nitems;
+    p.ytype = plan->ytype;
+    p.status = status;
+    kern<<<static_cast<unsigned>(plan->grid), kGThreads, kGSmem, s>>>(p);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+void grouped_destroy(tq_grouped plan) { delete plan; }
+
+int64_t grouped_weight_bytes(tq_grouped plan) { return plan->weight_bytes; }
+
+}  // namespace tq

@@ -26,7 +26,7 @@
 // Waits are bounded: on expiry the status word is set and the call's output
 // is left unwritten (tq_device_status reports it).
 
-#include "tq_internal.cuh"
+#include "tq_a16.cuh"
 
 namespace tq {
 namespace {
@@ -52,71 +52,8 @@ struct SmallParams {
     unsigned int *status;
 };
 
-constexpr long long kWaitLimit = 4000000000ll;  // clock cycles (about 2 s)
 constexpr unsigned int kStatusSmallTimeout = 4u;
 constexpr int NCH = 4;                          // accumulator chains per warp
-
-template <int BITS>
-__device__ __forceinline__ int xpos(int kl) {
-    if constexpr (BITS == 8) {
-        const int t = kl >> 4, q = (kl >> 2) & 3, r = kl & 3;
-        return q * 16 + 4 * t + (((r & 1) << 1) | (r >> 1));
-    } else {
-        const int t = kl >> 5, q = (kl >> 3) & 3, r = kl & 7;
-        const int jj = 2 * q + ((r >> 1) & 1);
-        return jj * 16 + 4 * t + ((r >> 2) | ((r & 1) << 1));
-    }
-}
-
-__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-// int8 codes (k0..k3) -> bf16 pairs (k0,k2), (k1,k3), exact.
-__device__ __forceinline__ void widen_i8(uint32_t x, uint32_t &p02, uint32_t &p13) {
-    p02 = bf16x2_sub((x & 0x007F007Fu) | 0x43004300u, (x & 0x00800080u) ^ 0x43004300u);
-    const uint32_t y = x >> 8;
-    p13 = bf16x2_sub((y & 0x007F007Fu) | 0x43004300u, (y & 0x00800080u) ^ 0x43004300u);
-}
-
-// int4 codes (k0..k7) -> bf16 pairs (k0,k4), (k1,k5), (k2,k6), (k3,k7), exact.
-__device__ __forceinline__ void widen_i4(uint32_t w, uint32_t (&p)[4]) {
-    const uint32_t c = 0x43084308u;
-    p[0] = bf16x2_sub((w & 0x000F000Fu) ^ c, c);
-    p[1] = bf16x2_sub(((w >> 4) & 0x000F000Fu) ^ c, c);
-    p[2] = bf16x2_sub(((w >> 8) & 0x000F000Fu) ^ c, c);
-    p[3] = bf16x2_sub(((w >> 12) & 0x000F000Fu) ^ c, c);
-}
-
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-    const long long t0 = clock64();
-    while (true) {
-        uint32_t ok;
-        asm volatile(
-            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            "selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if (clock64() - t0 > kWaitLimit) return false;
-    }
-}
 
 // PRE: every warp's K slice is at most one group (256 columns), so the warp's
 // weight fragments, widened to bf16 (16 MMA A-operands of 4 registers), fit in

@@ -3,6 +3,7 @@
 // oracle that checks it.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -69,6 +70,17 @@ tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M,
 // After the tiles (at byte tiled_act_tiles_bytes), a 256-byte trailer whose
 // first word is the largest sum of |codes| over the rows, word 1 + j the
 // largest such sum over an aligned window of 1024 << j columns (j < 5).
+bool make_map_u8(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int box_cols,
+                 int box_rows, CUtensorMapSwizzle swz);
+
+int grouped_item_rows(int64_t M, int64_t K, int bits);
+tq_status grouped_bytes(const tq_a16_call *calls, int64_t n, int bits, size_t *bytes);
+tq_status grouped_create(const tq_a16_call *calls, int64_t n, int bits, int ytype, void *dmem,
+                         size_t dbytes, const DeviceInfo &dev, tq_grouped *out);
+tq_status grouped_run(tq_grouped plan, const DeviceInfo &dev, cudaStream_t s);
+void grouped_destroy(tq_grouped plan);
+int64_t grouped_weight_bytes(tq_grouped plan);
+
 int64_t tiled_act_tiles_bytes(int64_t M, int64_t K);
 int64_t tiled_act_bytes(int64_t M, int64_t K);
 tq_status launch_rotate_quant_tiled(const uint16_t *X, int64_t M, int64_t K,

@@ -40,7 +40,18 @@ SIGNATURES = {
     "tq_act_tiled_bytes": (_Z, [_I, _I]),
     "tq_rotate_quant_act_tiled": (_C, [_P, _I, _I, _I, _P, _Z, _P, _P]),
     "tq_linear_tiled": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
+    "tq_grouped_bytes": (_C, [_P, _I, _C, ctypes.POINTER(ctypes.c_size_t)]),
+    "tq_grouped_create": (_C, [_P, _I, _C, _C, _P, _Z, ctypes.POINTER(ctypes.c_void_p)]),
+    "tq_grouped_run": (_C, [_P, _P]),
+    "tq_grouped_weight_bytes": (_I, [_P]),
+    "tq_grouped_destroy": (None, [_P]),
 }
+
+
+class A16Call(ctypes.Structure):
+    """``tq_a16_call``: one call of a grouped plan."""
+    _fields_ = [("X", _P), ("ldx", _I), ("Wq", _P), ("sw", _P), ("Y", _P), ("ldy", _I),
+                ("M", _I), ("N", _I), ("K", _I)]
 
 _lib = None
 
@@ -278,3 +289,67 @@ def linear_a8_static(X, Wq, sw, N: int, bits: int, Y, out: str = "f32", stream=N
 def device_status(stream=None) -> int:
     """Synchronise and return the library's device status (0 = TQ_OK)."""
     return int(lib().tq_device_status(_stream(stream)))
+
+
+def grouped_bytes(calls, bits: int) -> int:
+    """Device bytes a plan of these ``A16Call`` records needs."""
+    arr = (A16Call * max(len(calls), 1))(*calls)
+    out = ctypes.c_size_t(0)
+    _check(lib().tq_grouped_bytes(ctypes.addressof(arr), len(calls), bits, ctypes.byref(out)),
+           "tq_grouped_bytes")
+    return int(out.value)
+
+
+class GroupedPlan:
+    """Independent A16 calls run as one pass over their weights
+    (``tq_grouped_create`` / ``tq_grouped_run``).
+
+    ``calls`` is a list of ``(X, Wq, sw, N, Y)``: bf16 X [M, K] (M <= 8), the
+    codes and row scales of ``quantize_weights`` with ``bits``, and Y [M, N] of
+    dtype ``out``.  The plan keeps references to every tensor (their addresses
+    are in its tables) and owns the device buffer of its tables."""
+
+    def __init__(self, calls, bits: int, out: str = "f32"):
+        import torch
+        if out not in ("f32", "bf16"):
+            raise ValueError("a grouped plan writes f32 or bf16")
+        recs, keep, dev = [], [], None
+        for (X, Wq, sw, N, Y) in calls:
+            M, K = X.shape
+            _req(X, "X", dtype=torch.bfloat16, rows=M, cols=K)
+            _weights(Wq, sw, N, K, bits)
+            _req(Y, "Y", dtype=_dt(out), rows=M, cols=N)
+            dev = X.device if dev is None else dev
+            recs.append(A16Call(_ptr(X), X.stride(0), _ptr(Wq), _ptr(sw), _ptr(Y), Y.stride(0),
+                                M, N, K))
+            keep.extend([X, Wq, sw, Y])
+        need = grouped_bytes(recs, bits)
+        self.buffer = torch.empty(max(need, 1), dtype=torch.uint8,
+                                  device=dev if dev is not None else "cuda")
+        arr = (A16Call * max(len(recs), 1))(*recs)
+        h = ctypes.c_void_p(None)
+        _check(lib().tq_grouped_create(ctypes.addressof(arr), len(recs), bits, OUT[out],
+                                       _ptr(self.buffer), _nbytes(self.buffer), ctypes.byref(h)),
+               "tq_grouped_create")
+        self._h = h
+        self._keep = keep
+        self.bits = bits
+        self.ncalls = len(recs)
+
+    def run(self, stream=None):
+        if self._h is None:
+            raise ValueError("the plan is closed")
+        _check(lib().tq_grouped_run(self._h, _stream(stream)), "tq_grouped_run")
+
+    @property
+    def weight_bytes(self) -> int:
+        return int(lib().tq_grouped_weight_bytes(self._h)) if self._h is not None else 0
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and _lib is not None:
+            _lib.tq_grouped_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        self.close()
+

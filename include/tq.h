@@ -26,9 +26,10 @@
  *
  * Conventions for every entry point.
  *   - Every pointer is device memory owned by the caller (allocated, for
- *     example, by PyTorch).  The library never allocates or frees memory,
- *     never synchronises the host, and runs everything asynchronously on
- *     `stream` (0 = the legacy default stream).
+ *     example, by PyTorch).  The library never allocates or frees device
+ *     memory and runs everything asynchronously on `stream` (0 = the legacy
+ *     default stream).  Only the set-up call tq_grouped_create synchronises
+ *     the host (it copies its tables into the caller's buffer).
  *   - All checks (null pointers, shapes, strides, alignment, 64-bit size
  *     overflow, enum values) happen on the host before any launch; a refused
  *     call launches nothing and returns the status naming the reason.
@@ -248,6 +249,88 @@ tq_status tq_linear_a8_static(const void *X, int64_t M, int64_t K, int64_t ldx,
                               const void *Wq, const float *sw, int64_t N, int bits,
                               void *Y, tq_out ytype, int64_t ldy,
                               cudaStream_t stream);
+
+/*
+ * Grouped A16 product: many independent calls of tq_linear in mode TQ_W8A16
+ * or TQ_W4A16 run as one pass over their weights.
+ *
+ * Decode is bound by the weight stream (kvad-gpu internals, "Numbers"), but a
+ * call of a small model moves a few MB, and a call launched on its own must
+ * wait for the previous one before it reads its input: at that size the chain
+ * of waits, not the stream, sets the time.  Calls that do not depend on one
+ * another (the gate and up projections of a layer, or the calls of a batch of
+ * independent requests) can share one stream: the plan rotates every call's
+ * input once, then one CTA per SM streams the calls' weight rows through
+ * shared memory while the others compute.  The pages have no counterpart;
+ * the arithmetic of each call is that of tq_linear.
+ *
+ * Each call computes Y[m][n] = sw[n] * sum_k q_w[n][k] x'_bf16[m][k] with
+ * fp32 sums (same passages as tq_linear).  The order of the fp32 sums differs
+ * from tq_linear's, so the two agree to rounding, not bit for bit; a plan
+ * gives the same bytes on every run.
+ */
+
+/* Most token rows of one call in a grouped plan. */
+#define TQ_MAX_M_GROUPED 8
+
+/* One call of a grouped plan: the arguments of tq_linear in an A16 mode. */
+typedef struct {
+    const void *X;      /* bf16 [M, K], rules of tq_linear (16-byte aligned, ldx % 8 == 0) */
+    int64_t ldx;
+    const void *Wq;     /* codes from tq_quantize_weights with the plan's bits */
+    const float *sw;    /* fp32 [N] row scales */
+    void *Y;            /* [M, N] of the plan's output type, row m at Y + m * ldy */
+    int64_t ldy;
+    int64_t M, N, K;    /* 0 <= M <= TQ_MAX_M_GROUPED; M == 0 or N == 0: no work */
+} tq_a16_call;
+
+/* A plan (host handle; its device tables live in the caller's buffer). */
+typedef struct tq_grouped_s *tq_grouped;
+
+/*
+ * Bytes of device memory a plan of these calls needs (tables and the rotated
+ * inputs, about 64 bytes per 64 KB of weights plus 2 * M * K bytes per call).
+ * Refusals are those of tq_grouped_create (no device is needed).
+ */
+tq_status tq_grouped_bytes(const tq_a16_call *calls, int64_t ncalls, int bits, size_t *bytes);
+
+/*
+ * Checks every call and writes the plan's tables into `dmem`.
+ *   calls, ncalls  host array of the calls (copied; the array may be reused).
+ *   bits           8 (TQ_W8A16) or 4 (TQ_W4A16) for every call.
+ *   ytype          TQ_OUT_F32 or TQ_OUT_BF16 for every call.
+ *   dmem, dbytes   device buffer of at least tq_grouped_bytes(...) bytes,
+ *                  256-byte aligned, owned by the caller; it must outlive the
+ *                  plan and not be touched while the plan exists.
+ *   plan           receives the handle.
+ * Each call follows tq_linear's rules for X, Wq, sw, Y and its strides, with
+ * M <= TQ_MAX_M_GROUPED; in addition one work item (8 weight rows and the
+ * call's rotated input, 2 * M * K bytes, K rounded up to 64 for 8-bit and
+ * 128 for 4-bit weights) must fit 64 KB, or the call is refused with
+ * TQ_ERR_SHAPE (for M = 1: K up to 6400 with 8-bit weights, 10752 with
+ * 4-bit).  The calls' pointers are kept: their buffers must stay allocated at
+ * the same addresses while the plan is used.
+ * A set-up call: it copies its tables with cudaMemcpy (the host waits), so
+ * make it outside stream capture.  The device is the current one; runs on
+ * another device are refused.
+ */
+tq_status tq_grouped_create(const tq_a16_call *calls, int64_t ncalls, int bits, tq_out ytype,
+                            void *dmem, size_t dbytes, tq_grouped *plan);
+
+/*
+ * Runs every call of the plan on `stream` (two launches: the input rotation,
+ * then the product; capturable in a CUDA graph).  Requirements:
+ *   - the calls are independent: no call's Y overlaps any call's X, Wq, sw or
+ *     another call's Y;
+ *   - runs of one plan are ordered (they share the plan's rotated inputs).
+ */
+tq_status tq_grouped_run(tq_grouped plan, cudaStream_t stream);
+
+/* Algorithmic bytes one run streams: every call's weight codes and row scales. */
+int64_t tq_grouped_weight_bytes(tq_grouped plan);
+
+/* Frees the host handle (the device buffer stays the caller's).  NULL is ignored. */
+void tq_grouped_destroy(tq_grouped plan);
 
 #ifdef __cplusplus
 }

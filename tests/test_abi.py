@@ -149,3 +149,85 @@ def test_valid_call_without_a_gpu_reports_no_device(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert qw(L) == DEVICE
+
+
+# ------------------------------------------------------------------ grouped plans
+
+def gcalls(n=1, **kw):
+    from dit_convrot_linear_gb300.tq import A16Call
+    d = dict(X=FAKE, ldx=896, Wq=FAKE, sw=FAKE, Y=FAKE, ldy=4864, M=1, N=4864, K=896)
+    d.update(kw)
+    return [A16Call(**d) for _ in range(n)]
+
+
+def gbytes(L, calls, bits=8):
+    from dit_convrot_linear_gb300 import tq
+    arr = (tq.A16Call * max(len(calls), 1))(*calls)
+    out = ctypes.c_size_t(0)
+    rc = L.tq_grouped_bytes(ctypes.addressof(arr), len(calls), bits, ctypes.byref(out))
+    return rc, out.value
+
+
+def gcreate(L, calls, bits=8, ytype=0, dmem=FAKE, dbytes=1 << 20):
+    from dit_convrot_linear_gb300 import tq
+    arr = (tq.A16Call * max(len(calls), 1))(*calls)
+    h = ctypes.c_void_p(None)
+    rc = L.tq_grouped_create(ctypes.addressof(arr), len(calls), bits, ytype, dmem, dbytes,
+                             ctypes.byref(h))
+    return rc, h
+
+
+def test_grouped_refusals(L):
+    assert gbytes(L, gcalls(), bits=5)[0] == BITS
+    assert gbytes(L, gcalls(M=9))[0] == SHAPE             # above TQ_MAX_M_GROUPED
+    assert gbytes(L, gcalls(K=96))[0] == SHAPE            # K not 256q + {0, 32, 64, 128}
+    assert gbytes(L, gcalls(X=0))[0] == NULL
+    assert gbytes(L, gcalls(sw=0))[0] == NULL
+    assert gbytes(L, gcalls(X=FAKE + 2))[0] == ALIGN
+    assert gbytes(L, gcalls(ldx=900))[0] == ALIGN          # row stride not a multiple of 8
+    assert gbytes(L, gcalls(ldy=100))[0] == SHAPE          # ldy < N
+    assert gbytes(L, gcalls(Wq=FAKE + 8))[0] == ALIGN
+    assert gbytes(L, gcalls(K=12288, ldx=12288))[0] == SHAPE      # 8 rows + x' exceed a stage
+    assert gbytes(L, gcalls(M=8, K=4864, ldx=4864))[0] == SHAPE   # x' of 8 tokens too long
+    assert gbytes(L, gcalls(K=12288, ldx=12288), bits=4)[0] == SHAPE
+    assert gbytes(L, gcalls(K=6400, ldx=6400))[0] == OK           # the longest 8-bit K for M = 1
+    assert gbytes(L, gcalls(K=6432, ldx=6432))[0] == SHAPE
+    assert gbytes(L, gcalls(K=10752, ldx=10752), bits=4)[0] == OK  # and 4-bit
+    assert gbytes(L, gcalls(K=10784, ldx=10784), bits=4)[0] == SHAPE
+    # an empty call is skipped before its pointers are looked at
+    assert gbytes(L, gcalls(M=0, X=0, Wq=0)) == (OK, 0)
+    assert gbytes(L, []) == (OK, 0)
+    assert L.tq_grouped_bytes(FAKE, -1, 8, ctypes.byref(ctypes.c_size_t(0))) == SHAPE
+    # create: the call checks, then the buffer, all before any device work
+    assert gcreate(L, gcalls(M=9))[0] == SHAPE
+    assert gcreate(L, gcalls(), ytype=2)[0] == MODE        # i32 is not an A16 output
+    assert gcreate(L, gcalls(), dbytes=100)[0] == WORKSPACE
+    assert gcreate(L, gcalls(), dmem=0)[0] == WORKSPACE
+    assert gcreate(L, gcalls(), dmem=FAKE + 16)[0] == ALIGN
+    assert L.tq_grouped_create(FAKE, 1, 8, 0, FAKE, 1 << 20, None) == NULL
+    assert L.tq_grouped_run(None, S0) == NULL
+    assert L.tq_grouped_weight_bytes(None) == 0
+    L.tq_grouped_destroy(None)
+
+
+def test_grouped_bytes_count_tables_and_rotated_inputs(L):
+    # M = 1, K = 896, N = 4864, 8-bit: items of 64 rows (960-byte shared rows,
+    # 1792 bytes of x' per item) -> 76 items of 80 bytes (6080, rounded to
+    # 6144); one 40-byte call record and one 128-byte tensor map (rows of 7
+    # chunks of 128 bytes: the tile form), each rounded to 256; x' of 896 bf16
+    assert gbytes(L, gcalls()) == (OK, 256 + 6144 + 256 + 896 * 2)
+    # two tokens, K = 544 (x' padded to 640 columns), N = 100, 4-bit: two
+    # items of 64 rows, tile form
+    calls = gcalls(M=2, N=100, K=544, ldx=544, ldy=100)
+    assert gbytes(L, calls, bits=4) == (OK, 256 + 256 + 256 + 2 * 640 * 2)
+    # long rows (K = 4864: 38 chunks, items of 8 rows) stay in the row form:
+    # no tensor map; 112 items of 80 bytes
+    calls = gcalls(N=896, K=4864, ldx=4864, ldy=896)
+    assert gbytes(L, calls) == (OK, 256 + 8960 + 4864 * 2)
+
+
+def test_grouped_create_without_a_gpu_reports_no_device(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert gcreate(L, gcalls())[0] == DEVICE
