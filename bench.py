@@ -5,9 +5,12 @@ Metric: weight GB/s at M = 1 (decode) and TOPS at M = 4032 (DiT W8A8), each
 as a fraction of the measured roofline.  The headline line is the decode
 workload: a Qwen2.5-0.5B-like FFN (gate/up 896 -> 4864, down 4864 -> 896),
 1000 seeded calls cycling gate, up, down through enough layer sets that the
-distinct weights exceed three times L2; one step = the 1000 calls (replayed as
-one CUDA graph).  The W4A16 decode and the M = 4032 W8A8 DiT projections are
-reported beside it in the same JSON line.
+distinct weights exceed three times L2.  One step = the 1000 calls.  The calls
+are independent (each has its own input and output), so a step runs them as
+one grouped plan (tq_grouped_run: an input-rotation launch and one product
+launch streaming every call's weights); the same calls launched one by one
+(a CUDA graph of 1000 tq_linear launches) are reported beside it, as are the
+W4A16 decode and the M = 4032 W8A8 DiT projections.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
@@ -39,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--calls", type=int, default=1000)
@@ -101,10 +104,16 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        # start timing only once the sampler is writing
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < 5.0:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
         return self
 
     def __exit__(self, *exc):
@@ -264,6 +273,21 @@ class Decode:
         self.x_dev.copy_(self.x_host, non_blocking=True)
         self.gplan.run()
         self.y_host.copy_(self.y_dev, non_blocking=True)
+
+    def product_ms(self, reps):
+        """Mean duration of the product launch alone (CUDA events on the
+        stream it runs on), each after its own rotation launch."""
+        import torch
+        evs = []
+        for _ in range(reps):
+            self.gplan.rotate()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            self.gplan.product()
+            e1.record()
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
 
     def step(self):
         self.graph.replay()
@@ -460,32 +484,42 @@ def main():
                               "gemm_only_tops": round(gemm_tops, 2), "per_gemm": per}))
         return 0
 
-    # headline: decode W8A16
+    # headline: decode W8A16.  The 1000 calls are independent (each has its
+    # own input and output), so they run as one grouped plan: a rotation
+    # launch and one product launch that streams every call's weights.  The
+    # same calls launched one by one (a CUDA graph of 1000 launches) are
+    # reported beside it.
     dec8 = Decode(8, args.calls, device, l2)
-    dec8.capture()
+    dec8.make_grouped()
     with Clocks(local) as clk:
-        ms = time_steps(dec8.step, args.steps, args.warmup, world)
+        ms = time_steps(dec8.step_grouped, args.steps, args.warmup, world)
     clocks = clk.summary()
     ms_step = ms / args.steps
     gbs = dec8.weight_bytes / (ms_step * 1e-3) / 1e9 * world
-    per_launch_us = ms_step * 1e3 / args.calls
-    bytes_per_launch = dec8.weight_bytes / args.calls
-    achieved = bytes_per_launch / (per_launch_us * 1e-6) / 1e9
     hbm = float(pk["hbm_gbs"])
-    # the timed graph runs two kernels: gate/up calls k_gemv_small (weights
-    # widened in registers before the dependency wait), down calls k_gemv_rows8
-    dec_kernels = "k_gemv_small<8> (gate, up) + k_gemv_rows8<8> (down)"
-    traffic = traffic_for(dec_kernels, ["k_gemv_small.cu", "tq_internal.cuh"])
-    roof = {"bound": "hbm", "kernel": dec_kernels, "achieved": round(achieved, 1),
+    prod_ms = dec8.product_ms(max(3, args.steps))
+    achieved = dec8.weight_bytes / (prod_ms * 1e-3) / 1e9
+    dec_kernel = "k_gemv_grouped<8>"
+    traffic = traffic_for(dec_kernel, ["k_gemv_grouped.cu", "tq_a16.cuh", "tq_internal.cuh"])
+    roof = {"bound": "hbm", "kernel": dec_kernel, "achieved": round(achieved, 1),
             "peak": hbm, "peak_kind": f"{pk_kind} HBM copy", "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "traffic": traffic,
-            "bytes_per_launch_algorithmic": round(bytes_per_launch, 1)}
-    iso8 = dec8.isolated_call_us()
-    ms_e2e = time_steps(dec8.step_e2e, max(1, args.steps // 2), 2, world) / max(1, args.steps // 2)
+            "bytes_per_launch_algorithmic": dec8.weight_bytes,
+            "launch_ms": round(prod_ms, 4),
+            "step_kernels": "k_rotate_grouped<8> (inputs) + k_gemv_grouped<8> (product)"}
+    ms_e2e = time_steps(dec8.step_grouped_e2e, max(1, args.steps // 2), 2, world) / max(1, args.steps // 2)
     e2e = {"value": round(dec8.weight_bytes / (ms_e2e * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
            "h2d_bytes_per_step": dec8.x_host.numel() * 2,
            "d2h_bytes_per_step": dec8.y_host.numel() * 4}
-    launches = args.steps * args.calls
+    launches = args.steps * 2
+    # the same calls, one launch each
+    dec8.capture()
+    ms_pc = time_steps(dec8.step, args.steps, args.warmup, world) / args.steps
+    a_pc = dec8.weight_bytes / (ms_pc * 1e-3) / 1e9
+    per_call = {"value": round(a_pc * world, 1), "unit": "GB/s", "ms_per_step": round(ms_pc, 4),
+                "frac": round(a_pc / hbm, 4), "launches_per_step": args.calls,
+                "kernels": "k_gemv_small<8> (gate, up) + k_gemv_rows8<8> (down)",
+                "isolated_call_us": round(dec8.isolated_call_us(), 2)}
     del dec8
     torch.cuda.empty_cache()
 
@@ -497,12 +531,20 @@ def main():
         if args.only == "decode":
             raise RuntimeError("skipped (--only decode)")
         dec4 = Decode(4, args.calls, device, l2)
-        dec4.capture()
-        ms4 = time_steps(dec4.step, args.steps, args.warmup, world) / args.steps
+        dec4.make_grouped()
+        ms4 = time_steps(dec4.step_grouped, args.steps, args.warmup, world) / args.steps
         a4 = dec4.weight_bytes / (ms4 * 1e-3) / 1e9
+        p4 = dec4.product_ms(max(3, args.steps))
+        dec4.capture()
+        ms4pc = time_steps(dec4.step, args.steps, args.warmup, world) / args.steps
+        a4pc = dec4.weight_bytes / (ms4pc * 1e-3) / 1e9
         extra["decode_w4a16"] = {"value": round(a4 * world, 1), "unit": "GB/s",
                                  "ms_per_step": round(ms4, 4), "frac": round(a4 / hbm, 4),
-                                 "isolated_call_us": round(dec4.isolated_call_us(), 2),
+                                 "kernel": "k_gemv_grouped<4>",
+                                 "kernel_frac": round(dec4.weight_bytes / (p4 * 1e-3) / 1e9 / hbm, 4),
+                                 "per_call": {"value": round(a4pc * world, 1), "ms_per_step": round(ms4pc, 4),
+                                              "frac": round(a4pc / hbm, 4),
+                                              "isolated_call_us": round(dec4.isolated_call_us(), 2)},
                                  "layers": dec4.layers,
                                  "distinct_weight_mb": round(dec4.distinct_bytes / 2 ** 20, 1)}
         del dec4
@@ -543,9 +585,10 @@ def main():
             "config": {"workload": "decode M=1 W8A16, Qwen2.5-0.5B-like FFN (gate/up 896->4864, "
                                    "down 4864->896), 1000 seeded calls cycling gate, up, down",
                        "calls_per_step": args.calls,
+                       "execution": "the independent calls as one grouped plan (2 launches per step)",
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clocks, "isolated_call_us": round(iso8, 2), **extra,
+            "clocks": clocks, "decode_w8a16_per_call": per_call, **extra,
         }
         line["config"]["l2"] = (f"inputs larger than L2 ({l2 / 2 ** 20:.0f} MB): "
                                 f"{decode_layers(8, l2)} layer sets of weights cycled per step")

@@ -22,6 +22,8 @@
 // Every wait is bounded: on expiry the status word is set, the CTA stops, and
 // the outputs of the items it had not finished are left unwritten.
 
+#include <cuda_fp16.h>
+
 #include <new>
 #include <vector>
 
@@ -74,6 +76,7 @@ constexpr int kGHdrOff = kGRedOff + 2 * kGConsWarps * kGRed * 4;
 constexpr int kGBarOff = kGHdrOff + kGStages * 128;
 constexpr int kGSmem = kGBarOff + 2 * kGStages * 8 + 16 + 1024;   // + alignment of the stages
 constexpr unsigned int kStatusGroupedTimeout = 16u;
+constexpr int kXTail = 32;     // bytes after a call's x' rows: a float 2^-e per token
 
 struct GroupedParams {
     const GItem *items;
@@ -96,6 +99,86 @@ __device__ __forceinline__ bool consumers_sync_any(bool pred) {
     return r != 0;
 }
 
+// Wait with the thread suspended in the barrier between polls (up to ~1 us a
+// poll, woken early when the phase completes): no issue slots spent spinning.
+__device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+            "selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(1000u)
+            : "memory");
+        if (ok) return true;
+        if (clock64() - t0 > kA16WaitLimit) return false;
+    }
+}
+
+// One K block (64 bytes of each of the lane's two rows) into the four
+// accumulator chains.  HASB false: rows g + 8 do not exist (an 8-row item).
+template <int BITS, bool HASB>
+__device__ __forceinline__ void block_mma(float (&acc)[4][4], const unsigned char *pa,
+                                          const unsigned char *pb, const uint16_t *xblk) {
+    const uint4 wa = *reinterpret_cast<const uint4 *>(pa);
+    const uint4 wb = HASB ? *reinterpret_cast<const uint4 *>(pb) : make_uint4(0, 0, 0, 0);
+    const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w};
+    const uint32_t B[4] = {wb.x, wb.y, wb.z, wb.w};
+    if constexpr (BITS == 8) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t a0, a1 = 0, a2, a3 = 0;
+            widen_i8_f16(A[q], a0, a2);
+            if (HASB) widen_i8_f16(B[q], a1, a3);
+            const uint2 bv = *reinterpret_cast<const uint2 *>(xblk + q * 16);
+            mma_f16(acc[q], a0, a1, a2, a3, bv.x, bv.y);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t pa4[4], pb4[4] = {0, 0, 0, 0};
+            widen_i4_f16(A[q], pa4);
+            if (HASB) widen_i4_f16(B[q], pb4);
+            const uint2 b0 = *reinterpret_cast<const uint2 *>(xblk + (2 * q) * 16);
+            const uint2 b1 = *reinterpret_cast<const uint2 *>(xblk + (2 * q + 1) * 16);
+            mma_f16(acc[(2 * q) % 4], pa4[0], pb4[0], pa4[1], pb4[1], b0.x, b0.y);
+            mma_f16(acc[(2 * q + 1) % 4], pa4[2], pb4[2], pa4[3], pb4[3], b1.x, b1.y);
+        }
+    }
+}
+
+// Blocks [b, bend) of one 16-row tile: fragment rows at pA (rows g) and pB
+// (rows g + 8), x' of the lane at xb.  TILES: the tile form (chunks of two
+// blocks cst bytes apart; the lane's 16-byte unit of an even / odd block at
+// offE / offO within its swizzled row line); else rows of 64-byte blocks.
+// Blocks go in pairs, so each step has two blocks' loads in flight.
+template <int BITS, bool TILES, bool HASB>
+__device__ __forceinline__ void tile_blocks(float (&acc)[4][4], const unsigned char *pA,
+                                            const unsigned char *pB, const uint16_t *xb, int b,
+                                            int bend, int cst, int offE, int offO) {
+    constexpr int KB = BITS == 8 ? 64 : 128;   // k per block
+    auto off = [&](int blk) { return TILES ? (blk >> 1) * cst + ((blk & 1) ? offO : offE) : blk * 64; };
+    if (TILES && b < bend && (b & 1)) {        // a run that starts on an odd block
+        block_mma<BITS, HASB>(acc, pA + off(b), pB + off(b), xb + b * KB);
+        ++b;
+    }
+    for (; b + 1 < bend; b += 2) {
+        const int o0 = TILES ? (b >> 1) * cst + offE : b * 64;
+        const int o1 = TILES ? o0 - offE + offO : o0 + 64;
+        block_mma<BITS, HASB>(acc, pA + o0, pB + o0, xb + b * KB);
+        block_mma<BITS, HASB>(acc, pA + o1, pB + o1, xb + (b + 1) * KB);
+    }
+    if (b < bend) block_mma<BITS, HASB>(acc, pA + off(b), pB + off(b), xb + b * KB);
+}
+
+// x' of one call, in the order the product's lanes read it, as fp16: token
+// row m (warp m) is the bf16 rounding of the rotated row (the A16 operand),
+// times 2^e with e chosen so that its largest magnitude lies in [2^14, 2^15).
+// The multiplication by a power of two is exact, and so is the fp16 form of
+// every value not below 2^-31 of that largest one (smaller ones keep an
+// absolute error under 2^-39 of it).  The product multiplies Y by 2^-e, read
+// from the float after the M fp16 rows.
 template <int BITS>
 __global__ void __launch_bounds__(256)
 k_rotate_grouped(const GCall *calls, int64_t ncalls) {
@@ -103,29 +186,44 @@ k_rotate_grouped(const GCall *calls, int64_t ncalls) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int64_t c = blockIdx.x; c < ncalls; c += gridDim.x) {
         const GCall cl = calls[c];
+        if (warp >= cl.M) continue;
         const int G = (cl.K + kGroup - 1) / kGroup;
-        for (int job = warp; job < cl.M * G; job += 8) {
-            const int m = job / G, gi = job % G;
+        const uint16_t *xrow = cl.X + warp * cl.ldx;
+        uint16_t *row = cl.xq + static_cast<int64_t>(warp) * cl.xk;
+        float amax = 0.0f;
+        for (int gi = 0; gi < G; ++gi) {
             const int64_t gk = static_cast<int64_t>(gi) * kGroup;
             const int n = group_width(cl.K, gk);
-            const int E = n / 32;
-            const uint4 raw = load_group_raw(cl.X + m * cl.ldx + gk + lane * E, E);
             float v[8];
-            fwht_group_raw(raw, n, v);
-            uint16_t *row = cl.xq + static_cast<int64_t>(m) * cl.xk;
+            const int E = fwht_group_raw(load_group_raw(xrow + gk + lane * (n / 32), n / 32), n, v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (e < E) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(f32_to_bf16_bits(v[e]))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        int ex = 0;
+        if (amax > 0.0f) frexpf(amax, &ex);              // amax = f * 2^ex, f in [0.5, 1)
+        const int sh = amax > 0.0f ? max(-100, min(100, 15 - ex)) : 0;
+        const float up = ldexpf(1.0f, sh);
+        for (int gi = 0; gi < G; ++gi) {
+            const int64_t gk = static_cast<int64_t>(gi) * kGroup;
+            const int n = group_width(cl.K, gk);
+            float v[8];
+            const int E = fwht_group_raw(load_group_raw(xrow + gk + lane * (n / 32), n / 32), n, v);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 if (e < E) {
                     const int kl = static_cast<int>(gk) + lane * E + e;
-                    row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = f32_to_bf16_bits(v[e]);
+                    const float xb = bf16_bits_to_f32(f32_to_bf16_bits(v[e]));
+                    row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = __half_as_ushort(__float2half_rn(xb * up));
                 }
             }
         }
-        const int padw = cl.xk - cl.K;   // zeros after K, up to the block edge
-        for (int idx = threadIdx.x; idx < cl.M * padw; idx += blockDim.x) {
-            const int m = idx / padw, kl = cl.K + idx % padw;
-            cl.xq[static_cast<int64_t>(m) * cl.xk + (kl / KB) * KB + xpos<BITS>(kl % KB)] = 0;
-        }
+        for (int kl = cl.K + lane; kl < cl.xk; kl += 32)   // zeros after K, up to the block edge
+            row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = 0;
+        if (lane == 0)
+            reinterpret_cast<float *>(cl.xq + static_cast<int64_t>(cl.M) * cl.xk)[warp] = ldexpf(1.0f, -sh);
     }
 }
 
@@ -136,7 +234,6 @@ k_gemv_grouped(const GroupedParams p) {
     // stages on a 1024-byte boundary (the tensor copies' 128-byte swizzle)
     unsigned char *smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     constexpr int KB = BITS == 8 ? 64 : 128;   // k per block (16 bytes per lane)
-    constexpr int BB = 64;                     // weight bytes per row per block
     float *red = reinterpret_cast<float *>(smem + kGRedOff);
     unsigned char *hdr = smem + kGHdrOff;      // stage headers, 128 bytes apart
     const uint32_t full0 = smem_addr(smem + kGBarOff);
@@ -171,7 +268,7 @@ k_gemv_grouped(const GroupedParams p) {
             const int s = static_cast<int>(k % kGStages);
             const int64_t u = k / kGStages;
             bool ok = true;
-            if (lane == 0 && u > 0) ok = mbar_wait_bounded(empty0 + 8 * s, static_cast<uint32_t>((u - 1) & 1));
+            if (lane == 0 && u > 0) ok = mbar_wait_suspend(empty0 + 8 * s, static_cast<uint32_t>((u - 1) & 1));
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0) {
@@ -185,7 +282,7 @@ k_gemv_grouped(const GroupedParams p) {
             const int nch = (it.rbytes + 127) / 128;
             if (lane == 0) {
                 *reinterpret_cast<GItem *>(hdr + s * 128) = it;
-                const uint32_t xbytes = static_cast<uint32_t>(it.M) * it.xk * 2;
+                const uint32_t xbytes = static_cast<uint32_t>(it.M) * it.xk * 2 + kXTail;
                 // a tensor copy counts its whole box, zero fill included
                 const uint32_t wbytes = it.tiles ? static_cast<uint32_t>(nch * it.rb * 128)
                                                  : static_cast<uint32_t>(it.rows * it.rbytes);
@@ -238,7 +335,7 @@ k_gemv_grouped(const GroupedParams p) {
         const int64_t i = blockIdx.x + k * grid;
         if (i >= p.nitems) break;
         const int s = static_cast<int>(k % kGStages);
-        const bool ok = mbar_wait_bounded(full0 + 8 * s, static_cast<uint32_t>((k / kGStages) & 1));
+        const bool ok = mbar_wait_suspend(full0 + 8 * s, static_cast<uint32_t>((k / kGStages) & 1));
         float *rd = red + (k & 1) * kGConsWarps * kGRed;
         // the header is read before the stage is released
         int rows = 0, rb = 0, ws = 0, xk = KB, M = 1, xoff = 0;
@@ -261,10 +358,16 @@ k_gemv_grouped(const GroupedParams p) {
         }
         const int NB = xk / KB, U = ((rb + 15) / 16) * NB;
         const int u0 = U * warp / kGConsWarps, u1 = U * (warp + 1) / kGConsWarps;
+        // thread j < rows * M adds the partial sums of output (row j % rows,
+        // token j / rows) after the barrier: the first warps do it while the
+        // others already multiply the next item
         const int j = threadIdx.x;
         const bool store = ok && j < rows * M;
         const int m_st = store ? j / rows : 0, r_st = store ? j % rows : 0;
         const float swv = store ? __ldg(swp + r_st) : 0.0f;
+        // the token's 2^-e (after the x' rows), read before the stage is released
+        const float dsc = store ? reinterpret_cast<const float *>(smem + s * kGStageBytes + xoff + M * xk * 2)[m_st]
+                                : 1.0f;
         if (ok && u0 < u1) {
             const unsigned char *st = smem + s * kGStageBytes;
             const uint16_t *xb = reinterpret_cast<const uint16_t *>(st + xoff) + (g < M ? g : 0) * xk + 4 * t;
@@ -279,43 +382,23 @@ k_gemv_grouped(const GroupedParams p) {
                 int b = u - tile * NB;
                 const int bend = min(u1 - tile * NB, NB);
                 u = tile * NB + bend;
+                // rows g always exist (rb is a multiple of 8); rows g + 8 unless
+                // the item has 8 rows
                 const int rA = tile * 16 + gr, rB = rA + 8;
-                const bool hasA = rA < rb, hasB = rB < rb;
+                const bool hasB = rB < rb;
                 const unsigned char *pA = tiles ? st + rA * 128 : st + rA * ws + t * 16;
                 const unsigned char *pB = tiles ? st + rB * 128 : st + rB * ws + t * 16;
                 const int sw7 = rA & 7;          // = rB & 7
+                const int offE = (t ^ sw7) << 4, offO = ((4 | t) ^ sw7) << 4;
                 float acc[4][4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.0f;
-#pragma unroll 2
-                for (; b < bend; ++b) {
-                    const int off = tiles ? (b >> 1) * cst + (((((b & 1) << 2) | t) ^ sw7) << 4) : b * BB;
-                    const uint4 wa = hasA ? *reinterpret_cast<const uint4 *>(pA + off) : make_uint4(0, 0, 0, 0);
-                    const uint4 wb = hasB ? *reinterpret_cast<const uint4 *>(pB + off) : make_uint4(0, 0, 0, 0);
-                    const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w};
-                    const uint32_t B[4] = {wb.x, wb.y, wb.z, wb.w};
-                    const uint16_t *xblk = xb + b * KB;
-                    if constexpr (BITS == 8) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t a0, a1 = 0, a2, a3 = 0;
-                            widen_i8(A[q], a0, a2);
-                            if (hasB) widen_i8(B[q], a1, a3);
-                            const uint2 bv = *reinterpret_cast<const uint2 *>(xblk + q * 16);
-                            mma_bf16(acc[q], a0, a1, a2, a3, bv.x, bv.y);
-                        }
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t pa[4], pb[4] = {0, 0, 0, 0};
-                            widen_i4(A[q], pa);
-                            if (hasB) widen_i4(B[q], pb);
-                            const uint2 b0 = *reinterpret_cast<const uint2 *>(xblk + (2 * q) * 16);
-                            const uint2 b1 = *reinterpret_cast<const uint2 *>(xblk + (2 * q + 1) * 16);
-                            mma_bf16(acc[(2 * q) % 4], pa[0], pb[0], pa[1], pb[1], b0.x, b0.y);
-                            mma_bf16(acc[(2 * q + 1) % 4], pa[2], pb[2], pa[3], pb[3], b1.x, b1.y);
-                        }
-                    }
+                if (tiles) {
+                    if (hasB) tile_blocks<BITS, true, true>(acc, pA, pB, xb, b, bend, cst, offE, offO);
+                    else tile_blocks<BITS, true, false>(acc, pA, pB, xb, b, bend, cst, offE, offO);
+                } else {
+                    if (hasB) tile_blocks<BITS, false, true>(acc, pA, pB, xb, b, bend, cst, offE, offO);
+                    else tile_blocks<BITS, false, false>(acc, pA, pB, xb, b, bend, cst, offE, offO);
                 }
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -341,14 +424,14 @@ k_gemv_grouped(const GroupedParams p) {
         if (threadIdx.x == 0)
             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8 * s) : "memory");
         if (store) {
-            const int tile = r_st / 16;
+            const int tile = r_st >> 4;
             float sum = 0.0f;
             for (int w = 0; w < kGConsWarps; ++w) {
-                const int a = U * w / kGConsWarps, b = U * (w + 1) / kGConsWarps;
                 // warps whose (non-empty) run touches the row's tile wrote a partial
+                const int a = U * w / kGConsWarps, b = U * (w + 1) / kGConsWarps;
                 if (a < b && a < (tile + 1) * NB && b > tile * NB) sum += rd[w * kGRed + r_st * M + m_st];
             }
-            const float yv = swv * sum;
+            const float yv = swv * (dsc * sum);
             const int64_t off = static_cast<int64_t>(m_st) * ldy + r_st;
             if (p.ytype == 0)
                 static_cast<float *>(y)[off] = yv;
@@ -368,7 +451,7 @@ int grouped_item_rows(int64_t M, int64_t K, int bits) {
     const int64_t KB = bits == 8 ? 64 : 128;
     const int64_t rbytes = K * bits / 8;
     const int64_t ws = (rbytes + 127) / 128 * 128 + 64;
-    const int64_t xbytes = M * ((K + KB - 1) / KB * KB) * 2;
+    const int64_t xbytes = M * ((K + KB - 1) / KB * KB) * 2 + kXTail;
     int64_t rb = (kGStageBytes - xbytes) / ws;
     if (rb > kGRed / M) rb = kGRed / M;
     return rb >= 16 ? static_cast<int>(rb / 16 * 16) : (rb >= 8 ? 8 : 0);
@@ -422,7 +505,7 @@ tq_status grouped_tables(const tq_a16_call *calls, int64_t n, int bits, int ytyp
         g.xk = static_cast<int32_t>((a.K + KB - 1) / KB * KB);
         g.xq = reinterpret_cast<uint16_t *>(static_cast<uintptr_t>(t.x_bytes));
         t.calls.push_back(g);
-        t.x_bytes += static_cast<size_t>(a.M) * g.xk * 2;     // a multiple of 128
+        t.x_bytes += static_cast<size_t>(a.M) * g.xk * 2 + kXTail;   // a multiple of 32
         const int64_t rbytes = a.K * bits / 8;
         const int64_t ws = (rbytes + 127) / 128 * 128 + 64;
         const int64_t nch = (rbytes + 127) / 128;
@@ -512,7 +595,8 @@ tq_status grouped_create(const tq_a16_call *calls, int64_t n, int bits, int ytyp
     return TQ_OK;
 }
 
-tq_status grouped_run(tq_grouped plan, const DeviceInfo &dev, cudaStream_t s) {
+// phase 1: the rotation pre-pass; 2: the product; 3: both
+tq_status grouped_run(tq_grouped plan, const DeviceInfo &dev, int phase, cudaStream_t s) {
     if (plan->device != dev.id) return TQ_ERR_DEVICE;
     if (plan->nitems == 0) return TQ_OK;
     auto rot = plan->bits == 8 ? k_rotate_grouped<8> : k_rotate_grouped<4>;
@@ -526,18 +610,23 @@ tq_status grouped_run(tq_grouped plan, const DeviceInfo &dev, cudaStream_t s) {
     }
     unsigned int *status = status_word();
     if (!status) return TQ_ERR_CUDA;
-    const int64_t rgrid = plan->ncalls < 65536 ? plan->ncalls : 65536;
-    rot<<<static_cast<unsigned>(rgrid), 256, 0, s>>>(plan->calls, plan->ncalls);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e);
-    GroupedParams p;
-    p.items = plan->items;
-    p.nitems = plan->nitems;
-    p.ytype = plan->ytype;
-    p.status = status;
-    kern<<<static_cast<unsigned>(plan->grid), kGThreads, kGSmem, s>>>(p);
-    e = cudaGetLastError();
-    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+    if (phase & 1) {
+        const int64_t rgrid = plan->ncalls < 65536 ? plan->ncalls : 65536;
+        rot<<<static_cast<unsigned>(rgrid), 256, 0, s>>>(plan->calls, plan->ncalls);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (phase & 2) {
+        GroupedParams p;
+        p.items = plan->items;
+        p.nitems = plan->nitems;
+        p.ytype = plan->ytype;
+        p.status = status;
+        kern<<<static_cast<unsigned>(plan->grid), kGThreads, kGSmem, s>>>(p);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return TQ_OK;
 }
 
 void grouped_destroy(tq_grouped plan) { delete plan; }

@@ -52,6 +52,43 @@ __device__ __forceinline__ void widen_i4(uint32_t w, uint32_t (&p)[4]) {
     p[3] = bf16x2_sub(((w >> 12) & 0x000F000Fu) ^ c, c);
 }
 
+// fp16 forms of the widening, for products whose x' is fp16:
+//   int8 codes (k0..k3) -> fp16 pairs (k0,k2), (k1,k3): the byte u = b ^ 0x80
+//   under exponent 0x64 is 1024 + u exactly, minus 1152 is b;
+//   int4 codes (k0..k7) -> fp16 pairs (k0,k4), (k1,k5), (k2,k6), (k3,k7):
+//   0x6400 | (n ^ 8) is 1032 + n, minus 1032.
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ void widen_i8_f16(uint32_t x, uint32_t &p02, uint32_t &p13) {
+    const uint32_t u = x ^ 0x80808080u;
+    uint32_t lo, hi;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(u), "r"(0x64646464u), "r"(0x4240u));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(u), "r"(0x64646464u), "r"(0x4341u));
+    p02 = f16x2_sub(lo, 0x64806480u);
+    p13 = f16x2_sub(hi, 0x64806480u);
+}
+
+__device__ __forceinline__ void widen_i4_f16(uint32_t w, uint32_t (&p)[4]) {
+    const uint32_t c = 0x64086408u;
+    p[0] = f16x2_sub((w & 0x000F000Fu) ^ c, c);
+    p[1] = f16x2_sub(((w >> 4) & 0x000F000Fu) ^ c, c);
+    p[2] = f16x2_sub(((w >> 8) & 0x000F000Fu) ^ c, c);
+    p[3] = f16x2_sub(((w >> 12) & 0x000F000Fu) ^ c, c);
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1,
                                          uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {

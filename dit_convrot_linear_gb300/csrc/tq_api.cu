@@ -347,13 +347,19 @@ tq_status tq_grouped_create(const tq_a16_call *calls, int64_t ncalls, int bits, 
     return grouped_create(calls, ncalls, bits, ytype == TQ_OUT_BF16 ? 1 : 0, dmem, dbytes, dev, plan);
 }
 
-tq_status tq_grouped_run(tq_grouped plan, cudaStream_t stream) {
+static tq_status grouped_phase(tq_grouped plan, int phase, cudaStream_t stream) {
     if (!plan) return TQ_ERR_NULL;
     DeviceInfo dev;
     const tq_status st = current_device(&dev);
     if (st != TQ_OK) return st;
-    return grouped_run(plan, dev, stream);
+    return grouped_run(plan, dev, phase, stream);
 }
+
+tq_status tq_grouped_run(tq_grouped plan, cudaStream_t stream) { return grouped_phase(plan, 3, stream); }
+
+tq_status tq_grouped_rotate(tq_grouped plan, cudaStream_t stream) { return grouped_phase(plan, 1, stream); }
+
+tq_status tq_grouped_product(tq_grouped plan, cudaStream_t stream) { return grouped_phase(plan, 2, stream); }
 
 int64_t tq_grouped_weight_bytes(tq_grouped plan) { return plan ? grouped_weight_bytes(plan) : 0; }
 

@@ -43,6 +43,8 @@ SIGNATURES = {
     "tq_grouped_bytes": (_C, [_P, _I, _C, ctypes.POINTER(ctypes.c_size_t)]),
     "tq_grouped_create": (_C, [_P, _I, _C, _C, _P, _Z, ctypes.POINTER(ctypes.c_void_p)]),
     "tq_grouped_run": (_C, [_P, _P]),
+    "tq_grouped_rotate": (_C, [_P, _P]),
+    "tq_grouped_product": (_C, [_P, _P]),
     "tq_grouped_weight_bytes": (_I, [_P]),
     "tq_grouped_destroy": (None, [_P]),
 }
@@ -340,6 +342,18 @@ class GroupedPlan:
         if self._h is None:
             raise ValueError("the plan is closed")
         _check(lib().tq_grouped_run(self._h, _stream(stream)), "tq_grouped_run")
+
+    def rotate(self, stream=None):
+        """The first launch of run(): every call's input rotation."""
+        if self._h is None:
+            raise ValueError("the plan is closed")
+        _check(lib().tq_grouped_rotate(self._h, _stream(stream)), "tq_grouped_rotate")
+
+    def product(self, stream=None):
+        """The second launch of run(): the products, from the rotated inputs."""
+        if self._h is None:
+            raise ValueError("the plan is closed")
+        _check(lib().tq_grouped_product(self._h, _stream(stream)), "tq_grouped_product")
 
     @property
     def weight_bytes(self) -> int:

@@ -326,6 +326,16 @@ tq_status tq_grouped_create(const tq_a16_call *calls, int64_t ncalls, int bits, 
  */
 tq_status tq_grouped_run(tq_grouped plan, cudaStream_t stream);
 
+/*
+ * The two launches of tq_grouped_run on their own, in this order on one
+ * stream (or ordered by events): tq_grouped_rotate reads every call's X and
+ * writes the plan's rotated inputs; tq_grouped_product reads them and the
+ * weights and writes every Y.  The inputs may change between the two only if
+ * the rotation is run again.
+ */
+tq_status tq_grouped_rotate(tq_grouped plan, cudaStream_t stream);
+tq_status tq_grouped_product(tq_grouped plan, cudaStream_t stream);
+
 /* Algorithmic bytes one run streams: every call's weight codes and row scales. */
 int64_t tq_grouped_weight_bytes(tq_grouped plan);
 

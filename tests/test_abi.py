@@ -206,6 +206,8 @@ def test_grouped_refusals(L):
     assert gcreate(L, gcalls(), dmem=FAKE + 16)[0] == ALIGN
     assert L.tq_grouped_create(FAKE, 1, 8, 0, FAKE, 1 << 20, None) == NULL
     assert L.tq_grouped_run(None, S0) == NULL
+    assert L.tq_grouped_rotate(None, S0) == NULL
+    assert L.tq_grouped_product(None, S0) == NULL
     assert L.tq_grouped_weight_bytes(None) == 0
     L.tq_grouped_destroy(None)
 
@@ -214,16 +216,17 @@ def test_grouped_bytes_count_tables_and_rotated_inputs(L):
     # M = 1, K = 896, N = 4864, 8-bit: items of 64 rows (960-byte shared rows,
     # 1792 bytes of x' per item) -> 76 items of 80 bytes (6080, rounded to
     # 6144); one 40-byte call record and one 128-byte tensor map (rows of 7
-    # chunks of 128 bytes: the tile form), each rounded to 256; x' of 896 bf16
-    assert gbytes(L, gcalls()) == (OK, 256 + 6144 + 256 + 896 * 2)
+    # chunks of 128 bytes: the tile form), each rounded to 256; x' of 896 fp16
+    # and a 32-byte tail (the token scales)
+    assert gbytes(L, gcalls()) == (OK, 256 + 6144 + 256 + 896 * 2 + 32)
     # two tokens, K = 544 (x' padded to 640 columns), N = 100, 4-bit: two
     # items of 64 rows, tile form
     calls = gcalls(M=2, N=100, K=544, ldx=544, ldy=100)
-    assert gbytes(L, calls, bits=4) == (OK, 256 + 256 + 256 + 2 * 640 * 2)
+    assert gbytes(L, calls, bits=4) == (OK, 256 + 256 + 256 + 2 * 640 * 2 + 32)
     # long rows (K = 4864: 38 chunks, items of 8 rows) stay in the row form:
     # no tensor map; 112 items of 80 bytes
     calls = gcalls(N=896, K=4864, ldx=4864, ldy=896)
-    assert gbytes(L, calls) == (OK, 256 + 8960 + 4864 * 2)
+    assert gbytes(L, calls) == (OK, 256 + 8960 + 4864 * 2 + 32)
 
 
 def test_grouped_create_without_a_gpu_reports_no_device(L):

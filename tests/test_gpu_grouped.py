@@ -130,6 +130,13 @@ def test_grouped_deterministic_and_graph_replay(tq):
     torch.cuda.synchronize()
     for a, c in zip(first, calls):
         assert np.array_equal(a.view(np.uint32), to_np(c[4]).view(np.uint32))
+    # the two launches of run() on their own
+    for c in calls:
+        c[4].fill_(float("nan"))
+    plan.rotate()
+    plan.product()
+    for a, c in zip(first, calls):
+        assert np.array_equal(a.view(np.uint32), to_np(c[4]).view(np.uint32))
 
 
 def test_grouped_strided_input_padded_output_and_empty_calls(tq):
@@ -181,3 +188,26 @@ def test_grouped_decode_workload_sampled(tq):
         c = to_np(codes)
         Wc = oracle.weight_codes(c.view(np.int8), 8, K)
         check_call(tq, Y, xs[i][0], Xd, Wc, to_np(sw))
+
+
+def test_grouped_activation_scales_far_from_one(tq):
+    """The product's fp16 operand is x' times a per-token power of two: token
+    rows of very large, very small and mixed magnitude (and a zero row) give
+    the oracle's result."""
+    import torch
+    K, N = 896, 300
+    codes, sw, Wc = weights(tq, "gpu/grpscale/w", N, K, 8)
+    base = oracle.bf16_to_f64(synth.tensor("gpu/grpscale/x", 4, K, 1.0, 0.0, 1.0))
+    base[1] *= 2.0 ** 100                     # beyond fp16 range before scaling
+    base[2] *= 2.0 ** -100                    # below fp16's smallest normal
+    base[3] = 0.0
+    X = oracle.round_bf16(base)
+    Xd = to_dev_bf16(X)
+    Y = torch.full((4, N), float("nan"), dtype=torch.float32, device="cuda")
+    plan = tq.GroupedPlan([(Xd, codes, sw, N, Y)], 8)
+    plan.run()
+    Yn = to_np(Y)
+    ref = oracle.linear_a16(oracle.rotate_act_bf16(X), Wc, to_np(sw))
+    for m in range(3):
+        assert rel_l2(Yn[m], ref[m]) <= REL_L2_Y, m
+    assert np.all(Yn[3] == 0.0)
