@@ -138,8 +138,8 @@ __device__ __forceinline__ void block_mma(float (&acc)[4][4], const unsigned cha
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             uint32_t pa4[4], pb4[4] = {0, 0, 0, 0};
-            widen_i4_f16(A[q], pa4);
-            if (HASB) widen_i4_f16(B[q], pb4);
+            widen_i4_f16_odd16(A[q], pa4);
+            if (HASB) widen_i4_f16_odd16(B[q], pb4);
             const uint2 b0 = *reinterpret_cast<const uint2 *>(xblk + (2 * q) * 16);
             const uint2 b1 = *reinterpret_cast<const uint2 *>(xblk + (2 * q + 1) * 16);
             mma_f16(acc[(2 * q) % 4], pa4[0], pb4[0], pa4[1], pb4[1], b0.x, b0.y);
@@ -172,33 +172,47 @@ __device__ __forceinline__ void tile_blocks(float (&acc)[4][4], const unsigned c
     if (b < bend) block_mma<BITS, HASB>(acc, pA + off(b), pB + off(b), xb + b * KB);
 }
 
-// x' of one call, in the order the product's lanes read it, as fp16: token
-// row m (warp m) is the bf16 rounding of the rotated row (the A16 operand),
+// x' of one call (one warp per call, eight calls per CTA), in the order the
+// product's lanes read it, as fp16 (for 4-bit weights, odd k divided by 16 as
+// well, exactly): token row m is the bf16 rounding of the rotated row (the A16
+// operand),
 // times 2^e with e chosen so that its largest magnitude lies in [2^14, 2^15).
 // The multiplication by a power of two is exact, and so is the fp16 form of
 // every value not below 2^-31 of that largest one (smaller ones keep an
 // absolute error under 2^-39 of it).  The product multiplies Y by 2^-e, read
 // from the float after the M fp16 rows.
 template <int BITS>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 1)
 k_rotate_grouped(const GCall *calls, int64_t ncalls) {
     constexpr int KB = BITS == 8 ? 64 : 128;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int64_t c = blockIdx.x; c < ncalls; c += gridDim.x) {
-        const GCall cl = calls[c];
-        if (warp >= cl.M) continue;
+    for (int64_t c = static_cast<int64_t>(blockIdx.x) * 8 + warp; c < ncalls; c += static_cast<int64_t>(gridDim.x) * 8) {
+      const GCall cl = calls[c];
+      for (int m = 0; m < cl.M; ++m) {
         const int G = (cl.K + kGroup - 1) / kGroup;
-        const uint16_t *xrow = cl.X + warp * cl.ldx;
-        uint16_t *row = cl.xq + static_cast<int64_t>(warp) * cl.xk;
+        const uint16_t *xrow = cl.X + m * cl.ldx;
+        uint16_t *row = cl.xq + static_cast<int64_t>(m) * cl.xk;
+        // groups are taken four at a time, their loads issued before any
+        // butterfly, so a long row's reads overlap instead of queueing
+        constexpr int GB = 4;
         float amax = 0.0f;
-        for (int gi = 0; gi < G; ++gi) {
-            const int64_t gk = static_cast<int64_t>(gi) * kGroup;
-            const int n = group_width(cl.K, gk);
-            float v[8];
-            const int E = fwht_group_raw(load_group_raw(xrow + gk + lane * (n / 32), n / 32), n, v);
+        for (int g0 = 0; g0 < G; g0 += GB) {
+            uint4 raw[GB];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                if (e < E) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(f32_to_bf16_bits(v[e]))));
+            for (int u = 0; u < GB; ++u) {
+                const int64_t gk = static_cast<int64_t>(g0 + u) * kGroup;
+                const int n = g0 + u < G ? group_width(cl.K, gk) : 32;
+                raw[u] = g0 + u < G ? load_group_raw(xrow + gk + lane * (n / 32), n / 32) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < GB; ++u) {
+                if (g0 + u >= G) break;
+                float v[8];
+                const int E = fwht_group_raw(raw[u], group_width(cl.K, static_cast<int64_t>(g0 + u) * kGroup), v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (e < E) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(f32_to_bf16_bits(v[e]))));
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -206,24 +220,37 @@ k_rotate_grouped(const GCall *calls, int64_t ncalls) {
         if (amax > 0.0f) frexpf(amax, &ex);              // amax = f * 2^ex, f in [0.5, 1)
         const int sh = amax > 0.0f ? max(-100, min(100, 15 - ex)) : 0;
         const float up = ldexpf(1.0f, sh);
-        for (int gi = 0; gi < G; ++gi) {
-            const int64_t gk = static_cast<int64_t>(gi) * kGroup;
-            const int n = group_width(cl.K, gk);
-            float v[8];
-            const int E = fwht_group_raw(load_group_raw(xrow + gk + lane * (n / 32), n / 32), n, v);
+        for (int g0 = 0; g0 < G; g0 += GB) {
+            uint4 raw[GB];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (e < E) {
-                    const int kl = static_cast<int>(gk) + lane * E + e;
-                    const float xb = bf16_bits_to_f32(f32_to_bf16_bits(v[e]));
-                    row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = __half_as_ushort(__float2half_rn(xb * up));
+            for (int u = 0; u < GB; ++u) {
+                const int64_t gk = static_cast<int64_t>(g0 + u) * kGroup;
+                const int n = g0 + u < G ? group_width(cl.K, gk) : 32;
+                raw[u] = g0 + u < G ? load_group_raw(xrow + gk + lane * (n / 32), n / 32) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < GB; ++u) {
+                if (g0 + u >= G) break;
+                const int64_t gk = static_cast<int64_t>(g0 + u) * kGroup;
+                float v[8];
+                const int E = fwht_group_raw(raw[u], group_width(cl.K, gk), v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (e < E) {
+                        const int kl = static_cast<int>(gk) + lane * E + e;
+                        const float xb = bf16_bits_to_f32(f32_to_bf16_bits(v[e]));
+                        // 4-bit weights: odd k meets 16 times its code (widen_i4_f16_odd16)
+                        const float f = (BITS == 4 && (kl & 1)) ? up * 0.0625f : up;
+                        row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = __half_as_ushort(__float2half_rn(xb * f));
+                    }
                 }
             }
         }
         for (int kl = cl.K + lane; kl < cl.xk; kl += 32)   // zeros after K, up to the block edge
             row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = 0;
         if (lane == 0)
-            reinterpret_cast<float *>(cl.xq + static_cast<int64_t>(cl.M) * cl.xk)[warp] = ldexpf(1.0f, -sh);
+            reinterpret_cast<float *>(cl.xq + static_cast<int64_t>(cl.M) * cl.xk)[m] = ldexpf(1.0f, -sh);
+      }
     }
 }
 
@@ -611,7 +638,7 @@ tq_status grouped_run(tq_grouped plan, const DeviceInfo &dev, int phase, cudaStr
     unsigned int *status = status_word();
     if (!status) return TQ_ERR_CUDA;
     if (phase & 1) {
-        const int64_t rgrid = plan->ncalls < 65536 ? plan->ncalls : 65536;
+        const int64_t rgrid = (plan->ncalls + 7) / 8 < 65536 ? (plan->ncalls + 7) / 8 : 65536;
         rot<<<static_cast<unsigned>(rgrid), 256, 0, s>>>(plan->calls, plan->ncalls);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e);

@@ -52,11 +52,9 @@ __device__ __forceinline__ void widen_i4(uint32_t w, uint32_t (&p)[4]) {
     p[3] = bf16x2_sub(((w >> 12) & 0x000F000Fu) ^ c, c);
 }
 
-// fp16 forms of the widening, for products whose x' is fp16:
-//   int8 codes (k0..k3) -> fp16 pairs (k0,k2), (k1,k3): the byte u = b ^ 0x80
-//   under exponent 0x64 is 1024 + u exactly, minus 1152 is b;
-//   int4 codes (k0..k7) -> fp16 pairs (k0,k4), (k1,k5), (k2,k6), (k3,k7):
-//   0x6400 | (n ^ 8) is 1032 + n, minus 1032.
+// fp16 form of the int8 widening, for products whose x' is fp16: codes
+// (k0..k3) -> fp16 pairs (k0,k2), (k1,k3); the byte u = b ^ 0x80 under
+// exponent 0x64 is 1024 + u exactly, minus 1152 is b.
 __device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -72,12 +70,17 @@ __device__ __forceinline__ void widen_i8_f16(uint32_t x, uint32_t &p02, uint32_t
     p13 = f16x2_sub(hi, 0x64806480u);
 }
 
-__device__ __forceinline__ void widen_i4_f16(uint32_t w, uint32_t (&p)[4]) {
-    const uint32_t c = 0x64086408u;
-    p[0] = f16x2_sub((w & 0x000F000Fu) ^ c, c);
-    p[1] = f16x2_sub(((w >> 4) & 0x000F000Fu) ^ c, c);
-    p[2] = f16x2_sub(((w >> 8) & 0x000F000Fu) ^ c, c);
-    p[3] = f16x2_sub(((w >> 12) & 0x000F000Fu) ^ c, c);
+// int4 codes (k0..k7) -> fp16 pairs (k0,k4), (16 k1, 16 k5), (k2,k6),
+// (16 k3, 16 k7): the odd codes are read in place (bits 4..7 of each half)
+// under exponent 0x64, which makes them 16 times their value, so only the
+// even/odd split needs a shift.  The operand they meet must hold x'/16 at odd k.
+__device__ __forceinline__ void widen_i4_f16_odd16(uint32_t w, uint32_t (&p)[4]) {
+    const uint32_t ce = 0x64086408u, co = 0x64806480u;   // 1024 + 8, 1024 + 128
+    const uint32_t w8 = w >> 8;
+    p[0] = f16x2_sub((w & 0x000F000Fu) ^ ce, ce);
+    p[1] = f16x2_sub((w & 0x00F000F0u) ^ co, co);
+    p[2] = f16x2_sub((w8 & 0x000F000Fu) ^ ce, ce);
+    p[3] = f16x2_sub((w8 & 0x00F000F0u) ^ co, co);
 }
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
