@@ -60,15 +60,20 @@ constexpr int A_OP = HM * BK * 2;      // 16 KB fp16: this CTA's 128 rows of A
 constexpr int B_OP = HN * BK * 2;      // 16 KB fp16: this CTA's 128 rows of B
 constexpr int A_RAW = HM * BK;         // 8 KB int8 codes
 constexpr int B_RAW = HN * BK;         // 8 KB int8 codes (int4: half used)
-// Shared-memory plan of the two operand sources.  With raw A (AT false) the
-// TMA brings int8 codes of both operands and the converters widen both; with
-// pre-tiled A (AT true) the activations arrive as fp16 codes already in the
-// tensor core's layout, one 16 KB bulk copy per K step straight into the
-// operand ring (loaded by warp 14), and only B is widened.
-template <bool AT>
+// Shared-memory plan of the operand sources (MODE):
+//   0: raw A.  The TMA brings int8 codes of both operands and the converters
+//      widen both;
+//   1: pre-tiled A (AT).  The activations arrive as fp16 codes already in the
+//      tensor core's layout, one 16 KB bulk copy per K step straight into the
+//      operand ring (loaded by warp 14), and only B is widened;
+//   2: pre-tiled A and B (BT).  The weights too were widened once into fp16
+//      tiles (tq_tile_weights), so both arrive by tensor copies straight into
+//      the operand ring, no converter runs, and the ring is one stage deeper.
+template <int MODE>
 struct Plan {
-    static constexpr int O = AT ? 5 : 4;            // operand ring depth
-    static constexpr int R = AT ? 6 : 4;            // raw ring depth
+    static constexpr bool AT = MODE >= 1, BT = MODE == 2;
+    static constexpr int O = BT ? 6 : (AT ? 5 : 4);   // operand ring depth
+    static constexpr int R = BT ? 0 : (AT ? 6 : 4);   // raw ring depth
     static constexpr int NWARPS = AT ? 15 : 14;
     static constexpr int THREADS = NWARPS * 32;
     static constexpr int RAW_A = AT ? 0 : A_RAW;    // raw A bytes per slot
@@ -84,8 +89,8 @@ struct Plan {
     // A, for the A tile (previous use j - O).  Its own previous step j - G
     // waited for step j - G - O to be consumed, so the stage wait cannot see
     // step j - 2O still pending when G <= O.
-    static_assert(R >= O, "raw slot's previous use covered by the stage wait");
-    static_assert(O >= CONV_GROUPS, "operand stages for every group");
+    static_assert(BT || R >= O, "raw slot's previous use covered by the stage wait");
+    static_assert(BT || O >= CONV_GROUPS, "operand stages for every group");
 };
 constexpr uint32_t TMEM_COLS = 512;    // acc [0, 256) + running int32 sum [256, 512)
 constexpr uint32_t RUN_COL = 256;
@@ -295,15 +300,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// A tensor copy of this CTA's half of a pair operand, completing on a barrier
+// that may sit in the peer CTA (here the even CTA's stage barrier).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-template <int BITS, bool AT>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Plan<AT>::THREADS, 1)
+template <int BITS, int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Plan<MODE>::THREADS, 1)
 k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const TcParams p) {
-    using P = Plan<AT>;
+    using P = Plan<MODE>;
+    constexpr bool AT = P::AT, BT = P::BT;
     constexpr int OSTAGES = P::O, RSTAGES = P::R;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *opA = smem;                                       // [O][A_OP]
@@ -332,7 +349,10 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(raw_empty0 + 8 * s), "r"(WPG));
         }
         for (int s = 0; s < OSTAGES; ++s) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(op_full0 + 8 * s), "r"(2 * WPG));
+            // the converter warps of both CTAs; with both operands tiled, the
+            // even CTA's loader (its expected bytes cover both CTAs' copies)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(op_full0 + 8 * s),
+                         "r"(BT ? 1 : 2 * WPG));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(op_empty0 + 8 * s));
         }
         for (int h = 0; h < 2; ++h) {
@@ -340,7 +360,7 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(acc_empty0 + 8 * h));
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done));
-        if constexpr (AT) {
+        if constexpr (AT && !BT) {
             for (int s = 0; s < OSTAGES; ++s)
                 asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(a_full0 + 8 * s));
         }
@@ -387,14 +407,14 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
 
     if (warp == TMA_WARP) {
         // ------------------------------------------------ TMA producer
-        if (lane == 0) {
+        if (!BT && lane == 0) {
             uint32_t it = 0;
             for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
                 const int m0 = tile_m(tile, p) * 2 * HM + static_cast<int>(rank) * HM;
                 const int n0 = tile_n(tile, p) * BN + static_cast<int>(rank) * HN;
                 for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
-                    const int s = it % RSTAGES;
-                    if (!mbar_wait(raw_empty0 + 8 * s, ((it / RSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
+                    const int s = it % (BT ? 1 : RSTAGES);
+                    if (!mbar_wait(raw_empty0 + 8 * s, ((it / (BT ? 1 : RSTAGES)) & 1) ^ 1, &abort_sh, p.status)) break;
                     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                                  ::"r"(raw_full0 + 8 * s), "r"(static_cast<uint32_t>(P::RAW_A + BRAW)) : "memory");
                     if constexpr (!AT) tma_load_2d(smem_u32(rawA + s * A_RAW), &tmA, ks * BK, m0, raw_full0 + 8 * s);
@@ -404,6 +424,33 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         }
         __syncwarp();
     } else if (AT && warp == A_WARP) {
+        if constexpr (BT) {
+            // -------------------------------------------- A and B loader (both tiled)
+            // Tiles (mt, ks) of A and (nt, ks) of B are 16 KB rows of their
+            // tensor maps.  Both CTAs copy their own halves; the copies
+            // complete on the even CTA's stage barrier, whose expected bytes
+            // (all four tiles) the even CTA posts.
+            if (lane == 0) {
+                uint32_t it = 0;
+                for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
+                    const int mt = tile_m(tile, p) * 2 + static_cast<int>(rank);
+                    const int nt = tile_n(tile, p) * 2 + static_cast<int>(rank);
+                    for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
+                        const int s = it % OSTAGES;
+                        if (!mbar_wait(op_empty0 + 8 * s, ((it / OSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
+                        if (rank == 0)
+                            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                                         ::"r"(op_full0 + 8 * s), "r"(static_cast<uint32_t>(2 * (A_OP + B_OP)))
+                                         : "memory");
+                        uint32_t bar;
+                        asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(bar) : "r"(op_full0 + 8 * s));
+                        tma_load_2d_pair(smem_u32(opA + s * A_OP), &tmA, 0, (mt * p.ksteps + ks) * 128, bar);
+                        tma_load_2d_pair(smem_u32(opB + s * B_OP), &tmB, 0, (nt * p.ksteps + ks) * 128, bar);
+                    }
+                }
+            }
+            __syncwarp();
+        } else {
         // ------------------------------------------------ A loader (pre-tiled fp16 codes)
         // Tile (mt, ks) of the activations is 16 KB contiguous, already in the
         // operand layout: one bulk copy into the stage once the MMA is done
@@ -427,7 +474,9 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             }
         }
         __syncwarp();
+        }
     } else if (warp < NCONV) {
+        if constexpr (!BT) {
         // ------------------------------------------------ converters (shared -> shared)
         const int g = warp / WPG, tid = threadIdx.x % TPG;
         constexpr int NA = 512 / TPG;                          // A passes (and int8 B passes)
@@ -504,6 +553,7 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                     }
                 }
             }
+        }
         }
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------ MMA issue (CTA 0, one thread)
@@ -678,24 +728,32 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     }
 }
 
-// Shared launch of both operand paths: Xq int8 codes (AT false, A through a
-// tensor map) or At pre-tiled fp16 codes (AT true).
-template <bool AT>
-tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const float *sx, int64_t M, int64_t K,
-                    const uint8_t *Wq, const float *sw, int64_t N, int bits, void *Y, int ytype,
-                    int64_t ldy, const DeviceInfo &dev, cudaStream_t s) {
-    using P = Plan<AT>;
+// Shared launch of the operand paths (MODE as in Plan): Xq int8 codes (A
+// through a tensor map), At pre-tiled fp16 codes, or At and Wt both pre-tiled
+// (each read as rows of 128 bytes, one 16 KB tile a box).
+template <int MODE>
+tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const unsigned char *Wt, const float *sx,
+                    int64_t M, int64_t K, const uint8_t *Wq, const float *sw, int64_t N, int bits, void *Y,
+                    int ytype, int64_t ldy, const DeviceInfo &dev, cudaStream_t s) {
+    using P = Plan<MODE>;
+    constexpr bool AT = P::AT;
     unsigned int *status = status_word();
     if (!status) return TQ_ERR_DEVICE;
     if (M > (1ll << 31) - 1 || N > (1ll << 31) - 1) return TQ_ERR_OVERFLOW;
     CUtensorMap tmA, tmB;
-    const bool mapped = bits == 8 ? make_map_u8(&tmB, Wq, N, K, BK, 128, CU_TENSOR_MAP_SWIZZLE_64B)
-                                  : make_map_u8(&tmB, Wq, N, K / 2, BK / 2, 128, CU_TENSOR_MAP_SWIZZLE_32B);
-    if (!mapped) return TQ_ERR_DEVICE;
-    if constexpr (AT) {
-        tmA = tmB;   // not read on this path
+    if constexpr (MODE == 2) {
+        if (!make_map_u8(&tmA, At, tiled_act_tiles_bytes(M, K) / 128, 128, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !make_map_u8(&tmB, Wt, weights_tiled_bytes(N, K) / 128, 128, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return TQ_ERR_DEVICE;
     } else {
-        if (!make_map_u8(&tmA, Xq, M, K, BK, 128, CU_TENSOR_MAP_SWIZZLE_64B)) return TQ_ERR_DEVICE;
+        const bool mapped = bits == 8 ? make_map_u8(&tmB, Wq, N, K, BK, 128, CU_TENSOR_MAP_SWIZZLE_64B)
+                                      : make_map_u8(&tmB, Wq, N, K / 2, BK / 2, 128, CU_TENSOR_MAP_SWIZZLE_32B);
+        if (!mapped) return TQ_ERR_DEVICE;
+        if constexpr (AT) {
+            tmA = tmB;   // not read on this path
+        } else {
+            if (!make_map_u8(&tmA, Xq, M, K, BK, 128, CU_TENSOR_MAP_SWIZZLE_64B)) return TQ_ERR_DEVICE;
+        }
     }
     TcParams p{};
     p.sx = sx;
@@ -716,7 +774,7 @@ tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const float *sx, 
     p.max_l1 = AT ? reinterpret_cast<const unsigned int *>(At + tiled_act_tiles_bytes(M, K)) : nullptr;
     const int64_t tiles = static_cast<int64_t>(p.mtiles) * p.ntiles;
     if (tiles > (1ll << 30)) return TQ_ERR_OVERFLOW;
-    auto kern = bits == 8 ? k_gemm_a8_tc<8, AT> : k_gemm_a8_tc<4, AT>;
+    auto kern = bits == 8 ? k_gemm_a8_tc<8, MODE> : k_gemm_a8_tc<4, MODE>;
     static bool configured_for[64][2] = {{false}};
     const int bi = bits == 8 ? 0 : 1;
     if (dev.id < 0 || dev.id >= 64) return TQ_ERR_DEVICE;
@@ -738,15 +796,22 @@ tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M, int64_t K
                          const uint8_t *Wq, const float *sw, int64_t N, int bits,
                          void *Y, int ytype, int64_t ldy, const DeviceInfo &dev,
                          cudaStream_t s) {
-    return launch_tc<false>(Xq, nullptr, sx, M, K, Wq, sw, N, bits, Y, ytype, ldy, dev, s);
+    return launch_tc<0>(Xq, nullptr, nullptr, sx, M, K, Wq, sw, N, bits, Y, ytype, ldy, dev, s);
 }
 
 tq_status launch_gemm_a8_tiled(const void *At, const float *sx, int64_t M, int64_t K,
                                const uint8_t *Wq, const float *sw, int64_t N, int bits,
                                void *Y, int ytype, int64_t ldy, const DeviceInfo &dev,
                                cudaStream_t s) {
-    return launch_tc<true>(nullptr, static_cast<const unsigned char *>(At), sx, M, K, Wq, sw, N,
-                           bits, Y, ytype, ldy, dev, s);
+    return launch_tc<1>(nullptr, static_cast<const unsigned char *>(At), nullptr, sx, M, K, Wq, sw, N,
+                        bits, Y, ytype, ldy, dev, s);
+}
+
+tq_status launch_gemm_a8_tt(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
+                            const float *sw, int64_t N, int bits, void *Y, int ytype, int64_t ldy,
+                            const DeviceInfo &dev, cudaStream_t s) {
+    return launch_tc<2>(nullptr, static_cast<const unsigned char *>(At), static_cast<const unsigned char *>(Wt),
+                        sx, M, K, nullptr, sw, N, bits, Y, ytype, ldy, dev, s);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,

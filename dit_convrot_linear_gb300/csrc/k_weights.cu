@@ -18,6 +18,8 @@
 // row's amax, pass 2 recomputes the transform and writes codes (recomputing is
 // cheaper than holding up to 64K fp64 values per row).
 
+#include <cuda_fp16.h>
+
 #include "tq_internal.cuh"
 
 namespace tq {
@@ -121,6 +123,53 @@ k_quantize_weights(const uint16_t *__restrict__ W, int64_t N, int64_t K,
     }
 }
 
+// Weight codes widened once into the A8 product's own operand form: fp16 (the
+// codes are small integers, so exactly), in 128-row x 64-column tiles of 8x8
+// core matrices, the image the tensor core reads from shared memory.  Tile
+// (nt, kt) sits at byte (nt * KT + kt) * 16384; inside it core matrix
+// (r / 8, k / 8) is 128 contiguous bytes, K-adjacent ones 128 bytes apart and
+// row groups 1024 bytes apart.  Rows are padded to whole 256-row tile pairs and
+// columns past K to the tile edge, with zeros.  One thread writes one 16-byte
+// core-matrix row: 8 codes of one weight row.
+template <int BITS>
+__global__ void __launch_bounds__(256)
+k_tile_weights(const uint8_t *Wq, int64_t N, int64_t K, int64_t KT, int64_t Npad, uint16_t *Wt) {
+    const int64_t segs = KT * 8;                       // 8-column segments per row
+    const int64_t total = Npad * segs;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t n = i / segs, k0 = (i % segs) * 8;
+        uint32_t h[4] = {0, 0, 0, 0};
+        if (n < N && k0 < K) {                         // K is a multiple of 32: whole segments
+            int c[8];
+            if (BITS == 8) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(Wq + n * K + k0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    c[j] = static_cast<int8_t>((w.x >> (8 * j)) & 0xFF);
+                    c[4 + j] = static_cast<int8_t>((w.y >> (8 * j)) & 0xFF);
+                }
+            } else {
+                const uint32_t w = *reinterpret_cast<const uint32_t *>(Wq + n * (K / 2) + k0 / 2);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int v = static_cast<int>((w >> (4 * j)) & 0xF);
+                    c[j] = v >= 8 ? v - 16 : v;        // two's complement nibble, code k0 + j
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __half2 pr = __halves2half2(__int2half_rn(c[2 * j]), __int2half_rn(c[2 * j + 1]));
+                h[j] = *reinterpret_cast<const uint32_t *>(&pr);
+            }
+        }
+        const int64_t nt = n >> 7, kt = k0 >> 6;
+        const int r = static_cast<int>(n & 127), kk = static_cast<int>(k0 & 63);
+        uint16_t *dst = Wt + ((nt * KT + kt) << 13) + ((((r >> 3) << 3) + (kk >> 3)) << 6) + ((r & 7) << 3);
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
 }  // namespace
 
 tq_status launch_quantize_weights(const uint16_t *W, int64_t N, int64_t K,
@@ -133,6 +182,21 @@ tq_status launch_quantize_weights(const uint16_t *W, int64_t N, int64_t K,
     else
         k_quantize_weights<4><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(
             W, N, K, ldw, static_cast<uint8_t *>(codes), scales);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+int64_t weights_tiled_bytes(int64_t N, int64_t K) {
+    return ((N + 255) / 256) * 2 * ((K + 63) / 64) * 16384;
+}
+
+tq_status launch_tile_weights(const uint8_t *Wq, int64_t N, int64_t K, int bits, void *Wt, cudaStream_t s) {
+    const int64_t KT = (K + 63) / 64, Npad = (N + 255) / 256 * 256;
+    const int64_t total = Npad * KT * 8;
+    if (total == 0) return TQ_OK;
+    const int64_t blocks = (total + 255) / 256 < 152 * 64 ? (total + 255) / 256 : 152 * 64;
+    auto kern = bits == 8 ? k_tile_weights<8> : k_tile_weights<4>;
+    kern<<<static_cast<unsigned>(blocks), 256, 0, s>>>(Wq, N, K, KT, Npad, static_cast<uint16_t *>(Wt));
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }

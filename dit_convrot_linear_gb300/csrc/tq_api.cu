@@ -311,6 +311,46 @@ tq_status tq_linear_tiled(const void *At, const float *sx, int64_t M, int64_t K,
                                 static_cast<int>(ytype), ldy, dev, stream);
 }
 
+size_t tq_weights_tiled_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || !valid_k(K) || K > TQ_MAX_K_TILED) return 0;
+    if (!mul_ok(N + 256, K + 64, INT64_MAX / 8)) return 0;
+    return static_cast<size_t>(weights_tiled_bytes(N, K));
+}
+
+tq_status tq_tile_weights(const void *Wq, int64_t N, int64_t K, int bits, void *Wt, size_t wt_bytes,
+                          cudaStream_t stream) {
+    if (bits != 8 && bits != 4) return TQ_ERR_BITS;
+    if (N < 0 || !valid_k(K) || K > TQ_MAX_K_TILED) return TQ_ERR_SHAPE;
+    if (N == 0) return TQ_OK;
+    if (!Wq || !Wt) return TQ_ERR_NULL;
+    const size_t need = tq_weights_tiled_bytes(N, K);
+    if (need == 0) return TQ_ERR_OVERFLOW;
+    if (wt_bytes < need) return TQ_ERR_WORKSPACE;
+    if (!aligned(Wq, 16) || !aligned(Wt, 256)) return TQ_ERR_ALIGN;
+    DeviceInfo dev;
+    const tq_status st = current_device(&dev);
+    if (st != TQ_OK) return st;
+    return launch_tile_weights(static_cast<const uint8_t *>(Wq), N, K, bits, Wt, stream);
+}
+
+tq_status tq_linear_tt(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
+                       const float *sw, int64_t N, int bits, void *Y, tq_out ytype, int64_t ldy,
+                       cudaStream_t stream) {
+    if (ytype != TQ_OUT_F32 && ytype != TQ_OUT_BF16 && ytype != TQ_OUT_I32) return TQ_ERR_MODE;
+    if (bits != 8 && bits != 4) return TQ_ERR_BITS;
+    if (M < 0 || N < 0 || !valid_k(K) || K > TQ_MAX_K_TILED) return TQ_ERR_SHAPE;
+    if (M == 0 || N == 0) return TQ_OK;
+    if (!At || !Wt || !sw || (ytype != TQ_OUT_I32 && !sx)) return TQ_ERR_NULL;
+    if (tq_act_tiled_bytes(M, K) == 0 || tq_weights_tiled_bytes(N, K) == 0) return TQ_ERR_OVERFLOW;
+    if (!aligned(At, 256) || !aligned(Wt, 256) || !aligned(sw, 4) || (sx && !aligned(sx, 4)))
+        return TQ_ERR_ALIGN;
+    tq_status st = check_output(Y, M, N, ldy, out_size(ytype));
+    if (st != TQ_OK) return st;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    return launch_gemm_a8_tt(At, sx, M, K, Wt, sw, N, bits, Y, static_cast<int>(ytype), ldy, dev, stream);
+}
+
 tq_status tq_device_status(cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e);

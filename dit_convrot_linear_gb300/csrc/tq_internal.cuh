@@ -81,6 +81,12 @@ tq_status grouped_run(tq_grouped plan, const DeviceInfo &dev, int phase, cudaStr
 void grouped_destroy(tq_grouped plan);
 int64_t grouped_weight_bytes(tq_grouped plan);
 
+int64_t weights_tiled_bytes(int64_t N, int64_t K);
+tq_status launch_tile_weights(const uint8_t *Wq, int64_t N, int64_t K, int bits, void *Wt, cudaStream_t s);
+tq_status launch_gemm_a8_tt(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
+                            const float *sw, int64_t N, int bits, void *Y, int ytype, int64_t ldy,
+                            const DeviceInfo &dev, cudaStream_t s);
+
 int64_t tiled_act_tiles_bytes(int64_t M, int64_t K);
 int64_t tiled_act_bytes(int64_t M, int64_t K);
 tq_status launch_rotate_quant_tiled(const uint16_t *X, int64_t M, int64_t K,

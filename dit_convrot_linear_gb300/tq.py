@@ -40,6 +40,9 @@ SIGNATURES = {
     "tq_act_tiled_bytes": (_Z, [_I, _I]),
     "tq_rotate_quant_act_tiled": (_C, [_P, _I, _I, _I, _P, _Z, _P, _P]),
     "tq_linear_tiled": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
+    "tq_weights_tiled_bytes": (_Z, [_I, _I]),
+    "tq_tile_weights": (_C, [_P, _I, _I, _C, _P, _Z, _P]),
+    "tq_linear_tt": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
     "tq_grouped_bytes": (_C, [_P, _I, _C, ctypes.POINTER(ctypes.c_size_t)]),
     "tq_grouped_create": (_C, [_P, _I, _C, _C, _P, _Z, ctypes.POINTER(ctypes.c_void_p)]),
     "tq_grouped_run": (_C, [_P, _P]),
@@ -268,6 +271,42 @@ def linear_tiled(At, sx, M: int, K: int, Wq, sw, N: int, bits: int, Y=None, out:
     _req(Y, "Y", dtype=_dt(out), rows=M, cols=N)
     _check(lib().tq_linear_tiled(_ptr(At), _ptr(sx), M, K, _ptr(Wq), _ptr(sw), N, bits, _ptr(Y),
                                  OUT[out], Y.stride(0), _stream(stream)), "tq_linear_tiled")
+    return Y
+
+
+def weights_tiled_bytes(N: int, K: int) -> int:
+    return int(lib().tq_weights_tiled_bytes(N, K))
+
+
+def tile_weights(Wq, N: int, K: int, bits: int, Wt=None, stream=None):
+    """The codes of ``quantize_weights`` widened once into the A8 product's
+    operand form (fp16 tiles) for ``linear_tt``."""
+    import torch
+    need = weights_tiled_bytes(N, K)
+    if Wt is None:
+        Wt = torch.empty(max(need, 1), dtype=torch.uint8, device=Wq.device)
+    _req(Wq, "Wq", nbytes=N * K * bits // 8)
+    _req(Wt, "Wt", nbytes=need)
+    _check(lib().tq_tile_weights(_ptr(Wq), N, K, bits, _ptr(Wt), _nbytes(Wt), _stream(stream)),
+           "tq_tile_weights")
+    return Wt
+
+
+def linear_tt(At, sx, M: int, K: int, Wt, sw, N: int, bits: int, Y=None, out: str = "f32",
+              stream=None):
+    """The A8 product with both operands tiled (``rotate_quant_act_tiled`` and
+    ``tile_weights``)."""
+    import torch
+    if Y is None:
+        Y = torch.empty((M, N), dtype=_dt(out), device=At.device)
+    _req(At, "At", nbytes=act_tiled_bytes(M, K))
+    if out != "i32":
+        _req(sx, "sx", dtype=torch.float32, nbytes=4 * M)
+    _req(Wt, "Wt", nbytes=weights_tiled_bytes(N, K))
+    _req(sw, "sw", dtype=torch.float32, nbytes=4 * N)
+    _req(Y, "Y", dtype=_dt(out), rows=M, cols=N)
+    _check(lib().tq_linear_tt(_ptr(At), _ptr(sx), M, K, _ptr(Wt), _ptr(sw), N, bits, _ptr(Y),
+                              OUT[out], Y.stride(0), _stream(stream)), "tq_linear_tt")
     return Y
 
 

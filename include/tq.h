@@ -210,6 +210,39 @@ tq_status tq_linear_tiled(const void *At, const float *sx, int64_t M, int64_t K,
                           cudaStream_t stream);
 
 /*
+ * Bytes of the tiled weight operand (tq_tile_weights) of an N x K matrix: 0
+ * when K is not a valid row length or is above TQ_MAX_K_TILED.
+ */
+size_t tq_weights_tiled_bytes(int64_t N, int64_t K);
+
+/*
+ * The weight codes of tq_quantize_weights (with `bits`) widened once into the
+ * A8 product's own operand form.  The values are fp16, which holds the small
+ * integer codes exactly.  They sit in 128-row x 64-column tiles laid out as the
+ * tensor cores read them, with rows padded to 256 and columns to 64 by zeros.
+ * sm_103a has no integer tensor-core MMA, so the product otherwise widens the
+ * codes of every weight tile for every tile of activations.  With the tiled
+ * form it copies both operands straight into its stages instead.  The cost is
+ * device memory: twice the bytes of 8-bit codes, four times those of 4-bit
+ * codes.  A set-up step, run once per weight matrix like tq_quantize_weights;
+ * the pages have no counterpart.
+ *   Wq      codes [N, K] as written by tq_quantize_weights, 16-byte aligned.
+ *   Wt      at least tq_weights_tiled_bytes(N, K) bytes, 256-byte aligned; its
+ *           layout is private to this library (read it through tq_linear_tt).
+ */
+tq_status tq_tile_weights(const void *Wq, int64_t N, int64_t K, int bits, void *Wt,
+                          size_t wt_bytes, cudaStream_t stream);
+
+/*
+ * The A8 product with both operands in the tiled form: as tq_linear_tiled,
+ * with Wt from tq_tile_weights (same N, K and bits) in place of Wq.  The
+ * results are the same: the exact int32 sums and Y = sx[m] * sw[n] * acc.
+ */
+tq_status tq_linear_tt(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
+                       const float *sw, int64_t N, int bits, void *Y, tq_out ytype, int64_t ldy,
+                       cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  Returns TQ_ERR_DEVICE_TIMEOUT if a bounded
  * device-side wait expired in any call since the last check (that call's

@@ -234,3 +234,28 @@ def test_grouped_create_without_a_gpu_reports_no_device(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert gcreate(L, gcalls())[0] == DEVICE
+
+
+def test_tiled_weights_refusals_and_size(L):
+    # rows padded to 256, columns to 64: ceil(300/256)*2 row tiles x 48 column tiles x 16 KB
+    assert L.tq_weights_tiled_bytes(300, 3072) == 4 * 48 * 16384
+    assert L.tq_weights_tiled_bytes(256, 32) == 2 * 1 * 16384
+    assert L.tq_weights_tiled_bytes(1, 96) == 0                 # K not a valid row length
+    assert L.tq_weights_tiled_bytes(1, 16384 + 256) == 0        # above TQ_MAX_K_TILED
+    assert L.tq_tile_weights(FAKE, 16, 256, 5, FAKE, 1 << 20, S0) == BITS
+    assert L.tq_tile_weights(FAKE, 16, 96, 8, FAKE, 1 << 20, S0) == SHAPE
+    assert L.tq_tile_weights(0, 16, 256, 8, FAKE, 1 << 20, S0) == NULL
+    assert L.tq_tile_weights(FAKE, 16, 256, 8, FAKE, 100, S0) == WORKSPACE
+    assert L.tq_tile_weights(FAKE, 16, 256, 8, FAKE + 16, 1 << 20, S0) == ALIGN
+    assert L.tq_tile_weights(FAKE, 0, 256, 8, 0, 0, S0) == OK      # empty
+    tt = lambda **k: L.tq_linear_tt(*[k.get(n, d) for n, d in (
+        ("At", FAKE), ("sx", FAKE), ("M", 4), ("K", 512), ("Wt", FAKE), ("sw", FAKE), ("N", 256),
+        ("bits", 8), ("Y", FAKE), ("ytype", 0), ("ldy", 256), ("s", S0))])
+    assert tt(bits=3) == BITS
+    assert tt(ytype=7) == MODE
+    assert tt(K=96) == SHAPE
+    assert tt(Wt=0) == NULL
+    assert tt(At=FAKE + 16) == ALIGN
+    assert tt(Wt=FAKE + 16) == ALIGN
+    assert tt(ldy=100) == SHAPE
+    assert tt(M=0) == OK

@@ -246,6 +246,52 @@ def test_tiled_operand_matches_int8_path(tq, M, N, K, bits):
     assert np.array_equal(acc_t, ref_acc)
 
 
+@pytest.mark.parametrize("M,N,K,bits", [(300, 129, 3072, 8), (257, 300, 4096 + 32, 4), (1, 64, 288, 8),
+                                         (513, 520, 2304 + 64, 8), (64, 256, 12288, 4)])
+def test_tiled_weights_match_the_converting_product(tq, M, N, K, bits):
+    """Weights widened once into fp16 tiles (tq_tile_weights) give the same
+    exact int32 sums as the product that widens them itself, and the oracle's.
+    The tile buffer is filled with 0xFF first (fp16 NaN), so padding that was
+    not zeroed, or a pad row reaching an output, would show."""
+    import torch
+    X = to_dev_bf16(xgen(f"gpu/tt/x{M}x{K}", M, K, XD))
+    codes, sw = gpu_weights(tq, wgen(f"gpu/tt/w{N}x{K}", N, K, WD if bits == 8 else WB), bits)
+    At, sx = tq.rotate_quant_act_tiled(X)
+    Wt = torch.full((tq.weights_tiled_bytes(N, K),), 0xFF, dtype=torch.uint8, device="cuda")
+    tq.tile_weights(codes, N, K, bits, Wt=Wt)
+    acc_tt = to_np(tq.linear_tt(At, sx, M, K, Wt, sw, N, bits, out="i32"))
+    acc_t = to_np(tq.linear_tiled(At, sx, M, K, codes, sw, N, bits, out="i32"))
+    assert np.array_equal(acc_tt, acc_t)
+    Xq, sxq = tq.rotate_quant_act(X)
+    ref_acc, ref_Y = oracle.linear_a8(to_np(Xq), to_np(sxq), codes_np(codes, bits, K), to_np(sw))
+    assert np.array_equal(acc_tt, ref_acc)
+    Y = to_np(tq.linear_tt(At, sx, M, K, Wt, sw, N, bits))
+    assert rel_l2(Y, ref_Y) <= REL_L2_Y
+    assert tq.device_status() == 0
+
+
+@pytest.mark.parametrize("N,K", [(12288, 3072), (3072, 12288)])
+def test_tiled_weights_dit_m4032_sampled(tq, N, K):
+    """The DiT projections at full size through the both-tiled product, in the
+    launch configuration the bench times; sampled outputs against the oracle."""
+    M = 4032
+    X = xgen(f"gpu/ttdit/x{K}", M, K, XD)
+    W = wgen(f"gpu/ttdit/w{N}x{K}", N, K)
+    codes, sw = gpu_weights(tq, W, 8)
+    At, sx = tq.rotate_quant_act_tiled(to_dev_bf16(X))
+    Wt = tq.tile_weights(codes, N, K, 8)
+    acc = to_np(tq.linear_tt(At, sx, M, K, Wt, sw, N, 8, out="i32"))
+    Y = to_np(tq.linear_tt(At, sx, M, K, Wt, sw, N, 8))
+    rng = np.random.default_rng(7)
+    rows = np.sort(rng.choice(M, 24, replace=False))
+    Xq, sxq = tq.rotate_quant_act(to_dev_bf16(X))
+    pm = rng.integers(0, len(rows), 400)
+    pn = rng.integers(0, N, 400)
+    ref_acc, ref_Y = oracle.linear_a8_pairs(to_np(Xq)[rows], to_np(sxq)[rows], to_np(codes), to_np(sw), pm, pn)
+    assert np.array_equal(acc[rows[pm], pn], ref_acc)
+    assert rel_l2(Y[rows[pm], pn], ref_Y) <= REL_L2_Y
+
+
 @pytest.mark.parametrize("bits", [8, 4])
 def test_tiled_operand_flat_rows(tq, bits):
     """Rows whose rotation is flat (one nonzero per 256-group, so every rotated
