@@ -72,6 +72,7 @@ constexpr int B_RAW = HN * BK;         // 8 KB int8 codes (int4: half used)
 template <int MODE>
 struct Plan {
     static constexpr bool AT = MODE >= 1, BT = MODE == 2;
+    static constexpr int BAND = BT ? 8 : 0;         // tile order (tile_m / tile_n)
     static constexpr int O = BT ? 6 : (AT ? 5 : 4);   // operand ring depth
     static constexpr int R = BT ? 0 : (AT ? 6 : 4);   // raw ring depth
     static constexpr int NWARPS = AT ? 15 : 14;
@@ -116,8 +117,31 @@ struct TcParams {
 // Tile order: N fastest, so the pairs working at one time share a few strips
 // of A (each read from DRAM once) while all of B stays in L2; with M fastest,
 // every strip of A is in flight at once and a long-K product re-reads them.
-__device__ __forceinline__ int tile_m(int tile, const TcParams &p) { return tile / p.ntiles; }
-__device__ __forceinline__ int tile_n(int tile, const TcParams &p) { return tile % p.ntiles; }
+// Tile order: bands of BAND N-tiles (BAND 0: one band of all); inside a band
+// N fastest, then M.  The tiles in flight at once (one per CTA pair) then
+// share A strips (same M) and B strips (same band), so both stay in L2 while
+// the fp32 output streams out.  Measured: bands of 8 for the both-tiled
+// product, 1532 against 1402 TOPS on the DiT up projection; the converting
+// products do best with one band.
+template <int BAND>
+__device__ __forceinline__ int tile_m(int tile, const TcParams &p) {
+    if constexpr (BAND == 0) {
+        return tile / p.ntiles;
+    } else {
+        const int band = tile / (BAND * p.mtiles), r = tile - band * (BAND * p.mtiles);
+        return r / min(BAND, p.ntiles - band * BAND);
+    }
+}
+template <int BAND>
+__device__ __forceinline__ int tile_n(int tile, const TcParams &p) {
+    if constexpr (BAND == 0) {
+        return tile % p.ntiles;
+    } else {
+        const int band = tile / (BAND * p.mtiles), r = tile - band * (BAND * p.mtiles);
+        const int w = min(BAND, p.ntiles - band * BAND);
+        return band * BAND + r % w;
+    }
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -410,8 +434,8 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         if (!BT && lane == 0) {
             uint32_t it = 0;
             for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
-                const int m0 = tile_m(tile, p) * 2 * HM + static_cast<int>(rank) * HM;
-                const int n0 = tile_n(tile, p) * BN + static_cast<int>(rank) * HN;
+                const int m0 = tile_m<P::BAND>(tile, p) * 2 * HM + static_cast<int>(rank) * HM;
+                const int n0 = tile_n<P::BAND>(tile, p) * BN + static_cast<int>(rank) * HN;
                 for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
                     const int s = it % (BT ? 1 : RSTAGES);
                     if (!mbar_wait(raw_empty0 + 8 * s, ((it / (BT ? 1 : RSTAGES)) & 1) ^ 1, &abort_sh, p.status)) break;
@@ -433,8 +457,8 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             if (lane == 0) {
                 uint32_t it = 0;
                 for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
-                    const int mt = tile_m(tile, p) * 2 + static_cast<int>(rank);
-                    const int nt = tile_n(tile, p) * 2 + static_cast<int>(rank);
+                    const int mt = tile_m<P::BAND>(tile, p) * 2 + static_cast<int>(rank);
+                    const int nt = tile_n<P::BAND>(tile, p) * 2 + static_cast<int>(rank);
                     for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
                         const int s = it % OSTAGES;
                         if (!mbar_wait(op_empty0 + 8 * s, ((it / OSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
@@ -458,7 +482,7 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         if (lane == 0) {
             uint32_t it = 0;
             for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
-                const int64_t mt = static_cast<int64_t>(tile_m(tile, p)) * 2 + rank;
+                const int64_t mt = static_cast<int64_t>(tile_m<P::BAND>(tile, p)) * 2 + rank;
                 for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
                     const int s = it % OSTAGES;
                     if (!mbar_wait(op_empty0 + 8 * s, ((it / OSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
@@ -611,8 +635,8 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         const bool y16 = (reinterpret_cast<uintptr_t>(p.Y) & 15) == 0;
         const bool vec_ok = y16 && (p.ytype == 1 ? (p.ldy & 7) == 0 : (p.ldy & 3) == 0);
         for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters, ++tl) {
-            const int64_t m0 = static_cast<int64_t>(tile_m(tile, p)) * 2 * HM + rank * HM;
-            const int64_t n0 = static_cast<int64_t>(tile_n(tile, p)) * BN;
+            const int64_t m0 = static_cast<int64_t>(tile_m<P::BAND>(tile, p)) * 2 * HM + rank * HM;
+            const int64_t n0 = static_cast<int64_t>(tile_n<P::BAND>(tile, p)) * BN;
             const int64_t m = m0 + q * 32 + lane;
             const float xs = (p.ytype == 2 || m >= p.M) ? 1.0f : p.sx[m];
             // Y of this thread's row for output columns n0 + col .. + 31 from
