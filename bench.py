@@ -381,6 +381,11 @@ def dit_measure(device, reps=5, M=4032):
         At, sxt = tq.rotate_quant_act_tiled(X)
         At2 = torch.empty_like(At)
         sx2 = torch.empty_like(sxt)
+        # a DiT block's gated residual fused into the product, R + gate *
+        # product, written to a second bf16 buffer or in place
+        Rb = torch.zeros((M, p.N), dtype=torch.bfloat16, device=device)
+        Yb = torch.empty((M, p.N), dtype=torch.bfloat16, device=device)
+        gate = torch.full((p.N,), 0.5, dtype=torch.float32, device=device)
         for _ in range(3):
             tq.linear(X, codes, sw, p.N, 8, "W8A8", Y=Y, workspace=ws)
             tq.linear_tt(At, sxt, M, p.K, Wt, sw, p.N, 8, Y=Y)
@@ -389,7 +394,12 @@ def dit_measure(device, reps=5, M=4032):
                 "ms_tt": lambda: (tq.rotate_quant_act_tiled(X, At=At2, sx=sx2),
                                   tq.linear_tt(At2, sx2, M, p.K, Wt, sw, p.N, 8, Y=Y)),
                 "g": lambda: tq.linear_tiled(At, sxt, M, p.K, codes, sw, p.N, 8, Y=Y),
-                "g_tt": lambda: tq.linear_tt(At, sxt, M, p.K, Wt, sw, p.N, 8, Y=Y)}
+                "g_tt": lambda: tq.linear_tt(At, sxt, M, p.K, Wt, sw, p.N, 8, Y=Y),
+                "g_tt_bf16": lambda: tq.linear_tt(At, sxt, M, p.K, Wt, sw, p.N, 8, Y=Yb, out="bf16"),
+                "g_tt_res": lambda: tq.linear_tt_ex(At, sxt, M, p.K, Wt, sw, p.N, 8, Y=Yb, out="bf16",
+                                                    gate=gate, residual=Rb),
+                "g_tt_res_ip": lambda: tq.linear_tt_ex(At, sxt, M, p.K, Wt, sw, p.N, 8, Y=Rb, out="bf16",
+                                                       gate=gate, residual=Rb)}
         times = {k: [] for k in runs}
         for _ in range(reps):
             for k, fn in runs.items():
@@ -408,13 +418,16 @@ def dit_measure(device, reps=5, M=4032):
                        "tops_tiled_weights": round(ops / med["ms_tt"] / 1e9, 2),
                        "gemm_tops": round(ops / med["g"] / 1e9, 2),
                        "gemm_tiled_weights_ms": round(med["g_tt"], 4),
-                       "gemm_tiled_weights_tops": round(ops / med["g_tt"] / 1e9, 2)}
+                       "gemm_tiled_weights_tops": round(ops / med["g_tt"] / 1e9, 2),
+                       "gemm_tiled_weights_bf16_ms": round(med["g_tt_bf16"], 4),
+                       "gemm_tiled_weights_gated_residual_ms": round(med["g_tt_res"], 4),
+                       "gemm_tiled_weights_gated_residual_in_place_ms": round(med["g_tt_res_ip"], 4)}
         tot["ops"] += ops
         for k in ("ms", "ms_tt"):
             tot[k] += med[k]
         tot["g"] += med["g"]
         tot["g_tt"] += med["g_tt"]
-        del codes, sw, Wt, X, Y, ws, At, sxt, At2, sx2
+        del codes, sw, Wt, X, Y, ws, At, sxt, At2, sx2, Rb, Yb, gate
     o = tot["ops"] / 1e9
     return out, {"api": o / tot["ms"], "tiled_weights": o / tot["ms_tt"],
                  "gemm": o / tot["g"], "gemm_tiled_weights": o / tot["g_tt"]}

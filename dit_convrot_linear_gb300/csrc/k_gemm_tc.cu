@@ -112,11 +112,16 @@ struct TcParams {
     unsigned int *status;
     const unsigned char *At;   // pre-tiled fp16 A codes (AT path), else null
     const unsigned int *max_l1;  // largest row sum of |A codes| (tiled operand), or null
+    // epilogue: Y = R + g[n] * (sx sw acc + b[n]); any of them may be absent
+    const float *bias, *gate;
+    const void *R;
+    int64_t ldr;
+    int rtype;                 // 0 fp32, 1 bf16
+    int epi;                   // any of bias, gate, R given
+    int vcols;                 // sw, bias, gate all 16-byte aligned (float4 loads)
+    int vres;                  // R rows 16-byte aligned (16-byte loads)
 };
 
-// Tile order: N fastest, so the pairs working at one time share a few strips
-// of A (each read from DRAM once) while all of B stays in L2; with M fastest,
-// every strip of A is in flight at once and a long-K product re-reads them.
 // Tile order: bands of BAND N-tiles (BAND 0: one band of all); inside a band
 // N fastest, then M.  The tiles in flight at once (one per CTA pair) then
 // share A strips (same M) and B strips (same band), so both stay in L2 while
@@ -339,7 +344,7 @@ __device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-template <int BITS, int MODE>
+template <int BITS, int MODE, bool EPI = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Plan<MODE>::THREADS, 1)
 k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const TcParams p) {
@@ -381,7 +386,9 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         }
         for (int h = 0; h < 2; ++h) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(acc_full0 + 8 * h));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(acc_empty0 + 8 * h));
+            // the drain warps of both CTAs
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(acc_empty0 + 8 * h),
+                         "r"(EPI ? 24 : 8));
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done));
         if constexpr (AT && !BT) {
@@ -428,6 +435,219 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     }
     const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
     constexpr int BRAW = BITS == 8 ? B_RAW : B_RAW / 2;   // bytes of one raw B tile
+
+    // ---------------------------------------------------- epilogue (TMEM drain)
+    // A drain warp reads the TMEM lanes of its quarter (warp % 4) and takes the
+    // 32-column blocks slot, slot + nslots, ... of each tile.
+    auto drain = [&](int slot, int nslots) {
+        const int q = warp & 3;                       // TMEM lane quarter of this warp
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        uint32_t ch = 0, tl = 0;
+        const bool y16 = (reinterpret_cast<uintptr_t>(p.Y) & 15) == 0;
+        const bool vec_ok = y16 && (p.ytype == 1 ? (p.ldy & 7) == 0 : (p.ldy & 3) == 0);
+        for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters, ++tl) {
+            const int64_t m0 = static_cast<int64_t>(tile_m<P::BAND>(tile, p)) * 2 * HM + rank * HM;
+            const int64_t n0 = static_cast<int64_t>(tile_n<P::BAND>(tile, p)) * BN;
+            const int64_t m = m0 + q * 32 + lane;
+            const float xs = (p.ytype == 2 || m >= p.M) ? 1.0f : p.sx[m];
+            // Y of this thread's row for output columns n0 + col .. + 31 from
+            // their exact int32 sums
+            auto y_block = [&](int col, const uint32_t (&r)[32]) {
+                if (m >= p.M) return;
+                const int64_t nb = n0 + col;
+                if (p.ytype == 2) {
+                    int32_t *y = static_cast<int32_t *>(p.Y) + m * p.ldy + nb;
+                    if (vec_ok && nb + 32 <= p.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<uint4 *>(y + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+                    } else {
+                        for (int j = 0; j < 32; ++j)
+                            if (nb + j < p.N) y[j] = static_cast<int32_t>(r[j]);
+                    }
+                    return;
+                }
+                if constexpr (!EPI) {
+                    // all 32 scales loaded together, then the stores
+                    float f[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int64_t n = nb + j;
+                        const float wsc = n < p.N ? __ldg(p.sw + n) : 0.0f;
+                        f[j] = (xs * wsc) * static_cast<float>(static_cast<int>(r[j]));
+                    }
+                    if (p.ytype == 0) {
+                        float *y = static_cast<float *>(p.Y) + m * p.ldy + nb;
+                        if (vec_ok && nb + 32 <= p.N) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4)
+                                *reinterpret_cast<float4 *>(y + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+                        } else {
+                            for (int j = 0; j < 32; ++j)
+                                if (nb + j < p.N) y[j] = f[j];
+                        }
+                    } else {
+                        uint16_t *y = static_cast<uint16_t *>(p.Y) + m * p.ldy + nb;
+                        if (vec_ok && nb + 32 <= p.N) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 8) {
+                                uint4 u;
+                                u.x = f32_to_bf16_bits(f[j]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[j + 1])) << 16);
+                                u.y = f32_to_bf16_bits(f[j + 2]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[j + 3])) << 16);
+                                u.z = f32_to_bf16_bits(f[j + 4]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[j + 5])) << 16);
+                                u.w = f32_to_bf16_bits(f[j + 6]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[j + 7])) << 16);
+                                *reinterpret_cast<uint4 *>(y + j) = u;
+                            }
+                        } else {
+                            for (int j = 0; j < 32; ++j)
+                                if (nb + j < p.N) y[j] = f32_to_bf16_bits(f[j]);
+                        }
+                    }
+                } else {
+                // with the epilogue: eight columns at a time, values then their
+                // stores (few registers live, so it does not spill).  (Reading
+                // the block's whole residual first would spare an in-place
+                // update (R = Y) the L1 misses its own stores cause, but
+                // spills under the 128-register cap and costs more elsewhere.)
+#pragma unroll
+                for (int c = 0; c < 32; c += 8) {
+                    const int64_t nc = nb + c;
+                    float f[8];
+                    {
+                        // the chunk's loads issued together: column vectors as
+                        // float4 pairs and the residual as one or two 16-byte
+                        // loads when aligned, else element by element
+                        const bool whole8 = nc + 8 <= p.N;
+                        float wv[8], bv[8], gv[8], rv[8];
+                        auto cols = [&](const float *v, float (&o)[8], float absent) {
+                            if (v == nullptr) {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) o[j] = absent;
+                            } else if (whole8 && p.vcols) {
+                                const float4 a = __ldg(reinterpret_cast<const float4 *>(v + nc));
+                                const float4 b = __ldg(reinterpret_cast<const float4 *>(v + nc + 4));
+                                o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+                                o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) o[j] = nc + j < p.N ? __ldg(v + nc + j) : absent;
+                            }
+                        };
+                        cols(p.sw, wv, 0.0f);
+                        cols(p.bias, bv, 0.0f);
+                        cols(p.gate, gv, 1.0f);
+                        // R may be Y itself: this thread reads each element before writing it
+                        if (p.R == nullptr) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) rv[j] = 0.0f;
+                        } else if (p.rtype == 1) {
+                            const uint16_t *rr = static_cast<const uint16_t *>(p.R) + m * p.ldr + nc;
+                            if (whole8 && p.vres) {
+                                const uint4 u = *reinterpret_cast<const uint4 *>(rr);
+                                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    rv[2 * j] = __uint_as_float(w[j] << 16);
+                                    rv[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) rv[j] = nc + j < p.N ? bf16_bits_to_f32(rr[j]) : 0.0f;
+                            }
+                        } else {
+                            const float *rr = static_cast<const float *>(p.R) + m * p.ldr + nc;
+                            if (whole8 && p.vres) {
+                                const float4 a = *reinterpret_cast<const float4 *>(rr);
+                                const float4 b = *reinterpret_cast<const float4 *>(rr + 4);
+                                rv[0] = a.x; rv[1] = a.y; rv[2] = a.z; rv[3] = a.w;
+                                rv[4] = b.x; rv[5] = b.y; rv[6] = b.z; rv[7] = b.w;
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) rv[j] = nc + j < p.N ? rr[j] : 0.0f;
+                            }
+                        }
+                        // bias, then gate, then residual, in fp32
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            f[j] = rv[j] + gv[j] * ((xs * wv[j]) * static_cast<float>(static_cast<int>(r[c + j])) + bv[j]);
+                    }
+                    const bool whole = vec_ok && nc + 8 <= p.N;
+                    if (p.ytype == 0) {
+                        float *y = static_cast<float *>(p.Y) + m * p.ldy + nc;
+                        if (whole) {
+                            *reinterpret_cast<float4 *>(y) = make_float4(f[0], f[1], f[2], f[3]);
+                            *reinterpret_cast<float4 *>(y + 4) = make_float4(f[4], f[5], f[6], f[7]);
+                        } else {
+                            for (int j = 0; j < 8; ++j)
+                                if (nc + j < p.N) y[j] = f[j];
+                        }
+                    } else {
+                        uint16_t *y = static_cast<uint16_t *>(p.Y) + m * p.ldy + nc;
+                        if (whole) {
+                            uint4 u;
+                            u.x = f32_to_bf16_bits(f[0]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[1])) << 16);
+                            u.y = f32_to_bf16_bits(f[2]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[3])) << 16);
+                            u.z = f32_to_bf16_bits(f[4]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[5])) << 16);
+                            u.w = f32_to_bf16_bits(f[6]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[7])) << 16);
+                            *reinterpret_cast<uint4 *>(y) = u;
+                        } else {
+                            for (int j = 0; j < 8; ++j)
+                                if (nc + j < p.N) y[j] = f32_to_bf16_bits(f[j]);
+                        }
+                    }
+                }
+                }
+            };
+            if (single) {
+                // the tile's one chunk: fp32 sums, exact integers, straight to Y
+                const uint32_t buf = tl & 1;
+                if (!mbar_wait(acc_full0 + 8 * buf, (tl >> 1) & 1, &abort_sh, p.status)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                for (int col = 32 * slot; col < BN; col += 32 * nslots) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + 256u * buf + col, v);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[j])));
+                    y_block(col, v);
+                }
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive_leader(acc_empty0 + 8 * buf);
+                continue;
+            }
+            for (int c0 = 0; c0 < p.ksteps; c0 += cs, ++ch) {
+                const bool first = c0 == 0;
+                if (!mbar_wait(acc_full0, ch & 1, &abort_sh, p.status)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                for (int col = 32 * slot; col < BN; col += 32 * nslots) {
+                    uint32_t v[32], r[32];
+                    tmem_ld32(tmem + lane_base + col, v);
+                    if (!first) tmem_ld32(tmem + lane_base + RUN_COL + col, r);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int x = __float2int_rn(__uint_as_float(v[j]));
+                        r[j] = first ? static_cast<uint32_t>(x) : static_cast<uint32_t>(static_cast<int>(r[j]) + x);
+                    }
+                    tmem_st32(tmem + lane_base + RUN_COL + col, r);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive_leader(acc_empty0);
+            }
+            if (abort_sh) break;
+            // the tile's exact int32 sums are in the running region: write Y
+            for (int col = 32 * slot; col < BN; col += 32 * nslots) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + RUN_COL + col, r);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                y_block(col, r);
+            }
+        }
+        };
 
     if (warp == TMA_WARP) {
         // ------------------------------------------------ TMA producer
@@ -500,6 +720,10 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         __syncwarp();
         }
     } else if (warp < NCONV) {
+        if constexpr (EPI) {
+            // no conversion on this path: the converter warps help drain
+            drain(1 + warp / 4, 3);
+        }
         if constexpr (!BT) {
         // ------------------------------------------------ converters (shared -> shared)
         const int g = warp / WPG, tid = threadIdx.x % TPG;
@@ -628,120 +852,8 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue (TMEM drain)
-        const int q = warp & 3;                       // TMEM lane quarter of this warp
-        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        uint32_t ch = 0, tl = 0;
-        const bool y16 = (reinterpret_cast<uintptr_t>(p.Y) & 15) == 0;
-        const bool vec_ok = y16 && (p.ytype == 1 ? (p.ldy & 7) == 0 : (p.ldy & 3) == 0);
-        for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters, ++tl) {
-            const int64_t m0 = static_cast<int64_t>(tile_m<P::BAND>(tile, p)) * 2 * HM + rank * HM;
-            const int64_t n0 = static_cast<int64_t>(tile_n<P::BAND>(tile, p)) * BN;
-            const int64_t m = m0 + q * 32 + lane;
-            const float xs = (p.ytype == 2 || m >= p.M) ? 1.0f : p.sx[m];
-            // Y of this thread's row for output columns n0 + col .. + 31 from
-            // their exact int32 sums
-            auto y_block = [&](int col, const uint32_t (&r)[32]) {
-                if (m >= p.M) return;
-                const int64_t nb = n0 + col;
-                if (p.ytype == 2) {
-                    int32_t *y = static_cast<int32_t *>(p.Y) + m * p.ldy + nb;
-                    if (vec_ok && nb + 32 <= p.N) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<uint4 *>(y + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
-                    } else {
-                        for (int j = 0; j < 32; ++j)
-                            if (nb + j < p.N) y[j] = static_cast<int32_t>(r[j]);
-                    }
-                    return;
-                }
-                float f[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int64_t n = nb + j;
-                    const float wsc = n < p.N ? __ldg(p.sw + n) : 0.0f;
-                    f[j] = (xs * wsc) * static_cast<float>(static_cast<int>(r[j]));
-                }
-                if (p.ytype == 0) {
-                    float *y = static_cast<float *>(p.Y) + m * p.ldy + nb;
-                    if (vec_ok && nb + 32 <= p.N) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4 *>(y + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
-                    } else {
-                        for (int j = 0; j < 32; ++j)
-                            if (nb + j < p.N) y[j] = f[j];
-                    }
-                } else {
-                    uint16_t *y = static_cast<uint16_t *>(p.Y) + m * p.ldy + nb;
-                    if (vec_ok && nb + 32 <= p.N) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 8) {
-                            uint4 u;
-                            u.x = f32_to_bf16_bits(f[j]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[j + 1])) << 16);
-                            u.y = f32_to_bf16_bits(f[j + 2]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[j + 3])) << 16);
-                            u.z = f32_to_bf16_bits(f[j + 4]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[j + 5])) << 16);
-                            u.w = f32_to_bf16_bits(f[j + 6]) | (static_cast<uint32_t>(f32_to_bf16_bits(f[j + 7])) << 16);
-                            *reinterpret_cast<uint4 *>(y + j) = u;
-                        }
-                    } else {
-                        for (int j = 0; j < 32; ++j)
-                            if (nb + j < p.N) y[j] = f32_to_bf16_bits(f[j]);
-                    }
-                }
-            };
-            if (single) {
-                // the tile's one chunk: fp32 sums, exact integers, straight to Y
-                const uint32_t buf = tl & 1;
-                if (!mbar_wait(acc_full0 + 8 * buf, (tl >> 1) & 1, &abort_sh, p.status)) break;
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                for (int col = 0; col < BN; col += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + 256u * buf + col, v);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[j])));
-                    y_block(col, v);
-                }
-                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive_leader(acc_empty0 + 8 * buf);
-                continue;
-            }
-            for (int c0 = 0; c0 < p.ksteps; c0 += cs, ++ch) {
-                const bool first = c0 == 0;
-                if (!mbar_wait(acc_full0, ch & 1, &abort_sh, p.status)) break;
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                for (int col = 0; col < BN; col += 32) {
-                    uint32_t v[32], r[32];
-                    tmem_ld32(tmem + lane_base + col, v);
-                    if (!first) tmem_ld32(tmem + lane_base + RUN_COL + col, r);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int x = __float2int_rn(__uint_as_float(v[j]));
-                        r[j] = first ? static_cast<uint32_t>(x) : static_cast<uint32_t>(static_cast<int>(r[j]) + x);
-                    }
-                    tmem_st32(tmem + lane_base + RUN_COL + col, r);
-                }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive_leader(acc_empty0);
-            }
-            if (abort_sh) break;
-            // the tile's exact int32 sums are in the running region: write Y
-            for (int col = 0; col < BN; col += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + RUN_COL + col, r);
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                y_block(col, r);
-            }
-        }
+        drain(0, EPI ? 3 : 1);
     }
-
     // nobody leaves while the peer may still arrive on this CTA's barriers or
     // while MMAs of the pair are in flight (CTA 0 waited for them above)
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -758,7 +870,8 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
 template <int MODE>
 tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const unsigned char *Wt, const float *sx,
                     int64_t M, int64_t K, const uint8_t *Wq, const float *sw, int64_t N, int bits, void *Y,
-                    int ytype, int64_t ldy, const DeviceInfo &dev, cudaStream_t s) {
+                    int ytype, int64_t ldy, const DeviceInfo &dev, cudaStream_t s,
+                    const EpilogueArgs *ea = nullptr) {
     using P = Plan<MODE>;
     constexpr bool AT = P::AT;
     unsigned int *status = status_word();
@@ -796,11 +909,26 @@ tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const unsigned ch
     p.status = status;
     p.At = At;
     p.max_l1 = AT ? reinterpret_cast<const unsigned int *>(At + tiled_act_tiles_bytes(M, K)) : nullptr;
+    if (ea) {
+        p.bias = ea->bias;
+        p.gate = ea->gate;
+        p.R = ea->R;
+        p.ldr = ea->ldr;
+        p.rtype = ea->rtype;
+    }
+    p.epi = (p.bias || p.gate || p.R) ? 1 : 0;
+    auto a16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+    p.vcols = (a16(p.sw) && a16(p.bias) && a16(p.gate)) ? 1 : 0;
+    p.vres = (p.R && a16(p.R) && (p.ldr * (p.rtype == 1 ? 2 : 4)) % 16 == 0) ? 1 : 0;
     const int64_t tiles = static_cast<int64_t>(p.mtiles) * p.ntiles;
     if (tiles > (1ll << 30)) return TQ_ERR_OVERFLOW;
-    auto kern = bits == 8 ? k_gemm_a8_tc<8, MODE> : k_gemm_a8_tc<4, MODE>;
-    static bool configured_for[64][2] = {{false}};
-    const int bi = bits == 8 ? 0 : 1;
+    const bool epi = p.epi != 0;
+    if (epi && MODE != 2) return TQ_ERR_MODE;   // the epilogue is built for the both-tiled product
+    auto kern = MODE != 2 ? (bits == 8 ? k_gemm_a8_tc<8, MODE> : k_gemm_a8_tc<4, MODE>)
+              : epi ? (bits == 8 ? k_gemm_a8_tc<8, MODE, MODE == 2> : k_gemm_a8_tc<4, MODE, MODE == 2>)
+                    : (bits == 8 ? k_gemm_a8_tc<8, MODE> : k_gemm_a8_tc<4, MODE>);
+    static bool configured_for[64][4] = {{false}};
+    const int bi = (bits == 8 ? 0 : 1) + (epi ? 2 : 0);
     if (dev.id < 0 || dev.id >= 64) return TQ_ERR_DEVICE;
     if (!configured_for[dev.id][bi]) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -833,9 +961,9 @@ tq_status launch_gemm_a8_tiled(const void *At, const float *sx, int64_t M, int64
 
 tq_status launch_gemm_a8_tt(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
                             const float *sw, int64_t N, int bits, void *Y, int ytype, int64_t ldy,
-                            const DeviceInfo &dev, cudaStream_t s) {
+                            const DeviceInfo &dev, cudaStream_t s, const EpilogueArgs *ea) {
     return launch_tc<2>(nullptr, static_cast<const unsigned char *>(At), static_cast<const unsigned char *>(Wt),
-                        sx, M, K, nullptr, sw, N, bits, Y, ytype, ldy, dev, s);
+                        sx, M, K, nullptr, sw, N, bits, Y, ytype, ldy, dev, s, ea);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,

@@ -336,6 +336,12 @@ tq_status tq_tile_weights(const void *Wq, int64_t N, int64_t K, int bits, void *
 tq_status tq_linear_tt(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
                        const float *sw, int64_t N, int bits, void *Y, tq_out ytype, int64_t ldy,
                        cudaStream_t stream) {
+    return tq_linear_tt_ex(At, sx, M, K, Wt, sw, N, bits, nullptr, Y, ytype, ldy, stream);
+}
+
+tq_status tq_linear_tt_ex(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
+                          const float *sw, int64_t N, int bits, const tq_epilogue *epi, void *Y,
+                          tq_out ytype, int64_t ldy, cudaStream_t stream) {
     if (ytype != TQ_OUT_F32 && ytype != TQ_OUT_BF16 && ytype != TQ_OUT_I32) return TQ_ERR_MODE;
     if (bits != 8 && bits != 4) return TQ_ERR_BITS;
     if (M < 0 || N < 0 || !valid_k(K) || K > TQ_MAX_K_TILED) return TQ_ERR_SHAPE;
@@ -346,9 +352,35 @@ tq_status tq_linear_tt(const void *At, const float *sx, int64_t M, int64_t K, co
         return TQ_ERR_ALIGN;
     tq_status st = check_output(Y, M, N, ldy, out_size(ytype));
     if (st != TQ_OK) return st;
+    EpilogueArgs ea;
+    if (epi) {
+        if (ytype == TQ_OUT_I32) return TQ_ERR_MODE;
+        if (epi->rtype != TQ_OUT_F32 && epi->rtype != TQ_OUT_BF16) return TQ_ERR_MODE;
+        if ((epi->bias && !aligned(epi->bias, 4)) || (epi->gate && !aligned(epi->gate, 4))) return TQ_ERR_ALIGN;
+        if (epi->residual) {
+            const int rs = out_size(epi->rtype);
+            if ((st = check_output(epi->residual, M, N, epi->ldr, rs)) != TQ_OK) return st;
+            // the same buffer is an in-place update; any other overlap is refused
+            const uintptr_t r0 = reinterpret_cast<uintptr_t>(epi->residual);
+            const uintptr_t r1 = r0 + static_cast<uintptr_t>(((M - 1) * epi->ldr + N) * rs);
+            const uintptr_t y0 = reinterpret_cast<uintptr_t>(Y);
+            const uintptr_t y1 = y0 + static_cast<uintptr_t>(((M - 1) * ldy + N) * out_size(ytype));
+            if (r0 == y0) {
+                if (epi->ldr != ldy || epi->rtype != ytype) return TQ_ERR_SHAPE;
+            } else if (r0 < y1 && y0 < r1) {
+                return TQ_ERR_SHAPE;
+            }
+        }
+        ea.bias = epi->bias;
+        ea.gate = epi->gate;
+        ea.R = epi->residual;
+        ea.ldr = epi->ldr;
+        ea.rtype = epi->rtype == TQ_OUT_BF16 ? 1 : 0;
+    }
     DeviceInfo dev;
     if ((st = current_device(&dev)) != TQ_OK) return st;
-    return launch_gemm_a8_tt(At, sx, M, K, Wt, sw, N, bits, Y, static_cast<int>(ytype), ldy, dev, stream);
+    return launch_gemm_a8_tt(At, sx, M, K, Wt, sw, N, bits, Y, static_cast<int>(ytype), ldy, dev, stream,
+                             epi ? &ea : nullptr);
 }
 
 tq_status tq_device_status(cudaStream_t stream) {

@@ -83,9 +83,17 @@ int64_t grouped_weight_bytes(tq_grouped plan);
 
 int64_t weights_tiled_bytes(int64_t N, int64_t K);
 tq_status launch_tile_weights(const uint8_t *Wq, int64_t N, int64_t K, int bits, void *Wt, cudaStream_t s);
+// Optional epilogue of the A8 product: Y = R + gate[n] * (sx sw acc + bias[n]).
+struct EpilogueArgs {
+    const float *bias = nullptr;
+    const float *gate = nullptr;
+    const void *R = nullptr;
+    int64_t ldr = 0;
+    int rtype = 0;      // 0 fp32, 1 bf16
+};
 tq_status launch_gemm_a8_tt(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
                             const float *sw, int64_t N, int bits, void *Y, int ytype, int64_t ldy,
-                            const DeviceInfo &dev, cudaStream_t s);
+                            const DeviceInfo &dev, cudaStream_t s, const EpilogueArgs *ea = nullptr);
 
 int64_t tiled_act_tiles_bytes(int64_t M, int64_t K);
 int64_t tiled_act_bytes(int64_t M, int64_t K);

@@ -43,6 +43,7 @@ SIGNATURES = {
     "tq_weights_tiled_bytes": (_Z, [_I, _I]),
     "tq_tile_weights": (_C, [_P, _I, _I, _C, _P, _Z, _P]),
     "tq_linear_tt": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
+    "tq_linear_tt_ex": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _P, _C, _I, _P]),
     "tq_grouped_bytes": (_C, [_P, _I, _C, ctypes.POINTER(ctypes.c_size_t)]),
     "tq_grouped_create": (_C, [_P, _I, _C, _C, _P, _Z, ctypes.POINTER(ctypes.c_void_p)]),
     "tq_grouped_run": (_C, [_P, _P]),
@@ -51,6 +52,11 @@ SIGNATURES = {
     "tq_grouped_weight_bytes": (_I, [_P]),
     "tq_grouped_destroy": (None, [_P]),
 }
+
+
+class Epilogue(ctypes.Structure):
+    """``tq_epilogue``: Y = R + gate * (product + bias)."""
+    _fields_ = [("bias", _P), ("gate", _P), ("residual", _P), ("ldr", _I), ("rtype", _C)]
 
 
 class A16Call(ctypes.Structure):
@@ -307,6 +313,38 @@ def linear_tt(At, sx, M: int, K: int, Wt, sw, N: int, bits: int, Y=None, out: st
     _req(Y, "Y", dtype=_dt(out), rows=M, cols=N)
     _check(lib().tq_linear_tt(_ptr(At), _ptr(sx), M, K, _ptr(Wt), _ptr(sw), N, bits, _ptr(Y),
                               OUT[out], Y.stride(0), _stream(stream)), "tq_linear_tt")
+    return Y
+
+
+def linear_tt_ex(At, sx, M: int, K: int, Wt, sw, N: int, bits: int, Y=None, out: str = "f32",
+                 bias=None, gate=None, residual=None, stream=None):
+    """``linear_tt`` with the fused epilogue Y = residual + gate * (product + bias)
+    (each optional; ``residual`` may be ``Y`` itself)."""
+    import torch
+    if out not in ("f32", "bf16"):
+        raise ValueError("the epilogue writes f32 or bf16")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=_dt(out), device=At.device)
+    _req(At, "At", nbytes=act_tiled_bytes(M, K))
+    _req(sx, "sx", dtype=torch.float32, nbytes=4 * M)
+    _req(Wt, "Wt", nbytes=weights_tiled_bytes(N, K))
+    _req(sw, "sw", dtype=torch.float32, nbytes=4 * N)
+    _req(Y, "Y", dtype=_dt(out), rows=M, cols=N)
+    if bias is not None:
+        _req(bias, "bias", dtype=torch.float32, nbytes=4 * N)
+    if gate is not None:
+        _req(gate, "gate", dtype=torch.float32, nbytes=4 * N)
+    rtype, ldr = 0, 0
+    if residual is not None:
+        if residual.dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError("residual must be float32 or bfloat16")
+        _req(residual, "residual", dtype=residual.dtype, rows=M, cols=N)
+        rtype = OUT["f32" if residual.dtype == torch.float32 else "bf16"]
+        ldr = residual.stride(0)
+    epi = Epilogue(_ptr(bias), _ptr(gate), _ptr(residual), ldr, rtype)
+    _check(lib().tq_linear_tt_ex(_ptr(At), _ptr(sx), M, K, _ptr(Wt), _ptr(sw), N, bits,
+                                 ctypes.addressof(epi), _ptr(Y), OUT[out], Y.stride(0),
+                                 _stream(stream)), "tq_linear_tt_ex")
     return Y
 
 

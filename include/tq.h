@@ -243,6 +243,33 @@ tq_status tq_linear_tt(const void *At, const float *sx, int64_t M, int64_t K, co
                        cudaStream_t stream);
 
 /*
+ * Optional epilogue of the A8 product (tq_linear_tt_ex), computed in fp32:
+ *   Y[m][n] = R[m][n] + gate[n] * (sx[m] * sw[n] * acc[m][n] + bias[n]).
+ * Each of bias, gate and R may be absent: absent bias adds 0, absent gate is
+ * 1, absent R is 0.  This is a DiT block's gated residual, one of the row
+ * kernels next to the projections that the pages list as candidates for
+ * fusion (TensorFold PR #948, "What comes next").  Fused, the projection's
+ * output is never written and re-read by a separate kernel.
+ */
+typedef struct {
+    const float *bias;      /* fp32 [N], or NULL; 4-byte aligned */
+    const float *gate;      /* fp32 [N], or NULL; 4-byte aligned */
+    const void *residual;   /* [M, N] of rtype, row m at residual + m * ldr, or NULL.  It may
+                               be Y itself (an in-place update; then ldr == ldy and rtype ==
+                               ytype), but must not otherwise overlap Y */
+    int64_t ldr;            /* residual row stride (elements), >= N */
+    tq_out rtype;           /* TQ_OUT_F32 or TQ_OUT_BF16 */
+} tq_epilogue;
+
+/*
+ * tq_linear_tt with an epilogue.  epi == NULL is tq_linear_tt itself; with an
+ * epilogue, ytype is TQ_OUT_F32 or TQ_OUT_BF16 (not the raw int32 sums).
+ */
+tq_status tq_linear_tt_ex(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
+                          const float *sw, int64_t N, int bits, const tq_epilogue *epi, void *Y,
+                          tq_out ytype, int64_t ldy, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  Returns TQ_ERR_DEVICE_TIMEOUT if a bounded
  * device-side wait expired in any call since the last check (that call's

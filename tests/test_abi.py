@@ -259,3 +259,27 @@ def test_tiled_weights_refusals_and_size(L):
     assert tt(Wt=FAKE + 16) == ALIGN
     assert tt(ldy=100) == SHAPE
     assert tt(M=0) == OK
+
+
+def test_epilogue_refusals(L):
+    from dit_convrot_linear_gb300 import tq
+    Y = 0x100000
+    def ex(epi, ytype=0, ldy=256):
+        e = ctypes.addressof(epi) if epi is not None else None
+        return L.tq_linear_tt_ex(FAKE, FAKE, 4, 512, FAKE, FAKE, 256, 8, e, Y, ytype, ldy, S0)
+    E = lambda **k: tq.Epilogue(k.get("bias", 0), k.get("gate", 0), k.get("residual", 0),
+                                k.get("ldr", 256), k.get("rtype", 0))
+    assert ex(E(bias=FAKE), ytype=2) == MODE                   # no epilogue on raw int32 sums
+    assert ex(E(residual=FAKE, rtype=7)) == MODE
+    assert ex(E(bias=FAKE + 2)) == ALIGN
+    assert ex(E(gate=FAKE + 1)) == ALIGN
+    assert ex(E(residual=FAKE, ldr=100)) == SHAPE             # ldr < N
+    assert ex(E(residual=FAKE + 2, rtype=0)) == ALIGN          # fp32 residual on a 2-byte boundary
+    assert ex(E(residual=Y, ldr=512)) == SHAPE                 # the same buffer with another stride
+    assert ex(E(residual=Y, rtype=1)) == SHAPE                 # ... or another type
+    assert ex(E(residual=Y + 64)) == SHAPE                     # a partial overlap
+    import torch
+    if not torch.cuda.is_available():
+        assert ex(E(residual=Y)) == DEVICE                     # in place: accepted on the host
+        assert ex(E(bias=FAKE, gate=FAKE)) == DEVICE
+        assert ex(None) == DEVICE

@@ -292,6 +292,57 @@ def test_tiled_weights_dit_m4032_sampled(tq, N, K):
     assert rel_l2(Y[rows[pm], pn], ref_Y) <= REL_L2_Y
 
 
+@pytest.mark.parametrize("M,N,K,bits,parts", [
+    (300, 129, 3072, 8, "bgr32"), (257, 300, 4096 + 32, 4, "bgr16"), (64, 256, 512, 8, "b"),
+    (130, 200, 896, 8, "g"), (513, 520, 2304 + 64, 8, "r16")])
+def test_tiled_weights_fused_epilogue(tq, M, N, K, bits, parts):
+    """Y = R + gate * (product + bias) in the product's epilogue, against the
+    oracle's product with the same formula in fp64 (fp32 and bf16 residuals)."""
+    import torch
+    X = to_dev_bf16(xgen(f"gpu/epi/x{M}x{K}", M, K, XD))
+    codes, sw = gpu_weights(tq, wgen(f"gpu/epi/w{N}x{K}", N, K, WD if bits == 8 else WB), bits)
+    At, sx = tq.rotate_quant_act_tiled(X)
+    Wt = tq.tile_weights(codes, N, K, bits)
+    rng = np.random.default_rng(M + N)
+    bias = torch.from_numpy(rng.normal(0, 2.0, N).astype(np.float32)).cuda() if "b" in parts else None
+    gate = torch.from_numpy(rng.normal(0, 1.0, N).astype(np.float32)).cuda() if "g" in parts else None
+    R = None
+    if "r" in parts:
+        Rn = rng.normal(0, 30.0, (M, N)).astype(np.float32)
+        R = torch.from_numpy(Rn).cuda()
+        if parts.endswith("16"):
+            R = R.to(torch.bfloat16)
+    Y = tq.linear_tt_ex(At, sx, M, K, Wt, sw, N, bits, bias=bias, gate=gate, residual=R)
+    Xq, sxq = tq.rotate_quant_act(X)
+    _, Y0 = oracle.linear_a8(to_np(Xq), to_np(sxq), codes_np(codes, bits, K), to_np(sw))
+    b = to_np(bias).astype(np.float64) if bias is not None else 0.0
+    g = to_np(gate).astype(np.float64) if gate is not None else 1.0
+    r = to_np(R.float()).astype(np.float64) if R is not None else 0.0
+    ref = r + g * (Y0 + b)
+    assert rel_l2(to_np(Y), ref) <= REL_L2_Y
+    assert tq.device_status() == 0
+
+
+def test_tiled_weights_epilogue_in_place_bf16(tq):
+    """The residual stream updated in place (R is Y, bf16): each output within
+    one bf16 ulp of the oracle's value rounded to bf16."""
+    import torch
+    M, N, K = 260, 384, 3072
+    X = to_dev_bf16(xgen("gpu/epiip/x", M, K, XD))
+    codes, sw = gpu_weights(tq, wgen("gpu/epiip/w", N, K), 8)
+    At, sx = tq.rotate_quant_act_tiled(X)
+    Wt = tq.tile_weights(codes, N, K, 8)
+    rng = np.random.default_rng(5)
+    gate = torch.from_numpy(rng.normal(0, 1.0, N).astype(np.float32)).cuda()
+    R = torch.from_numpy(rng.normal(0, 30.0, (M, N)).astype(np.float32)).cuda().to(torch.bfloat16)
+    r = to_np(R.float()).astype(np.float64)
+    tq.linear_tt_ex(At, sx, M, K, Wt, sw, N, 8, Y=R, out="bf16", gate=gate, residual=R)
+    Xq, sxq = tq.rotate_quant_act(X)
+    _, Y0 = oracle.linear_a8(to_np(Xq), to_np(sxq), to_np(codes), to_np(sw))
+    ref = r + to_np(gate).astype(np.float64) * Y0
+    assert bf16_ulp_diff(bf16_bits(R), oracle.round_bf16(ref)).max() <= 1
+
+
 @pytest.mark.parametrize("bits", [8, 4])
 def test_tiled_operand_flat_rows(tq, bits):
     """Rows whose rotation is flat (one nonzero per 256-group, so every rotated
