@@ -67,6 +67,8 @@ _SIGS = {
     "or_linear_a16_pairs": (ctypes.c_int, [_P, _I, _I, _P, _P, _I, _P, _P, _I, _P,
                                            ctypes.c_int]),
     "or_matmul_f64": (ctypes.c_int, [_P, _I, _I, _P, _I, _P, ctypes.c_int]),
+    "or_swiglu_f64": (ctypes.c_int, [_P, _P, _I, _P]),
+    "or_swiglu_bf16": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _P]),
 }
 
 
@@ -302,6 +304,28 @@ def linear_a16_pairs(Xr, Wcodes, sw, pm, pn):
                                      pn.ctypes.data, pm.size, Y.ctypes.data,
                                      threads()), "linear_a16_pairs")
     return Y
+
+
+def swiglu_f64(g, u) -> np.ndarray:
+    """O8 in fp64: silu(g) * u, silu(g) = g / (1 + e^-g)."""
+    g, u = _c(g, np.float64), _c(u, np.float64)
+    h = np.empty(g.shape, dtype=np.float64)
+    _check(lib().or_swiglu_f64(g.ctypes.data, u.ctypes.data, g.size, h.ctypes.data), "swiglu_f64")
+    return h
+
+
+def swiglu_bf16(G: np.ndarray, U: np.ndarray) -> np.ndarray:
+    """O8: bf16 G, U [M, K] -> bf16 bits of silu(G) * U [M, K]."""
+    G, U = _c(G, np.uint16), _c(U, np.uint16)
+    M, K = G.shape
+    H = np.empty((M, K), dtype=np.uint16)
+    _check(lib().or_swiglu_bf16(G.ctypes.data, K, U.ctypes.data, K, M, K, H.ctypes.data), "swiglu_bf16")
+    return H
+
+
+def swiglu_quant_act(G: np.ndarray, U: np.ndarray):
+    """O8 then O1+O2+O4: the down projection's A8 operand from gate and up."""
+    return rotate_quant_act(swiglu_bf16(G, U))
 
 
 def matmul_f64(A, B):

@@ -34,6 +34,12 @@
  *   O6 A16 product: Y = s_w * sum_k q_w * x'_bf16 in fp64.
  *   O7 int4 packing: byte k/2 of a row holds code k (even) in its low nibble and
  *      code k+1 in its high nibble, two's complement.
+ *   O8 SwiGLU (the row kernel between a gate/up product and the down product;
+ *      the pages name it among the row kernels next to the projections,
+ *      TensorFold PR #948, "What comes next"): h = silu(g) * u with
+ *      silu(g) = g / (1 + e^-g), the gated unit of Shazeer, "GLU Variants
+ *      Improve Transformer" (2020), in fp64 from bf16 g and u, then rounded
+ *      to the nearest bf16 (the activations are bf16).
  *
  * Readings where the pages are silent (each listed in the design notes):
  *   Sylvester order and 1/sqrt(n) normalisation; a last group narrower than
@@ -404,5 +410,27 @@ int or_matmul_f64(const double *A, int64_t M, int64_t K, const double *B,
                   int64_t N, double *Y, int nthreads) {
     mm_arg a = {A, B, M, K, N, Y};
     parallel_for(N, nthreads, mm_cols, &a);
+    return 0;
+}
+
+/* -------------------------------------------------------------------------- */
+/* O8 SwiGLU                                                                   */
+
+int or_swiglu_f64(const double *g, const double *u, int64_t n, double *h) {
+    for (int64_t i = 0; i < n; ++i) h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
+    return 0;
+}
+
+/* H [M, K] dense bf16 bits from bf16 G, U [M, K] with row strides ldg, ldu. */
+int or_swiglu_bf16(const uint16_t *G, int64_t ldg, const uint16_t *U, int64_t ldu, int64_t M,
+                   int64_t K, uint16_t *H) {
+    fesetround(FE_TONEAREST);
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            const double g = or_bf16_to_f64(G[m * ldg + k]), u = or_bf16_to_f64(U[m * ldu + k]);
+            double h;
+            or_swiglu_f64(&g, &u, 1, &h);
+            H[m * K + k] = or_f64_to_bf16(h);
+        }
     return 0;
 }
