@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 import test_oracle_pins as pins
+import test_oracle_swiglu as swiglu_pins
 
 MUTANTS = {
     "sign_of_hadamard": ("& 1) ? -1 : 1", "& 1) ? 1 : -1"),
@@ -43,6 +44,9 @@ MUTANTS = {
     "a16_wrong_index": ("s += (double)w[k] * or_bf16_to_f64(x[k]);",
                         "s += (double)w[k] * or_bf16_to_f64(x[k ^ 1]);"),
     "bf16_truncates": ("nearbyint(ldexp(a, -q))", "floor(ldexp(a, -q))"),
+    "silu_sigmoid_of_minus_g": ("g[i] / (1.0 + exp(-g[i])) * u[i]", "g[i] / (1.0 + exp(g[i])) * u[i]"),
+    "swiglu_plain_sigmoid_gate": ("g[i] / (1.0 + exp(-g[i])) * u[i]", "1.0 / (1.0 + exp(-g[i])) * u[i]"),
+    "swiglu_gate_and_up_swapped": ("g[i] / (1.0 + exp(-g[i])) * u[i]", "u[i] / (1.0 + exp(-u[i])) * g[i]"),
 }
 
 PIN_TESTS = [
@@ -63,6 +67,9 @@ PIN_TESTS = [
     lambda: pins.test_a8_product_brute_force(),
     lambda: pins.test_a16_product_brute_force(),
     lambda: pins.test_bf16_rounding_matches_exact_nearest(),
+    lambda: swiglu_pins.test_silu_odd_part_is_the_identity(),
+    lambda: swiglu_pins.test_silu_special_values(),
+    lambda: swiglu_pins.test_swiglu_is_linear_in_up(),
 ]
 
 

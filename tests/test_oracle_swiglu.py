@@ -1,10 +1,11 @@
 """Pins of the oracle's SwiGLU step (O8), from the mathematics of the gated
 unit (Shazeer, "GLU Variants Improve Transformer", 2020: silu(g) * u with
 silu(g) = g * sigmoid(g)), not from a retyped formula:
-  - silu(g) - silu(-g) = g, since sigmoid(g) + sigmoid(-g) = 1 (catches a sign
-    error or sigmoid(-g) in place of sigmoid(g));
+  - silu(g) - silu(-g) = g, since sigmoid(g) + sigmoid(-g) = 1 (catches a
+    sign error on g);
   - silu(0) = 0, silu(g) -> g for large g and -> 0 for very negative g;
-  - sigmoid(ln 3) = 3/4, so silu(ln 3) = 0.75 ln 3;
+  - sigmoid(ln 3) = 3/4, so silu(ln 3) = 0.75 ln 3 (catches sigmoid(-g) in
+    place of sigmoid(g), a plain sigmoid gate, and gate and up swapped);
   - h is linear in u: doubling u doubles h exactly;
   - the bf16 output is the fp64 value rounded once (the rounding itself is
     pinned with the other bf16 tests)."""
