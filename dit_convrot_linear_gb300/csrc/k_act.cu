@@ -63,24 +63,53 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// SwiGLU of one gate value g and up value u, h = silu(g) * u with
+// silu(g) = g / (1 + e^-g) (Shazeer, "GLU Variants Improve Transformer"), in
+// fp32; the caller rounds h to bf16, as an unfused SwiGLU kernel would store it.
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// Two bf16 values a word: h = bf16(silu(g) * u) of the gate word and up word.
+__device__ __forceinline__ uint32_t swiglu_word(uint32_t gw, uint32_t uw) {
+    const float h0 = silu_mul(__uint_as_float(gw << 16), __uint_as_float(uw << 16));
+    const float h1 = silu_mul(__uint_as_float(gw & 0xFFFF0000u), __uint_as_float(uw & 0xFFFF0000u));
+    return f32_to_bf16_bits(h0) | (static_cast<uint32_t>(f32_to_bf16_bits(h1)) << 16);
+}
+
+// The lane's E bf16 values (E = 8, 4, 2, 1) at src as packed words; with
+// SWIGLU, those of h = bf16(silu(g) * u), g at src and u at src + up_off.
+template <bool SWIGLU>
+__device__ __forceinline__ void lane_words(const unsigned char *src, int up_off, int E, uint32_t (&w)[4]) {
+    auto load = [&](const unsigned char *a, uint32_t (&o)[4]) {
+        o[0] = o[1] = o[2] = o[3] = 0u;
+        if (E == 8) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(a);
+            o[0] = u.x; o[1] = u.y; o[2] = u.z; o[3] = u.w;
+        } else if (E == 4) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(a);
+            o[0] = u.x; o[1] = u.y;
+        } else if (E == 2) {
+            o[0] = *reinterpret_cast<const uint32_t *>(a);
+        } else {
+            o[0] = *reinterpret_cast<const uint16_t *>(a);
+        }
+    };
+    load(src, w);
+    if constexpr (SWIGLU) {
+        uint32_t u[4];
+        load(src + up_off, u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = swiglu_word(w[i], u[i]);
+    }
+}
+
 // Rotate one group (width n = 32*E) read from a shared-memory row buffer:
 // v = c_n * Hs_n * x in fp32, the same butterfly and scale as the global path.
-__device__ __forceinline__ int rotate_group_shared(const unsigned char *grp, int n, float (&v)[8]) {
+template <bool SWIGLU>
+__device__ __forceinline__ int rotate_group_shared(const unsigned char *grp, int up_off, int n, float (&v)[8]) {
     const int lane = threadIdx.x & 31;
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    uint32_t w[4];
     const int E = n >> 5;
-    const unsigned char *src = grp + lane * E * 2;
-    if (E == 8) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(src);
-        w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
-    } else if (E == 4) {
-        const uint2 u = *reinterpret_cast<const uint2 *>(src);
-        w[0] = u.x; w[1] = u.y;
-    } else if (E == 2) {
-        w[0] = *reinterpret_cast<const uint32_t *>(src);
-    } else {
-        w[0] = *reinterpret_cast<const uint16_t *>(src);
-    }
+    lane_words<SWIGLU>(grp + lane * E * 2, up_off, E, w);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         v[2 * i] = __uint_as_float(w[i] << 16);
@@ -115,10 +144,11 @@ __device__ __forceinline__ void store_codes(int8_t *dst, int e_per_lane, const f
 
 // Unnormalised transform (Hs x, Sylvester order) of one full 256-group read
 // from a shared-memory row buffer: 8 values a lane.
-__device__ __forceinline__ void fwht256_shared(const unsigned char *grp, float (&v)[8]) {
+template <bool SWIGLU>
+__device__ __forceinline__ void fwht256_shared(const unsigned char *grp, int up_off, float (&v)[8]) {
     const int lane = threadIdx.x & 31;
-    const uint4 u = *reinterpret_cast<const uint4 *>(grp + lane * 16);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t w[4];
+    lane_words<SWIGLU>(grp + lane * 16, up_off, 8, w);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         v[2 * i] = __uint_as_float(w[i] << 16);
@@ -191,12 +221,15 @@ __device__ __forceinline__ void put_tiled(uint16_t *At, int64_t KT, int64_t K, i
 // one bulk copy that completes on that buffer's barrier.  Warp w owns groups
 // w, w + 8, ...; the first GPW stay in registers between the amax pass and
 // the quantise pass, further ones are recomputed from the buffer.
-template <int GPW, bool TILED, int NT>
+// SWIGLU: the row is h = bf16(silu(g) * u), gate rows from X (ldx) and up
+// rows from U (ldu); a buffer then holds a gate row and an up row.
+template <int GPW, bool TILED, int NT, bool SWIGLU = false>
 __global__ void __launch_bounds__(NT)
 k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx,
                     void *__restrict__ out, float *__restrict__ sx, int S,
-                    unsigned int *status, unsigned int *max_l1) {
-    extern __shared__ __align__(128) unsigned char ring[];   // [S][2K] then S barriers
+                    unsigned int *status, unsigned int *max_l1, const uint16_t *__restrict__ U,
+                    int64_t ldu) {
+    extern __shared__ __align__(128) unsigned char ring[];   // [S][2K or 4K] then S barriers
     __shared__ float red[NT / 32];
     __shared__ unsigned int win[16];   // a row's sum of |codes| per 1024-column window
     __shared__ int abort_sh;
@@ -206,20 +239,30 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
     const int tail = static_cast<int>(K % kGroup);        // 0, 32, 64 or 128
     const int tail_warp = static_cast<int>(Gf % W);
     const uint32_t row_bytes = static_cast<uint32_t>(K * 2);
+    const uint32_t slot_bytes = SWIGLU ? 2 * row_bytes : row_bytes;
+    const int up_off = static_cast<int>(row_bytes);   // the up row, after the gate row (SWIGLU)
     const uint32_t ring0 = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
-    const uint32_t bar0 = ring0 + static_cast<uint32_t>(S) * row_bytes;
+    const uint32_t bar0 = ring0 + static_cast<uint32_t>(S) * slot_bytes;
     const int64_t nrows = blockIdx.x < M ? (M - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
     auto issue = [&](int64_t i) {   // thread 0: row i of this CTA into buffer i % S
         const int slot = static_cast<int>(i % S);
         const uint32_t bar = bar0 + 8u * slot;
-        const uint16_t *src = X + (blockIdx.x + i * gridDim.x) * ldx;
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(row_bytes)
+        const int64_t m = blockIdx.x + i * gridDim.x;
+        const uint16_t *src = X + m * ldx;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(slot_bytes)
                      : "memory");
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-            ::"r"(ring0 + static_cast<uint32_t>(slot) * row_bytes), "l"(src), "r"(row_bytes), "r"(bar)
+            ::"r"(ring0 + static_cast<uint32_t>(slot) * slot_bytes), "l"(src), "r"(row_bytes), "r"(bar)
             : "memory");
+        if constexpr (SWIGLU) {
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                ::"r"(ring0 + static_cast<uint32_t>(slot) * slot_bytes + row_bytes), "l"(U + m * ldu),
+                  "r"(row_bytes), "r"(bar)
+                : "memory");
+        }
     };
 
     if (threadIdx.x < 16) win[threadIdx.x] = 0;
@@ -247,7 +290,7 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
         }
         __syncthreads();
         if (abort_sh) break;
-        const unsigned char *buf = ring + static_cast<size_t>(slot) * row_bytes;
+        const unsigned char *buf = ring + static_cast<size_t>(slot) * slot_bytes;
         const int64_t m = blockIdx.x + i * gridDim.x;
 
         // Pass 1: the full 256-groups unscaled (Hs x; their factor 1/16 is a
@@ -258,21 +301,21 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
         for (int j = 0; j < GPW; ++j) {
             const int64_t g = warp + static_cast<int64_t>(j) * W;
             if (g < Gf) {
-                fwht256_shared(buf + g * kGroup * 2, v[j]);
+                fwht256_shared<SWIGLU>(buf + g * kGroup * 2, up_off, v[j]);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) amax_full = fmaxf(amax_full, fabsf(v[j][e]));
             }
         }
         for (int64_t g = warp + static_cast<int64_t>(GPW) * W; g < Gf; g += W) {
             float t[8];
-            fwht256_shared(buf + g * kGroup * 2, t);
+            fwht256_shared<SWIGLU>(buf + g * kGroup * 2, up_off, t);
 #pragma unroll
             for (int e = 0; e < 8; ++e) amax_full = fmaxf(amax_full, fabsf(t[e]));
         }
         float vt[8];
         int Et = 0;
         if (tail && warp == tail_warp) {
-            Et = rotate_group_shared(buf + Gf * kGroup * 2, tail, vt);
+            Et = rotate_group_shared<SWIGLU>(buf + Gf * kGroup * 2, up_off, tail, vt);
 #pragma unroll
             for (int e = 0; e < 8; ++e) amax_tail = fmaxf(amax_tail, fabsf(vt[e]));
         }
@@ -320,7 +363,7 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
         }
         for (int64_t g = warp + static_cast<int64_t>(GPW) * W; g < Gf; g += W) {
             float t[8], q[8];
-            fwht256_shared(buf + g * kGroup * 2, t);
+            fwht256_shared<SWIGLU>(buf + g * kGroup * 2, up_off, t);
 #pragma unroll
             for (int e = 0; e < 8; ++e) q[e] = code_of(t[e], 0.0625f, r16, s);
             put(g, 8, q);
@@ -458,9 +501,9 @@ k_rotate_bf16(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx,
     }
 }
 
-template <bool TILED>
+template <bool TILED, bool SWIGLU = false>
 tq_status launch_ring(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void *out, float *sx,
-                      unsigned int *max_l1, cudaStream_t s) {
+                      unsigned int *max_l1, cudaStream_t s, const uint16_t *U = nullptr, int64_t ldu = 0) {
     const int64_t G = (K + kGroup - 1) / kGroup;
     // rows of up to 16 groups: CTAs of 4 warps, more of them, so that more
     // rows are in flight per SM; longer rows: 8 warps
@@ -473,24 +516,26 @@ tq_status launch_ring(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void
     unsigned int *status = status_word();
     if (!status) return TQ_ERR_DEVICE;
     // rows in flight per CTA: about 48 KB of them (24 KB with 4 warps), 2 to 8 rows
-    const int64_t rb = 2 * K;
+    // (a gate and an up row per buffer with SWIGLU)
+    const int64_t rb = (SWIGLU ? 4 : 2) * K;
     int S = static_cast<int>(((small ? 24 : 48) * 1024) / rb);
     S = S < 2 ? 2 : (S > 8 ? 8 : S);
     const size_t smem = static_cast<size_t>(S) * rb + 8 * S;
     auto pick = [&](auto nt) {
         constexpr int N = decltype(nt)::value;
-        return gpw <= 1 ? k_rotate_quant_ring<1, TILED, N>
-             : gpw <= 2 ? k_rotate_quant_ring<2, TILED, N>
-             : gpw <= 4 ? k_rotate_quant_ring<4, TILED, N>
-                        : k_rotate_quant_ring<8, TILED, N>;
+        return gpw <= 1 ? k_rotate_quant_ring<1, TILED, N, SWIGLU>
+             : gpw <= 2 ? k_rotate_quant_ring<2, TILED, N, SWIGLU>
+             : gpw <= 4 ? k_rotate_quant_ring<4, TILED, N, SWIGLU>
+                        : k_rotate_quant_ring<8, TILED, N, SWIGLU>;
     };
     auto kern = small ? pick(std::integral_constant<int, 128>{}) : pick(std::integral_constant<int, 256>{});
     const int ki = (gpw <= 1 ? 0 : gpw <= 2 ? 1 : gpw <= 4 ? 2 : 3) + (small ? 4 : 0);
     static bool configured[64][8] = {{false}};
     if (dev.id < 0 || dev.id >= 64) return TQ_ERR_DEVICE;
     if (!configured[dev.id][ki]) {
+        // the largest ring: two of the longest rows (gate and up rows with SWIGLU)
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(kRingMaxK * 2 * 2 + 64));
+                                                   static_cast<int>(kRingMaxK * (SWIGLU ? 4 : 2) * 2 + 64));
         if (e != cudaSuccess) return cuda_fail(e);
         configured[dev.id][ki] = true;
     }
@@ -502,7 +547,7 @@ tq_status launch_ring(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void
     per_sm = per_sm < 1 ? 1 : (per_sm > cap ? cap : per_sm);
     const int64_t want = static_cast<int64_t>(dev.sms) * per_sm;
     const unsigned grid = static_cast<unsigned>(M < want ? M : want);
-    kern<<<grid, NT, smem, s>>>(X, M, K, ldx, out, sx, S, status, max_l1);
+    kern<<<grid, NT, smem, s>>>(X, M, K, ldx, out, sx, S, status, max_l1, U, ldu);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
@@ -524,6 +569,17 @@ tq_status launch_rotate_quant_tiled(const uint16_t *X, int64_t M, int64_t K, int
     const cudaError_t e = cudaMemsetAsync(max_l1, 0, 6 * sizeof(unsigned int), s);
     if (e != cudaSuccess) return cuda_fail(e);
     return launch_ring<true>(X, M, K, ldx, At, sx, max_l1, s);
+}
+
+tq_status launch_swiglu_quant_tiled(const uint16_t *G, int64_t ldg, const uint16_t *U, int64_t ldu,
+                                    int64_t M, int64_t K, void *At, float *sx, cudaStream_t s) {
+    if (M == 0) return TQ_OK;
+    if (K > kRingMaxK) return TQ_ERR_SHAPE;
+    unsigned int *max_l1 = reinterpret_cast<unsigned int *>(static_cast<unsigned char *>(At) +
+                                                            tiled_act_tiles_bytes(M, K));
+    const cudaError_t e = cudaMemsetAsync(max_l1, 0, 6 * sizeof(unsigned int), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return launch_ring<true, true>(G, M, K, ldg, At, sx, max_l1, s, U, ldu);
 }
 
 tq_status launch_rotate_quant_act(const uint16_t *X, int64_t M, int64_t K,

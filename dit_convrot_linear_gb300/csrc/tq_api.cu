@@ -292,6 +292,24 @@ tq_status tq_rotate_quant_act_tiled(const void *X, int64_t M, int64_t K, int64_t
     return launch_rotate_quant_tiled(static_cast<const uint16_t *>(X), M, K, ldx, At, sx, stream);
 }
 
+tq_status tq_swiglu_quant_act_tiled(const void *G, int64_t ldg, const void *U, int64_t ldu, int64_t M,
+                                    int64_t K, void *At, size_t at_bytes, float *sx, cudaStream_t stream) {
+    if (M < 0 || !valid_k(K) || K > TQ_MAX_K_TILED) return TQ_ERR_SHAPE;
+    if (M == 0) return TQ_OK;
+    tq_status st = check_bf16_rows(G, M, K, ldg);
+    if (st != TQ_OK) return st;
+    if ((st = check_bf16_rows(U, M, K, ldu)) != TQ_OK) return st;
+    if (!At || !sx) return TQ_ERR_NULL;
+    const size_t need = tq_act_tiled_bytes(M, K);
+    if (need == 0) return TQ_ERR_OVERFLOW;
+    if (at_bytes < need) return TQ_ERR_WORKSPACE;
+    if (!aligned(At, 256) || !aligned(sx, 4)) return TQ_ERR_ALIGN;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    return launch_swiglu_quant_tiled(static_cast<const uint16_t *>(G), ldg, static_cast<const uint16_t *>(U),
+                                     ldu, M, K, At, sx, stream);
+}
+
 tq_status tq_linear_tiled(const void *At, const float *sx, int64_t M, int64_t K, const void *Wq,
                           const float *sw, int64_t N, int bits, void *Y, tq_out ytype, int64_t ldy,
                           cudaStream_t stream) {

@@ -40,6 +40,7 @@ SIGNATURES = {
     "tq_act_tiled_bytes": (_Z, [_I, _I]),
     "tq_rotate_quant_act_tiled": (_C, [_P, _I, _I, _I, _P, _Z, _P, _P]),
     "tq_linear_tiled": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
+    "tq_swiglu_quant_act_tiled": (_C, [_P, _I, _P, _I, _I, _I, _P, _Z, _P, _P]),
     "tq_weights_tiled_bytes": (_Z, [_I, _I]),
     "tq_tile_weights": (_C, [_P, _I, _I, _C, _P, _Z, _P]),
     "tq_linear_tt": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
@@ -262,6 +263,29 @@ def rotate_quant_act_tiled(X, At=None, sx=None, stream=None):
     _req(sx, "sx", dtype=torch.float32, nbytes=4 * M)
     _check(lib().tq_rotate_quant_act_tiled(_ptr(X), M, K, X.stride(0), _ptr(At), _nbytes(At),
                                            _ptr(sx), _stream(stream)), "tq_rotate_quant_act_tiled")
+    return At, sx
+
+
+def swiglu_quant_act_tiled(G, U, At=None, sx=None, stream=None):
+    """The down projection's input from gate G and up U (bf16 [M, K], any row
+    stride): bf16(silu(G) * U), rotated and quantised into the tiled operand.
+    Returns (At, sx) for linear_tiled / linear_tt."""
+    import torch
+    M, K = G.shape
+    if tuple(U.shape) != (M, K):
+        raise ValueError(f"U is {tuple(U.shape)}, expected {(M, K)}")
+    need = act_tiled_bytes(M, K)
+    if At is None:
+        At = torch.empty(max(need, 1), dtype=torch.uint8, device=G.device)
+    if sx is None:
+        sx = torch.empty(M, dtype=torch.float32, device=G.device)
+    _req(G, "G", dtype=torch.bfloat16, rows=M, cols=K)
+    _req(U, "U", dtype=torch.bfloat16, rows=M, cols=K)
+    _req(At, "At", nbytes=need)
+    _req(sx, "sx", dtype=torch.float32, nbytes=4 * M)
+    _check(lib().tq_swiglu_quant_act_tiled(_ptr(G), G.stride(0), _ptr(U), U.stride(0), M, K, _ptr(At),
+                                           _nbytes(At), _ptr(sx), _stream(stream)),
+           "tq_swiglu_quant_act_tiled")
     return At, sx
 
 

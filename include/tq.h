@@ -202,6 +202,24 @@ tq_status tq_rotate_quant_act_tiled(const void *X, int64_t M, int64_t K, int64_t
                                     size_t at_bytes, float *sx, cudaStream_t stream);
 
 /*
+ * The SwiGLU row kernel fused with tq_rotate_quant_act_tiled: the input of a
+ * down projection, h = bf16(silu(G) * U) with silu(g) = g / (1 + e^-g) (the
+ * gated unit of Shazeer, "GLU Variants Improve Transformer", 2020), rotated
+ * and quantised per token into the tiled operand.  The pages name SwiGLU among
+ * the row kernels next to the projections, candidates for fusion (TensorFold
+ * PR #948, "What comes next").  Fused, h (bf16 [M, K]) is neither written nor
+ * read again.  silu and the product are computed in fp32 and rounded to bf16,
+ * as an unfused SwiGLU kernel would store h.  So a code may differ by one from
+ * the fp64 reference, as for tq_rotate_quant_act.
+ *   G, U   bf16 [M, K], rows at G + m * ldg and U + m * ldu (for example the
+ *          two halves of a fused gate/up product's output: U = G + K, both
+ *          strides 2K); each follows tq_rotate_quant_act's rules for X.
+ *   At, at_bytes, sx   as tq_rotate_quant_act_tiled.
+ */
+tq_status tq_swiglu_quant_act_tiled(const void *G, int64_t ldg, const void *U, int64_t ldu, int64_t M,
+                                    int64_t K, void *At, size_t at_bytes, float *sx, cudaStream_t stream);
+
+/*
  * The A8 product on a tiled operand: as tq_linear_q8 with At, sx from
  * tq_rotate_quant_act_tiled (same M and K) in place of Xq, sx.
  */

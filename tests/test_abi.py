@@ -283,3 +283,20 @@ def test_epilogue_refusals(L):
         assert ex(E(residual=Y)) == DEVICE                     # in place: accepted on the host
         assert ex(E(bias=FAKE, gate=FAKE)) == DEVICE
         assert ex(None) == DEVICE
+
+
+def test_swiglu_quant_refusals(L):
+    sq = lambda **k: L.tq_swiglu_quant_act_tiled(*[k.get(n, d) for n, d in (
+        ("G", FAKE), ("ldg", 1024), ("U", FAKE + 1024), ("ldu", 1024), ("M", 4), ("K", 512),
+        ("At", FAKE), ("at", 1 << 30), ("sx", FAKE), ("s", S0))])
+    assert sq(K=96) == SHAPE
+    assert sq(K=16384 + 256) == SHAPE                 # above TQ_MAX_K_TILED
+    assert sq(G=0) == NULL
+    assert sq(U=0) == NULL
+    assert sq(ldu=500) == SHAPE                       # ldu < K
+    assert sq(U=FAKE + 2) == ALIGN
+    assert sq(ldg=1028) == ALIGN                      # stride not a multiple of 8
+    assert sq(At=0) == NULL
+    assert sq(at=100) == WORKSPACE
+    assert sq(At=FAKE + 16) == ALIGN
+    assert sq(M=0) == OK

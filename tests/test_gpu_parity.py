@@ -15,7 +15,7 @@ import pytest
 import oracle
 from dit_convrot_linear_gb300 import synth
 from helpers import (CODE_FLIP_FRAC, REL_L2_Y, SCALE_REL, ULP_FLIP_FRAC, bf16_bits,
-                     bf16_ulp_diff, check_codes_close, parity_report, rel_l2,
+                     bf16_ulp_diff, check_codes_close, parity_report, rel_l2, untile_codes,
                      to_dev_bf16, to_np)
 
 pytestmark = pytest.mark.gpu
@@ -242,6 +242,8 @@ def test_tiled_operand_matches_int8_path(tq, M, N, K, bits):
     acc_t = to_np(tq.linear_tiled(At, sxt, M, K, codes, sw, N, bits, out="i32"))
     acc = to_np(tq.linear_q8(Xq, sx, codes, sw, N, bits, out="i32"))
     assert np.array_equal(acc_t, acc)
+    # the tests' decoding of the tiled layout gives the same codes
+    assert np.array_equal(untile_codes(At, M, K), to_np(Xq).astype(np.int64))
     ref_acc, _ = oracle.linear_a8(to_np(Xq), to_np(sx), codes_np(codes, bits, K), to_np(sw))
     assert np.array_equal(acc_t, ref_acc)
 
@@ -341,6 +343,47 @@ def test_tiled_weights_epilogue_in_place_bf16(tq):
     _, Y0 = oracle.linear_a8(to_np(Xq), to_np(sxq), to_np(codes), to_np(sw))
     ref = r + to_np(gate).astype(np.float64) * Y0
     assert bf16_ulp_diff(bf16_bits(R), oracle.round_bf16(ref)).max() <= 1
+
+
+@pytest.mark.parametrize("M,K", [(300, 3072), (257, 4096 + 32), (5, 544), (64, 12288), (130, 896)])
+def test_swiglu_fused_operand(tq, M, K):
+    """The down projection's operand made from gate and up in one pass: codes
+    and token scales against the oracle's SwiGLU (O8) then quantiser (O4), to
+    the activation-code bar; and the tiled form's own layout decodes to the
+    same codes as the unfused route (the oracle's bf16 h through
+    tq_rotate_quant_act_tiled), the two differing only where h does."""
+    import torch
+    G = xgen(f"gpu/swiglu/g{M}x{K}", M, K, (1.5, 0.0, 1.0))
+    U = xgen(f"gpu/swiglu/u{M}x{K}", M, K, XD)
+    # gate and up as the two halves of one fused gate/up output row
+    GU = np.concatenate([G, U], axis=1)
+    GUd = to_dev_bf16(GU)
+    At, sx = tq.swiglu_quant_act_tiled(GUd[:, :K], GUd[:, K:])
+    codes = untile_codes(At, M, K)
+    rq, rs = oracle.swiglu_quant_act(G, U)
+    check_codes_close(codes, rq, frac=CODE_FLIP_FRAC)
+    assert np.max(np.abs(to_np(sx).astype(np.float64) / np.where(rs == 0, 1, rs) - 1)) <= SCALE_REL
+    H = oracle.swiglu_bf16(G, U)
+    At2, sx2 = tq.rotate_quant_act_tiled(to_dev_bf16(H))
+    check_codes_close(codes, untile_codes(At2, M, K), frac=CODE_FLIP_FRAC)
+    assert tq.device_status() == 0
+
+
+def test_swiglu_fused_operand_feeds_the_product(tq):
+    """gate/up -> fused SwiGLU operand -> both-tiled down product, against the
+    oracle's int32 sums on the same codes (exact) and its Y."""
+    M, N, K = 260, 300, 4096
+    G = xgen("gpu/swiglu2/g", M, K, (1.5, 0.0, 1.0))
+    U = xgen("gpu/swiglu2/u", M, K, XD)
+    codes_w, sw = gpu_weights(tq, wgen("gpu/swiglu2/w", N, K), 8)
+    At, sx = tq.swiglu_quant_act_tiled(to_dev_bf16(G), to_dev_bf16(U))
+    Wt = tq.tile_weights(codes_w, N, K, 8)
+    acc = to_np(tq.linear_tt(At, sx, M, K, Wt, sw, N, 8, out="i32"))
+    xq = untile_codes(At, M, K).astype(np.int8)
+    ref_acc, ref_Y = oracle.linear_a8(xq, to_np(sx), to_np(codes_w), to_np(sw))
+    assert np.array_equal(acc, ref_acc)
+    Y = to_np(tq.linear_tt(At, sx, M, K, Wt, sw, N, 8))
+    assert rel_l2(Y, ref_Y) <= REL_L2_Y
 
 
 @pytest.mark.parametrize("bits", [8, 4])
