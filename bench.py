@@ -433,6 +433,40 @@ def dit_measure(device, reps=5, M=4032):
                  "gemm": o / tot["g"], "gemm_tiled_weights": o / tot["g_tt"]}
 
 
+def swiglu_measure(device, reps=5, M=4032, K=12288):
+    """The down projection's operand made from gate and up in one pass
+    (tq_swiglu_quant_act_tiled), and, for the unfused route, the rotation of
+    an h already made (tq_rotate_quant_act_tiled).  L2 flushed before each call.
+    Bytes: fused, read 2 x 2MK + write 2MK (fp16 codes); unfused, a SwiGLU
+    kernel (read 4MK, write 2MK) and then the rotation (read 2MK, write 2MK)."""
+    import torch
+    from dit_convrot_linear_gb300 import synth, tq
+    G = bf16_dev(synth.tensor("bench/swiglu/g", M, K, 1.5, 0.0, 1.0), device)
+    U = bf16_dev(synth.tensor("bench/swiglu/u", M, K, 1.0, 0.002, 40.0), device)
+    H = (torch.nn.functional.silu(G.float()) * U.float()).to(torch.bfloat16)
+    At, sx = tq.swiglu_quant_act_tiled(G, U)
+    At2, sx2 = tq.rotate_quant_act_tiled(H)
+    flush = L2Flush(device)
+    runs = {"fused": lambda: tq.swiglu_quant_act_tiled(G, U, At=At, sx=sx),
+            "rotation_of_h": lambda: tq.rotate_quant_act_tiled(H, At=At2, sx=sx2)}
+    times = {k: [] for k in runs}
+    for _ in range(reps):
+        for k, fn in runs.items():
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times[k].append(e0.elapsed_time(e1))
+    med = {k: statistics.median(v) for k, v in times.items()}
+    fused_bytes = 6 * M * K
+    return {"M": M, "K": K, "fused_ms": round(med["fused"], 4),
+            "fused_gbs": round(fused_bytes / (med["fused"] * 1e-3) / 1e9, 1),
+            "rotation_of_h_ms": round(med["rotation_of_h"], 4),
+            "fused_bytes": fused_bytes, "unfused_bytes": 10 * M * K}
+
+
 # ------------------------------------------------------------------ CPU oracle
 
 def cpu_oracle_decode(bits, budget_s=12.0, min_calls=3):
@@ -512,9 +546,11 @@ def main():
 
     if args.only == "dit":   # profiling case: the DiT products alone
         per, tops = dit_measure(device, reps=args.steps, M=args.dit_m)
+        sw = swiglu_measure(device, reps=args.steps, M=args.dit_m)
         if rank == 0:
             print(json.dumps({"case": f"dit W8A8 M={args.dit_m}",
-                              **{k: round(v, 2) for k, v in tops.items()}, "per_projection": per}))
+                              **{k: round(v, 2) for k, v in tops.items()}, "per_projection": per,
+                              "swiglu_operand": sw}))
         return 0
 
     # headline: decode W8A16.  The 1000 calls are independent (each has its
@@ -597,6 +633,7 @@ def main():
                 "gemm_tops": round(g, 2),
                 "gemm_converting_tops": round(tops["gemm"], 2),
                 "per_projection": per,
+                "swiglu_operand": swiglu_measure(device),
                 "roofline": {"bound": "tensor", "kernel": "k_gemm_a8_tc<8, both tiled>",
                              "achieved": round(g, 2),
                              "peak": bf16_peak, "unit": "TFLOP/s",
