@@ -69,6 +69,8 @@ _SIGS = {
     "or_matmul_f64": (ctypes.c_int, [_P, _I, _I, _P, _I, _P, ctypes.c_int]),
     "or_swiglu_f64": (ctypes.c_int, [_P, _P, _I, _P]),
     "or_swiglu_bf16": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _P]),
+    "or_quantize_blocks": (ctypes.c_int, [_P, _I, _I, _I, ctypes.c_int, _P, _P]),
+    "or_linear_a16_blocked": (ctypes.c_int, [_P, _I, _I, _P, _P, _I, _I, _P, ctypes.c_int]),
 }
 
 
@@ -326,6 +328,47 @@ def swiglu_bf16(G: np.ndarray, U: np.ndarray) -> np.ndarray:
 def swiglu_quant_act(G: np.ndarray, U: np.ndarray):
     """O8 then O1+O2+O4: the down projection's A8 operand from gate and up."""
     return rotate_quant_act(swiglu_bf16(G, U))
+
+
+def quantize_blocks(V: np.ndarray, qmax: int, G: int):
+    """O9: symmetric quantisation with one scale per block of G columns ->
+    (int8 codes [R, K], fp32 scales [R, K/G])."""
+    V = _c(V, np.float64)
+    R, K = V.shape
+    codes = np.empty((R, K), dtype=np.int8)
+    scales = np.empty((R, K // G if G else 0), dtype=np.float32)
+    _check(lib().or_quantize_blocks(V.ctypes.data, R, K, G, qmax, codes.ctypes.data,
+                                    scales.ctypes.data), "quantize_blocks")
+    return codes, scales
+
+
+def quantize_weights_blocked(W: np.ndarray, bits: int, G: int, rotate: bool = True):
+    """O1 (+O2 when rotate) + O9 (+O7 for 4 bits): bf16 W [N, K] -> (codes,
+    fp32 block scales [N, K/G]); codes as in quantize_weights."""
+    V = rotate_rows(W) if rotate else bf16_to_f64(W)
+    codes, scales = quantize_blocks(V, QMAX[bits], G)
+    return (codes if bits == 8 else pack_int4(codes)), scales
+
+
+def linear_a16_blocked(X, Wcodes, sw, G: int):
+    """O10: fp64 Y [M, N] from bf16 activations X (already rotated and
+    rounded when the weights were rotated) and block-scaled weight codes."""
+    X, Wcodes, sw = _c(X, np.uint16), _c(Wcodes, np.int8), _c(sw, np.float32)
+    M, K = X.shape
+    N = Wcodes.shape[0]
+    Y = np.empty((M, N), dtype=np.float64)
+    _check(lib().or_linear_a16_blocked(X.ctypes.data, M, K, Wcodes.ctypes.data, sw.ctypes.data,
+                                       G, N, Y.ctypes.data, threads()), "linear_a16_blocked")
+    return Y
+
+
+def linear_blocked(X, W, bits: int, G: int, rotate: bool = True):
+    """The whole block-scaled decode projection from bf16 inputs (O1-O2, O9,
+    O4' when rotated, O10). Returns fp64 Y [M, N]."""
+    Wq, sw = quantize_weights_blocked(W, bits, G, rotate)
+    K = W.shape[1]
+    Xa = rotate_act_bf16(X) if rotate else _c(X, np.uint16)
+    return linear_a16_blocked(Xa, weight_codes(Wq, bits, K), sw, G)
 
 
 def matmul_f64(A, B):

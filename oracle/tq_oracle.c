@@ -40,6 +40,18 @@
  *      silu(g) = g / (1 + e^-g), the gated unit of Shazeer, "GLU Variants
  *      Improve Transformer" (2020), in fp64 from bf16 g and u, then rounded
  *      to the nearest bf16 (the activations are bf16).
+ *   O9 block-scaled weights (a scale per block of G columns instead of per
+ *      row: the blocks with a shared scale of the GGML formats, Q8_0 and Q4_0
+ *      32 wide, and kvad's own q8 with an fp32 scale per 32 weights; kvad-gpu
+ *      internals, "Quantised weights on the GPU"; used on the rotated weights
+ *      to recover 4-bit accuracy, whose error the rotation lowers less than
+ *      8-bit's, tensai docs, "画像生成", section "幅とメモリ"): O3 applied to
+ *      every block on its own, s_b = fp32(amax_b / qmax), q = rint(v / s_b).
+ *      The blocks are taken of v' (rotated) or of the bf16 weights themselves
+ *      (the unrotated format).
+ *   O10 block-scaled A16 product: Y = sum_b s_b * sum_{k in block b} q_w * x
+ *      in fp64, x the bf16 activations (rotated and rounded as in O4' when
+ *      the weights were rotated, else as given).
  *
  * Readings where the pages are silent (each listed in the design notes):
  *   Sylvester order and 1/sqrt(n) normalisation; a last group narrower than
@@ -432,5 +444,78 @@ int or_swiglu_bf16(const uint16_t *G, int64_t ldg, const uint16_t *U, int64_t ld
             or_swiglu_f64(&g, &u, 1, &h);
             H[m * K + k] = or_f64_to_bf16(h);
         }
+    return 0;
+}
+
+/* -------------------------------------------------------------------------- */
+/* O9 block-scaled quantisation: O3 applied to every block of G columns of a   */
+/* row on its own (one scale per block instead of one per row).               */
+
+int or_quantize_blocks(const double *V, int64_t R, int64_t K, int64_t G, int qmax,
+                       int8_t *codes, float *scales) {
+    if (R < 0 || K < 0 || G < 1 || K % G || qmax < 1 || qmax > 127) return 2;
+    fesetround(FE_TONEAREST);
+    const int64_t nb = K / G;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const double *v = V + r * K + b * G;
+            int8_t *q = codes + r * K + b * G;
+            double amax = 0.0;
+            for (int64_t k = 0; k < G; ++k) {
+                const double a = fabs(v[k]);
+                if (a > amax) amax = a;
+            }
+            const float s = (float)(amax / (double)qmax);
+            scales[r * nb + b] = s;
+            for (int64_t k = 0; k < G; ++k) {
+                if (s == 0.0f) {
+                    q[k] = 0;
+                    continue;
+                }
+                double c = nearbyint(v[k] / (double)s);
+                if (c > qmax) c = qmax;
+                if (c < -qmax) c = -qmax;
+                q[k] = (int8_t)c;
+            }
+        }
+    return 0;
+}
+
+/* -------------------------------------------------------------------------- */
+/* O10 block-scaled A16 product: Y[m][n] = sum_b s[n][b] * sum_{k in b} q * x  */
+/* in fp64, x the bf16 activation row as given (rotated or not).              */
+
+typedef struct {
+    const uint16_t *X;
+    int64_t M, K, G;
+    const int8_t *Wq;
+    const float *sw;
+    int64_t N;
+    double *Y;
+} blk_arg;
+
+static void blk_cols(void *p, int64_t n0, int64_t n1) {
+    const blk_arg *a = (const blk_arg *)p;
+    const int64_t nb = a->K / a->G;
+    for (int64_t m = 0; m < a->M; ++m)
+        for (int64_t n = n0; n < n1; ++n) {
+            const uint16_t *x = a->X + m * a->K;
+            const int8_t *w = a->Wq + n * a->K;
+            double y = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                double part = 0.0;
+                for (int64_t k = b * a->G; k < (b + 1) * a->G; ++k)
+                    part += (double)w[k] * or_bf16_to_f64(x[k]);
+                y += (double)a->sw[n * nb + b] * part;
+            }
+            a->Y[m * a->N + n] = y;
+        }
+}
+
+int or_linear_a16_blocked(const uint16_t *X, int64_t M, int64_t K, const int8_t *Wq,
+                          const float *sw, int64_t G, int64_t N, double *Y, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || G < 1 || K % G) return 2;
+    blk_arg a = {X, M, K, G, Wq, sw, N, Y};
+    parallel_for(N, nthreads, blk_cols, &a);
     return 0;
 }

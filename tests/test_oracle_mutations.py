@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 import test_oracle_pins as pins
+import test_oracle_blocked as blocked_pins
 import test_oracle_swiglu as swiglu_pins
 
 MUTANTS = {
@@ -47,6 +48,17 @@ MUTANTS = {
     "silu_sigmoid_of_minus_g": ("g[i] / (1.0 + exp(-g[i])) * u[i]", "g[i] / (1.0 + exp(g[i])) * u[i]"),
     "swiglu_plain_sigmoid_gate": ("g[i] / (1.0 + exp(-g[i])) * u[i]", "1.0 / (1.0 + exp(-g[i])) * u[i]"),
     "swiglu_gate_and_up_swapped": ("g[i] / (1.0 + exp(-g[i])) * u[i]", "u[i] / (1.0 + exp(-u[i])) * g[i]"),
+    "block_amax_over_half_block": ("for (int64_t k = 0; k < G; ++k) {\n                const double a",
+                                   "for (int64_t k = 0; k < G / 2; ++k) {\n                const double a"),
+    "block_scale_stored_in_next_slot": ("scales[r * nb + b] = s;", "scales[r * nb + (b + 1) % nb] = s;"),
+    "block_amax_carried_over": ("            double amax = 0.0;\n            for (int64_t k = 0; k < G",
+                                "            static double amax = 0.0;\n            for (int64_t k = 0; k < G"),
+    "blocked_product_next_block_scale": ("y += (double)a->sw[n * nb + b] * part;",
+                                         "y += (double)a->sw[n * nb + (b + 1) % nb] * part;"),
+    "blocked_product_drops_last_block": ("for (int64_t b = 0; b < nb; ++b) {\n                double part",
+                                         "for (int64_t b = 0; b + 1 < nb; ++b) {\n                double part"),
+    "blocked_product_row_scale": ("y += (double)a->sw[n * nb + b] * part;",
+                                  "y += (double)a->sw[n * nb] * part;"),
 }
 
 PIN_TESTS = [
@@ -70,6 +82,10 @@ PIN_TESTS = [
     lambda: swiglu_pins.test_silu_odd_part_is_the_identity(),
     lambda: swiglu_pins.test_silu_special_values(),
     lambda: swiglu_pins.test_swiglu_is_linear_in_up(),
+    lambda: blocked_pins.test_block_quantiser_error_bound_range_and_scale(7, 32),
+    lambda: blocked_pins.test_blocks_scale_independently(),
+    lambda: blocked_pins.test_block_quantiser_ties_to_even_in_a_later_block(),
+    lambda: blocked_pins.test_blocked_product_brute_force(),
 ]
 
 
