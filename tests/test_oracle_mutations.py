@@ -34,8 +34,10 @@ MUTANTS = {
     # (dropping the clamp is an equivalent mutant: with s = fp32(amax/qmax),
     # |v'/s| <= qmax (1 + 2^-24) < qmax + 1/2, so the clamp never acts)
     "clamp_too_tight": ("if (q > qmax) q = qmax;", "if (q > qmax - 1) q = qmax - 1;"),
-    "scale_over_qmax_plus_1": ("(float)(amax / (double)qmax)",
-                               "(float)(amax / (double)(qmax + 1))"),
+    "scale_over_qmax_plus_1": ("(float)(amax / (double)qmax);\n        scales[r] = s;",
+                               "(float)(amax / (double)(qmax + 1));\n        scales[r] = s;"),
+    "block_scale_over_qmax_plus_1": ("(float)(amax / (double)qmax);\n            scales[r * nb + b] = s;",
+                                     "(float)(amax / (double)(qmax + 1));\n            scales[r * nb + b] = s;"),
     "nibble_order": ("(uint8_t)(lo | (hi << 4))", "(uint8_t)(hi | (lo << 4))"),
     "dropped_product_term": (
         "for (int64_t k = 0; k < K; ++k) s += (int64_t)x[k] * (int64_t)w[k];",
