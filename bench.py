@@ -47,8 +47,9 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--calls", type=int, default=1000)
     ap.add_argument("--skip-dit", action="store_true")
-    ap.add_argument("--only", default="all", choices=["all", "decode", "dit"],
-                    help="profiling cases: only the W8A16 decode graph, or only the DiT GEMMs")
+    ap.add_argument("--only", default="all", choices=["all", "decode", "dit", "blocked"],
+                    help="profiling cases: only the W8A16 decode graph, only the DiT GEMMs, or only "
+                         "the block-scaled decode products")
     ap.add_argument("--dit-m", type=int, default=4032, help="token rows of the DiT case")
     ap.add_argument("--skip-cpu", action="store_true")
     return ap.parse_args()
@@ -196,12 +197,13 @@ def decode_layers(bits, l2_bytes):
 
 
 class Decode:
-    """1000 seeded M=1 calls cycling gate, up, down through the layer sets."""
+    """1000 seeded M=1 calls cycling gate, up, down through the layer sets.
+    block = (G, rotate) uses block-scaled weights (tq_linear_blocked)."""
 
-    def __init__(self, bits, calls, device, l2_bytes):
+    def __init__(self, bits, calls, device, l2_bytes, block=None):
         import torch
         from dit_convrot_linear_gb300 import synth, tq
-        self.bits, self.calls, self.device = bits, calls, device
+        self.bits, self.calls, self.device, self.block = bits, calls, device, block
         self.mode = "W8A16" if bits == 8 else "W4A16"
         w = synth.DECODE
         self.layers = decode_layers(bits, l2_bytes)
@@ -210,7 +212,8 @@ class Decode:
             row = []
             for p in w.projs:
                 Wd = bf16_dev(w.weight(L, p), device)
-                row.append(tq.quantize_weights(Wd, bits))
+                row.append(tq.quantize_weights_blocked(Wd, bits, *block) if block
+                           else tq.quantize_weights(Wd, bits))
                 del Wd
             self.weights.append(row)
         torch.cuda.synchronize()
@@ -229,17 +232,24 @@ class Decode:
         self.x_dev = xs_host.to(device)
         self.y_dev = torch.empty(yoff, dtype=torch.float32, device=device)
         self.y_host = torch.empty(yoff, dtype=torch.float32).pin_memory()
-        self.weight_bytes = sum(p.N * p.K * bits // 8 + 4 * p.N for (_, _, _, p, _, _) in self.plan)
-        self.distinct_bytes = self.layers * sum(p.N * p.K * bits // 8 + 4 * p.N for p in w.projs)
+        nbytes = lambda p: p.N * p.K * bits // 8 + 4 * p.N * (p.K // block[0] if block else 1)
+        self.weight_bytes = sum(nbytes(p) for (_, _, _, p, _, _) in self.plan)
+        self.distinct_bytes = self.layers * sum(nbytes(p) for p in w.projs)
         self.graph = None
 
-    def run_calls(self):
+    def call(self, X, codes, sw, N, Y):
         from dit_convrot_linear_gb300 import tq
+        if self.block:
+            tq.linear_blocked(X, codes, sw, N, self.bits, self.block[0], self.block[1], Y=Y)
+        else:
+            tq.linear(X, codes, sw, N, self.bits, self.mode, Y=Y)
+
+    def run_calls(self):
         for (i, L, j, p, xo, yo) in self.plan:
             codes, sw = self.weights[L][j]
             X = self.x_dev[xo:xo + p.K].view(1, p.K)
             Y = self.y_dev[yo:yo + p.N].view(1, p.N)
-            tq.linear(X, codes, sw, p.N, self.bits, self.mode, Y=Y)
+            self.call(X, codes, sw, p.N, Y)
 
     def capture(self):
         import torch
@@ -300,7 +310,6 @@ class Decode:
     def isolated_call_us(self, reps=50):
         """One call at a time (no graph), CUDA events around each."""
         import torch
-        from dit_convrot_linear_gb300 import tq
         times = []
         for r in range(reps):
             i, L, j, p, xo, yo = self.plan[(r * 7) % len(self.plan)]
@@ -309,11 +318,63 @@ class Decode:
             Y = self.y_dev[yo:yo + p.N].view(1, p.N)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            tq.linear(X, codes, sw, p.N, self.bits, self.mode, Y=Y)
+            self.call(X, codes, sw, p.N, Y)
             e1.record()
             e1.synchronize()
             times.append(e0.elapsed_time(e1) * 1e3)
         return statistics.median(times)
+
+
+def blocked_measure(device, steps, warmup, world, calls, l2, hbm):
+    """Block-scaled weights (tq_linear_blocked): the decode calls one launch
+    each, as the per-row decode_w8a16_per_call line, for the rotated 4-bit
+    format with a scale per 32 columns and the unrotated 8-bit format with a
+    scale per 32 (kvad's q8); and one M = 1 product over a 16384 x 16384
+    matrix (larger than L2, flushed before each launch) for the kernel's
+    streaming rate.  Bytes are codes plus block scales."""
+    import torch
+    from dit_convrot_linear_gb300 import synth, tq
+    out = {}
+    for name, bits, block in (("w4_rotated_g32", 4, (32, True)), ("w8_unrotated_g32", 8, (32, False))):
+        if calls == 0:      # the streaming case alone (profiling)
+            break
+        dec = Decode(bits, calls, device, l2, block=block)
+        dec.capture()
+        ms = time_steps(dec.step, steps, warmup, world) / steps
+        a = dec.weight_bytes / (ms * 1e-3) / 1e9
+        out[name] = {"value": round(a * world, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+                     "frac": round(a / hbm, 4), "launches_per_step": calls,
+                     "isolated_call_us": round(dec.isolated_call_us(), 2)}
+        del dec
+        torch.cuda.empty_cache()
+    N = K = 16384
+    Wd = bf16_dev(synth.tensor("bench/blocked/w", N, K, 0.02, 0.01, 20.0), device)
+    X = bf16_dev(synth.tensor("bench/blocked/x", 1, K, 1.0, 0.002, 40.0), device)
+    Y = torch.empty((1, N), dtype=torch.float32, device=device)
+    flush = L2Flush(device)
+    stream = {}
+    for name, bits, G, rot in (("w8_unrotated_g32", 8, 32, False), ("w4_rotated_g64", 4, 64, True),
+                               ("w4_rotated_g32", 4, 32, True)):
+        codes, sw = tq.quantize_weights_blocked(Wd, bits, G, rot)
+        fn = lambda: tq.linear_blocked(X, codes, sw, N, bits, G, rot, Y=Y)
+        nbytes = N * K * bits // 8 + 4 * N * (K // G)
+        fn()
+        times = []
+        for _ in range(max(5, min(steps, 30))):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        stream[name] = {"ms": round(ms, 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                        "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4), "bytes": nbytes}
+        del codes, sw
+    out["stream_16384x16384_m1"] = stream
+    out["kernel"] = "k_gemv_blocked<bits, 1>"
+    return out
 
 
 def time_steps(fn, steps, warmup, world):
@@ -544,6 +605,13 @@ def main():
     l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
     pk, pk_kind = peaks()
 
+    if args.only == "blocked":   # profiling case: the block-scaled products alone
+        hbm = float(pk["hbm_gbs"])
+        res = blocked_measure(device, args.steps, args.warmup, world, args.calls, l2, hbm)
+        if rank == 0:
+            print(json.dumps({"case": "decode, block-scaled weights", **res}))
+        return 0
+
     if args.only == "dit":   # profiling case: the DiT products alone
         per, tops = dit_measure(device, reps=args.steps, M=args.dit_m)
         sw = swiglu_measure(device, reps=args.steps, M=args.dit_m)
@@ -620,6 +688,14 @@ def main():
         torch.cuda.empty_cache()
     except Exception as exc:  # reported, never hidden
         extra["decode_w4a16"] = {"error": repr(exc)}
+
+    if args.only != "decode":
+        try:
+            extra["decode_blocked"] = blocked_measure(device, args.steps, args.warmup, world, args.calls,
+                                                      l2, hbm)
+        except Exception as exc:
+            extra["decode_blocked"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
 
     if not args.skip_dit:
         try:

@@ -46,6 +46,39 @@ __device__ __forceinline__ int rotate_group64_any(const uint16_t *src, int n,
     }
 }
 
+// Store the E codes of this lane (columns k0 .. k0 + E - 1 of row n):
+// int8 as bytes, int4 two per byte with the low nibble the even column.
+template <int BITS>
+__device__ __forceinline__ void store_codes(uint8_t *codes, int64_t n, int64_t K, int64_t k0, int E,
+                                            const int (&q)[8]) {
+    const int lane = threadIdx.x & 31;
+    if constexpr (BITS == 8) {
+        uint8_t *dst = codes + n * K + k0;
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) lo |= (static_cast<uint32_t>(q[e]) & 0xFFu) << (8 * e);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) hi |= (static_cast<uint32_t>(q[4 + e]) & 0xFFu) << (8 * e);
+        if (E == 8) *reinterpret_cast<uint2 *>(dst) = make_uint2(lo, hi);
+        else if (E == 4) *reinterpret_cast<uint32_t *>(dst) = lo;
+        else if (E == 2) *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(lo);
+        else *dst = static_cast<uint8_t>(lo);
+    } else {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) packed |= (static_cast<uint32_t>(q[e]) & 0xFu) << (4 * e);
+        uint8_t *dst = codes + n * (K / 2) + k0 / 2;
+        if (E == 8) *reinterpret_cast<uint32_t *>(dst) = packed;
+        else if (E == 4) *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(packed);
+        else if (E == 2) *dst = static_cast<uint8_t>(packed);
+        else {
+            // one code per lane: even lanes pair with their odd neighbour
+            const uint32_t other = __shfl_down_sync(0xffffffffu, packed, 1);
+            if (!(lane & 1)) *dst = static_cast<uint8_t>((packed & 0xFu) | ((other & 0xFu) << 4));
+        }
+    }
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(kThreads)
 k_quantize_weights(const uint16_t *__restrict__ W, int64_t N, int64_t K,
@@ -92,34 +125,66 @@ k_quantize_weights(const uint16_t *__restrict__ W, int64_t N, int64_t K,
                 if (s != 0.0f) r = fmin(fmax(rint(v[e] / sd), -qmax), qmax);
                 q[e] = static_cast<int>(r);
             }
-            const int64_t k0 = g0 + static_cast<int64_t>(lane) * E;  // first column of this lane
-            if constexpr (BITS == 8) {
-                uint8_t *dst = codes + n * K + k0;
-                uint32_t lo = 0, hi = 0;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) lo |= (static_cast<uint32_t>(q[e]) & 0xFFu) << (8 * e);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) hi |= (static_cast<uint32_t>(q[4 + e]) & 0xFFu) << (8 * e);
-                if (E == 8) *reinterpret_cast<uint2 *>(dst) = make_uint2(lo, hi);
-                else if (E == 4) *reinterpret_cast<uint32_t *>(dst) = lo;
-                else if (E == 2) *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(lo);
-                else *dst = static_cast<uint8_t>(lo);
-            } else {
-                // two codes per byte, low nibble = even column
-                uint32_t packed = 0;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) packed |= (static_cast<uint32_t>(q[e]) & 0xFu) << (4 * e);
-                uint8_t *dst = codes + n * (K / 2) + k0 / 2;
-                if (E == 8) *reinterpret_cast<uint32_t *>(dst) = packed;
-                else if (E == 4) *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(packed);
-                else if (E == 2) *dst = static_cast<uint8_t>(packed);
-                else {
-                    // one code per lane: even lanes pair with their odd neighbour
-                    const uint32_t other = __shfl_down_sync(0xffffffffu, packed, 1);
-                    if (!(lane & 1)) *dst = static_cast<uint8_t>((packed & 0xFu) | ((other & 0xFu) << 4));
-                }
+            store_codes<BITS>(codes, n, K, g0 + static_cast<int64_t>(lane) * E, E, q);
+        }
+    }
+}
+
+// Block-scaled variant: one scale per block of G columns (G = 32, 64, 128 or
+// 256, dividing K) instead of one per row; the blocks with a shared scale of
+// the GGML formats and kvad's own q8 (kvad-gpu internals, "Quantised weights
+// on the GPU"), taken of the rotated row (rotate = 1) or of the bf16 weights
+// as they are (rotate = 0).  Every group width is a multiple of G, so a block
+// lies inside one group: the warp that transforms a group also finds each of
+// its blocks' amax (a shuffle reduction over the G/E lanes holding it), the
+// scale and the codes, in one pass.  Exactness as above: the fp64 values, the
+// ratio, its fp32 rounding and the quotients match the fp64 reference bit for
+// bit.  One warp per (row, group) item.
+template <int BITS>
+__global__ void __launch_bounds__(kThreads)
+k_quantize_weights_blocked(const uint16_t *__restrict__ W, int64_t N, int64_t K, int64_t ldw, int G,
+                           int rotate, uint8_t *__restrict__ codes, float *__restrict__ scales) {
+    constexpr double qmax = BITS == 8 ? 127.0 : 7.0;
+    const int lane = threadIdx.x & 31;
+    const int64_t NG = (K + kGroup - 1) / kGroup, nb = K / G;
+    const int64_t items = N * NG;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5); it < items;
+         it += stride) {
+        const int64_t n = it / NG, g0 = (it % NG) * kGroup;
+        const int w = group_width(K, g0);
+        const uint16_t *src = W + n * ldw + g0;
+        double v[8] = {};
+        int E;
+        if (rotate) {
+            E = rotate_group64_any(src, w, v);
+        } else {
+            E = w >> 5;
+            switch (E) {
+                case 8: load_bf16<8, double>(src + lane * 8, v); break;
+                case 4: load_bf16<4, double>(src + lane * 4, v); break;
+                case 2: load_bf16<2, double>(src + lane * 2, v); break;
+                default: load_bf16<1, double>(src + lane, v); break;
             }
         }
+        double amax = 0.0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (e < E) amax = fmax(amax, fabs(v[e]));
+        const int L = G / E;                       // lanes per block: 4..32, a power of two
+        for (int m = L >> 1; m > 0; m >>= 1) amax = fmax(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+        const float s = static_cast<float>(amax / qmax);
+        const int64_t k0 = g0 + static_cast<int64_t>(lane) * E;
+        if ((lane & (L - 1)) == 0) scales[n * nb + k0 / G] = s;
+        const double sd = static_cast<double>(s);
+        int q[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            double r = 0.0;
+            if (s != 0.0f) r = fmin(fmax(rint(v[e] / sd), -qmax), qmax);
+            q[e] = static_cast<int>(r);
+        }
+        store_codes<BITS>(codes, n, K, k0, E, q);
     }
 }
 
@@ -171,6 +236,22 @@ k_tile_weights(const uint8_t *Wq, int64_t N, int64_t K, int64_t KT, int64_t Npad
 }
 
 }  // namespace
+
+tq_status launch_quantize_weights_blocked(const uint16_t *W, int64_t N, int64_t K, int64_t ldw, int bits,
+                                          int G, int rotate, void *codes, float *scales, cudaStream_t s) {
+    const int64_t items = N * ((K + kGroup - 1) / kGroup);
+    const int64_t want = (items + kThreads / 32 - 1) / (kThreads / 32);
+    const unsigned grid = static_cast<unsigned>(want < (1ll << 20) ? want : (1ll << 20));
+    if (grid == 0) return TQ_OK;
+    if (bits == 8)
+        k_quantize_weights_blocked<8><<<grid, kThreads, 0, s>>>(W, N, K, ldw, G, rotate,
+                                                                 static_cast<uint8_t *>(codes), scales);
+    else
+        k_quantize_weights_blocked<4><<<grid, kThreads, 0, s>>>(W, N, K, ldw, G, rotate,
+                                                                 static_cast<uint8_t *>(codes), scales);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
 
 tq_status launch_quantize_weights(const uint16_t *W, int64_t N, int64_t K,
                                   int64_t ldw, int bits, void *codes,

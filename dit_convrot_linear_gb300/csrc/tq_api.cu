@@ -64,6 +64,11 @@ bool valid_k(int64_t K) {
     return t == 0 || t == 32 || t == 64 || t == 128;
 }
 
+// A block width of the block-scaled format: 32, 64, 128 or 256, dividing K.
+bool valid_block(int G, int64_t K) {
+    return (G == 32 || G == 64 || G == 128 || G == 256) && K % G == 0;
+}
+
 // a * b without int64 overflow, and within `limit`
 bool mul_ok(int64_t a, int64_t b, int64_t limit = INT64_MAX / 4) {
     if (a < 0 || b < 0) return false;
@@ -160,6 +165,44 @@ tq_status tq_quantize_weights(const void *W, int64_t N, int64_t K, int64_t ldw,
     if ((st = current_device(&dev)) != TQ_OK) return st;
     return launch_quantize_weights(static_cast<const uint16_t *>(W), N, K, ldw, bits,
                                    codes, scales, stream);
+}
+
+tq_status tq_quantize_weights_blocked(const void *W, int64_t N, int64_t K, int64_t ldw, int bits, int G,
+                                      int rotate, void *codes, float *scales, cudaStream_t stream) {
+    if (bits != 8 && bits != 4) return TQ_ERR_BITS;
+    if (rotate != 0 && rotate != 1) return TQ_ERR_MODE;
+    if (N < 0 || !valid_k(K) || !valid_block(G, K)) return TQ_ERR_SHAPE;
+    if (N == 0) return TQ_OK;
+    tq_status st = check_bf16_rows(W, N, K, ldw);
+    if (st != TQ_OK) return st;
+    if (!codes || !scales) return TQ_ERR_NULL;
+    if (!mul_ok(N, K)) return TQ_ERR_OVERFLOW;
+    if (!aligned(codes, 16) || !aligned(scales, 4)) return TQ_ERR_ALIGN;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    return launch_quantize_weights_blocked(static_cast<const uint16_t *>(W), N, K, ldw, bits, G, rotate, codes,
+                                           scales, stream);
+}
+
+tq_status tq_linear_blocked(const void *X, int64_t M, int64_t K, int64_t ldx, const void *Wq, const float *sw,
+                            int G, int64_t N, int bits, int rotate, void *Y, tq_out ytype, int64_t ldy,
+                            cudaStream_t stream) {
+    if (bits != 8 && bits != 4) return TQ_ERR_BITS;
+    if (rotate != 0 && rotate != 1) return TQ_ERR_MODE;
+    if (ytype != TQ_OUT_F32 && ytype != TQ_OUT_BF16) return TQ_ERR_MODE;
+    if (M < 0 || M > TQ_MAX_M_BLOCKED || N < 0 || !valid_k(K) || !valid_block(G, K)) return TQ_ERR_SHAPE;
+    if (M == 0 || N == 0) return TQ_OK;
+    tq_status st = check_bf16_rows(X, M, K, ldx);
+    if (st != TQ_OK) return st;
+    if ((st = check_weights(Wq, sw, N, K, bits)) != TQ_OK) return st;
+    if ((st = check_output(Y, M, N, ldy, out_size(ytype))) != TQ_OK) return st;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    // the token rows are staged in shared memory as fp32
+    if (static_cast<int64_t>(gemv_blocked_mt(static_cast<int>(M))) * K * 4 > dev.smem_optin) return TQ_ERR_SHAPE;
+    return launch_gemv_blocked(static_cast<const uint16_t *>(X), static_cast<int>(M), K, ldx,
+                               static_cast<const uint8_t *>(Wq), sw, G, N, bits, rotate, Y,
+                               ytype == TQ_OUT_BF16 ? 1 : 0, ldy, dev, stream);
 }
 
 tq_status tq_rotate_quant_act(const void *X, int64_t M, int64_t K, int64_t ldx,

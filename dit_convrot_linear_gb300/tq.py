@@ -52,6 +52,8 @@ SIGNATURES = {
     "tq_grouped_product": (_C, [_P, _P]),
     "tq_grouped_weight_bytes": (_I, [_P]),
     "tq_grouped_destroy": (None, [_P]),
+    "tq_quantize_weights_blocked": (_C, [_P, _I, _I, _I, _C, _C, _C, _P, _P, _P]),
+    "tq_linear_blocked": (_C, [_P, _I, _I, _I, _P, _P, _C, _I, _C, _C, _P, _C, _I, _P]),
 }
 
 
@@ -174,6 +176,46 @@ def quantize_weights(W, bits: int, codes=None, scales=None, stream=None):
     _check(lib().tq_quantize_weights(_ptr(W), N, K, W.stride(0), bits, 256, _ptr(codes),
                                      _ptr(scales), _stream(stream)), "tq_quantize_weights")
     return codes, scales
+
+
+def quantize_weights_blocked(W, bits: int, G: int, rotate: bool = True, codes=None, scales=None,
+                             stream=None):
+    """bf16 W [N, K] -> (codes, fp32 block scales [N, K / G]): one scale per
+    block of G columns, of the rotated row (rotate) or of W as it is."""
+    import torch
+    N, K = W.shape
+    if codes is None:
+        codes = torch.empty((N, K if bits == 8 else K // 2),
+                            dtype=torch.int8 if bits == 8 else torch.uint8, device=W.device)
+    if scales is None:
+        scales = torch.empty((N, K // G if G > 0 else 0), dtype=torch.float32, device=W.device)
+    _req(W, "W", dtype=torch.bfloat16, rows=N, cols=K)
+    _req(codes, "codes", nbytes=N * K * bits // 8)
+    if G > 0:
+        _req(scales, "scales", dtype=torch.float32, nbytes=4 * N * (K // G))
+    _check(lib().tq_quantize_weights_blocked(_ptr(W), N, K, W.stride(0), bits, G, int(rotate), _ptr(codes),
+                                             _ptr(scales), _stream(stream)), "tq_quantize_weights_blocked")
+    return codes, scales
+
+
+def linear_blocked(X, Wq, sw, N: int, bits: int, G: int, rotate: bool = True, Y=None, out: str = "f32",
+                   stream=None):
+    """Y [M, N] = the block-scaled decode product of bf16 X [M, K] (M <= 8)
+    with (Wq, sw) from quantize_weights_blocked (same G and rotate)."""
+    import torch
+    M, K = X.shape
+    if out not in ("f32", "bf16"):
+        raise ValueError("tq_linear_blocked writes f32 or bf16")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=_dt(out), device=X.device)
+    _req(X, "X", dtype=torch.bfloat16, rows=M, cols=K)
+    _req(Wq, "Wq", nbytes=N * K * bits // 8)
+    if G > 0:
+        _req(sw, "sw", dtype=torch.float32, nbytes=4 * N * (K // G))
+    _req(Y, "Y", dtype=_dt(out), rows=M, cols=N)
+    _check(lib().tq_linear_blocked(_ptr(X), M, K, X.stride(0), _ptr(Wq), _ptr(sw), G, N, bits, int(rotate),
+                                   _ptr(Y), OUT[out], Y.stride(0), _stream(stream)), "tq_linear_blocked")
+    return Y
 
 
 def rotate_quant_act(X, Xq=None, sx=None, stream=None):

@@ -288,6 +288,58 @@ tq_status tq_linear_tt_ex(const void *At, const float *sx, int64_t M, int64_t K,
                           tq_out ytype, int64_t ldy, cudaStream_t stream);
 
 /*
+ * Block-scaled weights: one fp32 scale per block of G input columns instead
+ * of one per row.  These are the blocks with a shared scale of the GGML
+ * formats (Q8_0 and Q4_0, 32 wide) and of kvad's own q8 (an fp32 scale per 32
+ * weights; kvad-gpu internals, "Quantised weights on the GPU").  On rotated
+ * weights they win back the 4-bit accuracy that one scale per row loses,
+ * since the rotation lowers 4-bit's error less than 8-bit's (tensai docs,
+ * "画像生成", section "幅とメモリ").
+ *
+ * The blocks are taken either of the rotated row (rotate = 1, the rotation of
+ * tq_quantize_weights) or of the bf16 weights as they are (rotate = 0, the
+ * unrotated format).  Block b of row n gets s = fp32(amax_b / qmax) and
+ * codes rint(v / s), exactly as tq_quantize_weights does for a whole row, so
+ * the codes and scales are bit-exact with the fp64 reference under the same
+ * condition.
+ *
+ *   W       as tq_quantize_weights.
+ *   K       a valid row length (K = 256 q + t, t in {0, 32, 64, 128}), with
+ *           K % G == 0.
+ *   bits    8 or 4.
+ *   G       32, 64, 128 or 256.  Other values give TQ_ERR_SHAPE.
+ *   rotate  1 or 0.  Other values give TQ_ERR_MODE.
+ *   codes   as tq_quantize_weights.
+ *   scales  fp32 [N, K / G], row n at scales + n * (K / G); 4-byte aligned.
+ */
+tq_status tq_quantize_weights_blocked(const void *W, int64_t N, int64_t K, int64_t ldw, int bits, int G,
+                                      int rotate, void *codes, float *scales, cudaStream_t stream);
+
+/* Largest M tq_linear_blocked accepts. */
+#define TQ_MAX_M_BLOCKED 8
+
+/*
+ * Decode product on block-scaled weights:
+ *   Y[m][n] = sum_b s[n][b] * sum_{k in block b} q[n][k] * x[m][k]
+ * with fp32 sums.  x is the token row's rotation rounded to bf16 when
+ * rotate = 1 (the product's own rotation, as tq_rotate_act_bf16 computes it),
+ * and the bf16 row itself when rotate = 0.  rotate and G must be those the
+ * weights were quantised with.
+ *
+ *   X        bf16 [M, K] (unrotated), layout as tq_rotate_quant_act;
+ *            0 <= M <= TQ_MAX_M_BLOCKED.
+ *   Wq, sw   from tq_quantize_weights_blocked.
+ *   Y        fp32 or bf16 [M, N], row m at Y + m * ldy; ldy >= N; aligned to
+ *            its element size.
+ * The token rows are held in shared memory as fp32: the M rounded up to a
+ * power of two, times K, times 4 bytes, must fit one CTA's shared memory
+ * (227 KB on sm_103), else TQ_ERR_SHAPE.  M == 0 or N == 0 is no work.
+ */
+tq_status tq_linear_blocked(const void *X, int64_t M, int64_t K, int64_t ldx, const void *Wq, const float *sw,
+                            int G, int64_t N, int bits, int rotate, void *Y, tq_out ytype, int64_t ldy,
+                            cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  Returns TQ_ERR_DEVICE_TIMEOUT if a bounded
  * device-side wait expired in any call since the last check (that call's

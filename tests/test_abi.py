@@ -300,3 +300,36 @@ def test_swiglu_quant_refusals(L):
     assert sq(at=100) == WORKSPACE
     assert sq(At=FAKE + 16) == ALIGN
     assert sq(M=0) == OK
+
+
+def test_blocked_refusals(L):
+    qb = lambda **k: L.tq_quantize_weights_blocked(*[k.get(n, d) for n, d in (
+        ("W", FAKE), ("N", 16), ("K", 896), ("ldw", 896), ("bits", 4), ("G", 32), ("rot", 1),
+        ("codes", FAKE), ("scales", FAKE), ("s", S0))])
+    assert qb(bits=2) == BITS
+    assert qb(rot=2) == MODE
+    for G in (16, 48, 512, 0, -32):
+        assert qb(G=G) == SHAPE                       # block widths 32, 64, 128, 256 only
+    assert qb(G=256) == SHAPE                          # 896 = 3 x 256 + 128: 256 does not divide K
+    assert qb(G=128) == DEVICE and qb(G=64, rot=0) == DEVICE
+    assert qb(K=96, ldw=96) == SHAPE                   # not a valid row length
+    assert qb(N=-1) == SHAPE
+    assert qb(W=0) == NULL and qb(codes=0) == NULL and qb(scales=0) == NULL
+    assert qb(W=FAKE + 2) == ALIGN and qb(ldw=900) == ALIGN
+    assert qb(codes=FAKE + 8) == ALIGN and qb(scales=FAKE + 2) == ALIGN
+    assert qb(N=2 ** 62, ldw=2 ** 20) == OVERFLOW
+    assert qb(N=0) == OK
+    lb = lambda **k: L.tq_linear_blocked(*[k.get(n, d) for n, d in (
+        ("X", FAKE), ("M", 1), ("K", 896), ("ldx", 896), ("W", FAKE), ("sw", FAKE), ("G", 32),
+        ("N", 4864), ("bits", 8), ("rot", 0), ("Y", FAKE), ("yt", 0), ("ldy", 4864), ("s", S0))])
+    assert lb() == DEVICE                              # every check passes; no GPU here
+    assert lb(bits=3) == BITS
+    assert lb(rot=-1) == MODE and lb(yt=2) == MODE     # no int32 output
+    assert lb(M=9) == SHAPE and lb(M=-1) == SHAPE      # TQ_MAX_M_BLOCKED = 8
+    assert lb(G=256) == SHAPE and lb(G=24) == SHAPE
+    assert lb(K=300, ldx=304) == SHAPE
+    assert lb(X=0) == NULL and lb(W=0) == NULL and lb(sw=0) == NULL and lb(Y=0) == NULL
+    assert lb(ldx=900) == ALIGN and lb(W=FAKE + 4) == ALIGN and lb(Y=FAKE + 2) == ALIGN
+    assert lb(Y=FAKE + 2, yt=1) == DEVICE              # bf16 output: 2-byte alignment
+    assert lb(ldy=100) == SHAPE
+    assert lb(M=0) == OK and lb(N=0) == OK
