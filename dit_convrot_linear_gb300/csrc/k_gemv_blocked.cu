@@ -13,10 +13,11 @@
 //   - Each CTA first stages the token rows in shared memory as fp32 (rotating
 //     them itself when asked), in 16-byte units swizzled so that the warp's
 //     vector reads below hit distinct banks.
-//   - A warp then takes one weight row at a time; each lane streams 16-byte
-//     chunks of codes (16 int8 or 32 int4 codes, inside one block) with
-//     L1-bypassing loads, and the block scale of each chunk; the loads of the
-//     next batch of chunks are issued before the current batch is used.
+//   - A warp then takes two adjacent weight rows at a time (one for four or
+//     more tokens), so that each x value read from shared memory serves both;
+//     each lane streams 16-byte chunks of codes (16 int8 or 32 int4 codes,
+//     inside one block) with L1-bypassing loads, and the block scale of each
+//     chunk; the next chunk of each row is loaded before this one is used.
 //   - Codes are widened to fp32 exactly (the biased byte, or nibble masked
 //     into a byte, is placed in the mantissa of 2^23 and the bias
 //     subtracted: one byte permute and one add a code), multiplied with x into a
@@ -47,10 +48,15 @@ struct BlockedParams {
 };
 
 constexpr int kBlkThreads = 256;
+// Chunks of each row a lane loads per batch: two while the sums are few (at
+// most two token-row pairs), else one.
+__host__ __device__ constexpr int blk_unr(int MT, int RW) { return MT * RW <= 2 ? 2 : 1; }
 // Resident CTAs per SM the register budget is set for: four (64 registers a
 // thread), three (80) for four and eight tokens, whose sums need the room and
-// whose staged rows allow few CTAs an SM anyway.
-__host__ __device__ constexpr int blk_min_ctas(int MT) { return MT >= 4 ? 3 : 4; }
+// whose staged rows allow few CTAs an SM anyway, and for two-chunk batches.
+__host__ __device__ constexpr int blk_min_ctas(int BITS, int MT, int RW) {
+    return MT >= 4 || blk_unr(MT, RW) == 2 ? 3 : 4;
+}
 
 // Swizzled position of 16-byte unit u of a staged token row: bits 3..5 of u
 // are folded into bits 0..2, so the eight lanes of a vector-load phase, which
@@ -71,11 +77,11 @@ __device__ __forceinline__ float i4b_to_f32(uint32_t t, int i) {
     return __int_as_float(static_cast<int>(__byte_perm(t, 0x4B000000u, 0x7650u + i))) - 8388616.0f;
 }
 
-template <int BITS, int MT>
-__global__ void __launch_bounds__(kBlkThreads, blk_min_ctas(MT))
+template <int BITS, int MT, int RW>
+__global__ void __launch_bounds__(kBlkThreads, blk_min_ctas(BITS, MT, RW))
 k_gemv_blocked(const BlockedParams p) {
     extern __shared__ __align__(16) float xs[];   // [MT][K] fp32, swizzled 16-byte units
-    constexpr int UNR = MT <= 2 ? 2 : 1;          // chunks a batch per lane (two batches in flight)
+    constexpr int UNR = blk_unr(MT, RW);    // RW: weight rows a warp takes at once
     constexpr int KPC = 128 / BITS;               // codes per 16-byte chunk
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t K = p.K;
@@ -116,130 +122,208 @@ k_gemv_blocked(const BlockedParams p) {
     const int C = static_cast<int>(rb >> 4);       // 16-byte chunks of a weight row
     const int64_t nb = K / p.G;
     const int cshift = __ffs(p.G / KPC) - 1;       // chunk -> block: c >> cshift
+    const int64_t nsets = (p.N + RW - 1) / RW;
 
-    for (int64_t n = static_cast<int64_t>(blockIdx.x) * (kBlkThreads / 32) + warp; n < p.N;
-         n += static_cast<int64_t>(gridDim.x) * (kBlkThreads / 32)) {
-        const uint8_t *wrow = p.W + n * rb;
-        const float *srow = p.sw + n * nb;
-        float acc[MT];
+    for (int64_t set = static_cast<int64_t>(blockIdx.x) * (kBlkThreads / 32) + warp; set < nsets;
+         set += static_cast<int64_t>(gridDim.x) * (kBlkThreads / 32)) {
+        const int64_t n0 = set * RW;
+        const uint8_t *wrow[RW];
+        const float *srow[RW];
+        bool valid[RW];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
-        // chunks c0 .. c0 + 32 (UNR - 1) of this lane, zeros past the row's end
-        auto load_batch = [&](int c0, uint4 (&q)[UNR], float (&s)[UNR]) {
+        for (int r = 0; r < RW; ++r) {
+            valid[r] = n0 + r < p.N;
+            const int64_t n = valid[r] ? n0 + r : n0;
+            wrow[r] = p.W + n * rb;
+            srow[r] = p.sw + n * nb;
+        }
+        float acc[RW][MT];
+#pragma unroll
+        for (int r = 0; r < RW; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[r][m] = 0.0f;
+        // chunks c0 + 32 u of each row (zeros past the row's end or for a row past N)
+        auto load_batch = [&](int c0, uint4 (&q)[RW][UNR], float (&sc)[RW][UNR]) {
 #pragma unroll
             for (int u = 0; u < UNR; ++u) {
                 const int c = c0 + 32 * u;
-                if (c < C) {
-                    q[u] = ldg_stream(wrow + (static_cast<int64_t>(c) << 4));
-                    s[u] = __ldg(srow + (c >> cshift));
-                } else {
-                    q[u] = make_uint4(0, 0, 0, 0);
-                    s[u] = 0.0f;
+#pragma unroll
+                for (int r = 0; r < RW; ++r) {
+                    if (c < C && valid[r]) {
+                        q[r][u] = ldg_stream(wrow[r] + (static_cast<int64_t>(c) << 4));
+                        sc[r][u] = __ldg(srow[r] + (c >> cshift));
+                    } else {
+                        q[r][u] = make_uint4(0, 0, 0, 0);
+                        sc[r][u] = 0.0f;
+                    }
                 }
             }
         };
-        // two batches in flight: the next one is loaded before this one is used
-        uint4 qn[UNR];
-        float sn[UNR];
+        // two batches in flight: the next is loaded before this one is used
+        uint4 qn[RW][UNR];
+        float sn[RW][UNR];
         load_batch(lane, qn, sn);
         for (int c0 = lane; c0 < C; c0 += 32 * UNR) {
-            uint4 q[UNR];
-            float s[UNR];
+            uint4 qb[RW][UNR];
+            float sb[RW][UNR];
 #pragma unroll
-            for (int u = 0; u < UNR; ++u) {
-                q[u] = qn[u];
-                s[u] = sn[u];
-            }
+            for (int r = 0; r < RW; ++r)
+#pragma unroll
+                for (int u = 0; u < UNR; ++u) {
+                    qb[r][u] = qn[r][u];
+                    sb[r][u] = sn[r][u];
+                }
             if (c0 + 32 * UNR < C) load_batch(c0 + 32 * UNR, qn, sn);
 #pragma unroll
             for (int u = 0; u < UNR; ++u) {
-                const int c = c0 + 32 * u;
-                if (c >= C) break;
-                const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-                float part[MT];
+            const int c = c0 + 32 * u;
+            if (c >= C) break;
+            uint4 q[RW];
+            float sc[RW];
 #pragma unroll
-                for (int m = 0; m < MT; ++m) part[m] = 0.0f;
-                if constexpr (BITS == 8) {
+            for (int r = 0; r < RW; ++r) {
+                q[r] = qb[r][u];
+                sc[r] = sb[r][u];
+            }
+            float part[RW][MT];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t wb = w[j] ^ 0x80808080u;
-                        const float f0 = i8_to_f32(wb, 0), f1 = i8_to_f32(wb, 1);
-                        const float f2 = i8_to_f32(wb, 2), f3 = i8_to_f32(wb, 3);
-                        const int ph = xunit(c * 4 + j);
+            for (int r = 0; r < RW; ++r)
 #pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            const float4 xv = xs4[m * U + ph];
-                            part[m] = fmaf(f0, xv.x, part[m]);
-                            part[m] = fmaf(f1, xv.y, part[m]);
-                            part[m] = fmaf(f2, xv.z, part[m]);
-                            part[m] = fmaf(f3, xv.w, part[m]);
+                for (int m = 0; m < MT; ++m) part[r][m] = 0.0f;
+            // the chunk's x units are xunit(first) ^ o for o = 0 .. units - 1: the
+            // first unit is a multiple of the unit count (4 or 8), so the fold of
+            // bits 3..5 is the same for all of them
+            if constexpr (BITS == 8) {
+                const int base = xunit(c * 4);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float f[RW][4];
+#pragma unroll
+                    for (int r = 0; r < RW; ++r) {
+                        const uint32_t wj = j == 0 ? q[r].x : (j == 1 ? q[r].y : (j == 2 ? q[r].z : q[r].w));
+                        const uint32_t wb = wj ^ 0x80808080u;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) f[r][i] = i8_to_f32(wb, i);
+                    }
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        const float4 xv = xs4[m * U + (base ^ j)];
+#pragma unroll
+                        for (int r = 0; r < RW; ++r) {
+                            part[r][m] = fmaf(f[r][0], xv.x, part[r][m]);
+                            part[r][m] = fmaf(f[r][1], xv.y, part[r][m]);
+                            part[r][m] = fmaf(f[r][2], xv.z, part[r][m]);
+                            part[r][m] = fmaf(f[r][3], xv.w, part[r][m]);
                         }
                     }
-                } else {
+                }
+            } else {
+                const int base = xunit(c * 8);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {          // word i: codes 8i .. 8i + 7, x units 2i, 2i + 1
-                        const uint32_t wb = w[i] ^ 0x88888888u;
-                        const uint32_t lo = wb & 0x0F0F0F0Fu;          // byte b: code 8i + 2b, plus 8
-                        const uint32_t hi = (wb >> 4) & 0x0F0F0F0Fu;   // byte b: code 8i + 2b + 1, plus 8
+                for (int i = 0; i < 4; ++i) {           // word i: codes 8i .. 8i + 7, x units 2i, 2i + 1
+                    uint32_t lo[RW], hi[RW];
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {                  // x unit 2i + h: bytes 2h, 2h + 1
-                            const float f0 = i4b_to_f32(lo, 2 * h), f1 = i4b_to_f32(hi, 2 * h);
-                            const float f2 = i4b_to_f32(lo, 2 * h + 1), f3 = i4b_to_f32(hi, 2 * h + 1);
-                            const int ph = xunit(c * 8 + 2 * i + h);
+                    for (int r = 0; r < RW; ++r) {
+                        const uint32_t wi = i == 0 ? q[r].x : (i == 1 ? q[r].y : (i == 2 ? q[r].z : q[r].w));
+                        const uint32_t wb = wi ^ 0x88888888u;
+                        lo[r] = wb & 0x0F0F0F0Fu;               // byte b: code 8i + 2b, plus 8
+                        hi[r] = (wb >> 4) & 0x0F0F0F0Fu;        // byte b: code 8i + 2b + 1, plus 8
+                    }
 #pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                const float4 xv = xs4[m * U + ph];
-                                part[m] = fmaf(f0, xv.x, part[m]);
-                                part[m] = fmaf(f1, xv.y, part[m]);
-                                part[m] = fmaf(f2, xv.z, part[m]);
-                                part[m] = fmaf(f3, xv.w, part[m]);
+                    for (int h = 0; h < 2; ++h) {               // x unit 2i + h: bytes 2h, 2h + 1
+                        float f[RW][4];
+#pragma unroll
+                        for (int r = 0; r < RW; ++r) {
+                            f[r][0] = i4b_to_f32(lo[r], 2 * h);
+                            f[r][1] = i4b_to_f32(hi[r], 2 * h);
+                            f[r][2] = i4b_to_f32(lo[r], 2 * h + 1);
+                            f[r][3] = i4b_to_f32(hi[r], 2 * h + 1);
+                        }
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            const float4 xv = xs4[m * U + (base ^ (2 * i + h))];
+#pragma unroll
+                            for (int r = 0; r < RW; ++r) {
+                                part[r][m] = fmaf(f[r][0], xv.x, part[r][m]);
+                                part[r][m] = fmaf(f[r][1], xv.y, part[r][m]);
+                                part[r][m] = fmaf(f[r][2], xv.z, part[r][m]);
+                                part[r][m] = fmaf(f[r][3], xv.w, part[r][m]);
                             }
                         }
                     }
                 }
+            }
 #pragma unroll
-                for (int m = 0; m < MT; ++m) acc[m] = fmaf(s[u], part[m], acc[m]);
+            for (int r = 0; r < RW; ++r)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) acc[r][m] = fmaf(sc[r], part[r][m], acc[r][m]);
             }
         }
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
+        for (int r = 0; r < RW; ++r)
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
-        }
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) acc[r][m] += __shfl_xor_sync(0xffffffffu, acc[r][m], off);
         if (lane == 0) {
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                if (m >= p.M) break;
-                if (p.ytype == 0)
-                    static_cast<float *>(p.Y)[m * p.ldy + n] = acc[m];
-                else
-                    static_cast<uint16_t *>(p.Y)[m * p.ldy + n] = f32_to_bf16_bits(acc[m]);
+            for (int r = 0; r < RW; ++r) {
+                if (!valid[r]) break;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (m >= p.M) break;
+                    if (p.ytype == 0)
+                        static_cast<float *>(p.Y)[m * p.ldy + n0 + r] = acc[r][m];
+                    else
+                        static_cast<uint16_t *>(p.Y)[m * p.ldy + n0 + r] = f32_to_bf16_bits(acc[r][m]);
+                }
             }
         }
     }
 }
 
-template <int BITS, int MT>
-tq_status launch_mt(const BlockedParams &p, const DeviceInfo &dev, cudaStream_t s) {
+template <int BITS, int MT, int RW>
+tq_status launch_rw(const BlockedParams &p, const DeviceInfo &dev, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(MT) * p.K * 4;
     static bool attr_set[64] = {};
     if (smem > 48 * 1024 && dev.id < 64 && !attr_set[dev.id]) {
-        const cudaError_t e = cudaFuncSetAttribute(k_gemv_blocked<BITS, MT>,
+        const cudaError_t e = cudaFuncSetAttribute(k_gemv_blocked<BITS, MT, RW>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    dev.smem_optin);
         if (e != cudaSuccess) return cuda_fail(e);
         attr_set[dev.id] = true;
     }
-    // resident CTAs per SM: as the register bound allows, fewer when the staged
-    // rows (plus the 1 KB each CTA reserves) do not fit the SM's 228 KB
+    // resident CTAs per SM: as the kernel's registers allow (64K a SM, taken in
+    // steps of 8 a thread), fewer when the staged rows (plus the 1 KB each CTA
+    // reserves) do not fit the SM's 228 KB
+    static int regs[64] = {};
+    if (dev.id < 64 && regs[dev.id] == 0) {
+        cudaFuncAttributes fa;
+        const cudaError_t e = cudaFuncGetAttributes(&fa, k_gemv_blocked<BITS, MT, RW>);
+        if (e != cudaSuccess) return cuda_fail(e);
+        regs[dev.id] = fa.numRegs > 0 ? fa.numRegs : 64;
+    }
+    const int r8 = ((dev.id < 64 ? regs[dev.id] : 80) + 7) / 8 * 8;
+    const int occ_regs = 65536 / (r8 * kBlkThreads);
     int occ = static_cast<int>((228 * 1024) / (smem + 1024));
-    occ = occ < 1 ? 1 : (occ > blk_min_ctas(MT) ? blk_min_ctas(MT) : occ);
-    const int64_t need = (p.N + kBlkThreads / 32 - 1) / (kBlkThreads / 32);
+    occ = occ > occ_regs ? occ_regs : occ;
+    occ = occ < 1 ? 1 : (occ > 8 ? 8 : occ);
+    const int64_t need = ((p.N + RW - 1) / RW + kBlkThreads / 32 - 1) / (kBlkThreads / 32);
     const int64_t wave = static_cast<int64_t>(dev.sms) * occ;
     const unsigned grid = static_cast<unsigned>(need < wave ? need : wave);
-    k_gemv_blocked<BITS, MT><<<grid, kBlkThreads, smem, s>>>(p);
+    k_gemv_blocked<BITS, MT, RW><<<grid, kBlkThreads, smem, s>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+// Two rows a warp only when they still fill every SM with three CTAs (up to
+// two tokens): fewer, longer warps stream better, but a short matrix would
+// leave SMs idle.
+template <int BITS, int MT>
+tq_status launch_mt(const BlockedParams &p, const DeviceInfo &dev, cudaStream_t s) {
+    if (MT <= 2 && p.N >= static_cast<int64_t>(2) * (kBlkThreads / 32) * 3 * dev.sms)
+        return launch_rw<BITS, MT, (MT <= 2 ? 2 : 1)>(p, dev, s);
+    return launch_rw<BITS, MT, 1>(p, dev, s);
 }
 
 template <int BITS>
