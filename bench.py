@@ -530,10 +530,12 @@ def swiglu_measure(device, reps=5, M=4032, K=12288):
 
 # ------------------------------------------------------------------ CPU oracle
 
-def cpu_oracle_decode(bits, budget_s=12.0, min_calls=3):
+def cpu_oracle_decode(bits, budget_s=12.0, min_calls=3, max_calls=60):
     """The oracle (as it stands) on a bounded sample of the decode workload:
     per call, the rotation of the input row and the A16 product with the
-    oracle's own weight codes (quantised once, untimed)."""
+    oracle's own weight codes (quantised once, untimed).  The sample ends at
+    max_calls calls or after budget_s seconds, whichever is first; the 60
+    seeded inputs are cycled."""
     import numpy as np
     import oracle
     from dit_convrot_linear_gb300 import synth
@@ -546,10 +548,10 @@ def cpu_oracle_decode(bits, budget_s=12.0, min_calls=3):
     nbytes = 0
     n = 0
     t0 = time.perf_counter()
-    while n < min_calls or (time.perf_counter() - t0 < budget_s and n < 60):
+    while n < min_calls or (time.perf_counter() - t0 < budget_s and n < max_calls):
         Wq, sw, p = qw[n % 3]
         codes = oracle.weight_codes(Wq, bits, p.K)
-        xr = oracle.rotate_act_bf16(xs[n])
+        xr = oracle.rotate_act_bf16(xs[n % 60])
         oracle.linear_a16(xr, codes, sw)
         nbytes += p.N * p.K * bits // 8 + 4 * p.N
         n += 1
@@ -723,7 +725,7 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
         try:
-            cpu = cpu_oracle_decode(8)
+            cpu = cpu_oracle_decode(8, budget_s=10.0, max_calls=10 ** 6)
         except Exception as exc:
             cpu = {"error": repr(exc)}
 
