@@ -158,3 +158,37 @@ def test_blocked_product_graph_replay_is_deterministic(tq):
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(first.view(np.uint32), to_np(Y).view(np.uint32))
+
+
+# int4 on matrices that fill the GPU (the two-rows-a-warp variants and their
+# last, ragged row pair), K with a partial last group, one to eight tokens,
+# both formats, fp32 and bf16 outputs
+TC4 = [(1, 4864, 896, 32, 1), (2, 5000, 2304 + 32, 32, 1), (3, 4870, 1024, 64, 0), (8, 4864, 896, 128, 1),
+       (5, 4900, 544, 32, 1), (4, 4880, 2304 + 64, 32, 0), (1, 6000, 4096, 256, 1), (6, 4864, 2304, 32, 0),
+       (1, 7297, 896, 32, 1), (2, 8001, 544, 32, 0)]
+
+
+@pytest.mark.parametrize("M,N,K,G,rotate", [(1, 7297, 896, 32, 0), (2, 8001, 2304 + 64, 64, 1)])
+def test_blocked_int8_two_rows_a_warp_ragged(tq, M, N, K, G, rotate):
+    """N large enough for two rows a warp, and odd: the last warp's second row
+    is past N (loads nothing, stores nothing)."""
+    W = synth.tensor(f"gpu/blk2r/w{N}x{K}", N, K, *WD)
+    X = synth.tensor(f"gpu/blk2r/x{M}x{K}", M, K, *XD)
+    codes, sw, Wc = gpu_blocked(tq, W, 8, G, rotate)
+    Y = tq.linear_blocked(to_dev_bf16(X), codes, sw, N, 8, G, bool(rotate))
+    assert tq.device_status() == 0
+    check_product(tq, X, Wc, sw, G, rotate, Y)
+
+
+@pytest.mark.parametrize("M,N,K,G,rotate", TC4)
+def test_blocked_int4_full_width_matches_the_oracle(tq, M, N, K, G, rotate):
+    W = synth.tensor(f"gpu/blkfw/w{N}x{K}", N, K, 0.015, 0.005, 30.0)
+    X = synth.tensor(f"gpu/blkfw/x{M}x{K}", M, K, *XD)
+    codes, sw, Wc = gpu_blocked(tq, W, 4, G, rotate)
+    Y = tq.linear_blocked(to_dev_bf16(X), codes, sw, N, 4, G, bool(rotate))
+    assert tq.device_status() == 0
+    check_product(tq, X, Wc, sw, G, rotate, Y)
+    Yb = tq.linear_blocked(to_dev_bf16(X), codes, sw, N, 4, G, bool(rotate), out="bf16")
+    Xa = bf16_bits(tq.rotate_act_bf16(to_dev_bf16(X))) if rotate else X
+    ref = oracle.linear_a16_blocked(Xa, Wc, to_np(sw), G)
+    assert bf16_ulp_diff(bf16_bits(Yb), oracle.round_bf16(ref)).max() <= 1
