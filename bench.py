@@ -726,6 +726,13 @@ def main():
     if rank == 0 and world == 1 and not args.skip_cpu:
         try:
             cpu = cpu_oracle_decode(8, budget_s=10.0, max_calls=10 ** 6)
+            import oracle
+            oracle.set_threads(1)
+            try:
+                one = cpu_oracle_decode(8, budget_s=3.0, max_calls=10 ** 6)
+            finally:
+                oracle.set_threads(None)
+            cpu["single_thread"] = {"value": one["value"], "unit": one["unit"], "sample": one["sample"]}
         except Exception as exc:
             cpu = {"error": repr(exc)}
 

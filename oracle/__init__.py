@@ -128,9 +128,18 @@ def source() -> str:
         return f.read()
 
 
+_threads = None
+
+
 def threads() -> int:
-    """Threads the oracle runs on: every host core."""
-    return max(1, os.cpu_count() or 1)
+    """Threads the oracle runs on: every host core, unless set_threads chose."""
+    return _threads or max(1, os.cpu_count() or 1)
+
+
+def set_threads(n=None):
+    """Run the oracle on n threads (None: every host core again)."""
+    global _threads
+    _threads = None if n is None else max(1, int(n))
 
 
 def _c(a, dtype):
