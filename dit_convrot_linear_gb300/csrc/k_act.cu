@@ -232,7 +232,7 @@ __device__ __forceinline__ void put_tiled(uint16_t *At, int64_t KT, int64_t K, i
 // SWIGLU: the row is h = bf16(silu(g) * u), gate rows from X (ldx) and up
 // rows from U (ldu); a buffer then holds a gate row and an up row.
 template <int GPW, bool TILED, int NT, bool SWIGLU = false>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, NT == 128 ? 5 : 2)   // 5 CTAs of 4 warps, or 2 of 8, an SM
 k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx,
                     void *__restrict__ out, float *__restrict__ sx, int S,
                     unsigned int *status, unsigned int *max_l1, const uint16_t *__restrict__ U,
@@ -240,6 +240,8 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
     extern __shared__ __align__(128) unsigned char ring[];   // [S][2K or 4K] then S barriers
     __shared__ float red[NT / 32];
     __shared__ unsigned int win[16];   // a row's sum of |codes| per 1024-column window
+    __shared__ unsigned int winq[16];  // a row's sum of codes squared per 1024-column window
+    __shared__ unsigned int run_sh[2][5][32];   // warp 0's largest run sums over the rows
     __shared__ int abort_sh;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int W = NT / 32;
@@ -273,7 +275,9 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
         }
     };
 
-    if (threadIdx.x < 16) win[threadIdx.x] = 0;
+    if (threadIdx.x < 16) win[threadIdx.x] = winq[threadIdx.x] = 0;
+    if (TILED && threadIdx.x < 32)
+        for (int j = 0; j < 5; ++j) run_sh[0][j][threadIdx.x] = run_sh[1][j][threadIdx.x] = 0u;
     if (threadIdx.x == 0) {
         abort_sh = 0;
         for (int i = 0; i < S; ++i)
@@ -344,17 +348,25 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
         if (threadIdx.x == 0) sx[m] = s;
         const int64_t KT = (K + 63) >> 6;
         // with the tiled operand, also the row's sum of |codes| per 1024-column
-        // window (each at most 127 * 1024)
+        // window (each at most 127 * 1024) and its sum of codes squared per
+        // window (a whole row at most 127^2 * 16384 < 2^32)
         auto put = [&](int64_t g, int e, const float (&q)[8]) {
             const int64_t k0 = g * kGroup + static_cast<int64_t>(lane) * e;
             if constexpr (TILED) {
                 put_tiled(static_cast<uint16_t *>(out), KT, K, m, k0, e, q);
-                unsigned int gs = 0;
+                float fs = 0.0f, fq = 0.0f;      // exact: at most 8 x 127 and 8 x 127^2
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    if (j < e) gs += static_cast<unsigned int>(fabsf(q[j]));
-                gs = __reduce_add_sync(0xffffffffu, gs);
-                if (lane == 0) atomicAdd(&win[g >> 2], gs);
+                    if (j < e) {
+                        fs += fabsf(q[j]);
+                        fq = fmaf(q[j], q[j], fq);
+                    }
+                const unsigned int gs = __reduce_add_sync(0xffffffffu, static_cast<unsigned int>(fs));
+                const unsigned int gq = __reduce_add_sync(0xffffffffu, static_cast<unsigned int>(fq));
+                if (lane == 0) {
+                    atomicAdd(&win[g >> 2], gs);
+                    atomicAdd(&winq[g >> 2], gq);
+                }
             } else
                 put_int8(static_cast<int8_t *>(out) + m * K + k0, e, q);
         };
@@ -388,25 +400,46 @@ k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         if (TILED && warp == 0) {
-            // lane l holds window l (1024 columns; zero past K).  Word 1 + j:
-            // the largest sum over an aligned run of 2^j windows; word 0: the
-            // whole row.  Sums by butterfly within aligned lane groups, then a
-            // maximum over the lanes.
+            // lane l holds window l (1024 columns; zero past K).  Sums over
+            // aligned runs of 2^j windows by butterfly within aligned lane
+            // groups; each lane keeps its largest over the rows in run_sh (the
+            // maximum over the lanes and CTAs is taken once, after the last row).
             unsigned int ws = lane < 16 ? win[lane] : 0u;
-            if (lane < 16) win[lane] = 0;
+            unsigned int wq = lane < 16 ? winq[lane] : 0u;
+            if (lane < 16) win[lane] = winq[lane] = 0;
 #pragma unroll
             for (int j = 0; j < 5; ++j) {
-                if (j > 0) ws += __shfl_xor_sync(0xffffffffu, ws, 1 << (j - 1));
-                unsigned int mx = ws;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                if (lane == 0) {
-                    atomicMax(max_l1 + 1 + j, mx);
-                    if (j == 4) atomicMax(max_l1, mx);
+                if (j > 0) {
+                    ws += __shfl_xor_sync(0xffffffffu, ws, 1 << (j - 1));
+                    wq += __shfl_xor_sync(0xffffffffu, wq, 1 << (j - 1));
                 }
+                run_sh[0][j][lane] = max(run_sh[0][j][lane], ws);
+                run_sh[1][j][lane] = max(run_sh[1][j][lane], wq);
             }
         }
         if (threadIdx.x == 0 && i + S < nrows) issue(i + S);
+    }
+    // Trailer: word 1 + j the largest sum of |codes| over an aligned run of
+    // 2^j windows, word 0 over a whole row (16 windows hold the longest row);
+    // words 7 + j and 6 the same for codes squared.
+    if (TILED && warp == 0) {
+#pragma unroll
+        for (int j = 0; j < 5; ++j) {
+            unsigned int mx = run_sh[0][j][lane], mq = run_sh[1][j][lane];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                mq = max(mq, __shfl_xor_sync(0xffffffffu, mq, o));
+            }
+            if (lane == 0 && nrows > 0) {
+                atomicMax(max_l1 + 1 + j, mx);
+                atomicMax(max_l1 + 7 + j, mq);
+                if (j == 4) {
+                    atomicMax(max_l1, mx);
+                    atomicMax(max_l1 + 6, mq);
+                }
+            }
+        }
     }
     // After an expired wait, let the copies still in flight land (bounded)
     // before the CTA's shared memory is released.
@@ -574,7 +607,7 @@ tq_status launch_rotate_quant_tiled(const uint16_t *X, int64_t M, int64_t K, int
     if (K > kRingMaxK) return TQ_ERR_SHAPE;
     unsigned int *max_l1 = reinterpret_cast<unsigned int *>(static_cast<unsigned char *>(At) +
                                                             tiled_act_tiles_bytes(M, K));
-    const cudaError_t e = cudaMemsetAsync(max_l1, 0, 6 * sizeof(unsigned int), s);
+    const cudaError_t e = cudaMemsetAsync(max_l1, 0, 12 * sizeof(unsigned int), s);
     if (e != cudaSuccess) return cuda_fail(e);
     return launch_ring<true>(X, M, K, ldx, At, sx, max_l1, s);
 }
@@ -585,7 +618,7 @@ tq_status launch_swiglu_quant_tiled(const uint16_t *G, int64_t ldg, const uint16
     if (K > kRingMaxK) return TQ_ERR_SHAPE;
     unsigned int *max_l1 = reinterpret_cast<unsigned int *>(static_cast<unsigned char *>(At) +
                                                             tiled_act_tiles_bytes(M, K));
-    const cudaError_t e = cudaMemsetAsync(max_l1, 0, 6 * sizeof(unsigned int), s);
+    const cudaError_t e = cudaMemsetAsync(max_l1, 0, 12 * sizeof(unsigned int), s);
     if (e != cudaSuccess) return cuda_fail(e);
     return launch_ring<true, true>(G, M, K, ldg, At, sx, max_l1, s, U, ldu);
 }

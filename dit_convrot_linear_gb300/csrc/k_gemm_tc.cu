@@ -111,7 +111,11 @@ struct TcParams {
     int mtiles, ntiles, ksteps, chunk_steps;
     unsigned int *status;
     const unsigned char *At;   // pre-tiled fp16 A codes (AT path), else null
-    const unsigned int *max_l1;  // largest row sum of |A codes| (tiled operand), or null
+    const unsigned int *max_l1;  // largest row sum of |A codes| (tiled operand), or null; word 6:
+                                 // the largest row sum of A codes squared
+    const unsigned int *w_sq;    // largest row sum of B codes squared (tiled weights), or null;
+                                 // word 1 + j: per aligned window of 1024 * 2^j columns
+                                 // (max_l1[7 + j] the same for A)
     // epilogue: Y = R + g[n] * (sx sw acc + b[n]); any of them may be absent
     const float *bias, *gate;
     const void *R;
@@ -424,9 +428,18 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     bool single = p.ksteps <= cs;
     if (!single && p.max_l1) {
         single = static_cast<double>(p.max_l1[0]) * qmax < 16777216.0;
+        // or by Cauchy-Schwarz: any partial sum is at most sum |a_k| |b_k| <=
+        // |a|_2 |b|_2, so the largest row sums of squares on both sides with a
+        // product below 2^48 keep every partial sum below 2^24 (the product of
+        // two integers below 2^32 rounds in double, but not below 2^48 when
+        // it is at least 2^48)
+        if (!single && p.w_sq)
+            single = static_cast<double>(p.max_l1[6]) * static_cast<double>(p.w_sq[0]) < 281474976710656.0;
         for (int j = 4; j >= 0 && !single; --j) {
             const int steps = (1024 << j) / BK;
-            if (steps > cs && static_cast<double>(p.max_l1[1 + j]) * qmax < 16777216.0) {
+            if (steps > cs && (static_cast<double>(p.max_l1[1 + j]) * qmax < 16777216.0 ||
+                               (p.w_sq && static_cast<double>(p.max_l1[7 + j]) *
+                                                  static_cast<double>(p.w_sq[1 + j]) < 281474976710656.0))) {
                 cs = steps;
                 break;
             }
@@ -880,7 +893,7 @@ tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const unsigned ch
     CUtensorMap tmA, tmB;
     if constexpr (MODE == 2) {
         if (!make_map_u8(&tmA, At, tiled_act_tiles_bytes(M, K) / 128, 128, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-            !make_map_u8(&tmB, Wt, weights_tiled_bytes(N, K) / 128, 128, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+            !make_map_u8(&tmB, Wt, (weights_tiled_bytes(N, K) - 256) / 128, 128, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
             return TQ_ERR_DEVICE;
     } else {
         const bool mapped = bits == 8 ? make_map_u8(&tmB, Wq, N, K, BK, 128, CU_TENSOR_MAP_SWIZZLE_64B)
@@ -909,6 +922,9 @@ tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const unsigned ch
     p.status = status;
     p.At = At;
     p.max_l1 = AT ? reinterpret_cast<const unsigned int *>(At + tiled_act_tiles_bytes(M, K)) : nullptr;
+    p.w_sq = (MODE == 2 && Wt) ? reinterpret_cast<const unsigned int *>(static_cast<const unsigned char *>(Wt) +
+                                                                        weights_tiled_bytes(N, K) - 256)
+                               : nullptr;
     if (ea) {
         p.bias = ea->bias;
         p.gate = ea->gate;

@@ -235,6 +235,62 @@ k_tile_weights(const uint8_t *Wq, int64_t N, int64_t K, int64_t KT, int64_t Npad
     }
 }
 
+// The largest row sums of codes squared, for the product's exactness bound:
+// word 0 of the tiled weights' trailer over whole rows, word 1 + j over
+// aligned runs of 2^j windows of 1024 columns (at most 127^2 * 16384 < 2^32).
+// One warp per row: window w's sum is reduced over the lanes into lane w,
+// then runs of windows are summed by butterfly within aligned lane groups.
+template <int BITS>
+__global__ void __launch_bounds__(256)
+k_weight_sq(const uint8_t *Wq, int64_t N, int64_t K, unsigned int *out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rb = K * BITS / 8;                   // a multiple of 16
+    const int64_t wb = 1024 * BITS / 8;                // bytes of a 1024-column window
+    for (int64_t n = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; n < N;
+         n += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
+        const uint8_t *row = Wq + n * rb;
+        unsigned int mine = 0;                         // lane w: window w (zero past K)
+        for (int w = 0; w * wb < rb; ++w) {
+            unsigned int sq = 0;
+            const int64_t end = (w + 1) * wb < rb ? (w + 1) * wb : rb;
+            for (int64_t b = w * wb + static_cast<int64_t>(lane) * 16; b < end; b += 32 * 16) {
+                const uint4 u = __ldg(reinterpret_cast<const uint4 *>(row + b));
+                const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if constexpr (BITS == 8) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int c = static_cast<int8_t>((q[i] >> (8 * j)) & 0xFFu);
+                            sq += static_cast<unsigned int>(c * c);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int v = static_cast<int>((q[i] >> (4 * j)) & 0xFu);
+                            const int c = v >= 8 ? v - 16 : v;
+                            sq += static_cast<unsigned int>(c * c);
+                        }
+                    }
+                }
+            }
+            sq = __reduce_add_sync(0xffffffffu, sq);
+            if (lane == w) mine = sq;
+        }
+#pragma unroll
+        for (int j = 0; j < 5; ++j) {
+            if (j > 0) mine += __shfl_xor_sync(0xffffffffu, mine, 1 << (j - 1));
+            unsigned int mx = mine;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (lane == 0) {
+                atomicMax(out + 1 + j, mx);
+                if (j == 4) atomicMax(out, mx);
+            }
+        }
+    }
+}
+
 }  // namespace
 
 tq_status launch_quantize_weights_blocked(const uint16_t *W, int64_t N, int64_t K, int64_t ldw, int bits,
@@ -267,8 +323,10 @@ tq_status launch_quantize_weights(const uint16_t *W, int64_t N, int64_t K,
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 
+// The tiles, then a 256-byte trailer of the largest row sums of codes squared
+// (k_weight_sq).
 int64_t weights_tiled_bytes(int64_t N, int64_t K) {
-    return ((N + 255) / 256) * 2 * ((K + 63) / 64) * 16384;
+    return ((N + 255) / 256) * 2 * ((K + 63) / 64) * 16384 + 256;
 }
 
 tq_status launch_tile_weights(const uint8_t *Wq, int64_t N, int64_t K, int bits, void *Wt, cudaStream_t s) {
@@ -278,7 +336,15 @@ tq_status launch_tile_weights(const uint8_t *Wq, int64_t N, int64_t K, int bits,
     const int64_t blocks = (total + 255) / 256 < 152 * 64 ? (total + 255) / 256 : 152 * 64;
     auto kern = bits == 8 ? k_tile_weights<8> : k_tile_weights<4>;
     kern<<<static_cast<unsigned>(blocks), 256, 0, s>>>(Wq, N, K, KT, Npad, static_cast<uint16_t *>(Wt));
-    const cudaError_t e = cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned int *trailer = reinterpret_cast<unsigned int *>(static_cast<unsigned char *>(Wt) +
+                                                             weights_tiled_bytes(N, K) - 256);
+    if ((e = cudaMemsetAsync(trailer, 0, 256, s)) != cudaSuccess) return cuda_fail(e);
+    const int64_t wblocks = (N + 7) / 8 < 152 * 64 ? (N + 7) / 8 : 152 * 64;   // 8 rows a block
+    auto sq = bits == 8 ? k_weight_sq<8> : k_weight_sq<4>;
+    sq<<<static_cast<unsigned>(wblocks), 256, 0, s>>>(Wq, N, K, trailer);
+    e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 

@@ -247,6 +247,9 @@ size_t tq_weights_tiled_bytes(int64_t N, int64_t K);
  *   Wq      codes [N, K] as written by tq_quantize_weights, 16-byte aligned.
  *   Wt      at least tq_weights_tiled_bytes(N, K) bytes, 256-byte aligned; its
  *           layout is private to this library (read it through tq_linear_tt).
+ *           After the tiles it records the rows' largest sum of codes
+ *           squared. With the activations' own, the product then knows when
+ *           one fp32 accumulation over all of K stays exact (Cauchy-Schwarz).
  */
 tq_status tq_tile_weights(const void *Wq, int64_t N, int64_t K, int bits, void *Wt,
                           size_t wt_bytes, cudaStream_t stream);

@@ -238,8 +238,8 @@ def test_grouped_create_without_a_gpu_reports_no_device(L):
 
 def test_tiled_weights_refusals_and_size(L):
     # rows padded to 256, columns to 64: ceil(300/256)*2 row tiles x 48 column tiles x 16 KB
-    assert L.tq_weights_tiled_bytes(300, 3072) == 4 * 48 * 16384
-    assert L.tq_weights_tiled_bytes(256, 32) == 2 * 1 * 16384
+    assert L.tq_weights_tiled_bytes(300, 3072) == 4 * 48 * 16384 + 256   # tiles, then a trailer
+    assert L.tq_weights_tiled_bytes(256, 32) == 2 * 1 * 16384 + 256
     assert L.tq_weights_tiled_bytes(1, 96) == 0                 # K not a valid row length
     assert L.tq_weights_tiled_bytes(1, 16384 + 256) == 0        # above TQ_MAX_K_TILED
     assert L.tq_tile_weights(FAKE, 16, 256, 5, FAKE, 1 << 20, S0) == BITS

@@ -272,6 +272,35 @@ def test_tiled_weights_match_the_converting_product(tq, M, N, K, bits):
     assert tq.device_status() == 0
 
 
+@pytest.mark.parametrize("M,N,K,bits", [(300, 129, 3072, 8), (257, 300, 4096 + 32, 4), (64, 256, 12288, 8)])
+def test_tiled_trailers_hold_the_largest_row_sums_of_squares(tq, M, N, K, bits):
+    """The product's exactness bound reads, after the tiles, the activation
+    rows' and the weight rows' largest sum of codes squared (word 6 of the
+    activation trailer, word 0 of the weights'): both equal the maximum over
+    the real rows computed from the codes themselves."""
+    X = to_dev_bf16(xgen(f"gpu/trail/x{M}x{K}", M, K, XD))
+    codes, sw = gpu_weights(tq, wgen(f"gpu/trail/w{N}x{K}", N, K, WD if bits == 8 else WB), bits)
+    At, sx = tq.rotate_quant_act_tiled(X)
+    a = untile_codes(At, M, K).astype(np.int64)
+    at_tr = to_np(At[tq.act_tiled_bytes(M, K) - 256:]).view(np.uint32)
+    def window_max(v, j):          # largest sum over an aligned run of 2^j 1024-column windows
+        L = 1024 << j
+        pad = np.zeros((v.shape[0], -v.shape[1] % L), dtype=np.int64)
+        return int(np.concatenate([v, pad], axis=1).reshape(v.shape[0], -1, L).sum(axis=2).max())
+    assert int(at_tr[6]) == int((a * a).sum(axis=1).max())
+    # words 0..5: the |code| row sums, whole and per aligned window; 7..11 the squares per window
+    assert int(at_tr[0]) == int(np.abs(a).sum(axis=1).max())
+    for j in range(5):
+        assert int(at_tr[1 + j]) == window_max(np.abs(a), j)
+        assert int(at_tr[7 + j]) == window_max(a * a, j)
+    Wt = tq.tile_weights(codes, N, K, bits)
+    w = codes_np(codes, bits, K).astype(np.int64)
+    wt_tr = to_np(Wt[tq.weights_tiled_bytes(N, K) - 256:]).view(np.uint32)
+    assert int(wt_tr[0]) == int((w * w).sum(axis=1).max())
+    for j in range(5):
+        assert int(wt_tr[1 + j]) == window_max(w * w, j)
+
+
 @pytest.mark.parametrize("N,K", [(12288, 3072), (3072, 12288)])
 def test_tiled_weights_dit_m4032_sampled(tq, N, K):
     """The DiT projections at full size through the both-tiled product, in the
