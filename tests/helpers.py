@@ -59,16 +59,16 @@ def check_codes_close(got, ref, frac=CODE_FLIP_FRAC):
     return flips
 
 
-def untile_codes(At, M, K):
+def untile_codes(At, M, K, rows=None):
     """Codes [M, K] (int) from a tiled activation operand (test decoding of the
     library's private layout: fp16 codes in 128-row x 64-column tiles, tile
     (mt, kt) at halfword (mt * ceil(K/64) + kt) * 8192, core matrix (r/8, k/8)
     of 64 halfwords at ((r/8) * 8 + k/8) * 64, element (r%8, k%8) at
-    (r%8) * 8 + k%8)."""
+    (r%8) * 8 + k%8).  With `rows`, only those rows, in that order."""
     import torch
     KT = (K + 63) // 64
     h = At.view(torch.uint8)[: ((M + 255) // 256) * 2 * KT * 16384].view(torch.float16).cpu().numpy()
-    m = np.arange(M)[:, None]
+    m = (np.arange(M) if rows is None else np.asarray(rows))[:, None]
     k = np.arange(K)[None, :]
     idx = ((m // 128) * KT + k // 64) * 8192 + (((m % 128) // 8) * 8 + (k % 64) // 8) * 64 + (m % 8) * 8 + k % 8
     return h[idx].astype(np.int64)

@@ -398,6 +398,26 @@ def test_swiglu_fused_operand(tq, M, K):
     assert tq.device_status() == 0
 
 
+def test_swiglu_fused_operand_full_size_sampled(tq):
+    """The DiT down projection's operand at the size the bench times (M = 4032,
+    K = 12288), from gate and up in one pass: sampled token rows against the
+    oracle's SwiGLU then quantiser on the same rows, and the trailer's exact
+    row sums on them."""
+    M, K = 4032, 12288
+    G = xgen("gpu/swfull/g", M, K, (1.5, 0.0, 1.0))
+    U = xgen("gpu/swfull/u", M, K, XD)
+    At, sx = tq.swiglu_quant_act_tiled(to_dev_bf16(G), to_dev_bf16(U))
+    assert tq.device_status() == 0
+    rows = np.sort(np.random.default_rng(11).choice(M, 24, replace=False))
+    codes = untile_codes(At, M, K, rows=rows)
+    rq, rs = oracle.swiglu_quant_act(G[rows], U[rows])
+    check_codes_close(codes, rq, frac=CODE_FLIP_FRAC)
+    assert np.max(np.abs(to_np(sx)[rows].astype(np.float64) / np.where(rs == 0, 1, rs) - 1)) <= SCALE_REL
+    tr = to_np(At[tq.act_tiled_bytes(M, K) - 256:]).view(np.uint32)
+    assert int(tr[0]) >= int(np.abs(codes).sum(axis=1).max())     # a maximum over all rows
+    assert int(tr[6]) >= int((codes * codes).sum(axis=1).max())
+
+
 def test_swiglu_fused_operand_feeds_the_product(tq):
     """gate/up -> fused SwiGLU operand -> both-tiled down product, against the
     oracle's int32 sums on the same codes (exact) and its Y."""
