@@ -13,8 +13,10 @@
 //   - Each CTA first stages the token rows in shared memory as fp32 (rotating
 //     them itself when asked), in 16-byte units swizzled so that the warp's
 //     vector reads below hit distinct banks.
-//   - A warp then takes two adjacent weight rows at a time (one for four or
-//     more tokens), so that each x value read from shared memory serves both;
+//   - A warp then takes two adjacent weight rows at a time when the matrix
+//     has rows enough to fill every SM that way and there are at most two
+//     tokens (else one), so that each x value read from shared memory serves
+//     both;
 //     each lane streams 16-byte chunks of codes (16 int8 or 32 int4 codes,
 //     inside one block) with L1-bypassing loads, and the block scale of each
 //     chunk; the next chunk of each row is loaded before this one is used.
