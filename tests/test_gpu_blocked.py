@@ -192,3 +192,20 @@ def test_blocked_int4_full_width_matches_the_oracle(tq, M, N, K, G, rotate):
     Xa = bf16_bits(tq.rotate_act_bf16(to_dev_bf16(X))) if rotate else X
     ref = oracle.linear_a16_blocked(Xa, Wc, to_np(sw), G)
     assert bf16_ulp_diff(bf16_bits(Yb), oracle.round_bf16(ref)).max() <= 1
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_one_block_per_row_is_the_per_row_format(tq, bits):
+    """With G = K (one block a row) and the rotation, the blocked quantiser is
+    the per-row one: the same codes and scales bit for bit, and the blocked
+    product agrees with the per-row A16 product to rounding."""
+    M, N, K = 3, 700, 256
+    W = synth.tensor(f"gpu/blkrow/w{bits}", N, K, *WD)
+    X = to_dev_bf16(synth.tensor(f"gpu/blkrow/x{bits}", M, K, *XD))
+    cb, sb = tq.quantize_weights_blocked(to_dev_bf16(W), bits, K, True)
+    cr, sr = tq.quantize_weights(to_dev_bf16(W), bits)
+    assert np.array_equal(to_np(cb).view(np.uint8), to_np(cr).view(np.uint8))
+    assert np.array_equal(to_np(sb)[:, 0].view(np.uint32), to_np(sr).view(np.uint32))
+    Yb = to_np(tq.linear_blocked(X, cb, sb, N, bits, K, True))
+    Yr = to_np(tq.linear(X, cr, sr, N, bits, "W8A16" if bits == 8 else "W4A16"))
+    assert rel_l2(Yb, Yr) <= 1e-5
