@@ -69,3 +69,20 @@ def test_traffic_lookup_goes_null_on_source_change(tmp_path, monkeypatch):
     assert bench.traffic_for("k_gemv_a16", ["k_gemv.cu", "tq_internal.cuh"]) == 123
     path.write_text(json.dumps({"k_gemv_a16": {"source_sha": "stale", "bytes_per_launch": 123}}))
     assert bench.traffic_for("k_gemv_a16", ["k_gemv.cu", "tq_internal.cuh"]) is None
+
+
+def test_cpu_baseline_sample_bounds_and_threads():
+    """The CPU-oracle baseline stops at its call cap or its time budget, cycles
+    its 60 seeded inputs past the cap of one pass, and reports the threads it
+    ran on (one when the oracle is set to one)."""
+    import oracle
+    r = bench.cpu_oracle_decode(8, budget_s=60.0, min_calls=3, max_calls=62)
+    assert r["sample"].startswith("62 decode calls") and r["kind"] == "oracle"
+    assert r["cores"] == oracle.threads() and r["value"] > 0
+    oracle.set_threads(1)
+    try:
+        one = bench.cpu_oracle_decode(8, budget_s=0.0, min_calls=3)
+        assert one["cores"] == 1 and one["sample"].startswith("3 decode calls")
+    finally:
+        oracle.set_threads(None)
+    assert oracle.threads() == max(1, os.cpu_count() or 1)
