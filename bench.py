@@ -47,9 +47,10 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--calls", type=int, default=1000)
     ap.add_argument("--skip-dit", action="store_true")
-    ap.add_argument("--only", default="all", choices=["all", "decode", "dit", "blocked"],
-                    help="profiling cases: only the W8A16 decode graph, only the DiT GEMMs, or only "
-                         "the block-scaled decode products")
+    ap.add_argument("--only", default="all", choices=["all", "decode", "dit", "blocked", "batched", "chain"],
+                    help="profiling cases: only the W8A16 decode graph, only the DiT GEMMs, only "
+                         "the block-scaled decode products, only the batched W4A16 decode, or only "
+                         "the DiT block chain")
     ap.add_argument("--dit-m", type=int, default=4032, help="token rows of the DiT case")
     ap.add_argument("--skip-cpu", action="store_true")
     return ap.parse_args()
@@ -494,6 +495,180 @@ def dit_measure(device, reps=5, M=4032):
                  "gemm": o / tot["g"], "gemm_tiled_weights": o / tot["g_tt"]}
 
 
+def graph_of(fn):
+    """A CUDA graph of fn's launches (fn run once first, outside the capture,
+    so kernel attributes are set)."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return g
+
+
+def batched_measure(device, steps, warmup, world, l2, hbm, bf16_peak):
+    """Batched decode W4A16 (8B-class projections up 4096 -> 12288 and down
+    12288 -> 4096) at M = 1, 8, 32, 64 token rows.  The seeded weights of the
+    two projections are quantised once and copied into enough distinct
+    buffers that a step's weights exceed three times L2 (identical values,
+    distinct memory: every call streams its weights from HBM).  One step =
+    one tq_linear call per buffer, cycling up and down (a CUDA graph of
+    independent calls, each with its own input and output).  Per M: weight
+    GB/s (packed codes + row scales per call / time) and TFLOP/s (2 M N K),
+    with the roofline min(HBM x bytes, tensor peak): HBM-bound at every M
+    here (2 M flops per weight byte at 4 bits: 128 at M = 64, below the
+    ridge of the measured peaks, 1945.4 / 6.69 = 291)."""
+    import torch
+    from dit_convrot_linear_gb300 import synth, tq
+    w = synth.BATCHED
+    base = []
+    for p in w.projs:
+        codes, sw = tq.quantize_weights(bf16_dev(w.weight(0, p), device), 4)
+        base.append((p, codes, sw))
+    pair_bytes = sum(p.N * p.K // 2 + 4 * p.N for p, _, _ in base)
+    copies = max(2, -(-3 * l2 // pair_bytes))
+    calls = []
+    for c in range(copies):
+        for p, codes, sw in base:
+            calls.append((p, codes.clone(), sw.clone()))
+    torch.cuda.synchronize()
+    out = {"copies": copies, "distinct_weight_mb": round(copies * pair_bytes / 2 ** 20, 1),
+           "calls_per_step": len(calls)}
+    for M in (1, 8, 32, 64):
+        xs = [bf16_dev(w.activation(i, p, M), device) for i, (p, _, _) in enumerate(base)]
+        ys = [torch.empty((M, p.N), dtype=torch.float32, device=device) for p, _, _ in calls]
+
+        def run():
+            for i, (p, codes, sw) in enumerate(calls):
+                tq.linear(xs[i % 2], codes, sw, p.N, 4, "W4A16", Y=ys[i])
+        g = graph_of(run)
+        n = max(20, steps // 10)
+        ms = time_steps(g.replay, n, max(3, warmup), world) / n
+        nbytes = sum(p.N * p.K // 2 + 4 * p.N for p, _, _ in calls)
+        flops = sum(2.0 * M * p.N * p.K for p, _, _ in calls)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        tflops = flops / (ms * 1e-3) / 1e12
+        roof = min(hbm * 1e9 * flops / nbytes, bf16_peak * 1e12) / 1e12
+        per = {}
+        for p, codes, sw in base:   # one projection alone: its CUDA-event time over the copies
+            sub = [(q, c, s) for (q, c, s) in calls if q.name == p.name]
+            x = xs[0] if p.name == base[0][0].name else xs[1]
+            y = torch.empty((M, p.N), dtype=torch.float32, device=device)
+
+            def run_p():
+                for q, c, s in sub:
+                    tq.linear(x, c, s, q.N, 4, "W4A16", Y=y)
+            gp = graph_of(run_p)
+            msp = time_steps(gp.replay, n, 3, world) / n / len(sub)
+            bp = p.N * p.K // 2 + 4 * p.N
+            per[p.name] = {"N": p.N, "K": p.K, "us_per_call": round(msp * 1e3, 2),
+                           "gbs": round(bp / (msp * 1e-3) / 1e9, 1),
+                           "frac": round(bp / (msp * 1e-3) / 1e9 / hbm, 4)}
+        out[f"m{M}"] = {"value": round(gbs * world, 1), "unit": "GB/s",
+                        "tflops": round(tflops * world, 2), "ms_per_step": round(ms, 4),
+                        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                                     "frac": round(gbs / hbm, 4),
+                                     "achieved_tflops": round(tflops, 2),
+                                     "roof_tflops": round(roof, 2)},
+                        "per_projection": per}
+        del xs, ys, g
+    out["kernels"] = "k_gemv_small<4> (M <= 8), k_gemv_a16<4> (M = 32, 64; cluster split-K)"
+    return out
+
+
+def chain_measure(device, steps, warmup, world, bf16_peak, blocks=32, M=1024):
+    """One DiT block's projection chain, 4-bit weights and int8 activations,
+    M = 1024 token rows (512 x 512), 32 blocks.  Per block: rotate + QKV
+    3072 -> 9216; rotate + out 3072 -> 3072; rotate + gate/up 3072 -> 24576
+    (bf16 out); the down operand made from gate and up in one pass (SwiGLU
+    fused into the rotation) + down 12288 -> 3072.  Weights are tiled once at
+    set-up (tq_tile_weights).  The seeded weights of one block are quantised
+    and tiled, then copied into every block's own buffers (identical values,
+    distinct memory, 302 MB a block, so each block streams its weights from
+    HBM); inputs are seeded per block for four blocks and cycled.  One step =
+    the 32 blocks as one CUDA graph.  TOPS = 2 M N K summed over the chain's
+    projections / time."""
+    import torch
+    from dit_convrot_linear_gb300 import synth, tq
+    w = synth.CHAIN
+    P = {p.name: p for p in w.projs}
+    Kd = P["down"].K
+    tiled = {}
+    for p in w.projs:
+        codes, sw = tq.quantize_weights(bf16_dev(w.weight(0, p), device), 4)
+        tiled[p.name] = (tq.tile_weights(codes, p.N, p.K, 4), sw, codes)
+    wts = [{n: (Wt.clone(), sw.clone()) for n, (Wt, sw, _) in tiled.items()} for _ in range(blocks)]
+    xin = [{n: bf16_dev(w.activation(b, P[n], M), device) for n in ("qkv", "out", "gateup")}
+           for b in range(4)]
+    At = {n: torch.empty(tq.act_tiled_bytes(M, P[n].K), dtype=torch.uint8, device=device) for n in P}
+    sx = {n: torch.empty(M, dtype=torch.float32, device=device) for n in P}
+    Y = {n: torch.empty((M, P[n].N), dtype=torch.bfloat16, device=device) for n in P}
+    torch.cuda.synchronize()
+
+    def block(b):
+        x = xin[b % 4]
+        for n in ("qkv", "out", "gateup"):
+            tq.rotate_quant_act_tiled(x[n], At=At[n], sx=sx[n])
+            Wt, sw = wts[b][n]
+            tq.linear_tt(At[n], sx[n], M, P[n].K, Wt, sw, P[n].N, 4, Y=Y[n], out="bf16")
+        gu = Y["gateup"]
+        tq.swiglu_quant_act_tiled(gu[:, :Kd], gu[:, Kd:], At=At["down"], sx=sx["down"])
+        Wt, sw = wts[b]["down"]
+        tq.linear_tt(At["down"], sx["down"], M, Kd, Wt, sw, P["down"].N, 4, Y=Y["down"], out="bf16")
+
+    def chain():
+        for b in range(blocks):
+            block(b)
+    g = graph_of(chain)
+    n = max(5, min(50, steps // 20))
+    ms = time_steps(g.replay, n, max(3, warmup), world) / n
+    ops_block = sum(2.0 * M * p.N * p.K for p in w.projs)
+    tops = blocks * ops_block / (ms * 1e-3) / 1e12
+    # each product alone, over the blocks' weight copies (operands prepared
+    # beforehand), and each operand kernel alone
+    per = {}
+    prod_ms_total = 0.0
+    for n_ in P:
+        p = P[n_]
+
+        def run_p():
+            for b in range(blocks):
+                Wt, sw = wts[b][n_]
+                tq.linear_tt(At[n_], sx[n_], M, p.K, Wt, sw, p.N, 4, Y=Y[n_], out="bf16")
+        gp = graph_of(run_p)
+        msp = time_steps(gp.replay, n, 3, world) / n / blocks
+        ops = 2.0 * M * p.N * p.K
+        prod_ms_total += msp
+        per[n_] = {"N": p.N, "K": p.K, "tiles": (-(-M // 256)) * (-(-p.N // 256)),
+                   "product_us": round(msp * 1e3, 2), "product_tops": round(ops / (msp * 1e-3) / 1e12, 1),
+                   "product_frac": round(ops / (msp * 1e-3) / 1e12 / bf16_peak, 4)}
+    for n_, fn in (("qkv", lambda: tq.rotate_quant_act_tiled(xin[0]["qkv"], At=At["qkv"], sx=sx["qkv"])),
+                   ("down", lambda: tq.swiglu_quant_act_tiled(Y["gateup"][:, :Kd], Y["gateup"][:, Kd:],
+                                                              At=At["down"], sx=sx["down"]))):
+        def run_o():
+            for _ in range(blocks):
+                fn()
+        go = graph_of(run_o)
+        per[n_]["operand_us"] = round(time_steps(go.replay, n, 3, world) / n / blocks * 1e3, 2)
+    prod_tops = ops_block / (prod_ms_total * 1e-3) / 1e12
+    return {"value": round(tops * world, 1), "unit": "TOPS", "ms_per_step": round(ms, 4),
+            "ms_per_block": round(ms / blocks, 4), "blocks": blocks, "M": M,
+            "ops_per_step": blocks * ops_block,
+            "value_is": "32 blocks x (rotation + product for QKV, out, gate/up; SwiGLU operand + down "
+                        "product), one CUDA graph, weights tiled at set-up",
+            "per_projection": per,
+            "roofline": {"bound": "tensor", "kernel": "k_gemm_a8_tc<4, both tiled>",
+                         "achieved": round(prod_tops, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": round(prod_tops / bf16_peak, 4),
+                         "achieved_is": "the block's four products alone, ops / summed product time"}}
+
+
 def swiglu_measure(device, reps=5, M=4032, K=12288):
     """The down projection's operand made from gate and up in one pass
     (tq_swiglu_quant_act_tiled), and, for the unfused route, the rotation of
@@ -614,6 +789,19 @@ def main():
             print(json.dumps({"case": "decode, block-scaled weights", **res}))
         return 0
 
+    bf16_peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    if args.only == "batched":   # profiling case: batched W4A16 decode alone
+        res = batched_measure(device, args.steps, args.warmup, world, l2, float(pk["hbm_gbs"]), bf16_peak)
+        if rank == 0:
+            print(json.dumps({"case": "batched decode W4A16", **res}))
+        return 0
+
+    if args.only == "chain":   # profiling case: the DiT block chain alone
+        res = chain_measure(device, args.steps, args.warmup, world, bf16_peak)
+        if rank == 0:
+            print(json.dumps({"case": "dit chain W4A8 M=1024", **res}))
+        return 0
+
     if args.only == "dit":   # profiling case: the DiT products alone
         per, tops = dit_measure(device, reps=args.steps, M=args.dit_m)
         sw = swiglu_measure(device, reps=args.steps, M=args.dit_m)
@@ -699,10 +887,21 @@ def main():
             extra["decode_blocked"] = {"error": repr(exc)}
         torch.cuda.empty_cache()
 
+    if args.only != "decode":
+        try:
+            extra["batched_w4a16"] = batched_measure(device, args.steps, args.warmup, world, l2, hbm, bf16_peak)
+        except Exception as exc:
+            extra["batched_w4a16"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
+
     if not args.skip_dit:
         try:
+            extra["dit_chain_w4a8_m1024"] = chain_measure(device, args.steps, args.warmup, world, bf16_peak)
+        except Exception as exc:
+            extra["dit_chain_w4a8_m1024"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
+        try:
             per, tops = dit_measure(device)
-            bf16_peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
             g = tops["gemm_tiled_weights"]
             extra["dit_w8a8_m4032"] = {
                 "value": round(tops["tiled_weights"], 2), "unit": "TOPS",

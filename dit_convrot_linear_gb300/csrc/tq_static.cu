@@ -13,8 +13,13 @@
 // library holds TQ_STATIC_SCRATCH_BYTES for it until the process exits.  In host
 // code its name is only a host-side stand-in, so its device address is looked
 // up with cudaGetSymbolAddress, once per device, on the first call made with
-// that device current, and then passed to the kernels.  Nothing here calls
-// cudaMalloc, cudaFree or any allocating routine.
+// that device current, and then passed to the kernels.  The lookup is tied to
+// the CUDA context it was made in: if that context is destroyed and another
+// one created for the device (cudaDeviceReset, for example), the module is
+// loaded anew at another address, so the next call repeats the lookup.
+// Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+
+#include <cuda.h>
 
 #include <mutex>
 
@@ -25,19 +30,56 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_static_scratch[TQ_STATIC_SCRATCH_BYTES];
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Process-unique identity of the context current on this thread (context ids
+// are never reused), or 0 when there is none or it cannot be read.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *a = nullptr, *b = nullptr;
+        cudaDriverEntryPointQueryResult qa{}, qb{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) ==
+                    cudaSuccess && qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+            get_id = reinterpret_cast<CtxGetIdFn>(b);
+        }
+        cudaGetLastError();
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+struct ScratchSlot {
+    void *ptr = nullptr;          // device address of g_static_scratch
+    unsigned long long ctx = 0;   // context it was looked up in
+};
+
 std::mutex g_static_mu;
-void *g_static_ptr[64] = {};  // device address of g_static_scratch, per device
+ScratchSlot g_static_slot[64];   // per device
 
 tq_status static_scratch(int dev, void **out) {
     if (dev < 0 || dev >= 64) return TQ_ERR_DEVICE;
     std::lock_guard<std::mutex> lock(g_static_mu);
-    if (!g_static_ptr[dev]) {
+    ScratchSlot &s = g_static_slot[dev];
+    const unsigned long long ctx = current_context_id();
+    if (!s.ptr || ctx == 0 || s.ctx != ctx) {
         void *p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
         if (e != cudaSuccess || !p) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
-        g_static_ptr[dev] = p;
+        s.ptr = p;
+        // read again: the lookup may itself have made the context current
+        s.ctx = current_context_id();
     }
-    *out = g_static_ptr[dev];
+    *out = s.ptr;
     return TQ_OK;
 }
 

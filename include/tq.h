@@ -28,8 +28,11 @@
  *   - Every pointer is device memory owned by the caller (allocated, for
  *     example, by PyTorch).  The library never allocates or frees device
  *     memory and runs everything asynchronously on `stream` (0 = the legacy
- *     default stream).  Only the set-up call tq_grouped_create synchronises
- *     the host (it copies its tables into the caller's buffer).
+ *     default stream).  Two calls synchronise the host, and only they: the
+ *     set-up call tq_grouped_create (it copies its tables into the caller's
+ *     buffer) and tq_device_status (it waits for `stream` before it reads
+ *     the status word).  Every product and quantiser call returns as soon as
+ *     its launches are queued.
  *   - All checks (null pointers, shapes, strides, alignment, 64-bit size
  *     overflow, enum values) happen on the host before any launch; a refused
  *     call launches nothing and returns the status naming the reason.
@@ -82,7 +85,12 @@ typedef enum {
 /* Largest M the A16 modes accept (the skinny decode kernel). */
 #define TQ_MAX_M_A16 64
 
-/* Human-readable name of a status. Never NULL. */
+/*
+ * Human-readable name of a status, naming the refused condition (the pages
+ * refuse a size a format cannot take by name before any work starts: kvad-gpu
+ * internals, "Quantised weights on the GPU"; TensorFold PR #948, review
+ * follow-up: overflowing size products refused by name).  Never NULL.
+ */
 const char *tq_status_str(tq_status s);
 
 /* CUDA error code of the most recent TQ_ERR_CUDA on this host thread. */
@@ -168,7 +176,11 @@ tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
 
 /*
  * The A8 product on activations that are already rotated and quantised
- * (tq_rotate_quant_act): Y = sx[m] * sw[n] * acc[m][n].
+ * (tq_rotate_quant_act): Y = sx[m] * sw[n] * acc[m][n].  The int8 x int8
+ * product of the rotated operands (tensai docs, "画像生成", section "幅とメモリ":
+ * both operands rotated, so the product is unchanged; section "GPU": the
+ * device quantises each product's activations).  Splitting the rotation and
+ * the product lets one quantised input serve several products.
  *   Xq   int8 [M, K] dense, 16-byte aligned;  sx fp32 [M].
  *   ytype TQ_OUT_I32 writes acc itself (int32 [M, N], ldy as for fp32).
  */
@@ -347,6 +359,13 @@ tq_status tq_linear_blocked(const void *X, int64_t M, int64_t K, int64_t ldx, co
  * word on the current device.  Returns TQ_ERR_DEVICE_TIMEOUT if a bounded
  * device-side wait expired in any call since the last check (that call's
  * output is then invalid), TQ_ERR_CUDA on a CUDA error, else TQ_OK.
+ *
+ * The pages' runtimes report a failure as a named error the caller can act
+ * on rather than stopping (TensorFold PR #948, review follow-up: errors such
+ * as error.ScratchTooLarge returned by name).  A device-side wait cannot
+ * return to the host, so the kernels record an expired wait here instead of
+ * trapping, which keeps the CUDA context usable.  This is the one call
+ * besides tq_grouped_create that synchronises the host.
  */
 tq_status tq_device_status(cudaStream_t stream);
 
@@ -372,7 +391,8 @@ tq_status tq_device_status(cudaStream_t stream);
  *   calls are refused with TQ_ERR_WORKSPACE before any launch.
  *   Set-up: the first call on a device looks up the array's device address
  *   (with that device current); make that first call before any stream
- *   capture.
+ *   capture.  The lookup is repeated if the device's CUDA context has been
+ *   replaced since (after cudaDeviceReset, for example).
  *   Sharing: every call uses the same array and leaves its contents there.
  *   Nothing in it has to start at zero (each call writes what it reads), but
  *   calls that overlap on the GPU (for example on two streams) race on it:
