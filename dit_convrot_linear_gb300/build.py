@@ -78,5 +78,36 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(tag: str, defines, sources) -> str:
+    """A copy of the library for the library's own tests: ``sources`` (file
+    names under csrc/) recompiled with ``defines`` (NAME=VALUE strings) and
+    linked with the regular objects of the other files.  Written to
+    _build/libtq_<tag>.so; the product library is left as it is."""
+    build()
+    if not all(os.path.exists(os.path.join(OBJ_DIR, os.path.basename(x)[:-3] + ".o")) for x in _sources()):
+        build(force=True)
+    vdir = os.path.join(OBJ_DIR, tag)
+    os.makedirs(vdir, exist_ok=True)
+    flags = [f"-D{d}" for d in defines]
+    objs = []
+    for src in _sources():
+        name = os.path.basename(src)
+        if name in sources:
+            obj = os.path.join(vdir, name[:-3] + ".o")
+            cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *flags, "-c", src, "-o", obj]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"nvcc failed on {name} ({tag}):\n{r.stdout}\n{r.stderr}")
+            objs.append(obj)
+        else:
+            objs.append(os.path.join(OBJ_DIR, name[:-3] + ".o"))
+    out = os.path.join(OBJ_DIR, f"libtq_{tag}.so")
+    r = subprocess.run([nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", out, *objs],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed ({tag}):\n{r.stdout}\n{r.stderr}")
+    return out
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

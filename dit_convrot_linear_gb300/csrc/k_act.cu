@@ -7,13 +7,13 @@
 // at a finer grain than the weights (section "GPU"), here one scale per token
 // over all of K.
 //
-// Memory-bound: read 2 B and write 1 B (A8) or 2 B (A16) per element.  One
-// warp holds one 256-group (8 values a lane) through the whole butterfly in
-// registers and shuffles.  For the A8 path, rows of up to 16384 values are
-// streamed through a ring of shared-memory row buffers filled by bulk copies
-// several rows ahead (persistent CTAs), so the HBM reads of the next rows
-// overlap the transform, amax and stores of the current one; longer rows use
-// a plain one-CTA-per-row kernel that loads each group straight from global.
+// Memory-bound in principle: read 2 B and write 1 B (int8 codes) or 2 B (fp16
+// codes of the tiled operand, or the A16 bf16 operand) per element.  Rows of
+// up to 16384 values go through k_rotq: one CTA per row at a time, a warp per
+// 1024-column window, each 256-group held by 8 lanes x 32 values in registers
+// (five butterfly stages inside a lane, three across lanes), the row's amax
+// after one CTA barrier, then the codes.  Longer rows (int8 codes only) use a
+// plain one-CTA-per-row kernel with a warp per group.
 
 #include <cfloat>
 #include <type_traits>
@@ -48,20 +48,7 @@ __device__ __forceinline__ uint32_t quant4(const float *v, float s, float r) {
     return w;
 }
 
-constexpr long long kWaitLimit = 4000000000ll;  // clock cycles (about 2 s)
-constexpr unsigned int kStatusActTimeout = 8u;
-constexpr int64_t kRingMaxK = TQ_MAX_K_TILED;    // longest row the ring path takes
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
+constexpr int64_t kRingMaxK = TQ_MAX_K_TILED;    // longest row k_rotq takes
 
 // SwiGLU of one gate value g and up value u, h = silu(g) * u with
 // silu(g) = g / (1 + e^-g) (Shazeer, "GLU Variants Improve Transformer"), in
@@ -83,58 +70,6 @@ __device__ __forceinline__ uint32_t swiglu_word(uint32_t gw, uint32_t uw) {
     return f32_to_bf16_bits(h0) | (static_cast<uint32_t>(f32_to_bf16_bits(h1)) << 16);
 }
 
-// The lane's E bf16 values (E = 8, 4, 2, 1) at src as packed words; with
-// SWIGLU, those of h = bf16(silu(g) * u), g at src and u at src + up_off.
-template <bool SWIGLU>
-__device__ __forceinline__ void lane_words(const unsigned char *src, int up_off, int E, uint32_t (&w)[4]) {
-    auto load = [&](const unsigned char *a, uint32_t (&o)[4]) {
-        o[0] = o[1] = o[2] = o[3] = 0u;
-        if (E == 8) {
-            const uint4 u = *reinterpret_cast<const uint4 *>(a);
-            o[0] = u.x; o[1] = u.y; o[2] = u.z; o[3] = u.w;
-        } else if (E == 4) {
-            const uint2 u = *reinterpret_cast<const uint2 *>(a);
-            o[0] = u.x; o[1] = u.y;
-        } else if (E == 2) {
-            o[0] = *reinterpret_cast<const uint32_t *>(a);
-        } else {
-            o[0] = *reinterpret_cast<const uint16_t *>(a);
-        }
-    };
-    load(src, w);
-    if constexpr (SWIGLU) {
-        uint32_t u[4];
-        load(src + up_off, u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) w[i] = swiglu_word(w[i], u[i]);
-    }
-}
-
-// Rotate one group (width n = 32*E) read from a shared-memory row buffer:
-// v = c_n * Hs_n * x in fp32, the same butterfly and scale as the global path.
-template <bool SWIGLU>
-__device__ __forceinline__ int rotate_group_shared(const unsigned char *grp, int up_off, int n, float (&v)[8]) {
-    const int lane = threadIdx.x & 31;
-    uint32_t w[4];
-    const int E = n >> 5;
-    lane_words<SWIGLU>(grp + lane * E * 2, up_off, E, w);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __uint_as_float(w[i] << 16);
-        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-    switch (E) {
-        case 8: warp_fwht<8, float>(v); break;
-        case 4: warp_fwht<4, float>(v); break;
-        case 2: warp_fwht<2, float>(v); break;
-        default: warp_fwht<1, float>(v); break;
-    }
-    const float c = sqrtf(1.0f / static_cast<float>(n));
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = e < E ? c * v[e] : 0.0f;
-    return E;
-}
-
 __device__ __forceinline__ void store_codes(int8_t *dst, int e_per_lane, const float *vals, float s,
                                             float r) {
     const uint32_t lo = quant4(vals, s, r);
@@ -148,21 +83,6 @@ __device__ __forceinline__ void store_codes(int8_t *dst, int e_per_lane, const f
     } else {
         *reinterpret_cast<uint8_t *>(dst) = static_cast<uint8_t>(lo);
     }
-}
-
-// Unnormalised transform (Hs x, Sylvester order) of one full 256-group read
-// from a shared-memory row buffer: 8 values a lane.
-template <bool SWIGLU>
-__device__ __forceinline__ void fwht256_shared(const unsigned char *grp, int up_off, float (&v)[8]) {
-    const int lane = threadIdx.x & 31;
-    uint32_t w[4];
-    lane_words<SWIGLU>(grp + lane * 16, up_off, 8, w);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __uint_as_float(w[i] << 16);
-        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-    warp_fwht<8, float>(v);
 }
 
 // Code of one rotated value x = k * v (k a power of two, so x is exact):
@@ -221,235 +141,6 @@ __device__ __forceinline__ void put_tiled(uint16_t *At, int64_t KT, int64_t K, i
     } else {
         *dst = static_cast<uint16_t>(h[0]);
         if ((K & 63) == 32) *at(k0 + 32) = 0;
-    }
-}
-
-// Persistent CTAs (8 warps); CTA b takes rows b, b + gridDim.x, ...  Thread 0
-// keeps S rows in flight: row i of this CTA goes to buffer i % S, copied by
-// one bulk copy that completes on that buffer's barrier.  Warp w owns groups
-// w, w + 8, ...; the first GPW stay in registers between the amax pass and
-// the quantise pass, further ones are recomputed from the buffer.
-// SWIGLU: the row is h = bf16(silu(g) * u), gate rows from X (ldx) and up
-// rows from U (ldu); a buffer then holds a gate row and an up row.
-template <int GPW, bool TILED, int NT, bool SWIGLU = false>
-__global__ void __launch_bounds__(NT, NT == 128 ? 5 : 2)   // 5 CTAs of 4 warps, or 2 of 8, an SM
-k_rotate_quant_ring(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx,
-                    void *__restrict__ out, float *__restrict__ sx, int S,
-                    unsigned int *status, unsigned int *max_l1, const uint16_t *__restrict__ U,
-                    int64_t ldu) {
-    extern __shared__ __align__(128) unsigned char ring[];   // [S][2K or 4K] then S barriers
-    __shared__ float red[NT / 32];
-    __shared__ unsigned int win[16];   // a row's sum of |codes| per 1024-column window
-    __shared__ unsigned int winq[16];  // a row's sum of codes squared per 1024-column window
-    __shared__ unsigned int run_sh[2][5][32];   // warp 0's largest run sums over the rows
-    __shared__ int abort_sh;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int W = NT / 32;
-    const int64_t Gf = K / kGroup;                        // full 256-groups
-    const int tail = static_cast<int>(K % kGroup);        // 0, 32, 64 or 128
-    const int tail_warp = static_cast<int>(Gf % W);
-    const uint32_t row_bytes = static_cast<uint32_t>(K * 2);
-    const uint32_t slot_bytes = SWIGLU ? 2 * row_bytes : row_bytes;
-    const int up_off = static_cast<int>(row_bytes);   // the up row, after the gate row (SWIGLU)
-    const uint32_t ring0 = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
-    const uint32_t bar0 = ring0 + static_cast<uint32_t>(S) * slot_bytes;
-    const int64_t nrows = blockIdx.x < M ? (M - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-
-    auto issue = [&](int64_t i) {   // thread 0: row i of this CTA into buffer i % S
-        const int slot = static_cast<int>(i % S);
-        const uint32_t bar = bar0 + 8u * slot;
-        const int64_t m = blockIdx.x + i * gridDim.x;
-        const uint16_t *src = X + m * ldx;
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(slot_bytes)
-                     : "memory");
-        asm volatile(
-            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-            ::"r"(ring0 + static_cast<uint32_t>(slot) * slot_bytes), "l"(src), "r"(row_bytes), "r"(bar)
-            : "memory");
-        if constexpr (SWIGLU) {
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                ::"r"(ring0 + static_cast<uint32_t>(slot) * slot_bytes + row_bytes), "l"(U + m * ldu),
-                  "r"(row_bytes), "r"(bar)
-                : "memory");
-        }
-    };
-
-    if (threadIdx.x < 16) win[threadIdx.x] = winq[threadIdx.x] = 0;
-    if (TILED && threadIdx.x < 32)
-        for (int j = 0; j < 5; ++j) run_sh[0][j][threadIdx.x] = run_sh[1][j][threadIdx.x] = 0u;
-    if (threadIdx.x == 0) {
-        abort_sh = 0;
-        for (int i = 0; i < S; ++i)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8u * i));
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int64_t i = 0; i < nrows && i < S; ++i) issue(i);
-    }
-    __syncthreads();
-
-    int64_t i = 0;
-    for (; i < nrows; ++i) {
-        const int slot = static_cast<int>(i % S);
-        const uint32_t parity = static_cast<uint32_t>((i / S) & 1);
-        const long long t0 = clock64();
-        bool ok = true;
-        while (!mbar_try(bar0 + 8u * slot, parity)) {
-            if (abort_sh || clock64() - t0 > kWaitLimit) { ok = false; break; }
-        }
-        if (!ok) {
-            abort_sh = 1;
-            if (lane == 0) atomicOr(status, kStatusActTimeout);
-        }
-        __syncthreads();
-        if (abort_sh) break;
-        const unsigned char *buf = ring + static_cast<size_t>(slot) * slot_bytes;
-        const int64_t m = blockIdx.x + i * gridDim.x;
-
-        // Pass 1: the full 256-groups unscaled (Hs x; their factor 1/16 is a
-        // power of two, applied exactly later), the tail group scaled.
-        float v[GPW][8];
-        float amax_full = 0.0f, amax_tail = 0.0f;
-#pragma unroll
-        for (int j = 0; j < GPW; ++j) {
-            const int64_t g = warp + static_cast<int64_t>(j) * W;
-            if (g < Gf) {
-                fwht256_shared<SWIGLU>(buf + g * kGroup * 2, up_off, v[j]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) amax_full = fmaxf(amax_full, fabsf(v[j][e]));
-            }
-        }
-        for (int64_t g = warp + static_cast<int64_t>(GPW) * W; g < Gf; g += W) {
-            float t[8];
-            fwht256_shared<SWIGLU>(buf + g * kGroup * 2, up_off, t);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) amax_full = fmaxf(amax_full, fabsf(t[e]));
-        }
-        float vt[8];
-        int Et = 0;
-        if (tail && warp == tail_warp) {
-            Et = rotate_group_shared<SWIGLU>(buf + Gf * kGroup * 2, up_off, tail, vt);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) amax_tail = fmaxf(amax_tail, fabsf(vt[e]));
-        }
-        // max |c x| over the row: fl(c v) is monotone in |v|, so the largest
-        // scaled value of the full groups is (largest unscaled) / 16 exactly
-        float amax = fmaxf(amax_full * 0.0625f, amax_tail);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        if (lane == 0) red[warp] = amax;
-        __syncthreads();
-        amax = red[0];
-#pragma unroll
-        for (int w = 1; w < W; ++w) amax = fmaxf(amax, red[w]);
-
-        const float s = __fdiv_rn(amax, 127.0f);
-        const float r = recip_or_zero(s);
-        const float r16 = r * 0.0625f >= FLT_MIN ? r * 0.0625f : 0.0f;   // exact: a power of two
-        if (threadIdx.x == 0) sx[m] = s;
-        const int64_t KT = (K + 63) >> 6;
-        // with the tiled operand, also the row's sum of |codes| per 1024-column
-        // window (each at most 127 * 1024) and its sum of codes squared per
-        // window (a whole row at most 127^2 * 16384 < 2^32)
-        auto put = [&](int64_t g, int e, const float (&q)[8]) {
-            const int64_t k0 = g * kGroup + static_cast<int64_t>(lane) * e;
-            if constexpr (TILED) {
-                put_tiled(static_cast<uint16_t *>(out), KT, K, m, k0, e, q);
-                float fs = 0.0f, fq = 0.0f;      // exact: at most 8 x 127 and 8 x 127^2
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (j < e) {
-                        fs += fabsf(q[j]);
-                        fq = fmaf(q[j], q[j], fq);
-                    }
-                const unsigned int gs = __reduce_add_sync(0xffffffffu, static_cast<unsigned int>(fs));
-                const unsigned int gq = __reduce_add_sync(0xffffffffu, static_cast<unsigned int>(fq));
-                if (lane == 0) {
-                    atomicAdd(&win[g >> 2], gs);
-                    atomicAdd(&winq[g >> 2], gq);
-                }
-            } else
-                put_int8(static_cast<int8_t *>(out) + m * K + k0, e, q);
-        };
-        // Pass 2: codes.  Full groups: x = v / 16.  Tail: x = v.
-#pragma unroll
-        for (int j = 0; j < GPW; ++j) {
-            const int64_t g = warp + static_cast<int64_t>(j) * W;
-            if (g < Gf) {
-                float q[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) q[e] = code_of(v[j][e], 0.0625f, r16, s);
-                put(g, 8, q);
-            }
-        }
-        for (int64_t g = warp + static_cast<int64_t>(GPW) * W; g < Gf; g += W) {
-            float t[8], q[8];
-            fwht256_shared<SWIGLU>(buf + g * kGroup * 2, up_off, t);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) q[e] = code_of(t[e], 0.0625f, r16, s);
-            put(g, 8, q);
-        }
-        if (Et) {
-            float q[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) q[e] = code_of(vt[e], 1.0f, r, s);
-            put(Gf, Et, q);
-        }
-        // This thread's reads of the buffer are ordered before the bulk copy
-        // (async proxy) that will refill it; the barrier then makes every
-        // thread's reads, and the reads of red[], precede the refill.
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
-        if (TILED && warp == 0) {
-            // lane l holds window l (1024 columns; zero past K).  Sums over
-            // aligned runs of 2^j windows by butterfly within aligned lane
-            // groups; each lane keeps its largest over the rows in run_sh (the
-            // maximum over the lanes and CTAs is taken once, after the last row).
-            unsigned int ws = lane < 16 ? win[lane] : 0u;
-            unsigned int wq = lane < 16 ? winq[lane] : 0u;
-            if (lane < 16) win[lane] = winq[lane] = 0;
-#pragma unroll
-            for (int j = 0; j < 5; ++j) {
-                if (j > 0) {
-                    ws += __shfl_xor_sync(0xffffffffu, ws, 1 << (j - 1));
-                    wq += __shfl_xor_sync(0xffffffffu, wq, 1 << (j - 1));
-                }
-                run_sh[0][j][lane] = max(run_sh[0][j][lane], ws);
-                run_sh[1][j][lane] = max(run_sh[1][j][lane], wq);
-            }
-        }
-        if (threadIdx.x == 0 && i + S < nrows) issue(i + S);
-    }
-    // Trailer: word 1 + j the largest sum of |codes| over an aligned run of
-    // 2^j windows, word 0 over a whole row (16 windows hold the longest row);
-    // words 7 + j and 6 the same for codes squared.
-    if (TILED && warp == 0) {
-#pragma unroll
-        for (int j = 0; j < 5; ++j) {
-            unsigned int mx = run_sh[0][j][lane], mq = run_sh[1][j][lane];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                mq = max(mq, __shfl_xor_sync(0xffffffffu, mq, o));
-            }
-            if (lane == 0 && nrows > 0) {
-                atomicMax(max_l1 + 1 + j, mx);
-                atomicMax(max_l1 + 7 + j, mq);
-                if (j == 4) {
-                    atomicMax(max_l1, mx);
-                    atomicMax(max_l1 + 6, mq);
-                }
-            }
-        }
-    }
-    // After an expired wait, let the copies still in flight land (bounded)
-    // before the CTA's shared memory is released.
-    if (threadIdx.x == 0 && i < nrows) {
-        const long long t0 = clock64();
-        for (int64_t j = i; j < nrows && j < i + S; ++j) {
-            while (!mbar_try(bar0 + 8u * static_cast<uint32_t>(j % S), static_cast<uint32_t>((j / S) & 1)) &&
-                   clock64() - t0 < kWaitLimit) {
-            }
-        }
     }
 }
 
@@ -542,53 +233,397 @@ k_rotate_bf16(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx,
     }
 }
 
+// ---------------------------------------------------------------- row kernel
+// A 256-group as 8 lanes x 32 values: lane j of the group holds the four runs
+// of 8 columns 8 j + 64 i .. 8 j + 64 i + 7 (i = 0 .. 3), value 8 i + e being
+// column 8 j + 64 i + e.  Column bits 0-2 and 6-7 are then inside a lane and
+// bits 3-5 are the lane's, so five butterfly stages run inside the lane (four
+// of them on two values per instruction, f32x2) and three across the group's
+// 8 lanes: 3 shuffles a value instead of 5 with 8 values a lane, and the 8
+// lanes of a group read 128 contiguous bytes per load.  (The transform does
+// not depend on the order of its stages, only on each stage pairing the
+// columns that differ in one bit, lower one first.)
+
+__device__ __forceinline__ unsigned long long f2pack(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ void f2unpack(unsigned long long r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+
+// (a, b) <- (a + b, a - b) for two pairs at once, each sum rounded once
+__device__ __forceinline__ void bfly_x2(float &a0, float &a1, float &b0, float &b1) {
+    const unsigned long long a = f2pack(a0, a1), b = f2pack(b0, b1);
+    unsigned long long s, d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(s) : "l"(a), "l"(b));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    f2unpack(s, a0, a1);
+    f2unpack(d, b0, b1);
+}
+
+// Unnormalised transform (Hs_256 x, Sylvester order) of the group this lane's
+// 8-lane slice holds; in-lane value index bits are column bits 0-2 and 6-7.
+__device__ __forceinline__ void fwht_8x32(float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const float a = v[i], b = v[i + 1];
+        v[i] = a + b;
+        v[i + 1] = a - b;
+    }
+#pragma unroll
+    for (int h = 2; h < 32; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2)
+            if (!(i & h)) {
+                bfly_x2(v[i], v[i + 1], v[i + h], v[i + h + 1]);
+            }
+    }
+    // across the 8 lanes: the lane whose bit m is set keeps o - v, its
+    // partner v + o (one fused multiply-add by +-1: one rounding, like the add)
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+        const float sg = (lane & m) ? -1.0f : 1.0f;
+        const unsigned long long sg2 = f2pack(sg, sg);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            const float o0 = __shfl_xor_sync(0xffffffffu, v[i], m);
+            const float o1 = __shfl_xor_sync(0xffffffffu, v[i + 1], m);
+            unsigned long long r;
+            asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(sg2), "l"(f2pack(v[i], v[i + 1])), "l"(f2pack(o0, o1)));
+            f2unpack(r, v[i], v[i + 1]);
+        }
+    }
+}
+
+// 32 bf16 values from 4 raw 16-byte words (two a word, low half first); with
+// SWIGLU, h = bf16(silu(g) * u) of gate words g and up words u.
+template <bool SWIGLU>
+__device__ __forceinline__ void unpack32(const uint4 (&g)[4], const uint4 (&u)[4], float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t w[4] = {g[i].x, g[i].y, g[i].z, g[i].w};
+        if constexpr (SWIGLU) {
+            const uint32_t uw[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w[k] = swiglu_word(w[k], uw[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[8 * i + 2 * k] = __uint_as_float(w[k] << 16);
+            v[8 * i + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+    }
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// The tail group (width n = 32, 64 or 128; E = n / 32 values a lane) of a
+// row, read from global memory and rotated by c_n * Hs_n, as the 32-lane
+// butterfly of the other rotation kernels.
+template <bool SWIGLU>
+__device__ __forceinline__ int rotate_tail_global(const uint16_t *x, const uint16_t *u, int n, float (&v)[8]) {
+    const int lane = threadIdx.x & 31;
+    const int E = n >> 5;
+    uint32_t w[4] = {0u, 0u, 0u, 0u}, uw[4] = {0u, 0u, 0u, 0u};
+    auto load = [&](const uint16_t *p, uint32_t (&o)[4]) {
+        const uint16_t *a = p + lane * E;
+        if (E == 4) {
+            const uint2 t = *reinterpret_cast<const uint2 *>(a);
+            o[0] = t.x; o[1] = t.y;
+        } else if (E == 2) {
+            o[0] = *reinterpret_cast<const uint32_t *>(a);
+        } else {
+            o[0] = *a;
+        }
+    };
+    load(x, w);
+    if constexpr (SWIGLU) {
+        load(u, uw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = swiglu_word(w[i], uw[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    switch (E) {
+        case 4: warp_fwht<4, float>(v); break;
+        case 2: warp_fwht<2, float>(v); break;
+        default: warp_fwht<1, float>(v); break;
+    }
+    const float c = sqrtf(1.0f / static_cast<float>(n));
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = e < E ? c * v[e] : 0.0f;
+    return E;
+}
+
+constexpr int kRotqMaxWarps = 17;   // 64 full groups (4 a warp) and a tail warp
+
+// Rotation + per-token int8 quantisation, one token row per CTA at a time
+// (persistent over rows m = blockIdx.x, blockIdx.x + gridDim.x, ...).  Warp
+// w < WF owns the full groups 4w .. 4w + 3, which are the 1024-column window
+// w; its lanes 8s .. 8s + 7 hold group 4w + s.  A tail group (width 32, 64 or
+// 128) has a warp of its own.  Per row: the transform in registers, the
+// row's amax (one CTA barrier), the codes.  Rows in flight come from the
+// several CTAs an SM holds (measured on M = 4032, K = 12288: two CTAs an SM
+// with the loads of each row issued at its start, 79 us, against 92 us with
+// one CTA an SM that loaded the next row during the current one).
+// TILED writes the codes as fp16 in the product's operand layout and records
+// the |code| and code-squared window sums for the product's exactness bound;
+// else int8 rows.  SWIGLU: the row is h = bf16(silu(g) * u), gate rows from X
+// and up rows from U.
+
+// CTAs an SM should hold, by warps a CTA: a thread keeps about 80 registers
+constexpr int rotq_min_blocks(int maxw) {
+    return maxw <= 4 ? 6 : maxw <= 8 ? 3 : maxw <= 12 ? 2 : 1;
+}
+template <bool TILED, bool SWIGLU, int MAXW>
+__global__ void __launch_bounds__(MAXW * 32, rotq_min_blocks(MAXW))
+k_rotq(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx, void *__restrict__ out,
+       float *__restrict__ sx, unsigned int *max_l1, const uint16_t *__restrict__ U, int64_t ldu) {
+    __shared__ float red[2][kRotqMaxWarps];
+    __shared__ unsigned int win[2][16], winq[2][16];   // a row's window sums of |codes|, codes squared
+    __shared__ unsigned int run_sh[2][5][32];           // warp 0's largest run sums over the rows
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int W = blockDim.x >> 5;
+    const int64_t Gf = K / kGroup;                   // full 256-groups
+    const int tail = static_cast<int>(K % kGroup);   // 0, 32, 64 or 128
+    const int WF = static_cast<int>((Gf + 3) / 4);   // warps of full groups
+    const bool tail_warp = tail != 0 && warp == WF;
+    const int64_t g = static_cast<int64_t>(warp) * 4 + (lane >> 3);   // this lane's group
+    const bool active = !tail_warp && g < Gf;
+    const int64_t col0 = g * kGroup + (lane & 7) * 8;    // first of this lane's 4 runs of 8 columns
+    constexpr int kRun = 64;                              // column step between the runs
+    const int64_t KT = (K + 63) >> 6;
+
+    if (threadIdx.x < 32) {
+        for (int p = 0; p < 2; ++p) {
+            if (lane < 16) win[p][lane] = winq[p][lane] = 0u;
+            for (int j = 0; j < 5; ++j) run_sh[p][j][lane] = 0u;
+        }
+    }
+    __syncthreads();
+
+    uint4 raw[4], rawu[4];
+    auto load_row = [&](int64_t m) {
+        if (!active) return;
+        const uint16_t *src = X + m * ldx + col0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) raw[i] = ld_stream(src + kRun * i);
+        if constexpr (SWIGLU) {
+            const uint16_t *us = U + m * ldu + col0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) rawu[i] = ld_stream(us + kRun * i);
+        }
+    };
+    // warp 0: fold a finished row's window sums into its running maxima over
+    // aligned runs of 2^j windows (lane l holds window l; zero past K)
+    auto fold_windows = [&](int p) {
+        unsigned int ws = lane < 16 ? win[p][lane] : 0u;
+        unsigned int wq = lane < 16 ? winq[p][lane] : 0u;
+        if (lane < 16) win[p][lane] = winq[p][lane] = 0u;
+#pragma unroll
+        for (int j = 0; j < 5; ++j) {
+            if (j > 0) {
+                ws += __shfl_xor_sync(0xffffffffu, ws, 1 << (j - 1));
+                wq += __shfl_xor_sync(0xffffffffu, wq, 1 << (j - 1));
+            }
+            run_sh[0][j][lane] = max(run_sh[0][j][lane], ws);
+            run_sh[1][j][lane] = max(run_sh[1][j][lane], wq);
+        }
+    };
+
+    int64_t m = blockIdx.x;
+    int par = 0;
+    bool pending = false;   // a row's window sums wait to be folded
+    for (; m < M; m += gridDim.x, par ^= 1) {
+        float v[32];
+        load_row(m);
+        if (active) {
+            unpack32<SWIGLU>(raw, rawu, v);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+        }
+
+        // transform; the full groups stay unscaled (their factor 1/16 is a
+        // power of two, applied exactly with the codes), the tail is scaled
+        float vt[8];
+        int Et = 0;
+        float amax = 0.0f;
+        if (tail_warp) {
+            const int64_t t0 = Gf * kGroup;
+            Et = rotate_tail_global<SWIGLU>(X + m * ldx + t0, SWIGLU ? U + m * ldu + t0 : nullptr, tail, vt);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(vt[e]));
+        } else {
+            fwht_8x32(v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(v[e]));
+            amax *= 0.0625f;   // exact; fl(c v) is monotone in |v|
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) red[par][warp] = amax;
+        __syncthreads();
+        amax = red[par][0];
+        for (int w = 1; w < W; ++w) amax = fmaxf(amax, red[par][w]);
+        if (TILED && warp == 0 && pending) fold_windows(par ^ 1);
+        pending = true;
+
+        const float s = __fdiv_rn(amax, 127.0f);
+        const float r = recip_or_zero(s);
+        const float r16 = r * 0.0625f >= FLT_MIN ? r * 0.0625f : 0.0f;   // exact: a power of two
+        if (threadIdx.x == 0) sx[m] = s;
+
+        if (!tail_warp) {
+            // codes eight at a time: 16 bytes of fp16 codes (one core-matrix
+            // row of the tiled operand) or 8 bytes of int8 codes
+            float fs = 0.0f, fq = 0.0f;   // exact: at most 32 x 127 and 32 x 127^2
+            uint16_t *tdst = nullptr;
+            if constexpr (TILED) {
+                const int64_t mt = m >> 7;
+                const int rr = static_cast<int>(m & 127);
+                tdst = static_cast<uint16_t *>(out) + ((mt * KT + (col0 >> 6)) << 13) +
+                       ((((rr >> 3) << 3) + static_cast<int>((col0 & 63) >> 3)) << 6) + ((rr & 7) << 3);
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float q[8];
+                // rint of the product; where it may differ from rint of the
+                // correctly rounded quotient (near a half-integer, or no
+                // reciprocal), the warp takes the division for those values
+                bool amb = r16 == 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float t = v[8 * c + e] * r16;
+                    q[e] = rintf(t);
+                    amb = amb || fabsf(t - q[e]) > 0.499f;
+                }
+                if (__any_sync(0xffffffffu, amb) && amb) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) q[e] = code_of(v[8 * c + e], 0.0625f, r16, s);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    fs += fabsf(q[e]);
+                    fq = fmaf(q[e], q[e], fq);
+                }
+                if (!active) continue;
+                if constexpr (TILED) {
+                    uint32_t h[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const __half2 p2 = __floats2half2_rn(q[2 * i], q[2 * i + 1]);
+                        h[i] = *reinterpret_cast<const uint32_t *>(&p2);
+                    }
+                    *reinterpret_cast<uint4 *>(tdst + (c << 13)) = make_uint4(h[0], h[1], h[2], h[3]);
+                } else {
+                    uint32_t wv[2] = {0u, 0u};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        wv[e >> 2] |= (static_cast<uint32_t>(__float2int_rz(q[e])) & 0xFFu) << (8 * (e & 3));
+                    *reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + m * K + col0 + kRun * c) =
+                        make_uint2(wv[0], wv[1]);
+                }
+            }
+            if constexpr (TILED) {
+                const unsigned int gs = __reduce_add_sync(0xffffffffu, static_cast<unsigned int>(fs));
+                const unsigned int gq = __reduce_add_sync(0xffffffffu, static_cast<unsigned int>(fq));
+                if (lane == 0 && warp < WF) {
+                    atomicAdd(&win[par][warp], gs);
+                    atomicAdd(&winq[par][warp], gq);
+                }
+            }
+        } else {
+            float q[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[e] = code_of(vt[e], 1.0f, r, s);
+            const int64_t k0 = Gf * kGroup + static_cast<int64_t>(lane) * Et;
+            if constexpr (TILED) {
+                put_tiled(static_cast<uint16_t *>(out), KT, K, m, k0, Et, q);
+                float fs = 0.0f, fq = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (e < Et) {
+                        fs += fabsf(q[e]);
+                        fq = fmaf(q[e], q[e], fq);
+                    }
+                const unsigned int gs = __reduce_add_sync(0xffffffffu, static_cast<unsigned int>(fs));
+                const unsigned int gq = __reduce_add_sync(0xffffffffu, static_cast<unsigned int>(fq));
+                if (lane == 0) {
+                    atomicAdd(&win[par][Gf >> 2], gs);
+                    atomicAdd(&winq[par][Gf >> 2], gq);
+                }
+            } else {
+                put_int8(static_cast<int8_t *>(out) + m * K + k0, Et, q);
+            }
+        }
+    }
+    if constexpr (TILED) {
+        __syncthreads();
+        if (warp == 0) {
+            if (pending) fold_windows(par ^ 1);
+            // Trailer: word 1 + j the largest sum of |codes| over an aligned
+            // run of 2^j windows, word 0 over a whole row (16 windows hold the
+            // longest row); words 7 + j and 6 the same for codes squared.
+#pragma unroll
+            for (int j = 0; j < 5; ++j) {
+                unsigned int mx = run_sh[0][j][lane], mq = run_sh[1][j][lane];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    mq = max(mq, __shfl_xor_sync(0xffffffffu, mq, o));
+                }
+                if (lane == 0 && pending) {
+                    atomicMax(max_l1 + 1 + j, mx);
+                    atomicMax(max_l1 + 7 + j, mq);
+                    if (j == 4) {
+                        atomicMax(max_l1, mx);
+                        atomicMax(max_l1 + 6, mq);
+                    }
+                }
+            }
+        }
+    }
+}
+
 template <bool TILED, bool SWIGLU = false>
-tq_status launch_ring(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void *out, float *sx,
+tq_status launch_rotq(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void *out, float *sx,
                       unsigned int *max_l1, cudaStream_t s, const uint16_t *U = nullptr, int64_t ldu = 0) {
-    const int64_t G = (K + kGroup - 1) / kGroup;
-    // rows of up to 16 groups: CTAs of 4 warps, more of them, so that more
-    // rows are in flight per SM; longer rows: 8 warps
-    const bool small = G <= 16;
-    const int NT = small ? 128 : 256;
-    const int64_t gpw = (G + NT / 32 - 1) / (NT / 32);
+    const int64_t Gf = K / kGroup;
+    const int warps = static_cast<int>((Gf + 3) / 4) + (K % kGroup ? 1 : 0);
+    if (warps < 1 || warps > kRotqMaxWarps) return TQ_ERR_SHAPE;
+    const int NT = warps * 32;
     DeviceInfo dev;
     const tq_status ds = current_device(&dev);
     if (ds != TQ_OK) return ds;
-    unsigned int *status = status_word();
-    if (!status) return TQ_ERR_DEVICE;
-    // rows in flight per CTA: about 48 KB of them (24 KB with 4 warps), 2 to 8 rows
-    // (a gate and an up row per buffer with SWIGLU)
-    const int64_t rb = (SWIGLU ? 4 : 2) * K;
-    int S = static_cast<int>(((small ? 24 : 48) * 1024) / rb);
-    S = S < 2 ? 2 : (S > 8 ? 8 : S);
-    const size_t smem = static_cast<size_t>(S) * rb + 8 * S;
-    auto pick = [&](auto nt) {
-        constexpr int N = decltype(nt)::value;
-        return gpw <= 1 ? k_rotate_quant_ring<1, TILED, N, SWIGLU>
-             : gpw <= 2 ? k_rotate_quant_ring<2, TILED, N, SWIGLU>
-             : gpw <= 4 ? k_rotate_quant_ring<4, TILED, N, SWIGLU>
-                        : k_rotate_quant_ring<8, TILED, N, SWIGLU>;
-    };
-    auto kern = small ? pick(std::integral_constant<int, 128>{}) : pick(std::integral_constant<int, 256>{});
-    const int ki = (gpw <= 1 ? 0 : gpw <= 2 ? 1 : gpw <= 4 ? 2 : 3) + (small ? 4 : 0);
-    static bool configured[64][8] = {{false}};
-    if (dev.id < 0 || dev.id >= 64) return TQ_ERR_DEVICE;
-    if (!configured[dev.id][ki]) {
-        // the largest ring: two of the longest rows (gate and up rows with SWIGLU)
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(kRingMaxK * (SWIGLU ? 4 : 2) * 2 + 64));
-        if (e != cudaSuccess) return cuda_fail(e);
-        configured[dev.id][ki] = true;
-    }
-    // persistent: as many CTAs as are resident at once, at most 4 (8 with 4 warps) per SM
+    // up to 16 warps (every row of at most 16384 columns but those of 63 full
+    // groups and a tail) with the register budget of 512 threads
+    auto kern = warps <= 4    ? k_rotq<TILED, SWIGLU, 4>
+                : warps <= 8  ? k_rotq<TILED, SWIGLU, 8>
+                : warps <= 12 ? k_rotq<TILED, SWIGLU, 12>
+                : warps <= 16 ? k_rotq<TILED, SWIGLU, 16>
+                              : k_rotq<TILED, SWIGLU, kRotqMaxWarps>;
+    // persistent: as many CTAs as are resident at once
     int per_sm = 0;
-    const cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem);
+    const cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, 0);
     if (oe != cudaSuccess) return cuda_fail(oe);
-    const int cap = small ? 8 : 4;
-    per_sm = per_sm < 1 ? 1 : (per_sm > cap ? cap : per_sm);
+    per_sm = per_sm < 1 ? 1 : per_sm;
     const int64_t want = static_cast<int64_t>(dev.sms) * per_sm;
     const unsigned grid = static_cast<unsigned>(M < want ? M : want);
-    kern<<<grid, NT, smem, s>>>(X, M, K, ldx, out, sx, S, status, max_l1, U, ldu);
+    kern<<<grid, NT, 0, s>>>(X, M, K, ldx, out, sx, max_l1, U, ldu);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
@@ -609,7 +644,7 @@ tq_status launch_rotate_quant_tiled(const uint16_t *X, int64_t M, int64_t K, int
                                                             tiled_act_tiles_bytes(M, K));
     const cudaError_t e = cudaMemsetAsync(max_l1, 0, 12 * sizeof(unsigned int), s);
     if (e != cudaSuccess) return cuda_fail(e);
-    return launch_ring<true>(X, M, K, ldx, At, sx, max_l1, s);
+    return launch_rotq<true>(X, M, K, ldx, At, sx, max_l1, s);
 }
 
 tq_status launch_swiglu_quant_tiled(const uint16_t *G, int64_t ldg, const uint16_t *U, int64_t ldu,
@@ -620,7 +655,7 @@ tq_status launch_swiglu_quant_tiled(const uint16_t *G, int64_t ldg, const uint16
                                                             tiled_act_tiles_bytes(M, K));
     const cudaError_t e = cudaMemsetAsync(max_l1, 0, 12 * sizeof(unsigned int), s);
     if (e != cudaSuccess) return cuda_fail(e);
-    return launch_ring<true, true>(G, M, K, ldg, At, sx, max_l1, s, U, ldu);
+    return launch_rotq<true, true>(G, M, K, ldg, At, sx, max_l1, s, U, ldu);
 }
 
 tq_status launch_rotate_quant_act(const uint16_t *X, int64_t M, int64_t K,
@@ -629,7 +664,7 @@ tq_status launch_rotate_quant_act(const uint16_t *X, int64_t M, int64_t K,
     const int64_t G = (K + kGroup - 1) / kGroup;
     const int64_t gpw = (G + 7) / 8;
     if (M == 0) return TQ_OK;
-    if (K <= kRingMaxK) return launch_ring<false>(X, M, K, ldx, Xq, sx, nullptr, s);
+    if (K <= kRingMaxK) return launch_rotq<false>(X, M, K, ldx, Xq, sx, nullptr, s);
     const unsigned grid = static_cast<unsigned>(M < (1ll << 30) ? M : (1ll << 30));
     if (gpw <= 1) k_rotate_quant_act<1><<<grid, kThreads, 0, s>>>(X, M, K, ldx, Xq, sx);
     else if (gpw <= 2) k_rotate_quant_act<2><<<grid, kThreads, 0, s>>>(X, M, K, ldx, Xq, sx);

@@ -35,9 +35,7 @@
 // status word, stops issuing work, lets in-flight MMAs finish (bounded), frees
 // its TMEM and returns.
 
-#include <cuda.h>
-
-#include "tq_internal.cuh"
+#include "tq_tc.cuh"
 
 namespace tq {
 namespace {
@@ -124,7 +122,73 @@ struct TcParams {
     int epi;                   // any of bias, gate, R given
     int vcols;                 // sw, bias, gate all 16-byte aligned (float4 loads)
     int vres;                  // R rows 16-byte aligned (16-byte loads)
+    // Split tiles (stream-K).  Tiles [0, sk_dp_tiles) are computed whole,
+    // tile = pair + i * pairs.  The K steps of the other tiles, sk_units in
+    // all (tile-major, K fastest), are cut into one contiguous run per pair;
+    // a pair takes its run from the top down.  A tile whose K steps fall to
+    // several pairs is finished by the pair that holds its last K step: the
+    // others store their exact int32 partial sums in their slot and raise
+    // one flag per drain warp; the finisher waits for those flags, adds the
+    // partials, writes Y and lowers the flags again.  sk_units == 0: every
+    // tile is whole.
+    int sk_dp_tiles;
+    long long sk_units;
+    unsigned int *sk_flags;    // [pairs][2 CTAs][kDrainWarps]
+    int *sk_slots;             // [pairs][2 CTAs][128 rows][256 columns]
 };
+
+constexpr int kDrainWarps = 12;   // flags per CTA: the drain warps of the epilogue path
+constexpr int kSlotInts = HM * BN;  // one CTA's partial tile
+
+// The pieces of work of one pair, in order: whole tiles first, then the pieces
+// of its run of split K steps from the top down.  kind 0: a whole tile; 1: a
+// piece that does not hold the tile's last K step (stored as a partial); 2: a
+// piece that does, with earlier pieces held by pairs first .. pair - 1.
+struct Seg {
+    int tile, k0, k1, kind, first;
+};
+
+// Pair owning K step x of the split run: the largest q with u0(q) <= x.
+__device__ __forceinline__ int sk_owner(long long x, long long units, int pairs) {
+    int q = static_cast<int>((x * pairs) / units);
+    while (q + 1 < pairs && units * (q + 1) / pairs <= x) ++q;
+    while (q > 0 && units * q / pairs > x) --q;
+    return q;
+}
+
+struct SegIter {
+    int pair, pairs, ksteps, dp_tiles, ntiles, i;
+    long long units, u0, u;
+    __device__ SegIter(const TcParams &p, int pair_, int pairs_)
+        : pair(pair_), pairs(pairs_), ksteps(p.ksteps), dp_tiles(p.sk_units ? p.sk_dp_tiles : p.mtiles * p.ntiles),
+          ntiles(p.mtiles * p.ntiles), i(0), units(p.sk_units) {
+        u0 = units ? units * pair / pairs : 0;
+        u = units ? units * (pair + 1) / pairs : 0;
+    }
+    __device__ bool next(Seg &s) {
+        const int t = pair + i * pairs;
+        if (t < dp_tiles) {
+            s.tile = t; s.k0 = 0; s.k1 = ksteps; s.kind = 0; s.first = 0;
+            ++i;
+            return true;
+        }
+        if (u <= u0) return false;
+        const long long tl = (u - 1) / ksteps, ts = tl * ksteps;
+        s.tile = dp_tiles + static_cast<int>(tl);
+        s.k0 = static_cast<int>((u0 > ts ? u0 : ts) - ts);
+        s.k1 = static_cast<int>(u - ts);
+        s.kind = (s.k0 == 0 && s.k1 == ksteps) ? 0 : (s.k1 < ksteps ? 1 : 2);
+        s.first = s.kind == 2 ? sk_owner(ts, units, pairs) : 0;
+        u = ts + s.k0;
+        return true;
+    }
+};
+
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 
 // Tile order: bands of BAND N-tiles (BAND 0: one band of all); inside a band
 // N fastest, then M.  The tiles in flight at once (one per CTA pair) then
@@ -152,17 +216,6 @@ __device__ __forceinline__ int tile_n(int tile, const TcParams &p) {
     }
 }
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// byte offset of (row r, k) in a [rows x 64] fp16 tile of 8x8 core matrices:
-// core matrix (r/8, k/8) is 128 contiguous bytes, K-adjacent ones 128 bytes
-// apart (leading offset), row groups 1024 bytes apart (stride offset)
-__device__ __forceinline__ int cm_off(int r, int k) {
-    return ((r >> 3) * 8 + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2;
-}
-
 // Converter thread (tid < TPG within its group) -> (row, 16-byte segment) of
 // a 128-row tile for pass j.  Each run of 8 consecutive lanes (one shared-store
 // phase) takes 8 consecutive rows of one segment, so its 16-byte stores fill
@@ -179,23 +232,6 @@ __device__ __forceinline__ void rows32(int tid, int j, int &r, int &seg) {
     const int lane = tid & 31, grp = (TPG * j + tid) >> 5;
     r = grp * 16 + ((lane >> 4) << 3) + (lane & 7);
     seg = (lane >> 3) & 1;
-}
-
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
-    constexpr uint64_t lbo = 128, sbo = 1024;
-    return static_cast<uint64_t>((addr & 0x3FFFF) >> 4) | ((lbo >> 4) << 16) | ((sbo >> 4) << 32) |
-           (1ull << 46);
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
 }
 
 // Bounded wait; on expiry raises the CTA abort flag and the status word.
@@ -226,113 +262,6 @@ __device__ __forceinline__ void commit_pair(uint32_t bar) {
         ::"r"(bar), "h"(static_cast<uint16_t>(3)) : "memory");
 }
 
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
-// four int8 codes -> fp16 pairs (k0,k1), (k2,k3): 0x64xx is 1024 + xx, and
-// xx = code + 128 after flipping the sign bit; subtract 1152.
-__device__ __forceinline__ void widen8(uint32_t w, uint32_t &p01, uint32_t &p23) {
-    const uint32_t u = w ^ 0x80808080u;
-    p01 = hsub2(prmt(u, 0x64646464u, 0x4140u), 0x64806480u);
-    p23 = hsub2(prmt(u, 0x64646464u, 0x4342u), 0x64806480u);
-}
-
-// eight int4 codes (low nibble first) -> fp16 pairs (k0,k1) .. (k6,k7).  With
-// u = code + 8: the low half is 0x6400 | u = 1024 + u, the high half
-// 0x6400 | (u << 4) = 1024 + 16u; one fma with (1, 1/16) and (-1032, -72).
-__device__ __forceinline__ void widen4(uint32_t w, uint32_t (&p)[4]) {
-    const uint32_t u = w ^ 0x88888888u;
-    const uint32_t scale = 0x2C003C00u;   // (1/16, 1.0)
-    const uint32_t bias = 0xD480E408u;    // (-72, -1032)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t t = prmt(u, 0u, 0x4040u + 0x0101u * i);  // byte i in both halves
-        p[i] = hfma2((t & 0x00F0000Fu) | 0x64006400u, scale, bias);
-    }
-}
-
-__device__ __forceinline__ void store_i8x16(unsigned char *tile, int r, int seg, const uint4 &w) {
-    uint4 lo, hi;
-    widen8(w.x, lo.x, lo.y);
-    widen8(w.y, lo.z, lo.w);
-    widen8(w.z, hi.x, hi.y);
-    widen8(w.w, hi.z, hi.w);
-    *reinterpret_cast<uint4 *>(tile + cm_off(r, seg * 16)) = lo;
-    *reinterpret_cast<uint4 *>(tile + cm_off(r, seg * 16 + 8)) = hi;
-}
-
-__device__ __forceinline__ void store_i4x32(unsigned char *tile, int r, int seg, const uint4 &w) {
-    const uint32_t v[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t pr[4];
-        widen4(v[q], pr);
-        *reinterpret_cast<uint4 *>(tile + cm_off(r, seg * 32 + q * 8)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-    }
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
-          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
-          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
-          "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
-          "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]),
-          "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
-          "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
-}
-
-
-// byte offset of the 16-byte chunk c of row r in a TMA tile with 64-byte rows
-// and 64-byte swizzle (chunk index XOR address bits 7-8), or with 32-byte rows
-// and 32-byte swizzle (chunk bit XOR address bit 7)
-__device__ __forceinline__ int swz64(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
-__device__ __forceinline__ int swz32(int r, int c) { return r * 32 + ((c ^ ((r >> 2) & 1)) << 4); }
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-
 // A tensor copy of this CTA's half of a pair operand, completing on a barrier
 // that may sit in the peer CTA (here the even CTA's stage barrier).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -342,10 +271,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "[%0], [%1, {%2, %3}], [%4];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
         : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 template <int BITS, int MODE, bool EPI = false>
@@ -412,7 +337,6 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tmem_base_sh;
 
-    const int ntiles_total = p.mtiles * p.ntiles;
     // One fp32 accumulation per tile is exact when no partial sum can reach
     // 2^24: K within one chunk, or the tiled operand's largest row sum of
     // |codes| times the largest weight code, since any partial sum of
@@ -458,7 +382,14 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         uint32_t ch = 0, tl = 0;
         const bool y16 = (reinterpret_cast<uintptr_t>(p.Y) & 15) == 0;
         const bool vec_ok = y16 && (p.ytype == 1 ? (p.ldy & 7) == 0 : (p.ldy & 3) == 0);
-        for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters, ++tl) {
+        // this warp's flag (one per drain warp; the same warp index drains the
+        // same rows and columns in every CTA of the same rank)
+        const int dw = warp < NCONV ? warp : NCONV + (warp - MMA_WARP - 1);
+        const int prow = q * 32 + lane;               // this thread's row of the partial tile
+        SegIter sit(p, cluster_id, nclusters);
+        Seg sg;
+        for (; !abort_sh && sit.next(sg); ++tl) {
+            const int tile = sg.tile;
             const int64_t m0 = static_cast<int64_t>(tile_m<P::BAND>(tile, p)) * 2 * HM + rank * HM;
             const int64_t n0 = static_cast<int64_t>(tile_n<P::BAND>(tile, p)) * BN;
             const int64_t m = m0 + q * 32 + lane;
@@ -611,11 +542,80 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 }
                 }
             };
+            // A split tile: a piece without the last K step stores its exact
+            // partial sums in this pair's slot; the piece with it first waits
+            // until the earlier pieces' partials are stored (this warp's part
+            // of them), then adds them before Y is written.
+            // a partial tile in a slot: 16-byte chunk j of the 32-column block
+            // col / 32 of row r at int4 index ((col / 32) * 8 + j) * 128 + r, so
+            // the 32 lanes of a warp store or load 512 contiguous bytes
+            int *my_slot = sg.kind == 1
+                               ? p.sk_slots + (static_cast<int64_t>(cluster_id) * 2 + rank) * kSlotInts + prow * 4
+                               : nullptr;
+            auto wait_partials = [&]() -> bool {
+                for (int c = sg.first; c < cluster_id; ++c) {
+                    const unsigned int *f = p.sk_flags + (c * 2 + static_cast<int>(rank)) * kDrainWarps + dw;
+                    const long long t0 = clock64();
+                    while (ld_acquire(f) == 0u) {
+                        if (abort_sh) return false;
+                        if (clock64() - t0 > kWaitLimit) {
+                            abort_sh = 1;
+                            atomicOr(p.status, kStatusGemmTimeout);
+                            return false;
+                        }
+                    }
+                }
+                return true;
+            };
+            auto finish = [&](int col, uint32_t (&r)[32]) {
+                if (sg.kind == 1) {
+                    int4 *d = reinterpret_cast<int4 *>(my_slot) + (col >> 5) * 8 * HM;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        d[j * HM] = make_int4(static_cast<int>(r[4 * j]), static_cast<int>(r[4 * j + 1]),
+                                              static_cast<int>(r[4 * j + 2]), static_cast<int>(r[4 * j + 3]));
+                    return;
+                }
+                if (sg.kind == 2) {
+                    for (int c = sg.first; c < cluster_id; ++c) {
+                        const int4 *src = reinterpret_cast<const int4 *>(
+                                              p.sk_slots + (static_cast<int64_t>(c) * 2 + rank) * kSlotInts + prow * 4) +
+                                          (col >> 5) * 8 * HM;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int4 v = __ldcg(src + j * HM);
+                            r[4 * j] += static_cast<uint32_t>(v.x);
+                            r[4 * j + 1] += static_cast<uint32_t>(v.y);
+                            r[4 * j + 2] += static_cast<uint32_t>(v.z);
+                            r[4 * j + 3] += static_cast<uint32_t>(v.w);
+                        }
+                    }
+                }
+                y_block(col, r);
+            };
+            // after a piece: raise this warp's flag (stored partial) or lower
+            // the flags it consumed, ready for the next launch
+            auto settle = [&]() {
+                if (sg.kind == 1) {
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) {
+                        unsigned int *f = p.sk_flags + (cluster_id * 2 + static_cast<int>(rank)) * kDrainWarps + dw;
+                        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
+                    }
+                } else if (sg.kind == 2) {
+                    __syncwarp();
+                    if (lane == 0)
+                        for (int c = sg.first; c < cluster_id; ++c)
+                            p.sk_flags[(c * 2 + static_cast<int>(rank)) * kDrainWarps + dw] = 0u;
+                }
+            };
             if (single) {
-                // the tile's one chunk: fp32 sums, exact integers, straight to Y
+                // the piece's one chunk: fp32 sums, exact integers
                 const uint32_t buf = tl & 1;
                 if (!mbar_wait(acc_full0 + 8 * buf, (tl >> 1) & 1, &abort_sh, p.status)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (sg.kind == 2 && !wait_partials()) break;
                 for (int col = 32 * slot; col < BN; col += 32 * nslots) {
                     uint32_t v[32];
                     tmem_ld32(tmem + lane_base + 256u * buf + col, v);
@@ -623,15 +623,20 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         v[j] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[j])));
-                    y_block(col, v);
+                    finish(col, v);
                 }
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) mbar_arrive_leader(acc_empty0 + 8 * buf);
+                settle();
                 continue;
             }
-            for (int c0 = 0; c0 < p.ksteps; c0 += cs, ++ch) {
-                const bool first = c0 == 0;
+            // chunks end at multiples of cs K steps (counted from K step 0,
+            // so each lies inside one aligned window of the exactness bound)
+            for (int c0 = sg.k0; c0 < sg.k1; ++ch) {
+                const int c1 = min((c0 / cs + 1) * cs, sg.k1);
+                const bool first = c0 == sg.k0;
+                c0 = c1;
                 if (!mbar_wait(acc_full0, ch & 1, &abort_sh, p.status)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 for (int col = 32 * slot; col < BN; col += 32 * nslots) {
@@ -652,13 +657,15 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 if (lane == 0) mbar_arrive_leader(acc_empty0);
             }
             if (abort_sh) break;
-            // the tile's exact int32 sums are in the running region: write Y
+            // the piece's exact int32 sums are in the running region
+            if (sg.kind == 2 && !wait_partials()) break;
             for (int col = 32 * slot; col < BN; col += 32 * nslots) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_base + RUN_COL + col, r);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                y_block(col, r);
+                finish(col, r);
             }
+            settle();
         }
         };
 
@@ -666,10 +673,13 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         // ------------------------------------------------ TMA producer
         if (!BT && lane == 0) {
             uint32_t it = 0;
-            for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
+            SegIter sit(p, cluster_id, nclusters);
+            Seg sg;
+            while (!abort_sh && sit.next(sg)) {
+                const int tile = sg.tile;
                 const int m0 = tile_m<P::BAND>(tile, p) * 2 * HM + static_cast<int>(rank) * HM;
                 const int n0 = tile_n<P::BAND>(tile, p) * BN + static_cast<int>(rank) * HN;
-                for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
+                for (int ks = sg.k0; ks < sg.k1; ++ks, ++it) {
                     const int s = it % (BT ? 1 : RSTAGES);
                     if (!mbar_wait(raw_empty0 + 8 * s, ((it / (BT ? 1 : RSTAGES)) & 1) ^ 1, &abort_sh, p.status)) break;
                     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
@@ -689,10 +699,13 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             // (all four tiles) the even CTA posts.
             if (lane == 0) {
                 uint32_t it = 0;
-                for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
+                SegIter sit(p, cluster_id, nclusters);
+                Seg sg;
+                while (!abort_sh && sit.next(sg)) {
+                    const int tile = sg.tile;
                     const int mt = tile_m<P::BAND>(tile, p) * 2 + static_cast<int>(rank);
                     const int nt = tile_n<P::BAND>(tile, p) * 2 + static_cast<int>(rank);
-                    for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
+                    for (int ks = sg.k0; ks < sg.k1; ++ks, ++it) {
                         const int s = it % OSTAGES;
                         if (!mbar_wait(op_empty0 + 8 * s, ((it / OSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
                         if (rank == 0)
@@ -714,9 +727,11 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         // with the stage's previous use.
         if (lane == 0) {
             uint32_t it = 0;
-            for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
-                const int64_t mt = static_cast<int64_t>(tile_m<P::BAND>(tile, p)) * 2 + rank;
-                for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
+            SegIter sit(p, cluster_id, nclusters);
+            Seg sg;
+            while (!abort_sh && sit.next(sg)) {
+                const int64_t mt = static_cast<int64_t>(tile_m<P::BAND>(sg.tile, p)) * 2 + rank;
+                for (int ks = sg.k0; ks < sg.k1; ++ks, ++it) {
                     const int s = it % OSTAGES;
                     if (!mbar_wait(op_empty0 + 8 * s, ((it / OSTAGES) & 1) ^ 1, &abort_sh, p.status)) break;
                     const unsigned char *src = p.At + (mt * p.ksteps + ks) * static_cast<int64_t>(A_OP);
@@ -743,8 +758,10 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         constexpr int NA = 512 / TPG;                          // A passes (and int8 B passes)
         constexpr int NB = BITS == 8 ? 512 / TPG : 256 / TPG;  // B passes
         uint32_t it = 0;
-        for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters) {
-            for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
+        SegIter sit(p, cluster_id, nclusters);
+        Seg sg;
+        while (!abort_sh && sit.next(sg)) {
+            for (int ks = sg.k0; ks < sg.k1; ++ks, ++it) {
                 if (static_cast<int>(it % CONV_GROUPS) != g) continue;
                 const int rs = it % RSTAGES, os = it % OSTAGES;
                 // stage first: see the ring plan for why the order matters
@@ -821,13 +838,15 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         if (rank == 0 && lane == 0) {
             uint32_t it = 0, ch = 0, tl = 0;
             bool issued = false;
-            for (int tile = cluster_id; tile < ntiles_total && !abort_sh; tile += nclusters, ++tl) {
-                // single: one chunk per tile into accumulator tl & 1;
-                // else: chunks into accumulator 0, each drained before the next
+            SegIter sit(p, cluster_id, nclusters);
+            Seg sg;
+            for (; !abort_sh && sit.next(sg); ++tl) {
+                // single: one chunk per piece into accumulator tl & 1;
+                // else: chunks into accumulator 0, each drained before the next,
+                // ending at multiples of cs K steps
                 const uint32_t buf = single ? (tl & 1) : 0;
-                const int cstep = single ? p.ksteps : cs;
-                for (int c0 = 0; c0 < p.ksteps && !abort_sh; c0 += cstep) {
-                    const int c1 = min(c0 + cstep, p.ksteps);
+                for (int c0 = sg.k0, c1 = 0; c0 < sg.k1 && !abort_sh; c0 = c1) {
+                    c1 = single ? sg.k1 : min((c0 / cs + 1) * cs, sg.k1);
                     const uint32_t use = single ? (tl >> 1) : ch;   // earlier uses of this accumulator
                     if (use > 0 && !mbar_wait(acc_empty0 + 8 * buf, (use - 1) & 1, &abort_sh, p.status)) break;
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -880,11 +899,20 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
 // Shared launch of the operand paths (MODE as in Plan): Xq int8 codes (A
 // through a tensor map), At pre-tiled fp16 codes, or At and Wt both pre-tiled
 // (each read as rows of 128 bytes, one 16 KB tile a box).
+// Split tiles (when the caller gives a split workspace) only where it was
+// measured to pay: fewer tiles than CTA pairs (one partial wave) and a long K.
+// Each piece costs a pipeline start, a drain and, for a partial, 128 KB stored
+// or added per CTA, so short K and full waves lose: measured on 4-bit weights
+// at M = 1024, 48 tiles, K = 12288: 70.9 -> 61.6 us; K = 3072: 29.9 -> 31.9 us;
+// 384 tiles (five waves and four tiles), K = 3072: 106.3 -> 107.8 us.
+constexpr double kSplitBelow = 0.85;
+constexpr int kSplitMinKSteps = 96;
+
 template <int MODE>
 tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const unsigned char *Wt, const float *sx,
                     int64_t M, int64_t K, const uint8_t *Wq, const float *sw, int64_t N, int bits, void *Y,
                     int ytype, int64_t ldy, const DeviceInfo &dev, cudaStream_t s,
-                    const EpilogueArgs *ea = nullptr) {
+                    const EpilogueArgs *ea = nullptr, void *split_ws = nullptr) {
     using P = Plan<MODE>;
     constexpr bool AT = P::AT;
     unsigned int *status = status_word();
@@ -952,7 +980,28 @@ tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const unsigned ch
         if (e != cudaSuccess) return cuda_fail(e);
         configured_for[dev.id][bi] = true;
     }
-    const int64_t pairs = tiles < dev.sms / 2 ? tiles : dev.sms / 2;
+    const int64_t pmax = dev.sms / 2;
+    int64_t pairs = tiles < pmax ? tiles : pmax;
+    p.sk_dp_tiles = 0;
+    p.sk_units = 0;
+    p.sk_flags = nullptr;
+    p.sk_slots = nullptr;
+    if (split_ws && pmax > 0) {
+        // One partial wave: the K steps of all tiles are split evenly over
+        // every pair (at least two K steps a pair).
+        if (tiles < pmax && p.ksteps >= kSplitMinKSteps &&
+            static_cast<double>(tiles) < kSplitBelow * static_cast<double>(pmax)) {
+            const int64_t dp = 0;
+            const int64_t units = tiles * p.ksteps;
+            if (units >= 2 * pmax) {
+                p.sk_dp_tiles = static_cast<int>(dp);
+                p.sk_units = units;
+                p.sk_flags = static_cast<unsigned int *>(split_ws);
+                p.sk_slots = reinterpret_cast<int *>(static_cast<unsigned char *>(split_ws) + split_flag_bytes(dev));
+                pairs = pmax;
+            }
+        }
+    }
     kern<<<static_cast<unsigned>(2 * pairs), P::THREADS, P::SMEM_BYTES, s>>>(tmA, tmB, p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
@@ -977,9 +1026,19 @@ tq_status launch_gemm_a8_tiled(const void *At, const float *sx, int64_t M, int64
 
 tq_status launch_gemm_a8_tt(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
                             const float *sw, int64_t N, int bits, void *Y, int ytype, int64_t ldy,
-                            const DeviceInfo &dev, cudaStream_t s, const EpilogueArgs *ea) {
+                            const DeviceInfo &dev, cudaStream_t s, const EpilogueArgs *ea, void *split_ws) {
     return launch_tc<2>(nullptr, static_cast<const unsigned char *>(At), static_cast<const unsigned char *>(Wt),
-                        sx, M, K, nullptr, sw, N, bits, Y, ytype, ldy, dev, s, ea);
+                        sx, M, K, nullptr, sw, N, bits, Y, ytype, ldy, dev, s, ea, split_ws);
+}
+
+// Split workspace: the flags ([pairs][2 CTAs][kDrainWarps] words, rounded up to
+// 256 bytes), then one partial tile per CTA ([pairs][2][128][256] int32).
+size_t split_flag_bytes(const DeviceInfo &dev) {
+    return (static_cast<size_t>(dev.sms / 2) * 2 * kDrainWarps * 4 + 255) / 256 * 256;
+}
+
+size_t split_workspace_bytes(const DeviceInfo &dev) {
+    return split_flag_bytes(dev) + static_cast<size_t>(dev.sms / 2) * 2 * kSlotInts * 4;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,

@@ -240,7 +240,7 @@ k_gemv_a16(const GemvParams p) {
     }
     if (C > 1) cg::this_cluster().sync();
     // never leave with bulk copies still landing in this CTA's shared memory
-    if (!have_w) mbar_wait_bounded(wbar, 0);
+    if (!have_w) mbar_wait_bounded(wbar, 0, kA16DrainLimit);
 }
 
 struct Plan {

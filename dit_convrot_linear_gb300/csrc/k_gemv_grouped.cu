@@ -346,7 +346,7 @@ k_gemv_grouped(const GroupedParams p) {
         if (lane == 0) {
             for (int s = 0; s < kGStages; ++s) {
                 const int64_t uses = k > s ? (k - s + kGStages - 1) / kGStages : 0;
-                if (uses > 0) mbar_wait_bounded(full0 + 8 * s, static_cast<uint32_t>((uses - 1) & 1));
+                if (uses > 0) mbar_wait_bounded(full0 + 8 * s, static_cast<uint32_t>((uses - 1) & 1), kA16DrainLimit);
             }
         }
         return;

@@ -82,8 +82,19 @@ k_gemv_small(const SmallParams p) {
         if (lane == 0) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(wbar));
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            // A build for the library's own tests (TQ_TEST_UNSET_BYTES) expects
+            // bytes that no copy brings, so the barrier's phase never completes
+            // and the bounded waits on it expire: the expiry path is then taken
+            // with every issued copy landed, the wait that a CTA keeps for its
+            // copies before it exits runs to its full limit, and nothing else
+            // changes.
+#ifdef TQ_TEST_UNSET_BYTES
+            constexpr uint32_t kUnset = TQ_TEST_UNSET_BYTES;
+#else
+            constexpr uint32_t kUnset = 0;
+#endif
             asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(wbar),
-                         "r"(static_cast<uint32_t>(rows * rbytes))
+                         "r"(static_cast<uint32_t>(rows * rbytes) + kUnset)
                          : "memory");
         }
         __syncwarp();
@@ -292,7 +303,7 @@ k_gemv_small(const SmallParams p) {
                 static_cast<uint16_t *>(p.Y)[m * p.ldy + n] = f32_to_bf16_bits(y);
         }
     } else {
-        mbar_wait_bounded(wbar, 0);  // never leave with copies landing in shared memory
+        mbar_wait_bounded(wbar, 0, kA16DrainLimit);  // never leave with copies landing in shared memory
     }
 }
 
@@ -354,8 +365,19 @@ k_gemv_rows8(const Rows8Params p) {
         if (lane == 0) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(wbar));
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            // A build for the library's own tests (TQ_TEST_UNSET_BYTES) expects
+            // bytes that no copy brings, so the barrier's phase never completes
+            // and the bounded waits on it expire: the expiry path is then taken
+            // with every issued copy landed, the wait that a CTA keeps for its
+            // copies before it exits runs to its full limit, and nothing else
+            // changes.
+#ifdef TQ_TEST_UNSET_BYTES
+            constexpr uint32_t kUnset = TQ_TEST_UNSET_BYTES;
+#else
+            constexpr uint32_t kUnset = 0;
+#endif
             asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(wbar),
-                         "r"(static_cast<uint32_t>(rows * rbytes))
+                         "r"(static_cast<uint32_t>(rows * rbytes) + kUnset)
                          : "memory");
         }
         __syncwarp();
@@ -495,7 +517,7 @@ k_gemv_rows8(const Rows8Params p) {
                 static_cast<uint16_t *>(p.Y)[m * p.ldy + n] = f32_to_bf16_bits(y);
         }
     } else {
-        mbar_wait_bounded(wbar, 0);  // never leave with copies landing in shared memory
+        mbar_wait_bounded(wbar, 0, kA16DrainLimit);  // never leave with copies landing in shared memory
     }
 }
 

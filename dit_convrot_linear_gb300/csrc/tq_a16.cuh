@@ -7,7 +7,17 @@
 
 namespace tq {
 
-constexpr long long kA16WaitLimit = 4000000000ll;  // clock cycles (about 2 s)
+// Bounded waits, in clock cycles (about 2 s each).  A build of the library
+// made for its own tests may shorten the wait for operands
+// (TQ_TEST_WAIT_CYCLES) so that an expiry can be provoked on purpose; the
+// wait that lets a CTA's copies in flight land before it exits keeps the full
+// limit in every build.
+#ifdef TQ_TEST_WAIT_CYCLES
+constexpr long long kA16WaitLimit = TQ_TEST_WAIT_CYCLES;
+#else
+constexpr long long kA16WaitLimit = 4000000000ll;
+#endif
+constexpr long long kA16DrainLimit = 4000000000ll;
 
 // x' layout inside each K block so that the 4 values one lane needs for one
 // mma (its k-slots 2t, 2t+1, 2t+8, 2t+9) are contiguous at jj*16 + 4t.
@@ -117,12 +127,13 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase of `parity` to complete, for at most kA16WaitLimit clock
-// cycles (about 2 s); false on expiry.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for the phase of `parity` to complete, for at most `limit` clock
+// cycles; false on expiry.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  long long limit = kA16WaitLimit) {
     const long long t0 = clock64();
     while (!mbar_try(bar, parity))
-        if (clock64() - t0 > kA16WaitLimit) return false;
+        if (clock64() - t0 > limit) return false;
     return true;
 }
 

@@ -241,9 +241,14 @@ size_t tq_act_tiled_bytes(int64_t M, int64_t K) {
 }
 
 size_t tq_linear_workspace_bytes(int64_t M, int64_t K, int64_t N, int bits, tq_mode mode) {
-    (void)N;
     (void)bits;
-    if (mode != TQ_W8A8 || M <= 0 || K <= 0) return 0;
+    if (M <= 0 || K <= 0) return 0;
+    if (mode == TQ_W8A16 || mode == TQ_W4A16) {
+        // optional: the tensor-core product's x' tiles (see tq.h)
+        if (M > TQ_MAX_M_A16 || N <= 0 || !valid_k(K) || !mul_ok(N, K)) return 0;
+        return skinny_tc_applies(M, N, K) ? static_cast<size_t>(skinny_tc_workspace(M, K)) : 0;
+    }
+    if (mode != TQ_W8A8) return 0;
     if (!mul_ok(M, K)) return 0;
     const size_t scales = (static_cast<size_t>(M) * 4 + 255) / 256 * 256;
     // K <= TQ_MAX_K_TILED: tiled fp16 codes, then fp32 token scales;
@@ -269,11 +274,18 @@ tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
     if ((st = check_weights(Wq, sw, N, K, bits)) != TQ_OK) return st;
     if ((st = check_output(Y, M, N, ldy, out_size(ytype))) != TQ_OK) return st;
     const size_t need = tq_linear_workspace_bytes(M, K, N, bits, mode);
-    if (need > 0 && (!workspace || ws_bytes < need)) return TQ_ERR_WORKSPACE;
-    if (need > 0 && !aligned(workspace, 256)) return TQ_ERR_ALIGN;
+    const bool a16 = mode != TQ_W8A8;
+    // A16: the workspace is optional (the tensor-core product uses it when
+    // given and large enough); W8A8: required
+    if (!a16 && need > 0 && (!workspace || ws_bytes < need)) return TQ_ERR_WORKSPACE;
+    const bool use_ws = need > 0 && workspace && ws_bytes >= need;
+    if (use_ws && !aligned(workspace, 256)) return TQ_ERR_ALIGN;
     DeviceInfo dev;
     if ((st = current_device(&dev)) != TQ_OK) return st;
-    if (mode != TQ_W8A8) {
+    if (a16) {
+        if (use_ws && skinny_tc_fits_device(N, dev))
+            return launch_skinny_tc(static_cast<const uint16_t *>(X), M, K, ldx, static_cast<const uint8_t *>(Wq),
+                                    sw, N, bits, Y, ytype == TQ_OUT_BF16 ? 1 : 0, ldy, workspace, dev, stream);
         if (gemv_small_fits(M, N, K, bits, dev))
             return launch_gemv_small(static_cast<const uint16_t *>(X), M, K, ldx,
                                      static_cast<const uint8_t *>(Wq), sw, N, bits, Y,
@@ -400,9 +412,33 @@ tq_status tq_linear_tt(const void *At, const float *sx, int64_t M, int64_t K, co
     return tq_linear_tt_ex(At, sx, M, K, Wt, sw, N, bits, nullptr, Y, ytype, ldy, stream);
 }
 
+static tq_status linear_tt_impl(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
+                                const float *sw, int64_t N, int bits, const tq_epilogue *epi, void *Y,
+                                tq_out ytype, int64_t ldy, void *split_ws, size_t split_bytes,
+                                cudaStream_t stream);
+
 tq_status tq_linear_tt_ex(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
                           const float *sw, int64_t N, int bits, const tq_epilogue *epi, void *Y,
                           tq_out ytype, int64_t ldy, cudaStream_t stream) {
+    return linear_tt_impl(At, sx, M, K, Wt, sw, N, bits, epi, Y, ytype, ldy, nullptr, 0, stream);
+}
+
+size_t tq_split_workspace_bytes(void) {
+    DeviceInfo dev;
+    if (current_device(&dev) != TQ_OK) return 0;
+    return split_workspace_bytes(dev);
+}
+
+tq_status tq_linear_tt_split(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
+                             const float *sw, int64_t N, int bits, const tq_epilogue *epi, void *Y,
+                             tq_out ytype, int64_t ldy, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    return linear_tt_impl(At, sx, M, K, Wt, sw, N, bits, epi, Y, ytype, ldy, workspace, ws_bytes, stream);
+}
+
+static tq_status linear_tt_impl(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
+                                const float *sw, int64_t N, int bits, const tq_epilogue *epi, void *Y,
+                                tq_out ytype, int64_t ldy, void *split_ws, size_t split_bytes,
+                                cudaStream_t stream) {
     if (ytype != TQ_OUT_F32 && ytype != TQ_OUT_BF16 && ytype != TQ_OUT_I32) return TQ_ERR_MODE;
     if (bits != 8 && bits != 4) return TQ_ERR_BITS;
     if (M < 0 || N < 0 || !valid_k(K) || K > TQ_MAX_K_TILED) return TQ_ERR_SHAPE;
@@ -440,8 +476,12 @@ tq_status tq_linear_tt_ex(const void *At, const float *sx, int64_t M, int64_t K,
     }
     DeviceInfo dev;
     if ((st = current_device(&dev)) != TQ_OK) return st;
+    if (split_ws) {
+        if (split_bytes < split_workspace_bytes(dev)) return TQ_ERR_WORKSPACE;
+        if (!aligned(split_ws, 256)) return TQ_ERR_ALIGN;
+    }
     return launch_gemm_a8_tt(At, sx, M, K, Wt, sw, N, bits, Y, static_cast<int>(ytype), ldy, dev, stream,
-                             epi ? &ea : nullptr);
+                             epi ? &ea : nullptr, split_ws);
 }
 
 tq_status tq_device_status(cudaStream_t stream) {

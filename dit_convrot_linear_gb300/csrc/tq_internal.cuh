@@ -54,6 +54,15 @@ tq_status launch_gemv_a16(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
                           int bits, void *Y, int ytype, int64_t ldy,
                           const DeviceInfo &dev, cudaStream_t s);
 
+// Batched A16 product on tcgen05 (M <= 64; large matrices or more than 8
+// tokens): a pre-pass writes x' as fp16 tiles into the workspace.
+bool skinny_tc_applies(int64_t M, int64_t N, int64_t K);
+int64_t skinny_tc_workspace(int64_t M, int64_t K);
+bool skinny_tc_fits_device(int64_t N, const DeviceInfo &dev);
+tq_status launch_skinny_tc(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, const uint8_t *Wq,
+                           const float *sw, int64_t N, int bits, void *Y, int ytype, int64_t ldy, void *ws,
+                           const DeviceInfo &dev, cudaStream_t s);
+
 // Decode product for M <= 8: whole rows per CTA, no cluster reduction.
 bool gemv_small_fits(int64_t M, int64_t N, int64_t K, int bits, const DeviceInfo &dev);
 tq_status launch_gemv_small(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
@@ -99,7 +108,12 @@ struct EpilogueArgs {
 };
 tq_status launch_gemm_a8_tt(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
                             const float *sw, int64_t N, int bits, void *Y, int ytype, int64_t ldy,
-                            const DeviceInfo &dev, cudaStream_t s, const EpilogueArgs *ea = nullptr);
+                            const DeviceInfo &dev, cudaStream_t s, const EpilogueArgs *ea = nullptr,
+                            void *split_ws = nullptr);
+// Bytes of the split workspace of the both-tiled product on this device, and
+// of its flag area at the start (the rest holds one partial tile per CTA).
+size_t split_workspace_bytes(const DeviceInfo &dev);
+size_t split_flag_bytes(const DeviceInfo &dev);
 
 int64_t tiled_act_tiles_bytes(int64_t M, int64_t K);
 int64_t tiled_act_bytes(int64_t M, int64_t K);

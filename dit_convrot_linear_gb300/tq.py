@@ -45,6 +45,8 @@ SIGNATURES = {
     "tq_tile_weights": (_C, [_P, _I, _I, _C, _P, _Z, _P]),
     "tq_linear_tt": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
     "tq_linear_tt_ex": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _P, _C, _I, _P]),
+    "tq_split_workspace_bytes": (_Z, []),
+    "tq_linear_tt_split": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _P, _C, _I, _P, _Z, _P]),
     "tq_grouped_bytes": (_C, [_P, _I, _C, ctypes.POINTER(ctypes.c_size_t)]),
     "tq_grouped_create": (_C, [_P, _I, _C, _C, _P, _Z, ctypes.POINTER(ctypes.c_void_p)]),
     "tq_grouped_run": (_C, [_P, _P]),
@@ -364,10 +366,23 @@ def tile_weights(Wq, N: int, K: int, bits: int, Wt=None, stream=None):
     return Wt
 
 
+def split_workspace_bytes() -> int:
+    return int(lib().tq_split_workspace_bytes())
+
+
+def split_workspace(device="cuda"):
+    """A zeroed split workspace for ``linear_tt(..., split=ws)`` (one per
+    stream; every completed call leaves it zeroed)."""
+    import torch
+    return torch.zeros(split_workspace_bytes(), dtype=torch.uint8, device=device)
+
+
 def linear_tt(At, sx, M: int, K: int, Wt, sw, N: int, bits: int, Y=None, out: str = "f32",
-              stream=None):
+              split=None, stream=None):
     """The A8 product with both operands tiled (``rotate_quant_act_tiled`` and
-    ``tile_weights``)."""
+    ``tile_weights``).  ``split``: a workspace from ``split_workspace()`` lets
+    the product split the K steps of its last waves of tiles over every CTA
+    pair (tq_linear_tt_split)."""
     import torch
     if Y is None:
         Y = torch.empty((M, N), dtype=_dt(out), device=At.device)
@@ -377,13 +392,19 @@ def linear_tt(At, sx, M: int, K: int, Wt, sw, N: int, bits: int, Y=None, out: st
     _req(Wt, "Wt", nbytes=weights_tiled_bytes(N, K))
     _req(sw, "sw", dtype=torch.float32, nbytes=4 * N)
     _req(Y, "Y", dtype=_dt(out), rows=M, cols=N)
+    if split is not None:
+        _req(split, "split", nbytes=split_workspace_bytes())
+        _check(lib().tq_linear_tt_split(_ptr(At), _ptr(sx), M, K, _ptr(Wt), _ptr(sw), N, bits, None, _ptr(Y),
+                                        OUT[out], Y.stride(0), _ptr(split), _nbytes(split), _stream(stream)),
+               "tq_linear_tt_split")
+        return Y
     _check(lib().tq_linear_tt(_ptr(At), _ptr(sx), M, K, _ptr(Wt), _ptr(sw), N, bits, _ptr(Y),
                               OUT[out], Y.stride(0), _stream(stream)), "tq_linear_tt")
     return Y
 
 
 def linear_tt_ex(At, sx, M: int, K: int, Wt, sw, N: int, bits: int, Y=None, out: str = "f32",
-                 bias=None, gate=None, residual=None, stream=None):
+                 bias=None, gate=None, residual=None, split=None, stream=None):
     """``linear_tt`` with the fused epilogue Y = residual + gate * (product + bias)
     (each optional; ``residual`` may be ``Y`` itself)."""
     import torch
@@ -408,6 +429,12 @@ def linear_tt_ex(At, sx, M: int, K: int, Wt, sw, N: int, bits: int, Y=None, out:
         rtype = OUT["f32" if residual.dtype == torch.float32 else "bf16"]
         ldr = residual.stride(0)
     epi = Epilogue(_ptr(bias), _ptr(gate), _ptr(residual), ldr, rtype)
+    if split is not None:
+        _req(split, "split", nbytes=split_workspace_bytes())
+        _check(lib().tq_linear_tt_split(_ptr(At), _ptr(sx), M, K, _ptr(Wt), _ptr(sw), N, bits,
+                                        ctypes.addressof(epi), _ptr(Y), OUT[out], Y.stride(0), _ptr(split),
+                                        _nbytes(split), _stream(stream)), "tq_linear_tt_split")
+        return Y
     _check(lib().tq_linear_tt_ex(_ptr(At), _ptr(sx), M, K, _ptr(Wt), _ptr(sw), N, bits,
                                  ctypes.addressof(epi), _ptr(Y), OUT[out], Y.stride(0),
                                  _stream(stream)), "tq_linear_tt_ex")

@@ -143,7 +143,8 @@ tq_status tq_rotate_act_bf16(const void *X, int64_t M, int64_t K, int64_t ldx,
                              void *Xr, cudaStream_t stream);
 
 /*
- * Bytes of workspace tq_linear needs for these sizes (0 when none).  The
+ * Bytes of workspace tq_linear needs for these sizes (0 when none; for the
+ * A16 modes, the bytes of the optional tensor-core operand).  The
  * projections are about 80% of a DiT step's GPU time (TensorFold PR #948,
  * "What comes next" and "Receipts").
  */
@@ -168,6 +169,16 @@ size_t tq_linear_workspace_bytes(int64_t M, int64_t K, int64_t N, int bits,
  *            tq_linear_workspace_bytes(M, K, N, bits, mode) bytes, 256-byte
  *            aligned (may be NULL when that is 0).  Its contents on entry do
  *            not matter; the call overwrites it.
+ *            TQ_W8A8: required.  A16 modes: optional.  With it, products of
+ *            more than 8 token rows, or of weights of at least 2^24 codes,
+ *            run on the tensor cores (the rotated rows are first written to
+ *            the workspace as fp16 tiles, each token scaled by a power of two,
+ *            which keeps every bf16 value exact); without it (or smaller than
+ *            that size) the CUDA-core kernels run.  Both compute the same Y
+ *            within fp32 rounding.  Calls in order on one stream may share a
+ *            workspace (the next call's weights stream early, but its operand
+ *            is written only after this call ends); calls on different
+ *            streams need their own.
  */
 tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
                     const void *Wq, const float *sw, int64_t N, int bits,
@@ -301,6 +312,41 @@ typedef struct {
 tq_status tq_linear_tt_ex(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
                           const float *sw, int64_t N, int bits, const tq_epilogue *epi, void *Y,
                           tq_out ytype, int64_t ldy, cudaStream_t stream);
+
+/*
+ * Bytes of the split workspace of tq_linear_tt_split on the current device (0
+ * when no usable device is current).  It does not depend on the sizes of a
+ * call: one workspace serves every product that runs on one stream.
+ */
+size_t tq_split_workspace_bytes(void);
+
+/*
+ * tq_linear_tt_ex with the tiles of the last waves split along K.  The
+ * projections are most of a DiT step (TensorFold PR #948, "What comes next":
+ * about 80% of the GPU time); a product whose 256 x 256 output tiles leave the
+ * last wave of CTA pairs mostly idle (the out and down projections of a
+ * 1024-token block are 48 tiles) spends that share of its time with part of
+ * the tensor cores unused.  With a workspace, the K steps of those tiles are
+ * shared evenly by every pair; a pair that holds only part of a tile stores
+ * its exact int32 partial sums, and the pair that holds the tile's last K step
+ * adds them before the epilogue.  The sums are integers, so the result is
+ * bit-identical to tq_linear_tt_ex, whatever the split (the library decides
+ * it from the tile count).
+ *
+ *   workspace  tq_split_workspace_bytes() bytes of device memory, 256-byte
+ *              aligned, ZEROED before its first use (cudaMemsetAsync).  Every
+ *              call that completes leaves it zeroed again.  After a call
+ *              returned TQ_ERR_DEVICE_TIMEOUT from tq_device_status, zero it
+ *              again before reuse.  Calls that may run at the same time on
+ *              the GPU (different streams) need workspaces of their own.
+ *              NULL: no split (tq_linear_tt_ex).
+ * Other arguments as tq_linear_tt_ex.  TQ_ERR_WORKSPACE if ws_bytes is too
+ * small, TQ_ERR_ALIGN if the workspace is not 256-byte aligned.
+ */
+tq_status tq_linear_tt_split(const void *At, const float *sx, int64_t M, int64_t K, const void *Wt,
+                             const float *sw, int64_t N, int bits, const tq_epilogue *epi, void *Y,
+                             tq_out ytype, int64_t ldy, void *workspace, size_t ws_bytes,
+                             cudaStream_t stream);
 
 /*
  * Block-scaled weights: one fp32 scale per block of G input columns instead

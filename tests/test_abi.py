@@ -104,9 +104,22 @@ def test_linear_refusals(L):
     assert lin(L, M=2 ** 62, ldx=2 ** 10, K=512, mode=2, ws=FAKE, wsb=2 ** 62) == OVERFLOW
 
 
-def test_workspace_is_zero_for_a16(L):
-    assert L.tq_linear_workspace_bytes(64, 4096, 12288, 4, 1) == 0
+def test_a16_workspace_is_the_tensor_core_operand(L):
+    """A16 modes: the optional workspace holds the x' tiles of the tensor-core
+    product ([ceil(K/64)] tiles of M rounded up to 16 rows x 64 fp16, then the
+    token factors), for more than 8 tokens or weights of at least 2^24 codes;
+    0 for decode-sized products, which need none."""
+    assert L.tq_linear_workspace_bytes(64, 4096, 12288, 4, 1) == 64 * 64 * 64 * 2 + 256
+    assert L.tq_linear_workspace_bytes(13, 896, 300, 8, 0) == 14 * 16 * 64 * 2 + 256
+    assert L.tq_linear_workspace_bytes(1, 4096, 12288, 4, 1) == 64 * 16 * 64 * 2 + 256
+    assert L.tq_linear_workspace_bytes(1, 896, 4864, 8, 0) == 0          # decode: none
+    assert L.tq_linear_workspace_bytes(8, 4096, 1000, 4, 1) == 0
+    assert L.tq_linear_workspace_bytes(64, 16384 + 256, 256, 8, 0) == 0   # K above the tiled limit
     assert L.tq_linear_workspace_bytes(4032, 12288, 3072, 8, 2) >= 4032 * 12288 + 4032 * 4
+    # an A16 call without a workspace is not refused (the CUDA-core kernels run)
+    import torch
+    if not torch.cuda.is_available():
+        assert lin(L, M=13, K=896, ldx=896, N=300, ldy=300, mode=0, bits=8, ws=0, wsb=0) == DEVICE
 
 
 def test_linear_q8_refusals(L):
@@ -259,6 +272,27 @@ def test_tiled_weights_refusals_and_size(L):
     assert tt(Wt=FAKE + 16) == ALIGN
     assert tt(ldy=100) == SHAPE
     assert tt(M=0) == OK
+
+
+def test_split_refusals(L):
+    """tq_linear_tt_split checks what tq_linear_tt does, and its workspace;
+    without a device the workspace size is 0 and a valid call reports it."""
+    sp = lambda **k: L.tq_linear_tt_split(*[k.get(n, d) for n, d in (
+        ("At", FAKE), ("sx", FAKE), ("M", 4), ("K", 512), ("Wt", FAKE), ("sw", FAKE), ("N", 256),
+        ("bits", 8), ("epi", None), ("Y", FAKE), ("ytype", 0), ("ldy", 256), ("ws", FAKE),
+        ("wsb", 1 << 30), ("s", S0))])
+    assert sp(bits=3) == BITS
+    assert sp(ytype=7) == MODE
+    assert sp(K=96) == SHAPE
+    assert sp(Wt=0) == NULL
+    assert sp(At=FAKE + 16) == ALIGN
+    assert sp(ldy=100) == SHAPE
+    assert sp(M=0) == OK
+    import torch
+    if not torch.cuda.is_available():
+        assert L.tq_split_workspace_bytes() == 0
+        assert sp() == DEVICE
+        assert sp(ws=None, wsb=0) == DEVICE
 
 
 def test_epilogue_refusals(L):
