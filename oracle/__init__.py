@@ -7,7 +7,7 @@ no code with the CUDA library: the arithmetic is the plain C in
 code products), compiled here with gcc.
 
 Every function takes and returns numpy arrays; bf16 tensors travel as their
-``uint16`` bit patterns.  Step names (O1..O7) are those of ``tq_oracle.c``.
+``uint16`` bit patterns.  Step names (O1..O11) are those of ``tq_oracle.c``.
 """
 from __future__ import annotations
 
@@ -69,6 +69,8 @@ _SIGS = {
     "or_matmul_f64": (ctypes.c_int, [_P, _I, _I, _P, _I, _P, ctypes.c_int]),
     "or_swiglu_f64": (ctypes.c_int, [_P, _P, _I, _P]),
     "or_swiglu_bf16": (ctypes.c_int, [_P, _I, _P, _I, _I, _I, _P]),
+    "or_modnorm_f64": (ctypes.c_int, [_P, _I, _P, _P, ctypes.c_double, _P]),
+    "or_modnorm_bf16": (ctypes.c_int, [_P, _I, _I, _I, _P, _P, ctypes.c_float, _P]),
     "or_quantize_blocks": (ctypes.c_int, [_P, _I, _I, _I, ctypes.c_int, _P, _P]),
     "or_linear_a16_blocked": (ctypes.c_int, [_P, _I, _I, _P, _P, _I, _I, _P, ctypes.c_int]),
 }
@@ -337,6 +339,41 @@ def swiglu_bf16(G: np.ndarray, U: np.ndarray) -> np.ndarray:
 def swiglu_quant_act(G: np.ndarray, U: np.ndarray):
     """O8 then O1+O2+O4: the down projection's A8 operand from gate and up."""
     return rotate_quant_act(swiglu_bf16(G, U))
+
+
+def modnorm_f64(x, shift, scale, eps: float) -> np.ndarray:
+    """O11 in fp64 on rows x [R, K] (fp64 values): (x - mu) / sqrt(var + eps)
+    * (1 + scale) + shift, mu and var the row's mean and biased variance."""
+    x = _c(np.atleast_2d(x), np.float64)
+    sh, sc = _c(shift, np.float64), _c(scale, np.float64)
+    R, K = x.shape
+    if sh.shape != (K,) or sc.shape != (K,):
+        raise ValueError("shift and scale must have K entries")
+    h = np.empty_like(x)
+    for r in range(R):
+        _check(lib().or_modnorm_f64(x[r].ctypes.data, K, sh.ctypes.data, sc.ctypes.data, float(eps),
+                                    h[r].ctypes.data), "modnorm_f64")
+    return h
+
+
+def modnorm_bf16(X: np.ndarray, shift, scale, eps: float) -> np.ndarray:
+    """O11: bf16 X [M, K], fp32 shift and scale [K] -> bf16 bits of the
+    modulated layer norm [M, K]."""
+    X = _c(X, np.uint16)
+    M, K = X.shape
+    sh, sc = _c(shift, np.float32), _c(scale, np.float32)
+    if sh.shape != (K,) or sc.shape != (K,):
+        raise ValueError("shift and scale must have K entries")
+    H = np.empty((M, K), dtype=np.uint16)
+    _check(lib().or_modnorm_bf16(X.ctypes.data, K, M, K, sh.ctypes.data, sc.ctypes.data,
+                                 float(np.float32(eps)), H.ctypes.data), "modnorm_bf16")
+    return H
+
+
+def modnorm_quant_act(X: np.ndarray, shift, scale, eps: float):
+    """O11 then O1+O2+O4: a QKV or gate/up projection's A8 operand from the
+    block input X and its modulation."""
+    return rotate_quant_act(modnorm_bf16(X, shift, scale, eps))
 
 
 def quantize_blocks(V: np.ndarray, qmax: int, G: int):

@@ -52,6 +52,18 @@
  *   O10 block-scaled A16 product: Y = sum_b s_b * sum_{k in block b} q_w * x
  *      in fp64, x the bf16 activations (rotated and rounded as in O4' when
  *      the weights were rotated, else as given).
+ *   O11 modulated layer norm (the row kernel in front of a DiT block's
+ *      query/key/value and gate/up products; the pages name "the modulated
+ *      layer norm" among the row kernels next to the projections, with fp32
+ *      norms, TensorFold PR #948, "What comes next" and the precision list of
+ *      its summary; the modulation is shared by every block, same PR, "What it
+ *      adds", host.zig): per row, mu = mean(x), var = mean((x - mu)^2) (the
+ *      biased variance: a layer norm divides by K), and
+ *      h = (x - mu) / sqrt(var + eps) * (1 + scale) + shift, in fp64 from bf16
+ *      x and fp32 shift, scale [K] (one modulation for all rows), then
+ *      rounded to the nearest bf16.  The form LN(x) (1 + scale) + shift with no
+ *      affine parameters of its own is the adaptive layer norm of Peebles and
+ *      Xie, "Scalable Diffusion Models with Transformers" (2023).
  *
  * Readings where the pages are silent (each listed in the design notes):
  *   Sylvester order and 1/sqrt(n) normalisation; a last group narrower than
@@ -444,6 +456,46 @@ int or_swiglu_bf16(const uint16_t *G, int64_t ldg, const uint16_t *U, int64_t ld
             or_swiglu_f64(&g, &u, 1, &h);
             H[m * K + k] = or_f64_to_bf16(h);
         }
+    return 0;
+}
+
+/* -------------------------------------------------------------------------- */
+/* O11 modulated layer norm                                                    */
+
+/* One row: h = (x - mu) / sqrt(var + eps) * (1 + scale) + shift in fp64. */
+int or_modnorm_f64(const double *x, int64_t K, const double *shift, const double *scale, double eps,
+                   double *h) {
+    if (K <= 0) return 1;
+    double mu = 0.0;
+    for (int64_t k = 0; k < K; ++k) mu += x[k];
+    mu /= (double)K;
+    double var = 0.0;
+    for (int64_t k = 0; k < K; ++k) var += (x[k] - mu) * (x[k] - mu);
+    var /= (double)K;
+    const double rstd = 1.0 / sqrt(var + eps);
+    for (int64_t k = 0; k < K; ++k) h[k] = (x[k] - mu) * rstd * (1.0 + scale[k]) + shift[k];
+    return 0;
+}
+
+/* H [M, K] dense bf16 bits from bf16 X [M, K] (row stride ldx), fp32 shift and
+ * scale [K] and eps. */
+int or_modnorm_bf16(const uint16_t *X, int64_t ldx, int64_t M, int64_t K, const float *shift,
+                    const float *scale, float eps, uint16_t *H) {
+    if (K <= 0) return 1;
+    fesetround(FE_TONEAREST);
+    double *x = malloc(sizeof(double) * (size_t)K * 4);
+    if (!x) return 2;
+    double *sh = x + K, *sc = x + 2 * K, *h = x + 3 * K;
+    for (int64_t k = 0; k < K; ++k) {
+        sh[k] = (double)shift[k];
+        sc[k] = (double)scale[k];
+    }
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t k = 0; k < K; ++k) x[k] = or_bf16_to_f64(X[m * ldx + k]);
+        or_modnorm_f64(x, K, sh, sc, (double)eps, h);
+        for (int64_t k = 0; k < K; ++k) H[m * K + k] = or_f64_to_bf16(h[k]);
+    }
+    free(x);
     return 0;
 }
 

@@ -15,6 +15,7 @@ import oracle
 import test_oracle_pins as pins
 import test_oracle_blocked as blocked_pins
 import test_oracle_swiglu as swiglu_pins
+import test_oracle_modnorm as modnorm_pins
 
 MUTANTS = {
     "sign_of_hadamard": ("& 1) ? -1 : 1", "& 1) ? 1 : -1"),
@@ -50,6 +51,12 @@ MUTANTS = {
     "silu_sigmoid_of_minus_g": ("g[i] / (1.0 + exp(-g[i])) * u[i]", "g[i] / (1.0 + exp(g[i])) * u[i]"),
     "swiglu_plain_sigmoid_gate": ("g[i] / (1.0 + exp(-g[i])) * u[i]", "1.0 / (1.0 + exp(-g[i])) * u[i]"),
     "swiglu_gate_and_up_swapped": ("g[i] / (1.0 + exp(-g[i])) * u[i]", "u[i] / (1.0 + exp(-u[i])) * g[i]"),
+    "modnorm_unbiased_variance": ("    var /= (double)K;", "    var /= (double)(K - 1);"),
+    "modnorm_eps_outside_sqrt": ("1.0 / sqrt(var + eps)", "1.0 / (sqrt(var) + eps)"),
+    "modnorm_eps_dropped": ("1.0 / sqrt(var + eps)", "1.0 / sqrt(var)"),
+    "modnorm_mean_not_subtracted": ("h[k] = (x[k] - mu) * rstd", "h[k] = x[k] * rstd"),
+    "modnorm_scale_without_one": ("* (1.0 + scale[k]) + shift[k]", "* scale[k] + shift[k]"),
+    "modnorm_shift_and_scale_swapped": ("* (1.0 + scale[k]) + shift[k]", "* (1.0 + shift[k]) + scale[k]"),
     "block_amax_over_half_block": ("for (int64_t k = 0; k < G; ++k) {\n                const double a",
                                    "for (int64_t k = 0; k < G / 2; ++k) {\n                const double a"),
     "block_scale_stored_in_next_slot": ("scales[r * nb + b] = s;", "scales[r * nb + (b + 1) % nb] = s;"),
@@ -84,6 +91,10 @@ PIN_TESTS = [
     lambda: swiglu_pins.test_silu_odd_part_is_the_identity(),
     lambda: swiglu_pins.test_silu_special_values(),
     lambda: swiglu_pins.test_swiglu_is_linear_in_up(),
+    lambda: modnorm_pins.test_worked_row(),
+    lambda: modnorm_pins.test_moments_and_invariances(),
+    lambda: modnorm_pins.test_modulation_special_values(),
+    lambda: modnorm_pins.test_constant_row_gives_the_shift(),
     lambda: blocked_pins.test_block_quantiser_error_bound_range_and_scale(7, 32),
     lambda: blocked_pins.test_blocks_scale_independently(),
     lambda: blocked_pins.test_block_quantiser_ties_to_even_in_a_later_block(),
