@@ -47,10 +47,11 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--calls", type=int, default=1000)
     ap.add_argument("--skip-dit", action="store_true")
-    ap.add_argument("--only", default="all", choices=["all", "decode", "dit", "blocked", "batched", "chain"],
+    ap.add_argument("--only", default="all",
+                    choices=["all", "decode", "dit", "blocked", "batched", "chain", "modnorm"],
                     help="profiling cases: only the W8A16 decode graph, only the DiT GEMMs, only "
-                         "the block-scaled decode products, only the batched W4A16 decode, or only "
-                         "the DiT block chain")
+                         "the block-scaled decode products, only the batched W4A16 decode, only "
+                         "the DiT block chain, or only the fused modulated-norm operand")
     ap.add_argument("--dit-m", type=int, default=4032, help="token rows of the DiT case")
     ap.add_argument("--skip-cpu", action="store_true")
     return ap.parse_args()
@@ -714,6 +715,59 @@ def swiglu_measure(device, reps=5, M=4032, K=12288):
             "fused_bytes": fused_bytes, "unfused_bytes": 10 * M * K}
 
 
+def modnorm_measure(device, reps=5, M=4032, K=3072, hbm_peak=None):
+    """The QKV / gate-up operand made from the block input in one pass
+    (tq_modnorm_quant_act_tiled: modulated layer norm, rotation, per-token
+    int8), against the unfused route: a modulated layer norm in PyTorch
+    (fp32 norm, bf16 h written) and then the rotation of h
+    (tq_rotate_quant_act_tiled), and against the rotation alone.  L2 flushed
+    before each call.  Bytes: fused, read 2MK + write 2MK (fp16 codes) + the
+    modulation 8K; unfused, the norm (read 2MK, write 2MK) and the rotation
+    (read 2MK, write 2MK)."""
+    import numpy as np
+    import torch
+    from dit_convrot_linear_gb300 import synth, tq
+    X = bf16_dev(synth.tensor("bench/modnorm/x", M, K, 1.0, 0.002, 40.0), device)
+    rng = np.random.default_rng(21)
+    shift = torch.from_numpy(rng.normal(0.0, 0.5, K).astype(np.float32)).to(device)
+    scale = torch.from_numpy(rng.normal(0.0, 0.3, K).astype(np.float32)).to(device)
+    eps = 1e-6
+    At, sx = tq.modnorm_quant_act_tiled(X, shift, scale, eps)
+    At2, sx2 = tq.rotate_quant_act_tiled(X)
+    H = torch.empty_like(X)
+
+    def unfused():
+        h = torch.nn.functional.layer_norm(X.float(), (K,), eps=eps) * (1.0 + scale) + shift
+        H.copy_(h)
+        tq.rotate_quant_act_tiled(H, At=At2, sx=sx2)
+
+    flush = L2Flush(device)
+    runs = {"fused": lambda: tq.modnorm_quant_act_tiled(X, shift, scale, eps, At=At, sx=sx),
+            "rotation_only": lambda: tq.rotate_quant_act_tiled(X, At=At2, sx=sx2),
+            "unfused_torch_norm_then_rotation": unfused}
+    times = {k: [] for k in runs}
+    for _ in range(max(reps, 5)):
+        for k, fn in runs.items():
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times[k].append(e0.elapsed_time(e1))
+    med = {k: statistics.median(v) for k, v in times.items()}
+    fused_bytes = 4 * M * K + 8 * K
+    gbs = fused_bytes / (med["fused"] * 1e-3) / 1e9
+    out = {"M": M, "K": K, "kernel": "k_rotq<tiled, modulated norm>",
+           "fused_us": round(med["fused"] * 1e3, 2), "fused_gbs": round(gbs, 1),
+           "rotation_only_us": round(med["rotation_only"] * 1e3, 2),
+           "unfused_us": round(med["unfused_torch_norm_then_rotation"] * 1e3, 2),
+           "fused_bytes": fused_bytes, "unfused_bytes": 8 * M * K}
+    if hbm_peak:
+        out["frac"] = round(gbs / hbm_peak, 4)
+    return out
+
+
 # ------------------------------------------------------------------ CPU oracle
 
 def cpu_oracle_decode(bits, budget_s=12.0, min_calls=3, max_calls=60):
@@ -816,10 +870,18 @@ def main():
     if args.only == "dit":   # profiling case: the DiT products alone
         per, tops = dit_measure(device, reps=args.steps, M=args.dit_m)
         sw = swiglu_measure(device, reps=args.steps, M=args.dit_m)
+        mn = modnorm_measure(device, reps=args.steps, M=args.dit_m, hbm_peak=float(pk["hbm_gbs"]))
         if rank == 0:
             print(json.dumps({"case": f"dit W8A8 M={args.dit_m}",
                               **{k: round(v, 2) for k, v in tops.items()}, "per_projection": per,
-                              "swiglu_operand": sw}))
+                              "swiglu_operand": sw, "modnorm_operand": mn}))
+        return 0
+
+    if args.only == "modnorm":   # profiling case: the fused modulated-norm operand alone
+        res = {f"m{m}": modnorm_measure(device, reps=args.steps, M=m, hbm_peak=float(pk["hbm_gbs"]))
+               for m in (args.dit_m, 1024)}
+        if rank == 0:
+            print(json.dumps({"case": "modulated norm operand", **res}))
         return 0
 
     # headline: decode W8A16.  The 1000 calls are independent (each has its
@@ -924,6 +986,7 @@ def main():
                 "gemm_converting_tops": round(tops["gemm"], 2),
                 "per_projection": per,
                 "swiglu_operand": swiglu_measure(device),
+                "modnorm_operand": modnorm_measure(device, hbm_peak=float(pk["hbm_gbs"])),
                 "roofline": {"bound": "tensor", "kernel": "k_gemm_a8_tc<8, both tiled> (split tiles)",
                              "achieved": round(g, 2),
                              "peak": bf16_peak, "unit": "TFLOP/s",

@@ -14,6 +14,13 @@
 // (five butterfly stages inside a lane, three across lanes), the row's amax
 // after one CTA barrier, then the codes.  Longer rows (int8 codes only) use a
 // plain one-CTA-per-row kernel with a warp per group.
+//
+// Two row kernels that sit in front of a product are fused into k_rotq's
+// prologue, so their bf16 output is never written: SwiGLU (the down
+// projection's input) and the modulated layer norm (the input of a DiT
+// block's QKV and gate/up products).  The pages list both among the row
+// kernels next to the projections, candidates for fusion, with fp32 norms
+// (TensorFold PR #948, "What comes next").
 
 #include <cfloat>
 #include <type_traits>
@@ -328,10 +335,10 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
 }
 
 // The tail group (width n = 32, 64 or 128; E = n / 32 values a lane) of a
-// row, read from global memory and rotated by c_n * Hs_n, as the 32-lane
-// butterfly of the other rotation kernels.
+// row, read from global memory: lane l holds columns l E .. l E + E - 1 as
+// values 0 .. E - 1 (with SWIGLU, h of the gate and up rows).
 template <bool SWIGLU>
-__device__ __forceinline__ int rotate_tail_global(const uint16_t *x, const uint16_t *u, int n, float (&v)[8]) {
+__device__ __forceinline__ int load_tail_global(const uint16_t *x, const uint16_t *u, int n, float (&v)[8]) {
     const int lane = threadIdx.x & 31;
     const int E = n >> 5;
     uint32_t w[4] = {0u, 0u, 0u, 0u}, uw[4] = {0u, 0u, 0u, 0u};
@@ -357,6 +364,13 @@ __device__ __forceinline__ int rotate_tail_global(const uint16_t *x, const uint1
         v[2 * i] = __uint_as_float(w[i] << 16);
         v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
+    return E;
+}
+
+// The tail group's rotation by c_n * Hs_n, as the 32-lane butterfly of the
+// other rotation kernels; values past E come out 0.
+__device__ __forceinline__ void rotate_tail(int n, float (&v)[8]) {
+    const int E = n >> 5;
     switch (E) {
         case 4: warp_fwht<4, float>(v); break;
         case 2: warp_fwht<2, float>(v); break;
@@ -365,7 +379,28 @@ __device__ __forceinline__ int rotate_tail_global(const uint16_t *x, const uint1
     const float c = sqrtf(1.0f / static_cast<float>(n));
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] = e < E ? c * v[e] : 0.0f;
-    return E;
+}
+
+// Row prologues of k_rotq: the row as given, SwiGLU of a gate and an up row,
+// or the modulated layer norm of the row.
+constexpr int kPrePlain = 0, kPreSwiglu = 1, kPreNorm = 2;
+
+// The modulated layer norm's fp32 arithmetic on one value, rounded to bf16
+// as an unfused norm kernel would store it: h = (x - mu) rstd (1 + sc) + sh.
+__device__ __forceinline__ float modnorm_value(float x, float mu, float rstd, float sc, float sh) {
+    return __uint_as_float(static_cast<uint32_t>(f32_to_bf16_bits(fmaf((x - mu) * rstd, 1.0f + sc, sh))) << 16);
+}
+
+// Sum over the CTA's warps of one value a lane: the warp's sum goes to
+// slot[warp], and after the barrier every thread adds the W slots in order.
+__device__ __forceinline__ float cta_sum(float x, float *slot, int W) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if ((threadIdx.x & 31) == 0) slot[threadIdx.x >> 5] = x;
+    __syncthreads();
+    float t = slot[0];
+    for (int w = 1; w < W; ++w) t += slot[w];
+    return t;
 }
 
 constexpr int kRotqMaxWarps = 17;   // 64 full groups (4 a warp) and a tail warp
@@ -381,18 +416,25 @@ constexpr int kRotqMaxWarps = 17;   // 64 full groups (4 a warp) and a tail warp
 // one CTA an SM that loaded the next row during the current one).
 // TILED writes the codes as fp16 in the product's operand layout and records
 // the |code| and code-squared window sums for the product's exactness bound;
-// else int8 rows.  SWIGLU: the row is h = bf16(silu(g) * u), gate rows from X
-// and up rows from U.
+// else int8 rows.  PRE = kPreSwiglu: the row is h = bf16(silu(g) * u), gate
+// rows from X and up rows from U.  PRE = kPreNorm: the row is the modulated
+// layer norm h = bf16((x - mu) rstd (1 + scale) + shift), mu and the biased
+// variance var over the row in fp32 (two more CTA barriers: the sum, then the
+// sum of squared deviations, a two-pass variance), rstd = rsqrtf(var + eps),
+// the modulation read per column through the read-only cache.
 
 // CTAs an SM should hold, by warps a CTA: a thread keeps about 80 registers
 constexpr int rotq_min_blocks(int maxw) {
     return maxw <= 4 ? 6 : maxw <= 8 ? 3 : maxw <= 12 ? 2 : 1;
 }
-template <bool TILED, bool SWIGLU, int MAXW>
+template <bool TILED, int PRE, int MAXW>
 __global__ void __launch_bounds__(MAXW * 32, rotq_min_blocks(MAXW))
 k_rotq(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx, void *__restrict__ out,
-       float *__restrict__ sx, unsigned int *max_l1, const uint16_t *__restrict__ U, int64_t ldu) {
+       float *__restrict__ sx, unsigned int *max_l1, const uint16_t *__restrict__ U, int64_t ldu,
+       const float *__restrict__ shift, const float *__restrict__ scale, float eps) {
+    constexpr bool SWIGLU = PRE == kPreSwiglu;
     __shared__ float red[2][kRotqMaxWarps];
+    __shared__ float red_n[2][PRE == kPreNorm ? kRotqMaxWarps : 1];   // the norm's two sums
     __shared__ unsigned int win[2][16], winq[2][16];   // a row's window sums of |codes|, codes squared
     __shared__ unsigned int run_sh[2][5][32];           // warp 0's largest run sums over the rows
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -462,9 +504,56 @@ k_rotq(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx, void *
         float vt[8];
         int Et = 0;
         float amax = 0.0f;
+        const int64_t t0 = Gf * kGroup;
+        if (tail_warp) Et = load_tail_global<SWIGLU>(X + m * ldx + t0, SWIGLU ? U + m * ldu + t0 : nullptr, tail, vt);
+        if constexpr (PRE == kPreNorm) {
+            // mean, then the mean squared deviation, over the K values (the
+            // lanes of groups past K hold zeros and add nothing)
+            float s1 = 0.0f;
+            if (tail_warp) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s1 += e < Et ? vt[e] : 0.0f;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s1 += v[e];
+            }
+            const float mu = cta_sum(s1, red_n[0], W) / static_cast<float>(K);
+            float s2 = 0.0f;
+            if (tail_warp) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float d = vt[e] - mu;
+                    s2 = e < Et ? fmaf(d, d, s2) : s2;
+                }
+            } else if (active) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float d = v[e] - mu;
+                    s2 = fmaf(d, d, s2);
+                }
+            }
+            const float var = cta_sum(s2, red_n[1], W) / static_cast<float>(K);
+            const float rstd = rsqrtf(var + eps);
+            if (tail_warp) {
+                const int64_t c0 = t0 + static_cast<int64_t>(lane) * Et;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (e < Et) vt[e] = modnorm_value(vt[e], mu, rstd, __ldg(scale + c0 + e), __ldg(shift + c0 + e));
+            } else if (active) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 *sc4 = reinterpret_cast<const float4 *>(scale + col0 + kRun * i);
+                    const float4 *sh4 = reinterpret_cast<const float4 *>(shift + col0 + kRun * i);
+                    const float4 a = __ldg(sc4), b = __ldg(sc4 + 1), c = __ldg(sh4), d = __ldg(sh4 + 1);
+                    const float sc[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                    const float sh[8] = {c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[8 * i + e] = modnorm_value(v[8 * i + e], mu, rstd, sc[e], sh[e]);
+                }
+            }
+        }
         if (tail_warp) {
-            const int64_t t0 = Gf * kGroup;
-            Et = rotate_tail_global<SWIGLU>(X + m * ldx + t0, SWIGLU ? U + m * ldu + t0 : nullptr, tail, vt);
+            rotate_tail(tail, vt);
 #pragma unroll
             for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(vt[e]));
         } else {
@@ -599,9 +688,10 @@ k_rotq(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx, void *
     }
 }
 
-template <bool TILED, bool SWIGLU = false>
+template <bool TILED, int PRE = kPrePlain>
 tq_status launch_rotq(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void *out, float *sx,
-                      unsigned int *max_l1, cudaStream_t s, const uint16_t *U = nullptr, int64_t ldu = 0) {
+                      unsigned int *max_l1, cudaStream_t s, const uint16_t *U = nullptr, int64_t ldu = 0,
+                      const float *shift = nullptr, const float *scale = nullptr, float eps = 0.0f) {
     const int64_t Gf = K / kGroup;
     const int warps = static_cast<int>((Gf + 3) / 4) + (K % kGroup ? 1 : 0);
     if (warps < 1 || warps > kRotqMaxWarps) return TQ_ERR_SHAPE;
@@ -611,11 +701,11 @@ tq_status launch_rotq(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void
     if (ds != TQ_OK) return ds;
     // up to 16 warps (every row of at most 16384 columns but those of 63 full
     // groups and a tail) with the register budget of 512 threads
-    auto kern = warps <= 4    ? k_rotq<TILED, SWIGLU, 4>
-                : warps <= 8  ? k_rotq<TILED, SWIGLU, 8>
-                : warps <= 12 ? k_rotq<TILED, SWIGLU, 12>
-                : warps <= 16 ? k_rotq<TILED, SWIGLU, 16>
-                              : k_rotq<TILED, SWIGLU, kRotqMaxWarps>;
+    auto kern = warps <= 4    ? k_rotq<TILED, PRE, 4>
+                : warps <= 8  ? k_rotq<TILED, PRE, 8>
+                : warps <= 12 ? k_rotq<TILED, PRE, 12>
+                : warps <= 16 ? k_rotq<TILED, PRE, 16>
+                              : k_rotq<TILED, PRE, kRotqMaxWarps>;
     // persistent: as many CTAs as are resident at once
     int per_sm = 0;
     const cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, 0);
@@ -623,7 +713,7 @@ tq_status launch_rotq(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void
     per_sm = per_sm < 1 ? 1 : per_sm;
     const int64_t want = static_cast<int64_t>(dev.sms) * per_sm;
     const unsigned grid = static_cast<unsigned>(M < want ? M : want);
-    kern<<<grid, NT, 0, s>>>(X, M, K, ldx, out, sx, max_l1, U, ldu);
+    kern<<<grid, NT, 0, s>>>(X, M, K, ldx, out, sx, max_l1, U, ldu, shift, scale, eps);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
@@ -655,7 +745,18 @@ tq_status launch_swiglu_quant_tiled(const uint16_t *G, int64_t ldg, const uint16
                                                             tiled_act_tiles_bytes(M, K));
     const cudaError_t e = cudaMemsetAsync(max_l1, 0, 12 * sizeof(unsigned int), s);
     if (e != cudaSuccess) return cuda_fail(e);
-    return launch_rotq<true, true>(G, M, K, ldg, At, sx, max_l1, s, U, ldu);
+    return launch_rotq<true, kPreSwiglu>(G, M, K, ldg, At, sx, max_l1, s, U, ldu);
+}
+
+tq_status launch_modnorm_quant_tiled(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, const float *shift,
+                                     const float *scale, float eps, void *At, float *sx, cudaStream_t s) {
+    if (M == 0) return TQ_OK;
+    if (K > kRingMaxK) return TQ_ERR_SHAPE;
+    unsigned int *max_l1 = reinterpret_cast<unsigned int *>(static_cast<unsigned char *>(At) +
+                                                            tiled_act_tiles_bytes(M, K));
+    const cudaError_t e = cudaMemsetAsync(max_l1, 0, 12 * sizeof(unsigned int), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return launch_rotq<true, kPreNorm>(X, M, K, ldx, At, sx, max_l1, s, nullptr, 0, shift, scale, eps);
 }
 
 tq_status launch_rotate_quant_act(const uint16_t *X, int64_t M, int64_t K,

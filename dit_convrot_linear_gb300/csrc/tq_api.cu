@@ -7,6 +7,8 @@
 
 #include <limits.h>
 
+#include <cmath>
+
 #include "tq_internal.cuh"
 
 namespace tq {
@@ -363,6 +365,25 @@ tq_status tq_swiglu_quant_act_tiled(const void *G, int64_t ldg, const void *U, i
     if ((st = current_device(&dev)) != TQ_OK) return st;
     return launch_swiglu_quant_tiled(static_cast<const uint16_t *>(G), ldg, static_cast<const uint16_t *>(U),
                                      ldu, M, K, At, sx, stream);
+}
+
+tq_status tq_modnorm_quant_act_tiled(const void *X, int64_t M, int64_t K, int64_t ldx, const float *shift,
+                                     const float *scale, float eps, void *At, size_t at_bytes, float *sx,
+                                     cudaStream_t stream) {
+    if (M < 0 || !valid_k(K) || K > TQ_MAX_K_TILED) return TQ_ERR_SHAPE;
+    if (!(eps >= 0.0f) || !std::isfinite(eps)) return TQ_ERR_MODE;   // NaN, negative or infinite
+    if (M == 0) return TQ_OK;
+    tq_status st = check_bf16_rows(X, M, K, ldx);
+    if (st != TQ_OK) return st;
+    if (!shift || !scale || !At || !sx) return TQ_ERR_NULL;
+    const size_t need = tq_act_tiled_bytes(M, K);
+    if (need == 0) return TQ_ERR_OVERFLOW;
+    if (at_bytes < need) return TQ_ERR_WORKSPACE;
+    if (!aligned(At, 256) || !aligned(sx, 4) || !aligned(shift, 16) || !aligned(scale, 16)) return TQ_ERR_ALIGN;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    return launch_modnorm_quant_tiled(static_cast<const uint16_t *>(X), M, K, ldx, shift, scale, eps, At, sx,
+                                      stream);
 }
 
 tq_status tq_linear_tiled(const void *At, const float *sx, int64_t M, int64_t K, const void *Wq,

@@ -121,6 +121,8 @@ tq_status launch_rotate_quant_tiled(const uint16_t *X, int64_t M, int64_t K,
                                     int64_t ldx, void *At, float *sx, cudaStream_t s);
 tq_status launch_swiglu_quant_tiled(const uint16_t *G, int64_t ldg, const uint16_t *U, int64_t ldu,
                                     int64_t M, int64_t K, void *At, float *sx, cudaStream_t s);
+tq_status launch_modnorm_quant_tiled(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, const float *shift,
+                                     const float *scale, float eps, void *At, float *sx, cudaStream_t s);
 tq_status launch_gemm_a8_tiled(const void *At, const float *sx, int64_t M, int64_t K,
                                const uint8_t *Wq, const float *sw, int64_t N, int bits,
                                void *Y, int ytype, int64_t ldy, const DeviceInfo &dev,

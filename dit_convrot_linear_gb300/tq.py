@@ -41,6 +41,7 @@ SIGNATURES = {
     "tq_rotate_quant_act_tiled": (_C, [_P, _I, _I, _I, _P, _Z, _P, _P]),
     "tq_linear_tiled": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
     "tq_swiglu_quant_act_tiled": (_C, [_P, _I, _P, _I, _I, _I, _P, _Z, _P, _P]),
+    "tq_modnorm_quant_act_tiled": (_C, [_P, _I, _I, _I, _P, _P, ctypes.c_float, _P, _Z, _P, _P]),
     "tq_weights_tiled_bytes": (_Z, [_I, _I]),
     "tq_tile_weights": (_C, [_P, _I, _I, _C, _P, _Z, _P]),
     "tq_linear_tt": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
@@ -307,6 +308,30 @@ def rotate_quant_act_tiled(X, At=None, sx=None, stream=None):
     _req(sx, "sx", dtype=torch.float32, nbytes=4 * M)
     _check(lib().tq_rotate_quant_act_tiled(_ptr(X), M, K, X.stride(0), _ptr(At), _nbytes(At),
                                            _ptr(sx), _stream(stream)), "tq_rotate_quant_act_tiled")
+    return At, sx
+
+
+def modnorm_quant_act_tiled(X, shift, scale, eps=1e-6, At=None, sx=None, stream=None):
+    """A QKV or gate/up projection's input from the block input X (bf16
+    [M, K], any row stride) and its modulation (fp32 shift and scale [K]):
+    bf16((X - mean) / sqrt(var + eps) * (1 + scale) + shift) per row, rotated
+    and quantised into the tiled operand.  Returns (At, sx) for linear_tiled /
+    linear_tt."""
+    import torch
+    M, K = X.shape
+    need = act_tiled_bytes(M, K)
+    if At is None:
+        At = torch.empty(max(need, 1), dtype=torch.uint8, device=X.device)
+    if sx is None:
+        sx = torch.empty(M, dtype=torch.float32, device=X.device)
+    _req(X, "X", dtype=torch.bfloat16, rows=M, cols=K)
+    _req(shift, "shift", dtype=torch.float32, nbytes=4 * K)
+    _req(scale, "scale", dtype=torch.float32, nbytes=4 * K)
+    _req(At, "At", nbytes=need)
+    _req(sx, "sx", dtype=torch.float32, nbytes=4 * M)
+    _check(lib().tq_modnorm_quant_act_tiled(_ptr(X), M, K, X.stride(0), _ptr(shift), _ptr(scale), float(eps),
+                                            _ptr(At), _nbytes(At), _ptr(sx), _stream(stream)),
+           "tq_modnorm_quant_act_tiled")
     return At, sx
 
 

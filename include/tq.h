@@ -59,7 +59,7 @@ typedef enum {
     TQ_ERR_NULL = 1,        /* a required pointer is NULL */
     TQ_ERR_SHAPE = 2,       /* M, N, K, a stride or the group width is not allowed */
     TQ_ERR_BITS = 3,        /* bits is not 8 or 4 */
-    TQ_ERR_MODE = 4,        /* unknown mode / output type, or bits disagree with mode */
+    TQ_ERR_MODE = 4,        /* unknown mode / output type, bits disagree with mode, or eps out of range */
     TQ_ERR_OVERFLOW = 5,    /* a size product overflows 64 bits or a kernel index */
     TQ_ERR_ALIGN = 6,       /* a pointer or stride breaks the alignment rule */
     TQ_ERR_WORKSPACE = 7,   /* workspace missing or smaller than required */
@@ -241,6 +241,34 @@ tq_status tq_rotate_quant_act_tiled(const void *X, int64_t M, int64_t K, int64_t
  */
 tq_status tq_swiglu_quant_act_tiled(const void *G, int64_t ldg, const void *U, int64_t ldu, int64_t M,
                                     int64_t K, void *At, size_t at_bytes, float *sx, cudaStream_t stream);
+
+/*
+ * The modulated layer norm fused with tq_rotate_quant_act_tiled: the input of
+ * a DiT block's query/key/value or gate/up projection,
+ *   h = bf16((x - mu) / sqrt(var + eps) * (1 + scale) + shift),
+ * mu and var the mean and biased variance of the row x (a layer norm with no
+ * affine parameters of its own, modulated as in the adaptive layer norm of
+ * Peebles and Xie, "Scalable Diffusion Models with Transformers", 2023),
+ * rotated and quantised per token into the tiled operand.  The pages name the
+ * modulated layer norm among the row kernels next to the projections,
+ * candidates for fusion, and keep norms in fp32 (TensorFold PR #948, "What
+ * comes next" and its precision list); the modulation is shared by every
+ * block (same PR, "What it adds").  Fused, h (bf16 [M, K]) is neither
+ * written nor read again.  mu, var and h are computed in fp32 (two passes
+ * over the row held in registers) and h is rounded to bf16, as an unfused
+ * norm kernel would store it.  So a code may differ by one from the fp64
+ * reference, as for tq_rotate_quant_act.
+ *   X          as tq_rotate_quant_act; K <= TQ_MAX_K_TILED.
+ *   shift, scale  fp32 [K], 16-byte aligned: one modulation for all M rows
+ *              (rows with different modulations, such as the prompt rows and
+ *              image rows of a step, are separate calls).
+ *   eps        added to the variance; finite and >= 0, else TQ_ERR_MODE
+ *              (DiT blocks use 1e-6).
+ *   At, at_bytes, sx   as tq_rotate_quant_act_tiled.
+ */
+tq_status tq_modnorm_quant_act_tiled(const void *X, int64_t M, int64_t K, int64_t ldx, const float *shift,
+                                     const float *scale, float eps, void *At, size_t at_bytes, float *sx,
+                                     cudaStream_t stream);
 
 /*
  * The A8 product on a tiled operand: as tq_linear_q8 with At, sx from

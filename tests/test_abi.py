@@ -367,3 +367,27 @@ def test_blocked_refusals(L):
     assert lb(Y=FAKE + 2, yt=1) == DEVICE              # bf16 output: 2-byte alignment
     assert lb(ldy=100) == SHAPE
     assert lb(M=0) == OK and lb(N=0) == OK
+
+
+def test_modnorm_quant_refusals(L):
+    import ctypes
+    mq = lambda **k: L.tq_modnorm_quant_act_tiled(*[k.get(n, d) for n, d in (
+        ("X", FAKE), ("M", 4), ("K", 512), ("ldx", 512), ("shift", FAKE), ("scale", FAKE + 4096),
+        ("eps", ctypes.c_float(1e-6)), ("At", FAKE), ("at", 1 << 30), ("sx", FAKE), ("s", S0))])
+    assert mq(K=96) == SHAPE
+    assert mq(K=16384 + 256) == SHAPE                 # above TQ_MAX_K_TILED
+    assert mq(X=0) == NULL
+    assert mq(shift=0) == NULL
+    assert mq(scale=0) == NULL
+    assert mq(ldx=500) == SHAPE                       # ldx < K
+    assert mq(ldx=1028) == ALIGN                      # stride not a multiple of 8
+    assert mq(shift=FAKE + 4) == ALIGN                # modulation vectors 16-byte aligned
+    assert mq(scale=FAKE + 8) == ALIGN
+    assert mq(eps=ctypes.c_float(-1e-6)) == MODE
+    assert mq(eps=ctypes.c_float(float("nan"))) == MODE
+    assert mq(eps=ctypes.c_float(float("inf"))) == MODE
+    assert mq(At=0) == NULL
+    assert mq(at=100) == WORKSPACE
+    assert mq(At=FAKE + 16) == ALIGN
+    assert mq(M=0) == OK
+    assert mq(M=0, eps=ctypes.c_float(-1.0)) == MODE  # eps is checked even for an empty call
