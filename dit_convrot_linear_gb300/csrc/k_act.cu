@@ -271,6 +271,23 @@ __device__ __forceinline__ void bfly_x2(float &a0, float &a1, float &b0, float &
     f2unpack(d, b0, b1);
 }
 
+// modnorm_value on two values at once, each operation rounded as there (the
+// pair's sums and products on f32x2, one conversion to a bf16 pair).
+__device__ __forceinline__ void modnorm_pair(float &x0, float &x1, unsigned long long mu2, unsigned long long r2,
+                                             float sc0, float sc1, float sh0, float sh1) {
+    unsigned long long d, n, k, h;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2pack(x0, x1)), "l"(mu2));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(n) : "l"(d), "l"(r2));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(k) : "l"(f2pack(sc0, sc1)), "l"(f2pack(1.0f, 1.0f)));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(h) : "l"(n), "l"(k), "l"(f2pack(sh0, sh1)));
+    float h0, h1;
+    f2unpack(h, h0, h1);
+    uint32_t w;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(h1), "f"(h0));   // h0 in the low half
+    x0 = __uint_as_float(w << 16);
+    x1 = __uint_as_float(w & 0xFFFF0000u);
+}
+
 // Unnormalised transform (Hs_256 x, Sylvester order) of the group this lane's
 // 8-lane slice holds; in-lane value index bits are column bits 0-2 and 6-7.
 __device__ __forceinline__ void fwht_8x32(float (&v)[32]) {
@@ -391,18 +408,6 @@ __device__ __forceinline__ float modnorm_value(float x, float mu, float rstd, fl
     return __uint_as_float(static_cast<uint32_t>(f32_to_bf16_bits(fmaf((x - mu) * rstd, 1.0f + sc, sh))) << 16);
 }
 
-// Sum over the CTA's warps of one value a lane: the warp's sum goes to
-// slot[warp], and after the barrier every thread adds the W slots in order.
-__device__ __forceinline__ float cta_sum(float x, float *slot, int W) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if ((threadIdx.x & 31) == 0) slot[threadIdx.x >> 5] = x;
-    __syncthreads();
-    float t = slot[0];
-    for (int w = 1; w < W; ++w) t += slot[w];
-    return t;
-}
-
 constexpr int kRotqMaxWarps = 17;   // 64 full groups (4 a warp) and a tail warp
 
 // Rotation + per-token int8 quantisation, one token row per CTA at a time
@@ -419,9 +424,9 @@ constexpr int kRotqMaxWarps = 17;   // 64 full groups (4 a warp) and a tail warp
 // else int8 rows.  PRE = kPreSwiglu: the row is h = bf16(silu(g) * u), gate
 // rows from X and up rows from U.  PRE = kPreNorm: the row is the modulated
 // layer norm h = bf16((x - mu) rstd (1 + scale) + shift), mu and the biased
-// variance var over the row in fp32 (two more CTA barriers: the sum, then the
-// sum of squared deviations, a two-pass variance), rstd = rsqrtf(var + eps),
-// the modulation read per column through the read-only cache.
+// variance var over the row in fp32 (one more CTA barrier: two passes inside
+// each warp, then the warps' moments merged), rstd = rsqrtf(var + eps), the
+// modulation read per column through the read-only cache.
 
 // CTAs an SM should hold, by warps a CTA: a thread keeps about 80 registers
 constexpr int rotq_min_blocks(int maxw) {
@@ -430,11 +435,11 @@ constexpr int rotq_min_blocks(int maxw) {
 template <bool TILED, int PRE, int MAXW>
 __global__ void __launch_bounds__(MAXW * 32, rotq_min_blocks(MAXW))
 k_rotq(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx, void *__restrict__ out,
-       float *__restrict__ sx, unsigned int *max_l1, const uint16_t *__restrict__ U, int64_t ldu,
+       float *__restrict__ sx, unsigned int *trl, const uint16_t *__restrict__ U, int64_t ldu,
        const float *__restrict__ shift, const float *__restrict__ scale, float eps) {
     constexpr bool SWIGLU = PRE == kPreSwiglu;
     __shared__ float red[2][kRotqMaxWarps];
-    __shared__ float red_n[2][PRE == kPreNorm ? kRotqMaxWarps : 1];   // the norm's two sums
+    __shared__ float red_n[2][PRE == kPreNorm ? kRotqMaxWarps : 1];   // the warps' means and M2
     __shared__ unsigned int win[2][16], winq[2][16];   // a row's window sums of |codes|, codes squared
     __shared__ unsigned int run_sh[2][5][32];           // warp 0's largest run sums over the rows
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -507,32 +512,66 @@ k_rotq(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx, void *
         const int64_t t0 = Gf * kGroup;
         if (tail_warp) Et = load_tail_global<SWIGLU>(X + m * ldx + t0, SWIGLU ? U + m * ldu + t0 : nullptr, tail, vt);
         if constexpr (PRE == kPreNorm) {
-            // mean, then the mean squared deviation, over the K values (the
-            // lanes of groups past K hold zeros and add nothing)
+            // each warp's mean and sum of squared deviations over its own
+            // values (two passes inside the warp), merged after one barrier
+            // by the parallel formula of Chan, Golub and LeVeque (1979):
+            // mean = sum_w n_w m_w / K, M2 = sum_w (M2_w + n_w (m_w - mean)^2)
+            auto warp_n = [&](int w) {   // values warp w holds
+                const int64_t ng = Gf - 4 * static_cast<int64_t>(w);
+                return w < WF ? static_cast<float>((ng < 4 ? ng : 4) * kGroup) : static_cast<float>(tail);
+            };
             float s1 = 0.0f;
             if (tail_warp) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) s1 += e < Et ? vt[e] : 0.0f;
             } else {
+                unsigned long long acc = f2pack(v[0], v[1]);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s1 += v[e];
+                for (int e = 2; e < 32; e += 2)
+                    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(f2pack(v[e], v[e + 1])));
+                float a0, a1;
+                f2unpack(acc, a0, a1);
+                s1 = a0 + a1;
             }
-            const float mu = cta_sum(s1, red_n[0], W) / static_cast<float>(K);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+            const float mw = s1 / warp_n(warp);
             float s2 = 0.0f;
             if (tail_warp) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float d = vt[e] - mu;
+                    const float d = vt[e] - mw;
                     s2 = e < Et ? fmaf(d, d, s2) : s2;
                 }
             } else if (active) {
+                const unsigned long long m2w = f2pack(mw, mw);
+                unsigned long long acc = f2pack(0.0f, 0.0f);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float d = v[e] - mu;
-                    s2 = fmaf(d, d, s2);
+                for (int e = 0; e < 32; e += 2) {
+                    unsigned long long d;
+                    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2pack(v[e], v[e + 1])), "l"(m2w));
+                    asm("fma.rn.f32x2 %0, %1, %1, %0;" : "+l"(acc) : "l"(d));
                 }
+                float a0, a1;
+                f2unpack(acc, a0, a1);
+                s2 = a0 + a1;
             }
-            const float var = cta_sum(s2, red_n[1], W) / static_cast<float>(K);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+            if (lane == 0) {
+                red_n[0][warp] = mw;
+                red_n[1][warp] = s2;
+            }
+            __syncthreads();
+            float msum = 0.0f;
+            for (int w = 0; w < W; ++w) msum = fmaf(warp_n(w), red_n[0][w], msum);
+            const float mu = msum / static_cast<float>(K);
+            float m2 = 0.0f;
+            for (int w = 0; w < W; ++w) {
+                const float d = red_n[0][w] - mu;
+                m2 += fmaf(warp_n(w) * d, d, red_n[1][w]);
+            }
+            const float var = m2 / static_cast<float>(K);
             const float rstd = rsqrtf(var + eps);
             if (tail_warp) {
                 const int64_t c0 = t0 + static_cast<int64_t>(lane) * Et;
@@ -540,6 +579,7 @@ k_rotq(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx, void *
                 for (int e = 0; e < 8; ++e)
                     if (e < Et) vt[e] = modnorm_value(vt[e], mu, rstd, __ldg(scale + c0 + e), __ldg(shift + c0 + e));
             } else if (active) {
+                const unsigned long long mu2 = f2pack(mu, mu), r2 = f2pack(rstd, rstd);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float4 *sc4 = reinterpret_cast<const float4 *>(scale + col0 + kRun * i);
@@ -548,7 +588,8 @@ k_rotq(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx, void *
                     const float sc[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
                     const float sh[8] = {c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v[8 * i + e] = modnorm_value(v[8 * i + e], mu, rstd, sc[e], sh[e]);
+                    for (int e = 0; e < 8; e += 2)
+                        modnorm_pair(v[8 * i + e], v[8 * i + e + 1], mu2, r2, sc[e], sc[e + 1], sh[e], sh[e + 1]);
                 }
             }
         }
@@ -667,6 +708,10 @@ k_rotq(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx, void *
             // Trailer: word 1 + j the largest sum of |codes| over an aligned
             // run of 2^j windows, word 0 over a whole row (16 windows hold the
             // longest row); words 7 + j and 6 the same for codes squared.
+            // This CTA's maxima go into copy blockIdx % 16, once the kernel
+            // that zeroes the copies has finished (this launch's primary).
+            unsigned int *cp = trl + (blockIdx.x % kTrailerCopies) * kTrailerStride;
+            asm volatile("griddepcontrol.wait;" ::: "memory");
 #pragma unroll
             for (int j = 0; j < 5; ++j) {
                 unsigned int mx = run_sh[0][j][lane], mq = run_sh[1][j][lane];
@@ -675,22 +720,29 @@ k_rotq(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx, void *
                     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                     mq = max(mq, __shfl_xor_sync(0xffffffffu, mq, o));
                 }
-                if (lane == 0 && pending) {
-                    atomicMax(max_l1 + 1 + j, mx);
-                    atomicMax(max_l1 + 7 + j, mq);
-                    if (j == 4) {
-                        atomicMax(max_l1, mx);
-                        atomicMax(max_l1 + 6, mq);
-                    }
+                if (pending && lane == j) {
+                    atomicMax(cp + 1 + j, mx);
+                    atomicMax(cp + 7 + j, mq);
+                }
+                if (pending && j == 4 && lane == 5) {
+                    atomicMax(cp, mx);
+                    atomicMax(cp + 6, mq);
                 }
             }
         }
     }
 }
 
+// Zeroes a tiled operand's trailer copies; the rotation launched next is its
+// programmatic dependent, released at once.
+__global__ void __launch_bounds__(32) k_zero_trailer(unsigned int *trl) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int i = threadIdx.x; i < kTrailerCopies * kTrailerStride; i += 32) trl[i] = 0u;
+}
+
 template <bool TILED, int PRE = kPrePlain>
 tq_status launch_rotq(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void *out, float *sx,
-                      unsigned int *max_l1, cudaStream_t s, const uint16_t *U = nullptr, int64_t ldu = 0,
+                      unsigned int *trl, cudaStream_t s, const uint16_t *U = nullptr, int64_t ldu = 0,
                       const float *shift = nullptr, const float *scale = nullptr, float eps = 0.0f) {
     const int64_t Gf = K / kGroup;
     const int warps = static_cast<int>((Gf + 3) / 4) + (K % kGroup ? 1 : 0);
@@ -713,9 +765,26 @@ tq_status launch_rotq(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, void
     per_sm = per_sm < 1 ? 1 : per_sm;
     const int64_t want = static_cast<int64_t>(dev.sms) * per_sm;
     const unsigned grid = static_cast<unsigned>(M < want ? M : want);
-    kern<<<grid, NT, 0, s>>>(X, M, K, ldx, out, sx, max_l1, U, ldu, shift, scale, eps);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+    if constexpr (TILED) {
+        k_zero_trailer<<<1, 32, 0, s>>>(trl);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(NT);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, X, M, K, ldx, out, sx, trl, U, ldu, shift, scale, eps);
+        return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+    } else {
+        kern<<<grid, NT, 0, s>>>(X, M, K, ldx, out, sx, trl, U, ldu, shift, scale, eps);
+        const cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+    }
 }
 
 }  // namespace
@@ -724,39 +793,32 @@ int64_t tiled_act_tiles_bytes(int64_t M, int64_t K) {
     return ((M + 255) / 256) * 2 * ((K + 63) / 64) * 16384;
 }
 
-int64_t tiled_act_bytes(int64_t M, int64_t K) { return tiled_act_tiles_bytes(M, K) + 256; }
+int64_t tiled_act_bytes(int64_t M, int64_t K) { return tiled_act_tiles_bytes(M, K) + kTrailerBytes; }
+
+unsigned int *tiled_act_trailer(void *At, int64_t M, int64_t K) {
+    return reinterpret_cast<unsigned int *>(static_cast<unsigned char *>(At) + tiled_act_tiles_bytes(M, K));
+}
 
 tq_status launch_rotate_quant_tiled(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
                                     void *At, float *sx, cudaStream_t s) {
     if (M == 0) return TQ_OK;
     if (K > kRingMaxK) return TQ_ERR_SHAPE;
-    unsigned int *max_l1 = reinterpret_cast<unsigned int *>(static_cast<unsigned char *>(At) +
-                                                            tiled_act_tiles_bytes(M, K));
-    const cudaError_t e = cudaMemsetAsync(max_l1, 0, 12 * sizeof(unsigned int), s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    return launch_rotq<true>(X, M, K, ldx, At, sx, max_l1, s);
+    return launch_rotq<true>(X, M, K, ldx, At, sx, tiled_act_trailer(At, M, K), s);
 }
 
 tq_status launch_swiglu_quant_tiled(const uint16_t *G, int64_t ldg, const uint16_t *U, int64_t ldu,
                                     int64_t M, int64_t K, void *At, float *sx, cudaStream_t s) {
     if (M == 0) return TQ_OK;
     if (K > kRingMaxK) return TQ_ERR_SHAPE;
-    unsigned int *max_l1 = reinterpret_cast<unsigned int *>(static_cast<unsigned char *>(At) +
-                                                            tiled_act_tiles_bytes(M, K));
-    const cudaError_t e = cudaMemsetAsync(max_l1, 0, 12 * sizeof(unsigned int), s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    return launch_rotq<true, kPreSwiglu>(G, M, K, ldg, At, sx, max_l1, s, U, ldu);
+    return launch_rotq<true, kPreSwiglu>(G, M, K, ldg, At, sx, tiled_act_trailer(At, M, K), s, U, ldu);
 }
 
 tq_status launch_modnorm_quant_tiled(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, const float *shift,
                                      const float *scale, float eps, void *At, float *sx, cudaStream_t s) {
     if (M == 0) return TQ_OK;
     if (K > kRingMaxK) return TQ_ERR_SHAPE;
-    unsigned int *max_l1 = reinterpret_cast<unsigned int *>(static_cast<unsigned char *>(At) +
-                                                            tiled_act_tiles_bytes(M, K));
-    const cudaError_t e = cudaMemsetAsync(max_l1, 0, 12 * sizeof(unsigned int), s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    return launch_rotq<true, kPreNorm>(X, M, K, ldx, At, sx, max_l1, s, nullptr, 0, shift, scale, eps);
+    return launch_rotq<true, kPreNorm>(X, M, K, ldx, At, sx, tiled_act_trailer(At, M, K), s, nullptr, 0, shift,
+                                       scale, eps);
 }
 
 tq_status launch_rotate_quant_act(const uint16_t *X, int64_t M, int64_t K,

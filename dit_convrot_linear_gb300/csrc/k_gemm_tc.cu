@@ -109,11 +109,11 @@ struct TcParams {
     int mtiles, ntiles, ksteps, chunk_steps;
     unsigned int *status;
     const unsigned char *At;   // pre-tiled fp16 A codes (AT path), else null
-    const unsigned int *max_l1;  // largest row sum of |A codes| (tiled operand), or null; word 6:
-                                 // the largest row sum of A codes squared
+    const unsigned int *a_trl;   // the tiled operand's trailer of bounds (word 0 the largest row
+                                 // sum of |A codes|, word 6 of A codes squared), or null
     const unsigned int *w_sq;    // largest row sum of B codes squared (tiled weights), or null;
                                  // word 1 + j: per aligned window of 1024 * 2^j columns
-                                 // (max_l1[7 + j] the same for A)
+                                 // (A's words 1 + j and 7 + j the same)
     // epilogue: Y = R + g[n] * (sx sw acc + b[n]); any of them may be absent
     const float *bias, *gate;
     const void *R;
@@ -290,6 +290,7 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     //       acc_full[2], acc_empty[2] (CTA 0), done, a_full[O] (AT)
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
+    __shared__ unsigned int a_bound[12];   // the A trailer's bounds, read once per CTA
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint32_t rank;
@@ -327,6 +328,7 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         abort_sh = 0;
     }
+    if (warp == 1 && lane < 12 && p.a_trl) a_bound[lane] = trailer_bound(p.a_trl, lane);
     if (warp == MMA_WARP) {
         asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_u32(&tmem_base_sh)), "r"(TMEM_COLS));
@@ -350,19 +352,19 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     const double qmax = BITS == 8 ? 127.0 : 7.0;
     int cs = p.chunk_steps;
     bool single = p.ksteps <= cs;
-    if (!single && p.max_l1) {
-        single = static_cast<double>(p.max_l1[0]) * qmax < 16777216.0;
+    if (!single && p.a_trl) {
+        single = static_cast<double>(a_bound[0]) * qmax < 16777216.0;
         // or by Cauchy-Schwarz: any partial sum is at most sum |a_k| |b_k| <=
         // |a|_2 |b|_2, so the largest row sums of squares on both sides with a
         // product below 2^48 keep every partial sum below 2^24 (the product of
         // two integers below 2^32 rounds in double, but not below 2^48 when
         // it is at least 2^48)
         if (!single && p.w_sq)
-            single = static_cast<double>(p.max_l1[6]) * static_cast<double>(p.w_sq[0]) < 281474976710656.0;
+            single = static_cast<double>(a_bound[6]) * static_cast<double>(p.w_sq[0]) < 281474976710656.0;
         for (int j = 4; j >= 0 && !single; --j) {
             const int steps = (1024 << j) / BK;
-            if (steps > cs && (static_cast<double>(p.max_l1[1 + j]) * qmax < 16777216.0 ||
-                               (p.w_sq && static_cast<double>(p.max_l1[7 + j]) *
+            if (steps > cs && (static_cast<double>(a_bound[1 + j]) * qmax < 16777216.0 ||
+                               (p.w_sq && static_cast<double>(a_bound[7 + j]) *
                                                   static_cast<double>(p.w_sq[1 + j]) < 281474976710656.0))) {
                 cs = steps;
                 break;
@@ -949,7 +951,7 @@ tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const unsigned ch
     p.chunk_steps = bits == 8 ? 1024 / BK : 16384 / BK;
     p.status = status;
     p.At = At;
-    p.max_l1 = AT ? reinterpret_cast<const unsigned int *>(At + tiled_act_tiles_bytes(M, K)) : nullptr;
+    p.a_trl = AT ? tiled_act_trailer(const_cast<unsigned char *>(At), M, K) : nullptr;
     p.w_sq = (MODE == 2 && Wt) ? reinterpret_cast<const unsigned int *>(static_cast<const unsigned char *>(Wt) +
                                                                         weights_tiled_bytes(N, K) - 256)
                                : nullptr;

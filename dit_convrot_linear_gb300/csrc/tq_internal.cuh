@@ -82,9 +82,28 @@ tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M,
 // order (core matrix (r/8, k/8) is 128 contiguous bytes, K-adjacent ones 128
 // bytes apart, row groups 1024 bytes apart).  Rows are padded to a whole
 // number of 256-row tile pairs; columns past K inside the last tile are zero.
-// After the tiles (at byte tiled_act_tiles_bytes), a 256-byte trailer whose
-// first word is the largest sum of |codes| over the rows, word 1 + j the
-// largest such sum over an aligned window of 1024 << j columns (j < 5).
+// After the tiles (at byte tiled_act_tiles_bytes), a 2048-byte trailer of 12
+// bounds: word 0 the largest sum of |codes| over the rows, word 1 + j the
+// largest such sum over an aligned window of 1024 << j columns (j < 5), words
+// 6 and 7 + j the same for codes squared.  It holds 16 copies of the 12 words,
+// 128 bytes apart: each CTA of the rotation takes the atomic maximum into copy
+// blockIdx % 16 (so that the CTAs' atomics spread over 16 lines), and a reader
+// takes the maximum over the copies.  The copies are zeroed by a one-warp
+// kernel launched just before the rotation, which the rotation follows as a
+// programmatic dependent: its rows run while the zeroing does, and it waits
+// for it (griddepcontrol.wait) only before its atomics.
+constexpr int kTrailerCopies = 16;
+constexpr int kTrailerStride = 32;       // 32-bit words between copies
+constexpr int kTrailerBytes = kTrailerCopies * kTrailerStride * 4;
+unsigned int *tiled_act_trailer(void *At, int64_t M, int64_t K);
+
+// Bound j of a tiled operand's trailer: the maximum over its copies.
+__device__ __forceinline__ unsigned int trailer_bound(const unsigned int *trl, int j) {
+    unsigned int best = 0u;
+#pragma unroll
+    for (int c = 0; c < kTrailerCopies; ++c) best = max(best, trl[c * kTrailerStride + j]);
+    return best;
+}
 bool make_map_u8(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int box_cols,
                  int box_rows, CUtensorMapSwizzle swz);
 

@@ -72,3 +72,12 @@ def untile_codes(At, M, K, rows=None):
     k = np.arange(K)[None, :]
     idx = ((m // 128) * KT + k // 64) * 8192 + (((m % 128) // 8) * 8 + (k % 64) // 8) * 64 + (m % 8) * 8 + k % 8
     return h[idx].astype(np.int64)
+
+
+def act_trailer(tq, At, M, K):
+    """The 12 bounds of a tiled activation operand's trailer (the library's
+    private layout, decoded for tests): after the tiles, 16 copies 128 bytes
+    apart of 12 32-bit words; bound j is the maximum over the copies."""
+    start = tq.act_tiled_bytes(M, K) - 2048
+    raw = to_np(At[start:start + 2048]).view(np.uint32).reshape(16, 32)
+    return raw[:, :12].max(axis=0).astype(np.int64)

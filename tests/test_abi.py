@@ -136,7 +136,7 @@ def test_tiled_refusals(L):
     assert L.tq_act_tiled_bytes(4, 16384 + 256) == 0          # above TQ_MAX_K_TILED
     assert L.tq_act_tiled_bytes(4, 500) == 0
     need = L.tq_act_tiled_bytes(300, 3072)
-    assert need == 4 * 48 * 16384 + 256  # rows padded to two 256-row tile pairs, 48 K steps; trailer
+    assert need == 4 * 48 * 16384 + 2048  # rows padded to two 256-row tile pairs, 48 K steps; trailer
     r = L.tq_rotate_quant_act_tiled
     assert r(FAKE, 4, 16384 + 256, 16384 + 256, FAKE, 1 << 30, FAKE, S0) == SHAPE
     assert r(FAKE, 4, 512, 512, 0, 1 << 20, FAKE, S0) == NULL

@@ -28,8 +28,8 @@ import pytest
 
 import oracle
 from dit_convrot_linear_gb300 import synth
-from helpers import (CODE_FLIP_FRAC, REL_L2_Y, SCALE_REL, check_codes_close, rel_l2, to_dev_bf16,
-                     to_np, untile_codes)
+from helpers import (CODE_FLIP_FRAC, REL_L2_Y, SCALE_REL, act_trailer, check_codes_close, rel_l2,
+                     to_dev_bf16, to_np, untile_codes)
 
 pytestmark = pytest.mark.gpu
 
@@ -160,7 +160,7 @@ def test_modnorm_fused_operand_full_size_sampled(tq):
     rows = np.sort(np.random.default_rng(13).choice(M, 48, replace=False))
     _check(tq, X, shift, scale, At, sx, rows=rows)
     codes = untile_codes(At, M, K, rows=rows)
-    tr = to_np(At[tq.act_tiled_bytes(M, K) - 256:]).view(np.uint32)
+    tr = act_trailer(tq, At, M, K)
     assert int(tr[0]) >= int(np.abs(codes).sum(axis=1).max())
     assert int(tr[6]) >= int((codes * codes).sum(axis=1).max())
 

@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 from dit_convrot_linear_gb300 import synth
-from helpers import (CODE_FLIP_FRAC, REL_L2_Y, SCALE_REL, ULP_FLIP_FRAC, bf16_bits,
+from helpers import (CODE_FLIP_FRAC, REL_L2_Y, SCALE_REL, ULP_FLIP_FRAC, act_trailer, bf16_bits,
                      bf16_ulp_diff, check_codes_close, parity_report, rel_l2, untile_codes,
                      to_dev_bf16, to_np)
 
@@ -282,7 +282,7 @@ def test_tiled_trailers_hold_the_largest_row_sums_of_squares(tq, M, N, K, bits):
     codes, sw = gpu_weights(tq, wgen(f"gpu/trail/w{N}x{K}", N, K, WD if bits == 8 else WB), bits)
     At, sx = tq.rotate_quant_act_tiled(X)
     a = untile_codes(At, M, K).astype(np.int64)
-    at_tr = to_np(At[tq.act_tiled_bytes(M, K) - 256:]).view(np.uint32)
+    at_tr = act_trailer(tq, At, M, K)
     def window_max(v, j):          # largest sum over an aligned run of 2^j 1024-column windows
         L = 1024 << j
         pad = np.zeros((v.shape[0], -v.shape[1] % L), dtype=np.int64)
@@ -413,7 +413,7 @@ def test_swiglu_fused_operand_full_size_sampled(tq):
     rq, rs = oracle.swiglu_quant_act(G[rows], U[rows])
     check_codes_close(codes, rq, frac=CODE_FLIP_FRAC)
     assert np.max(np.abs(to_np(sx)[rows].astype(np.float64) / np.where(rs == 0, 1, rs) - 1)) <= SCALE_REL
-    tr = to_np(At[tq.act_tiled_bytes(M, K) - 256:]).view(np.uint32)
+    tr = act_trailer(tq, At, M, K)
     assert int(tr[0]) >= int(np.abs(codes).sum(axis=1).max())     # a maximum over all rows
     assert int(tr[6]) >= int((codes * codes).sum(axis=1).max())
 
