@@ -39,6 +39,27 @@ TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# One kernel on one shape, for ncu captures (--only case --case NAME): the
+# set-up runs first, then --steps launches of the named operation with a
+# synchronize after each (so `ncu -k <kernel> -s <n> -c 1` picks one launch
+# past the set-up).  name: (description, kernel regex for ncu)
+PROFILE_CASES = {
+    "tt8_up": ("DiT FFN up W8A8, M=4032 N=12288 K=3072, both operands tiled, split workspace",
+               "k_gemm_a8_tc"),
+    "tt8_down": ("DiT FFN down W8A8, M=4032 N=3072 K=12288, both operands tiled, split workspace",
+                 "k_gemm_a8_tc"),
+    "tt4_qkv": ("DiT chain QKV W4A8, M=1024 N=9216 K=3072, both operands tiled", "k_gemm_a8_tc"),
+    "tt4_down": ("DiT chain down W4A8, M=1024 N=3072 K=12288, both operands tiled, split tiles",
+                 "k_gemm_a8_tc"),
+    "rot_modnorm": ("modulated norm + rotation + int8 tiled operand, M=4032 K=3072", "k_rotq"),
+    "rot_swiglu": ("SwiGLU + rotation + int8 tiled operand, M=4032 K=12288", "k_rotq"),
+    "rot_tiled": ("rotation + int8 tiled operand, M=4032 K=12288", "k_rotq"),
+    "skinny_m64": ("batched W4A16 on the tensor cores, M=64 N=12288 K=4096", "k_skinny_tc"),
+    "skinny_m8": ("batched W4A16 on the tensor cores, M=8 N=4096 K=12288", "k_skinny_tc"),
+    "gemv_m1": ("decode W4A16 CUDA-core product, M=1 N=12288 K=4096", "k_gemv"),
+}
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -48,10 +69,13 @@ def parse_args():
     ap.add_argument("--calls", type=int, default=1000)
     ap.add_argument("--skip-dit", action="store_true")
     ap.add_argument("--only", default="all",
-                    choices=["all", "decode", "dit", "blocked", "batched", "chain", "modnorm"],
+                    choices=["all", "decode", "dit", "blocked", "batched", "chain", "modnorm", "case"],
                     help="profiling cases: only the W8A16 decode graph, only the DiT GEMMs, only "
                          "the block-scaled decode products, only the batched W4A16 decode, only "
-                         "the DiT block chain, or only the fused modulated-norm operand")
+                         "the DiT block chain, only the fused modulated-norm operand, or one "
+                         "kernel on one shape (--case)")
+    ap.add_argument("--case", default="tt8_up", choices=sorted(PROFILE_CASES),
+                    help="with --only case: the kernel and shape to run --steps times")
     ap.add_argument("--dit-m", type=int, default=4032, help="token rows of the DiT case")
     ap.add_argument("--skip-cpu", action="store_true")
     return ap.parse_args()
@@ -585,7 +609,9 @@ def batched_measure(device, steps, warmup, world, l2, hbm, bf16_peak):
                                      "roof_tflops": round(roof, 2)},
                         "per_projection": per}
         del xs, ys, g
-    out["kernels"] = "k_gemv_small<4> (M <= 8), k_gemv_a16<4> (M = 32, 64; cluster split-K)"
+    out["kernels"] = ("k_gemv_small<4> (M = 1: the CUDA-core kernel, faster for one token); "
+                      "k_rotate_tiles16 (x' pre-pass) + k_skinny_tc<4> (M = 8, 32, 64: tcgen05, "
+                      "A operand from TMEM, cluster split-K)")
     return out
 
 
@@ -713,6 +739,64 @@ def swiglu_measure(device, reps=5, M=4032, K=12288):
             "fused_gbs": round(fused_bytes / (med["fused"] * 1e-3) / 1e9, 1),
             "rotation_of_h_ms": round(med["rotation_of_h"], 4),
             "fused_bytes": fused_bytes, "unfused_bytes": 10 * M * K}
+
+
+def profile_case(device, name, steps):
+    """Runs one PROFILE_CASES entry: set-up, then `steps` launches of its
+    operation, each followed by a synchronize; returns the median time."""
+    import numpy as np
+    import torch
+    from dit_convrot_linear_gb300 import synth, tq
+    XD, WD, WB = (1.0, 0.002, 40.0), (0.02, 0.01, 20.0), (0.015, 0.005, 30.0)
+
+    def xw(M, N, K, bits):
+        X = bf16_dev(synth.tensor(f"case/{name}/x", M, K, *XD), device)
+        W = bf16_dev(synth.tensor(f"case/{name}/w", N, K, *(WD if bits == 8 else WB)), device)
+        codes, sw = tq.quantize_weights(W, bits)
+        return X, codes, sw
+
+    if name.startswith("tt"):
+        M, N, K, bits = {"tt8_up": (4032, 12288, 3072, 8), "tt8_down": (4032, 3072, 12288, 8),
+                         "tt4_qkv": (1024, 9216, 3072, 4), "tt4_down": (1024, 3072, 12288, 4)}[name]
+        X, codes, sw = xw(M, N, K, bits)
+        At, sx = tq.rotate_quant_act_tiled(X)
+        Wt = tq.tile_weights(codes, N, K, bits)
+        ws = tq.split_workspace()
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        op = lambda: tq.linear_tt(At, sx, M, K, Wt, sw, N, bits, Y=Y, out="bf16", split=ws)
+    elif name.startswith("rot"):
+        M, K = (4032, 3072) if name == "rot_modnorm" else (4032, 12288)
+        X = bf16_dev(synth.tensor(f"case/{name}/x", M, K, *XD), device)
+        At, sx = tq.rotate_quant_act_tiled(X)
+        if name == "rot_modnorm":
+            rng = np.random.default_rng(21)
+            shift = torch.from_numpy(rng.normal(0.0, 0.5, K).astype(np.float32)).to(device)
+            scale = torch.from_numpy(rng.normal(0.0, 0.3, K).astype(np.float32)).to(device)
+            op = lambda: tq.modnorm_quant_act_tiled(X, shift, scale, 1e-6, At=At, sx=sx)
+        elif name == "rot_swiglu":
+            G = bf16_dev(synth.tensor(f"case/{name}/g", M, K, 1.5, 0.0, 1.0), device)
+            op = lambda: tq.swiglu_quant_act_tiled(G, X, At=At, sx=sx)
+        else:
+            op = lambda: tq.rotate_quant_act_tiled(X, At=At, sx=sx)
+    else:
+        M, N, K = {"skinny_m64": (64, 12288, 4096), "skinny_m8": (8, 4096, 12288),
+                   "gemv_m1": (1, 12288, 4096)}[name]
+        X, codes, sw = xw(M, N, K, 4)
+        Y = torch.empty((M, N), dtype=torch.float32, device=device)
+        need = tq.linear_workspace_bytes(M, K, N, 4, "W4A16")
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device) if need else None
+        op = lambda: tq.linear(X, codes, sw, N, 4, "W4A16", Y=Y, workspace=ws)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        op()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return {"case": name, "what": PROFILE_CASES[name][0], "kernel": PROFILE_CASES[name][1],
+            "launches": steps, "median_us": round(statistics.median(times) * 1e3, 2)}
 
 
 def modnorm_measure(device, reps=5, M=4032, K=3072, hbm_peak=None):
@@ -875,6 +959,12 @@ def main():
             print(json.dumps({"case": f"dit W8A8 M={args.dit_m}",
                               **{k: round(v, 2) for k, v in tops.items()}, "per_projection": per,
                               "swiglu_operand": sw, "modnorm_operand": mn}))
+        return 0
+
+    if args.only == "case":   # one kernel on one shape, for ncu
+        res = profile_case(device, args.case, args.steps)
+        if rank == 0:
+            print(json.dumps(res))
         return 0
 
     if args.only == "modnorm":   # profiling case: the fused modulated-norm operand alone

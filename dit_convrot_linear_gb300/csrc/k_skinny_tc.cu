@@ -530,9 +530,18 @@ int64_t skinny_tc_workspace(int64_t M, int64_t K) {
     return (ks * skinny_tc_mp(M) * SK_BK * 2 + 255) / 256 * 256 + 256;
 }
 
+// Where the tensor-core product beats the CUDA-core kernels (measured with
+// 4-bit weights of 12288 x 4096 and 4096 x 12288, calls back to back): from
+// three tokens on for matrices of at least 2^24 weights (27.5 against 32 to
+// 43 us at M = 4), and at two tokens when N >= K (27.6 against 34.9 us; 30.5
+// against 27.5 us the other way); a single token streams faster through the
+// CUDA-core kernel (24.5 and 19.8 us against 27.4 and 30.5 us).  Below 2^24
+// weights the CUDA-core kernels keep M <= 8.
 bool skinny_tc_applies(int64_t M, int64_t N, int64_t K) {
     if (M < 1 || M > SK_MAXMP || K > TQ_MAX_K_TILED) return false;
-    return M > 8 || N * K >= (int64_t(1) << 24);
+    if (M > 8) return true;
+    if (N * K < (int64_t(1) << 24) || M == 1) return false;
+    return M >= 3 || N >= K;
 }
 
 // One wave of CTAs (at most a tile of 256 rows per SM): a later wave could
