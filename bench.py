@@ -69,11 +69,12 @@ def parse_args():
     ap.add_argument("--calls", type=int, default=1000)
     ap.add_argument("--skip-dit", action="store_true")
     ap.add_argument("--only", default="all",
-                    choices=["all", "decode", "dit", "blocked", "batched", "chain", "modnorm", "case"],
+                    choices=["all", "decode", "dit", "blocked", "batched", "chain", "modnorm", "case",
+                             "decode_chain"],
                     help="profiling cases: only the W8A16 decode graph, only the DiT GEMMs, only "
                          "the block-scaled decode products, only the batched W4A16 decode, only "
-                         "the DiT block chain, only the fused modulated-norm operand, or one "
-                         "kernel on one shape (--case)")
+                         "the DiT block chain, only the fused modulated-norm operand, one "
+                         "kernel on one shape (--case), or only the dependent decode chain")
     ap.add_argument("--case", default="tt8_up", choices=sorted(PROFILE_CASES),
                     help="with --only case: the kernel and shape to run --steps times")
     ap.add_argument("--dit-m", type=int, default=4032, help="token rows of the DiT case")
@@ -349,6 +350,74 @@ class Decode:
             e1.synchronize()
             times.append(e0.elapsed_time(e1) * 1e3)
         return statistics.median(times)
+
+
+class DecodeChain:
+    """A dependent decode chain, M=1: through the layer sets, gate (896 ->
+    4864) then down (4864 -> 896), each call's input the previous call's bf16
+    output, so no call can start its product before the previous one ends
+    (its weights still stream early: the per-call kernels copy them before
+    waiting on the previous launch).  Synthetic weights: each matrix's row
+    scales are multiplied by 1 / sqrt(mean_n sum_k w_nk^2), so that a call
+    keeps its input's RMS and the chain stays finite; the rest as the decode
+    workload.  One CUDA graph of 2 x layers launches."""
+
+    def __init__(self, bits, device, l2_bytes):
+        import torch
+        from dit_convrot_linear_gb300 import synth, tq
+        self.bits, self.mode = bits, ("W8A16" if bits == 8 else "W4A16")
+        w = synth.DECODE
+        self.projs = [w.projs[0], w.projs[2]]          # gate, down
+        self.layers = decode_layers(bits, l2_bytes)
+        self.weights = []
+        for L in range(self.layers):
+            for p in self.projs:
+                codes, sw = tq.quantize_weights(bf16_dev(w.weight(L, p), device), bits)
+                # the row norms from the codes, widened here (set-up only; low nibble = even k)
+                if bits == 4:
+                    c = codes.view(torch.uint8).to(torch.int16)
+                    lo, hi = c & 15, (c >> 4) & 15
+                    lo, hi = torch.where(lo > 7, lo - 16, lo), torch.where(hi > 7, hi - 16, hi)
+                    q = torch.stack([lo, hi], dim=-1).reshape(p.N, p.K).float()
+                else:
+                    q = codes.view(torch.int8).view(p.N, p.K).float()
+                gain2 = torch.mean(sw.double() ** 2 * (q.double() ** 2).sum(dim=1))
+                self.weights.append((p, codes, (sw.double() / torch.sqrt(gain2)).float()))
+        self.x0 = bf16_dev(w.activation(0, self.projs[0], 1), device)
+        self.bufs = [torch.empty((1, p.N), dtype=torch.bfloat16, device=device) for p in self.projs]
+        self.weight_bytes = sum(p.N * p.K * bits // 8 + 4 * p.N for (p, _, _) in self.weights)
+        self.calls = len(self.weights)
+        torch.cuda.synchronize()
+
+    def run(self, record=None):
+        from dit_convrot_linear_gb300 import tq
+        x = self.x0
+        for i, (p, codes, sw) in enumerate(self.weights):
+            y = self.bufs[i % 2]
+            tq.linear(x, codes, sw, p.N, self.bits, self.mode, Y=y, out="bf16")
+            if record is not None:
+                record.append((x.clone(), y.clone()))
+            x = y
+
+
+def chain_decode_measure(device, steps, warmup, world, l2, hbm):
+    """Both formats' dependent chains: weight GB/s over the chain and the
+    time per call."""
+    import torch
+    out = {}
+    for bits in (8, 4):
+        ch = DecodeChain(bits, device, l2)
+        g = graph_of(ch.run)
+        n = max(20, steps // 5)
+        ms = time_steps(g.replay, n, max(3, warmup), world) / n
+        gbs = ch.weight_bytes / (ms * 1e-3) / 1e9
+        out[f"w{bits}a16"] = {"value": round(gbs * world, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+                              "frac": round(gbs / hbm, 4), "calls_per_step": ch.calls,
+                              "us_per_call": round(ms * 1e3 / ch.calls, 2), "layers": ch.layers}
+        del ch, g
+        torch.cuda.empty_cache()
+    out["kernels"] = "k_gemv_small (gate) + k_gemv_rows8 (down), one launch a call, programmatic dependent launches"
+    return out
 
 
 def blocked_measure(device, steps, warmup, world, calls, l2, hbm):
@@ -961,6 +1030,12 @@ def main():
                               "swiglu_operand": sw, "modnorm_operand": mn}))
         return 0
 
+    if args.only == "decode_chain":   # the dependent decode chain alone
+        res = chain_decode_measure(device, args.steps, args.warmup, world, l2, float(pk["hbm_gbs"]))
+        if rank == 0:
+            print(json.dumps({"case": "dependent decode chain M=1", **res}))
+        return 0
+
     if args.only == "case":   # one kernel on one shape, for ncu
         res = profile_case(device, args.case, args.steps)
         if rank == 0:
@@ -1041,6 +1116,11 @@ def main():
         torch.cuda.empty_cache()
     except Exception as exc:  # reported, never hidden
         extra["decode_w4a16"] = {"error": repr(exc)}
+    if args.only != "decode":
+        try:
+            extra["decode_chain_dependent"] = chain_decode_measure(device, args.steps, args.warmup, world, l2, hbm)
+        except Exception as exc:  # reported, never hidden
+            extra["decode_chain_dependent"] = {"error": repr(exc)}
 
     if args.only != "decode":
         try:
