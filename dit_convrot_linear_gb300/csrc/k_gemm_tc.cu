@@ -902,11 +902,13 @@ k_gemm_a8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
 // through a tensor map), At pre-tiled fp16 codes, or At and Wt both pre-tiled
 // (each read as rows of 128 bytes, one 16 KB tile a box).
 // Split tiles (when the caller gives a split workspace) only where it was
-// measured to pay: fewer tiles than CTA pairs (one partial wave) and a long K.
-// Each piece costs a pipeline start, a drain and, for a partial, 128 KB stored
-// or added per CTA, so short K and full waves lose: measured on 4-bit weights
-// at M = 1024, 48 tiles, K = 12288: 70.9 -> 61.6 us; K = 3072: 29.9 -> 31.9 us;
-// 384 tiles (five waves and four tiles), K = 3072: 106.3 -> 107.8 us.
+// measured to pay: the tiles of a last wave that leaves pairs idle, and a long
+// K.  Each piece costs a pipeline start, a drain and, for a partial, 128 KB
+// stored or added per CTA, so short K and full waves lose: measured on 4-bit
+// weights at M = 1024, 48 tiles, K = 12288: 70.9 -> 61.6 us; K = 3072: 29.9 ->
+// 31.9 us; 384 tiles (five waves and four tiles), K = 3072: 106.3 -> 107.8
+// us (the last wave's four tiles split: 144.9); 8-bit, M = 4032, 768 tiles,
+// K = 3072: 186.4 -> 205.5 us.
 constexpr double kSplitBelow = 0.85;
 constexpr int kSplitMinKSteps = 96;
 
@@ -988,13 +990,17 @@ tq_status launch_tc(const int8_t *Xq, const unsigned char *At, const unsigned ch
     p.sk_units = 0;
     p.sk_flags = nullptr;
     p.sk_slots = nullptr;
-    if (split_ws && pmax > 0) {
-        // One partial wave: the K steps of all tiles are split evenly over
-        // every pair (at least two K steps a pair).
-        if (tiles < pmax && p.ksteps >= kSplitMinKSteps &&
-            static_cast<double>(tiles) < kSplitBelow * static_cast<double>(pmax)) {
-            const int64_t dp = 0;
-            const int64_t units = tiles * p.ksteps;
+    if (split_ws && pmax > 0 && p.ksteps >= kSplitMinKSteps) {
+        // The tiles of the whole waves stay whole; the K steps of the tiles of
+        // a last wave that would leave more than 15% of the pairs idle are
+        // split evenly over every pair (at least two K steps a pair).  With
+        // fewer tiles than pairs that is every tile.  Measured on the DiT down
+        // projection (192 tiles on 76 pairs, K = 12288, 8-bit): 189.5 against
+        // 201.8 us; splitting one more wave, 198.7.
+        const int64_t rem = tiles % pmax;
+        if (rem > 0 && static_cast<double>(rem) < kSplitBelow * static_cast<double>(pmax)) {
+            const int64_t dp = tiles - rem;
+            const int64_t units = rem * p.ksteps;
             if (units >= 2 * pmax) {
                 p.sk_dp_tiles = static_cast<int>(dp);
                 p.sk_units = units;

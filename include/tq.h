@@ -350,17 +350,19 @@ tq_status tq_linear_tt_ex(const void *At, const float *sx, int64_t M, int64_t K,
 size_t tq_split_workspace_bytes(void);
 
 /*
- * tq_linear_tt_ex with the tiles of the last waves split along K.  The
+ * tq_linear_tt_ex with the tiles of the last wave split along K.  The
  * projections are most of a DiT step (TensorFold PR #948, "What comes next":
  * about 80% of the GPU time); a product whose 256 x 256 output tiles leave the
- * last wave of CTA pairs mostly idle (the out and down projections of a
- * 1024-token block are 48 tiles) spends that share of its time with part of
- * the tensor cores unused.  With a workspace, the K steps of those tiles are
- * shared evenly by every pair; a pair that holds only part of a tile stores
- * its exact int32 partial sums, and the pair that holds the tile's last K step
- * adds them before the epilogue.  The sums are integers, so the result is
- * bit-identical to tq_linear_tt_ex, whatever the split (the library decides
- * it from the tile count).
+ * last wave of CTA pairs partly idle (the down projection of a 1024-token
+ * block is 48 tiles, of a 4032-token one 192 = 2 x 76 + 40) spends that share
+ * of its time with part of the tensor cores unused.  With a workspace, the
+ * tiles of the whole waves stay whole and the K steps of the last wave's
+ * tiles are shared evenly by every pair; a pair that holds only part of a
+ * tile stores its exact int32 partial sums, and the pair that holds the
+ * tile's last K step adds them before the epilogue.  The sums are integers, so
+ * the result is bit-identical to tq_linear_tt_ex, whatever the split (the
+ * library decides it from the tile count and K: long K only, where it was
+ * measured to pay).
  *
  *   workspace  tq_split_workspace_bytes() bytes of device memory, 256-byte
  *              aligned, ZEROED before its first use (cudaMemsetAsync).  Every

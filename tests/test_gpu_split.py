@@ -9,8 +9,9 @@ product (and its int32 sums equal to the oracle's), whatever the split.  The
 shapes cover a tile shared by every pair (one tile, 192 K steps), the DiT
 block chain's down projection (48 tiles, long K), chunked accumulation (8-bit
 weights over 12288 columns), ragged sizes with a K tail, bf16 output, the
-fused epilogue in place, and shapes the library leaves unsplit (short K, more
-tiles than CTA pairs), which must be unchanged too.  The workspace's flags must be zero again after each
+fused epilogue in place, products whose whole waves stay whole and whose last
+wave is split (the DiT down projection), and shapes the library leaves
+unsplit (short K), which must be unchanged too.  The workspace's flags must be zero again after each
 call, so the same workspace serves the next call.
 """
 import numpy as np
@@ -49,7 +50,9 @@ SHAPES = [
     (1024, 3072, 12288, 8),    # the same with 8-bit weights: chunked exact accumulation
     (257, 300, 12288 + 32, 8), # ragged rows and columns, a K tail, 4 tiles split
     (1024, 3072, 3072, 4),     # chain out projection: short K, left whole
-    (4032, 3072, 12288, 8),    # DiT down: 192 tiles (more than the pairs), left whole
+    (4032, 3072, 12288, 8),    # DiT down: 192 tiles, two whole waves, the last wave's 40 split
+    (900, 5400, 12288 + 32, 8),  # 88 tiles: one whole wave, 12 split; ragged, a K tail
+    (1024, 5120, 8192, 4),     # 80 tiles: one whole wave, 4 split over every pair
 ]
 
 
