@@ -620,7 +620,9 @@ k_rotq(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx, void *
         if (!tail_warp) {
             // codes eight at a time: 16 bytes of fp16 codes (one core-matrix
             // row of the tiled operand) or 8 bytes of int8 codes
-            float fs = 0.0f, fq = 0.0f;   // exact: at most 32 x 127 and 32 x 127^2
+            float fs = 0.0f;                                   // exact: at most 32 x 127
+            unsigned long long fq2 = f2pack(0.0f, 0.0f);       // exact: at most 16 x 127^2 a half
+            const unsigned long long r2 = f2pack(r16, r16);
             uint16_t *tdst = nullptr;
             if constexpr (TILED) {
                 const int64_t mt = m >> 7;
@@ -634,21 +636,31 @@ k_rotq(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx, void *
                 // rint of the product; where it may differ from rint of the
                 // correctly rounded quotient (near a half-integer, or no
                 // reciprocal), the warp takes the division for those values
-                bool amb = r16 == 0.0f;
+                // (products and differences on pairs, each rounded as a
+                // single one; the largest distance decides for the eight)
+                float dmax = 0.0f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float t = v[8 * c + e] * r16;
-                    q[e] = rintf(t);
-                    amb = amb || fabsf(t - q[e]) > 0.499f;
+                for (int e = 0; e < 8; e += 2) {
+                    unsigned long long t2, d2;
+                    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(t2) : "l"(f2pack(v[8 * c + e], v[8 * c + e + 1])), "l"(r2));
+                    float t0, t1, d0, d1;
+                    f2unpack(t2, t0, t1);
+                    q[e] = rintf(t0);
+                    q[e + 1] = rintf(t1);
+                    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d2) : "l"(t2), "l"(f2pack(q[e], q[e + 1])));
+                    f2unpack(d2, d0, d1);
+                    dmax = fmaxf(dmax, fmaxf(fabsf(d0), fabsf(d1)));
                 }
+                const bool amb = r16 == 0.0f || dmax > 0.499f;
                 if (__any_sync(0xffffffffu, amb) && amb) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) q[e] = code_of(v[8 * c + e], 0.0625f, r16, s);
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    fs += fabsf(q[e]);
-                    fq = fmaf(q[e], q[e], fq);
+                for (int e = 0; e < 8; e += 2) {
+                    fs += fabsf(q[e]) + fabsf(q[e + 1]);
+                    const unsigned long long q2 = f2pack(q[e], q[e + 1]);
+                    asm("fma.rn.f32x2 %0, %1, %1, %0;" : "+l"(fq2) : "l"(q2));
                 }
                 if (!active) continue;
                 if constexpr (TILED) {
@@ -669,8 +681,10 @@ k_rotq(const uint16_t *__restrict__ X, int64_t M, int64_t K, int64_t ldx, void *
                 }
             }
             if constexpr (TILED) {
+                float fq0, fq1;
+                f2unpack(fq2, fq0, fq1);
                 const unsigned int gs = __reduce_add_sync(0xffffffffu, static_cast<unsigned int>(fs));
-                const unsigned int gq = __reduce_add_sync(0xffffffffu, static_cast<unsigned int>(fq));
+                const unsigned int gq = __reduce_add_sync(0xffffffffu, static_cast<unsigned int>(fq0 + fq1));
                 if (lane == 0 && warp < WF) {
                     atomicAdd(&win[par][warp], gs);
                     atomicAdd(&winq[par][warp], gq);
