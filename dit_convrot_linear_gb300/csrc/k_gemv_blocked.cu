@@ -1,6 +1,7 @@
 // Decode product on block-scaled weights, M <= 8 tokens:
 //   Y[m][n] = sum_b s[n][b] * sum_{k in block b} q[n][k] * x[m][k],  fp32 sums,
-// one fp32 scale per block of G weight columns (G = 32, 64, 128, 256): the
+// one fp32 scale per block of G weight columns (G = 32, 64, 128, 256; G = 0,
+// one scale per row, serves the per-row format's large single-token calls): the
 // blocks with a shared scale of the GGML formats and kvad's own q8 (kvad-gpu
 // internals, "Quantised weights on the GPU").  With rotate = 1 the weights
 // were rotated before quantisation and x is the token row's group-256
@@ -122,8 +123,9 @@ k_gemv_blocked(const BlockedParams p) {
     const int U = static_cast<int>(K >> 2);        // 16-byte units of a staged row
     const int64_t rb = K * BITS / 8;               // code bytes of a weight row
     const int C = static_cast<int>(rb >> 4);       // 16-byte chunks of a weight row
-    const int64_t nb = K / p.G;
-    const int cshift = __ffs(p.G / KPC) - 1;       // chunk -> block: c >> cshift
+    // G == 0: one scale per row (the per-row format of tq_quantize_weights)
+    const int64_t nb = p.G ? K / p.G : 1;
+    const int cshift = p.G ? __ffs(p.G / KPC) - 1 : 31;   // chunk -> block: c >> cshift
     const int64_t nsets = (p.N + RW - 1) / RW;
 
     for (int64_t set = static_cast<int64_t>(blockIdx.x) * (kBlkThreads / 32) + warp; set < nsets;

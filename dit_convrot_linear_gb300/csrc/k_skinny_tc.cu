@@ -534,18 +534,26 @@ int64_t skinny_tc_workspace(int64_t M, int64_t K) {
     return (ks * skinny_tc_mp(M) * SK_BK * 2 + 255) / 256 * 256 + 256;
 }
 
-// Where the tensor-core product beats the CUDA-core kernels (measured with
-// 4-bit weights of 12288 x 4096 and 4096 x 12288, calls back to back): from
-// three tokens on for matrices of at least 2^24 weights (27.5 against 32 to
-// 43 us at M = 4), and at two tokens when N >= K (27.6 against 34.9 us; 30.5
-// against 27.5 us the other way); a single token streams faster through the
-// CUDA-core kernel (24.5 and 19.8 us against 27.4 and 30.5 us).  Below 2^24
-// weights the CUDA-core kernels keep M <= 8.
+// Which A16 kernel a call takes, measured with 4-bit weights of 12288 x 4096
+// and 4096 x 12288, calls back to back (us a call):
+//   tokens   tensor cores   streaming (a row a warp)   small kernel
+//   1        27.4 / 30.5    13.4 / 20.5                24.5 / 19.8
+//   2        25.4 / 30.5    20.0 / 26.2                34.9 / 27.5
+//   3, 4     25.3 / 28.1    -                          27.0 / 35.5, 32.6 / 43.7
+// So one token over a matrix of at least 2^24 weights streams when N >= K
+// (the staged rotated row is short next to a CTA's rows), two tokens always;
+// from three tokens on the tensor cores take it.  Below 2^24 weights the
+// small kernel keeps M <= 8 (its weight copies start before the previous
+// launch ends, which is what short decode calls need).
+bool a16_streams(int64_t M, int64_t N, int64_t K, int bits) {
+    if (M < 1 || M > 2 || N * K < (int64_t(1) << 24) || (K * bits / 8) % 16 != 0) return false;
+    return M == 2 || N >= K;
+}
+
 bool skinny_tc_applies(int64_t M, int64_t N, int64_t K) {
     if (M < 1 || M > SK_MAXMP || K > TQ_MAX_K_TILED) return false;
     if (M > 8) return true;
-    if (N * K < (int64_t(1) << 24) || M == 1) return false;
-    return M >= 3 || N >= K;
+    return M >= 3 && N * K >= (int64_t(1) << 24);
 }
 
 // One wave of CTAs (at most a tile of 256 rows per SM): a later wave could

@@ -288,6 +288,11 @@ tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
         if (use_ws && skinny_tc_fits_device(N, dev))
             return launch_skinny_tc(static_cast<const uint16_t *>(X), M, K, ldx, static_cast<const uint8_t *>(Wq),
                                     sw, N, bits, Y, ytype == TQ_OUT_BF16 ? 1 : 0, ldy, workspace, dev, stream);
+        if (a16_streams(M, N, K, bits) &&
+            static_cast<int64_t>(gemv_blocked_mt(static_cast<int>(M))) * K * 4 <= dev.smem_optin)
+            return launch_gemv_blocked(static_cast<const uint16_t *>(X), static_cast<int>(M), K, ldx,
+                                       static_cast<const uint8_t *>(Wq), sw, 0, N, bits, 1, Y,
+                                       ytype == TQ_OUT_BF16 ? 1 : 0, ldy, dev, stream);
         if (gemv_small_fits(M, N, K, bits, dev))
             return launch_gemv_small(static_cast<const uint16_t *>(X), M, K, ldx,
                                      static_cast<const uint8_t *>(Wq), sw, N, bits, Y,

@@ -46,6 +46,7 @@ bool gemv_fits(int64_t M, int64_t K, int bits, const DeviceInfo &dev);
 tq_status launch_quantize_weights_blocked(const uint16_t *W, int64_t N, int64_t K, int64_t ldw, int bits,
                                           int G, int rotate, void *codes, float *scales, cudaStream_t s);
 int gemv_blocked_mt(int M);
+bool a16_streams(int64_t M, int64_t N, int64_t K, int bits);
 tq_status launch_gemv_blocked(const uint16_t *X, int M, int64_t K, int64_t ldx, const uint8_t *Wq,
                               const float *sw, int G, int64_t N, int bits, int rotate, void *Y, int ytype,
                               int64_t ldy, const DeviceInfo &dev, cudaStream_t s);

@@ -171,8 +171,9 @@ size_t tq_linear_workspace_bytes(int64_t M, int64_t K, int64_t N, int bits,
  *            not matter; the call overwrites it.
  *            TQ_W8A8: required.  A16 modes: optional.  With it, products of
  *            more than 8 token rows, or of weights of at least 2^24 codes
- *            with 3 to 8 token rows (2 when N >= K), run on the tensor cores
- *            (where they are faster; the rotated rows are first written to
+ *            with 3 to 8 token rows, run on the tensor cores (where they are
+ *            faster; one or two token rows over such a matrix stream through
+ *            the CUDA cores instead, and need no workspace; the rotated rows are first written to
  *            the workspace as fp16 tiles, each token scaled by a power of two,
  *            which keeps every bf16 value exact); without it (or smaller than
  *            that size) the CUDA-core kernels run.  Both compute the same Y

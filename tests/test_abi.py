@@ -108,14 +108,14 @@ def test_a16_workspace_is_the_tensor_core_operand(L):
     """A16 modes: the optional workspace holds the x' tiles of the tensor-core
     product ([ceil(K/64)] tiles of M rounded up to 16 rows x 64 fp16, then the
     token factors), for more than 8 tokens, or for weights of at least 2^24
-    codes with 3 to 8 tokens (2 when N >= K); 0 for a single token and for
-    decode-sized products, which need none."""
+    codes with 3 to 8 tokens; 0 for one or two tokens (they stream through
+    the CUDA cores) and for decode-sized products, which need none."""
     assert L.tq_linear_workspace_bytes(64, 4096, 12288, 4, 1) == 64 * 64 * 64 * 2 + 256
     assert L.tq_linear_workspace_bytes(13, 896, 300, 8, 0) == 14 * 16 * 64 * 2 + 256
     assert L.tq_linear_workspace_bytes(3, 4096, 12288, 4, 1) == 64 * 16 * 64 * 2 + 256
-    assert L.tq_linear_workspace_bytes(2, 4096, 12288, 4, 1) == 64 * 16 * 64 * 2 + 256   # N >= K
-    assert L.tq_linear_workspace_bytes(2, 12288, 4096, 4, 1) == 0                         # N < K
-    assert L.tq_linear_workspace_bytes(1, 4096, 12288, 4, 1) == 0     # one token: the CUDA-core kernel
+    assert L.tq_linear_workspace_bytes(2, 4096, 12288, 4, 1) == 0     # two tokens: streaming
+    assert L.tq_linear_workspace_bytes(2, 12288, 4096, 4, 1) == 0
+    assert L.tq_linear_workspace_bytes(1, 4096, 12288, 4, 1) == 0     # one token: a CUDA-core kernel
     assert L.tq_linear_workspace_bytes(1, 896, 4864, 8, 0) == 0          # decode: none
     assert L.tq_linear_workspace_bytes(8, 4096, 1000, 4, 1) == 0
     assert L.tq_linear_workspace_bytes(64, 16384 + 256, 256, 8, 0) == 0   # K above the tiled limit

@@ -3,9 +3,9 @@ mode W4A16 / W8A16 with its workspace): 8B-class projections (K = 4096 ->
 N = 12288 and K = 12288 -> N = 4096, 4-bit weights N(0, 0.015) with 0.5% of
 columns x30) at M = 1, 8, 32 and 64 token rows, the batched-decode sizes the
 pages' decode/prefill discussion spans (kvad-gpu internals, "Numbers" and
-"Quantised weights on the GPU").  A single token runs on the CUDA-core kernel
-(faster there); two tokens on the tensor cores when N >= K, three and more
-always.
+"Quantised weights on the GPU").  One or two tokens over these matrices
+stream through the CUDA cores (one token only when N >= K; else the small
+decode kernel), three and more run on the tensor cores.
 
 The operand is the A16 one (the rotated row rounded to bf16); the kernel holds
 it as fp16 times a power of two per token, which is the same value exactly,
@@ -52,11 +52,11 @@ def _no_workspace(tq, X, codes, sw, N, bits, out="f32"):
     return Y
 
 
-@pytest.mark.parametrize("M", [1, 8, 32, 64])
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 32, 64])
 @pytest.mark.parametrize("N,K", [(12288, 4096), (4096, 12288)])
 def test_batched_w4a16_full_size_sampled(tq, M, N, K):
     Xb, X, codes, sw = _setup(tq, M, N, K, 4, "full")
-    assert (tq.linear_workspace_bytes(M, K, N, 4, "W4A16") > 0) == (M > 1)
+    assert (tq.linear_workspace_bytes(M, K, N, 4, "W4A16") > 0) == (M > 2)
     Y = to_np(tq.linear(X, codes, sw, N, 4, "W4A16"))
     rng = np.random.default_rng(M * 7 + N)
     pm = np.concatenate([rng.integers(0, M, 3000), [0, M - 1]])
@@ -75,8 +75,9 @@ def test_batched_w4a16_full_size_sampled(tq, M, N, K):
     (64, 257, 12288, 4),        # ragged rows (the last tile one row), long K
     (33, 1000, 4096 + 32, 4),   # K tail of 32 (half a K step), 48 token columns
     (16, 4096, 4096, 8),        # 8-bit weights
-    (2, 12288, 4096 + 64, 8),   # two tokens, N >= K: a matrix of 2^25 codes
-    (3, 4096, 12288, 4),        # three tokens, N < K
+    (2, 12288, 4096 + 64, 8),   # two tokens: streaming, 8-bit, a K tail of 64
+    (1, 9000, 4096 + 32, 4),    # one token, N >= K: streaming, ragged N, a K tail of 32
+    (3, 4096, 12288, 4),        # three tokens, N < K: tensor cores
 ])
 def test_batched_matches_the_oracle_and_the_cuda_core_path(tq, M, N, K, bits):
     mode = "W8A16" if bits == 8 else "W4A16"
