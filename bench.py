@@ -678,9 +678,9 @@ def batched_measure(device, steps, warmup, world, l2, hbm, bf16_peak):
                                      "roof_tflops": round(roof, 2)},
                         "per_projection": per}
         del xs, ys, g
-    out["kernels"] = ("k_gemv_small<4> (M = 1: the CUDA-core kernel, faster for one token); "
-                      "k_rotate_tiles16 (x' pre-pass) + k_skinny_tc<4> (M = 8, 32, 64: tcgen05, "
-                      "A operand from TMEM, cluster split-K)")
+    out["kernels"] = ("M = 1: k_gemv_blocked<4> with one scale a row (12288x4096, streaming) and "
+                      "k_gemv_small<4> (4096x12288); M = 8, 32, 64: k_rotate_tiles16 (x' pre-pass) + "
+                      "k_skinny_tc<4> (tcgen05, A operand from TMEM, cluster split-K)")
     return out
 
 
