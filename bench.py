@@ -56,7 +56,8 @@ PROFILE_CASES = {
     "rot_tiled": ("rotation + int8 tiled operand, M=4032 K=12288", "k_rotq"),
     "skinny_m64": ("batched W4A16 on the tensor cores, M=64 N=12288 K=4096", "k_skinny_tc"),
     "skinny_m8": ("batched W4A16 on the tensor cores, M=8 N=4096 K=12288", "k_skinny_tc"),
-    "gemv_m1": ("decode W4A16 CUDA-core product, M=1 N=12288 K=4096", "k_gemv"),
+    "gemv_m1": ("batched W4A16 with one token, M=1 N=12288 K=4096 (the streaming product, a scale a row)",
+                "k_gemv"),
 }
 
 
