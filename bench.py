@@ -354,51 +354,86 @@ class Decode:
 
 
 class DecodeChain:
-    """A dependent decode chain, M=1: through the layer sets, gate (896 ->
-    4864) then down (4864 -> 896), each call's input the previous call's bf16
-    output, so no call can start its product before the previous one ends
-    (its weights still stream early: the per-call kernels copy them before
-    waiting on the previous launch).  Synthetic weights: each matrix's row
-    scales are multiplied by 1 / sqrt(mean_n sum_k w_nk^2), so that a call
-    keeps its input's RMS and the chain stays finite; the rest as the decode
-    workload.  One CUDA graph of 2 x layers launches."""
+    """A dependent decode chain, M=1, through the layer sets as a gated FFN
+    decodes one token: gate and up (896 -> 4864 each) as one product over
+    their stacked rows (9728 x 896), then the down projection (4864 -> 896) of
+    h = silu(gate) * up, formed as the down call loads its input
+    (tq_linear_swiglu), its output the next layer's input.  No call can start
+    its product before the previous one ends (its weights still stream early:
+    the per-call kernels copy them before waiting on the previous launch).
+    Synthetic weights as the decode workload; each matrix's row scales are set
+    at set-up so that every call's output has RMS 1 (the gate/up rows from
+    their code norms, the down rows from one calibration pass), so the chain
+    stays finite.  One CUDA graph of 2 x layers launches."""
 
     def __init__(self, bits, device, l2_bytes):
         import torch
         from dit_convrot_linear_gb300 import synth, tq
         self.bits, self.mode = bits, ("W8A16" if bits == 8 else "W4A16")
         w = synth.DECODE
-        self.projs = [w.projs[0], w.projs[2]]          # gate, down
+        gate, up, down = w.projs
+        self.K, self.F = gate.K, gate.N                 # 896, 4864
         self.layers = decode_layers(bits, l2_bytes)
         self.weights = []
         for L in range(self.layers):
-            for p in self.projs:
+            cs, ss = [], []
+            for p in (gate, up):
                 codes, sw = tq.quantize_weights(bf16_dev(w.weight(L, p), device), bits)
-                # the row norms from the codes, widened here (set-up only; low nibble = even k)
-                if bits == 4:
-                    c = codes.view(torch.uint8).to(torch.int16)
-                    lo, hi = c & 15, (c >> 4) & 15
-                    lo, hi = torch.where(lo > 7, lo - 16, lo), torch.where(hi > 7, hi - 16, hi)
-                    q = torch.stack([lo, hi], dim=-1).reshape(p.N, p.K).float()
-                else:
-                    q = codes.view(torch.int8).view(p.N, p.K).float()
-                gain2 = torch.mean(sw.double() ** 2 * (q.double() ** 2).sum(dim=1))
-                self.weights.append((p, codes, (sw.double() / torch.sqrt(gain2)).float()))
-        self.x0 = bf16_dev(w.activation(0, self.projs[0], 1), device)
-        self.bufs = [torch.empty((1, p.N), dtype=torch.bfloat16, device=device) for p in self.projs]
-        self.weight_bytes = sum(p.N * p.K * bits // 8 + 4 * p.N for (p, _, _) in self.weights)
-        self.calls = len(self.weights)
+                gain2 = torch.mean(sw.double() ** 2 * (_codes_f32(codes, p.N, p.K, bits).double() ** 2).sum(dim=1))
+                cs.append(codes)
+                ss.append((sw.double() / torch.sqrt(gain2)).float())
+            gu = (torch.cat(cs, dim=0).contiguous(), torch.cat(ss).contiguous())
+            dc, dsw = tq.quantize_weights(bf16_dev(w.weight(L, down), device), bits)
+            self.weights.append((gu, (dc, dsw)))
+        self.x0 = bf16_dev(w.activation(0, gate, 1), device)
+        self.gu = torch.empty((1, 2 * self.F), dtype=torch.bfloat16, device=device)
+        self.bufs = [torch.empty((1, self.K), dtype=torch.bfloat16, device=device) for _ in range(2)]
+        self._calibrate()
+        self.weight_bytes = self.layers * (2 * self.F * self.K * bits // 8 + 8 * self.F +
+                                           self.K * self.F * bits // 8 + 4 * self.K)
+        self.calls = 2 * self.layers
         torch.cuda.synchronize()
 
-    def run(self, record=None):
+    def _layer(self, x, L, y):
         from dit_convrot_linear_gb300 import tq
+        (guc, gus), (dc, dsw) = self.weights[L]
+        tq.linear(x, guc, gus, 2 * self.F, self.bits, self.mode, Y=self.gu, out="bf16")
+        tq.linear_swiglu(self.gu[:, :self.F], self.gu[:, self.F:], dc, dsw, self.K, self.bits, self.mode,
+                         Y=y, out="bf16")
+
+    def _calibrate(self):
+        """Down-row scales so that each layer's output has RMS 1 (set-up only)."""
+        import torch
         x = self.x0
-        for i, (p, codes, sw) in enumerate(self.weights):
-            y = self.bufs[i % 2]
-            tq.linear(x, codes, sw, p.N, self.bits, self.mode, Y=y, out="bf16")
-            if record is not None:
-                record.append((x.clone(), y.clone()))
+        for L in range(self.layers):
+            y = self.bufs[L % 2]
+            self._layer(x, L, y)
+            r = float(torch.sqrt(torch.mean(y.float() ** 2)))
+            if r > 0 and r == r:
+                self.weights[L][1][1].div_(r)
+                self._layer(x, L, y)
             x = y
+
+    def run(self, record=None):
+        x = self.x0
+        for L in range(self.layers):
+            y = self.bufs[L % 2]
+            self._layer(x, L, y)
+            if record is not None:
+                record.append((x.clone(), self.gu.clone(), y.clone()))
+            x = y
+
+
+def _codes_f32(codes, N, K, bits):
+    """Signed weight codes [N, K] as fp32, widened (set-up only; low nibble =
+    even k)."""
+    import torch
+    if bits == 4:
+        c = codes.view(torch.uint8).to(torch.int16)
+        lo, hi = c & 15, (c >> 4) & 15
+        lo, hi = torch.where(lo > 7, lo - 16, lo), torch.where(hi > 7, hi - 16, hi)
+        return torch.stack([lo, hi], dim=-1).reshape(N, K).float()
+    return codes.view(torch.int8).view(N, K).float()
 
 
 def chain_decode_measure(device, steps, warmup, world, l2, hbm):
@@ -414,10 +449,13 @@ def chain_decode_measure(device, steps, warmup, world, l2, hbm):
         gbs = ch.weight_bytes / (ms * 1e-3) / 1e9
         out[f"w{bits}a16"] = {"value": round(gbs * world, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
                               "frac": round(gbs / hbm, 4), "calls_per_step": ch.calls,
-                              "us_per_call": round(ms * 1e3 / ch.calls, 2), "layers": ch.layers}
+                              "us_per_call": round(ms * 1e3 / ch.calls, 2),
+                              "us_per_layer": round(ms * 1e3 / ch.layers, 2), "layers": ch.layers}
         del ch, g
         torch.cuda.empty_cache()
-    out["kernels"] = "k_gemv_small (gate) + k_gemv_rows8 (down), one launch a call, programmatic dependent launches"
+    out["layer"] = "gate+up 9728x896 (one call) -> SwiGLU fused into the down call 896x4864"
+    out["kernels"] = ("k_gemv_small (gate+up) + k_gemv_rows8 with the SwiGLU prologue (down), "
+                      "one launch a call, programmatic dependent launches")
     return out
 
 

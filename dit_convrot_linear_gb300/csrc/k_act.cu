@@ -57,26 +57,6 @@ __device__ __forceinline__ uint32_t quant4(const float *v, float s, float r) {
 
 constexpr int64_t kRingMaxK = TQ_MAX_K_TILED;    // longest row k_rotq takes
 
-// SwiGLU of one gate value g and up value u, h = silu(g) * u with
-// silu(g) = g / (1 + e^-g) (Shazeer, "GLU Variants Improve Transformer"), in
-// fp32; the caller rounds h to bf16, as an unfused SwiGLU kernel would store it.
-// The exponential and the division are the hardware's approximate ones
-// (__expf, __fdividef): a relative error of a few parts in 10^6 at most for
-// |g| < 16, so h's bf16 rounding (a step of 2^-8) differs from that of the
-// exact value only for the rare h within that distance of a rounding tie, and
-// it cuts this pass's arithmetic to about a third.  For g <= -87 the quotient
-// is 0 (|h| < 1e-36 |u|), as the exact fp32 form gives -0 below -88.7.
-__device__ __forceinline__ float silu_mul(float g, float u) {
-    return __fdividef(g, 1.0f + __expf(-g)) * u;
-}
-
-// Two bf16 values a word: h = bf16(silu(g) * u) of the gate word and up word.
-__device__ __forceinline__ uint32_t swiglu_word(uint32_t gw, uint32_t uw) {
-    const float h0 = silu_mul(__uint_as_float(gw << 16), __uint_as_float(uw << 16));
-    const float h1 = silu_mul(__uint_as_float(gw & 0xFFFF0000u), __uint_as_float(uw & 0xFFFF0000u));
-    return f32_to_bf16_bits(h0) | (static_cast<uint32_t>(f32_to_bf16_bits(h1)) << 16);
-}
-
 __device__ __forceinline__ void store_codes(int8_t *dst, int e_per_lane, const float *vals, float s,
                                             float r) {
     const uint32_t lo = quant4(vals, s, r);

@@ -34,6 +34,8 @@ namespace {
 struct SmallParams {
     const uint16_t *X;
     int64_t ldx;
+    const uint16_t *U;   // with U: the input row is h = bf16(silu(x) * u) (SwiGLU), else x
+    int64_t ldu;
     int M;
     int64_t K;
     int G;
@@ -116,6 +118,7 @@ k_gemv_small(const SmallParams p) {
             const int64_t k0 = static_cast<int64_t>(g0) * kGroup;
             const int64_t k1 = min(static_cast<int64_t>(g1) * kGroup, p.K);
             if (k1 > k0) prefetch_l2(p.X + m * p.ldx + k0, static_cast<uint32_t>((k1 - k0) * 2));
+            if (k1 > k0 && p.U) prefetch_l2(p.U + m * p.ldu + k0, static_cast<uint32_t>((k1 - k0) * 2));
         }
     }
     __syncthreads();  // barrier initialised; row scales in place
@@ -175,16 +178,21 @@ k_gemv_small(const SmallParams p) {
     for (int m = 0; m < M; ++m) {
         uint16_t *xrow = xw + m * XS;
         for (int gb = 0; gb < ng; gb += GB) {
-            uint4 raw[GB];
+            uint4 raw[GB], rawu[GB];
 #pragma unroll
             for (int u = 0; u < GB; ++u) {
-                raw[u] = make_uint4(0, 0, 0, 0);
+                raw[u] = rawu[u] = make_uint4(0, 0, 0, 0);
                 const int gi = gb + u;
                 if (gi < ng) {
                     const int64_t gk = kslice0 + static_cast<int64_t>(gi) * kGroup;
                     const int E = group_width(p.K, gk) / 32;
                     raw[u] = load_group_raw(p.X + m * p.ldx + gk + lane * E, E);
+                    if (p.U) rawu[u] = load_group_raw(p.U + m * p.ldu + gk + lane * E, E);
                 }
+            }
+            if (p.U) {
+#pragma unroll
+                for (int u = 0; u < GB; ++u) raw[u] = swiglu_raw(raw[u], rawu[u]);
             }
 #pragma unroll
             for (int u = 0; u < GB; ++u) {
@@ -321,6 +329,8 @@ constexpr int RB_NF = 40;
 struct Rows8Params {
     const uint16_t *X;
     int64_t ldx;
+    const uint16_t *U;   // as SmallParams
+    int64_t ldu;
     int M;
     int64_t K;
     const uint8_t *W;
@@ -393,7 +403,10 @@ k_gemv_rows8(const Rows8Params p) {
     for (int g = warp; g < G; g += W) {   // coherent L2 prefetch: safe before the wait
         const int64_t k0 = static_cast<int64_t>(g) * kGroup;
         const int64_t k1 = min(k0 + kGroup, p.K);
-        for (int m = lane; m < p.M; m += 32) prefetch_l2(p.X + m * p.ldx + k0, static_cast<uint32_t>((k1 - k0) * 2));
+        for (int m = lane; m < p.M; m += 32) {
+            prefetch_l2(p.X + m * p.ldx + k0, static_cast<uint32_t>((k1 - k0) * 2));
+            if (p.U) prefetch_l2(p.U + m * p.ldu + k0, static_cast<uint32_t>((k1 - k0) * 2));
+        }
     }
     __syncthreads();
     pdl_launch_dependents();
@@ -432,16 +445,21 @@ k_gemv_rows8(const Rows8Params p) {
     constexpr int GW = 3;                       // groups per warp at most (K <= 24 groups)
     for (int m = 0; m < M; ++m) {
         uint16_t *xrow = xs + m * XK;
-        uint4 raw[GW];
+        uint4 raw[GW], rawu[GW];
 #pragma unroll
         for (int u = 0; u < GW; ++u) {
             const int gi = warp + u * W;
-            raw[u] = make_uint4(0, 0, 0, 0);
+            raw[u] = rawu[u] = make_uint4(0, 0, 0, 0);
             if (gi < G) {
                 const int64_t gk = static_cast<int64_t>(gi) * kGroup;
                 const int E = group_width(p.K, gk) / 32;
                 raw[u] = load_group_raw(p.X + m * p.ldx + gk + lane * E, E);
+                if (p.U) rawu[u] = load_group_raw(p.U + m * p.ldu + gk + lane * E, E);
             }
+        }
+        if (p.U) {
+#pragma unroll
+            for (int u = 0; u < GW; ++u) raw[u] = swiglu_raw(raw[u], rawu[u]);
         }
 #pragma unroll
         for (int u = 0; u < GW; ++u) {
@@ -579,12 +597,15 @@ Rows8Plan plan_rows8(int64_t M, int64_t N, int64_t K, int bits, const DeviceInfo
 
 tq_status launch_rows8(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, const uint8_t *Wq,
                        const float *sw, int64_t N, int bits, void *Y, int ytype, int64_t ldy,
-                       const Rows8Plan &pl, const DeviceInfo &dev, cudaStream_t s) {
+                       const Rows8Plan &pl, const DeviceInfo &dev, cudaStream_t s, const uint16_t *U,
+                       int64_t ldu) {
     unsigned int *status = status_word();
     if (!status) return TQ_ERR_DEVICE;
     Rows8Params p{};
     p.X = X;
     p.ldx = ldx;
+    p.U = U;
+    p.ldu = ldu;
     p.M = static_cast<int>(M);
     p.K = K;
     p.W = Wq;
@@ -631,14 +652,21 @@ bool gemv_small_fits(int64_t M, int64_t N, int64_t K, int bits, const DeviceInfo
     return plan_small(M, N, K, bits, dev).smem <= kSmallSmemMax;
 }
 
+bool gemv_decode_fits(int64_t M, int64_t N, int64_t K, int bits, const DeviceInfo &dev) {
+    if (M < 1 || M > 8) return false;
+    const SmallPlan pl = plan_small(M, N, K, bits, dev);
+    if (pl.gpw > 1 && plan_rows8(M, N, K, bits, dev).ok) return true;
+    return pl.smem <= kSmallSmemMax;
+}
+
 tq_status launch_gemv_small(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
                             const uint8_t *Wq, const float *sw, int64_t N, int bits,
                             void *Y, int ytype, int64_t ldy, const DeviceInfo &dev,
-                            cudaStream_t s) {
+                            cudaStream_t s, const uint16_t *U, int64_t ldu) {
     const SmallPlan pl = plan_small(M, N, K, bits, dev);
     if (pl.gpw > 1) {   // 16-row fragments would not fit: eight rows per CTA if the shape allows
         const Rows8Plan r8 = plan_rows8(M, N, K, bits, dev);
-        if (r8.ok) return launch_rows8(X, M, K, ldx, Wq, sw, N, bits, Y, ytype, ldy, r8, dev, s);
+        if (r8.ok) return launch_rows8(X, M, K, ldx, Wq, sw, N, bits, Y, ytype, ldy, r8, dev, s, U, ldu);
     }
     if (pl.smem > kSmallSmemMax) return TQ_ERR_SHAPE;
     unsigned int *status = status_word();
@@ -646,6 +674,8 @@ tq_status launch_gemv_small(const uint16_t *X, int64_t M, int64_t K, int64_t ldx
     SmallParams p{};
     p.X = X;
     p.ldx = ldx;
+    p.U = U;
+    p.ldu = ldu;
     p.M = static_cast<int>(M);
     p.K = K;
     p.G = static_cast<int>((K + kGroup - 1) / kGroup);

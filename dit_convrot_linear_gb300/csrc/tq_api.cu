@@ -207,6 +207,28 @@ tq_status tq_linear_blocked(const void *X, int64_t M, int64_t K, int64_t ldx, co
                                ytype == TQ_OUT_BF16 ? 1 : 0, ldy, dev, stream);
 }
 
+tq_status tq_linear_swiglu(const void *G, int64_t ldg, const void *U, int64_t ldu, int64_t M, int64_t K,
+                           const void *Wq, const float *sw, int64_t N, int bits, tq_mode mode, void *Y,
+                           tq_out ytype, int64_t ldy, cudaStream_t stream) {
+    if (bits != 8 && bits != 4) return TQ_ERR_BITS;
+    if (mode != TQ_W8A16 && mode != TQ_W4A16) return TQ_ERR_MODE;
+    if ((mode == TQ_W8A16 && bits != 8) || (mode == TQ_W4A16 && bits != 4)) return TQ_ERR_MODE;
+    if (ytype != TQ_OUT_F32 && ytype != TQ_OUT_BF16) return TQ_ERR_MODE;
+    if (M < 0 || M > 8 || N < 0 || !valid_k(K)) return TQ_ERR_SHAPE;
+    if (M == 0 || N == 0) return TQ_OK;
+    tq_status st = check_bf16_rows(G, M, K, ldg);
+    if (st != TQ_OK) return st;
+    if ((st = check_bf16_rows(U, M, K, ldu)) != TQ_OK) return st;
+    if ((st = check_weights(Wq, sw, N, K, bits)) != TQ_OK) return st;
+    if ((st = check_output(Y, M, N, ldy, out_size(ytype))) != TQ_OK) return st;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    if (!gemv_decode_fits(M, N, K, bits, dev)) return TQ_ERR_SHAPE;
+    return launch_gemv_small(static_cast<const uint16_t *>(G), M, K, ldg, static_cast<const uint8_t *>(Wq), sw, N,
+                             bits, Y, ytype == TQ_OUT_BF16 ? 1 : 0, ldy, dev, stream,
+                             static_cast<const uint16_t *>(U), ldu);
+}
+
 tq_status tq_rotate_quant_act(const void *X, int64_t M, int64_t K, int64_t ldx,
                               int8_t *Xq, float *sx, cudaStream_t stream) {
     if (M < 0 || !valid_k(K)) return TQ_ERR_SHAPE;

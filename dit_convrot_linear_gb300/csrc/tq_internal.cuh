@@ -66,10 +66,13 @@ tq_status launch_skinny_tc(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
 
 // Decode product for M <= 8: whole rows per CTA, no cluster reduction.
 bool gemv_small_fits(int64_t M, int64_t N, int64_t K, int bits, const DeviceInfo &dev);
+// U non-null: the input row is h = bf16(silu(x) * u) of X's and U's rows (SwiGLU)
 tq_status launch_gemv_small(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
                             const uint8_t *Wq, const float *sw, int64_t N, int bits,
                             void *Y, int ytype, int64_t ldy, const DeviceInfo &dev,
-                            cudaStream_t s);
+                            cudaStream_t s, const uint16_t *U = nullptr, int64_t ldu = 0);
+// the small kernel or the eight-row kernel takes this decode shape
+bool gemv_decode_fits(int64_t M, int64_t N, int64_t K, int bits, const DeviceInfo &dev);
 
 // A8 product on quantised activations: tcgen05 / TMEM, exact int32 sums.
 tq_status launch_gemm_a8(const int8_t *Xq, const float *sx, int64_t M,
@@ -258,6 +261,32 @@ __device__ __forceinline__ uint4 load_group_raw(const uint16_t *p, int E) {
     }
     if (E == 2) return make_uint4(__ldg(reinterpret_cast<const unsigned int *>(p)), 0, 0, 0);
     return make_uint4(__ldg(reinterpret_cast<const unsigned short *>(p)), 0, 0, 0);
+}
+
+// SwiGLU of one gate value g and up value u, h = silu(g) * u with
+// silu(g) = g / (1 + e^-g) (Shazeer, "GLU Variants Improve Transformer"), in
+// fp32; the caller rounds h to bf16, as an unfused SwiGLU kernel would store it.
+// The exponential and the division are the hardware's approximate ones
+// (__expf, __fdividef): a relative error of a few parts in 10^6 at most for
+// |g| < 16, so h's bf16 rounding (a step of 2^-8) differs from that of the
+// exact value only for the rare h within that distance of a rounding tie, and
+// it cuts this pass's arithmetic to about a third.  For g <= -87 the quotient
+// is 0 (|h| < 1e-36 |u|), as the exact fp32 form gives -0 below -88.7.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+// Two bf16 values a word: h = bf16(silu(g) * u) of the gate word and up word.
+__device__ __forceinline__ uint32_t swiglu_word(uint32_t gw, uint32_t uw) {
+    const float h0 = silu_mul(__uint_as_float(gw << 16), __uint_as_float(uw << 16));
+    const float h1 = silu_mul(__uint_as_float(gw & 0xFFFF0000u), __uint_as_float(uw & 0xFFFF0000u));
+    return f32_to_bf16_bits(h0) | (static_cast<uint32_t>(f32_to_bf16_bits(h1)) << 16);
+}
+
+// The SwiGLU of a gate group's raw words and an up group's (E bf16 values a
+// lane each, as load_group_raw returns them), packed the same way.
+__device__ __forceinline__ uint4 swiglu_raw(const uint4 &g, const uint4 &u) {
+    return make_uint4(swiglu_word(g.x, u.x), swiglu_word(g.y, u.y), swiglu_word(g.z, u.z), swiglu_word(g.w, u.w));
 }
 
 // ...and their transform: widen, butterfly, scale by sqrt(1/n).  Returns E.

@@ -42,6 +42,7 @@ SIGNATURES = {
     "tq_linear_tiled": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
     "tq_swiglu_quant_act_tiled": (_C, [_P, _I, _P, _I, _I, _I, _P, _Z, _P, _P]),
     "tq_modnorm_quant_act_tiled": (_C, [_P, _I, _I, _I, _P, _P, ctypes.c_float, _P, _Z, _P, _P]),
+    "tq_linear_swiglu": (_C, [_P, _I, _P, _I, _I, _I, _P, _P, _I, _C, _C, _P, _C, _I, _P]),
     "tq_weights_tiled_bytes": (_Z, [_I, _I]),
     "tq_tile_weights": (_C, [_P, _I, _I, _C, _P, _Z, _P]),
     "tq_linear_tt": (_C, [_P, _P, _I, _I, _P, _P, _I, _C, _P, _C, _I, _P]),
@@ -271,6 +272,28 @@ def linear(X, Wq, sw, N: int, bits: int, mode: str, Y=None, out: str = "f32",
     _check(lib().tq_linear(_ptr(X), M, K, X.stride(0), _ptr(Wq), _ptr(sw), N, bits,
                            MODES[mode], _ptr(Y), OUT[out], Y.stride(0), _ptr(workspace),
                            ws_bytes, _stream(stream)), "tq_linear")
+    return Y
+
+
+def linear_swiglu(G, U, Wq, sw, N: int, bits: int, mode: str, Y=None, out: str = "f32", stream=None):
+    """Y [M, N] = the decode product (A16, M <= 8) of h = bf16(silu(G) * U):
+    G and U bf16 [M, K] with any row stride (for example the two halves of a
+    fused gate+up output)."""
+    import torch
+    M, K = G.shape
+    if tuple(U.shape) != (M, K):
+        raise ValueError(f"U is {tuple(U.shape)}, expected {(M, K)}")
+    if out not in ("f32", "bf16"):
+        raise ValueError("tq_linear_swiglu writes f32 or bf16")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=_dt(out), device=G.device)
+    _req(G, "G", dtype=torch.bfloat16, rows=M, cols=K)
+    _req(U, "U", dtype=torch.bfloat16, rows=M, cols=K)
+    _weights(Wq, sw, N, K, bits)
+    _req(Y, "Y", dtype=_dt(out), rows=M, cols=N)
+    _check(lib().tq_linear_swiglu(_ptr(G), G.stride(0), _ptr(U), U.stride(0), M, K, _ptr(Wq), _ptr(sw), N, bits,
+                                  MODES[mode], _ptr(Y), OUT[out], Y.stride(0), _stream(stream)),
+           "tq_linear_swiglu")
     return Y
 
 

@@ -273,6 +273,28 @@ tq_status tq_modnorm_quant_act_tiled(const void *X, int64_t M, int64_t K, int64_
                                      cudaStream_t stream);
 
 /*
+ * The decode product (A16 modes, M <= 8 tokens) of the SwiGLU of two rows:
+ * Y = the rotated low-bit product of h = bf16(silu(G) * U), silu(g) =
+ * g / (1 + e^-g), with (Wq, sw).  The down projection of a gated FFN layer
+ * takes h made from its gate and up outputs; fused, h is formed as the
+ * decode kernel loads its input (the same arithmetic as
+ * tq_swiglu_quant_act_tiled), so a layer's gate+up call can feed its down
+ * call directly.  The pages name SwiGLU among the row kernels beside the
+ * projections, candidates for fusion (TensorFold PR #948, "What comes
+ * next"), and decode as one projection at a time, each input the previous
+ * output (kvad-gpu internals, "Numbers").
+ *   G, U     bf16 [M, K], rows at G + m * ldg and U + m * ldu (for example
+ *            the two halves of a fused gate+up output row: U = G + K); each
+ *            follows tq_rotate_quant_act's rules for X.
+ *   mode     TQ_W8A16 or TQ_W4A16 (bits to match); other arguments as
+ *            tq_linear.  Shapes the decode kernels do not take (M > 8, or K
+ *            past their shared-memory plan) are refused with TQ_ERR_SHAPE.
+ */
+tq_status tq_linear_swiglu(const void *G, int64_t ldg, const void *U, int64_t ldu, int64_t M, int64_t K,
+                           const void *Wq, const float *sw, int64_t N, int bits, tq_mode mode, void *Y,
+                           tq_out ytype, int64_t ldy, cudaStream_t stream);
+
+/*
  * The A8 product on a tiled operand: as tq_linear_q8 with At, sx from
  * tq_rotate_quant_act_tiled (same M and K) in place of Xq, sx.
  */

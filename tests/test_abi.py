@@ -18,10 +18,22 @@ S0 = None               # default stream
 
 
 @pytest.fixture(scope="module")
-def L():
+def lib_loaded():
     from dit_convrot_linear_gb300 import build, tq
     build.build()
     return tq.load()
+
+
+@pytest.fixture(scope="module")
+def L(lib_loaded):
+    """The library for the refusal checks.  These pass fake device addresses
+    (FAKE): a call that no host check refuses would launch a kernel on them,
+    so with a GPU visible they do not run at all (they test the host logic,
+    on a machine without a GPU, where such a call stops at the device query)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("refusal checks use fake device addresses: run them where no GPU is visible")
+    return lib_loaded
 
 
 def declared_functions():
@@ -37,14 +49,16 @@ def test_header_declares_the_entry_points():
         assert required in names
 
 
-def test_library_exports_every_declared_symbol(L):
+def test_library_exports_every_declared_symbol(lib_loaded):
+    L = lib_loaded
     from dit_convrot_linear_gb300 import tq
     for name in declared_functions():
         assert hasattr(L, name), f"{name} declared in tq.h but not exported"
         assert name in tq.SIGNATURES, f"{name} has no binding"
 
 
-def test_status_strings(L):
+def test_status_strings(lib_loaded):
+    L = lib_loaded
     for s in range(11):
         assert L.tq_status_str(s).decode().startswith(
             ["TQ_OK", "TQ_ERR_NULL", "TQ_ERR_SHAPE", "TQ_ERR_BITS", "TQ_ERR_MODE",
@@ -395,3 +409,25 @@ def test_modnorm_quant_refusals(L):
     assert mq(At=FAKE + 16) == ALIGN
     assert mq(M=0) == OK
     assert mq(M=0, eps=ctypes.c_float(-1.0)) == MODE  # eps is checked even for an empty call
+
+
+def test_linear_swiglu_refusals(L):
+    sg = lambda **k: L.tq_linear_swiglu(*[k.get(n, d) for n, d in (
+        ("G", FAKE), ("ldg", 1024), ("U", FAKE + 1024), ("ldu", 1024), ("M", 1), ("K", 512),
+        ("W", FAKE), ("sw", FAKE), ("N", 256), ("bits", 8), ("mode", 0), ("Y", FAKE), ("yt", 0),
+        ("ldy", 256), ("s", S0))])
+    assert sg(mode=2) == MODE                         # A16 modes only: the input is bf16
+    assert sg(mode=1) == MODE                         # W4A16 needs 4-bit weights
+    assert sg(bits=5) == BITS
+    assert sg(yt=2) == MODE
+    assert sg(M=9) == SHAPE                           # the decode kernels take M <= 8
+    assert sg(K=200, ldg=200, ldu=200) == SHAPE
+    assert sg(G=0) == NULL
+    assert sg(U=0) == NULL
+    assert sg(W=0) == NULL
+    assert sg(Y=0) == NULL
+    assert sg(ldu=500) == SHAPE                       # ldu < K
+    assert sg(ldg=1028) == ALIGN
+    assert sg(U=FAKE + 8) == ALIGN                    # each half 16-byte aligned
+    assert sg(M=0) == OK and sg(N=0) == OK
+    assert sg(M=0, mode=2) == MODE                    # the mode is checked even for an empty call

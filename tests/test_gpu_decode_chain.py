@@ -12,7 +12,7 @@ import pytest
 
 import oracle
 from dit_convrot_linear_gb300 import synth
-from helpers import bf16_bits, bf16_ulp_diff, to_dev_bf16, to_np
+from helpers import REL_L2_Y, bf16_bits, bf16_ulp_diff, rel_l2, to_dev_bf16, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -66,3 +66,171 @@ def test_dependent_chain_each_call_against_the_oracle(tq, bits):
         if i > 0:   # the chain: this call's input is the previous call's output
             assert np.array_equal(xb, bf16_bits(outs[i - 1]))
     assert tq.device_status() == 0
+
+
+# ---- the decode product of a SwiGLU input (tq_linear_swiglu)
+
+TIE_WINDOW = 2.0 ** -16
+
+
+def _near_ties(h):
+    """Boolean: the fp64 h lies within TIE_WINDOW |h| of a bf16 rounding
+    boundary (the midpoint of two neighbouring bf16 values).  The kernel's
+    silu uses the hardware's approximate exponential and division, a relative
+    error under 2^-19 for the gate values here, so only such h may round to
+    the other bf16 neighbour than the exact value does."""
+    a = np.abs(h)
+    nz = a > 0
+    e = np.floor(np.log2(np.where(nz, a, 1.0)))
+    ulp = np.exp2(e - 7)
+    mid = np.floor(a / ulp) * ulp + ulp / 2
+    return nz & (np.abs(a - mid) <= TIE_WINDOW * a)
+
+
+def _swiglu_inputs(tag, M, K):
+    """Seeded gate and up rows, with each up value whose h = silu(g) u lies
+    near a bf16 rounding tie moved by one bf16 step (an input choice made with
+    the oracle alone), so the kernel's h must equal the oracle's bit for bit."""
+    G = synth.tensor(f"gpu/dswiglu/g/{tag}", M, K, 1.5, 0.0, 1.0)
+    U = synth.tensor(f"gpu/dswiglu/u/{tag}", M, K, 1.0, 0.002, 40.0)
+    g = oracle.bf16_to_f64(G)
+    for _ in range(16):
+        near = _near_ties(oracle.swiglu_f64(g, oracle.bf16_to_f64(U)))
+        if not near.any():
+            return G, U
+        U[near] = U[near] + 1          # one step away from zero in magnitude
+    raise AssertionError("could not move every h off a rounding tie")
+
+
+SWIGLU_CASES = [  # M, N, K, bits, out
+    (1, 896, 4864, 8, "bf16"),       # the decode down projection (eight-row kernel)
+    (1, 896, 4864, 4, "f32"),
+    (2, 896, 4864, 4, "bf16"),
+    (8, 896, 4864, 8, "f32"),        # 16-row fragments, three groups a warp
+    (3, 300, 2048 + 32, 8, "f32"),   # a ragged 32-wide last group
+    (2, 4864, 896, 4, "f32"),        # one group a warp, fragments in registers
+    (5, 1000, 4096 + 128, 4, "bf16"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,bits,out", SWIGLU_CASES)
+def test_swiglu_decode_product(tq, M, N, K, bits, out):
+    """Y of h = bf16(silu(G) U), G and U the two halves of one gate/up row
+    (strided views): against the oracle's O8 then O6 (f32 Y to REL_L2_Y, bf16
+    Y within one ulp of the oracle's value rounded to bf16), and equal bit for
+    bit to the unfused route (the oracle's h through tq_linear, the same
+    decode kernel without the SwiGLU prologue)."""
+    import torch
+    mode = "W8A16" if bits == 8 else "W4A16"
+    G, U = _swiglu_inputs(f"{M}x{N}x{K}b{bits}", M, K)
+    GU = to_dev_bf16(np.concatenate([G, U], axis=1))
+    codes, sw = tq.quantize_weights(to_dev_bf16(synth.tensor(f"gpu/dswiglu/w{N}x{K}", N, K, *WD)), bits)
+    Y = tq.linear_swiglu(GU[:, :K], GU[:, K:], codes, sw, N, bits, mode, out=out)
+    H = oracle.swiglu_bf16(G, U)
+    Y0 = tq.linear(to_dev_bf16(H), codes, sw, N, bits, mode, out=out)
+    assert tq.device_status() == 0
+    assert torch.equal(Y.view(torch.int16) if out == "bf16" else Y, Y0.view(torch.int16) if out == "bf16" else Y0)
+    c = to_np(codes)
+    wc = oracle.weight_codes(c.view(np.int8) if bits == 8 else c.view(np.uint8), bits, K)
+    ref = oracle.linear_a16(oracle.rotate_act_bf16(H), wc, to_np(sw))
+    if out == "bf16":
+        assert bf16_ulp_diff(bf16_bits(Y), oracle.round_bf16(ref)).max() <= 1
+    else:
+        assert rel_l2(to_np(Y), ref) <= REL_L2_Y
+
+
+def test_swiglu_decode_product_padded_rows_and_output_stride(tq):
+    """Gate and up from separate buffers with row strides above K, Y written
+    into a wider matrix: the columns past N stay untouched."""
+    import torch
+    M, N, K, bits = 2, 640, 1024 + 64, 8
+    G, U = _swiglu_inputs("strided", M, K)
+    Gd = to_dev_bf16(np.pad(G, ((0, 0), (0, 40))))[:, :K]
+    Ud = to_dev_bf16(np.pad(U, ((0, 0), (16, 24))))[:, 16:16 + K]
+    codes, sw = tq.quantize_weights(to_dev_bf16(synth.tensor("gpu/dswiglu/ws", N, K, *WD)), bits)
+    Yw = torch.full((M, N + 24), 7.0, dtype=torch.float32, device="cuda")
+    tq.linear_swiglu(Gd, Ud, codes, sw, N, bits, "W8A16", Y=Yw[:, :N])
+    assert tq.device_status() == 0
+    ref = oracle.linear_a16(oracle.rotate_act_bf16(oracle.swiglu_bf16(G, U)), to_np(codes), to_np(sw))
+    assert rel_l2(to_np(Yw[:, :N]), ref) <= REL_L2_Y
+    assert torch.all(Yw[:, N:] == 7.0)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_ffn_layer_chain_each_call_against_the_oracle(tq, bits):
+    """Three gated FFN layers at decode (M = 1) in one CUDA graph, as the
+    bench runs them: gate+up as one product over the stacked rows (9728 x
+    896, bf16 out), then the down product of the SwiGLU of its two halves
+    (896 x 4864), its output the next layer's input.  Each call against the
+    oracle on the GPU's own input for that call.  The gate+up calls: within
+    one bf16 ulp.  The down calls: the GPU's h may differ from the oracle's
+    by one bf16 step where h lies within the kernel's silu error (under 2^-19
+    relative) of a rounding tie, a few elements a row; each such flip moves
+    Y_n by ulp(h_k) |w_nk|, about 2^-8 / sqrt(K) of Y's RMS, so the bar is a
+    relative L2 error of 2^-8 (the bf16 output rounding alone gives up to
+    2^-9) and 99% of the outputs within one ulp."""
+    import torch
+    mode = "W8A16" if bits == 8 else "W4A16"
+    K, F = 896, 4864
+    def weights(name, N, Kw, post):
+        # row scales over the RMS row norm, so a call keeps its input's RMS
+        # (times post: 1 / 0.596, the RMS of silu(z) z' for standard normals,
+        # for the down rows)
+        W = synth.tensor(name, N, Kw, *WD)
+        gain = np.sqrt(np.mean(np.sum(oracle.bf16_to_f64(W) ** 2, axis=1)))
+        c, s = tq.quantize_weights(to_dev_bf16(W), bits)
+        return c, (s * float(post / gain)).contiguous()
+    layers = []
+    for L in range(3):
+        gc, gs = weights(f"gpu/ffn/gu{L}", 2 * F, K, 1.0)
+        dc, ds = weights(f"gpu/ffn/d{L}", K, F, 1.0 / 0.596)
+        layers.append((gc, gs, dc, ds))
+    x0 = to_dev_bf16(synth.tensor("gpu/ffn/x", 1, K, 1.0))
+    gu = torch.empty((1, 2 * F), dtype=torch.bfloat16, device="cuda")
+    bufs = [torch.empty((1, K), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    rec_x = [torch.empty((1, K), dtype=torch.bfloat16, device="cuda") for _ in layers]
+    rec_gu = [torch.empty((1, 2 * F), dtype=torch.bfloat16, device="cuda") for _ in layers]
+    rec_y = [torch.empty((1, K), dtype=torch.bfloat16, device="cuda") for _ in layers]
+
+    def run():
+        x = x0
+        for L, (gc, gs, dc, ds) in enumerate(layers):
+            y = bufs[L % 2]
+            rec_x[L].copy_(x)
+            tq.linear(x, gc, gs, 2 * F, bits, mode, Y=gu, out="bf16")
+            rec_gu[L].copy_(gu)
+            tq.linear_swiglu(gu[:, :F], gu[:, F:], dc, ds, K, bits, mode, Y=y, out="bf16")
+            rec_y[L].copy_(y)
+            x = y
+    run()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            run()
+    torch.cuda.current_stream().wait_stream(s)
+    for r in rec_x + rec_gu + rec_y:
+        r.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert tq.device_status() == 0
+
+    def wcodes(c, Kc):
+        c = to_np(c)
+        return oracle.weight_codes(c.view(np.int8) if bits == 8 else c.view(np.uint8), bits, Kc)
+    for L, (gc, gs, dc, ds) in enumerate(layers):
+        xb, gub, yb = bf16_bits(rec_x[L]), bf16_bits(rec_gu[L]), bf16_bits(rec_y[L])
+        if L > 0:
+            assert np.array_equal(xb, bf16_bits(rec_y[L - 1]))
+        ref_gu = oracle.linear_a16(oracle.rotate_act_bf16(xb), wcodes(gc, K), to_np(gs))
+        assert bf16_ulp_diff(gub, oracle.round_bf16(ref_gu)).max() <= 1, f"layer {L} gate+up"
+        h = oracle.swiglu_bf16(gub[:, :F], gub[:, F:])
+        assert np.count_nonzero(h) > F // 2
+        ref_y = oracle.linear_a16(oracle.rotate_act_bf16(h), wcodes(dc, F), to_np(ds))
+        got = oracle.bf16_to_f64(yb)
+        assert rel_l2(got, ref_y) <= 2.0 ** -8, f"layer {L} down"
+        d = bf16_ulp_diff(yb, oracle.round_bf16(ref_y))
+        assert np.mean(d <= 1) >= 0.99, f"layer {L} down: {np.mean(d <= 1)} within one ulp"
+        assert 0.05 < np.sqrt(np.mean(got ** 2)) < 50.0     # the chain stays O(1)
