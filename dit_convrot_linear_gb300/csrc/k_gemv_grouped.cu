@@ -19,6 +19,16 @@
 //      consumer warps multiply (codes widened to exact bf16 pairs in
 //      registers, mma.sync m16n8k16, fp32), add the K blocks in a fixed order
 //      and store Y.  The stream never waits for a call to finish.
+// A chained plan runs calls that do depend on one another, in order, the way
+// a decoder walks its layers: call c may read the output of any earlier call
+// (kvad-gpu internals, "Numbers": one projection at a time, each input the
+// previous output).  The same persistent kernel (a cooperative launch: every
+// CTA resident) keeps streaming weights ahead, so call c's rows are in shared
+// memory before call c - 1 ends; the consumers of a CTA's first item of call
+// c wait until every item of call c - 1 has counted itself done (a counter per
+// call in device memory), then rotate the call's input themselves (optionally
+// the SwiGLU of two rows, as a gated FFN's down projection takes it) and
+// multiply.  There is no launch and no rotation pre-pass between calls.
 // Every wait is bounded: on expiry the status word is set, the CTA stops, and
 // the outputs of the items it had not finished are left unwritten.
 
@@ -56,8 +66,10 @@ struct GItem {
     int32_t xoff;          // byte offset of x' in the stage
     int16_t M;             // token rows
     int16_t tiles;         // 1: tile form
+    int32_t call;          // chained plans: index of the item's call
+    uint32_t wait;         // chained plans: items of the previous call (0: none)
 };
-static_assert(sizeof(GItem) == 80, "item record of 80 bytes");
+static_assert(sizeof(GItem) == 88, "item record of 88 bytes");
 
 struct GCall {
     const uint16_t *X;
@@ -78,11 +90,32 @@ constexpr int kGSmem = kGBarOff + 2 * kGStages * 8 + 16 + 1024;   // + alignment
 constexpr unsigned int kStatusGroupedTimeout = 16u;
 constexpr int kXTail = 32;     // bytes after a call's x' rows: a float 2^-e per token
 
+// One call of a chained plan, as its consumers read it.
+struct CCall {
+    const uint16_t *X;
+    const uint16_t *U;     // NULL, or the up rows: the input is bf16(silu(X) * U)
+    int64_t ldx, ldu;
+    int32_t M, K, xk, pad;
+};
+
+// Chained plans: the consumers build each call's x' in shared memory of
+// their own, after the stages (no x' travels with the items).  It is the
+// bf16 operand itself (the rotated rows rounded to bf16, in the lanes' MMA
+// order): no scaling into fp16, so no pass over the row for its largest value.
+constexpr int kCPairs = 3;                                 // (token, group) pairs a warp rotates
+constexpr int kCXOff = kGBarOff + 2 * kGStages * 8 + 16;
+constexpr int kCXBytes = 17984;                            // x' rows
+constexpr int kCSmem = kCXOff + kCXBytes + 1024;
+static_assert(kCXOff % 16 == 0, "x' rows 16-byte aligned");
+static_assert(kCSmem <= 232448, "within the opt-in shared memory of a CTA");
+
 struct GroupedParams {
     const GItem *items;
     int64_t nitems;
     int ytype;
     unsigned int *status;
+    const CCall *chain;    // chained plans: the calls
+    unsigned int *done;    // chained plans: finished items per call (zero at launch)
 };
 
 // Barrier 1 among the consumer threads, returning whether any of them
@@ -97,6 +130,120 @@ __device__ __forceinline__ bool consumers_sync_any(bool pred) {
         : "r"(static_cast<uint32_t>(pred)), "r"(kGConsWarps * 32)
         : "memory");
     return r != 0;
+}
+
+// Barrier 2 among the consumer threads (chained plans).
+__device__ __forceinline__ void chain_sync() {
+    asm volatile("bar.sync 2, %0;" ::"r"(kGConsWarps * 32) : "memory");
+}
+
+// Chained plans: wait until *done reaches `target` (every item of the
+// previous call has stored its outputs), for at most kA16WaitLimit cycles.
+// The acquire load orders this thread's later reads after the count; the
+// consumer barrier that follows orders the other threads' reads after it.
+__device__ __forceinline__ bool chain_wait(const unsigned int *done, unsigned int target) {
+    const long long t0 = clock64();
+    while (true) {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(done) : "memory");
+        if (v >= target) return true;
+        if (clock64() - t0 > kA16WaitLimit) return false;
+        __nanosleep(32);
+    }
+}
+
+// A lane's E bf16 values of a group through L2 (ld.global.cg): rows that
+// other CTAs wrote during this launch are never read through the
+// non-coherent path or a stale L1 line.
+__device__ __forceinline__ uint4 load_group_raw_cg(const uint16_t *p, int E) {
+    if (E == 8) return __ldcg(reinterpret_cast<const uint4 *>(p));
+    if (E == 4) {
+        const uint2 u = __ldcg(reinterpret_cast<const uint2 *>(p));
+        return make_uint4(u.x, u.y, 0, 0);
+    }
+    if (E == 2) return make_uint4(__ldcg(reinterpret_cast<const unsigned int *>(p)), 0, 0, 0);
+    return make_uint4(__ldcg(reinterpret_cast<const unsigned short *>(p)), 0, 0, 0);
+}
+
+// Two floats rounded to bf16 (nearest, ties to even) and packed, a low.
+__device__ __forceinline__ uint32_t bf16x2_bits(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+// Chained plans: call cl's input rotated into x' (M bf16 rows of xk in the
+// lanes' MMA order, xpos), by all consumer warps: warp w rotates the (token,
+// group) pairs w, w + 16 and w + 32 (M * groups <= 48).  The arithmetic is
+// that of the decode kernels: the group-256 transform in fp32 rounded to bf16
+// (with U, of h = bf16(silu(X) * U) first).
+template <int BITS>
+__device__ __forceinline__ void chain_rotate(const CCall &cl, uint16_t *xs, int warp, int lane) {
+    constexpr int KB = BITS == 8 ? 64 : 128;
+    const int G = (cl.K + kGroup - 1) / kGroup;
+    const int pairs = cl.M * G;
+    // every load first: the rows come from L2, one round trip for all pairs
+    uint4 raw[kCPairs], rawu[kCPairs];
+#pragma unroll
+    for (int j = 0; j < kCPairs; ++j) {
+        const int q = warp + kGConsWarps * j;
+        raw[j] = rawu[j] = make_uint4(0, 0, 0, 0);
+        if (q < pairs) {
+            const int m = q / G, g = q - m * G;
+            const int64_t gk = static_cast<int64_t>(g) * kGroup;
+            const int e = group_width(cl.K, gk) / 32;
+            raw[j] = load_group_raw_cg(cl.X + m * cl.ldx + gk + lane * e, e);
+            if (cl.U) rawu[j] = load_group_raw_cg(cl.U + m * cl.ldu + gk + lane * e, e);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kCPairs; ++j) {
+        const int q = warp + kGConsWarps * j;
+        if (q < pairs) {
+            const int m = q / G, g = q - m * G;
+            const int gk = g * kGroup;
+            const int n = group_width(cl.K, gk);
+            if (cl.U) raw[j] = swiglu_raw(raw[j], rawu[j]);
+            float v[8];
+            const int E = fwht_group_raw(raw[j], n, v);
+            uint16_t *row = xs + m * cl.xk;
+            if (E == 8) {
+                // a full group: the lane's 8 values land in two runs of 4
+                // (xpos): 8-bit blocks of 64 hold k = 8l..8l+7 at q = 2(l&1)
+                // and q + 1, each run (k0, k2, k1, k3); 4-bit blocks of 128 at
+                // jj = 2(l&3) and jj + 1, runs (k0, k4, k1, k5), (k2, k6, k3, k7)
+                uint16_t *p0, *p1;
+                uint2 w0, w1;
+                if constexpr (BITS == 8) {
+                    p0 = row + gk + (lane >> 3) * 64 + ((lane & 1) * 2) * 16 + 4 * ((lane & 7) >> 1);
+                    p1 = p0 + 16;
+                    w0 = make_uint2(bf16x2_bits(v[0], v[2]), bf16x2_bits(v[1], v[3]));
+                    w1 = make_uint2(bf16x2_bits(v[4], v[6]), bf16x2_bits(v[5], v[7]));
+                } else {
+                    p0 = row + gk + (lane >> 4) * 128 + (2 * (lane & 3)) * 16 + 4 * ((lane & 15) >> 2);
+                    p1 = p0 + 16;
+                    w0 = make_uint2(bf16x2_bits(v[0], v[4]), bf16x2_bits(v[1], v[5]));
+                    w1 = make_uint2(bf16x2_bits(v[2], v[6]), bf16x2_bits(v[3], v[7]));
+                }
+                *reinterpret_cast<uint2 *>(p0) = w0;
+                *reinterpret_cast<uint2 *>(p1) = w1;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (e < E) {
+                        const int kl = gk + lane * E + e;
+                        row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = f32_to_bf16_bits(v[e]);
+                    }
+                }
+            }
+        }
+    }
+    const int tail = cl.xk - cl.K;                  // zeros after K, up to the block edge
+    for (int i = warp * 32 + lane; i < cl.M * tail; i += kGConsWarps * 32) {
+        const int m = i / tail, kl = cl.K + (i - m * tail);
+        xs[m * cl.xk + (kl / KB) * KB + xpos<BITS>(kl % KB)] = 0;
+    }
+    chain_sync();
 }
 
 // Wait with the thread suspended in the barrier between polls (up to ~1 us a
@@ -118,14 +265,36 @@ __device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity)
 
 // One K block (64 bytes of each of the lane's two rows) into the four
 // accumulator chains.  HASB false: rows g + 8 do not exist (an 8-row item).
-template <int BITS, bool HASB>
+// BF: x' is the bf16 operand (chained plans), codes widened to bf16 pairs;
+// else x' is the scaled fp16 form, codes widened to fp16 (4-bit: odd k x16).
+template <int BITS, bool HASB, bool BF>
 __device__ __forceinline__ void block_mma(float (&acc)[4][4], const unsigned char *pa,
                                           const unsigned char *pb, const uint16_t *xblk) {
     const uint4 wa = *reinterpret_cast<const uint4 *>(pa);
     const uint4 wb = HASB ? *reinterpret_cast<const uint4 *>(pb) : make_uint4(0, 0, 0, 0);
     const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w};
     const uint32_t B[4] = {wb.x, wb.y, wb.z, wb.w};
-    if constexpr (BITS == 8) {
+    if constexpr (BF && BITS == 8) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t a0, a1 = 0, a2, a3 = 0;
+            widen_i8(A[q], a0, a2);
+            if (HASB) widen_i8(B[q], a1, a3);
+            const uint2 bv = *reinterpret_cast<const uint2 *>(xblk + q * 16);
+            mma_bf16(acc[q], a0, a1, a2, a3, bv.x, bv.y);
+        }
+    } else if constexpr (BF) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t pa4[4], pb4[4] = {0, 0, 0, 0};
+            widen_i4(A[q], pa4);
+            if (HASB) widen_i4(B[q], pb4);
+            const uint2 b0 = *reinterpret_cast<const uint2 *>(xblk + (2 * q) * 16);
+            const uint2 b1 = *reinterpret_cast<const uint2 *>(xblk + (2 * q + 1) * 16);
+            mma_bf16(acc[(2 * q) % 4], pa4[0], pb4[0], pa4[1], pb4[1], b0.x, b0.y);
+            mma_bf16(acc[(2 * q + 1) % 4], pa4[2], pb4[2], pa4[3], pb4[3], b1.x, b1.y);
+        }
+    } else if constexpr (BITS == 8) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             uint32_t a0, a1 = 0, a2, a3 = 0;
@@ -153,23 +322,23 @@ __device__ __forceinline__ void block_mma(float (&acc)[4][4], const unsigned cha
 // blocks cst bytes apart; the lane's 16-byte unit of an even / odd block at
 // offE / offO within its swizzled row line); else rows of 64-byte blocks.
 // Blocks go in pairs, so each step has two blocks' loads in flight.
-template <int BITS, bool TILES, bool HASB>
+template <int BITS, bool TILES, bool HASB, bool BF>
 __device__ __forceinline__ void tile_blocks(float (&acc)[4][4], const unsigned char *pA,
                                             const unsigned char *pB, const uint16_t *xb, int b,
                                             int bend, int cst, int offE, int offO) {
     constexpr int KB = BITS == 8 ? 64 : 128;   // k per block
     auto off = [&](int blk) { return TILES ? (blk >> 1) * cst + ((blk & 1) ? offO : offE) : blk * 64; };
     if (TILES && b < bend && (b & 1)) {        // a run that starts on an odd block
-        block_mma<BITS, HASB>(acc, pA + off(b), pB + off(b), xb + b * KB);
+        block_mma<BITS, HASB, BF>(acc, pA + off(b), pB + off(b), xb + b * KB);
         ++b;
     }
     for (; b + 1 < bend; b += 2) {
         const int o0 = TILES ? (b >> 1) * cst + offE : b * 64;
         const int o1 = TILES ? o0 - offE + offO : o0 + 64;
-        block_mma<BITS, HASB>(acc, pA + o0, pB + o0, xb + b * KB);
-        block_mma<BITS, HASB>(acc, pA + o1, pB + o1, xb + (b + 1) * KB);
+        block_mma<BITS, HASB, BF>(acc, pA + o0, pB + o0, xb + b * KB);
+        block_mma<BITS, HASB, BF>(acc, pA + o1, pB + o1, xb + (b + 1) * KB);
     }
-    if (b < bend) block_mma<BITS, HASB>(acc, pA + off(b), pB + off(b), xb + b * KB);
+    if (b < bend) block_mma<BITS, HASB, BF>(acc, pA + off(b), pB + off(b), xb + b * KB);
 }
 
 // x' of one call (one warp per call, eight calls per CTA), in the order the
@@ -254,7 +423,7 @@ k_rotate_grouped(const GCall *calls, int64_t ncalls) {
     }
 }
 
-template <int BITS>
+template <int BITS, bool CHAIN>
 __global__ void __launch_bounds__(kGThreads, 1)
 k_gemv_grouped(const GroupedParams p) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -309,17 +478,19 @@ k_gemv_grouped(const GroupedParams p) {
             const int nch = (it.rbytes + 127) / 128;
             if (lane == 0) {
                 *reinterpret_cast<GItem *>(hdr + s * 128) = it;
-                const uint32_t xbytes = static_cast<uint32_t>(it.M) * it.xk * 2 + kXTail;
+                // chained plans: no x' with the item (its consumers rotate the input)
+                const uint32_t xbytes = CHAIN ? 0u : static_cast<uint32_t>(it.M) * it.xk * 2 + kXTail;
                 // a tensor copy counts its whole box, zero fill included
                 const uint32_t wbytes = it.tiles ? static_cast<uint32_t>(nch * it.rb * 128)
                                                  : static_cast<uint32_t>(it.rows * it.rbytes);
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full),
                              "r"(wbytes + xbytes)
                              : "memory");
-                asm volatile(
-                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                    ::"r"(smem_addr(st + it.xoff)), "l"(it.xq), "r"(xbytes), "r"(full)
-                    : "memory");
+                if (!CHAIN)
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                        ::"r"(smem_addr(st + it.xoff)), "l"(it.xq), "r"(xbytes), "r"(full)
+                        : "memory");
             }
             __syncwarp();
             if (it.tiles) {
@@ -358,6 +529,8 @@ k_gemv_grouped(const GroupedParams p) {
     // run leaves the tile.  The partial sums of a row are then added over the
     // warps in warp order: the result does not depend on timing.
     const int g = lane >> 2, t = lane & 3;
+    int cur = -1;                                  // chained plans: the call x' holds
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem + kCXOff);
     for (int64_t k = 0;; ++k) {
         const int64_t i = blockIdx.x + k * grid;
         if (i >= p.nitems) break;
@@ -370,6 +543,8 @@ k_gemv_grouped(const GroupedParams p) {
         const float *swp = nullptr;
         void *y = nullptr;
         int64_t ldy = 0;
+        int ci = 0;
+        uint32_t cwait = 0;
         if (ok) {
             const GItem &h = *reinterpret_cast<const GItem *>(hdr + s * 128);
             rows = h.rows;
@@ -382,6 +557,34 @@ k_gemv_grouped(const GroupedParams p) {
             swp = h.sw;
             y = h.y;
             ldy = h.ldy;
+            ci = h.call;
+            cwait = h.wait;
+        }
+        if constexpr (CHAIN) {
+            // the first item of a call in this CTA: wait for the previous
+            // call, then rotate this call's input (every consumer holds the
+            // same header once the barrier passes, or all of them stop)
+            if (consumers_sync_any(!ok)) {
+                if (threadIdx.x == 0) {
+                    *abort_sh = 1;
+                    atomicOr(p.status, kStatusGroupedTimeout);
+                }
+                break;
+            }
+            if (ci != cur) {
+                const CCall cl = p.chain[ci];          // its load overlaps the wait
+                bool dep = true;
+                if (threadIdx.x == 0 && cwait > 0) dep = chain_wait(p.done + ci - 1, cwait);
+                if (consumers_sync_any(!dep)) {
+                    if (threadIdx.x == 0) {
+                        *abort_sh = 1;
+                        atomicOr(p.status, kStatusGroupedTimeout);
+                    }
+                    break;
+                }
+                chain_rotate<BITS>(cl, xs, warp, lane);
+                cur = ci;
+            }
         }
         const int NB = xk / KB, U = ((rb + 15) / 16) * NB;
         const int u0 = U * warp / kGConsWarps, u1 = U * (warp + 1) / kGConsWarps;
@@ -393,11 +596,11 @@ k_gemv_grouped(const GroupedParams p) {
         const int m_st = store ? j / rows : 0, r_st = store ? j % rows : 0;
         const float swv = store ? __ldg(swp + r_st) : 0.0f;
         // the token's 2^-e (after the x' rows), read before the stage is released
-        const float dsc = store ? reinterpret_cast<const float *>(smem + s * kGStageBytes + xoff + M * xk * 2)[m_st]
-                                : 1.0f;
+        const float dsc = (!store || CHAIN) ? 1.0f
+                          : reinterpret_cast<const float *>(smem + s * kGStageBytes + xoff + M * xk * 2)[m_st];
         if (ok && u0 < u1) {
             const unsigned char *st = smem + s * kGStageBytes;
-            const uint16_t *xb = reinterpret_cast<const uint16_t *>(st + xoff) + (g < M ? g : 0) * xk + 4 * t;
+            const uint16_t *xb = (CHAIN ? xs : reinterpret_cast<const uint16_t *>(st + xoff)) + (g < M ? g : 0) * xk + 4 * t;
             // shared row of fragment row g: in the tile form the two rows a
             // quarter-warp reads are 4 apart, so their swizzled units fall in
             // opposite halves of the 128-byte line (no bank conflict)
@@ -421,11 +624,11 @@ k_gemv_grouped(const GroupedParams p) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.0f;
                 if (tiles) {
-                    if (hasB) tile_blocks<BITS, true, true>(acc, pA, pB, xb, b, bend, cst, offE, offO);
-                    else tile_blocks<BITS, true, false>(acc, pA, pB, xb, b, bend, cst, offE, offO);
+                    if (hasB) tile_blocks<BITS, true, true, CHAIN>(acc, pA, pB, xb, b, bend, cst, offE, offO);
+                    else tile_blocks<BITS, true, false, CHAIN>(acc, pA, pB, xb, b, bend, cst, offE, offO);
                 } else {
-                    if (hasB) tile_blocks<BITS, false, true>(acc, pA, pB, xb, b, bend, cst, offE, offO);
-                    else tile_blocks<BITS, false, false>(acc, pA, pB, xb, b, bend, cst, offE, offO);
+                    if (hasB) tile_blocks<BITS, false, true, CHAIN>(acc, pA, pB, xb, b, bend, cst, offE, offO);
+                    else tile_blocks<BITS, false, false, CHAIN>(acc, pA, pB, xb, b, bend, cst, offE, offO);
                 }
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -453,6 +656,7 @@ k_gemv_grouped(const GroupedParams p) {
         if (store) {
             const int tile = r_st >> 4;
             float sum = 0.0f;
+#pragma unroll
             for (int w = 0; w < kGConsWarps; ++w) {
                 // warps whose (non-empty) run touches the row's tile wrote a partial
                 const int a = U * w / kGConsWarps, b = U * (w + 1) / kGConsWarps;
@@ -464,6 +668,13 @@ k_gemv_grouped(const GroupedParams p) {
                 static_cast<float *>(y)[off] = yv;
             else
                 static_cast<uint16_t *>(y)[off] = f32_to_bf16_bits(yv);
+        }
+        if constexpr (CHAIN) {
+            // every output of the item is stored (the barrier orders them
+            // before thread 0's release): count it done
+            chain_sync();
+            if (threadIdx.x == 0)
+                asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p.done + ci), "r"(1u) : "memory");
         }
     }
 }
@@ -484,6 +695,30 @@ int grouped_item_rows(int64_t M, int64_t K, int bits) {
     return rb >= 16 ? static_cast<int>(rb / 16 * 16) : (rb >= 8 ? 8 : 0);
 }
 
+// Rows of one work item of a chained plan.  The stage holds weight rows only
+// (the consumers rotate the input into x' of their own, which must hold the
+// call: M * xk * 2 bytes, M * groups <= 48), and a call is spread over
+// up to `grid` CTAs so that each call runs on as many SMs as it can: the
+// fewest rows (8, else a multiple of 16) that deal the call over the grid,
+// at most a stage's worth.  grid 0: 8 rows (the most items a call can have).
+int chain_item_rows(int64_t M, int64_t K, int64_t N, int bits, int grid) {
+    if (M < 1 || M > TQ_MAX_M_GROUPED || K < 1 || N < 1) return 0;
+    const int64_t KB = bits == 8 ? 64 : 128;
+    const int64_t xk = (K + KB - 1) / KB * KB;
+    if (M * xk * 2 > kCXBytes) return 0;
+    if (M * ((K + kGroup - 1) / kGroup) > kGConsWarps * kCPairs) return 0;
+    const int64_t rbytes = K * bits / 8;
+    const int64_t ws = (rbytes + 127) / 128 * 128 + 64;
+    int64_t fit = kGStageBytes / ws;
+    if (fit > kGRed / M) fit = kGRed / M;
+    fit = fit >= 16 ? fit / 16 * 16 : (fit >= 8 ? 8 : 0);
+    if (fit == 0) return 0;
+    if (grid <= 0) return 8;
+    int64_t want = (N + grid - 1) / grid;
+    want = want <= 8 ? 8 : (want + 15) / 16 * 16;
+    return static_cast<int>(want < fit ? want : fit);
+}
+
 }  // namespace tq
 
 // The plan: where its tables and x' workspace sit in the caller's device
@@ -498,6 +733,10 @@ struct tq_grouped_s {
     tq::GCall *calls;
     tq::GItem *items;
     int64_t weight_bytes;
+    int chain;            // 1: a chained plan (calls in order, one cooperative launch)
+    int64_t nccalls;
+    tq::CCall *ccalls;
+    unsigned int *done;   // finished items per call, zeroed before each run
 };
 
 namespace tq {
@@ -506,23 +745,26 @@ namespace {
 
 struct GroupedTables {
     std::vector<GCall> calls;
+    std::vector<CCall> ccalls;         // chained plans
     std::vector<GItem> items;
     std::vector<CUtensorMap> maps;     // one per call in the tile form
-    size_t calls_bytes = 0, items_bytes = 0, maps_bytes = 0, x_bytes = 0;
+    size_t calls_bytes = 0, items_bytes = 0, maps_bytes = 0, x_bytes = 0, ccalls_bytes = 0, done_bytes = 0;
     int64_t weight_bytes = 0;
-    size_t total() const { return calls_bytes + items_bytes + maps_bytes + x_bytes; }
+    size_t total() const { return calls_bytes + items_bytes + maps_bytes + x_bytes + ccalls_bytes + done_bytes; }
 };
 
 // Host tables of a plan, with x' and tensor-map addresses as offsets into
 // their areas.  `encode` false: sizes only (every short-row call counted in
-// the tile form).
-tq_status grouped_tables(const tq_a16_call *calls, int64_t n, int bits, int ytype, bool encode,
-                         GroupedTables &t) {
+// the tile form).  `chain` non-NULL: a chained plan of those calls (`calls`
+// unused), its items sized for `grid` CTAs (0: the most items).
+tq_status grouped_tables(const tq_a16_call *calls, const tq_chain_call *chain, int64_t n, int bits, int ytype,
+                         bool encode, int grid, GroupedTables &t) {
     const int64_t KB = bits == 8 ? 64 : 128;
+    uint32_t prev_items = 0, wait = 0;
     for (int64_t c = 0; c < n; ++c) {
-        const tq_a16_call &a = calls[c];
+        const tq_a16_call &a = chain ? chain[c].call : calls[c];
         if (a.M == 0 || a.N == 0) continue;
-        const int rb = grouped_item_rows(a.M, a.K, bits);
+        const int rb = chain ? chain_item_rows(a.M, a.K, a.N, bits, grid) : grouped_item_rows(a.M, a.K, bits);
         if (rb == 0) return TQ_ERR_SHAPE;
         GCall g{};
         g.X = static_cast<const uint16_t *>(a.X);
@@ -530,16 +772,32 @@ tq_status grouped_tables(const tq_a16_call *calls, int64_t n, int bits, int ytyp
         g.M = static_cast<int32_t>(a.M);
         g.K = static_cast<int32_t>(a.K);
         g.xk = static_cast<int32_t>((a.K + KB - 1) / KB * KB);
-        g.xq = reinterpret_cast<uint16_t *>(static_cast<uintptr_t>(t.x_bytes));
-        t.calls.push_back(g);
-        t.x_bytes += static_cast<size_t>(a.M) * g.xk * 2 + kXTail;   // a multiple of 32
+        if (chain) {
+            CCall cc{};
+            cc.X = g.X;
+            cc.U = static_cast<const uint16_t *>(chain[c].U);
+            cc.ldx = a.ldx;
+            cc.ldu = chain[c].U ? chain[c].ldu : 0;
+            cc.M = g.M;
+            cc.K = g.K;
+            cc.xk = g.xk;
+            t.ccalls.push_back(cc);
+            wait = prev_items;
+            prev_items = static_cast<uint32_t>((a.N + rb - 1) / rb);
+        } else {
+            g.xq = reinterpret_cast<uint16_t *>(static_cast<uintptr_t>(t.x_bytes));
+            t.calls.push_back(g);
+            t.x_bytes += static_cast<size_t>(a.M) * g.xk * 2 + kXTail;   // a multiple of 32
+        }
         const int64_t rbytes = a.K * bits / 8;
         const int64_t ws = (rbytes + 127) / 128 * 128 + 64;
         const int64_t nch = (rbytes + 127) / 128;
         t.weight_bytes += a.N * rbytes + 4 * a.N;
         // the tile form when its copies (one per 128-byte chunk) are fewer
-        // than the rows of an item
-        bool tiles = nch < rb;
+        // than the rows of an item (sizes of a chained plan: its largest
+        // items, so that every tensor map a plan may hold is counted)
+        const int rb_form = chain && !encode ? chain_item_rows(a.M, a.K, a.N, bits, 1) : rb;
+        bool tiles = nch < rb_form;
         const void *map_off = nullptr;
         if (tiles) {
             CUtensorMap m;
@@ -567,9 +825,13 @@ tq_status grouped_tables(const tq_a16_call *calls, int64_t n, int bits, int ytyp
             it.ws = static_cast<int32_t>(ws);
             it.xk = g.xk;
             it.M = static_cast<int16_t>(a.M);
+            it.call = chain ? static_cast<int32_t>(t.ccalls.size() - 1) : 0;
+            it.wait = chain ? wait : 0;
             t.items.push_back(it);
         }
     }
+    t.ccalls_bytes = (t.ccalls.size() * sizeof(CCall) + 255) / 256 * 256;
+    t.done_bytes = (t.ccalls.size() * 4 + 255) / 256 * 256;
     t.calls_bytes = (t.calls.size() * sizeof(GCall) + 255) / 256 * 256;
     t.items_bytes = (t.items.size() * sizeof(GItem) + 255) / 256 * 256;
     t.maps_bytes = (t.maps.size() * sizeof(CUtensorMap) + 255) / 256 * 256;
@@ -580,27 +842,43 @@ tq_status grouped_tables(const tq_a16_call *calls, int64_t n, int bits, int ytyp
 
 tq_status grouped_bytes(const tq_a16_call *calls, int64_t n, int bits, size_t *bytes) {
     GroupedTables t;
-    const tq_status st = grouped_tables(calls, n, bits, 0, false, t);
+    const tq_status st = grouped_tables(calls, nullptr, n, bits, 0, false, 0, t);
     if (st == TQ_OK) *bytes = t.total();
     return st;
 }
 
-tq_status grouped_create(const tq_a16_call *calls, int64_t n, int bits, int ytype, void *dmem,
-                         size_t dbytes, const DeviceInfo &dev, tq_grouped *out) {
+tq_status chain_bytes(const tq_chain_call *calls, int64_t n, int bits, size_t *bytes) {
     GroupedTables t;
-    tq_status st = grouped_tables(calls, n, bits, ytype, true, t);
+    const tq_status st = grouped_tables(nullptr, calls, n, bits, 0, false, 0, t);
+    if (st == TQ_OK) *bytes = t.total();
+    return st;
+}
+
+namespace {
+
+// Both kinds of plan: tables into `dmem` (calls, items, tensor maps, x' or
+// the chained calls and their counters, in that order), then the handle.
+tq_status plan_create(const tq_a16_call *calls, const tq_chain_call *chain, int64_t n, int bits, int ytype,
+                      void *dmem, size_t dbytes, const DeviceInfo &dev, tq_grouped *out) {
+    GroupedTables t;
+    tq_status st = grouped_tables(calls, chain, n, bits, ytype, true, chain ? dev.sms : 0, t);
     if (st != TQ_OK) return st;
     if (t.total() > 0 && (!dmem || dbytes < t.total())) return TQ_ERR_WORKSPACE;
     unsigned char *base = static_cast<unsigned char *>(dmem);
     unsigned char *mbase = base + t.calls_bytes + t.items_bytes;
     unsigned char *xbase = mbase + t.maps_bytes;
+    unsigned char *cbase = xbase + t.x_bytes;
+    unsigned char *dbase = cbase + t.ccalls_bytes;
     for (GCall &g : t.calls) g.xq = reinterpret_cast<uint16_t *>(xbase + reinterpret_cast<uintptr_t>(g.xq));
     for (GItem &it : t.items) {
-        it.xq = reinterpret_cast<const uint16_t *>(xbase + reinterpret_cast<uintptr_t>(it.xq));
+        it.xq = chain ? nullptr : reinterpret_cast<const uint16_t *>(xbase + reinterpret_cast<uintptr_t>(it.xq));
         if (it.tiles) it.tmap = mbase + reinterpret_cast<uintptr_t>(it.tmap);
     }
     cudaError_t e = cudaSuccess;
-    if (!t.calls.empty()) e = cudaMemcpy(base, t.calls.data(), t.calls.size() * sizeof(GCall), cudaMemcpyHostToDevice);
+    if (!t.ccalls.empty())
+        e = cudaMemcpy(cbase, t.ccalls.data(), t.ccalls.size() * sizeof(CCall), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !t.calls.empty())
+        e = cudaMemcpy(base, t.calls.data(), t.calls.size() * sizeof(GCall), cudaMemcpyHostToDevice);
     if (e == cudaSuccess && !t.items.empty())
         e = cudaMemcpy(base + t.calls_bytes, t.items.data(), t.items.size() * sizeof(GItem),
                        cudaMemcpyHostToDevice);
@@ -618,16 +896,80 @@ tq_status grouped_create(const tq_a16_call *calls, int64_t n, int bits, int ytyp
     plan->calls = reinterpret_cast<GCall *>(base);
     plan->items = reinterpret_cast<GItem *>(base + t.calls_bytes);
     plan->weight_bytes = t.weight_bytes;
+    plan->chain = chain ? 1 : 0;
+    plan->nccalls = static_cast<int64_t>(t.ccalls.size());
+    plan->ccalls = reinterpret_cast<CCall *>(cbase);
+    plan->done = reinterpret_cast<unsigned int *>(dbase);
     *out = plan;
     return TQ_OK;
 }
 
+}  // namespace
+
+tq_status grouped_create(const tq_a16_call *calls, int64_t n, int bits, int ytype, void *dmem,
+                         size_t dbytes, const DeviceInfo &dev, tq_grouped *out) {
+    return plan_create(calls, nullptr, n, bits, ytype, dmem, dbytes, dev, out);
+}
+
+tq_status chain_create(const tq_chain_call *calls, int64_t n, int bits, int ytype, void *dmem,
+                       size_t dbytes, const DeviceInfo &dev, tq_grouped *out) {
+    return plan_create(nullptr, calls, n, bits, ytype, dmem, dbytes, dev, out);
+}
+
+namespace {
+
+// A chained plan's run: the counters zeroed, then one cooperative launch
+// (every CTA resident, as the waits between calls need).
+tq_status chain_run(tq_grouped plan, const DeviceInfo &dev, cudaStream_t s) {
+    auto kern = plan->bits == 8 ? k_gemv_grouped<8, true> : k_gemv_grouped<4, true>;
+    static int configured_for[64][2] = {{0}};
+    const int bi = plan->bits == 8 ? 0 : 1;
+    if (dev.id < 0 || dev.id >= 64) return TQ_ERR_DEVICE;
+    if (!configured_for[dev.id][bi]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCSmem);
+        if (e != cudaSuccess) return cuda_fail(e);
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGThreads, kCSmem);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (per_sm < 1) return TQ_ERR_DEVICE;
+        configured_for[dev.id][bi] = 1;
+    }
+    if (plan->grid > dev.sms) return TQ_ERR_DEVICE;
+    unsigned int *status = status_word();
+    if (!status) return TQ_ERR_CUDA;
+    cudaError_t e = cudaMemsetAsync(plan->done, 0, static_cast<size_t>(plan->nccalls) * 4, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    GroupedParams p;
+    p.items = plan->items;
+    p.nitems = plan->nitems;
+    p.ytype = plan->ytype;
+    p.status = status;
+    p.chain = plan->ccalls;
+    p.done = plan->done;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan->grid));
+    cfg.blockDim = dim3(kGThreads);
+    cfg.dynamicSmemBytes = kCSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+}  // namespace
+
 // phase 1: the rotation pre-pass; 2: the product; 3: both
 tq_status grouped_run(tq_grouped plan, const DeviceInfo &dev, int phase, cudaStream_t s) {
     if (plan->device != dev.id) return TQ_ERR_DEVICE;
+    if (plan->chain && phase != 3) return TQ_ERR_MODE;    // one launch: no phases to split
     if (plan->nitems == 0) return TQ_OK;
+    if (plan->chain) return chain_run(plan, dev, s);
     auto rot = plan->bits == 8 ? k_rotate_grouped<8> : k_rotate_grouped<4>;
-    auto kern = plan->bits == 8 ? k_gemv_grouped<8> : k_gemv_grouped<4>;
+    auto kern = plan->bits == 8 ? k_gemv_grouped<8, false> : k_gemv_grouped<4, false>;
     static int configured_for[64][2] = {{0}};
     const int bi = plan->bits == 8 ? 0 : 1;
     if (dev.id >= 0 && dev.id < 64 && !configured_for[dev.id][bi]) {
@@ -649,6 +991,8 @@ tq_status grouped_run(tq_grouped plan, const DeviceInfo &dev, int phase, cudaStr
         p.nitems = plan->nitems;
         p.ytype = plan->ytype;
         p.status = status;
+        p.chain = nullptr;
+        p.done = nullptr;
         kern<<<static_cast<unsigned>(plan->grid), kGThreads, kGSmem, s>>>(p);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e);

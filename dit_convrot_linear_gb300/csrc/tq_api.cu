@@ -124,6 +124,26 @@ tq_status check_grouped(const tq_a16_call *calls, int64_t n, int bits, tq_out yt
     return TQ_OK;
 }
 
+// The checks of a chained plan: each call as a grouped call, plus its up rows.
+tq_status check_chain(const tq_chain_call *calls, int64_t n, int bits, tq_out ytype) {
+    if (bits != 8 && bits != 4) return TQ_ERR_BITS;
+    if (ytype != TQ_OUT_F32 && ytype != TQ_OUT_BF16) return TQ_ERR_MODE;
+    if (n < 0) return TQ_ERR_SHAPE;
+    if (n > 0 && !calls) return TQ_ERR_NULL;
+    for (int64_t c = 0; c < n; ++c) {
+        const tq_a16_call &a = calls[c].call;
+        if (a.M < 0 || a.M > TQ_MAX_M_GROUPED || a.N < 0 || !valid_k(a.K)) return TQ_ERR_SHAPE;
+        if (a.M == 0 || a.N == 0) continue;
+        tq_status st = check_bf16_rows(a.X, a.M, a.K, a.ldx);
+        if (st != TQ_OK) return st;
+        if (calls[c].U && (st = check_bf16_rows(calls[c].U, a.M, a.K, calls[c].ldu)) != TQ_OK) return st;
+        if ((st = check_weights(a.Wq, a.sw, a.N, a.K, bits)) != TQ_OK) return st;
+        if ((st = check_output(a.Y, a.M, a.N, a.ldy, out_size(ytype))) != TQ_OK) return st;
+        if (chain_item_rows(a.M, a.K, a.N, bits, 0) == 0) return TQ_ERR_SHAPE;
+    }
+    return TQ_OK;
+}
+
 }  // namespace
 }  // namespace tq
 
@@ -581,6 +601,27 @@ tq_status tq_grouped_run(tq_grouped plan, cudaStream_t stream) { return grouped_
 tq_status tq_grouped_rotate(tq_grouped plan, cudaStream_t stream) { return grouped_phase(plan, 1, stream); }
 
 tq_status tq_grouped_product(tq_grouped plan, cudaStream_t stream) { return grouped_phase(plan, 2, stream); }
+
+tq_status tq_chain_bytes(const tq_chain_call *calls, int64_t ncalls, int bits, size_t *bytes) {
+    if (!bytes) return TQ_ERR_NULL;
+    const tq_status st = check_chain(calls, ncalls, bits, TQ_OUT_F32);
+    if (st != TQ_OK) return st;
+    return chain_bytes(calls, ncalls, bits, bytes);
+}
+
+tq_status tq_chain_create(const tq_chain_call *calls, int64_t ncalls, int bits, tq_out ytype,
+                          void *dmem, size_t dbytes, tq_grouped *plan) {
+    if (!plan) return TQ_ERR_NULL;
+    tq_status st = check_chain(calls, ncalls, bits, ytype);
+    if (st != TQ_OK) return st;
+    size_t need = 0;
+    if ((st = chain_bytes(calls, ncalls, bits, &need)) != TQ_OK) return st;
+    if (need > 0 && (!dmem || dbytes < need)) return TQ_ERR_WORKSPACE;
+    if (dmem && !aligned(dmem, 256)) return TQ_ERR_ALIGN;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != TQ_OK) return st;
+    return chain_create(calls, ncalls, bits, ytype == TQ_OUT_BF16 ? 1 : 0, dmem, dbytes, dev, plan);
+}
 
 int64_t tq_grouped_weight_bytes(tq_grouped plan) { return plan ? grouped_weight_bytes(plan) : 0; }
 

@@ -115,6 +115,10 @@ int grouped_item_rows(int64_t M, int64_t K, int bits);
 tq_status grouped_bytes(const tq_a16_call *calls, int64_t n, int bits, size_t *bytes);
 tq_status grouped_create(const tq_a16_call *calls, int64_t n, int bits, int ytype, void *dmem,
                          size_t dbytes, const DeviceInfo &dev, tq_grouped *out);
+tq_status chain_bytes(const tq_chain_call *calls, int64_t n, int bits, size_t *bytes);
+tq_status chain_create(const tq_chain_call *calls, int64_t n, int bits, int ytype, void *dmem,
+                       size_t dbytes, const DeviceInfo &dev, tq_grouped *out);
+int chain_item_rows(int64_t M, int64_t K, int64_t N, int bits, int grid);
 tq_status grouped_run(tq_grouped plan, const DeviceInfo &dev, int phase, cudaStream_t s);
 void grouped_destroy(tq_grouped plan);
 int64_t grouped_weight_bytes(tq_grouped plan);

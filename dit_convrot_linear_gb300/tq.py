@@ -56,6 +56,8 @@ SIGNATURES = {
     "tq_grouped_product": (_C, [_P, _P]),
     "tq_grouped_weight_bytes": (_I, [_P]),
     "tq_grouped_destroy": (None, [_P]),
+    "tq_chain_bytes": (_C, [_P, _I, _C, ctypes.POINTER(ctypes.c_size_t)]),
+    "tq_chain_create": (_C, [_P, _I, _C, _C, _P, _Z, ctypes.POINTER(ctypes.c_void_p)]),
     "tq_quantize_weights_blocked": (_C, [_P, _I, _I, _I, _C, _C, _C, _P, _P, _P]),
     "tq_linear_blocked": (_C, [_P, _I, _I, _I, _P, _P, _C, _I, _C, _C, _P, _C, _I, _P]),
 }
@@ -70,6 +72,11 @@ class A16Call(ctypes.Structure):
     """``tq_a16_call``: one call of a grouped plan."""
     _fields_ = [("X", _P), ("ldx", _I), ("Wq", _P), ("sw", _P), ("Y", _P), ("ldy", _I),
                 ("M", _I), ("N", _I), ("K", _I)]
+
+
+class ChainCall(ctypes.Structure):
+    """``tq_chain_call``: one call of a chained plan (U NULL, or the up rows)."""
+    _fields_ = [("call", A16Call), ("U", _P), ("ldu", _I)]
 
 _lib = None
 
@@ -520,6 +527,14 @@ def grouped_bytes(calls, bits: int) -> int:
     return int(out.value)
 
 
+def chain_bytes(calls, bits: int) -> int:
+    """Device bytes a chained plan of these ``ChainCall`` records needs."""
+    arr = (ChainCall * max(len(calls), 1))(*calls)
+    out = ctypes.c_size_t(0)
+    _check(lib().tq_chain_bytes(ctypes.addressof(arr), len(calls), bits, ctypes.byref(out)), "tq_chain_bytes")
+    return int(out.value)
+
+
 class GroupedPlan:
     """Independent A16 calls run as one pass over their weights
     (``tq_grouped_create`` / ``tq_grouped_run``).
@@ -584,4 +599,47 @@ class GroupedPlan:
 
     def __del__(self):
         self.close()
+
+
+class ChainPlan(GroupedPlan):
+    """Dependent A16 calls run in order in one launch (``tq_chain_create``,
+    run with ``tq_grouped_run``): call c may read any earlier call's Y.
+
+    ``calls`` is a list of ``(X, Wq, sw, N, Y)`` or ``(X, Wq, sw, N, Y, U)``:
+    as ``GroupedPlan``'s, U (bf16 [M, K], any row stride) making the call's
+    input the SwiGLU of X and U."""
+
+    def __init__(self, calls, bits: int, out: str = "f32"):
+        import torch
+        if out not in ("f32", "bf16"):
+            raise ValueError("a chained plan writes f32 or bf16")
+        recs, keep, dev = [], [], None
+        for c in calls:
+            X, Wq, sw, N, Y = c[:5]
+            U = c[5] if len(c) > 5 else None
+            M, K = X.shape
+            _req(X, "X", dtype=torch.bfloat16, rows=M, cols=K)
+            if U is not None:
+                if tuple(U.shape) != (M, K):
+                    raise ValueError(f"U is {tuple(U.shape)}, expected {(M, K)}")
+                _req(U, "U", dtype=torch.bfloat16, rows=M, cols=K)
+            _weights(Wq, sw, N, K, bits)
+            _req(Y, "Y", dtype=_dt(out), rows=M, cols=N)
+            dev = X.device if dev is None else dev
+            recs.append(ChainCall(A16Call(_ptr(X), X.stride(0), _ptr(Wq), _ptr(sw), _ptr(Y), Y.stride(0),
+                                          M, N, K),
+                                  _ptr(U), U.stride(0) if U is not None else 0))
+            keep.extend([X, Wq, sw, Y] + ([U] if U is not None else []))
+        need = chain_bytes(recs, bits)
+        self.buffer = torch.empty(max(need, 1), dtype=torch.uint8,
+                                  device=dev if dev is not None else "cuda")
+        arr = (ChainCall * max(len(recs), 1))(*recs)
+        h = ctypes.c_void_p(None)
+        _check(lib().tq_chain_create(ctypes.addressof(arr), len(recs), bits, OUT[out],
+                                     _ptr(self.buffer), _nbytes(self.buffer), ctypes.byref(h)),
+               "tq_chain_create")
+        self._h = h
+        self._keep = keep
+        self.bits = bits
+        self.ncalls = len(recs)
 

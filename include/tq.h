@@ -595,6 +595,52 @@ int64_t tq_grouped_weight_bytes(tq_grouped plan);
 /* Frees the host handle (the device buffer stays the caller's).  NULL is ignored. */
 void tq_grouped_destroy(tq_grouped plan);
 
+/*
+ * Chained plans: decode calls that depend on one another, run in order in
+ * one launch, the way a decoder walks its layers (kvad-gpu internals,
+ * "Numbers": decode runs one projection at a time, each input the previous
+ * output, and is bound by the weight stream).  Call c starts only after every
+ * earlier call has finished, so its X (and U) may be any earlier call's Y.
+ * The launch keeps streaming later calls' weights into shared memory while
+ * earlier calls finish; between calls its CTAs wait on counters in the plan's
+ * buffer (bounded waits: on expiry tq_device_status reports
+ * TQ_ERR_DEVICE_TIMEOUT and the outputs of unfinished calls are unwritten).
+ * The launch is cooperative: it needs every SM free of other work while it
+ * runs (another kernel on the device delays its start).
+ *
+ * Each call is a grouped call, optionally with the SwiGLU of two rows as its
+ * input: with U set, the product reads h = bf16(silu(X) * U), silu(g) =
+ * g / (1 + e^-g) (the arithmetic of tq_linear_swiglu), as a gated FFN's down
+ * projection takes the two halves of its gate+up output.
+ */
+typedef struct {
+    tq_a16_call call;   /* as in a grouped plan; X holds the gate rows when U is set */
+    const void *U;      /* NULL, or bf16 [M, K] up rows at U + m * ldu (X's rules) */
+    int64_t ldu;
+} tq_chain_call;
+
+/* Bytes of device memory a chained plan of these calls needs (no device
+ * needed; the refusals of tq_chain_create). */
+tq_status tq_chain_bytes(const tq_chain_call *calls, int64_t ncalls, int bits, size_t *bytes);
+
+/*
+ * Checks every call and writes the chained plan's tables into `dmem`;
+ * arguments and ownership as tq_grouped_create.  Each call follows
+ * tq_linear's rules for X, U, Wq, sw, Y and strides, with M <= 8; in
+ * addition its rotated input must fit the launch's own buffer (2 * M * K
+ * bytes, K rounded up to 64 for 8-bit and 128 for 4-bit weights, at most
+ * 17984) and eight weight rows a 64 KB stage, or the call is refused with
+ * TQ_ERR_SHAPE (for M = 1: K up to 8064 with 8-bit weights, 8960 with 4-bit).
+ * A call's Y must not overlap its own X or U, nor any call's Wq or sw; it
+ * may overlap an earlier call's X, U or Y (later calls run after them).
+ * Run the plan with tq_grouped_run (the counters are zeroed, then one
+ * launch; capturable in a CUDA graph); tq_grouped_rotate and
+ * tq_grouped_product refuse a chained plan with TQ_ERR_MODE.  Runs of one
+ * plan are ordered (they share its counters).
+ */
+tq_status tq_chain_create(const tq_chain_call *calls, int64_t ncalls, int bits, tq_out ytype,
+                          void *dmem, size_t dbytes, tq_grouped *plan);
+
 #ifdef __cplusplus
 }
 #endif

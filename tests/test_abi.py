@@ -245,19 +245,19 @@ def test_grouped_refusals(L):
 
 def test_grouped_bytes_count_tables_and_rotated_inputs(L):
     # M = 1, K = 896, N = 4864, 8-bit: items of 64 rows (960-byte shared rows,
-    # 1792 bytes of x' per item) -> 76 items of 80 bytes (6080, rounded to
-    # 6144); one 40-byte call record and one 128-byte tensor map (rows of 7
+    # 1792 bytes of x' per item) -> 76 items of 88 bytes (6688, rounded to
+    # 6912); one 40-byte call record and one 128-byte tensor map (rows of 7
     # chunks of 128 bytes: the tile form), each rounded to 256; x' of 896 fp16
     # and a 32-byte tail (the token scales)
-    assert gbytes(L, gcalls()) == (OK, 256 + 6144 + 256 + 896 * 2 + 32)
+    assert gbytes(L, gcalls()) == (OK, 256 + 6912 + 256 + 896 * 2 + 32)
     # two tokens, K = 544 (x' padded to 640 columns), N = 100, 4-bit: two
     # items of 64 rows, tile form
     calls = gcalls(M=2, N=100, K=544, ldx=544, ldy=100)
     assert gbytes(L, calls, bits=4) == (OK, 256 + 256 + 256 + 2 * 640 * 2 + 32)
     # long rows (K = 4864: 38 chunks, items of 8 rows) stay in the row form:
-    # no tensor map; 112 items of 80 bytes
+    # no tensor map; 112 items of 88 bytes
     calls = gcalls(N=896, K=4864, ldx=4864, ldy=896)
-    assert gbytes(L, calls) == (OK, 256 + 8960 + 4864 * 2 + 32)
+    assert gbytes(L, calls) == (OK, 256 + 9984 + 4864 * 2 + 32)
 
 
 def test_grouped_create_without_a_gpu_reports_no_device(L):
@@ -431,3 +431,57 @@ def test_linear_swiglu_refusals(L):
     assert sg(U=FAKE + 8) == ALIGN                    # each half 16-byte aligned
     assert sg(M=0) == OK and sg(N=0) == OK
     assert sg(M=0, mode=2) == MODE                    # the mode is checked even for an empty call
+
+
+# ------------------------------------------------------------------ chained plans
+
+def ccalls(n=1, U=0, ldu=0, **kw):
+    from dit_convrot_linear_gb300.tq import ChainCall
+    return [ChainCall(c, U, ldu) for c in gcalls(n, **kw)]
+
+
+def cbytes(L, calls, bits=8):
+    from dit_convrot_linear_gb300 import tq
+    arr = (tq.ChainCall * max(len(calls), 1))(*calls)
+    out = ctypes.c_size_t(0)
+    rc = L.tq_chain_bytes(ctypes.addressof(arr), len(calls), bits, ctypes.byref(out))
+    return rc, out.value
+
+
+def test_chain_refusals(L):
+    from dit_convrot_linear_gb300 import tq
+    assert cbytes(L, ccalls(), bits=5)[0] == BITS
+    assert cbytes(L, ccalls(M=9))[0] == SHAPE
+    assert cbytes(L, ccalls(X=0))[0] == NULL
+    assert cbytes(L, ccalls(U=FAKE + 8, ldu=896))[0] == ALIGN      # up rows 16-byte aligned
+    assert cbytes(L, ccalls(U=FAKE, ldu=500))[0] == SHAPE          # ldu < K
+    assert cbytes(L, ccalls(U=FAKE, ldu=900))[0] == ALIGN
+    assert cbytes(L, ccalls(U=FAKE + 4096, ldu=896))[0] == OK
+    # the longest rows: eight 8-bit rows must fit a 64 KB stage (K = 8064),
+    # the rotated 4-bit input the launch's own buffer (K = 8960 at M = 1)
+    assert cbytes(L, ccalls(K=8064, ldx=8064))[0] == OK
+    assert cbytes(L, ccalls(K=8192, ldx=8192))[0] == SHAPE
+    assert cbytes(L, ccalls(K=8960, ldx=8960), bits=4)[0] == OK
+    assert cbytes(L, ccalls(K=8992, ldx=8992), bits=4)[0] == SHAPE
+    assert cbytes(L, ccalls(M=8, K=1024, ldx=1024), bits=4)[0] == OK
+    assert cbytes(L, ccalls(M=8, K=1024 + 64, ldx=1088), bits=4)[0] == SHAPE   # x' of 8 tokens too long
+    assert cbytes(L, ccalls(M=0, X=0, Wq=0)) == (OK, 0)
+    assert L.tq_chain_bytes(FAKE, -1, 8, ctypes.byref(ctypes.c_size_t(0))) == SHAPE
+    arr = (tq.ChainCall * 1)(*ccalls())
+    h = ctypes.c_void_p(None)
+    assert L.tq_chain_create(ctypes.addressof(arr), 1, 8, 2, FAKE, 1 << 20, ctypes.byref(h)) == MODE
+    assert L.tq_chain_create(ctypes.addressof(arr), 1, 8, 0, FAKE, 100, ctypes.byref(h)) == WORKSPACE
+    assert L.tq_chain_create(ctypes.addressof(arr), 1, 8, 0, FAKE + 16, 1 << 20, ctypes.byref(h)) == ALIGN
+    assert L.tq_chain_create(ctypes.addressof(arr), 1, 8, 0, FAKE, 1 << 20, None) == NULL
+
+
+def test_chain_bytes_count_the_most_items(L):
+    """Sizes need no device: every call counted with items of 8 rows (the
+    most a plan can have), every short-row call with a tensor map; no x'
+    workspace, a call record of 48 bytes and a counter of 4 per call."""
+    # a gated FFN layer at decode: gate+up 9728 x 896 (1216 items, tile
+    # form), down 896 x 4864 with the SwiGLU of the halves (112 items, rows)
+    gu = ccalls(N=9728, ldy=9728)
+    down = ccalls(N=896, K=4864, ldx=9728, ldy=896, U=FAKE + 4864 * 2, ldu=9728)
+    items = -(-(1216 + 112) * 88 // 256) * 256
+    assert cbytes(L, gu + down) == (OK, items + 256 + 256 + 256)
