@@ -424,15 +424,19 @@ class DecodeChain:
             x = y
 
     def make_plan(self):
-        """The same calls, on the same buffers, as one chained plan (one
-        cooperative launch walks the layers)."""
+        """The same calls as one chained plan (one cooperative launch walks
+        the layers), each call writing a buffer of its own."""
+        import torch
         from dit_convrot_linear_gb300 import tq
         calls, x = [], self.x0
+        self.plan_bufs = []
         for L in range(self.layers):
             (guc, gus), (dc, dsw) = self.weights[L]
-            y = self.bufs[L % 2]
-            calls.append((x, guc, gus, 2 * self.F, self.gu))
-            calls.append((self.gu[:, :self.F], dc, dsw, self.K, y, self.gu[:, self.F:]))
+            gu = torch.empty((1, 2 * self.F), dtype=torch.bfloat16, device=self.x0.device)
+            y = torch.empty((1, self.K), dtype=torch.bfloat16, device=self.x0.device)
+            self.plan_bufs += [gu, y]
+            calls.append((x, guc, gus, 2 * self.F, gu))
+            calls.append((gu[:, :self.F], dc, dsw, self.K, y, gu[:, self.F:]))
             x = y
         self.plan = tq.ChainPlan(calls, self.bits, out="bf16")
 

@@ -354,6 +354,21 @@ def test_chained_plan_ffn_layers(tq, bits):
     torch.cuda.synchronize()
     assert tq.device_status() == 0
     assert all(np.array_equal(a, bf16_bits(t)) for a, t in zip(first, gus + ys))
+    # a run with another input: every call must read this run's values, never
+    # the last run's (the counters start from zero each run).  The input differs in
+    # 16 signs, which changes every later value by far more than the bars
+    # while keeping the chain's scale (h is quadratic in the input: a new
+    # random input would drift from the calibrated scale layer by layer)
+    x2 = x0_bits.copy()
+    x2[0, :16] ^= 0x8000
+    x0.copy_(to_dev_bf16(x2))
+    g.replay()
+    torch.cuda.synchronize()
+    assert tq.device_status() == 0
+    x = bf16_bits(x0)
+    for L, (gc, gs, dc, ds) in enumerate(ws):
+        _check_ffn_layer(bits, L, x, bf16_bits(gus[L]), bf16_bits(ys[L]), gc, gs, dc, ds, F)
+        x = bf16_bits(ys[L])
 
 
 @pytest.mark.parametrize("bits", [8, 4])
