@@ -78,6 +78,15 @@ struct GCall {
     int32_t M, K, xk, pad;
 };
 
+// A build for the library's own tests (TQ_TEST_CHAIN_WAIT_EXTRA) waits for
+// that many items more than the previous call of a chained plan has, so the
+// wait between calls cannot end and its bounded expiry is taken.
+#ifdef TQ_TEST_CHAIN_WAIT_EXTRA
+constexpr unsigned int kChainWaitExtra = TQ_TEST_CHAIN_WAIT_EXTRA;
+#else
+constexpr unsigned int kChainWaitExtra = 0;
+#endif
+
 constexpr int kGStages = 3;
 constexpr int kGStageBytes = 64 * 1024;
 constexpr int kGConsWarps = 16;
@@ -574,7 +583,7 @@ k_gemv_grouped(const GroupedParams p) {
             if (ci != cur) {
                 const CCall cl = p.chain[ci];          // its load overlaps the wait
                 bool dep = true;
-                if (threadIdx.x == 0 && cwait > 0) dep = chain_wait(p.done + ci - 1, cwait);
+                if (threadIdx.x == 0 && cwait > 0) dep = chain_wait(p.done + ci - 1, cwait + kChainWaitExtra);
                 if (consumers_sync_any(!dep)) {
                     if (threadIdx.x == 0) {
                         *abort_sh = 1;

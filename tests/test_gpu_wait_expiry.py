@@ -62,3 +62,62 @@ def test_expired_wait_is_reported_and_the_context_stays_usable(tq, expiring_lib)
     ref = oracle.linear_a16(oracle.rotate_act_bf16(synth.tensor("gpu/expiry/x", M, K, 1.0)),
                             to_np(codes), to_np(sw))
     assert rel_l2(Y2, ref) <= REL_L2_Y
+
+
+@pytest.fixture(scope="module")
+def chain_expiring_lib():
+    """A copy whose chained plans wait for one item more than the previous
+    call has (so the wait between calls cannot end), every wait of the
+    grouped kernel limited to 2e6 cycles."""
+    from dit_convrot_linear_gb300 import build, tq
+    path = build.build_variant("chain_expiry", ["TQ_TEST_CHAIN_WAIT_EXTRA=1", "TQ_TEST_WAIT_CYCLES=2000000"],
+                               ["k_gemv_grouped.cu"])
+    L = ctypes.CDLL(path)
+    for name in ("tq_chain_bytes", "tq_chain_create", "tq_grouped_run", "tq_grouped_destroy",
+                 "tq_device_status"):
+        res, args = tq.SIGNATURES[name]
+        fn = getattr(L, name)
+        fn.restype, fn.argtypes = res, args
+    return L
+
+
+def test_chained_plan_expired_wait_is_reported(tq, chain_expiring_lib):
+    """Two dependent calls through the test copy: the first (nothing to wait
+    for) completes and is right; the second's wait for the first runs out on
+    every CTA that has its items, which stop; the status reports the expiry
+    once; the product library then runs the same chain correctly."""
+    import torch
+    L = chain_expiring_lib
+    M, K0, N0, N1 = 1, 512, 256, 128
+    x = synth.tensor("gpu/cexp/x", M, K0, 1.0)
+    X = to_dev_bf16(x)
+    c0, s0 = tq.quantize_weights(to_dev_bf16(synth.tensor("gpu/cexp/w0", N0, K0, 0.02, 0.01, 20.0)), 8)
+    c1, s1 = tq.quantize_weights(to_dev_bf16(synth.tensor("gpu/cexp/w1", N1, N0, 0.02, 0.01, 20.0)), 8)
+    Y0 = torch.zeros((M, N0), dtype=torch.bfloat16, device="cuda")
+    Y1 = torch.zeros((M, N1), dtype=torch.bfloat16, device="cuda")
+    recs = [tq.ChainCall(tq.A16Call(X.data_ptr(), K0, c0.data_ptr(), s0.data_ptr(), Y0.data_ptr(), N0, M, N0, K0),
+                         None, 0),
+            tq.ChainCall(tq.A16Call(Y0.data_ptr(), N0, c1.data_ptr(), s1.data_ptr(), Y1.data_ptr(), N1, M, N1, N0),
+                         None, 0)]
+    arr = (tq.ChainCall * 2)(*recs)
+    need = ctypes.c_size_t(0)
+    assert L.tq_chain_bytes(ctypes.addressof(arr), 2, 8, ctypes.byref(need)) == 0
+    buf = torch.empty(need.value, dtype=torch.uint8, device="cuda")
+    h = ctypes.c_void_p(None)
+    assert L.tq_chain_create(ctypes.addressof(arr), 2, 8, 1, buf.data_ptr(), need.value, ctypes.byref(h)) == 0
+    assert tq.device_status() == 0
+    s = torch.cuda.current_stream().cuda_stream
+    assert L.tq_grouped_run(h, s) == 0              # launched; the second call's wait runs out
+    assert L.tq_device_status(s) == TIMEOUT
+    assert L.tq_device_status(s) == 0
+    L.tq_grouped_destroy(h)
+    assert torch.all(Y1 == 0)                       # the second call wrote nothing
+    ref0 = oracle.linear_a16(oracle.rotate_act_bf16(x), to_np(c0), to_np(s0))
+    assert rel_l2(Y0.float().cpu().numpy(), ref0) <= 2.0 ** -8     # the first call is done (bf16 out)
+    # the product library on the same context
+    plan = tq.ChainPlan([(X, c0, s0, N0, Y0), (Y0, c1, s1, N1, Y1)], 8, out="bf16")
+    plan.run()
+    assert tq.device_status() == 0
+    y0 = Y0.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref1 = oracle.linear_a16(oracle.rotate_act_bf16(y0), to_np(c1), to_np(s1))
+    assert rel_l2(Y1.float().cpu().numpy(), ref1) <= 2.0 ** -8
