@@ -312,6 +312,58 @@ class Decode:
         self.gplan.run()
         self.y_host.copy_(self.y_dev, non_blocking=True)
 
+    def make_e2e_pipeline(self):
+        """Two device sets of the calls' inputs and outputs, each with its own
+        grouped plan, so that each step's copies overlap the neighbouring
+        steps' products: step k's input is copied in (one copy stream) while
+        step k - 1 runs, and its outputs are copied out (another) while step
+        k + 1 runs.  Events order the reuse of each set: its input is
+        overwritten only after the product that read it, its outputs only
+        after the copy that took them to the host."""
+        import torch
+        from dit_convrot_linear_gb300 import tq
+        x2, y2 = torch.empty_like(self.x_dev), torch.empty_like(self.y_dev)
+        calls = []
+        for (i, L, j, p, xo, yo) in self.plan:
+            codes, sw = self.weights[L][j]
+            calls.append((x2[xo:xo + p.K].view(1, p.K), codes, sw, p.N, y2[yo:yo + p.N].view(1, p.N)))
+        self.sets = [(self.x_dev, self.y_dev, self.gplan), (x2, y2, tq.GroupedPlan(calls, self.bits))]
+        self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        self.ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+        self.ev_run = [torch.cuda.Event(), torch.cuda.Event()]
+        self.ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+        self.used = [False, False]
+        self.k = 0
+        with torch.cuda.stream(self.s_in):
+            self.x_dev.copy_(self.x_host, non_blocking=True)
+            self.ev_in[0].record(self.s_in)
+
+    def step_grouped_e2e_pipelined(self):
+        import torch
+        a, b = self.k % 2, 1 - self.k % 2
+        S = torch.cuda.current_stream()
+        x, y, plan = self.sets[a]
+        S.wait_event(self.ev_in[a])                  # this step's input is on the device
+        if self.used[a]:
+            S.wait_event(self.ev_out[a])             # the outputs this set held are on the host
+        plan.run()
+        self.ev_run[a].record(S)
+        self.s_out.wait_event(self.ev_run[a])
+        with torch.cuda.stream(self.s_out):
+            self.y_host.copy_(y, non_blocking=True)
+            self.ev_out[a].record(self.s_out)
+        if self.used[b]:
+            self.s_in.wait_event(self.ev_run[b])     # the product that read set b's input is done
+        with torch.cuda.stream(self.s_in):
+            self.sets[b][0].copy_(self.x_host, non_blocking=True)
+            self.ev_in[b].record(self.s_in)
+        self.used[a] = True
+        self.k += 1
+
+    def join_e2e(self):
+        import torch
+        torch.cuda.current_stream().wait_event(self.ev_out[(self.k - 1) % 2])
+
     def product_ms(self, reps):
         """Mean duration of the product launch alone (CUDA events on the
         stream it runs on), each after its own rotation launch."""
@@ -537,7 +589,11 @@ def blocked_measure(device, steps, warmup, world, calls, l2, hbm):
     return out
 
 
-def time_steps(fn, steps, warmup, world):
+def time_steps(fn, steps, warmup, world, join=None):
+    """Device time of `steps` calls of fn (CUDA events on the current stream,
+    after `warmup` untimed calls, a barrier and a synchronize on both sides),
+    max over ranks.  join: makes the current stream wait, before the end
+    event, for work fn left on other streams."""
     import torch
     for _ in range(warmup):
         fn()
@@ -548,6 +604,8 @@ def time_steps(fn, steps, warmup, world):
     e0.record()
     for _ in range(steps):
         fn()
+    if join is not None:
+        join()
     e1.record()
     torch.cuda.synchronize()
     barrier(world)
@@ -1137,10 +1195,19 @@ def main():
             "bytes_per_launch_algorithmic": dec8.weight_bytes,
             "launch_ms": round(prod_ms, 4),
             "step_kernels": "k_rotate_grouped<8> (inputs) + k_gemv_grouped<8> (product)"}
-    ms_e2e = time_steps(dec8.step_grouped_e2e, max(1, args.steps // 2), 2, world) / max(1, args.steps // 2)
+    ne = max(1, args.steps // 2)
+    ms_serial = time_steps(dec8.step_grouped_e2e, ne, 2, world) / ne
+    dec8.make_e2e_pipeline()
+    ms_e2e = time_steps(dec8.step_grouped_e2e_pipelined, ne, 3, world, join=dec8.join_e2e) / ne
     e2e = {"value": round(dec8.weight_bytes / (ms_e2e * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
            "h2d_bytes_per_step": dec8.x_host.numel() * 2,
-           "d2h_bytes_per_step": dec8.y_host.numel() * 4}
+           "d2h_bytes_per_step": dec8.y_host.numel() * 4,
+           "ms_per_step": round(ms_e2e, 4),
+           "execution": "pinned host inputs copied in and outputs copied out every step, on copy streams "
+                        "overlapping the neighbouring steps' products (two device sets, each its own plan)",
+           "serial": {"value": round(dec8.weight_bytes / (ms_serial * 1e-3) / 1e9 * world, 2),
+                      "ms_per_step": round(ms_serial, 4),
+                      "execution": "copy in, product, copy out, in order on one stream"}}
     launches = args.steps * 2
     # the same calls, one launch each
     dec8.capture()
