@@ -439,3 +439,33 @@ def test_chained_plan_refuses_split_phases(tq):
     plan.run()
     ref = oracle.linear_a16(oracle.rotate_act_bf16(bf16_bits(X)), to_np(codes), to_np(sw))
     assert rel_l2(to_np(Y), ref) <= REL_L2_Y
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_chained_plan_eight_tokens(tq, bits):
+    """Eight-token calls (the most a chained call takes): three dependent
+    calls, the middle one with a ragged last group for 8-bit weights
+    (K = 1024 + 32), each against the oracle on its GPU input."""
+    import torch
+    M = 8
+    shapes = [(1056 if bits == 8 else 1024, 1024), (512, 1056 if bits == 8 else 1024), (300, 512)]
+    x0b = synth.tensor(f"gpu/c8/x{bits}", M, 1024, 1.0)
+    x0 = to_dev_bf16(x0b)
+    calls, keep, x = [], [], x0
+    for c, (N, K) in enumerate(shapes):
+        W = synth.tensor(f"gpu/c8/w{bits}/{c}", N, K, *WD)
+        gain = np.sqrt(np.mean(np.sum(oracle.bf16_to_f64(W) ** 2, axis=1)))
+        codes, sw = tq.quantize_weights(to_dev_bf16(W), bits)
+        sw = (sw / float(gain)).contiguous()
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        calls.append((x, codes, sw, N, Y))
+        keep.append((codes, sw, Y, K))
+        x = Y
+    plan = tq.ChainPlan(calls, bits, out="bf16")
+    plan.run()
+    assert tq.device_status() == 0
+    xb = x0b
+    for c, (codes, sw, Y, K) in enumerate(keep):
+        worst, _ = a16_close(bf16_bits(Y), xb, _wcodes(codes, bits, K), to_np(sw))
+        assert worst <= 0, f"call {c}: {worst}"
+        xb = bf16_bits(Y)
