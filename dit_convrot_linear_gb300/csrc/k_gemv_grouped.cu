@@ -14,8 +14,10 @@
 //   2. k_gemv_grouped runs one CTA per SM.  Work items are (call, block of
 //      weight rows, all of K), dealt round-robin, so the SMs sweep through the
 //      calls together and a weight matrix is never read by two SMs at once.
-//      A producer warp bulk-copies each item's weight rows and x' into a ring
-//      of shared-memory stages and stays up to three items ahead; sixteen
+//      A producer warp bulk-copies each item's weight rows and x' into two
+//      96 KB shared-memory stages and stays an item ahead (two large items
+//      amortise each item's fixed cost better than three smaller ones: 0.89
+//      against 0.75 of the HBM copy rate on 1000 decode calls); sixteen
 //      consumer warps multiply (codes widened to exact bf16 pairs in
 //      registers, mma.sync m16n8k16, fp32), add the K blocks in a fixed order
 //      and store Y.  The stream never waits for a call to finish.
@@ -87,8 +89,8 @@ constexpr unsigned int kChainWaitExtra = TQ_TEST_CHAIN_WAIT_EXTRA;
 constexpr unsigned int kChainWaitExtra = 0;
 #endif
 
-constexpr int kGStages = 3;
-constexpr int kGStageBytes = 64 * 1024;
+constexpr int kGStages = 2;
+constexpr int kGStageBytes = 96 * 1024;
 constexpr int kGConsWarps = 16;
 constexpr int kGThreads = (kGConsWarps + 1) * 32;     // + the producer warp
 constexpr int kGRed = 128;                            // rows x tokens of one item at most

@@ -542,7 +542,7 @@ typedef struct tq_grouped_s *tq_grouped;
 
 /*
  * Bytes of device memory a plan of these calls needs (tables and the rotated
- * inputs, about 64 bytes per 64 KB of weights plus 2 * M * K bytes per call).
+ * inputs, about 88 bytes per 96 KB of weights plus 2 * M * K bytes per call).
  * Refusals are those of tq_grouped_create (no device is needed).
  */
 tq_status tq_grouped_bytes(const tq_a16_call *calls, int64_t ncalls, int bits, size_t *bytes);
@@ -559,8 +559,8 @@ tq_status tq_grouped_bytes(const tq_a16_call *calls, int64_t ncalls, int bits, s
  * Each call follows tq_linear's rules for X, Wq, sw, Y and its strides, with
  * M <= TQ_MAX_M_GROUPED; in addition one work item (8 weight rows and the
  * call's rotated input, 2 * M * K bytes, K rounded up to 64 for 8-bit and
- * 128 for 4-bit weights) must fit 64 KB, or the call is refused with
- * TQ_ERR_SHAPE (for M = 1: K up to 6400 with 8-bit weights, 10752 with
+ * 128 for 4-bit weights) must fit 96 KB, or the call is refused with
+ * TQ_ERR_SHAPE (for M = 1: K up to 9728 with 8-bit weights, 16128 with
  * 4-bit).  The calls' pointers are kept: their buffers must stay allocated at
  * the same addresses while the plan is used.
  * A set-up call: it copies its tables with cudaMemcpy (the host waits), so
@@ -629,8 +629,8 @@ tq_status tq_chain_bytes(const tq_chain_call *calls, int64_t ncalls, int bits, s
  * tq_linear's rules for X, U, Wq, sw, Y and strides, with M <= 8; in
  * addition its rotated input must fit the launch's own buffer (2 * M * K
  * bytes, K rounded up to 64 for 8-bit and 128 for 4-bit weights, at most
- * 17984) and eight weight rows a 64 KB stage, or the call is refused with
- * TQ_ERR_SHAPE (for M = 1: K up to 8064 with 8-bit weights, 8960 with 4-bit).
+ * 17984) and eight weight rows a 96 KB stage, or the call is refused with
+ * TQ_ERR_SHAPE (for M = 1: K up to 8960 with 8- or 4-bit weights).
  * A call's Y must not overlap its own X or U, nor any call's Wq or sw; it
  * may overlap an earlier call's X, U or Y (later calls run after them).
  * Run the plan with tq_grouped_run (the counters are zeroed, then one

@@ -220,11 +220,11 @@ def test_grouped_refusals(L):
     assert gbytes(L, gcalls(Wq=FAKE + 8))[0] == ALIGN
     assert gbytes(L, gcalls(K=12288, ldx=12288))[0] == SHAPE      # 8 rows + x' exceed a stage
     assert gbytes(L, gcalls(M=8, K=4864, ldx=4864))[0] == SHAPE   # x' of 8 tokens too long
-    assert gbytes(L, gcalls(K=12288, ldx=12288), bits=4)[0] == SHAPE
-    assert gbytes(L, gcalls(K=6400, ldx=6400))[0] == OK           # the longest 8-bit K for M = 1
-    assert gbytes(L, gcalls(K=6432, ldx=6432))[0] == SHAPE
-    assert gbytes(L, gcalls(K=10752, ldx=10752), bits=4)[0] == OK  # and 4-bit
-    assert gbytes(L, gcalls(K=10784, ldx=10784), bits=4)[0] == SHAPE
+    assert gbytes(L, gcalls(K=16384, ldx=16384), bits=4)[0] == SHAPE
+    assert gbytes(L, gcalls(K=9728, ldx=9728))[0] == OK           # the longest 8-bit K for M = 1
+    assert gbytes(L, gcalls(K=9760, ldx=9760))[0] == SHAPE
+    assert gbytes(L, gcalls(K=16128, ldx=16128), bits=4)[0] == OK  # and 4-bit
+    assert gbytes(L, gcalls(K=16160, ldx=16160), bits=4)[0] == SHAPE
     # an empty call is skipped before its pointers are looked at
     assert gbytes(L, gcalls(M=0, X=0, Wq=0)) == (OK, 0)
     assert gbytes(L, []) == (OK, 0)
@@ -244,20 +244,20 @@ def test_grouped_refusals(L):
 
 
 def test_grouped_bytes_count_tables_and_rotated_inputs(L):
-    # M = 1, K = 896, N = 4864, 8-bit: items of 64 rows (960-byte shared rows,
-    # 1792 bytes of x' per item) -> 76 items of 88 bytes (6688, rounded to
-    # 6912); one 40-byte call record and one 128-byte tensor map (rows of 7
-    # chunks of 128 bytes: the tile form), each rounded to 256; x' of 896 fp16
-    # and a 32-byte tail (the token scales)
-    assert gbytes(L, gcalls()) == (OK, 256 + 6912 + 256 + 896 * 2 + 32)
+    # M = 1, K = 896, N = 4864, 8-bit: items of 96 rows (960-byte shared rows,
+    # 1792 bytes of x' per item, a 96 KB stage) -> 51 items of 88 bytes (4488,
+    # rounded to 4608); one 40-byte call record and one 128-byte tensor map
+    # (rows of 7 chunks of 128 bytes: the tile form), each rounded to 256; x'
+    # of 896 fp16 and a 32-byte tail (the token scales)
+    assert gbytes(L, gcalls()) == (OK, 256 + 4608 + 256 + 896 * 2 + 32)
     # two tokens, K = 544 (x' padded to 640 columns), N = 100, 4-bit: two
     # items of 64 rows, tile form
     calls = gcalls(M=2, N=100, K=544, ldx=544, ldy=100)
     assert gbytes(L, calls, bits=4) == (OK, 256 + 256 + 256 + 2 * 640 * 2 + 32)
-    # long rows (K = 4864: 38 chunks, items of 8 rows) stay in the row form:
-    # no tensor map; 112 items of 88 bytes
+    # long rows (K = 4864: 38 chunks, items of 16 rows) stay in the row form:
+    # no tensor map; 56 items of 88 bytes
     calls = gcalls(N=896, K=4864, ldx=4864, ldy=896)
-    assert gbytes(L, calls) == (OK, 256 + 9984 + 4864 * 2 + 32)
+    assert gbytes(L, calls) == (OK, 256 + 5120 + 4864 * 2 + 32)
 
 
 def test_grouped_create_without_a_gpu_reports_no_device(L):
@@ -457,10 +457,10 @@ def test_chain_refusals(L):
     assert cbytes(L, ccalls(U=FAKE, ldu=500))[0] == SHAPE          # ldu < K
     assert cbytes(L, ccalls(U=FAKE, ldu=900))[0] == ALIGN
     assert cbytes(L, ccalls(U=FAKE + 4096, ldu=896))[0] == OK
-    # the longest rows: eight 8-bit rows must fit a 64 KB stage (K = 8064),
-    # the rotated 4-bit input the launch's own buffer (K = 8960 at M = 1)
-    assert cbytes(L, ccalls(K=8064, ldx=8064))[0] == OK
-    assert cbytes(L, ccalls(K=8192, ldx=8192))[0] == SHAPE
+    # the longest rows: the rotated input must fit the launch's own buffer
+    # (K = 8960 at M = 1, 8- or 4-bit weights)
+    assert cbytes(L, ccalls(K=8960, ldx=8960))[0] == OK
+    assert cbytes(L, ccalls(K=8992, ldx=8992))[0] == SHAPE
     assert cbytes(L, ccalls(K=8960, ldx=8960), bits=4)[0] == OK
     assert cbytes(L, ccalls(K=8992, ldx=8992), bits=4)[0] == SHAPE
     assert cbytes(L, ccalls(M=8, K=1024, ldx=1024), bits=4)[0] == OK
