@@ -9,8 +9,9 @@
 // not the weight stream, sets the time.  Calls that do not depend on one
 // another (gate and up of a layer, or the independent calls of a batch) can
 // instead share one weight stream:
-//   1. k_rotate_grouped rotates every call's token rows once, into a
-//      workspace of the plan, in the lane-contiguous x' order of the MMAs.
+//   1. k_rotate_grouped rotates every call's token rows once (a CTA per
+//      call), into a workspace of the plan, in the lane-contiguous x' order
+//      of the MMAs.
 //   2. k_gemv_grouped runs one CTA per SM.  Work items are (call, block of
 //      weight rows, all of K), dealt round-robin, so the SMs sweep through the
 //      calls together and a weight matrix is never read by two SMs at once.
@@ -352,86 +353,87 @@ __device__ __forceinline__ void tile_blocks(float (&acc)[4][4], const unsigned c
     if (b < bend) block_mma<BITS, HASB, BF>(acc, pA + off(b), pB + off(b), xb + b * KB);
 }
 
-// x' of one call (one warp per call, eight calls per CTA), in the order the
-// product's lanes read it, as fp16 (for 4-bit weights, odd k divided by 16 as
-// well, exactly): token row m is the bf16 rounding of the rotated row (the A16
-// operand),
-// times 2^e with e chosen so that its largest magnitude lies in [2^14, 2^15).
-// The multiplication by a power of two is exact, and so is the fp16 form of
-// every value not below 2^-31 of that largest one (smaller ones keep an
-// absolute error under 2^-39 of it).  The product multiplies Y by 2^-e, read
-// from the float after the M fp16 rows.
+// x' of one call (a CTA per call), in the order the product's lanes read it,
+// as fp16 (for 4-bit weights, odd k divided by 16 as well, exactly): token
+// row m is the bf16 rounding of the rotated row (the A16 operand), times 2^e
+// with e chosen so that its largest magnitude lies in [2^14, 2^15).  The
+// multiplication by a power of two is exact, and so is the fp16 form of every
+// value not below 2^-31 of that largest one (smaller ones keep an absolute
+// error under 2^-39 of it).  The product multiplies Y by 2^-e, read from the
+// float after the M fp16 rows.
+// The eight warps share the call's (token, group) pairs: a first pass puts
+// each pair's largest |x'| in shared memory, one warp turns them into the
+// tokens' exponents, and a second pass transforms the pairs again (their
+// rows are in L2 by then) and stores them scaled.  Every call's CTA runs at
+// once, so the pass costs about one call's latency.
+constexpr int kRotPairsMax = TQ_MAX_M_GROUPED * 64;   // tokens x groups (K <= 16384)
+
 template <int BITS>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256)
 k_rotate_grouped(const GCall *calls, int64_t ncalls) {
     constexpr int KB = BITS == 8 ? 64 : 128;
+    __shared__ float pam[kRotPairsMax];
+    __shared__ int tok_sh[TQ_MAX_M_GROUPED];
+    if (blockIdx.x >= ncalls) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int64_t c = static_cast<int64_t>(blockIdx.x) * 8 + warp; c < ncalls; c += static_cast<int64_t>(gridDim.x) * 8) {
-      const GCall cl = calls[c];
-      for (int m = 0; m < cl.M; ++m) {
-        const int G = (cl.K + kGroup - 1) / kGroup;
-        const uint16_t *xrow = cl.X + m * cl.ldx;
-        uint16_t *row = cl.xq + static_cast<int64_t>(m) * cl.xk;
-        // groups are taken four at a time, their loads issued before any
-        // butterfly, so a long row's reads overlap instead of queueing
-        constexpr int GB = 4;
+    const GCall cl = calls[blockIdx.x];
+    const int G = (cl.K + kGroup - 1) / kGroup;
+    const int pairs = cl.M * G;
+    if (pairs > kRotPairsMax) return;              // not reached: plans refuse such calls
+    for (int q = warp; q < pairs; q += 8) {
+        const int m = q / G, g = q - m * G;
+        const int64_t gk = static_cast<int64_t>(g) * kGroup;
+        const int n = group_width(cl.K, gk);
+        float v[8];
+        const int E = fwht_group_raw(load_group_raw(cl.X + m * cl.ldx + gk + lane * (n / 32), n / 32), n, v);
         float amax = 0.0f;
-        for (int g0 = 0; g0 < G; g0 += GB) {
-            uint4 raw[GB];
 #pragma unroll
-            for (int u = 0; u < GB; ++u) {
-                const int64_t gk = static_cast<int64_t>(g0 + u) * kGroup;
-                const int n = g0 + u < G ? group_width(cl.K, gk) : 32;
-                raw[u] = g0 + u < G ? load_group_raw(xrow + gk + lane * (n / 32), n / 32) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < GB; ++u) {
-                if (g0 + u >= G) break;
-                float v[8];
-                const int E = fwht_group_raw(raw[u], group_width(cl.K, static_cast<int64_t>(g0 + u) * kGroup), v);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (e < E) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(f32_to_bf16_bits(v[e]))));
-            }
-        }
+        for (int e = 0; e < 8; ++e)
+            if (e < E) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(f32_to_bf16_bits(v[e]))));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        int ex = 0;
-        if (amax > 0.0f) frexpf(amax, &ex);              // amax = f * 2^ex, f in [0.5, 1)
-        const int sh = amax > 0.0f ? max(-100, min(100, 15 - ex)) : 0;
-        const float up = ldexpf(1.0f, sh);
-        for (int g0 = 0; g0 < G; g0 += GB) {
-            uint4 raw[GB];
+        if (lane == 0) pam[q] = amax;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        for (int m = 0; m < cl.M; ++m) {
+            float amax = 0.0f;
+            for (int g2 = lane; g2 < G; g2 += 32) amax = fmaxf(amax, pam[m * G + g2]);
 #pragma unroll
-            for (int u = 0; u < GB; ++u) {
-                const int64_t gk = static_cast<int64_t>(g0 + u) * kGroup;
-                const int n = g0 + u < G ? group_width(cl.K, gk) : 32;
-                raw[u] = g0 + u < G ? load_group_raw(xrow + gk + lane * (n / 32), n / 32) : make_uint4(0, 0, 0, 0);
-            }
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            int ex = 0;
+            if (amax > 0.0f) frexpf(amax, &ex);              // amax = f * 2^ex, f in [0.5, 1)
+            if (lane == 0) tok_sh[m] = amax > 0.0f ? max(-100, min(100, 15 - ex)) : 0;
+        }
+    }
+    __syncthreads();
+    for (int q = warp; q < pairs; q += 8) {
+        const int m = q / G, g = q - m * G;
+        const int64_t gk = static_cast<int64_t>(g) * kGroup;
+        const int n = group_width(cl.K, gk);
+        float v[8];
+        const int E = fwht_group_raw(load_group_raw(cl.X + m * cl.ldx + gk + lane * (n / 32), n / 32), n, v);
+        const float up = ldexpf(1.0f, tok_sh[m]);
+        uint16_t *row = cl.xq + static_cast<int64_t>(m) * cl.xk;
 #pragma unroll
-            for (int u = 0; u < GB; ++u) {
-                if (g0 + u >= G) break;
-                const int64_t gk = static_cast<int64_t>(g0 + u) * kGroup;
-                float v[8];
-                const int E = fwht_group_raw(raw[u], group_width(cl.K, gk), v);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    if (e < E) {
-                        const int kl = static_cast<int>(gk) + lane * E + e;
-                        const float xb = bf16_bits_to_f32(f32_to_bf16_bits(v[e]));
-                        // 4-bit weights: odd k meets 16 times its code (widen_i4_f16_odd16)
-                        const float f = (BITS == 4 && (kl & 1)) ? up * 0.0625f : up;
-                        row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = __half_as_ushort(__float2half_rn(xb * f));
-                    }
-                }
+        for (int e = 0; e < 8; ++e) {
+            if (e < E) {
+                const int kl = static_cast<int>(gk) + lane * E + e;
+                const float xb = bf16_bits_to_f32(f32_to_bf16_bits(v[e]));
+                // 4-bit weights: odd k meets 16 times its code (widen_i4_f16_odd16)
+                const float f = (BITS == 4 && (kl & 1)) ? up * 0.0625f : up;
+                row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = __half_as_ushort(__float2half_rn(xb * f));
             }
         }
-        for (int kl = cl.K + lane; kl < cl.xk; kl += 32)   // zeros after K, up to the block edge
-            row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = 0;
-        if (lane == 0)
-            reinterpret_cast<float *>(cl.xq + static_cast<int64_t>(cl.M) * cl.xk)[m] = ldexpf(1.0f, -sh);
-      }
     }
+    const int tail = cl.xk - cl.K;                 // zeros after K, up to the block edge
+    for (int i = threadIdx.x; i < cl.M * tail; i += 256) {
+        const int m = i / tail, kl = cl.K + (i - m * tail);
+        cl.xq[static_cast<int64_t>(m) * cl.xk + (kl / KB) * KB + xpos<BITS>(kl % KB)] = 0;
+    }
+    if (threadIdx.x < cl.M)
+        reinterpret_cast<float *>(cl.xq + static_cast<int64_t>(cl.M) * cl.xk)[threadIdx.x] =
+            ldexpf(1.0f, -tok_sh[threadIdx.x]);
 }
 
 template <int BITS, bool CHAIN>
@@ -991,8 +993,8 @@ tq_status grouped_run(tq_grouped plan, const DeviceInfo &dev, int phase, cudaStr
     unsigned int *status = status_word();
     if (!status) return TQ_ERR_CUDA;
     if (phase & 1) {
-        const int64_t rgrid = (plan->ncalls + 7) / 8 < 65536 ? (plan->ncalls + 7) / 8 : 65536;
-        rot<<<static_cast<unsigned>(rgrid), 256, 0, s>>>(plan->calls, plan->ncalls);
+        if (plan->ncalls > (1ll << 31) - 1) return TQ_ERR_OVERFLOW;
+        rot<<<static_cast<unsigned>(plan->ncalls), 256, 0, s>>>(plan->calls, plan->ncalls);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e);
     }
