@@ -94,11 +94,19 @@ constexpr int kGStages = 2;
 constexpr int kGStageBytes = 96 * 1024;
 constexpr int kGConsWarps = 16;
 constexpr int kGThreads = (kGConsWarps + 1) * 32;     // + the producer warp
-constexpr int kGRed = 128;                            // rows x tokens of one item at most
+// Rows x tokens of one item at most (the partial sums' area): independent
+// plans take 160 (a 96 KB stage holds 160 rows of 896 4-bit codes); chained
+// plans 128, which leaves their own x' buffer room.
+constexpr int kGRedInd = 160, kGRedChain = 128;
+constexpr int kGRed = kGRedChain;                      // the chained plans' layout below
 constexpr int kGRedOff = kGStages * kGStageBytes;
 constexpr int kGHdrOff = kGRedOff + 2 * kGConsWarps * kGRed * 4;
 constexpr int kGBarOff = kGHdrOff + kGStages * 128;
-constexpr int kGSmem = kGBarOff + 2 * kGStages * 8 + 16 + 1024;   // + alignment of the stages
+// independent plans: the same layout with the larger partial-sum area
+constexpr int kGHdrOffInd = kGRedOff + 2 * kGConsWarps * kGRedInd * 4;
+constexpr int kGBarOffInd = kGHdrOffInd + kGStages * 128;
+constexpr int kGSmem = kGBarOffInd + 2 * kGStages * 8 + 16 + 1024;   // + alignment of the stages
+static_assert(kGSmem <= 232448, "within the opt-in shared memory of a CTA");
 constexpr unsigned int kStatusGroupedTimeout = 16u;
 constexpr int kXTail = 32;     // bytes after a call's x' rows: a float 2^-e per token
 
@@ -443,11 +451,13 @@ k_gemv_grouped(const GroupedParams p) {
     // stages on a 1024-byte boundary (the tensor copies' 128-byte swizzle)
     unsigned char *smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     constexpr int KB = BITS == 8 ? 64 : 128;   // k per block (16 bytes per lane)
+    constexpr int RED = CHAIN ? kGRedChain : kGRedInd;
+    constexpr int HDR_OFF = CHAIN ? kGHdrOff : kGHdrOffInd, BAR_OFF = CHAIN ? kGBarOff : kGBarOffInd;
     float *red = reinterpret_cast<float *>(smem + kGRedOff);
-    unsigned char *hdr = smem + kGHdrOff;      // stage headers, 128 bytes apart
-    const uint32_t full0 = smem_addr(smem + kGBarOff);
+    unsigned char *hdr = smem + HDR_OFF;       // stage headers, 128 bytes apart
+    const uint32_t full0 = smem_addr(smem + BAR_OFF);
     const uint32_t empty0 = full0 + 8 * kGStages;
-    volatile int *abort_sh = reinterpret_cast<volatile int *>(smem + kGBarOff + 2 * kGStages * 8);
+    volatile int *abort_sh = reinterpret_cast<volatile int *>(smem + BAR_OFF + 2 * kGStages * 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t grid = gridDim.x;
@@ -549,7 +559,7 @@ k_gemv_grouped(const GroupedParams p) {
         if (i >= p.nitems) break;
         const int s = static_cast<int>(k % kGStages);
         const bool ok = mbar_wait_suspend(full0 + 8 * s, static_cast<uint32_t>((k / kGStages) & 1));
-        float *rd = red + (k & 1) * kGConsWarps * kGRed;
+        float *rd = red + (k & 1) * kGConsWarps * RED;
         // the header is read before the stage is released
         int rows = 0, rb = 0, ws = 0, xk = KB, M = 1, xoff = 0;
         bool tiles = false;
@@ -649,8 +659,8 @@ k_gemv_grouped(const GroupedParams p) {
                     if (row >= rb) continue;
                     const float s0 = (acc[0][2 * h] + acc[1][2 * h]) + (acc[2][2 * h] + acc[3][2 * h]);
                     const float s1 = (acc[0][2 * h + 1] + acc[1][2 * h + 1]) + (acc[2][2 * h + 1] + acc[3][2 * h + 1]);
-                    if (2 * t < M) rd[warp * kGRed + row * M + 2 * t] = s0;
-                    if (2 * t + 1 < M) rd[warp * kGRed + row * M + 2 * t + 1] = s1;
+                    if (2 * t < M) rd[warp * RED + row * M + 2 * t] = s0;
+                    if (2 * t + 1 < M) rd[warp * RED + row * M + 2 * t + 1] = s1;
                 }
             }
         }
@@ -673,7 +683,7 @@ k_gemv_grouped(const GroupedParams p) {
             for (int w = 0; w < kGConsWarps; ++w) {
                 // warps whose (non-empty) run touches the row's tile wrote a partial
                 const int a = U * w / kGConsWarps, b = U * (w + 1) / kGConsWarps;
-                if (a < b && a < (tile + 1) * NB && b > tile * NB) sum += rd[w * kGRed + r_st * M + m_st];
+                if (a < b && a < (tile + 1) * NB && b > tile * NB) sum += rd[w * RED + r_st * M + m_st];
             }
             const float yv = swv * (dsc * sum);
             const int64_t off = static_cast<int64_t>(m_st) * ldy + r_st;
@@ -695,7 +705,7 @@ k_gemv_grouped(const GroupedParams p) {
 }  // namespace
 
 // Rows of one work item for calls of these sizes: the largest multiple of 16
-// whose weight rows and the call's x' fit one stage (rows x tokens <= kGRed),
+// whose weight rows and the call's x' fit one stage (rows x tokens <= 160),
 // else 8, else 0 (the call cannot be grouped).
 int grouped_item_rows(int64_t M, int64_t K, int bits) {
     if (M < 1 || M > TQ_MAX_M_GROUPED || K < 1) return 0;
@@ -704,7 +714,7 @@ int grouped_item_rows(int64_t M, int64_t K, int bits) {
     const int64_t ws = (rbytes + 127) / 128 * 128 + 64;
     const int64_t xbytes = M * ((K + KB - 1) / KB * KB) * 2 + kXTail;
     int64_t rb = (kGStageBytes - xbytes) / ws;
-    if (rb > kGRed / M) rb = kGRed / M;
+    if (rb > kGRedInd / M) rb = kGRedInd / M;
     return rb >= 16 ? static_cast<int>(rb / 16 * 16) : (rb >= 8 ? 8 : 0);
 }
 
@@ -723,7 +733,7 @@ int chain_item_rows(int64_t M, int64_t K, int64_t N, int bits, int grid) {
     const int64_t rbytes = K * bits / 8;
     const int64_t ws = (rbytes + 127) / 128 * 128 + 64;
     int64_t fit = kGStageBytes / ws;
-    if (fit > kGRed / M) fit = kGRed / M;
+    if (fit > kGRedChain / M) fit = kGRedChain / M;
     fit = fit >= 16 ? fit / 16 * 16 : (fit >= 8 ? 8 : 0);
     if (fit == 0) return 0;
     if (grid <= 0) return 8;
