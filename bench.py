@@ -56,6 +56,10 @@ PROFILE_CASES = {
     "rot_tiled": ("rotation + int8 tiled operand, M=4032 K=12288", "k_rotq"),
     "skinny_m64": ("batched W4A16 on the tensor cores, M=64 N=12288 K=4096", "k_skinny_tc"),
     "skinny_m8": ("batched W4A16 on the tensor cores, M=8 N=4096 K=12288", "k_skinny_tc"),
+    "grouped_w4": ("grouped decode W4A16, 300 M=1 calls cycling gate/up 4864x896 and down 896x4864 "
+                   "over 31 layer sets (the product launch)", "k_gemv_grouped"),
+    "grouped_w8": ("grouped decode W8A16, 300 M=1 calls cycling gate/up 4864x896 and down 896x4864 "
+                   "over 31 layer sets (the product launch)", "k_gemv_grouped"),
     "gemv_m1": ("batched W4A16 with one token, M=1 N=12288 K=4096 (the streaming product, a scale a row)",
                 "k_gemv"),
 }
@@ -956,6 +960,13 @@ def profile_case(device, name, steps):
         ws = tq.split_workspace()
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
         op = lambda: tq.linear_tt(At, sx, M, K, Wt, sw, N, bits, Y=Y, out="bf16", split=ws)
+    elif name.startswith("grouped"):
+        props = torch.cuda.get_device_properties(device)
+        l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+        dec = Decode(4 if name == "grouped_w4" else 8, 300, device, l2)
+        dec.make_grouped()
+        dec.gplan.rotate()
+        op = dec.gplan.product
     elif name.startswith("rot"):
         M, K = (4032, 3072) if name == "rot_modnorm" else (4032, 12288)
         X = bf16_dev(synth.tensor(f"case/{name}/x", M, K, *XD), device)

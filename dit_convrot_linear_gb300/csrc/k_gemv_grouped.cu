@@ -71,8 +71,40 @@ struct GItem {
     int16_t tiles;         // 1: tile form
     int32_t call;          // chained plans: index of the item's call
     uint32_t wait;         // chained plans: items of the previous call (0: none)
+    // Set by the host so that the consumers divide by none of the item's
+    // sizes (an integer division is about twenty instructions a thread):
+    uint32_t nbm;          // ceil(2^20 / NB), NB = xk / (k per block): u / NB = (u nbm) >> 20
+    uint32_t rowm;         // ceil(2^20 / rows): j / rows = (j rowm) >> 20 for j < rows M
+    uint8_t wf[10], wl[10];  // per 16-row tile: the first and last consumer warp whose units touch it
+    uint8_t pad[12];
 };
-static_assert(sizeof(GItem) == 88, "item record of 88 bytes");
+static_assert(sizeof(GItem) == 128, "item record of 128 bytes, one stage header");
+
+// The fields of an item its producer needs to issue the copies (the whole
+// record reaches the stage header by a bulk copy of its own).
+struct GIssue {
+    const uint8_t *w;
+    const void *tmap;
+    const uint16_t *xq;
+    int32_t rows, rb, rbytes, ws, xk, n0, xoff, M, tiles;
+};
+
+__device__ __forceinline__ GIssue issue_of(const GItem *ip) {
+    GIssue r;
+    r.w = ip->w;
+    r.tmap = ip->tmap;
+    r.xq = ip->xq;
+    r.rows = ip->rows;
+    r.rb = ip->rb;
+    r.rbytes = ip->rbytes;
+    r.ws = ip->ws;
+    r.xk = ip->xk;
+    r.n0 = ip->n0;
+    r.xoff = ip->xoff;
+    r.M = ip->M;
+    r.tiles = ip->tiles;
+    return r;
+}
 
 struct GCall {
     const uint16_t *X;
@@ -99,6 +131,7 @@ constexpr int kGThreads = (kGConsWarps + 1) * 32;     // + the producer warp
 // plans 128, which leaves their own x' buffer room.
 constexpr int kGRedInd = 160, kGRedChain = 128;
 constexpr int kGRed = kGRedChain;                      // the chained plans' layout below
+static_assert(kGRedInd / 16 <= 10 && kGRedChain / 16 <= 10, "an item's tiles fit the record's warp ranges");
 constexpr int kGRedOff = kGStages * kGStageBytes;
 constexpr int kGHdrOff = kGRedOff + 2 * kGConsWarps * kGRed * 4;
 constexpr int kGBarOff = kGHdrOff + kGStages * 128;
@@ -108,7 +141,9 @@ constexpr int kGBarOffInd = kGHdrOffInd + kGStages * 128;
 constexpr int kGSmem = kGBarOffInd + 2 * kGStages * 8 + 16 + 1024;   // + alignment of the stages
 static_assert(kGSmem <= 232448, "within the opt-in shared memory of a CTA");
 constexpr unsigned int kStatusGroupedTimeout = 16u;
-constexpr int kXTail = 32;     // bytes after a call's x' rows: a float 2^-e per token
+// bytes after a call's x' rows: a float 2^-e per token, then the token's sum
+// of x' (the fp16 values as the product multiplies them)
+constexpr int kXTail = 64;
 
 // One call of a chained plan, as its consumers read it.
 struct CCall {
@@ -286,7 +321,9 @@ __device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity)
 // One K block (64 bytes of each of the lane's two rows) into the four
 // accumulator chains.  HASB false: rows g + 8 do not exist (an 8-row item).
 // BF: x' is the bf16 operand (chained plans), codes widened to bf16 pairs;
-// else x' is the scaled fp16 form, codes widened to fp16 (4-bit: odd k x16).
+// else x' is the scaled fp16 form and the codes are widened with their bias
+// as fp16 subnormals (4-bit: odd k x16); the sums then hold 2^-24 (sum c x' +
+// bias sum x'), which the store corrects with the token's sum of x'.
 template <int BITS, bool HASB, bool BF>
 __device__ __forceinline__ void block_mma(float (&acc)[4][4], const unsigned char *pa,
                                           const unsigned char *pb, const uint16_t *xblk) {
@@ -318,8 +355,8 @@ __device__ __forceinline__ void block_mma(float (&acc)[4][4], const unsigned cha
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             uint32_t a0, a1 = 0, a2, a3 = 0;
-            widen_i8_f16(A[q], a0, a2);
-            if (HASB) widen_i8_f16(B[q], a1, a3);
+            widen_i8_f16_biased(A[q], a0, a2);
+            if (HASB) widen_i8_f16_biased(B[q], a1, a3);
             const uint2 bv = *reinterpret_cast<const uint2 *>(xblk + q * 16);
             mma_f16(acc[q], a0, a1, a2, a3, bv.x, bv.y);
         }
@@ -327,8 +364,8 @@ __device__ __forceinline__ void block_mma(float (&acc)[4][4], const unsigned cha
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             uint32_t pa4[4], pb4[4] = {0, 0, 0, 0};
-            widen_i4_f16_odd16(A[q], pa4);
-            if (HASB) widen_i4_f16_odd16(B[q], pb4);
+            widen_i4_f16_biased(A[q], pa4);
+            if (HASB) widen_i4_f16_biased(B[q], pb4);
             const uint2 b0 = *reinterpret_cast<const uint2 *>(xblk + (2 * q) * 16);
             const uint2 b1 = *reinterpret_cast<const uint2 *>(xblk + (2 * q + 1) * 16);
             mma_f16(acc[(2 * q) % 4], pa4[0], pb4[0], pa4[1], pb4[1], b0.x, b0.y);
@@ -368,7 +405,9 @@ __device__ __forceinline__ void tile_blocks(float (&acc)[4][4], const unsigned c
 // multiplication by a power of two is exact, and so is the fp16 form of every
 // value not below 2^-31 of that largest one (smaller ones keep an absolute
 // error under 2^-39 of it).  The product multiplies Y by 2^-e, read from the
-// float after the M fp16 rows.
+// float after the M fp16 rows; the M floats after those hold each token's sum
+// of x' as the product multiplies it (16 times the stored value at odd k for
+// 4-bit weights), for the codes' bias.
 // The eight warps share the call's (token, group) pairs: a first pass puts
 // each pair's largest |x'| in shared memory, one warp turns them into the
 // tokens' exponents, and a second pass transforms the pairs again (their
@@ -423,25 +462,40 @@ k_rotate_grouped(const GCall *calls, int64_t ncalls) {
         const int E = fwht_group_raw(load_group_raw(cl.X + m * cl.ldx + gk + lane * (n / 32), n / 32), n, v);
         const float up = ldexpf(1.0f, tok_sh[m]);
         uint16_t *row = cl.xq + static_cast<int64_t>(m) * cl.xk;
+        float ls = 0.0f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             if (e < E) {
                 const int kl = static_cast<int>(gk) + lane * E + e;
                 const float xb = bf16_bits_to_f32(f32_to_bf16_bits(v[e]));
-                // 4-bit weights: odd k meets 16 times its code (widen_i4_f16_odd16)
-                const float f = (BITS == 4 && (kl & 1)) ? up * 0.0625f : up;
-                row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = __half_as_ushort(__float2half_rn(xb * f));
+                // 4-bit weights: odd k meets 16 times its code (widen_i4_f16_biased)
+                const bool odd4 = BITS == 4 && (kl & 1);
+                const __half h = __float2half_rn(xb * (odd4 ? up * 0.0625f : up));
+                row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = __half_as_ushort(h);
+                ls += odd4 ? 16.0f * __half2float(h) : __half2float(h);
             }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+        if (lane == 0) pam[q] = ls;       // the first pass's maxima are spent
     }
     const int tail = cl.xk - cl.K;                 // zeros after K, up to the block edge
     for (int i = threadIdx.x; i < cl.M * tail; i += 256) {
         const int m = i / tail, kl = cl.K + (i - m * tail);
         cl.xq[static_cast<int64_t>(m) * cl.xk + (kl / KB) * KB + xpos<BITS>(kl % KB)] = 0;
     }
-    if (threadIdx.x < cl.M)
-        reinterpret_cast<float *>(cl.xq + static_cast<int64_t>(cl.M) * cl.xk)[threadIdx.x] =
-            ldexpf(1.0f, -tok_sh[threadIdx.x]);
+    float *tailf = reinterpret_cast<float *>(cl.xq + static_cast<int64_t>(cl.M) * cl.xk);
+    if (threadIdx.x < cl.M) tailf[threadIdx.x] = ldexpf(1.0f, -tok_sh[threadIdx.x]);
+    __syncthreads();
+    if (warp == 0) {   // the tokens' sums over their groups, in a fixed order
+        for (int m = 0; m < cl.M; ++m) {
+            float s = 0.0f;
+            for (int g2 = lane; g2 < G; g2 += 32) s += pam[m * G + g2];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) tailf[cl.M + m] = s;
+        }
+    }
 }
 
 template <int BITS, bool CHAIN>
@@ -476,14 +530,14 @@ k_gemv_grouped(const GroupedParams p) {
         // Item k goes to stage k % kGStages once the consumers have released
         // the stage's previous item (this warp is the only waiter, in order).
         int64_t k = 0;
-        GItem nxt;                       // the next record, loaded one item ahead
-        if (blockIdx.x < p.nitems) nxt = p.items[blockIdx.x];
+        GIssue nxt;                      // the next item's copy fields, loaded one item ahead
+        if (blockIdx.x < p.nitems) nxt = issue_of(p.items + blockIdx.x);
         for (;; ++k) {
             const int64_t i = blockIdx.x + k * grid;
             const bool stop = __shfl_sync(0xffffffffu, *abort_sh, 0) != 0;   // one decision per warp
             if (i >= p.nitems || stop) break;
-            const GItem it = nxt;
-            if (i + grid < p.nitems) nxt = p.items[i + grid];
+            const GIssue it = nxt;
+            if (i + grid < p.nitems) nxt = issue_of(p.items + i + grid);
             const int s = static_cast<int>(k % kGStages);
             const int64_t u = k / kGStages;
             bool ok = true;
@@ -500,15 +554,20 @@ k_gemv_grouped(const GroupedParams p) {
             const uint32_t full = full0 + 8 * s;
             const int nch = (it.rbytes + 127) / 128;
             if (lane == 0) {
-                *reinterpret_cast<GItem *>(hdr + s * 128) = it;
                 // chained plans: no x' with the item (its consumers rotate the input)
                 const uint32_t xbytes = CHAIN ? 0u : static_cast<uint32_t>(it.M) * it.xk * 2 + kXTail;
                 // a tensor copy counts its whole box, zero fill included
                 const uint32_t wbytes = it.tiles ? static_cast<uint32_t>(nch * it.rb * 128)
                                                  : static_cast<uint32_t>(it.rows * it.rbytes);
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full),
-                             "r"(wbytes + xbytes)
+                             "r"(wbytes + xbytes + static_cast<uint32_t>(sizeof(GItem)))
                              : "memory");
+                // the record itself, into the stage's header
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                    ::"r"(smem_addr(hdr + s * 128)), "l"(p.items + i), "r"(static_cast<uint32_t>(sizeof(GItem))),
+                      "r"(full)
+                    : "memory");
                 if (!CHAIN)
                     asm volatile(
                         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -562,6 +621,7 @@ k_gemv_grouped(const GroupedParams p) {
         float *rd = red + (k & 1) * kGConsWarps * RED;
         // the header is read before the stage is released
         int rows = 0, rb = 0, ws = 0, xk = KB, M = 1, xoff = 0;
+        uint32_t nbm = 1u << 20, rowm = 1u << 20;
         bool tiles = false;
         const float *swp = nullptr;
         void *y = nullptr;
@@ -582,6 +642,8 @@ k_gemv_grouped(const GroupedParams p) {
             ldy = h.ldy;
             ci = h.call;
             cwait = h.wait;
+            nbm = h.nbm;
+            rowm = h.rowm;
         }
         if constexpr (CHAIN) {
             // the first item of a call in this CTA: wait for the previous
@@ -616,11 +678,21 @@ k_gemv_grouped(const GroupedParams p) {
         // others already multiply the next item
         const int j = threadIdx.x;
         const bool store = ok && j < rows * M;
-        const int m_st = store ? j / rows : 0, r_st = store ? j % rows : 0;
+        const int m_st = store ? static_cast<int>((static_cast<uint32_t>(j) * rowm) >> 20) : 0;
+        const int r_st = store ? j - m_st * rows : 0;
+        // the warps whose runs touch the row's tile (read before the release)
+        int w_lo = 0, w_hi = -1;
+        if (store) {
+            const GItem &h = *reinterpret_cast<const GItem *>(hdr + s * 128);
+            w_lo = h.wf[r_st >> 4];
+            w_hi = h.wl[r_st >> 4];
+        }
         const float swv = store ? __ldg(swp + r_st) : 0.0f;
         // the token's 2^-e (after the x' rows), read before the stage is released
-        const float dsc = (!store || CHAIN) ? 1.0f
-                          : reinterpret_cast<const float *>(smem + s * kGStageBytes + xoff + M * xk * 2)[m_st];
+        const float *tailf = reinterpret_cast<const float *>(smem + s * kGStageBytes + xoff + M * xk * 2);
+        const float dsc = (!store || CHAIN) ? 1.0f : tailf[m_st];
+        // the codes' bias times the token's sum of x' (independent plans)
+        const float bsum = (!store || CHAIN) ? 0.0f : (BITS == 8 ? 128.0f : 8.0f) * tailf[M + m_st];
         if (ok && u0 < u1) {
             const unsigned char *st = smem + s * kGStageBytes;
             const uint16_t *xb = (CHAIN ? xs : reinterpret_cast<const uint16_t *>(st + xoff)) + (g < M ? g : 0) * xk + 4 * t;
@@ -630,8 +702,8 @@ k_gemv_grouped(const GroupedParams p) {
             const int gr = tiles ? ((g >> 1) | ((g & 1) << 2)) : g;
             const int cst = rb * 128;
             // the run, one tile at a time: blocks [b, bend) of tile `tile`
-            for (int u = u0; u < u1;) {
-                const int tile = u / NB;
+            int tile = static_cast<int>((static_cast<uint32_t>(u0) * nbm) >> 20);
+            for (int u = u0; u < u1; ++tile) {
                 int b = u - tile * NB;
                 const int bend = min(u1 - tile * NB, NB);
                 u = tile * NB + bend;
@@ -677,15 +749,12 @@ k_gemv_grouped(const GroupedParams p) {
         if (threadIdx.x == 0)
             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8 * s) : "memory");
         if (store) {
-            const int tile = r_st >> 4;
             float sum = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kGConsWarps; ++w) {
-                // warps whose (non-empty) run touches the row's tile wrote a partial
-                const int a = U * w / kGConsWarps, b = U * (w + 1) / kGConsWarps;
-                if (a < b && a < (tile + 1) * NB && b > tile * NB) sum += rd[w * RED + r_st * M + m_st];
+            for (int w = w_lo; w <= w_hi; ++w) {
+                // warps of a non-empty run in that range wrote a partial
+                if (U * w / kGConsWarps < U * (w + 1) / kGConsWarps) sum += rd[w * RED + r_st * M + m_st];
             }
-            const float yv = swv * (dsc * sum);
+            const float yv = CHAIN ? swv * sum : swv * (dsc * fmaf(sum, 16777216.0f, -bsum));
             const int64_t off = static_cast<int64_t>(m_st) * ldy + r_st;
             if (p.ytype == 0)
                 static_cast<float *>(y)[off] = yv;
@@ -850,6 +919,19 @@ tq_status grouped_tables(const tq_a16_call *calls, const tq_chain_call *chain, i
             it.M = static_cast<int16_t>(a.M);
             it.call = chain ? static_cast<int32_t>(t.ccalls.size() - 1) : 0;
             it.wait = chain ? wait : 0;
+            // the consumers' divisions, done here: u / NB and j / rows by
+            // multiplication are exact while u NB and j rows stay below 2^20
+            // (a 96 KB stage keeps u NB under 2^15, and j rows <= 160^2)
+            const int64_t NB = g.xk / KB, U = (rb + 15) / 16 * NB;
+            it.nbm = static_cast<uint32_t>(((int64_t(1) << 20) + NB - 1) / NB);
+            it.rowm = static_cast<uint32_t>(((int64_t(1) << 20) + it.rows - 1) / it.rows);
+            // unit u belongs to the warp w with floor(U w / W) <= u < floor(U (w + 1) / W),
+            // W = kGConsWarps: w = ceil(W (u + 1) / U) - 1
+            auto owner = [&](int64_t u) { return (kGConsWarps * (u + 1) + U - 1) / U - 1; };
+            for (int64_t tl = 0; tl < (rb + 15) / 16; ++tl) {
+                it.wf[tl] = static_cast<uint8_t>(owner(tl * NB));
+                it.wl[tl] = static_cast<uint8_t>(owner(tl * NB + NB - 1));
+            }
             t.items.push_back(it);
         }
     }
@@ -1016,7 +1098,7 @@ tq_status grouped_run(tq_grouped plan, const DeviceInfo &dev, int phase, cudaStr
         p.status = status;
         p.chain = nullptr;
         p.done = nullptr;
-        kern<<<static_cast<unsigned>(plan->grid), kGThreads, kGSmem, s>>>(p);
+            kern<<<static_cast<unsigned>(plan->grid), kGThreads, kGSmem, s>>>(p);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e);
     }

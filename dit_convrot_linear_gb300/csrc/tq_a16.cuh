@@ -93,6 +93,28 @@ __device__ __forceinline__ void widen_i4_f16_odd16(uint32_t w, uint32_t (&p)[4])
     p[3] = f16x2_sub((w8 & 0x00F000F0u) ^ co, co);
 }
 
+// Biased widenings without the subtraction: a 16-bit pattern u < 2^10 is the
+// fp16 subnormal u * 2^-24 exactly, so the code c plus its bias B (128 for
+// int8, 8 for int4: c + B >= 0) is an fp16 value by a mask or a byte permute
+// alone.  A product of these with x' holds 2^-24 (sum_k c_k x'_k + B sum_k
+// x'_k); whoever consumes it takes off B times the token's sum of x'.
+// int8: pairs (k0, k2), (k1, k3) of (c + 128) 2^-24.
+__device__ __forceinline__ void widen_i8_f16_biased(uint32_t x, uint32_t &p02, uint32_t &p13) {
+    const uint32_t u = x ^ 0x80808080u;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p02) : "r"(u), "r"(0u), "r"(0x4240u));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p13) : "r"(u), "r"(0u), "r"(0x4341u));
+}
+
+// int4: pairs (k0, k4), (16 k1, 16 k5), (k2, k6), (16 k3, 16 k7) of
+// (c + 8) 2^-24, the odd codes in place as in widen_i4_f16_odd16.
+__device__ __forceinline__ void widen_i4_f16_biased(uint32_t w, uint32_t (&p)[4]) {
+    const uint32_t w8 = w >> 8;
+    p[0] = (w & 0x000F000Fu) ^ 0x00080008u;
+    p[1] = (w & 0x00F000F0u) ^ 0x00800080u;
+    p[2] = (w8 & 0x000F000Fu) ^ 0x00080008u;
+    p[3] = (w8 & 0x00F000F0u) ^ 0x00800080u;
+}
+
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                         uint32_t a3, uint32_t b0, uint32_t b1) {
     asm volatile(

@@ -542,7 +542,7 @@ typedef struct tq_grouped_s *tq_grouped;
 
 /*
  * Bytes of device memory a plan of these calls needs (tables and the rotated
- * inputs, about 88 bytes per 96 KB of weights plus 2 * M * K bytes per call).
+ * inputs, about 128 bytes per 96 KB of weights plus 2 * M * K bytes per call).
  * Refusals are those of tq_grouped_create (no device is needed).
  */
 tq_status tq_grouped_bytes(const tq_a16_call *calls, int64_t ncalls, int bits, size_t *bytes);

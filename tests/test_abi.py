@@ -245,19 +245,19 @@ def test_grouped_refusals(L):
 
 def test_grouped_bytes_count_tables_and_rotated_inputs(L):
     # M = 1, K = 896, N = 4864, 8-bit: items of 96 rows (960-byte shared rows,
-    # 1792 bytes of x' per item, a 96 KB stage) -> 51 items of 88 bytes (4488,
-    # rounded to 4608); one 40-byte call record and one 128-byte tensor map
+    # 1792 bytes of x' per item, a 96 KB stage) -> 51 items of 128 bytes (6528,
+    # rounded to 6656); one 40-byte call record and one 128-byte tensor map
     # (rows of 7 chunks of 128 bytes: the tile form), each rounded to 256; x'
-    # of 896 fp16 and a 32-byte tail (the token scales)
-    assert gbytes(L, gcalls()) == (OK, 256 + 4608 + 256 + 896 * 2 + 32)
+    # of 896 fp16 and a 64-byte tail (the token scales and sums of x')
+    assert gbytes(L, gcalls()) == (OK, 256 + 6656 + 256 + 896 * 2 + 64)
     # two tokens, K = 544 (x' padded to 640 columns), N = 100, 4-bit: two
     # items of 64 rows, tile form
     calls = gcalls(M=2, N=100, K=544, ldx=544, ldy=100)
-    assert gbytes(L, calls, bits=4) == (OK, 256 + 256 + 256 + 2 * 640 * 2 + 32)
+    assert gbytes(L, calls, bits=4) == (OK, 256 + 256 + 256 + 2 * 640 * 2 + 64)
     # long rows (K = 4864: 38 chunks, items of 16 rows) stay in the row form:
-    # no tensor map; 56 items of 88 bytes
+    # no tensor map; 56 items of 128 bytes
     calls = gcalls(N=896, K=4864, ldx=4864, ldy=896)
-    assert gbytes(L, calls) == (OK, 256 + 5120 + 4864 * 2 + 32)
+    assert gbytes(L, calls) == (OK, 256 + 7168 + 4864 * 2 + 64)
 
 
 def test_grouped_create_without_a_gpu_reports_no_device(L):
@@ -483,5 +483,5 @@ def test_chain_bytes_count_the_most_items(L):
     # form), down 896 x 4864 with the SwiGLU of the halves (112 items, rows)
     gu = ccalls(N=9728, ldy=9728)
     down = ccalls(N=896, K=4864, ldx=9728, ldy=896, U=FAKE + 4864 * 2, ldu=9728)
-    items = -(-(1216 + 112) * 88 // 256) * 256
+    items = -(-(1216 + 112) * 128 // 256) * 256
     assert cbytes(L, gu + down) == (OK, items + 256 + 256 + 256)

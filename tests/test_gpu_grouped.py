@@ -101,12 +101,30 @@ def test_grouped_many_calls_wrap_the_ring(tq):
         assert torch.isfinite(c[4]).all()
 
 
-def test_grouped_bf16_output_within_one_ulp(tq):
-    plan, calls, host = build(tq, 4, [(1, 4864, 896), (8, 1000, 2304 + 128)], out="bf16", tag="b")
+@pytest.mark.parametrize("bits", [4, 8])
+def test_grouped_bf16_output_within_one_ulp_or_fp32_rounding(tq, bits):
+    """bf16 Y against the oracle's O6 on the GPU's own rotated operand: within
+    one bf16 step of the exact value, or, for outputs near zero, within the
+    rounding of the fp32 sums.  The product sums the codes with their bias B
+    (q + 8 or q + 128, then takes off B times the sum of x'), so its fp32
+    partial sums reach sw sum_k |q_nk + B| |x'_k|, and so does their rounding
+    error, times a few units of 2^-24: the bar allows 2^-20 of that sum.  It
+    stays near 1e-4 of a typical output, while one wrong code, scale or index
+    moves Y by about 1e-2 of it."""
+    plan, calls, host = build(tq, bits, [(1, 4864, 896), (8, 1000, 2304 + 128)], out="bf16", tag=f"b{bits}")
     plan.run()
+    B = 8.0 if bits == 4 else 128.0
     for (_, _, _, _, Y), (X, Xd, Wc, sw) in zip(calls, host):
-        ref = oracle.linear_a16(bf16_bits(tq.rotate_act_bf16(Xd)), Wc, sw)
-        assert bf16_ulp_diff(bf16_bits(Y), oracle.round_bf16(ref)).max() <= 1
+        xr = bf16_bits(tq.rotate_act_bf16(Xd))
+        ref = oracle.linear_a16(xr, Wc, sw)
+        got = bf16_bits(Y)
+        one_ulp = bf16_ulp_diff(got, oracle.round_bf16(ref)) <= 1
+        mag = (np.abs(oracle.bf16_to_f64(xr)) @ np.abs(Wc.astype(np.float64) + B).T) * sw.astype(np.float64)[None, :]
+        a = np.abs(ref)
+        step = np.exp2(np.floor(np.log2(np.where(a > 0, a, 2.0 ** -133))) - 7)
+        near = np.abs(oracle.bf16_to_f64(got) - ref) <= step + 2.0 ** -20 * mag
+        assert np.all(one_ulp | near)
+        assert one_ulp.mean() >= 0.999     # the rest are outputs near zero
 
 
 def test_grouped_deterministic_and_graph_replay(tq):
