@@ -55,13 +55,12 @@ PROFILE_CASES = {
     "rot_swiglu": ("SwiGLU + rotation + int8 tiled operand, M=4032 K=12288", "k_rotq"),
     "rot_tiled": ("rotation + int8 tiled operand, M=4032 K=12288", "k_rotq"),
     "skinny_m64": ("batched W4A16 on the tensor cores, M=64 N=12288 K=4096", "k_skinny_tc"),
-    "skinny_m8": ("batched W4A16 on the tensor cores, M=8 N=4096 K=12288", "k_skinny_tc"),
+    "splitk_m8": ("batched W4A16, split-K product, M=8 N=4096 K=12288", "k_gemv_splitk"),
     "grouped_w4": ("grouped decode W4A16, 300 M=1 calls cycling gate/up 4864x896 and down 896x4864 "
                    "over 31 layer sets (the product launch)", "k_gemv_grouped"),
     "grouped_w8": ("grouped decode W8A16, 300 M=1 calls cycling gate/up 4864x896 and down 896x4864 "
                    "over 31 layer sets (the product launch)", "k_gemv_grouped"),
-    "gemv_m1": ("batched W4A16 with one token, M=1 N=12288 K=4096 (the streaming product, a scale a row)",
-                "k_gemv"),
+    "splitk_m1": ("batched W4A16 with one token, split-K product, M=1 N=12288 K=4096", "k_gemv_splitk"),
 }
 
 
@@ -805,8 +804,8 @@ def batched_measure(device, steps, warmup, world, l2, hbm, bf16_peak):
                                      "roof_tflops": round(roof, 2)},
                         "per_projection": per}
         del xs, ys, g
-    out["kernels"] = ("M = 1: k_gemv_blocked<4> with one scale a row (12288x4096, streaming) and "
-                      "k_gemv_small<4> (4096x12288); M = 8, 32, 64: k_rotate_tiles16 (x' pre-pass) + "
+    out["kernels"] = ("M = 1, 8: k_gemv_splitk<4, 1> (clusters along K, each CTA rotating its run of the "
+                      "input, mma.sync with the tokens as N); M = 32, 64: k_rotate_tiles16 (x' pre-pass) + "
                       "k_skinny_tc<4> (tcgen05, A operand from TMEM, cluster split-K)")
     return out
 
@@ -982,8 +981,8 @@ def profile_case(device, name, steps):
         else:
             op = lambda: tq.rotate_quant_act_tiled(X, At=At, sx=sx)
     else:
-        M, N, K = {"skinny_m64": (64, 12288, 4096), "skinny_m8": (8, 4096, 12288),
-                   "gemv_m1": (1, 12288, 4096)}[name]
+        M, N, K = {"skinny_m64": (64, 12288, 4096), "splitk_m8": (8, 4096, 12288),
+                   "splitk_m1": (1, 12288, 4096)}[name]
         X, codes, sw = xw(M, N, K, 4)
         Y = torch.empty((M, N), dtype=torch.float32, device=device)
         need = tq.linear_workspace_bytes(M, K, N, 4, "W4A16")

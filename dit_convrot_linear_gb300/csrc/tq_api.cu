@@ -327,6 +327,9 @@ tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
     DeviceInfo dev;
     if ((st = current_device(&dev)) != TQ_OK) return st;
     if (a16) {
+        if (splitk_fits(M, N, K, bits, dev))
+            return launch_splitk(static_cast<const uint16_t *>(X), M, K, ldx, static_cast<const uint8_t *>(Wq), sw,
+                                 N, bits, Y, ytype == TQ_OUT_BF16 ? 1 : 0, ldy, dev, stream);
         if (use_ws && skinny_tc_fits_device(N, dev))
             return launch_skinny_tc(static_cast<const uint16_t *>(X), M, K, ldx, static_cast<const uint8_t *>(Wq),
                                     sw, N, bits, Y, ytype == TQ_OUT_BF16 ? 1 : 0, ldy, workspace, dev, stream);

@@ -57,6 +57,10 @@ tq_status launch_gemv_a16(const uint16_t *X, int64_t M, int64_t K, int64_t ldx,
 
 // Batched A16 product on tcgen05 (M <= 64; large matrices or more than 8
 // tokens): a pre-pass writes x' as fp16 tiles into the workspace.
+bool splitk_fits(int64_t M, int64_t N, int64_t K, int bits, const DeviceInfo &dev);
+tq_status launch_splitk(const uint16_t *X, int64_t M, int64_t K, int64_t ldx, const uint8_t *Wq, const float *sw,
+                        int64_t N, int bits, void *Y, int ytype, int64_t ldy, const DeviceInfo &dev,
+                        cudaStream_t s);
 bool skinny_tc_applies(int64_t M, int64_t N, int64_t K);
 int64_t skinny_tc_workspace(int64_t M, int64_t K);
 bool skinny_tc_fits_device(int64_t N, const DeviceInfo &dev);

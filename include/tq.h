@@ -169,18 +169,20 @@ size_t tq_linear_workspace_bytes(int64_t M, int64_t K, int64_t N, int bits,
  *            tq_linear_workspace_bytes(M, K, N, bits, mode) bytes, 256-byte
  *            aligned (may be NULL when that is 0).  Its contents on entry do
  *            not matter; the call overwrites it.
- *            TQ_W8A8: required.  A16 modes: optional.  With it, products of
- *            more than 8 token rows, or of weights of at least 2^24 codes
- *            with 3 to 8 token rows, run on the tensor cores (where they are
- *            faster; one or two token rows over such a matrix stream through
- *            the CUDA cores instead, and need no workspace; the rotated rows are first written to
- *            the workspace as fp16 tiles, each token scaled by a power of two,
- *            which keeps every bf16 value exact); without it (or smaller than
- *            that size) the CUDA-core kernels run.  Both compute the same Y
- *            within fp32 rounding.  Calls in order on one stream may share a
- *            workspace (the next call's weights stream early, but its operand
- *            is written only after this call ends); calls on different
- *            streams need their own.
+ *            TQ_W8A8: required.  A16 modes: optional.  Up to 16 token rows
+ *            over weights of at least 2^24 codes that fill the GPU in one
+ *            wave run the split-K product (clusters of CTAs along K, each
+ *            rotating its own run of the input; no workspace).  Otherwise,
+ *            with the workspace, products of more than 8 token rows, or of
+ *            such weights with 3 to 8 token rows, run on the tensor cores
+ *            (the rotated rows are first written to the workspace as fp16
+ *            tiles, each token scaled by a power of two, which keeps every
+ *            bf16 value exact); without it (or smaller than that size) the
+ *            CUDA-core kernels run.  All compute the same Y within fp32
+ *            rounding.  Calls in order on one stream may share a workspace
+ *            (the next call's weights stream early, but its operand is
+ *            written only after this call ends); calls on different streams
+ *            need their own.
  */
 tq_status tq_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
                     const void *Wq, const float *sw, int64_t N, int bits,
