@@ -167,6 +167,28 @@ __device__ __forceinline__ constexpr int xpos8(int e) {
                      : (((e >> 1) & 1) * 16 + ((e >> 2) | ((e & 1) << 1)));
 }
 
+// The last group of a row when K is not a multiple of 256 (width n = 32, 64
+// or 128): its transform, scaled stores and sum of x', out of line so that
+// the unrolled full-group code stays small (the kernel is otherwise bound by
+// instruction fetch in its rotation phase).  Returns the warp's sum.
+template <int BITS>
+__device__ __noinline__ float sp_tail_group(uint4 r, int n, int gl, float up, uint16_t *row) {
+    constexpr int KB = BITS == 8 ? 64 : 128;
+    const int lane = threadIdx.x & 31;
+    float v[8];
+    const int E = fwht_group_raw(r, n, v);
+    float ls = 0.0f;
+    for (int e = 0; e < E; ++e) {
+        const int kl = gl * kGroup + lane * E + e;
+        const float xb = bf16_bits_to_f32(f32_to_bf16_bits(v[e]));
+        const bool odd4 = BITS == 4 && (kl & 1);
+        const __half h = __float2half_rn(xb * (odd4 ? up * 0.0625f : up));
+        row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = __half_as_ushort(h);
+        ls += odd4 ? 16.0f * __half2float(h) : __half2float(h);
+    }
+    return warp_sum(ls);
+}
+
 template <int BITS, int NG>
 __global__ void __launch_bounds__(SP_THREADS, 1)
 k_gemv_splitk(const __grid_constant__ CUtensorMap tmW, const SplitParams p) {
@@ -312,36 +334,34 @@ k_gemv_splitk(const __grid_constant__ CUtensorMap tmW, const SplitParams p) {
             const int ex = mx == 0 ? 0 : min(max(10 - (static_cast<int>((mx >> 7) & 0xFF) - 127), -100), 100);
             const float up = __uint_as_float(static_cast<uint32_t>(127 + ex) << 23);
             const int n = group_width(p.K, static_cast<int64_t>(g0 + gl) * kGroup);
-            float v[8];
-            const int E = fwht_group_raw(raw[i], n, v);
             uint16_t *row = xs + m * XS;
-            float ls = 0.0f;
-            if (E == 8) {
-                // eight consecutive columns at a multiple of 8: fixed offsets
+            float ls;
+            if (n == kGroup) {
+                // a full group: eight consecutive columns a lane, at fixed
+                // offsets from the first
+                const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+                float v[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    v[2 * k] = __uint_as_float(w[k] << 16);
+                    v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+                }
+                warp_fwht<8, float>(v);
                 const int kl0 = gl * kGroup + lane * 8;
                 uint16_t *base = row + (kl0 / KB) * KB + xpos<BITS>(kl0 % KB);
+                ls = 0.0f;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float xb = bf16_bits_to_f32(f32_to_bf16_bits(v[e]));
+                    const float xb = bf16_bits_to_f32(f32_to_bf16_bits(0.0625f * v[e]));   // exact: 1/sqrt(256)
                     const bool odd4 = BITS == 4 && (e & 1);
                     const __half h = __float2half_rn(xb * (odd4 ? up * 0.0625f : up));
                     base[xpos8<BITS>(e)] = __half_as_ushort(h);
                     ls += odd4 ? 16.0f * __half2float(h) : __half2float(h);
                 }
+                ls = warp_sum(ls);
             } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    if (e < E) {
-                        const int kl = gl * kGroup + lane * E + e;
-                        const float xb = bf16_bits_to_f32(f32_to_bf16_bits(v[e]));
-                        const bool odd4 = BITS == 4 && (kl & 1);
-                        const __half h = __float2half_rn(xb * (odd4 ? up * 0.0625f : up));
-                        row[(kl / KB) * KB + xpos<BITS>(kl % KB)] = __half_as_ushort(h);
-                        ls += odd4 ? 16.0f * __half2float(h) : __half2float(h);
-                    }
-                }
+                ls = sp_tail_group<BITS>(raw[i], n, gl, up, row);
             }
-            ls = warp_sum(ls);
             if (lane == 0) pss[q] = ls;
         }
         consumers_sync();
