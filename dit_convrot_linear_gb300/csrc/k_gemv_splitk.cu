@@ -255,9 +255,18 @@ k_gemv_splitk(const __grid_constant__ CUtensorMap tmW, const SplitParams p) {
                     break;
                 const uint32_t full = full0 + 8 * s;
                 const int nc = min(2, nch - 2 * it);
+                // A build for the library's own tests (TQ_TEST_UNSET_BYTES)
+                // expects bytes that no copy brings, so no stage's phase
+                // completes and the bounded waits expire, with every issued
+                // copy landed; the drain below then runs to its full limit.
+#ifdef TQ_TEST_UNSET_BYTES
+                constexpr uint32_t kUnset = TQ_TEST_UNSET_BYTES;
+#else
+                constexpr uint32_t kUnset = 0;
+#endif
                 // a tensor copy counts its whole box, zero fill included
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full),
-                             "r"(static_cast<uint32_t>(nc * (SP_ST / 2)))
+                             "r"(static_cast<uint32_t>(nc * (SP_ST / 2)) + kUnset)
                              : "memory");
                 for (int c = 0; c < nc; ++c) {
                     const int x = static_cast<int>((kc0 + static_cast<int64_t>(2 * it + c) * KC) * BITS / 8);

@@ -65,6 +65,48 @@ def test_expired_wait_is_reported_and_the_context_stays_usable(tq, expiring_lib)
 
 
 @pytest.fixture(scope="module")
+def splitk_expiring_lib():
+    """A copy whose split-K product expects 16 bytes more than its copies
+    bring on every stage, its operand waits limited to 2e6 cycles."""
+    from dit_convrot_linear_gb300 import build, tq
+    path = build.build_variant("splitk_expiry", ["TQ_TEST_UNSET_BYTES=16", "TQ_TEST_WAIT_CYCLES=2000000"],
+                               ["k_gemv_splitk.cu"])
+    L = ctypes.CDLL(path)
+    for name in ("tq_linear", "tq_device_status"):
+        res, args = tq.SIGNATURES[name]
+        fn = getattr(L, name)
+        fn.restype, fn.argtypes = res, args
+    return L
+
+
+def test_split_k_expired_wait_is_reported_and_the_cluster_stores_nothing(tq, splitk_expiring_lib):
+    """Every CTA of every cluster gives up its wait (no stage completes);
+    each still reaches both cluster barriers, none stores, the status is
+    reported once, and the product library then runs the same call right."""
+    import torch
+    M, N, K = 8, 4096, 12288          # the batched down projection at eight tokens (split-K)
+    W = synth.tensor("gpu/expiry/skw", N, K, 0.015, 0.005, 30.0)
+    Xh = synth.tensor("gpu/expiry/skx", M, K, 1.0)
+    X = to_dev_bf16(Xh)
+    codes, sw = tq.quantize_weights(to_dev_bf16(W), 4)
+    assert tq.device_status() == 0
+    s = torch.cuda.current_stream().cuda_stream
+    Y = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    L = splitk_expiring_lib
+    rc = L.tq_linear(X.data_ptr(), M, K, X.stride(0), codes.data_ptr(), sw.data_ptr(), N, 4, 1,
+                     Y.data_ptr(), 0, Y.stride(0), None, 0, s)
+    assert rc == 0
+    assert L.tq_device_status(s) == TIMEOUT
+    assert L.tq_device_status(s) == 0
+    assert torch.all(Y == 0)
+    Y2 = to_np(tq.linear(X, codes, sw, N, 4, "W4A16"))
+    assert tq.device_status() == 0
+    c = to_np(codes)
+    ref = oracle.linear_a16(oracle.rotate_act_bf16(Xh), oracle.weight_codes(c.view(np.uint8), 4, K), to_np(sw))
+    assert rel_l2(Y2, ref) <= REL_L2_Y
+
+
+@pytest.fixture(scope="module")
 def chain_expiring_lib():
     """A copy whose chained plans wait for one item more than the previous
     call has (so the wait between calls cannot end), every wait of the
