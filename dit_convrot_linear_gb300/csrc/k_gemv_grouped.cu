@@ -19,9 +19,11 @@
 //      96 KB shared-memory stages and stays an item ahead (two large items
 //      amortise each item's fixed cost better than three smaller ones: 0.89
 //      against 0.75 of the HBM copy rate on 1000 decode calls); sixteen
-//      consumer warps multiply (codes widened to exact bf16 pairs in
-//      registers, mma.sync m16n8k16, fp32), add the K blocks in a fixed order
-//      and store Y.  The stream never waits for a call to finish.
+//      consumer warps multiply (each code plus its bias widened into an
+//      exact fp16 subnormal in registers against the scaled fp16 x',
+//      mma.sync m16n8k16, fp32), add the K blocks in a fixed order, take off
+//      the bias times the token's sum of x' and store Y.  The stream never
+//      waits for a call to finish.
 // A chained plan runs calls that do depend on one another, in order, the way
 // a decoder walks its layers: call c may read the output of any earlier call
 // (kvad-gpu internals, "Numbers": one projection at a time, each input the
