@@ -534,8 +534,11 @@ int64_t skinny_tc_workspace(int64_t M, int64_t K) {
     return (ks * skinny_tc_mp(M) * SK_BK * 2 + 255) / 256 * 256 + 256;
 }
 
-// Which A16 kernel a call takes, measured with 4-bit weights of 12288 x 4096
-// and 4096 x 12288, calls back to back (us a call):
+// Which A16 kernel a call takes when the split-K product (k_gemv_splitk.cu,
+// up to 16 tokens over a matrix that fills the GPU in one wave of clusters:
+// 10.9 / 11.5 us a call at one token, 15.0 / 15.6 at eight) does not,
+// measured with 4-bit weights of 12288 x 4096 and 4096 x 12288, calls back
+// to back (us a call):
 //   tokens   tensor cores   streaming (a row a warp)   small kernel
 //   1        27.4 / 30.5    13.4 / 20.5                24.5 / 19.8
 //   2        25.4 / 30.5    20.0 / 26.2                34.9 / 27.5
