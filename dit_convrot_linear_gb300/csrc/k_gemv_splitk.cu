@@ -14,9 +14,11 @@
 //     producer warp streams the run through two 64 KB stages by tensor
 //     copies, a stage 256 contiguous bytes of every row (two 128-byte
 //     chunks, each stored with the 128-byte swizzle); every consumer warp
-//     takes every stage, in order.  (Stages of 128 bytes a row streamed at
-//     under half the HBM rate, each row's bytes a separate short burst.)  The
-//     weights do not depend on the launch before, so the copies start at once.
+//     takes every stage, in order (ring slots are never shared between
+//     different warps' uses, which would make a barrier's phase parity
+//     ambiguous).  256 bytes of a row a request rather than 128: each row's
+//     bytes reach DRAM in longer bursts.  The weights do not depend on the
+//     launch before, so the copies start at once.
 //   - Its 16 consumer warps wait for the launch before (X may come from it),
 //     rotate the tokens' groups of the run, round them to bf16 and keep them
 //     in shared memory as fp16 times 2^e, e per token from the run's largest
